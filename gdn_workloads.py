@@ -1,0 +1,210 @@
+"""Seeded synthetic inputs for the Gated DeltaNet (GDN) decode / MTP-verify state update.
+
+This module is shared by the CPU oracle side (``oracle/``, ``tests/``) and the CUDA side (``bench.py``,
+the GPU tests).  It holds NO arithmetic of the method: it only draws random numbers, casts them to the
+storage types and lays them out.  Both sides receive the same bytes.
+
+Workload shapes follow the serving setups on the pages:
+
+* T = 4 tokens per verify (three drafted tokens plus one) -- sglang PR #23273 "[GDN] Enable FlashInfer MTP
+  verify on SM100+ (Blackwell)", launch command (``--speculative-num-steps 3 --speculative-num-draft-tokens
+  4``);
+* T = 8 (beyond 4, with intermediate caching) -- same page, Requirements (FlashInfer #2679);
+* bf16 state pool (``--mamba-ssm-dtype bfloat16``) -- same page, Throughput Benchmark server settings;
+* padded lanes carry pool index -1 -- same page, Requirements (FlashInfer #2810, padding index guard);
+* concurrency up to 256 requests -- same page, Mean TPOT table.
+
+Layouts (row-major, last index contiguous):
+
+====================  =======================  ==============================
+tensor                shape                    storage
+====================  =======================  ==============================
+q, k                  [B, T, HK, DK]           f32 or bf16 (``qkv_dtype``)
+v                     [B, T, HV, DV]           f32 or bf16
+a, b                  [B, T, HV]               same as q/k/v
+A_log, dt_bias        [HV]                     f32
+pool                  [num_slots, HV, DV, DK]  f32 or bf16 (``state_dtype``)
+indices               [B]                      int32, -1 = padded lane
+accept_len            [B]                      int32 in 1..T
+====================  =======================  ==============================
+
+bf16 arrays are returned as ``uint16`` bit patterns (round-to-nearest-even from the fp32 draw, done by
+``torch``'s cast).  Every tensor has its own random stream, ``numpy.random.default_rng([seed, tensor_id])``,
+so that a large tensor (the pool) can be drawn or skipped without changing the others.
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, List, Optional
+
+import numpy as np
+
+F32 = "f32"
+BF16 = "bf16"
+POOL_BLOCK = 16  # slots per independent pool stream
+
+# stream ids: one independent generator per tensor
+_STREAM = {"q": 1, "k": 2, "v": 3, "a": 4, "b": 5, "dt_bias": 6, "A_log": 7, "pool": 8,
+           "slots": 9, "pad": 10, "accept_len": 11}
+
+
+def _rng(seed: int, name: str) -> np.random.Generator:
+    return np.random.default_rng([int(seed), _STREAM[name]])
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even, via torch's cast."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp32 values (exact widening)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _store(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == F32:
+        return np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == BF16:
+        return to_bf16_bits(x)
+    raise ValueError(dtype)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic GDN workload.  ``mode`` is ``"decode"`` (write-back, no cache) or ``"verify"``."""
+
+    name: str
+    B: int
+    T: int
+    HK: int
+    HV: int
+    DK: int
+    DV: int
+    num_slots: int
+    qkv_dtype: str
+    state_dtype: str
+    out_dtype: str
+    mode: str
+    cache: bool
+    commit: bool
+    seed: int
+    pool_std: float = 0.05
+    pad_fraction: float = 0.0
+    scale: float = 1.0
+    l2_eps: float = 1e-6
+
+    @property
+    def n_padded(self) -> int:
+        return int(round(self.pad_fraction * self.B))
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    # -- draws -----------------------------------------------------------------------------------
+    def small_arrays(self) -> Dict[str, np.ndarray]:
+        """Everything except the pool."""
+        B, T, HK, HV, DK, DV = self.B, self.T, self.HK, self.HV, self.DK, self.DV
+        s = self.seed
+        out: Dict[str, np.ndarray] = {}
+        f32 = np.float32
+        out["q"] = _store(_rng(s, "q").standard_normal((B, T, HK, DK), dtype=f32), self.qkv_dtype)
+        out["k"] = _store(_rng(s, "k").standard_normal((B, T, HK, DK), dtype=f32), self.qkv_dtype)
+        out["v"] = _store(_rng(s, "v").standard_normal((B, T, HV, DV), dtype=f32), self.qkv_dtype)
+        out["a"] = _store(_rng(s, "a").standard_normal((B, T, HV), dtype=f32), self.qkv_dtype)
+        out["b"] = _store(_rng(s, "b").standard_normal((B, T, HV), dtype=f32), self.qkv_dtype)
+        out["dt_bias"] = _rng(s, "dt_bias").standard_normal(HV, dtype=f32)
+        out["A_log"] = np.log(_rng(s, "A_log").uniform(1.0, 16.0, HV)).astype(f32)
+        if B > self.num_slots:
+            raise ValueError("more lanes than pool slots: distinct slots are impossible")
+        slots = _rng(s, "slots").permutation(self.num_slots)[:B].astype(np.int32)
+        if self.n_padded:
+            pad = _rng(s, "pad").permutation(B)[: self.n_padded]
+            slots[pad] = -1
+        out["indices"] = slots
+        out["accept_len"] = _rng(s, "accept_len").integers(1, T + 1, B).astype(np.int32)
+        return out
+
+    def pool(self) -> np.ndarray:
+        """Pool ~ N(0, pool_std^2); drawn in blocks of POOL_BLOCK slots, each from its own stream
+        ``default_rng([seed, pool_id, block])`` so that blocks can be filled by parallel threads."""
+        shape = (self.num_slots, self.HV, self.DV, self.DK)
+        x = np.empty(shape, np.float32)
+        nblk = (self.num_slots + POOL_BLOCK - 1) // POOL_BLOCK
+
+        def fill(i: int) -> None:
+            g = np.random.default_rng([int(self.seed), _STREAM["pool"], i])
+            blk = x[i * POOL_BLOCK:(i + 1) * POOL_BLOCK]
+            g.standard_normal(out=blk, dtype=np.float32)
+            blk *= np.float32(self.pool_std)
+
+        with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+            list(ex.map(fill, range(nblk)))
+        return _store(x, self.state_dtype)
+
+    def arrays(self) -> Dict[str, np.ndarray]:
+        out = self.small_arrays()
+        out["pool"] = self.pool()
+        return out
+
+    def active_lanes(self, indices: Optional[np.ndarray] = None) -> int:
+        if indices is None:
+            indices = self.small_arrays()["indices"]
+        return int((indices >= 0).sum())
+
+
+def tiny() -> Workload:
+    """B=2, 4 slots, HK=HV=2, DK=DV=16, T=2, all fp32, pool ~ N(0, 0.1), seed 0."""
+    return Workload("tiny_B2_T2_d16_f32", B=2, T=2, HK=2, HV=2, DK=16, DV=16, num_slots=4,
+                    qkv_dtype=F32, state_dtype=F32, out_dtype=F32, mode="verify", cache=True,
+                    commit=True, seed=0, pool_std=0.1)
+
+
+def decode_t1() -> Workload:
+    """Decode T=1: B=64, HK=16, HV=32, 128x128, bf16 q/k/v, fp32 pool of 256 slots ~ N(0, 0.05)."""
+    return Workload("decode_T1_B64_f32state", B=64, T=1, HK=16, HV=32, DK=128, DV=128, num_slots=256,
+                    qkv_dtype=BF16, state_dtype=F32, out_dtype=BF16, mode="decode", cache=False,
+                    commit=False, seed=1)
+
+
+def verify_t4() -> Workload:
+    """MTP verify T=4 (3 drafts + 1): B=128, bf16 state pool of 512 slots, bf16 cache, then commit."""
+    return Workload("mtp_verify_T4_B128_bf16state", B=128, T=4, HK=16, HV=32, DK=128, DV=128,
+                    num_slots=512, qkv_dtype=BF16, state_dtype=BF16, out_dtype=BF16, mode="verify",
+                    cache=True, commit=True, seed=2)
+
+
+def verify_t8() -> Workload:
+    """MTP verify T=8: B=256 with 10% padded lanes (index -1), bf16 pool of 1024 slots, cache, commit."""
+    return Workload("mtp_verify_T8_B256_pad10_bf16state", B=256, T=8, HK=16, HV=32, DK=128, DV=128,
+                    num_slots=1024, qkv_dtype=BF16, state_dtype=BF16, out_dtype=BF16, mode="verify",
+                    cache=True, commit=True, seed=3, pad_fraction=0.1)
+
+
+SWEEP_B = (1, 4, 16, 64, 128, 256)
+SWEEP_T = (1, 2, 4, 8)
+SWEEP_STATE = (F32, BF16)
+
+
+def sweep() -> List[Workload]:
+    """B x T x state dtype; T=1 runs as decode, T>1 as verify with caching; pool 1024 slots."""
+    pts = []
+    i = 0
+    for st in SWEEP_STATE:
+        for T in SWEEP_T:
+            for B in SWEEP_B:
+                dec = T == 1
+                pts.append(Workload(f"sweep_B{B}_T{T}_{st}state", B=B, T=T, HK=16, HV=32, DK=128, DV=128,
+                                    num_slots=1024, qkv_dtype=BF16, state_dtype=st, out_dtype=BF16,
+                                    mode="decode" if dec else "verify", cache=not dec, commit=not dec,
+                                    seed=1000 + i))
+                i += 1
+    return pts
+
+
+NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8}

@@ -1,0 +1,177 @@
+"""CPU oracle for the Gated DeltaNet decode / MTP-verify / commit path.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline`` leg
+and ``--impl reference`` arm may import this package.  It shares no code with the CUDA library in
+``gated_deltanet_linear_mtp_gb300`` and neither imports the other.
+
+* ``gdn_oracle.c``  -- the loop oracle (fp64, plain loops); wrapped here through ``ctypes``.
+* ``brute.py``      -- an independent NumPy product-form restatement used to pin the loop oracle.
+* ``build.py``      -- compiles ``gdn_oracle.c`` with gcc into ``oracle/_build/libgdn_oracle.so``.
+
+Arrays are passed in their storage form: fp32 as ``float32``, bf16 as ``uint16`` bit patterns, fp64 as
+``float64`` (fp64 storage exists only here, for chained-call pins without storage rounding).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms, library special
+cases, brute force on tiny inputs, chained-call identities); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+
+from . import build as _build
+
+DTYPE_CODE = {"f32": 0, "bf16": 1, "f64": 2}
+NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("HK", ctypes.c_int32), ("HV", ctypes.c_int32),
+                ("DK", ctypes.c_int32), ("DV", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+                ("qkv_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32), ("cache_dtype", ctypes.c_int32),
+                ("scale", ctypes.c_double), ("l2_eps", ctypes.c_double)]
+
+
+def _ptr(x: Optional[np.ndarray]):
+    if x is None:
+        return None
+    assert x.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return x.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes handle on one build of ``gdn_oracle.c`` (the default build, or a test's variant)."""
+
+    def __init__(self, lib_path: Optional[str] = None):
+        if lib_path is None:
+            lib_path = _build.library_path()
+            if not os.path.exists(lib_path):
+                _build.build()
+        self.path = lib_path
+        self.lib = ctypes.CDLL(lib_path)
+        vp, dp, ip = ctypes.c_void_p, ctypes.POINTER(_Dims), ctypes.c_void_p
+        self.lib.orc_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp]
+        self.lib.orc_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp]
+        self.lib.orc_commit.argtypes = [dp, vp, ip, vp, ip]
+        for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit):
+            f.restype = ctypes.c_int
+        for name in ("orc_round_bf16", "orc_softplus", "orc_sigmoid"):
+            getattr(self.lib, name).argtypes = [ctypes.c_double]
+            getattr(self.lib, name).restype = ctypes.c_double
+        self.lib.orc_gate.argtypes = [ctypes.c_double] * 3
+        self.lib.orc_gate.restype = ctypes.c_double
+
+    # -- scalar helpers (exported for the pins) --------------------------------------------------
+    def round_bf16(self, x: float) -> float:
+        return self.lib.orc_round_bf16(float(x))
+
+    def softplus(self, x: float) -> float:
+        return self.lib.orc_softplus(float(x))
+
+    def sigmoid(self, x: float) -> float:
+        return self.lib.orc_sigmoid(float(x))
+
+    def gate(self, A_log: float, a: float, dt_bias: float) -> float:
+        return self.lib.orc_gate(float(A_log), float(a), float(dt_bias))
+
+    # -- calls -----------------------------------------------------------------------------------
+    @staticmethod
+    def _dims(d: Dict, B: int) -> _Dims:
+        cache_dtype = d.get("cache_dtype", d["state_dtype"])
+        return _Dims(B, d["T"], d["HK"], d["HV"], d["DK"], d["DV"], d["num_slots"],
+                     DTYPE_CODE[d["qkv_dtype"]], DTYPE_CODE[d["state_dtype"]], DTYPE_CODE[cache_dtype],
+                     float(d.get("scale", 1.0)), float(d.get("l2_eps", 1e-6)))
+
+    @staticmethod
+    def _check(x: np.ndarray, dtype: str, shape: Tuple[int, ...], name: str) -> np.ndarray:
+        want = NP_STORAGE[dtype]
+        if x.dtype != want or tuple(x.shape) != tuple(shape):
+            raise ValueError(f"{name}: expected {want.__name__}{shape}, got {x.dtype}{x.shape}")
+        return np.ascontiguousarray(x)
+
+    def _inputs(self, d: Dict, x: Dict[str, np.ndarray], B: int):
+        T, HK, HV, DK, DV = d["T"], d["HK"], d["HV"], d["DK"], d["DV"]
+        qd = d["qkv_dtype"]
+        q = self._check(x["q"], qd, (B, T, HK, DK), "q")
+        k = self._check(x["k"], qd, (B, T, HK, DK), "k")
+        v = self._check(x["v"], qd, (B, T, HV, DV), "v")
+        a = self._check(x["a"], qd, (B, T, HV), "a")
+        b = self._check(x["b"], qd, (B, T, HV), "b")
+        A_log = self._check(x["A_log"], "f32", (HV,), "A_log")
+        dt_bias = self._check(x["dt_bias"], "f32", (HV,), "dt_bias")
+        idx = np.ascontiguousarray(x["indices"], dtype=np.int32)
+        if idx.shape != (B,):
+            raise ValueError("indices shape")
+        return q, k, v, a, b, A_log, dt_bias, idx
+
+    def verify(self, d: Dict, x: Dict[str, np.ndarray], cache: bool = True,
+               o: Optional[np.ndarray] = None, cache_out: Optional[np.ndarray] = None):
+        """Returns (o [B,T,HV,DV] fp64, cache [B,T,HV,DV,DK] storage or None, flag word).
+
+        ``o`` / ``cache_out`` may be passed pre-filled (canaries): entries of skipped lanes are left as given.
+        """
+        B = x["q"].shape[0]
+        T, HV, DV, DK = d["T"], d["HV"], d["DV"], d["DK"]
+        q, k, v, a, b, A_log, dt_bias, idx = self._inputs(d, x, B)
+        pool = self._check(x["pool"], d["state_dtype"], (d["num_slots"], HV, DV, DK), "pool")
+        if o is None:
+            o = np.zeros((B, T, HV, DV), np.float64)
+        cd = d.get("cache_dtype", d["state_dtype"])
+        if cache and cache_out is None:
+            cache_out = np.zeros((B, T, HV, DV, DK), NP_STORAGE[cd])
+        dims = self._dims(d, B)
+        flags = self.lib.orc_verify(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                                    _ptr(dt_bias), _ptr(pool), _ptr(idx), _ptr(o),
+                                    _ptr(cache_out) if cache else None)
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return o, (cache_out if cache else None), flags
+
+    def decode(self, d: Dict, x: Dict[str, np.ndarray], pool: np.ndarray, o: Optional[np.ndarray] = None):
+        """Updates ``pool`` in place (active slots); returns (o fp64, flag word)."""
+        B = x["q"].shape[0]
+        q, k, v, a, b, A_log, dt_bias, idx = self._inputs(d, x, B)
+        assert pool.flags["C_CONTIGUOUS"]
+        self._check(pool, d["state_dtype"], (d["num_slots"], d["HV"], d["DV"], d["DK"]), "pool")
+        if o is None:
+            o = np.zeros((B, d["T"], d["HV"], d["DV"]), np.float64)
+        dims = self._dims(d, B)
+        flags = self.lib.orc_decode(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                                    _ptr(dt_bias), _ptr(pool), _ptr(idx), _ptr(o))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return o, flags
+
+    def commit(self, d: Dict, pool: np.ndarray, indices: np.ndarray, cache: np.ndarray,
+               accept_len: np.ndarray) -> int:
+        """pool[idx[b]] = cache[b, L_b - 1] in place; returns the flag word."""
+        B = indices.shape[0]
+        assert pool.flags["C_CONTIGUOUS"] and cache.flags["C_CONTIGUOUS"]
+        self._check(cache, d["state_dtype"], (B, d["T"], d["HV"], d["DV"], d["DK"]), "cache")
+        idx = np.ascontiguousarray(indices, dtype=np.int32)
+        L = np.ascontiguousarray(accept_len, dtype=np.int32)
+        dims = self._dims(d, B)
+        flags = self.lib.orc_commit(ctypes.byref(dims), _ptr(pool), _ptr(idx), _ptr(cache), _ptr(L))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return flags
+
+
+_default: Optional[Oracle] = None
+
+
+def default() -> Oracle:
+    """The oracle built from ``gdn_oracle.c`` as committed (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def dims_of(w) -> Dict:
+    """Dims dict from a ``gdn_workloads.Workload``."""
+    return dict(T=w.T, HK=w.HK, HV=w.HV, DK=w.DK, DV=w.DV, num_slots=w.num_slots, qkv_dtype=w.qkv_dtype,
+                state_dtype=w.state_dtype, scale=w.scale, l2_eps=w.l2_eps)

@@ -1,0 +1,239 @@
+/*
+ * gdn_oracle.c -- plain, slow, obviously-correct CPU reference of the Gated DeltaNet (GDN) recurrent
+ * state update used for decode and for multi-token-prediction (MTP) speculative verify.
+ *
+ * TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * arm may call this.  It shares no code, header or helper with the CUDA library.
+ *
+ * What it computes (the gated delta rule behind FlashInfer's gated_delta_rule_mtp, named in sglang
+ * PR #23273 "[GDN] Enable FlashInfer MTP verify on SM100+ (Blackwell)", Summary; the pages never write the
+ * recurrence out, so it is restated here):
+ *
+ *   for every lane b whose pool index slot = idx[b] is >= 0, and every value head h
+ *   (key head hk = h / (HV / HK), contiguous groups):
+ *     S = pool[slot, h]                                  (DV x DK, read as the exact stored value)
+ *     for t = 0 .. T-1:
+ *       qh = q[b,t,hk] / sqrt(sum(q^2) + eps)            (L2 normalisation, eps inside the root)
+ *       kh = k[b,t,hk] / sqrt(sum(k^2) + eps)
+ *       g    = exp(-exp(A_log[h]) * softplus(a[b,t,h] + dt_bias[h]))
+ *       beta = 1 / (1 + exp(-b[b,t,h]))
+ *       S = g * S
+ *       u = S kh
+ *       S = S + beta * (v[b,t,h] - u) kh^T
+ *       o[b,t,h] = scale * S qh
+ *       verify with caching: cache[b,t,h] = R(S)
+ *     decode: pool[slot, h] = R(S)
+ *   commit: pool[idx[b], h] = cache[b, L_b - 1, h] for lanes with L_b >= 1.
+ *
+ * Padded lanes (index -1) are skipped: the page's padding index guard (sglang PR #23273, Requirements,
+ * FlashInfer #2810).  bf16 state with intermediate caching beyond T > 4: same page, Requirements
+ * (FlashInfer #2679).  A_log is fp32: same page, Summary (A_log.detach().float()).
+ *
+ * Arithmetic is fp64.  R rounds the fp64 running state to the storage type only where a state is stored
+ * (each cache write, the decode write-back): round-to-nearest-even, directly from fp64 (no double
+ * rounding).  The running state of one call is never rounded between tokens.
+ *
+ * Out-of-range data (index < -1 or >= num_slots, accept length outside 0..T) skips the lane and sets a
+ * bit in the returned flag word: bit 0 = index, bit 1 = accept length.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+
+typedef struct {
+    int32_t B, T, HK, HV, DK, DV, num_slots;
+    int32_t qkv_dtype;   /* q, k, v, a, b storage type */
+    int32_t state_dtype; /* pool storage type */
+    int32_t cache_dtype; /* intermediate cache storage type */
+    double scale;
+    double l2_eps;
+} orc_dims;
+
+/* ---- storage types --------------------------------------------------------------------------- */
+
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t w = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Nearest bfloat16 value to x, ties to even, overflow to infinity; returned as a double. */
+double orc_round_bf16(double x) {
+    if (isnan(x) || isinf(x) || x == 0.0) return x;
+    int e;
+    frexp(x, &e);       /* |x| in [2^(e-1), 2^e) */
+    int q = e - 8;      /* bf16 keeps 8 significant bits: the last one weighs 2^(e-8) */
+    if (q < -133) q = -133; /* below the normal range the step is that of the subnormals, 2^-133 */
+    double y = ldexp(nearbyint(ldexp(x, -q)), q);
+    if (fabs(y) >= 0x1p128) y = copysign(INFINITY, x);
+    return y;
+}
+
+static uint16_t double_to_bf16_bits(double x) {
+    if (isnan(x)) return (uint16_t)0x7FC0;
+    float f = (float)orc_round_bf16(x); /* exact: the rounded value is a bf16 value */
+    uint32_t w;
+    memcpy(&w, &f, sizeof w);
+    return (uint16_t)(w >> 16);
+}
+
+static double load(const void* base, int dtype, int64_t i) {
+    switch (dtype) {
+    case ORC_F32: return (double)((const float*)base)[i];
+    case ORC_BF16: return bf16_bits_to_double(((const uint16_t*)base)[i]);
+    case ORC_F64: return ((const double*)base)[i];
+    }
+    return NAN;
+}
+
+static void store(void* base, int dtype, int64_t i, double x) {
+    switch (dtype) {
+    case ORC_F32: ((float*)base)[i] = (float)x; break; /* C conversion: nearest, ties to even */
+    case ORC_BF16: ((uint16_t*)base)[i] = double_to_bf16_bits(x); break;
+    case ORC_F64: ((double*)base)[i] = x; break;
+    }
+}
+
+static size_t dtype_size(int dtype) { return dtype == ORC_F32 ? 4 : dtype == ORC_BF16 ? 2 : 8; }
+
+/* ---- scalar functions ------------------------------------------------------------------------- */
+
+/* softplus(x) = log(1 + e^x); for x > 0 written as x + log(1 + e^-x), the same value without overflow */
+double orc_softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+double orc_gate(double A_log, double a, double dt_bias) {
+    return exp(-exp(A_log) * orc_softplus(a + dt_bias));
+}
+
+/* ---- the recurrence ----------------------------------------------------------------------------- */
+
+static int lane_slot(const orc_dims* d, const int32_t* idx, int b, int* flags) {
+    int32_t slot = idx[b];
+    if (slot == -1) return -1;
+    if (slot < -1 || slot >= d->num_slots) {
+        *flags |= 1;
+        return -1;
+    }
+    return slot;
+}
+
+/* Runs the T tokens of every active lane.  If cache != NULL, stores R(S) after every token (verify).
+ * If write_back, stores R(S) of the last token into the lane's pool slot (decode). */
+static int run(const orc_dims* d, const void* q, const void* k, const void* v, const void* a,
+               const void* bb, const float* A_log, const float* dt_bias, void* pool, const int32_t* idx,
+               double* o, void* cache, int write_back) {
+    const int B = d->B, T = d->T, HK = d->HK, HV = d->HV, DK = d->DK, DV = d->DV;
+    const int r = HV / HK;
+    int flags = 0;
+    double* S = (double*)malloc(sizeof(double) * (size_t)DV * DK);
+    double* qh = (double*)malloc(sizeof(double) * DK);
+    double* kh = (double*)malloc(sizeof(double) * DK);
+    double* u = (double*)malloc(sizeof(double) * DV);
+    if (!S || !qh || !kh || !u) {
+        free(S); free(qh); free(kh); free(u);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        int slot = lane_slot(d, idx, b, &flags);
+        if (slot < 0) continue;
+        for (int h = 0; h < HV; ++h) {
+            const int hk = h / r;
+            const int64_t state_off = ((int64_t)slot * HV + h) * DV * DK;
+            for (int i = 0; i < DV; ++i)
+                for (int j = 0; j < DK; ++j) S[i * DK + j] = load(pool, d->state_dtype, state_off + i * DK + j);
+
+            for (int t = 0; t < T; ++t) {
+                const int64_t qk_off = (((int64_t)b * T + t) * HK + hk) * DK;
+                const int64_t ab_off = ((int64_t)b * T + t) * HV + h;
+                const int64_t v_off = (((int64_t)b * T + t) * HV + h) * DV;
+
+                double qq = 0.0, kk = 0.0;
+                for (int j = 0; j < DK; ++j) {
+                    double qj = load(q, d->qkv_dtype, qk_off + j), kj = load(k, d->qkv_dtype, qk_off + j);
+                    qq += qj * qj;
+                    kk += kj * kj;
+                }
+                const double qn = sqrt(qq + d->l2_eps), kn = sqrt(kk + d->l2_eps);
+                for (int j = 0; j < DK; ++j) {
+                    qh[j] = load(q, d->qkv_dtype, qk_off + j) / qn;
+                    kh[j] = load(k, d->qkv_dtype, qk_off + j) / kn;
+                }
+                const double g = orc_gate(A_log[h], load(a, d->qkv_dtype, ab_off), dt_bias[h]);
+                const double beta = orc_sigmoid(load(bb, d->qkv_dtype, ab_off));
+
+                for (int i = 0; i < DV * DK; ++i) S[i] *= g;
+                for (int i = 0; i < DV; ++i) {
+                    double s = 0.0;
+                    for (int j = 0; j < DK; ++j) s += S[i * DK + j] * kh[j];
+                    u[i] = s;
+                }
+                for (int i = 0; i < DV; ++i) {
+                    const double delta = beta * (load(v, d->qkv_dtype, v_off + i) - u[i]);
+                    for (int j = 0; j < DK; ++j) S[i * DK + j] += delta * kh[j];
+                }
+                for (int i = 0; i < DV; ++i) {
+                    double s = 0.0;
+                    for (int j = 0; j < DK; ++j) s += S[i * DK + j] * qh[j];
+                    o[v_off + i] = d->scale * s;
+                }
+                if (cache) {
+                    const int64_t c_off = ((((int64_t)b * T + t) * HV) + h) * DV * DK;
+                    for (int i = 0; i < DV * DK; ++i) store(cache, d->cache_dtype, c_off + i, S[i]);
+                }
+            }
+            if (write_back)
+                for (int i = 0; i < DV * DK; ++i) store(pool, d->state_dtype, state_off + i, S[i]);
+        }
+    }
+    free(S); free(qh); free(kh); free(u);
+    return flags;
+}
+
+static int dims_ok(const orc_dims* d) {
+    return d->B >= 0 && d->T >= 1 && d->HK >= 1 && d->HV >= 1 && d->HV % d->HK == 0 && d->DK >= 1 &&
+           d->DV >= 1 && d->num_slots >= 1;
+}
+
+/* T tokens from pool[idx[b]] (read only); o in fp64; cache (nullable) in cache_dtype. */
+int orc_verify(const orc_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
+               const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, double* o,
+               void* cache) {
+    if (!dims_ok(d)) return -2;
+    return run(d, q, k, v, a, b, A_log, dt_bias, (void*)pool, idx, o, cache, 0);
+}
+
+/* T tokens from pool[idx[b]], final state written back into the same slot. */
+int orc_decode(const orc_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
+               const float* A_log, const float* dt_bias, void* pool, const int32_t* idx, double* o) {
+    if (!dims_ok(d)) return -2;
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1);
+}
+
+/* pool[idx[b], :] = cache[b, L_b - 1, :] (all heads), bit for bit, for active lanes with L_b >= 1. */
+int orc_commit(const orc_dims* d, void* pool, const int32_t* idx, const void* cache, const int32_t* accept_len) {
+    if (!dims_ok(d)) return -2;
+    if (d->cache_dtype != d->state_dtype) return -3;
+    int flags = 0;
+    const size_t es = dtype_size(d->state_dtype);
+    const int64_t per_lane = (int64_t)d->HV * d->DV * d->DK;
+    for (int b = 0; b < d->B; ++b) {
+        int slot = lane_slot(d, idx, b, &flags);
+        if (slot < 0) continue;
+        const int L = accept_len[b];
+        if (L < 0 || L > d->T) {
+            flags |= 2;
+            continue;
+        }
+        if (L == 0) continue;
+        const char* src = (const char*)cache + (((int64_t)b * d->T) + (L - 1)) * per_lane * (int64_t)es;
+        char* dst = (char*)pool + (int64_t)slot * per_lane * (int64_t)es;
+        memcpy(dst, src, (size_t)(per_lane * (int64_t)es));
+    }
+    return flags;
+}

@@ -1,0 +1,77 @@
+"""The oracle's pins are strong enough: a plausible mistake planted in a copy of the oracle fails at least
+one of them.  Every mutant is compiled from a text-substituted copy of ``oracle/gdn_oracle.c`` into a
+temporary directory, on the CPU; the committed oracle is never modified."""
+import os
+
+import pytest
+
+import oracle
+import oracle_checks as C
+from oracle import build as obuild
+
+# (name, text in gdn_oracle.c, replacement)
+MUTANTS = [
+    ("gate_sign", "return exp(-exp(A_log) * orc_softplus(a + dt_bias));",
+     "return exp(exp(A_log) * orc_softplus(a + dt_bias));"),
+    ("dt_bias_sign", "return exp(-exp(A_log) * orc_softplus(a + dt_bias));",
+     "return exp(-exp(A_log) * orc_softplus(a - dt_bias));"),
+    ("gate_no_exp_of_A_log", "return exp(-exp(A_log) * orc_softplus(a + dt_bias));",
+     "return exp(-A_log * orc_softplus(a + dt_bias));"),
+    ("gate_softplus_dropped", "return exp(-exp(A_log) * orc_softplus(a + dt_bias));",
+     "return exp(-exp(A_log) * (a + dt_bias));"),
+    ("softplus_positive_branch", "return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));",
+     "return x > 0.0 ? x : log1p(exp(x));"),
+    ("sigmoid_sign", "double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }",
+     "double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(x)); }"),
+    ("eps_outside_root", "const double qn = sqrt(qq + d->l2_eps), kn = sqrt(kk + d->l2_eps);",
+     "const double qn = sqrt(qq) + d->l2_eps, kn = sqrt(kk) + d->l2_eps;"),
+    ("k_not_normalised", "kh[j] = load(k, d->qkv_dtype, qk_off + j) / kn;",
+     "kh[j] = load(k, d->qkv_dtype, qk_off + j);"),
+    ("decay_dropped", "for (int i = 0; i < DV * DK; ++i) S[i] *= g;", ""),
+    ("u_uses_query", "for (int j = 0; j < DK; ++j) s += S[i * DK + j] * kh[j];",
+     "for (int j = 0; j < DK; ++j) s += S[i * DK + j] * qh[j];"),
+    ("beta_dropped", "const double delta = beta * (load(v, d->qkv_dtype, v_off + i) - u[i]);",
+     "const double delta = (load(v, d->qkv_dtype, v_off + i) - u[i]);"),
+    ("delta_sign", "const double delta = beta * (load(v, d->qkv_dtype, v_off + i) - u[i]);",
+     "const double delta = beta * (load(v, d->qkv_dtype, v_off + i) + u[i]);"),
+    ("v_index", "load(v, d->qkv_dtype, v_off + i)", "load(v, d->qkv_dtype, v_off)"),
+    ("head_mapping_modulo", "const int hk = h / r;", "const int hk = h % HK;"),
+    ("output_skips_scale", "o[v_off + i] = d->scale * s;", "o[v_off + i] = s;"),
+    ("cache_token_index", "const int64_t c_off = ((((int64_t)b * T + t) * HV) + h) * DV * DK;",
+     "const int64_t c_off = ((((int64_t)b * T + 0) * HV) + h) * DV * DK;"),
+    ("bf16_truncates", "double y = ldexp(nearbyint(ldexp(x, -q)), q);",
+     "double y = ldexp(trunc(ldexp(x, -q)), q);"),
+    ("bf16_keeps_9_bits", "int q = e - 8;", "int q = e - 9;"),
+    ("commit_first_token", "(((int64_t)b * d->T) + (L - 1)) * per_lane", "(((int64_t)b * d->T) + 0) * per_lane"),
+    ("padding_not_skipped", "if (slot == -1) return -1;", "if (slot == -1) return 0;"),
+    ("accept_len_unchecked", "if (L < 0 || L > d->T) {", "if (0) {"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(obuild.SOURCE) as f:
+        return f.read()
+
+
+def test_mutant_targets_present(source):
+    for name, old, _ in MUTANTS:
+        assert source.count(old) >= 1, name
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, source, name, old, new):
+    mutated = source.replace(old, new)
+    assert mutated != source
+    src = tmp_path / "gdn_oracle_mutant.c"
+    src.write_text(mutated)
+    lib = obuild.build(str(src), str(tmp_path / "libmutant.so"), extra=["-w"])
+    orc = oracle.Oracle(lib)
+    failures = []
+    for check in C.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, ValueError, FloatingPointError) as e:  # a pin caught it
+            failures.append(check.__name__)
+    assert failures, f"mutant {name} passed every pin"
+    os.remove(lib)
