@@ -1,0 +1,539 @@
+"""Benchmark of the GDN MTP-verify step on one GB300 (or N independent replicas under torchrun).
+
+One step = ``gdn_mtp_verify`` (T=4 draft tokens, B=128 requests, HK=16, HV=32, 128x128 bf16 states from a
+512-slot pool, intermediate states cached) followed by ``gdn_commit`` of the accepted prefixes -- the MTP
+verify step of sglang PR #23273 "[GDN] Enable FlashInfer MTP verify on SM100+ (Blackwell)" (NEXTN, 3 steps +
+1 token; bf16 SSM state) on synthetic data.  Inputs are resident in HBM when the timed region starts;
+L2 (129 MB) is flushed between steps, outside each step's CUDA events: a 256 MiB write, then a 256 MiB read
+so that the lines left in L2 are clean.
+
+    python bench.py [--steps K] [--warmup W] [--workload verify4|verify8|decode|sweep] [--impl reference]
+
+Prints one JSON line (``--workload sweep``: one per point).  ``value`` = verified tokens/s (A x T per step,
+A = non-padded lanes, summed over ranks, divided by the slowest rank's device time).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_workloads as W  # noqa: E402
+
+METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
+                  "gated_deltanet_linear_mtp_gb300/csrc/gdn_commit.cu"]
+
+
+# ---------------------------------------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_workload(w: W.Workload, rank: int) -> W.Workload:
+    """Weak scaling: every rank runs its own batch of the same shape (independent requests, no exchange)."""
+    if rank == 0:
+        return w
+    return w.replace(seed=w.seed + 7919 * rank, pool_seed=None if w.pool_seed is None else w.pool_seed + 7919 * rank)
+
+
+# ---- algorithmic bytes ------------------------------------------------------------------------------------
+def esize(d: str) -> int:
+    return 4 if d == "f32" else 2
+
+
+def recurrent_bytes(w: W.Workload, A: int) -> int:
+    """Bytes the method must move in one decode / verify launch for A active lanes."""
+    s, i, ob = esize(w.state_dtype), esize(w.qkv_dtype), esize(w.out_dtype)
+    E = w.DV * w.DK
+    state_read = A * w.HV * E * s
+    state_write = A * w.T * w.HV * E * s if w.cache else 0
+    if w.mode == "decode":
+        state_write = A * w.HV * E * s
+    per_tok = 2 * w.HK * w.DK * i + w.HV * w.DV * i + w.HV * w.DV * ob + 2 * w.HV * i
+    return state_read + state_write + A * w.T * per_tok + w.HV * 8 + w.B * 4
+
+
+def commit_bytes(w: W.Workload, A: int) -> int:
+    return 2 * A * w.HV * w.DV * w.DK * esize(w.state_dtype) + 2 * w.B * 4
+
+
+# ---- peaks, traffic, clocks -------------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the verify/decode kernel from a committed ncu summary, if it was taken on the
+    current kernel sources (``kernel_source_sha256`` line); else None."""
+    p = os.path.join(ROOT, "profiles", f"gdn_recurrent_{workload_name}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons of the benchmarked GPU while the timed region runs.
+
+    Read-only NVML queries through ctypes (libnvidia-ml ships with the driver); falls back to an
+    ``nvidia-smi -lms`` subprocess.  Changes no setting."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.samples = []
+        self.period = period_s
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self.source = None
+        try:
+            import torch
+
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise RuntimeError("handle")
+            self._nvml, self._handle = nv, h
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.source = "nvml"
+        except Exception:
+            self.source = "nvidia-smi"
+            self._bus = None
+
+    def _sample_nvml(self):
+        nv, h = self._nvml, self._handle
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            self._reasons_fn(h, ctypes.byref(rs))
+            if ok:
+                self.samples.append((clk.value, pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.source == "nvml":
+            self._thread = threading.Thread(target=self._sample_nvml, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE, text=True)
+            except Exception:
+                self._proc = None
+
+    def stop(self):
+        if self.source == "nvml":
+            self._stop.set()
+            self._thread.join()
+        elif getattr(self, "_proc", None) is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                try:
+                    c, m, p, r = [x.strip() for x in line.split(",")]
+                    self.samples.append((float(c), float(p), int(r, 16)))
+                    self.max_mhz = float(m)
+                except Exception:
+                    pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.source}
+        clocks = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[2]
+        reasons = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(clocks), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "power_w_max": max(s[1] for s in self.samples), "source": self.source}
+
+
+# ---- the CUDA arm -----------------------------------------------------------------------------------------
+class Step:
+    """Device buffers of one workload and the calls of one step, through the public binding."""
+
+    def __init__(self, w: W.Workload, device):
+        import torch
+
+        import gated_deltanet_linear_mtp_gb300 as gdn
+
+        self.gdn, self.torch, self.w = gdn, torch, w
+        x = w.arrays()
+        self.x = x
+        self.A = int((x["indices"] >= 0).sum())
+
+        def t(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+            return torch.from_numpy(a).to(device)
+
+        self.d = {k: t(v) for k, v in x.items()}
+        td = {"f32": torch.float32, "bf16": torch.bfloat16}
+        self.o = torch.empty((w.B, w.T, w.HV, w.DV), dtype=td[w.out_dtype], device=device)
+        self.cache = (torch.empty((w.B, w.T, w.HV, w.DV, w.DK), dtype=td[w.state_dtype], device=device)
+                      if w.cache else None)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        # pinned host copies of the per-step inputs (end-to-end leg)
+        self.step_keys = ["q", "k", "v", "a", "b", "indices"] + (["accept_len"] if w.commit else [])
+        self.h_in = {k: self.d[k].cpu().pin_memory() for k in self.step_keys}
+        self.h_out = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.h_in.values())
+        self.d2h_bytes = self.o.numel() * self.o.element_size()
+
+    def recurrent(self):
+        d, w = self.d, self.w
+        if w.mode == "decode":
+            self.gdn.gdn_decode(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
+                                d["indices"], self.o, self.err, scale=w.scale, l2_eps=w.l2_eps)
+        else:
+            self.gdn.gdn_mtp_verify(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
+                                    d["indices"], self.o, self.cache, self.err, scale=w.scale, l2_eps=w.l2_eps)
+
+    def commit(self):
+        if self.w.commit:
+            d = self.d
+            self.gdn.gdn_commit(d["pool"], d["indices"], self.cache, d["accept_len"], self.err)
+
+    def upload(self):
+        for k in self.step_keys:
+            self.d[k].copy_(self.h_in[k], non_blocking=True)
+
+    def download(self):
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 1 + (1 if self.w.commit else 0)
+
+
+def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, emit=True):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(world, "nccl")
+    wr = rank_workload(w, rank)
+    st = Step(wr, device)
+    props = torch.cuda.get_device_properties(device)
+    nflush = max(256 << 20, 2 * props.L2_cache_size) // 4
+    flush_w = torch.empty(nflush, dtype=torch.float32, device=device)
+    flush_r = torch.zeros(nflush, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def flush_l2():
+        # write a buffer larger than L2 (evicts everything), then read another one so that the lines left
+        # in L2 are clean and the timed step does not pay for writing the flush's dirty lines back
+        flush_w.fill_(1.0)
+        flush_r.sum()
+
+    def one(ev=None, e2e=False):
+        flush_l2()
+        if ev is not None:
+            ev[0].record(stream)
+        if e2e:
+            st.upload()
+        st.recurrent()
+        if ev is not None:
+            ev[1].record(stream)
+        st.commit()
+        if e2e:
+            st.download()
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error word {st.err.item()} after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        one(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    rec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(sum(step_ms), dist, device)
+    tokens_rank = st.A * wr.T * K
+    tokens_all = sum_over_ranks(tokens_rank, dist, device)
+
+    # end-to-end: host->device inputs, the two calls, device->host o, every step
+    for _ in range(max(1, args.warmup)):
+        one(e2e=True)
+    torch.cuda.synchronize()
+    evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    for i in range(K):
+        one(evs2[i], e2e=True)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in evs2), dist, device)
+
+    peak, peak_src = hbm_peak()
+    rb = recurrent_bytes(wr, st.A)
+    rec_avg_ms = statistics.mean(rec_ms)
+    achieved = rb / (rec_avg_ms * 1e-3) / 1e9
+    step_bytes = rb + (commit_bytes(wr, st.A) if wr.commit else 0)
+    clocks = sampler.summary()
+    result = {
+        "metric": METRIC,
+        "value": tokens_all / (total_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy draws; shapes and distributions of the named workload)",
+        "config": {
+            "workload": w.name, "B": w.B, "active_lanes": st.A, "T": w.T, "HK": w.HK, "HV": w.HV, "DK": w.DK,
+            "DV": w.DV, "num_slots": w.num_slots, "state_dtype": w.state_dtype, "qkv_dtype": w.qkv_dtype,
+            "out_dtype": w.out_dtype, "intermediate_cache": w.cache, "commit_per_step": w.commit,
+            "step": ("gdn_mtp_verify + gdn_commit" if w.commit else ("gdn_decode" if w.mode == "decode"
+                                                                      else "gdn_mtp_verify")),
+            "l2": "flushed before every step outside its CUDA events (256 MiB write, then 256 MiB read: clean lines)",
+            "parallelism": f"replicas x{world} (independent batches, no collective)",
+            "timing": "CUDA events per step on the launch stream, summed; max over ranks",
+        },
+        "verify_steps_per_s": K * world / (total_ms * 1e-3),
+        "hbm_gbs_step": step_bytes * world * K / (total_ms * 1e-3) / 1e9,
+        "roofline": {
+            "kernel": "gdn_recurrent_kernel (" + ("decode" if w.mode == "decode" else "verify") + ")",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
+            "algorithmic_bytes_per_launch": rb,
+            "avg_launch_us": rec_avg_ms * 1e3,
+            "traffic": recorded_traffic(w.name),
+        },
+        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": st.h2d_bytes,
+                "d2h_bytes_per_step": st.d2h_bytes},
+        "gpu_launches": st.launches_per_step * K,
+        "clocks": clocks,
+        "device": props.name,
+        "sm_count": props.multi_processor_count,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline and emit:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0 and emit:
+        print(json.dumps(result), flush=True)
+    return result
+
+
+# ---- the oracle as CPU baseline / reference arm -----------------------------------------------------------
+def oracle_pairs(w: W.Workload, x: dict, pairs):
+    """Per (lane, value head) inputs for the oracle: one lane, one head, its own one-slot pool copy."""
+    r = w.HV // w.HK
+    out = []
+    for b, h in pairs:
+        hk = h // r
+        slot = int(x["indices"][b])
+        y = {
+            "q": np.ascontiguousarray(x["q"][b:b + 1, :, hk:hk + 1]),
+            "k": np.ascontiguousarray(x["k"][b:b + 1, :, hk:hk + 1]),
+            "v": np.ascontiguousarray(x["v"][b:b + 1, :, h:h + 1]),
+            "a": np.ascontiguousarray(x["a"][b:b + 1, :, h:h + 1]),
+            "b": np.ascontiguousarray(x["b"][b:b + 1, :, h:h + 1]),
+            "A_log": np.ascontiguousarray(x["A_log"][h:h + 1]),
+            "dt_bias": np.ascontiguousarray(x["dt_bias"][h:h + 1]),
+            "pool": np.ascontiguousarray(x["pool"][slot:slot + 1, h:h + 1]),
+            "indices": np.zeros(1, np.int32),
+            "accept_len": np.ascontiguousarray(x["accept_len"][b:b + 1]),
+        }
+        out.append(y)
+    return out
+
+
+def oracle_pair_step(orc, w: W.Workload, d: dict, y: dict):
+    """The oracle's share of one step for one (lane, head): verify (+ commit), or decode."""
+    if w.mode == "decode":
+        orc.decode(d, y, y["pool"])
+        return
+    _, cache, _ = orc.verify(d, y, cache=w.cache)
+    if w.commit:
+        orc.commit(d, y["pool"], y["indices"], cache, y["accept_len"])
+
+
+def _pair_setup(w: W.Workload):
+    import oracle
+
+    orc = oracle.default()
+    x = w.arrays()
+    d = dict(oracle.dims_of(w), HV=1, HK=1, num_slots=1)
+    active = np.flatnonzero(x["indices"] >= 0)
+    pairs = [(int(b), h) for b in active for h in range(w.HV)]
+    return orc, x, d, pairs
+
+
+def cpu_baseline(w: W.Workload, seconds: float):
+    """The oracle as it stands (one thread, fp64 C loops) on a bounded sample of the workload: (lane, head)
+    pairs in order until `seconds` of CPU work; tokens/s = pairs * T / HV / time."""
+    orc, x, d, pairs = _pair_setup(w)
+    done, t0 = 0, time.perf_counter()
+    for chunk in range(0, len(pairs), 32):
+        for y in oracle_pairs(w, x, pairs[chunk:chunk + 32]):
+            oracle_pair_step(orc, w, d, y)
+            done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done * w.T / w.HV / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle step (verify+commit) of the first {done} of {len(pairs)} (lane, head) pairs of "
+                      f"{w.name}, fp64 C loops, one thread, {dt:.1f} s"}
+
+
+def run_reference_arm(args, w: W.Workload, rank: int, world: int):
+    """The reference arm is the oracle: each step runs a bounded sample of (lane, head) pairs, sized so that
+    warm-up + steps take about --ref-seconds in total.  Only rank 0 works."""
+    if rank != 0:
+        return
+    orc, x, d, pairs = _pair_setup(w)
+    probe = oracle_pairs(w, x, pairs[:1])[0]
+    t0 = time.perf_counter()
+    oracle_pair_step(orc, w, d, probe)
+    t_pair = max(time.perf_counter() - t0, 1e-6)
+    per_step = args.ref_seconds / (args.steps + args.warmup)
+    n = int(max(1, min(len(pairs), per_step // t_pair)))
+    sample = oracle_pairs(w, x, pairs[:n])
+    for _ in range(args.warmup):
+        for y in sample:
+            oracle_pair_step(orc, w, d, y)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for y in sample:
+            oracle_pair_step(orc, w, d, y)
+    dt = time.perf_counter() - t0
+    v = n * w.T / w.HV * args.steps / dt
+    desc = (f"each step: oracle verify+commit of {n} of {len(pairs)} (lane, head) pairs of {w.name}, "
+            f"fp64 C loops, one thread; tokens/s = pairs * T / HV / time")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w.name},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["verify4", "verify8", "decode", "sweep", "tiny"], default="verify4")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.workload == "sweep":
+        pts = W.sweep()
+    else:
+        pts = [W.NAMED[args.workload]()]
+    for w in pts:
+        if args.impl == "reference":
+            run_reference_arm(args, w, rank, world)
+        else:
+            run_cuda_arm(args, w, rank, world, local_rank)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+"""Gated DeltaNet (GDN) decode / MTP-verify / commit on one GB300 -- Python binding of ``libgdn.so``.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA kernels
+(``csrc/``); PyTorch supplies device memory and the current stream.  There is no CPU fallback: if the
+library has not been built, every call raises.
+
+    gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, scale=1.0, l2_eps=1e-6)
+    gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
+    gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
+
+Shapes and semantics are those of ``include/gdn.h``: q, k ``[B,T,HK,DK]``; v, o ``[B,T,HV,DV]``; a, b
+``[B,T,HV]``; A_log, dt_bias ``[HV]`` fp32; state_pool ``[num_slots,HV,DV,DK]``; state_indices, accept_len
+``[B]`` int32; intermediate_states ``[B,T,HV,DV,DK]``; err_word a 1-element int32 device tensor.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIB_PATH
+
+__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "GdnError", "GdnDims", "lib", "STATUS",
+           "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "MAX_T", "EXPORTS"]
+
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
+          5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_VALUE"}
+ERRBIT_INDEX = 1
+ERRBIT_ACCEPT_LEN = 2
+MAX_T = 16
+F32, BF16 = 0, 1
+EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_status_string", "gdn_last_cuda_error",
+           "gdn_abi_version")
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("HK", ctypes.c_int32), ("HV", ctypes.c_int32),
+                ("DK", ctypes.c_int32), ("DV", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+                ("qkv_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib_handle.gdn_status_string(status).decode() if _lib_handle is not None else STATUS.get(status)
+        if status == 6 and _lib_handle is not None:
+            msg += f" (cudaError {_lib_handle.gdn_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libgdn.so``; raises if it has not been built (no fallback exists)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m gated_deltanet_linear_mtp_gb300.build` (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, dp, ip = ctypes.c_void_p, ctypes.POINTER(GdnDims), ctypes.c_void_p
+        L.gdn_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, ip, vp]
+        L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
+        L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
+        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit):
+            f.restype = ctypes.c_int
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_last_cuda_error.restype = ctypes.c_int32
+        L.gdn_abi_version.restype = ctypes.c_int32
+        _lib_handle = L
+    return _lib_handle
+
+
+# ---- marshalling -------------------------------------------------------------------------------------
+def _code(t, name: str) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"{name}: dtype {t.dtype} (fp32 or bf16 expected)")
+
+
+def _dev(t, name: str, dtype=None):
+    """Pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _shape(t, want, name: str):
+    if tuple(t.shape) != tuple(want):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(want)}")
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps) -> GdnDims:
+    import torch
+
+    if q.dim() != 4 or v.dim() != 4 or state_pool.dim() != 4:
+        raise ValueError("q/k and v/o are 4-D, state_pool is 4-D")
+    B, T, HK, DK = q.shape
+    HV, DV = v.shape[2], v.shape[3]
+    _shape(k, q.shape, "k")
+    _shape(v, (B, T, HV, DV), "v")
+    _shape(o, (B, T, HV, DV), "o")
+    _shape(a, (B, T, HV), "a")
+    _shape(b, (B, T, HV), "b")
+    _shape(A_log, (HV,), "A_log")
+    _shape(dt_bias, (HV,), "dt_bias")
+    _shape(state_indices, (B,), "state_indices")
+    num_slots = state_pool.shape[0]
+    _shape(state_pool, (num_slots, HV, DV, DK), "state_pool")
+    qkv = _code(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (a, "a"), (b, "b")):
+        if _code(t, n) != qkv:
+            raise TypeError(f"{n} must have q's dtype")
+    for t, n in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if t.dtype != torch.float32:
+            raise TypeError(f"{n} must be fp32")
+    if state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
+    return GdnDims(B, T, HK, HV, DK, DV, num_slots, qkv, _code(state_pool, "state_pool"), _code(o, "o"),
+                   float(scale), float(l2_eps))
+
+
+def _call(status: int, what: str) -> None:
+    if status != 0:
+        raise GdnError(status, what)
+
+
+# ---- the three calls -----------------------------------------------------------------------------------
+def gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, *, scale=1.0,
+               l2_eps=1e-6, stream=None) -> None:
+    """T tokens (normally 1) from ``state_pool[state_indices[b]]``; the final state is written back in place."""
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
+    _call(L.gdn_decode(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+                       _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+                       _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word"),
+                       _stream(stream)), "gdn_decode")
+
+
+def gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None,
+                   err_word=None, *, scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """T draft tokens from ``state_pool[state_indices[b]]`` (read only); optional per-token state cache."""
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
+    if intermediate_states is not None:
+        _shape(intermediate_states, (d.B, d.T, d.HV, d.DV, d.DK), "intermediate_states")
+        if intermediate_states.dtype != state_pool.dtype:
+            raise TypeError("intermediate_states must have state_pool's dtype")
+    _call(L.gdn_mtp_verify(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+                           _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+                           _dev(state_indices, "state_indices"), _dev(o, "o"),
+                           _dev(intermediate_states, "intermediate_states"), _dev(err_word, "err_word"),
+                           _stream(stream)), "gdn_mtp_verify")
+
+
+def gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None, *, stream=None) -> None:
+    """``state_pool[state_indices[b]] = intermediate_states[b, accept_len[b] - 1]`` for active lanes."""
+    import torch
+
+    L = lib()
+    if intermediate_states.dim() != 5 or state_pool.dim() != 4:
+        raise ValueError("intermediate_states is [B,T,HV,DV,DK], state_pool is [num_slots,HV,DV,DK]")
+    B, T, HV, DV, DK = intermediate_states.shape
+    num_slots = state_pool.shape[0]
+    _shape(state_pool, (num_slots, HV, DV, DK), "state_pool")
+    _shape(state_indices, (B,), "state_indices")
+    _shape(accept_len, (B,), "accept_len")
+    if state_indices.dtype != torch.int32 or accept_len.dtype != torch.int32:
+        raise TypeError("state_indices and accept_len must be int32")
+    if intermediate_states.dtype != state_pool.dtype:
+        raise TypeError("intermediate_states must have state_pool's dtype")
+    sd = _code(state_pool, "state_pool")
+    d = GdnDims(B, T, 1, HV, DK, DV, num_slots, sd, sd, sd, 1.0, 0.0)
+    _call(L.gdn_commit(ctypes.byref(d), _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
+                       _dev(intermediate_states, "intermediate_states"), _dev(accept_len, "accept_len"),
+                       _dev(err_word, "err_word"), _stream(stream)), "gdn_commit")

@@ -1,0 +1,171 @@
+// gdn_api.cu -- the C ABI of libgdn.so (include/gdn.h): host-side validation, then one kernel launch on the
+// caller's stream.  Every check that needs no device data happens here, before anything is enqueued, so a
+// rejected call has no side effect.  No allocation, no synchronisation, no global mutable state (the last
+// CUDA error is thread-local).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_dtype(int32_t d) { return d == GDN_F32 || d == GDN_BF16; }
+
+size_t dtype_bytes(int32_t d) { return d == GDN_F32 ? 4 : 2; }
+
+bool supported_dk(int32_t dk) { return dk == 16 || dk == 32 || dk == 64 || dk == 128 || dk == 256; }
+
+// Sizes common to every call.  `need_io`: q/k/v/o dtypes and the scalars matter (decode, verify).
+gdn_status check_dims(const gdn_dims* d, bool need_io) {
+    if (d == nullptr) return GDN_ERR_NULL;
+    if (d->B < 0 || d->B > 65535) return GDN_ERR_SHAPE;
+    if (d->T < 1 || d->T > GDN_MAX_T) return GDN_ERR_SHAPE;
+    if (d->HV < 1 || d->HV > 65535 || d->DV < 1 || d->num_slots < 1) return GDN_ERR_SHAPE;
+    if (!valid_dtype(d->state_dtype)) return GDN_ERR_DTYPE;
+    if (need_io) {
+        if (d->HK < 1 || d->HV % d->HK != 0) return GDN_ERR_SHAPE;
+        if (!valid_dtype(d->qkv_dtype) || !valid_dtype(d->out_dtype)) return GDN_ERR_DTYPE;
+        if (!std::isfinite(d->scale) || !std::isfinite(d->l2_eps) || d->l2_eps < 0.f) return GDN_ERR_VALUE;
+    }
+    if (d->DK < 1) return GDN_ERR_SHAPE;
+    if (!supported_dk(d->DK)) return GDN_ERR_UNSUPPORTED;
+    // every element offset is formed in int64: bound the largest array (the cache) well inside it
+    const double cache_elems = (double)d->B * d->T * d->HV * (double)d->DV * d->DK;
+    const double pool_elems = (double)d->num_slots * d->HV * (double)d->DV * d->DK;
+    if (cache_elems > 4.0e18 || pool_elems > 4.0e18) return GDN_ERR_SHAPE;
+    return GDN_OK;
+}
+
+gdn_status check_io(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
+                    const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, const void* o,
+                    const int32_t* err) {
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !pool || !idx || !o) return GDN_ERR_NULL;
+    const uintptr_t in_sz = dtype_bytes(d->qkv_dtype);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(pool, 16)) return GDN_ERR_ALIGN;
+    if (!aligned(v, in_sz) || !aligned(a, in_sz) || !aligned(b, in_sz)) return GDN_ERR_ALIGN;
+    if (!aligned(A_log, 4) || !aligned(dt_bias, 4) || !aligned(idx, 4)) return GDN_ERR_ALIGN;
+    if (!aligned(o, dtype_bytes(d->out_dtype))) return GDN_ERR_ALIGN;
+    if (err && !aligned(err, 4)) return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+gdn_status finish(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    g_last_cuda_error = (int32_t)e;
+    return GDN_ERR_CUDA;
+}
+
+gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a,
+                         const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
+                         void* pool_out, const int32_t* idx, void* o, void* cache, int32_t* err,
+                         cudaStream_t stream) {
+    RecurrentParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.a = a;
+    p.b = b;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.pool_in = pool_in;
+    p.pool_out = pool_out;
+    p.indices = idx;
+    p.o = o;
+    p.cache = cache;
+    p.err = err;
+    p.T = d->T;
+    p.HK = d->HK;
+    p.HV = d->HV;
+    p.DV = d->DV;
+    p.num_slots = d->num_slots;
+    p.out_bf16 = d->out_dtype == GDN_BF16;
+    p.scale = d->scale;
+    p.l2_eps = d->l2_eps;
+    const bool qkv_bf16 = d->qkv_dtype == GDN_BF16;
+    if (d->state_dtype == GDN_F32) return finish(launch_recurrent_f32state(p, d->B, d->DK, qkv_bf16, stream));
+    return finish(launch_recurrent_bf16state(p, d->B, d->DK, qkv_bf16, stream));
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                      const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                      const int32_t* state_indices, void* o, int32_t* err_word, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, o, nullptr,
+                         err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                          const void* b, const float* A_log, const float* dt_bias, const void* state_pool,
+                          const int32_t* state_indices, void* o, void* intermediate_states,
+                          int32_t* err_word, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    if (intermediate_states && !aligned(intermediate_states, 16)) return GDN_ERR_ALIGN;
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, o,
+                         intermediate_states, err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* state_indices,
+                      const void* intermediate_states, const int32_t* accept_len, int32_t* err_word,
+                      gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, false);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    if (!state_pool || !state_indices || !intermediate_states || !accept_len) return GDN_ERR_NULL;
+    if (!aligned(state_pool, 16) || !aligned(intermediate_states, 16)) return GDN_ERR_ALIGN;
+    if (!aligned(state_indices, 4) || !aligned(accept_len, 4) || (err_word && !aligned(err_word, 4)))
+        return GDN_ERR_ALIGN;
+    CommitParams p;
+    p.pool = state_pool;
+    p.indices = state_indices;
+    p.cache = intermediate_states;
+    p.accept_len = accept_len;
+    p.err = err_word;
+    p.T = dims->T;
+    p.num_slots = dims->num_slots;
+    p.lane_bytes = (int64_t)dims->HV * dims->DV * dims->DK * (int64_t)dtype_bytes(dims->state_dtype);
+    return finish(launch_commit(p, dims->B, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* gdn_status_string(gdn_status status) {
+    switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL: return "GDN_ERR_NULL: a required pointer is NULL";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: a size is out of range or inconsistent";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE: unknown dtype code";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: a pointer is misaligned";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: DK must be 16, 32, 64, 128 or 256";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: kernel launch failed (see gdn_last_cuda_error)";
+    case GDN_ERR_VALUE: return "GDN_ERR_VALUE: scale or l2_eps not finite, or l2_eps < 0";
+    }
+    return "unknown gdn_status";
+}
+
+int32_t gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t gdn_abi_version(void) { return 1; }
+
+}  // extern "C"

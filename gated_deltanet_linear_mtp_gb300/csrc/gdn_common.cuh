@@ -1,0 +1,233 @@
+// gdn_common.cuh -- device building blocks of the decode / verify kernel (sm_103a): storage conversions,
+// 16-byte global accesses, the lane layout of a block of state rows, the per-token row update of the gated
+// delta rule, and the gate and beta scalars.
+//
+// The rows of one state S[DV, DK] evolve independently:
+//     u_i = (g s_i) . kh,   s_i <- g s_i + beta (v_i - u_i) kh,   o_i = s_i . qh
+// so a CTA owns a block of rows of one (lane, value head) and keeps them in fp32 registers for all T tokens
+// (layout: Split below).
+//
+// One sweep per token.  With a = s.kh and c = s.qh taken on the state before the token,
+//     u = g a,  delta = beta (v_i - u),  s' = g s + delta kh,  o_i = g c + delta (kh . qh)
+// which equals the plain order in exact arithmetic: both dot products come out of one pass over the
+// registers, then one fused update.  kh . qh is formed once per token by the caller.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 16-byte state load, coherent, no L1 allocation (the state is read exactly once).
+__device__ __forceinline__ uint4 ld_state16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte streaming store (evict-first): intermediate states are written once and not re-read here.
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_plain16(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Conversions between one 16-byte chunk and CH fp32 values.
+template <typename StT>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+    static constexpr int CH = 4;
+    __device__ __forceinline__ static void unpack(const uint4& r, float* s) {
+        s[0] = __uint_as_float(r.x);
+        s[1] = __uint_as_float(r.y);
+        s[2] = __uint_as_float(r.z);
+        s[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* s) {
+        return make_uint4(__float_as_uint(s[0]), __float_as_uint(s[1]), __float_as_uint(s[2]), __float_as_uint(s[3]));
+    }
+};
+
+template <>
+struct Chunk<__nv_bfloat16> {
+    static constexpr int CH = 8;
+    __device__ __forceinline__ static void unpack(const uint4& r, float* s) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // element 2m sits in the low half (little endian)
+            s[2 * m] = __uint_as_float(w[m] << 16);
+            s[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<const uint32_t*>(&v);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* s) {
+        return make_uint4(pack2(s[0], s[1]), pack2(s[2], s[3]), pack2(s[4], s[5]), pack2(s[6], s[7]));
+    }
+};
+
+// Lane layout of one CTA's block of RPC state rows.  A row is split into P = DK / 8 slices of 8
+// consecutive columns, one per lane; each lane holds the same slice of RL rows (RL = 4, or 2 when DK = 16),
+// so the normalised k and q a lane needs for a token are only 8 columns of each.  A warp holds NRG = 32 / P
+// row groups; lane (rg, p) of warp w owns rows w * RPW + i * NRG + rg (i < RL), columns [8p, 8p + 8).  A
+// warp-wide access to "row i" of every row group thus covers NRG consecutive whole rows.
+template <int DK>
+struct Split {
+    static constexpr int COLS = 8;
+    static constexpr int P = DK / COLS;                     // lanes per row
+    static constexpr int RL = P >= 4 ? 4 : P;               // rows per lane
+    static constexpr int LOG_RL = RL == 4 ? 2 : (RL == 2 ? 1 : 0);
+    static constexpr int NRG = 32 / P;                      // row groups per warp
+    static constexpr int RPW = NRG * RL;                    // rows per warp
+    static constexpr int RPC = RPW * (kRecurrentThreads / 32);  // rows per CTA
+    static_assert(P >= RL && 32 % P == 0, "DK must be 16, 32, 64, 128 or 256");
+
+    // row (inside the CTA's block) of slot i of lane (warp, rg)
+    __device__ __forceinline__ static int row(int warp, int rg, int i) { return warp * RPW + i * NRG + rg; }
+    // slot whose complete dot products lane p holds after the reduction in token_update
+    __device__ __forceinline__ static int own_slot(int p) {
+        int i = 0;
+#pragma unroll
+        for (int l = 0; l < LOG_RL; ++l)
+            if (p & (P >> (l + 1))) i += RL >> (l + 1);
+        return i;
+    }
+    // the lowest lane (p) holding the complete dot products of slot i
+    __device__ __forceinline__ static int owner_p(int i) {
+        int p = 0;
+#pragma unroll
+        for (int l = 0; l < LOG_RL; ++l)
+            if (i & (RL >> (l + 1))) p += P >> (l + 1);
+        return p;
+    }
+};
+
+// 8 consecutive state elements <-> 16-byte chunks (1 for bf16, 2 for fp32)
+template <typename StT>
+struct Slice8 {
+    static constexpr int NC = 8 / Chunk<StT>::CH;
+    __device__ __forceinline__ static void unpack(const uint4 (&r)[NC], float* s) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) Chunk<StT>::unpack(r[c], s + c * Chunk<StT>::CH);
+    }
+    __device__ __forceinline__ static void load_global(const StT* src, uint4 (&r)[NC]) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) r[c] = ld_state16(src + c * Chunk<StT>::CH);
+    }
+    __device__ __forceinline__ static void load_shared(const StT* src, float* s) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+            Chunk<StT>::unpack(*reinterpret_cast<const uint4*>(src + c * Chunk<StT>::CH), s + c * Chunk<StT>::CH);
+    }
+    template <bool kStreaming>
+    __device__ __forceinline__ static void store_global(StT* dst, const float* s) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 v = Chunk<StT>::pack(s + c * Chunk<StT>::CH);
+            if (kStreaming)
+                st_stream16(dst + c * Chunk<StT>::CH, v);
+            else
+                st_plain16(dst + c * Chunk<StT>::CH, v);
+        }
+    }
+};
+
+// One token on a lane's RL x 8 state elements.
+//   kt, qt   normalised k and q of the token (fp32, shared memory, DK each)
+//   v_rows   v of the token for the CTA's RPC rows (shared memory, element type VT)
+// Row dot products a = s.kh and c = s.qh: 8-column partial sums, then a transposed butterfly over the P
+// lanes of the row group: at each of log2(RL) halving steps a lane keeps half of its rows and swaps the
+// other half with its partner, then plain xor steps finish the sum.  Lane p ends with the complete sums of
+// row slot own_slot(p), forms that row's delta and output, and the deltas of its RL rows are gathered back
+// with shuffles for the update.  Returns the output (before scale) of row slot own_slot(p).
+template <int DK, typename VT>
+__device__ __forceinline__ float token_update(float (&S)[Split<DK>::RL][8], const float* kt, const float* qt, float g,
+                                              float beta, const VT* v_rows, int warp, int rg, int p, float kq) {
+    using SP = Split<DK>;
+    constexpr int RL = SP::RL;
+    constexpr int P = SP::P;
+    float k8[8], q8[8];
+    {
+        const float4 k0 = *reinterpret_cast<const float4*>(kt + 8 * p);
+        const float4 k1 = *reinterpret_cast<const float4*>(kt + 8 * p + 4);
+        const float4 q0 = *reinterpret_cast<const float4*>(qt + 8 * p);
+        const float4 q1 = *reinterpret_cast<const float4*>(qt + 8 * p + 4);
+        k8[0] = k0.x; k8[1] = k0.y; k8[2] = k0.z; k8[3] = k0.w;
+        k8[4] = k1.x; k8[5] = k1.y; k8[6] = k1.z; k8[7] = k1.w;
+        q8[0] = q0.x; q8[1] = q0.y; q8[2] = q0.z; q8[3] = q0.w;
+        q8[4] = q1.x; q8[5] = q1.y; q8[6] = q1.z; q8[7] = q1.w;
+    }
+    float a[RL], c[RL];
+#pragma unroll
+    for (int i = 0; i < RL; ++i) {
+        float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            a0 = fmaf(S[i][e], k8[e], a0);
+            a1 = fmaf(S[i][e + 1], k8[e + 1], a1);
+            c0 = fmaf(S[i][e], q8[e], c0);
+            c1 = fmaf(S[i][e + 1], q8[e + 1], c1);
+        }
+        a[i] = a0 + a1;
+        c[i] = c0 + c1;
+    }
+#pragma unroll
+    for (int l = 0; l < SP::LOG_RL; ++l) {
+        const int m = P >> (l + 1);
+        const bool up = (p & m) != 0;
+#pragma unroll
+        for (int j = 0; j < (RL >> (l + 1)); ++j) {
+            const int hj = j + (RL >> (l + 1));
+            const float sa = up ? a[j] : a[hj];
+            const float sc = up ? c[j] : c[hj];
+            const float ka = up ? a[hj] : a[j];
+            const float kc = up ? c[hj] : c[j];
+            a[j] = ka + __shfl_xor_sync(0xffffffffu, sa, m);
+            c[j] = kc + __shfl_xor_sync(0xffffffffu, sc, m);
+        }
+    }
+#pragma unroll
+    for (int m = P >> (SP::LOG_RL + 1); m >= 1; m >>= 1) {
+        a[0] += __shfl_xor_sync(0xffffffffu, a[0], m);
+        c[0] += __shfl_xor_sync(0xffffffffu, c[0], m);
+    }
+    const int own = SP::own_slot(p);
+    const float delta = beta * (to_f32(v_rows[SP::row(warp, rg, own)]) - g * a[0]);
+    const float out = fmaf(g, c[0], delta * kq);
+#pragma unroll
+    for (int i = 0; i < RL; ++i) {
+        const float d = __shfl_sync(0xffffffffu, delta, rg * P + SP::owner_p(i));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) S[i][e] = fmaf(d, k8[e], g * S[i][e]);
+    }
+    return out;
+}
+
+// g = exp(-exp(A_log) * softplus(a + dt_bias)),  softplus(x) = log(1 + e^x) (written x + log(1 + e^-x) for x > 0)
+__device__ __forceinline__ float gate(float A_log, float a, float dt_bias) {
+    const float x = a + dt_bias;
+    const float sp = x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+    return expf(-expf(A_log) * sp);
+}
+
+__device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+
+}  // namespace gdn

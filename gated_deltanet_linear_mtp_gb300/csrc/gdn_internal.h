@@ -1,0 +1,48 @@
+// gdn_internal.h -- launch parameters shared by the C-ABI layer (gdn_api.cu) and the kernel translation
+// units.  Not installed; the public interface is include/gdn.h.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace gdn {
+
+constexpr int kRecurrentThreads = 128;  // one CTA = 4 warps over a block of state rows of one (lane, head)
+
+// Decode and verify share one kernel: decode writes the final state back (pool_out == pool_in),
+// verify optionally stores every intermediate state (cache != nullptr) and never writes the pool.
+struct RecurrentParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* a;
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+    const void* pool_in;
+    void* pool_out;  // nullptr: no write-back (verify)
+    const int32_t* indices;
+    void* o;
+    void* cache;     // nullptr: no intermediate states
+    int32_t* err;    // nullable
+    int T, HK, HV, DV, num_slots;
+    int out_bf16;
+    float scale, l2_eps;
+};
+
+struct CommitParams {
+    void* pool;
+    const int32_t* indices;
+    const void* cache;
+    const int32_t* accept_len;
+    int32_t* err;
+    int T, num_slots;
+    int64_t lane_bytes;  // HV * DV * DK * element size: one lane's state, all heads
+};
+
+cudaError_t launch_recurrent_f32state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
+cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
+cudaError_t launch_commit(const CommitParams& p, int B, cudaStream_t s);
+
+}  // namespace gdn

@@ -98,6 +98,7 @@ class Workload:
     pad_fraction: float = 0.0
     scale: float = 1.0
     l2_eps: float = 1e-6
+    pool_seed: Optional[int] = None  # None: the pool is drawn from `seed`
 
     @property
     def n_padded(self) -> int:
@@ -134,11 +135,12 @@ class Workload:
         """Pool ~ N(0, pool_std^2); drawn in blocks of POOL_BLOCK slots, each from its own stream
         ``default_rng([seed, pool_id, block])`` so that blocks can be filled by parallel threads."""
         shape = (self.num_slots, self.HV, self.DV, self.DK)
+        seed = self.seed if self.pool_seed is None else self.pool_seed
         x = np.empty(shape, np.float32)
         nblk = (self.num_slots + POOL_BLOCK - 1) // POOL_BLOCK
 
         def fill(i: int) -> None:
-            g = np.random.default_rng([int(self.seed), _STREAM["pool"], i])
+            g = np.random.default_rng([int(seed), _STREAM["pool"], i])
             blk = x[i * POOL_BLOCK:(i + 1) * POOL_BLOCK]
             g.standard_normal(out=blk, dtype=np.float32)
             blk *= np.float32(self.pool_std)
@@ -192,7 +194,10 @@ SWEEP_STATE = (F32, BF16)
 
 
 def sweep() -> List[Workload]:
-    """B x T x state dtype; T=1 runs as decode, T>1 as verify with caching; pool 1024 slots."""
+    """B x T x state dtype; T=1 runs as decode, T>1 as verify with caching; pool 1024 slots.
+
+    Point i draws its inputs from seed 1000 + i; all points of one state dtype share one pool (seed 2000
+    for fp32, 2001 for bf16), so the sweep needs two pool draws instead of 48."""
     pts = []
     i = 0
     for st in SWEEP_STATE:
@@ -202,7 +207,7 @@ def sweep() -> List[Workload]:
                 pts.append(Workload(f"sweep_B{B}_T{T}_{st}state", B=B, T=T, HK=16, HV=32, DK=128, DV=128,
                                     num_slots=1024, qkv_dtype=BF16, state_dtype=st, out_dtype=BF16,
                                     mode="decode" if dec else "verify", cache=not dec, commit=not dec,
-                                    seed=1000 + i))
+                                    seed=1000 + i, pool_seed=2000 + SWEEP_STATE.index(st)))
                 i += 1
     return pts
 

@@ -1,0 +1,140 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: the Gated DeltaNet (GDN) recurrent state update for decode and for
+ * multi-token-prediction (MTP) speculative verify, on one GB300 (sm_103a).
+ *
+ * The operation (the gated delta rule behind FlashInfer's gated_delta_rule_mtp, which sglang PR #23273
+ * "[GDN] Enable FlashInfer MTP verify on SM100+ (Blackwell)" calls through its pool API, Summary):
+ * for every request lane b whose pool index slot = state_indices[b] is not -1, and every value head h
+ * (key/query head hk = h / (HV / HK): each group of HV/HK consecutive value heads shares one key head),
+ *
+ *     S = state_pool[slot, h]                                   (DV x DK, computed in fp32)
+ *     for t in 0 .. T-1:
+ *         qh = q[b,t,hk] / sqrt(|q[b,t,hk]|^2 + l2_eps)         (L2 normalisation)
+ *         kh = k[b,t,hk] / sqrt(|k[b,t,hk]|^2 + l2_eps)
+ *         g    = exp(-exp(A_log[h]) * softplus(a[b,t,h] + dt_bias[h]))
+ *         beta = sigmoid(b[b,t,h])
+ *         S = g * S
+ *         S = S + beta * (v[b,t,h] - S kh) kh^T                 (delta rule)
+ *         o[b,t,h] = scale * S qh
+ *
+ * Layouts: row-major, last index contiguous, no strides.
+ *     q, k                    [B, T, HK, DK]          qkv_dtype
+ *     v                       [B, T, HV, DV]          qkv_dtype
+ *     a, b                    [B, T, HV]              qkv_dtype
+ *     A_log, dt_bias          [HV]                    fp32 (A_log is fp32: same page, Summary)
+ *     state_pool              [num_slots, HV, DV, DK] state_dtype (fp32, or bf16 as with
+ *                                                     --mamba-ssm-dtype bfloat16, same page, Throughput)
+ *     state_indices           [B]                     int32; -1 = padded lane
+ *     o                       [B, T, HV, DV]          out_dtype
+ *     intermediate_states     [B, T, HV, DV, DK]      state_dtype
+ *     accept_len              [B]                     int32
+ *
+ * Common rules.
+ *   - Every pointer is DEVICE memory owned by the caller.  The library allocates nothing, holds no mutable
+ *     global state, never synchronises, and enqueues its work asynchronously on `stream` (0 = legacy
+ *     default stream).  Calls are thread-safe.  A call with B == 0 enqueues nothing and returns GDN_OK.
+ *   - Alignment: q, k, state_pool and intermediate_states start on 16 bytes; the other arrays on their
+ *     element size.  Outputs must not overlap inputs (decode updates state_pool in place by design).
+ *   - Errors the host can see are returned as a status before anything is enqueued.  Errors that depend on
+ *     device data are defined, never a fault: a lane whose index is < -1 or >= num_slots, or (commit) whose
+ *     accept length is outside 0..T, is skipped and a bit is OR-ed into *err_word (if err_word is not NULL):
+ *     GDN_ERRBIT_INDEX, GDN_ERRBIT_ACCEPT_LEN.  The kernels never wait on other CTAs or on flags, so
+ *     they cannot hang.  The caller zeroes *err_word and reads it when it wants.
+ *   - Padded lanes (index -1, the padding index guard of FlashInfer #2810, same page, Requirements) are
+ *     skipped: their o, intermediate states and pool slots are left untouched, bit for bit.
+ *   - Distinct active lanes must use distinct slots in gdn_decode and gdn_commit (they write the pool);
+ *     gdn_mtp_verify only reads the pool, so lanes may share a slot there.
+ *   - GDN_ERR_CUDA: the launch failed; gdn_last_cuda_error() returns the cudaError_t of this thread's last
+ *     failed launch.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that C callers need no CUDA header. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* a size is out of range or inconsistent (HV % HK, T range, ...) */
+    GDN_ERR_DTYPE = 3,       /* a dtype code is not a gdn_dtype */
+    GDN_ERR_ALIGN = 4,       /* a pointer is misaligned */
+    GDN_ERR_UNSUPPORTED = 5, /* a valid but unsupported configuration (DK not in {16,32,64,128,256}) */
+    GDN_ERR_CUDA = 6,        /* the kernel launch failed */
+    GDN_ERR_VALUE = 7        /* a scalar is not finite, or l2_eps < 0 */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+enum { GDN_ERRBIT_INDEX = 1, GDN_ERRBIT_ACCEPT_LEN = 2 };
+
+enum { GDN_MAX_T = 16 }; /* tokens per call: decode (T >= 1), verify up to 16 (the page's MTP beyond T > 4) */
+
+typedef struct gdn_dims {
+    int32_t B;           /* request lanes, 0 .. 65535 */
+    int32_t T;           /* tokens per lane, 1 .. GDN_MAX_T */
+    int32_t HK;          /* query/key heads, >= 1 */
+    int32_t HV;          /* value heads, multiple of HK, <= 65535 */
+    int32_t DK;          /* key dimension: 16, 32, 64, 128 or 256 */
+    int32_t DV;          /* value dimension (state rows), >= 1 */
+    int32_t num_slots;   /* pool slots, >= 1 */
+    int32_t qkv_dtype;   /* gdn_dtype of q, k, v, a, b */
+    int32_t state_dtype; /* gdn_dtype of state_pool and intermediate_states */
+    int32_t out_dtype;   /* gdn_dtype of o */
+    float scale;         /* multiplies o (1.0 for o = S q) */
+    float l2_eps;        /* added to |x|^2 inside the square root of the L2 normalisation (1e-6) */
+} gdn_dims;
+
+/*
+ * gdn_decode -- T tokens (normally T = 1) from state_pool[state_indices[b]]; the final state is written
+ * back into the same slot, rounded to state_dtype (round to nearest even for bf16).  The running state
+ * stays fp32 between the tokens of one call.  Defines the SM100+ decode path of sglang PR #23273,
+ * Summary, with the padding index guard of its Requirements.
+ */
+gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                      const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                      const int32_t* state_indices, void* o, int32_t* err_word, gdn_stream_t stream);
+
+/*
+ * gdn_mtp_verify -- T draft tokens from state_pool[state_indices[b]] (read only: the pool is never
+ * written).  If intermediate_states is not NULL, the state after token t is stored, rounded to
+ * state_dtype, in intermediate_states[b, t].  MTP verify through the pool API (initial_state_indices) of
+ * sglang PR #23273, Summary; bf16 state, T beyond 4 and intermediate caching from its Requirements
+ * (FlashInfer #2679).
+ */
+gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                          const void* b, const float* A_log, const float* dt_bias, const void* state_pool,
+                          const int32_t* state_indices, void* o, void* intermediate_states,
+                          int32_t* err_word, gdn_stream_t stream);
+
+/*
+ * gdn_commit -- state_pool[state_indices[b], :] = intermediate_states[b, accept_len[b] - 1, :] (all heads),
+ * bit for bit, for every active lane with accept_len[b] >= 1; accept_len 0 leaves the slot as it is.
+ * Uses dims->B, T, HV, DK, DV, num_slots and state_dtype only.  The accepted-prefix checkpoint write of
+ * the commit contract in TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), "Moved out of this PR"
+ * (the manager's all-layer commit) and its commit message, MTP > Verify (checkpoint-commit contract).
+ */
+gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* state_indices,
+                      const void* intermediate_states, const int32_t* accept_len, int32_t* err_word,
+                      gdn_stream_t stream);
+
+/* Static string naming a status; never NULL. */
+const char* gdn_status_string(gdn_status status);
+
+/* cudaError_t of the calling thread's last GDN_ERR_CUDA (0 if none). */
+int32_t gdn_last_cuda_error(void);
+
+/* ABI version of this header: 1. */
+int32_t gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

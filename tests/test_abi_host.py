@@ -1,0 +1,143 @@
+"""libgdn.so loads, exports every function ``include/gdn.h`` declares, and rejects bad arguments on the host
+with the documented status before touching CUDA (no call here reaches a kernel launch; no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_linear_mtp_gb300 as gdn
+from gated_deltanet_linear_mtp_gb300 import build as gbuild
+
+HEADER = os.path.join(gbuild.INCLUDE, "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(gbuild.LIB_PATH):
+        gbuild.build()
+    return gdn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(gdn.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    for code, name in gdn.STATUS.items():
+        assert L.gdn_status_string(code).decode().startswith(name)
+    assert L.gdn_status_string(99).decode() == "unknown gdn_status"
+    assert L.gdn_abi_version() == 1
+    assert L.gdn_last_cuda_error() == 0
+
+
+# fake, aligned, never dereferenced device addresses: validation fails before any CUDA call
+P = ctypes.c_void_p(0x10000)
+P2 = ctypes.c_void_p(0x20000)
+ODD = ctypes.c_void_p(0x10002)
+
+
+def dims(**kw):
+    base = dict(B=4, T=4, HK=2, HV=4, DK=128, DV=128, num_slots=8, qkv_dtype=1, state_dtype=1, out_dtype=1,
+                scale=1.0, l2_eps=1e-6)
+    base.update(kw)
+    return gdn.GdnDims(**base)
+
+
+def verify(L, d, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, o=P, cache=None, err=None)
+    a.update(ptrs)
+    return L.gdn_mtp_verify(ctypes.byref(d) if d is not None else None, a["q"], a["k"], a["v"], a["a"], a["b"],
+                            a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["o"], a["cache"], a["err"], None)
+
+
+def decode(L, d, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, o=P, err=None)
+    a.update(ptrs)
+    return L.gdn_decode(ctypes.byref(d) if d is not None else None, a["q"], a["k"], a["v"], a["a"], a["b"],
+                        a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["o"], a["err"], None)
+
+
+def commit(L, d, **ptrs):
+    a = dict(pool=P2, idx=P, cache=P, acc=P, err=None)
+    a.update(ptrs)
+    return L.gdn_commit(ctypes.byref(d) if d is not None else None, a["pool"], a["idx"], a["cache"], a["acc"],
+                        a["err"], None)
+
+
+@pytest.mark.parametrize("call", [verify, decode, commit])
+def test_null_dims(L, call):
+    assert call(L, None) == 1
+
+
+@pytest.mark.parametrize("call", [verify, decode])
+@pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o"])
+def test_null_pointer(L, call, ptr):
+    assert call(L, dims(), **{ptr: None}) == 1
+
+
+@pytest.mark.parametrize("ptr", ["pool", "idx", "cache", "acc"])
+def test_commit_null_pointer(L, ptr):
+    assert commit(L, dims(), **{ptr: None}) == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 2), (dict(T=17), 2), (dict(B=-1), 2), (dict(B=65536), 2), (dict(HK=3), 2), (dict(HK=0), 2),
+    (dict(HV=0), 2), (dict(DV=0), 2), (dict(num_slots=0), 2), (dict(DK=0), 2),
+    (dict(DK=48), 5), (dict(DK=512), 5), (dict(DK=8), 5),
+    (dict(qkv_dtype=2), 3), (dict(state_dtype=-1), 3), (dict(out_dtype=7), 3),
+    (dict(l2_eps=-1.0), 7), (dict(l2_eps=float("nan")), 7), (dict(scale=float("inf")), 7),
+])
+def test_bad_dims(L, kw, status):
+    assert verify(L, dims(**kw)) == status
+    assert decode(L, dims(**kw)) == status
+
+
+def test_commit_ignores_io_fields_but_checks_the_rest(L):
+    assert commit(L, dims(HK=3, qkv_dtype=9, l2_eps=-1.0, B=0)) == 0
+    assert commit(L, dims(T=0)) == 2
+    assert commit(L, dims(state_dtype=5)) == 3
+    assert commit(L, dims(DK=24)) == 5
+
+
+@pytest.mark.parametrize("ptr", ["q", "k", "pool"])
+def test_misaligned_16(L, ptr):
+    assert verify(L, dims(), **{ptr: ODD}) == 4
+    assert decode(L, dims(), **{ptr: ODD}) == 4
+
+
+def test_misaligned_other(L):
+    assert verify(L, dims(), cache=ODD) == 4
+    assert verify(L, dims(), A_log=ctypes.c_void_p(0x10002)) == 4
+    assert verify(L, dims(qkv_dtype=0), v=ctypes.c_void_p(0x10002)) == 4
+    assert verify(L, dims(out_dtype=0), o=ctypes.c_void_p(0x10002)) == 4
+    assert verify(L, dims(), err=ctypes.c_void_p(0x10001)) == 4
+    assert commit(L, dims(), cache=ODD) == 4
+    assert commit(L, dims(), pool=ODD) == 4
+    assert commit(L, dims(), acc=ctypes.c_void_p(0x10001)) == 4
+
+
+def test_empty_batch_is_a_no_op(L):
+    # B == 0: nothing is enqueued, so even NULL data pointers are accepted
+    z = dict(q=None, k=None, v=None, a=None, b=None, A_log=None, dt_bias=None, pool=None, idx=None, o=None)
+    assert verify(L, dims(B=0), **z) == 0
+    assert decode(L, dims(B=0), **z) == 0
+    assert commit(L, dims(B=0), pool=None, idx=None, cache=None, acc=None) == 0
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gdn, "_lib_handle", None)
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        gdn.lib()

@@ -1,0 +1,387 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on the same seeded inputs.
+
+Full-size checks use the workloads the benchmark times (decode T=1 B=64 fp32 state; verify T=4 B=128 bf16
+state + commit; verify T=8 B=256 with 10 % padded lanes), plus the B x T x dtype sweep on sampled lanes and
+small edge cases that span several row tiles with a ragged tail.  Tolerances: see ``gpu_util``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_mtp_gb300 as gdn
+import gdn_workloads as W
+import oracle
+from gpu_util import (Dev, assert_f32_close, canary, check_o, check_state, dev, host, is_canary, run_decode,
+                      run_verify, storage_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+LANE_KEYS = ("q", "k", "v", "a", "b", "indices", "accept_len")
+
+
+def take_lanes(x: dict, lanes) -> dict:
+    lanes = np.asarray(lanes)
+    y = dict(x)
+    for k in LANE_KEYS:
+        y[k] = np.ascontiguousarray(x[k][lanes])
+    return y
+
+
+def compare_verify(w, x, o_gpu, cache_gpu, lanes=None, chunk=16):
+    """o / cache of the given lanes against the oracle; padded and invalid lanes must hold canaries."""
+    orc = oracle.default()
+    d = oracle.dims_of(w)
+    B = x["q"].shape[0]
+    lanes = np.arange(B) if lanes is None else np.asarray(lanes)
+    for i in range(0, len(lanes), chunk):
+        sel = lanes[i:i + chunk]
+        xs = take_lanes(x, sel)
+        o_ref, c_ref, _ = orc.verify(d, xs, cache=cache_gpu is not None)
+        act = (xs["indices"] >= 0) & (xs["indices"] < w.num_slots)
+        og = o_gpu[sel]
+        if act.any():
+            check_o(w, og[act], o_ref[act], f"o lanes {sel[act][:4]}..")
+        if (~act).any():
+            assert is_canary(og[~act]).all(), "o of a skipped lane was written"
+        if cache_gpu is not None:
+            cg = cache_gpu[sel]
+            if act.any():
+                check_state(w, cg[act], c_ref[act], f"cache lanes {sel[act][:4]}..")
+            if (~act).any():
+                assert is_canary(cg[~act]).all(), "cache of a skipped lane was written"
+
+
+def check_commit(w, x, pool_before_gpu, pool_after, cache_gpu):
+    """Committed slots equal cache[b, L-1] bit for bit; every other slot is unchanged bit for bit."""
+    idx, acc = x["indices"], x["accept_len"]
+    touched = np.zeros(w.num_slots, bool)
+    for b in range(len(idx)):
+        s = idx[b]
+        if 0 <= s < w.num_slots and 1 <= acc[b] <= w.T:
+            assert np.array_equal(pool_after[s], cache_gpu[b, acc[b] - 1]), f"lane {b}"
+            touched[s] = True
+    assert np.array_equal(pool_after[~touched], pool_before_gpu[~touched]), "an uncommitted slot changed"
+
+
+def pool_host_pair(t):
+    return host(t["pool"])
+
+
+# ---------------------------------------------------------------------------------------------------------
+def test_tiny_verify_commit_decode():
+    w = W.tiny()
+    x = w.arrays()
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    o_h, c_h = host(o), host(cache)
+    compare_verify(w, x, o_h, c_h)
+    # commit
+    before = host(t["pool"])
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
+    after = host(t["pool"])
+    check_commit(w, x, before, after, c_h)
+    # decode of the same tokens one at a time from the original pool == the cached states
+    pool = dev(x["pool"])
+    w1 = w.replace(T=1, mode="decode")
+    for tok in range(w.T):
+        xt = dict(x)
+        for k in ("q", "k", "v", "a", "b"):
+            xt[k] = np.ascontiguousarray(x[k][:, tok:tok + 1])
+        ot = run_decode(w1, Dev(xt), pool)
+        ph = host(pool)
+        for b, s in enumerate(x["indices"]):
+            assert_f32_close(ph[s], c_h[b, tok], f"decode step {tok} lane {b}")
+        assert_f32_close(host(ot)[:, 0], o_h[:, tok], f"decode o step {tok}")
+
+
+def test_decode_t1_full():
+    w = W.decode_t1()
+    x = w.arrays()
+    t = Dev(x)
+    pool_before = host(t["pool"])
+    o = run_decode(w, t, t["pool"])
+    torch.cuda.synchronize()
+    o_h, pool_gpu = host(o), host(t["pool"])
+    orc = oracle.default()
+    pool_ref = x["pool"].copy()
+    o_ref, fl = orc.decode(oracle.dims_of(w), x, pool_ref)
+    assert fl == 0
+    check_o(w, o_h, o_ref)
+    idx = x["indices"]
+    check_state(w, pool_gpu[idx], pool_ref[idx], "pool write-back")
+    untouched = np.setdiff1d(np.arange(w.num_slots), idx)
+    assert np.array_equal(pool_gpu[untouched], pool_before[untouched])
+
+
+def test_verify_t4_full_and_commit():
+    w = W.verify_t4()
+    x = w.arrays()
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, cache = run_verify(w, t, cache=True, err=err)
+    torch.cuda.synchronize()
+    pool_before = host(t["pool"])
+    assert np.array_equal(pool_before, x["pool"]), "verify wrote the pool"
+    o_h, c_h = host(o), host(cache)
+    compare_verify(w, x, o_h, c_h)
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"], err)
+    check_commit(w, x, pool_before, host(t["pool"]), c_h)
+    assert int(err.item()) == 0
+
+
+def test_verify_t8_padded_sampled_and_commit():
+    w = W.verify_t8()
+    x = w.arrays()
+    idx = x["indices"]
+    assert (idx == -1).sum() == 26
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    o_h, c_h = host(o), host(cache)
+    rng = np.random.default_rng(5)
+    active = np.flatnonzero(idx >= 0)
+    lanes = np.sort(np.concatenate([np.flatnonzero(idx < 0), rng.choice(active, 40, replace=False)]))
+    compare_verify(w, x, o_h, c_h, lanes=lanes)
+    # every padded lane untouched, everywhere
+    assert is_canary(o_h[idx < 0]).all() and is_canary(c_h[idx < 0]).all()
+    pool_before = host(t["pool"])
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
+    check_commit(w, x, pool_before, host(t["pool"]), c_h)
+
+
+# ---- the sweep, on sampled lanes ---------------------------------------------------------------------
+_POOLS = {}
+
+
+def _sweep_pool(w):
+    key = (w.state_dtype, w.pool_seed)
+    if key not in _POOLS:
+        p = w.pool()
+        _POOLS.clear()
+        _POOLS[key] = (p, dev(p))
+    return _POOLS[key]
+
+
+@pytest.mark.parametrize("w", W.sweep(), ids=lambda w: w.name)
+def test_sweep_point(w):
+    x = w.small_arrays()
+    pool_h, pool_d = _sweep_pool(w)
+    x["pool"] = pool_h
+    t = Dev({k: v for k, v in x.items() if k != "pool"})
+    t.t["pool"] = pool_d
+    lanes = np.arange(w.B) if w.B <= 8 else np.sort(np.random.default_rng(w.seed).choice(w.B, 8, replace=False))
+    if w.mode == "decode":
+        pool = pool_d.clone()
+        o = run_decode(w, t, pool)
+        torch.cuda.synchronize()
+        orc = oracle.default()
+        xs = take_lanes(x, lanes)
+        pool_ref = pool_h.copy()
+        o_ref, _ = orc.decode(oracle.dims_of(w), xs, pool_ref)
+        check_o(w, host(o)[lanes], o_ref)
+        sl = xs["indices"]
+        check_state(w, host(pool[torch.from_numpy(sl).long().cuda()]), pool_ref[sl], "pool write-back")
+        del pool
+    else:
+        o, cache = run_verify(w, t, cache=True)
+        torch.cuda.synchronize()
+        o_h, c_h = host(o), host(cache)
+        compare_verify(w, x, o_h, c_h, lanes=lanes)
+        pool = pool_d.clone()
+        gdn.gdn_commit(pool, t["indices"], cache, t["accept_len"])
+        torch.cuda.synchronize()
+        sl = x["indices"]
+        after = host(pool[torch.from_numpy(sl).long().cuda()])
+        for j, b in enumerate(range(w.B)):
+            assert np.array_equal(after[j], c_h[b, x["accept_len"][b] - 1])
+        del pool, cache
+
+
+# ---- edge cases: several row tiles, ragged tails, every DK, dtype mixes -----------------------------
+def small(name, B=3, T=3, HK=2, HV=4, DK=64, DV=40, num_slots=7, qkv="bf16", state="bf16", out="bf16",
+          seed=0, scale=1.0, pad=0.0):
+    return W.Workload(name, B=B, T=T, HK=HK, HV=HV, DK=DK, DV=DV, num_slots=num_slots, qkv_dtype=qkv,
+                      state_dtype=state, out_dtype=out, mode="verify", cache=True, commit=True, seed=seed,
+                      pool_std=0.1, scale=scale, pad_fraction=pad)
+
+
+EDGE = [
+    small("dk16_dv16_f32_all", DK=16, DV=16, qkv="f32", state="f32", out="f32"),
+    small("dk16_dv200_ragged", DK=16, DV=200),
+    small("dk32_dv33_f32state", DK=32, DV=33, state="f32"),
+    small("dk64_dv40_ragged", DK=64, DV=40),
+    small("dk128_dv100_ragged_T16", DK=128, DV=100, T=16),
+    small("dk128_dv128_T1", DK=128, DV=128, T=1),
+    small("dk256_dv24_ragged", DK=256, DV=24, state="f32", out="f32"),
+    small("dk256_dv64_bf16", DK=256, DV=64, T=5),
+    small("hk_eq_hv", HK=4, HV=4, DK=128, DV=64),
+    small("hv_8x_hk", HK=1, HV=8, DK=128, DV=48, qkv="f32"),
+    small("scale_half_f32out", DK=128, DV=64, out="f32", scale=0.5),
+    small("b1", B=1, DK=128, DV=128),
+    small("padded_half", B=8, num_slots=12, DK=128, DV=72, pad=0.5),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
+def test_edge_verify(w):
+    x = w.arrays()
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    compare_verify(w, x, host(o), host(cache))
+    # the same call without the cache gives the same o, bit for bit
+    o2, _ = run_verify(w, t, cache=False)
+    assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o.view(torch.int32),
+                       o2.view(torch.int16) if o2.dtype == torch.bfloat16 else o2.view(torch.int32))
+
+
+@pytest.mark.parametrize("w", [e for e in EDGE if e.name in ("dk16_dv200_ragged", "dk128_dv100_ragged_T16",
+                                                                 "dk256_dv24_ragged", "padded_half")],
+                         ids=lambda w: w.name)
+def test_edge_decode(w):
+    w = w.replace(mode="decode")
+    x = w.arrays()
+    t = Dev(x)
+    o = run_decode(w, t, t["pool"])
+    torch.cuda.synchronize()
+    pool_ref = x["pool"].copy()
+    o_ref, _ = oracle.default().decode(oracle.dims_of(w), x, pool_ref)
+    act = x["indices"] >= 0
+    check_o(w, host(o)[act], o_ref[act])
+    assert is_canary(host(o)[~act]).all()
+    pg = host(t["pool"])
+    check_state(w, pg[x["indices"][act]], pool_ref[x["indices"][act]], "pool")
+    untouched = np.setdiff1d(np.arange(w.num_slots), x["indices"][act])
+    assert np.array_equal(pg[untouched], x["pool"][untouched])
+
+
+def test_all_lanes_padded_touch_nothing():
+    w = small("all_pad", B=4, DK=128, DV=64)
+    x = w.arrays()
+    x["indices"][:] = -1
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, cache = run_verify(w, t, cache=True, err=err)
+    run_decode(w, t, t["pool"], err=err, o=o)
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert is_canary(host(o)).all() and is_canary(host(cache)).all()
+    assert np.array_equal(host(t["pool"]), x["pool"])
+    assert int(err.item()) == 0
+
+
+def test_bad_indices_and_accept_lengths_set_error_bits():
+    w = small("bad", B=6, DK=64, DV=32, num_slots=8)
+    x = w.arrays()
+    x["indices"][:] = [0, -1, 8, -2, 3, 5]         # 8 and -2 are out of range
+    x["accept_len"][:] = [1, 1, 1, 1, 0, w.T + 1]  # lane 4: no-op; lane 5: out of range
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, cache = run_verify(w, t, cache=True, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.ERRBIT_INDEX
+    oh, ch = host(o), host(cache)
+    for b in (1, 2, 3):
+        assert is_canary(oh[b]).all() and is_canary(ch[b]).all()
+    compare_verify(w, x, oh, ch, lanes=[0, 4, 5])
+    err.zero_()
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.ERRBIT_INDEX | gdn.ERRBIT_ACCEPT_LEN
+    after = host(t["pool"])
+    assert np.array_equal(after[0], ch[0, 0])
+    keep = [s for s in range(8) if s != 0]
+    assert np.array_equal(after[keep], x["pool"][keep])   # lanes 4 (L=0) and 5 (L>T) left slots 3, 5 alone
+
+
+def test_duplicate_slots_in_verify_read_the_same_state():
+    w = small("dup", B=4, DK=128, DV=64)
+    x = w.arrays()
+    x["indices"][:] = [2, 2, 2, 2]
+    for k in ("q", "k", "v", "a", "b"):
+        x[k][1:] = x[k][0]
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    oh, ch = host(o), host(cache)
+    for b in (1, 2, 3):
+        assert np.array_equal(oh[b], oh[0]) and np.array_equal(ch[b], ch[0])
+    compare_verify(w, x, oh, ch, lanes=[0])
+
+
+def test_empty_batch():
+    w = small("b0", B=1)
+    x = w.arrays()
+    t = Dev(x)
+    e = {k: v[:0] for k, v in t.t.items() if k in LANE_KEYS}
+    o = torch.empty((0, w.T, w.HV, w.DV), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_mtp_verify(e["q"], e["k"], e["v"], e["a"], e["b"], t["A_log"], t["dt_bias"], t["pool"], e["indices"], o)
+    torch.cuda.synchronize()
+
+
+# ---- chained calls on the GPU: verify(T) == T decodes, commit(L) == L decodes ------------------------
+def test_chain_verify_equals_decodes_f32():
+    w = small("chain", B=5, T=6, DK=128, DV=128, num_slots=9, state="f32", out="f32")
+    x = w.arrays()
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    pool = t["pool"].clone()
+    w1 = w.replace(T=1, mode="decode")
+    oh, ch = host(o), host(cache)
+    for tok in range(w.T):
+        xt = dict(x)
+        for k in ("q", "k", "v", "a", "b"):
+            xt[k] = np.ascontiguousarray(x[k][:, tok:tok + 1])
+        ot = run_decode(w1, Dev(xt), pool)
+        torch.cuda.synchronize()
+        assert_f32_close(host(ot)[:, 0], oh[:, tok], f"o step {tok}")
+        ph = host(pool)
+        assert_f32_close(ph[x["indices"]], ch[:, tok], f"state step {tok}")
+    # commit(L) == state after L decodes
+    L = x["accept_len"]
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
+    ref = dev(x["pool"])
+    for tok in range(w.T):
+        xt = dict(x)
+        for k in ("q", "k", "v", "a", "b"):
+            xt[k] = np.ascontiguousarray(x[k][:, tok:tok + 1])
+        xt["indices"] = np.where(L > tok, x["indices"], -1).astype(np.int32)
+        run_decode(w1, Dev(xt), ref)
+    torch.cuda.synchronize()
+    assert_f32_close(host(t["pool"])[x["indices"]], host(ref)[x["indices"]], "commit vs decodes")
+
+
+# ---- streams and CUDA graphs -------------------------------------------------------------------------
+def test_side_stream_and_graph_replay():
+    w = small("graph", B=16, T=4, DK=128, DV=128, num_slots=32)
+    x = w.arrays()
+    t = Dev(x)
+    pool0 = t["pool"].clone()
+    o = canary((w.B, w.T, w.HV, w.DV), w.out_dtype)
+    cache = canary((w.B, w.T, w.HV, w.DV, w.DK), w.state_dtype)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on a side stream
+        run_verify(w, t, cache=True, o=o, cache_buf=cache, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    o_eager, c_eager = host(o), host(cache)
+    compare_verify(w, x, o_eager, c_eager)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_verify(w, t, cache=True, o=o, cache_buf=cache)
+        gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
+    rng = np.random.default_rng(3)
+    for rep in range(3):
+        t["pool"].copy_(pool0)
+        acc = rng.integers(1, w.T + 1, w.B).astype(np.int32)
+        t["accept_len"].copy_(torch.from_numpy(acc))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host(o), o_eager) and np.array_equal(host(cache), c_eager)
+        xr = dict(x, accept_len=acc)
+        check_commit(w, xr, host(pool0), host(t["pool"]), c_eager)
