@@ -97,7 +97,12 @@ struct Split {
     static constexpr int LOG_RL = RL == 4 ? 2 : (RL == 2 ? 1 : 0);
     static constexpr int NRG = 32 / P;                      // row groups per warp
     static constexpr int RPW = NRG * RL;                    // rows per warp
-    static constexpr int RPC = RPW * (kRecurrentThreads / 32);  // rows per CTA
+    // 4 warps per CTA: measured faster than 8-warp CTAs, whose prologue barrier idles more warps
+    static constexpr int WARPS = 4;
+    static constexpr int THREADS = 32 * WARPS;
+    // resident CTAs an SM must fit (register cap, 80 a thread): 24 warps per SM hide the prologue's loads
+    static constexpr int MIN_CTAS_PER_SM = 24 / WARPS;
+    static constexpr int RPC = RPW * WARPS;                 // rows per CTA
     static_assert(P >= RL && 32 % P == 0, "DK must be 16, 32, 64, 128 or 256");
 
     // row (inside the CTA's block) of slot i of lane (warp, rg)
@@ -120,28 +125,32 @@ struct Split {
     }
 };
 
-// 8 consecutive state elements <-> 16-byte chunks (1 for bf16, 2 for fp32)
+// 8 consecutive state elements (as 4 column pairs) <-> 16-byte chunks (1 for bf16, 2 for fp32)
 template <typename StT>
 struct Slice8 {
     static constexpr int NC = 8 / Chunk<StT>::CH;
-    __device__ __forceinline__ static void unpack(const uint4 (&r)[NC], float* s) {
+    __device__ __forceinline__ static void unpack(const uint4 (&r)[NC], float2 (&s)[4]) {
+        float f[8];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) Chunk<StT>::unpack(r[c], s + c * Chunk<StT>::CH);
+        for (int c = 0; c < NC; ++c) Chunk<StT>::unpack(r[c], f + c * Chunk<StT>::CH);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] = make_float2(f[2 * e], f[2 * e + 1]);
     }
     __device__ __forceinline__ static void load_global(const StT* src, uint4 (&r)[NC]) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) r[c] = ld_state16(src + c * Chunk<StT>::CH);
     }
-    __device__ __forceinline__ static void load_shared(const StT* src, float* s) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-            Chunk<StT>::unpack(*reinterpret_cast<const uint4*>(src + c * Chunk<StT>::CH), s + c * Chunk<StT>::CH);
-    }
     template <bool kStreaming>
-    __device__ __forceinline__ static void store_global(StT* dst, const float* s) {
+    __device__ __forceinline__ static void store_global(StT* dst, const float2 (&s)[4]) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = s[e].x;
+            f[2 * e + 1] = s[e].y;
+        }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            const uint4 v = Chunk<StT>::pack(s + c * Chunk<StT>::CH);
+            const uint4 v = Chunk<StT>::pack(f + c * Chunk<StT>::CH);
             if (kStreaming)
                 st_stream16(dst + c * Chunk<StT>::CH, v);
             else
@@ -150,44 +159,48 @@ struct Slice8 {
     }
 };
 
-// One token on a lane's RL x 8 state elements.
+// One token on a lane's RL x 8 state elements, held as RL x 4 pairs of adjacent columns so that the dot
+// products and the update run on packed fp32x2 multiply-adds (each half rounds like a scalar fmaf).
 //   kt, qt   normalised k and q of the token (fp32, shared memory, DK each)
 //   v_rows   v of the token for the CTA's RPC rows (shared memory, element type VT)
-// Row dot products a = s.kh and c = s.qh: 8-column partial sums, then a transposed butterfly over the P
-// lanes of the row group: at each of log2(RL) halving steps a lane keeps half of its rows and swaps the
-// other half with its partner, then plain xor steps finish the sum.  Lane p ends with the complete sums of
-// row slot own_slot(p), forms that row's delta and output, and the deltas of its RL rows are gathered back
-// with shuffles for the update.  Returns the output (before scale) of row slot own_slot(p).
+// Row dot products a = s.kh and c = s.qh: 8-column partial sums (even and odd columns accumulate
+// separately), then a transposed butterfly over the P lanes of the row group: at each of log2(RL) halving
+// steps a lane keeps half of its rows and swaps the other half with its partner, then plain xor steps
+// finish the sum.  Lane p ends with the complete sums of row slot own_slot(p), forms that row's delta and
+// output, and the deltas of its RL rows are gathered back with shuffles for the update.  Returns the
+// output (before scale) of row slot own_slot(p).
 template <int DK, typename VT>
-__device__ __forceinline__ float token_update(float (&S)[Split<DK>::RL][8], const float* kt, const float* qt, float g,
+__device__ __forceinline__ float token_update(float2 (&S)[Split<DK>::RL][4], const float* kt, const float* qt, float g,
                                               float beta, const VT* v_rows, int warp, int rg, int p, float kq) {
     using SP = Split<DK>;
     constexpr int RL = SP::RL;
     constexpr int P = SP::P;
-    float k8[8], q8[8];
+    float2 k2[4], q2[4];
     {
         const float4 k0 = *reinterpret_cast<const float4*>(kt + 8 * p);
         const float4 k1 = *reinterpret_cast<const float4*>(kt + 8 * p + 4);
         const float4 q0 = *reinterpret_cast<const float4*>(qt + 8 * p);
         const float4 q1 = *reinterpret_cast<const float4*>(qt + 8 * p + 4);
-        k8[0] = k0.x; k8[1] = k0.y; k8[2] = k0.z; k8[3] = k0.w;
-        k8[4] = k1.x; k8[5] = k1.y; k8[6] = k1.z; k8[7] = k1.w;
-        q8[0] = q0.x; q8[1] = q0.y; q8[2] = q0.z; q8[3] = q0.w;
-        q8[4] = q1.x; q8[5] = q1.y; q8[6] = q1.z; q8[7] = q1.w;
+        k2[0] = make_float2(k0.x, k0.y);
+        k2[1] = make_float2(k0.z, k0.w);
+        k2[2] = make_float2(k1.x, k1.y);
+        k2[3] = make_float2(k1.z, k1.w);
+        q2[0] = make_float2(q0.x, q0.y);
+        q2[1] = make_float2(q0.z, q0.w);
+        q2[2] = make_float2(q1.x, q1.y);
+        q2[3] = make_float2(q1.z, q1.w);
     }
     float a[RL], c[RL];
 #pragma unroll
     for (int i = 0; i < RL; ++i) {
-        float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+        float2 ak = make_float2(0.f, 0.f), cq = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            a0 = fmaf(S[i][e], k8[e], a0);
-            a1 = fmaf(S[i][e + 1], k8[e + 1], a1);
-            c0 = fmaf(S[i][e], q8[e], c0);
-            c1 = fmaf(S[i][e + 1], q8[e + 1], c1);
+        for (int e = 0; e < 4; ++e) {
+            ak = __ffma2_rn(S[i][e], k2[e], ak);
+            cq = __ffma2_rn(S[i][e], q2[e], cq);
         }
-        a[i] = a0 + a1;
-        c[i] = c0 + c1;
+        a[i] = ak.x + ak.y;
+        c[i] = cq.x + cq.y;
     }
 #pragma unroll
     for (int l = 0; l < SP::LOG_RL; ++l) {
@@ -212,11 +225,13 @@ __device__ __forceinline__ float token_update(float (&S)[Split<DK>::RL][8], cons
     const int own = SP::own_slot(p);
     const float delta = beta * (to_f32(v_rows[SP::row(warp, rg, own)]) - g * a[0]);
     const float out = fmaf(g, c[0], delta * kq);
+    const float2 g2 = make_float2(g, g);
 #pragma unroll
     for (int i = 0; i < RL; ++i) {
         const float d = __shfl_sync(0xffffffffu, delta, rg * P + SP::owner_p(i));
+        const float2 d2 = make_float2(d, d);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) S[i][e] = fmaf(d, k8[e], g * S[i][e]);
+        for (int e = 0; e < 4; ++e) S[i][e] = __ffma2_rn(d2, k2[e], __fmul2_rn(g2, S[i][e]));
     }
     return out;
 }

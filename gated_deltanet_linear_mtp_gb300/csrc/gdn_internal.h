@@ -8,8 +8,6 @@
 
 namespace gdn {
 
-constexpr int kRecurrentThreads = 128;  // one CTA = 4 warps over a block of state rows of one (lane, head)
-
 // Decode and verify share one kernel: decode writes the final state back (pool_out == pool_in),
 // verify optionally stores every intermediate state (cache != nullptr) and never writes the pool.
 struct RecurrentParams {

@@ -21,11 +21,13 @@ __host__ __device__ inline size_t general_smem_floats(int DK, int RPC, int T) {
 }
 
 template <int DK, typename InT, typename StT>
-__global__ void __launch_bounds__(kRecurrentThreads) gdn_recurrent_kernel(const RecurrentParams p) {
+__global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM)
+    gdn_recurrent_kernel(const RecurrentParams p) {
     using SP = Split<DK>;
     using SL = Slice8<StT>;
     constexpr int RL = SP::RL;
     constexpr int RPC = SP::RPC;
+    constexpr int NT = SP::THREADS;
 
     const int b = blockIdx.z;
     const int h = blockIdx.y;
@@ -46,7 +48,7 @@ __global__ void __launch_bounds__(kRecurrentThreads) gdn_recurrent_kernel(const 
     float qv[kPrefetchTokens][QPL], kv[kPrefetchTokens][QPL];
 #pragma unroll
     for (int u = 0; u < kPrefetchTokens; ++u) {
-        const int t = warp + u * (kRecurrentThreads / 32);
+        const int t = warp + u * (SP::WARPS);
         const int64_t off = (((int64_t)b * T + t) * p.HK + hk) * DK;
 #pragma unroll
         for (int i = 0; i < QPL; ++i) {
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(kRecurrentThreads) gdn_recurrent_kernel(const 
     float vpre[kPrefetchV];
 #pragma unroll
     for (int u = 0; u < kPrefetchV; ++u) {
-        const int i = tid + u * kRecurrentThreads;
+        const int i = tid + u * NT;
         vpre[u] = i < T * RPC ? v_at(i) : 0.f;
     }
     float a_raw = 0.f, b_raw = 0.f, A_h = 0.f, dt_h = 0.f;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kRecurrentThreads) gdn_recurrent_kernel(const 
     float* gs = vs + T * RPC;  // [T] decay g
     float* bs = gs + T;        // [T] beta
     float* kqs = bs + T;       // [T] kh . qh
-    for (int t = warp, u = 0; t < T; t += kRecurrentThreads / 32, ++u) {
+    for (int t = warp, u = 0; t < T; t += SP::WARPS, ++u) {
         float q_[QPL], k_[QPL];
         if (u < kPrefetchTokens) {
 #pragma unroll
@@ -154,13 +156,13 @@ __global__ void __launch_bounds__(kRecurrentThreads) gdn_recurrent_kernel(const 
     }
 #pragma unroll
     for (int u = 0; u < kPrefetchV; ++u) {
-        const int i = tid + u * kRecurrentThreads;
+        const int i = tid + u * NT;
         if (i < T * RPC) vs[i] = vpre[u];
     }
-    for (int i = tid + kPrefetchV * kRecurrentThreads; i < T * RPC; i += kRecurrentThreads) vs[i] = v_at(i);
+    for (int i = tid + kPrefetchV * NT; i < T * RPC; i += NT) vs[i] = v_at(i);
     __syncthreads();
 
-    float S[RL][8];
+    float2 S[RL][4];
 #pragma unroll
     for (int i = 0; i < RL; ++i) SL::unpack(raw[i], S[i]);
 

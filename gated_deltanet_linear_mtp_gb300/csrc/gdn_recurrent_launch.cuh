@@ -1,5 +1,5 @@
 // gdn_recurrent_launch.cuh -- launches the decode / verify kernel for one (q/k/v type, state type) pair:
-// grid = (ceil(DV / RPC), HV, B), one CTA of kRecurrentThreads per (lane, value head, block of RPC rows).
+// grid = (ceil(DV / RPC), HV, B), one CTA of Split<DK>::THREADS per (lane, value head, block of RPC rows).
 #pragma once
 
 #include "gdn_recurrent.cuh"
@@ -11,7 +11,7 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int RPC = Split<DK>::RPC;
     const size_t smem = sizeof(float) * general_smem_floats(DK, RPC, p.T);
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
-    gdn_recurrent_kernel<DK, InT, StT><<<grid, kRecurrentThreads, smem, s>>>(p);
+    gdn_recurrent_kernel<DK, InT, StT><<<grid, Split<DK>::THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
 
