@@ -36,6 +36,7 @@ import gdn_workloads as W  # noqa: E402
 METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
+                  "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_commit.cu"]
 
 
@@ -96,8 +97,14 @@ def recurrent_bytes(w: W.Workload, A: int) -> int:
     return state_read + state_write + A * w.T * per_tok + w.HV * 8 + w.B * 4
 
 
-def commit_bytes(w: W.Workload, A: int) -> int:
-    return 2 * A * w.HV * w.DV * w.DK * esize(w.state_dtype) + 2 * w.B * 4
+def commit_bytes(w: W.Workload, A: int, accepted_tokens: int = 0) -> int:
+    """Copy commit: one state read and one written per active lane.  Replay commit: the same, plus the
+    accepted tokens' q, k, v, a, b (no outputs)."""
+    b = 2 * A * w.HV * w.DV * w.DK * esize(w.state_dtype) + 2 * w.B * 4
+    if w.commit_mode == "replay":
+        i = esize(w.qkv_dtype)
+        b += accepted_tokens * (2 * w.HK * w.DK * i + w.HV * w.DV * i + 2 * w.HV * i) + w.HV * 8
+    return b
 
 
 # ---- peaks, traffic, clocks -------------------------------------------------------------------------------
@@ -119,10 +126,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
-    """DRAM bytes per launch of the verify/decode kernel from a committed ncu summary, if it was taken on the
-    current kernel sources (``kernel_source_sha256`` line); else None."""
-    p = os.path.join(ROOT, "profiles", f"gdn_recurrent_{workload_name}.md")
+def recorded_traffic(role: str, workload_name: str):
+    """DRAM bytes per launch of the kernel in `role` from the committed ncu summary
+    ``profiles/<role>_<workload>.md``, if it was taken on the current kernel sources
+    (``kernel_source_sha256`` line); else None."""
+    p = os.path.join(ROOT, "profiles", f"{role}_{workload_name}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
@@ -236,7 +244,9 @@ class Step:
         self.gdn, self.torch, self.w = gdn, torch, w
         x = w.arrays()
         self.x = x
-        self.A = int((x["indices"] >= 0).sum())
+        active = x["indices"] >= 0
+        self.A = int(active.sum())
+        self.accepted = int(x["accept_len"][active].sum())
 
         def t(a):
             if a.dtype == np.uint16:
@@ -266,8 +276,13 @@ class Step:
                                     d["indices"], self.o, self.cache, self.err, scale=w.scale, l2_eps=w.l2_eps)
 
     def commit(self):
-        if self.w.commit:
-            d = self.d
+        if not self.w.commit:
+            return
+        d, w = self.d, self.w
+        if w.commit_mode == "replay":
+            self.gdn.gdn_commit_replay(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
+                                       d["indices"], d["accept_len"], self.err, scale=w.scale, l2_eps=w.l2_eps)
+        else:
             self.gdn.gdn_commit(d["pool"], d["indices"], self.cache, d["accept_len"], self.err)
 
     def upload(self):
@@ -358,9 +373,20 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
 
     peak, peak_src = hbm_peak()
     rb = recurrent_bytes(wr, st.A)
-    rec_avg_ms = statistics.mean(rec_ms)
-    achieved = rb / (rec_avg_ms * 1e-3) / 1e9
-    step_bytes = rb + (commit_bytes(wr, st.A) if wr.commit else 0)
+    cb = commit_bytes(wr, st.A, st.accepted) if wr.commit else 0
+    com_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    role = "decode" if w.mode == "decode" else "verify"
+    kernels = [{"role": role, "kernel": "gdn_recurrent_kernel", "avg_us": statistics.mean(rec_ms) * 1e3,
+                "algorithmic_bytes": rb}]
+    if wr.commit:
+        kernels.append({"role": "commit_replay" if wr.commit_mode == "replay" else "commit",
+                        "kernel": "gdn_recurrent_kernel" if wr.commit_mode == "replay" else "gdn_commit_kernel",
+                        "avg_us": statistics.mean(com_ms) * 1e3, "algorithmic_bytes": cb})
+    for k in kernels:
+        k["achieved_gbs"] = k["algorithmic_bytes"] / (k["avg_us"] * 1e-6) / 1e9
+        k["frac"] = k["achieved_gbs"] / peak
+    dom = max(kernels, key=lambda k: k["avg_us"])
+    step_bytes = rb + cb
     clocks = sampler.summary()
     result = {
         "metric": METRIC,
@@ -379,8 +405,8 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
             "workload": w.name, "B": w.B, "active_lanes": st.A, "T": w.T, "HK": w.HK, "HV": w.HV, "DK": w.DK,
             "DV": w.DV, "num_slots": w.num_slots, "state_dtype": w.state_dtype, "qkv_dtype": w.qkv_dtype,
             "out_dtype": w.out_dtype, "intermediate_cache": w.cache, "commit_per_step": w.commit,
-            "step": ("gdn_mtp_verify + gdn_commit" if w.commit else ("gdn_decode" if w.mode == "decode"
-                                                                      else "gdn_mtp_verify")),
+            "step": ("gdn_decode" if w.mode == "decode" else "gdn_mtp_verify" + (
+                (" + gdn_commit_replay" if w.commit_mode == "replay" else " + gdn_commit") if w.commit else "")),
             "l2": "flushed before every step outside its CUDA events (256 MiB write, then 256 MiB read: clean lines)",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
             "timing": "CUDA events per step on the launch stream, summed; max over ranks",
@@ -388,17 +414,18 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
         "verify_steps_per_s": K * world / (total_ms * 1e-3),
         "hbm_gbs_step": step_bytes * world * K / (total_ms * 1e-3) / 1e9,
         "roofline": {
-            "kernel": "gdn_recurrent_kernel (" + ("decode" if w.mode == "decode" else "verify") + ")",
+            "kernel": f"{dom['kernel']} ({dom['role']})",
             "bound": "hbm",
-            "achieved": achieved,
+            "achieved": dom["achieved_gbs"],
             "peak": peak,
             "unit": "GB/s",
-            "frac": achieved / peak,
+            "frac": dom["frac"],
             "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
-            "algorithmic_bytes_per_launch": rb,
-            "avg_launch_us": rec_avg_ms * 1e3,
-            "traffic": recorded_traffic(w.name),
+            "algorithmic_bytes_per_launch": dom["algorithmic_bytes"],
+            "avg_launch_us": dom["avg_us"],
+            "traffic": recorded_traffic(dom["role"], w.name),
         },
+        "kernels": kernels,
         "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": st.h2d_bytes,
                 "d2h_bytes_per_step": st.d2h_bytes},
         "gpu_launches": st.launches_per_step * K,
@@ -444,7 +471,9 @@ def oracle_pair_step(orc, w: W.Workload, d: dict, y: dict):
         orc.decode(d, y, y["pool"])
         return
     _, cache, _ = orc.verify(d, y, cache=w.cache)
-    if w.commit:
+    if w.commit and w.commit_mode == "replay":
+        orc.commit_replay(d, y, y["pool"], y["accept_len"])
+    elif w.commit:
         orc.commit(d, y["pool"], y["indices"], cache, y["accept_len"])
 
 
@@ -515,7 +544,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["verify4", "verify8", "decode", "sweep", "tiny"], default="verify4")
+    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep"], default="verify4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

@@ -7,6 +7,7 @@ library has not been built, every call raises.
     gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, scale=1.0, l2_eps=1e-6)
     gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
     gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
+    gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, ...)
 
 Shapes and semantics are those of ``include/gdn.h``: q, k ``[B,T,HK,DK]``; v, o ``[B,T,HV,DV]``; a, b
 ``[B,T,HV]``; A_log, dt_bias ``[HV]`` fp32; state_pool ``[num_slots,HV,DV,DK]``; state_indices, accept_len
@@ -20,7 +21,7 @@ from typing import Optional
 
 from .build import LIB_PATH
 
-__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "GdnError", "GdnDims", "lib", "STATUS",
+__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "GdnError", "GdnDims", "lib", "STATUS",
            "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "MAX_T", "EXPORTS"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
@@ -29,8 +30,8 @@ ERRBIT_INDEX = 1
 ERRBIT_ACCEPT_LEN = 2
 MAX_T = 16
 F32, BF16 = 0, 1
-EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_status_string", "gdn_last_cuda_error",
-           "gdn_abi_version")
+EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_status_string",
+           "gdn_last_cuda_error", "gdn_abi_version")
 
 
 class GdnDims(ctypes.Structure):
@@ -64,7 +65,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, ip, vp]
         L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
         L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
-        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit):
+        L.gdn_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip, ip, vp]
+        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay):
             f.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -119,7 +121,8 @@ def _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale,
     HV, DV = v.shape[2], v.shape[3]
     _shape(k, q.shape, "k")
     _shape(v, (B, T, HV, DV), "v")
-    _shape(o, (B, T, HV, DV), "o")
+    if o is not None:
+        _shape(o, (B, T, HV, DV), "o")
     _shape(a, (B, T, HV), "a")
     _shape(b, (B, T, HV), "b")
     _shape(A_log, (HV,), "A_log")
@@ -136,8 +139,9 @@ def _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale,
             raise TypeError(f"{n} must be fp32")
     if state_indices.dtype != torch.int32:
         raise TypeError("state_indices must be int32")
-    return GdnDims(B, T, HK, HV, DK, DV, num_slots, qkv, _code(state_pool, "state_pool"), _code(o, "o"),
-                   float(scale), float(l2_eps))
+    out = _code(o, "o") if o is not None else _code(state_pool, "state_pool")
+    return GdnDims(B, T, HK, HV, DK, DV, num_slots, qkv, _code(state_pool, "state_pool"), out, float(scale),
+                   float(l2_eps))
 
 
 def _call(status: int, what: str) -> None:
@@ -194,3 +198,20 @@ def gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_w
     _call(L.gdn_commit(ctypes.byref(d), _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
                        _dev(intermediate_states, "intermediate_states"), _dev(accept_len, "accept_len"),
                        _dev(err_word, "err_word"), _stream(stream)), "gdn_commit")
+
+
+def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, *,
+                      scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """The first ``accept_len[b]`` tokens again from ``state_pool[state_indices[b]]``, final state written back
+    (the verify call's inputs; no outputs).  Same pool bits as ``gdn_commit`` after a caching verify."""
+    import torch
+
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, None, scale, l2_eps)
+    _shape(accept_len, (d.B,), "accept_len")
+    if accept_len.dtype != torch.int32:
+        raise TypeError("accept_len must be int32")
+    _call(L.gdn_commit_replay(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+                              _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+                              _dev(state_indices, "state_indices"), _dev(accept_len, "accept_len"),
+                              _dev(err_word, "err_word"), _stream(stream)), "gdn_commit_replay")

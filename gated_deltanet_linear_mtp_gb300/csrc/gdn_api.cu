@@ -45,10 +45,11 @@ gdn_status check_dims(const gdn_dims* d, bool need_io) {
     return GDN_OK;
 }
 
+// `o` may be NULL only where the call has no outputs (replay commit: need_o = false).
 gdn_status check_io(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
                     const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, const void* o,
-                    const int32_t* err) {
-    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !pool || !idx || !o) return GDN_ERR_NULL;
+                    const int32_t* err, bool need_o = true) {
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !pool || !idx || (need_o && !o)) return GDN_ERR_NULL;
     const uintptr_t in_sz = dtype_bytes(d->qkv_dtype);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(pool, 16)) return GDN_ERR_ALIGN;
     if (!aligned(v, in_sz) || !aligned(a, in_sz) || !aligned(b, in_sz)) return GDN_ERR_ALIGN;
@@ -66,8 +67,8 @@ gdn_status finish(cudaError_t e) {
 
 gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a,
                          const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
-                         void* pool_out, const int32_t* idx, void* o, void* cache, int32_t* err,
-                         cudaStream_t stream) {
+                         void* pool_out, const int32_t* idx, const int32_t* steps, void* o, void* cache,
+                         int32_t* err, cudaStream_t stream) {
     RecurrentParams p;
     p.q = q;
     p.k = k;
@@ -79,6 +80,7 @@ gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const 
     p.pool_in = pool_in;
     p.pool_out = pool_out;
     p.indices = idx;
+    p.steps = steps;
     p.o = o;
     p.cache = cache;
     p.err = err;
@@ -88,6 +90,7 @@ gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const 
     p.DV = d->DV;
     p.num_slots = d->num_slots;
     p.out_bf16 = d->out_dtype == GDN_BF16;
+    p.v_vec = aligned(v, 16) && ((int64_t)d->DV * (int64_t)dtype_bytes(d->qkv_dtype)) % 16 == 0;
     p.scale = d->scale;
     p.l2_eps = d->l2_eps;
     const bool qkv_bf16 = d->qkv_dtype == GDN_BF16;
@@ -110,8 +113,8 @@ gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const 
     if (dims->B == 0) return GDN_OK;
     s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
     if (s != GDN_OK) return s;
-    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, o, nullptr,
-                         err_word, reinterpret_cast<cudaStream_t>(stream));
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, nullptr, o,
+                         nullptr, err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
@@ -124,7 +127,7 @@ gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, co
     s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
     if (s != GDN_OK) return s;
     if (intermediate_states && !aligned(intermediate_states, 16)) return GDN_ERR_ALIGN;
-    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, o,
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o,
                          intermediate_states, err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -148,6 +151,21 @@ gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* sta
     p.num_slots = dims->num_slots;
     p.lane_bytes = (int64_t)dims->HV * dims->DV * dims->DK * (int64_t)dtype_bytes(dims->state_dtype);
     return finish(launch_commit(p, dims->B, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                             const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                             const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
+                             gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, nullptr, err_word, false);
+    if (s != GDN_OK) return s;
+    if (!accept_len) return GDN_ERR_NULL;
+    if (!aligned(accept_len, 4)) return GDN_ERR_ALIGN;
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, accept_len,
+                         nullptr, nullptr, err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gdn_status_string(gdn_status status) {

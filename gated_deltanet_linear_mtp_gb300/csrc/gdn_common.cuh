@@ -105,9 +105,11 @@ struct Split {
     static constexpr int RPC = RPW * WARPS;                 // rows per CTA
     static_assert(P >= RL && 32 % P == 0, "DK must be 16, 32, 64, 128 or 256");
 
-    // row (inside the CTA's block) of slot i of lane (warp, rg)
-    __device__ __forceinline__ static int row(int warp, int rg, int i) { return warp * RPW + i * NRG + rg; }
-    // slot whose complete dot products lane p holds after the reduction in token_update
+    // row (inside the CTA's block) of logical row slot j of lane (warp, rg)
+    __device__ __forceinline__ static int row(int warp, int rg, int j) { return warp * RPW + j * NRG + rg; }
+    // The logical row slot whose complete dot products lane p holds after the reduction in token_update.
+    // A lane stores its rows in the order "register slot s holds logical slot s ^ own_slot(p)", so that at
+    // every halving step of the reduction all lanes keep their first half and send their second half.
     __device__ __forceinline__ static int own_slot(int p) {
         int i = 0;
 #pragma unroll
@@ -115,7 +117,13 @@ struct Split {
             if (p & (P >> (l + 1))) i += RL >> (l + 1);
         return i;
     }
-    // the lowest lane (p) holding the complete dot products of slot i
+    // Shared-memory position of column `col` of a normalised k or q row.  Lane p reads its columns
+    // [8p, 8p + 4) as one float4 at 4p and [8p + 4, 8p + 8) as one float4 at DK/2 + 4p, so the P lanes of a
+    // row group read one contiguous, bank-conflict-free span per load.
+    __host__ __device__ __forceinline__ static int kq_pos(int col) {
+        return (col >> 3) * 4 + ((col & 4) ? DK / 2 : 0) + (col & 3);
+    }
+    // the lowest lane (p) holding the complete dot products of logical slot i
     __device__ __forceinline__ static int owner_p(int i) {
         int p = 0;
 #pragma unroll
@@ -159,28 +167,48 @@ struct Slice8 {
     }
 };
 
+// Per-lane constants of the token loop, computed once per CTA.
+template <int DK>
+struct LaneRows {
+    using SP = Split<DK>;
+    int code;               // own_slot(p): register slot s holds logical slot s ^ code
+    int row[SP::RL];        // row (inside the CTA's block) held in register slot s
+    int src[SP::RL];        // lane holding the delta of register slot s's row
+    int own_row;            // row whose delta and output this lane forms
+    __device__ __forceinline__ LaneRows(int warp, int rg, int p) {
+        code = SP::own_slot(p);
+#pragma unroll
+        for (int s = 0; s < SP::RL; ++s) {
+            row[s] = SP::row(warp, rg, s ^ code);
+            src[s] = rg * SP::P + SP::owner_p(s ^ code);
+        }
+        own_row = SP::row(warp, rg, code);
+    }
+};
+
 // One token on a lane's RL x 8 state elements, held as RL x 4 pairs of adjacent columns so that the dot
 // products and the update run on packed fp32x2 multiply-adds (each half rounds like a scalar fmaf).
-//   kt, qt   normalised k and q of the token (fp32, shared memory, DK each)
-//   v_rows   v of the token for the CTA's RPC rows (shared memory, element type VT)
+//   kt, qt   normalised k and q of the token (fp32, shared memory, DK each, columns at Split::kq_pos)
+//   v_own    v of the token for the lane's own row (LaneRows::own_row)
 // Row dot products a = s.kh and c = s.qh: 8-column partial sums (even and odd columns accumulate
 // separately), then a transposed butterfly over the P lanes of the row group: at each of log2(RL) halving
-// steps a lane keeps half of its rows and swaps the other half with its partner, then plain xor steps
-// finish the sum.  Lane p ends with the complete sums of row slot own_slot(p), forms that row's delta and
-// output, and the deltas of its RL rows are gathered back with shuffles for the update.  Returns the
-// output (before scale) of row slot own_slot(p).
-template <int DK, typename VT>
+// steps every lane keeps the first half of its rows and sends the second half to its partner (the
+// lane-dependent register order of LaneRows makes the halves line up), then plain xor steps finish the
+// sum.  Lane p ends with the complete sums of its own row, forms that row's delta and output, and the
+// deltas of its RL rows are gathered back with shuffles for the update.  Returns the output (before
+// scale) of the own row.
+template <int DK>
 __device__ __forceinline__ float token_update(float2 (&S)[Split<DK>::RL][4], const float* kt, const float* qt, float g,
-                                              float beta, const VT* v_rows, int warp, int rg, int p, float kq) {
+                                              float beta, float v_own, float kq, int p, const LaneRows<DK>& lr) {
     using SP = Split<DK>;
     constexpr int RL = SP::RL;
     constexpr int P = SP::P;
     float2 k2[4], q2[4];
     {
-        const float4 k0 = *reinterpret_cast<const float4*>(kt + 8 * p);
-        const float4 k1 = *reinterpret_cast<const float4*>(kt + 8 * p + 4);
-        const float4 q0 = *reinterpret_cast<const float4*>(qt + 8 * p);
-        const float4 q1 = *reinterpret_cast<const float4*>(qt + 8 * p + 4);
+        const float4 k0 = *reinterpret_cast<const float4*>(kt + 4 * p);
+        const float4 k1 = *reinterpret_cast<const float4*>(kt + DK / 2 + 4 * p);
+        const float4 q0 = *reinterpret_cast<const float4*>(qt + 4 * p);
+        const float4 q1 = *reinterpret_cast<const float4*>(qt + DK / 2 + 4 * p);
         k2[0] = make_float2(k0.x, k0.y);
         k2[1] = make_float2(k0.z, k0.w);
         k2[2] = make_float2(k1.x, k1.y);
@@ -205,16 +233,10 @@ __device__ __forceinline__ float token_update(float2 (&S)[Split<DK>::RL][4], con
 #pragma unroll
     for (int l = 0; l < SP::LOG_RL; ++l) {
         const int m = P >> (l + 1);
-        const bool up = (p & m) != 0;
 #pragma unroll
         for (int j = 0; j < (RL >> (l + 1)); ++j) {
-            const int hj = j + (RL >> (l + 1));
-            const float sa = up ? a[j] : a[hj];
-            const float sc = up ? c[j] : c[hj];
-            const float ka = up ? a[hj] : a[j];
-            const float kc = up ? c[hj] : c[j];
-            a[j] = ka + __shfl_xor_sync(0xffffffffu, sa, m);
-            c[j] = kc + __shfl_xor_sync(0xffffffffu, sc, m);
+            a[j] += __shfl_xor_sync(0xffffffffu, a[j + (RL >> (l + 1))], m);
+            c[j] += __shfl_xor_sync(0xffffffffu, c[j + (RL >> (l + 1))], m);
         }
     }
 #pragma unroll
@@ -222,13 +244,12 @@ __device__ __forceinline__ float token_update(float2 (&S)[Split<DK>::RL][4], con
         a[0] += __shfl_xor_sync(0xffffffffu, a[0], m);
         c[0] += __shfl_xor_sync(0xffffffffu, c[0], m);
     }
-    const int own = SP::own_slot(p);
-    const float delta = beta * (to_f32(v_rows[SP::row(warp, rg, own)]) - g * a[0]);
+    const float delta = beta * (v_own - g * a[0]);
     const float out = fmaf(g, c[0], delta * kq);
     const float2 g2 = make_float2(g, g);
 #pragma unroll
     for (int i = 0; i < RL; ++i) {
-        const float d = __shfl_sync(0xffffffffu, delta, rg * P + SP::owner_p(i));
+        const float d = __shfl_sync(0xffffffffu, delta, lr.src[i]);
         const float2 d2 = make_float2(d, d);
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[i][e] = __ffma2_rn(d2, k2[e], __fmul2_rn(g2, S[i][e]));

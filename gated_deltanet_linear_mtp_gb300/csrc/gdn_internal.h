@@ -8,8 +8,9 @@
 
 namespace gdn {
 
-// Decode and verify share one kernel: decode writes the final state back (pool_out == pool_in),
-// verify optionally stores every intermediate state (cache != nullptr) and never writes the pool.
+// Decode, verify and replay commit share one kernel: decode writes the final state back (pool_out ==
+// pool_in); verify optionally stores every intermediate state (cache != nullptr) and never writes the
+// pool; replay commit runs steps[b] tokens per lane, writes no outputs and writes the state back.
 struct RecurrentParams {
     const void* q;
     const void* k;
@@ -21,11 +22,13 @@ struct RecurrentParams {
     const void* pool_in;
     void* pool_out;  // nullptr: no write-back (verify)
     const int32_t* indices;
-    void* o;
-    void* cache;     // nullptr: no intermediate states
+    const int32_t* steps;  // nullptr: T tokens per lane; else steps[b] in 0..T (replay commit)
+    void* o;               // nullptr: no outputs (replay commit)
+    void* cache;           // nullptr: no intermediate states
     int32_t* err;    // nullable
     int T, HK, HV, DV, num_slots;
     int out_bf16;
+    int v_vec;  // v starts on 16 bytes and DV * sizeof(v) % 16 == 0: v is read in 16-byte chunks
     float scale, l2_eps;
 };
 

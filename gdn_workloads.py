@@ -99,6 +99,7 @@ class Workload:
     scale: float = 1.0
     l2_eps: float = 1e-6
     pool_seed: Optional[int] = None  # None: the pool is drawn from `seed`
+    commit_mode: str = "copy"        # "copy": from the cached states; "replay": re-run the accepted tokens
 
     @property
     def n_padded(self) -> int:
@@ -188,6 +189,17 @@ def verify_t8() -> Workload:
                     cache=True, commit=True, seed=3, pad_fraction=0.1)
 
 
+def verify_t4_replay() -> Workload:
+    """verify_t4 without intermediate caching; the accepted prefix is committed by replaying it."""
+    return verify_t4().replace(name="mtp_verify_T4_B128_bf16state_replay_commit", cache=False, commit_mode="replay")
+
+
+def verify_t8_replay() -> Workload:
+    """verify_t8 without intermediate caching; the accepted prefix is committed by replaying it."""
+    return verify_t8().replace(name="mtp_verify_T8_B256_pad10_bf16state_replay_commit", cache=False,
+                               commit_mode="replay")
+
+
 SWEEP_B = (1, 4, 16, 64, 128, 256)
 SWEEP_T = (1, 2, 4, 8)
 SWEEP_STATE = (F32, BF16)
@@ -212,4 +224,5 @@ def sweep() -> List[Workload]:
     return pts
 
 
-NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8}
+NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8,
+         "verify4_replay": verify_t4_replay, "verify8_replay": verify_t8_replay}

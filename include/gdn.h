@@ -124,6 +124,22 @@ gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* sta
                       const void* intermediate_states, const int32_t* accept_len, int32_t* err_word,
                       gdn_stream_t stream);
 
+/*
+ * gdn_commit_replay -- the same pool update as gdn_commit, without intermediate states: for every active
+ * lane with accept_len[b] >= 1, the first accept_len[b] tokens are run again from state_pool[slot] (which
+ * gdn_mtp_verify left unchanged) and the final state is written back into that slot, rounded to
+ * state_dtype.  Same arithmetic as gdn_mtp_verify, so the slot receives exactly the bits gdn_commit would
+ * copy from intermediate_states[b, accept_len[b] - 1].  q, k, v, a, b, A_log, dt_bias, scale and l2_eps
+ * must be those the verify call used; no outputs are written; accept_len 0 leaves the slot as it is,
+ * lengths outside 0..T set GDN_ERRBIT_ACCEPT_LEN.  Verify then moves 1 state instead of 1 + T, at the cost
+ * of reading each state once more here: the cached replay with in-kernel commit of TensorRT-LLM PR #20937
+ * (GB300 Qwen3.8-Flash-Next NVFP4), "MTP > Verify" and "Moved out of this PR".
+ */
+gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                             const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                             const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
+                             gdn_stream_t stream);
+
 /* Static string naming a status; never NULL. */
 const char* gdn_status_string(gdn_status status);
 

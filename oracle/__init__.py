@@ -56,7 +56,8 @@ class Oracle:
         self.lib.orc_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp]
         self.lib.orc_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp]
         self.lib.orc_commit.argtypes = [dp, vp, ip, vp, ip]
-        for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit):
+        self.lib.orc_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip]
+        for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit, self.lib.orc_commit_replay):
             f.restype = ctypes.c_int
         for name in ("orc_round_bf16", "orc_softplus", "orc_sigmoid"):
             getattr(self.lib, name).argtypes = [ctypes.c_double]
@@ -144,6 +145,20 @@ class Oracle:
         if flags < 0:
             raise ValueError(f"oracle rejected dims ({flags})")
         return o, flags
+
+    def commit_replay(self, d: Dict, x: Dict[str, np.ndarray], pool: np.ndarray, accept_len: np.ndarray) -> int:
+        """Replay commit in place: the first accept_len[b] tokens from pool[idx[b]], written back."""
+        B = x["q"].shape[0]
+        q, k, v, a, b, A_log, dt_bias, idx = self._inputs(d, x, B)
+        assert pool.flags["C_CONTIGUOUS"]
+        self._check(pool, d["state_dtype"], (d["num_slots"], d["HV"], d["DV"], d["DK"]), "pool")
+        L = np.ascontiguousarray(accept_len, dtype=np.int32)
+        dims = self._dims(d, B)
+        flags = self.lib.orc_commit_replay(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                           _ptr(A_log), _ptr(dt_bias), _ptr(pool), _ptr(idx), _ptr(L))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return flags
 
     def commit(self, d: Dict, pool: np.ndarray, indices: np.ndarray, cache: np.ndarray,
                accept_len: np.ndarray) -> int:

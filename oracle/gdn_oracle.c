@@ -24,6 +24,8 @@
  *       verify with caching: cache[b,t,h] = R(S)
  *     decode: pool[slot, h] = R(S)
  *   commit: pool[idx[b], h] = cache[b, L_b - 1, h] for lanes with L_b >= 1.
+ *   replay commit: the first L_b tokens again from pool[idx[b], h], then pool[idx[b], h] = R(S): the
+ *     same value as the commit above, without caching every intermediate state.
  *
  * Padded lanes (index -1) are skipped: the page's padding index guard (sglang PR #23273, Requirements,
  * FlashInfer #2810).  bf16 state with intermediate caching beyond T > 4: same page, Requirements
@@ -123,11 +125,13 @@ static int lane_slot(const orc_dims* d, const int32_t* idx, int b, int* flags) {
     return slot;
 }
 
-/* Runs the T tokens of every active lane.  If cache != NULL, stores R(S) after every token (verify).
- * If write_back, stores R(S) of the last token into the lane's pool slot (decode). */
+/* Runs the tokens of every active lane: all T, or steps[b] of them if steps != NULL (a count outside 0..T
+ * sets flag bit 1 and skips the lane).  If o != NULL, stores the outputs.  If cache != NULL, stores R(S)
+ * after every token (verify).  If write_back, stores R(S) of the last token run into the lane's pool slot
+ * (decode; replay commit). */
 static int run(const orc_dims* d, const void* q, const void* k, const void* v, const void* a,
                const void* bb, const float* A_log, const float* dt_bias, void* pool, const int32_t* idx,
-               double* o, void* cache, int write_back) {
+               double* o, void* cache, int write_back, const int32_t* steps) {
     const int B = d->B, T = d->T, HK = d->HK, HV = d->HV, DK = d->DK, DV = d->DV;
     const int r = HV / HK;
     int flags = 0;
@@ -142,13 +146,19 @@ static int run(const orc_dims* d, const void* q, const void* k, const void* v, c
     for (int b = 0; b < B; ++b) {
         int slot = lane_slot(d, idx, b, &flags);
         if (slot < 0) continue;
+        const int n_tok = steps ? steps[b] : T;
+        if (n_tok < 0 || n_tok > T) {
+            flags |= 2;
+            continue;
+        }
+        if (n_tok == 0) continue;
         for (int h = 0; h < HV; ++h) {
             const int hk = h / r;
             const int64_t state_off = ((int64_t)slot * HV + h) * DV * DK;
             for (int i = 0; i < DV; ++i)
                 for (int j = 0; j < DK; ++j) S[i * DK + j] = load(pool, d->state_dtype, state_off + i * DK + j);
 
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < n_tok; ++t) {
                 const int64_t qk_off = (((int64_t)b * T + t) * HK + hk) * DK;
                 const int64_t ab_off = ((int64_t)b * T + t) * HV + h;
                 const int64_t v_off = (((int64_t)b * T + t) * HV + h) * DV;
@@ -177,7 +187,7 @@ static int run(const orc_dims* d, const void* q, const void* k, const void* v, c
                     const double delta = beta * (load(v, d->qkv_dtype, v_off + i) - u[i]);
                     for (int j = 0; j < DK; ++j) S[i * DK + j] += delta * kh[j];
                 }
-                for (int i = 0; i < DV; ++i) {
+                for (int i = 0; o && i < DV; ++i) {
                     double s = 0.0;
                     for (int j = 0; j < DK; ++j) s += S[i * DK + j] * qh[j];
                     o[v_off + i] = d->scale * s;
@@ -205,14 +215,23 @@ int orc_verify(const orc_dims* d, const void* q, const void* k, const void* v, c
                const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, double* o,
                void* cache) {
     if (!dims_ok(d)) return -2;
-    return run(d, q, k, v, a, b, A_log, dt_bias, (void*)pool, idx, o, cache, 0);
+    return run(d, q, k, v, a, b, A_log, dt_bias, (void*)pool, idx, o, cache, 0, NULL);
 }
 
 /* T tokens from pool[idx[b]], final state written back into the same slot. */
 int orc_decode(const orc_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
                const float* A_log, const float* dt_bias, void* pool, const int32_t* idx, double* o) {
     if (!dims_ok(d)) return -2;
-    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1);
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1, NULL);
+}
+
+/* Replay commit: the first accept_len[b] tokens of every active lane from pool[idx[b]], the final state
+ * written back into that slot (no outputs).  Equals orc_commit after orc_verify with caching. */
+int orc_commit_replay(const orc_dims* d, const void* q, const void* k, const void* v, const void* a,
+                      const void* b, const float* A_log, const float* dt_bias, void* pool, const int32_t* idx,
+                      const int32_t* accept_len) {
+    if (!dims_ok(d)) return -2;
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, NULL, NULL, 1, accept_len);
 }
 
 /* pool[idx[b], :] = cache[b, L_b - 1, :] (all heads), bit for bit, for active lanes with L_b >= 1. */

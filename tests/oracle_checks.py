@@ -20,6 +20,7 @@ What pins what:
 * chained calls         -- verify(T) == T decodes; cache[t] == state after t+1 decodes; commit(L) == state
   after L decodes == cache[L-1] bit for bit.
 * padding / bad data    -- canaries untouched, flag bits set.
+* replay commit         -- equals the cached commit bit for bit and the product form after L tokens.
 """
 from __future__ import annotations
 
@@ -326,6 +327,38 @@ def check_padding_and_bad_data(orc):
     assert np.array_equal(pool, x["pool"])
 
 
+def check_commit_replay(orc):
+    """Replay commit == cached commit, bit for bit; == the product-form state after L tokens (brute.py),
+    rounded to bf16; accept length 0 is a no-op; lengths outside 0..T set flag 2 and touch nothing."""
+    from gdn_workloads import to_bf16_bits
+
+    T = 4
+    d, x = _random_case(B=4, T=T, HK=2, HV=4, DK=8, DV=6, seed=51)
+    d = dict(d, state_dtype="bf16")
+    x["pool"] = to_bf16_bits((np.random.default_rng(52).standard_normal(x["pool"].shape) * 0.2).astype(np.float32))
+    x["indices"][2] = -1
+    _, cache, _ = orc.verify(d, x, cache=True)
+    acc = np.array([1, 3, 2, 4], np.int32)
+    p_copy = x["pool"].copy()
+    assert orc.commit(d, p_copy, x["indices"], cache, acc) == 0
+    p_replay = x["pool"].copy()
+    assert orc.commit_replay(d, x, p_replay, acc) == 0
+    assert np.array_equal(p_copy, p_replay)
+    untouched = np.setdiff1d(np.arange(d["num_slots"]), x["indices"][[0, 1, 3]])
+    assert np.array_equal(p_replay[untouched], x["pool"][untouched])
+    for b in (0, 1, 3):
+        slot = x["indices"][b]
+        for h in range(d["HV"]):
+            _, states = brute.lane_head(d, x, b, h)
+            want = np.array([orc.round_bf16(v) for v in states[acc[b] - 1].ravel()])
+            got = brute.decode_storage(p_replay[slot, h], "bf16").ravel()
+            assert np.array_equal(got, want), (b, h)
+    p_bad = x["pool"].copy()
+    assert orc.commit_replay(d, x, p_bad, np.array([0, T + 1, 1, -1], np.int32)) == 2
+    assert np.array_equal(p_bad, x["pool"])
+
+
 ALL_CHECKS = [check_bf16_rounding, check_scalar_functions, check_gate_closed_form, check_beta_sigmoid,
               check_beta_zero_pure_decay, check_orthonormal_keys_write_v, check_l2norm_eps, check_scale,
-              check_head_mapping, check_product_form, check_chained_calls, check_padding_and_bad_data]
+              check_head_mapping, check_product_form, check_chained_calls, check_padding_and_bad_data,
+              check_commit_replay]

@@ -76,7 +76,30 @@ def commit(L, d, **ptrs):
                         a["err"], None)
 
 
-@pytest.mark.parametrize("call", [verify, decode, commit])
+def replay(L, d, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, acc=P, err=None)
+    a.update(ptrs)
+    return L.gdn_commit_replay(ctypes.byref(d) if d is not None else None, a["q"], a["k"], a["v"], a["a"], a["b"],
+                               a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["acc"], a["err"], None)
+
+
+@pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "acc"])
+def test_replay_null_pointer(L, ptr):
+    assert replay(L, dims(), **{ptr: None}) == 1
+
+
+def test_replay_checks(L):
+    assert replay(L, None) == 1
+    assert replay(L, dims(T=0)) == 2
+    assert replay(L, dims(DK=48)) == 5
+    assert replay(L, dims(l2_eps=-1.0)) == 7
+    assert replay(L, dims(), q=ODD) == 4
+    assert replay(L, dims(), acc=ctypes.c_void_p(0x10002)) == 4
+    z = dict(q=None, k=None, v=None, a=None, b=None, A_log=None, dt_bias=None, pool=None, idx=None, acc=None)
+    assert replay(L, dims(B=0), **z) == 0
+
+
+@pytest.mark.parametrize("call", [verify, decode, commit, replay])
 def test_null_dims(L, call):
     assert call(L, None) == 1
 
@@ -102,6 +125,7 @@ def test_commit_null_pointer(L, ptr):
 def test_bad_dims(L, kw, status):
     assert verify(L, dims(**kw)) == status
     assert decode(L, dims(**kw)) == status
+    assert replay(L, dims(**kw)) == status
 
 
 def test_commit_ignores_io_fields_but_checks_the_rest(L):

@@ -1,0 +1,93 @@
+"""Host logic of bench.py, on the CPU: algorithmic byte counts, per-rank workloads, the max/sum over ranks
+with two gloo ranks, and the reference arm (the oracle) end to end on the tiny workload."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import gdn_workloads as W
+
+
+def test_algorithmic_bytes_verify_t4():
+    w = W.verify_t4()
+    # state read 128*32*16384*2 + cache write 4x that + per token q,k (2*16*128*2), v, o (32*128*2 each), a, b
+    state = 128 * 32 * 128 * 128 * 2
+    per_tok = 2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 2
+    assert bench.recurrent_bytes(w, 128) == state + 4 * state + 128 * 4 * per_tok + 32 * 8 + 128 * 4
+    assert bench.commit_bytes(w, 128) == 2 * state + 2 * 128 * 4
+
+
+def test_algorithmic_bytes_replay_and_decode():
+    w = W.verify_t4_replay()
+    state = 128 * 32 * 128 * 128 * 2
+    per_tok = 2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 2
+    assert bench.recurrent_bytes(w, 128) == state + 128 * 4 * per_tok + 32 * 8 + 128 * 4
+    in_tok = 2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 2
+    assert bench.commit_bytes(w, 128, 300) == 2 * state + 2 * 128 * 4 + 300 * in_tok + 32 * 8
+    d = W.decode_t1()
+    fstate = 64 * 32 * 128 * 128 * 4
+    assert bench.recurrent_bytes(d, 64) == 2 * fstate + 64 * (2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 2) \
+        + 32 * 8 + 64 * 4
+
+
+def test_rank_workloads_differ_only_in_seed():
+    w = W.verify_t4()
+    w1 = bench.rank_workload(w, 1)
+    assert bench.rank_workload(w, 0) is w
+    assert w1.seed != w.seed and w1.replace(seed=w.seed) == w
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    dist = bench.init_dist(world, "gloo")
+    mx = bench.max_over_ranks(10.0 + rank, dist)
+    sm = bench.sum_over_ranks(1.0 + rank, dist)
+    q.put((rank, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out == [(0, 11.0, 3.0), (1, 11.0, 3.0)]
+
+
+def test_reference_arm_tiny():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+                           "--ref-seconds", "2"]) == 0
+    j = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["cpu_baseline"]["kind"] == "oracle"
+    assert j["config"]["workload"] == W.tiny().name
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"]) == 0
+    assert buf.getvalue() == ""

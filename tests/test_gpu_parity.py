@@ -385,3 +385,60 @@ def test_side_stream_and_graph_replay():
         assert np.array_equal(host(o), o_eager) and np.array_equal(host(cache), c_eager)
         xr = dict(x, accept_len=acc)
         check_commit(w, xr, host(pool0), host(t["pool"]), c_eager)
+
+
+# ---- replay commit: the same pool bits as the cached commit, without caching ----------------------------
+def run_replay(w, t: Dev, pool, accept_len, err=None):
+    gdn.gdn_commit_replay(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], pool, t["indices"],
+                          accept_len, err, scale=w.scale, l2_eps=w.l2_eps)
+
+
+REPLAY = [W.tiny(), W.verify_t4(), W.verify_t8()] + [e for e in EDGE if e.name in (
+    "dk16_dv200_ragged", "dk32_dv33_f32state", "dk128_dv100_ragged_T16", "dk256_dv24_ragged", "hv_8x_hk",
+    "padded_half", "scale_half_f32out")]
+
+
+@pytest.mark.parametrize("w", REPLAY, ids=lambda w: w.name)
+def test_commit_replay_equals_cached_commit(w):
+    x = w.arrays()
+    t = Dev(x)
+    _, cache = run_verify(w, t, cache=True)
+    pool_copy = t["pool"].clone()
+    gdn.gdn_commit(pool_copy, t["indices"], cache, t["accept_len"])
+    pool_rep = t["pool"].clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_replay(w, t, pool_rep, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rep = host(pool_rep)
+    assert np.array_equal(rep, host(pool_copy)), "replay commit differs from the cached commit"
+    # and against the oracle's replay, on sampled lanes
+    idx = x["indices"]
+    act = np.flatnonzero(idx >= 0)
+    lanes = act if len(act) <= 24 else np.sort(np.random.default_rng(9).choice(act, 24, replace=False))
+    xs = take_lanes(x, lanes)
+    pool_ref = x["pool"].copy()
+    assert oracle.default().commit_replay(oracle.dims_of(w), xs, pool_ref, xs["accept_len"]) == 0
+    sl = xs["indices"]
+    check_state(w, rep[sl], pool_ref[sl], "replayed slots")
+    untouched = np.setdiff1d(np.arange(w.num_slots), idx[idx >= 0])
+    assert np.array_equal(rep[untouched], x["pool"][untouched])
+
+
+def test_commit_replay_accept_lengths():
+    w = small("replay_len", B=5, T=4, DK=128, DV=64, num_slots=9)
+    x = w.arrays()
+    x["accept_len"][:] = [0, w.T + 1, -1, 2, w.T]
+    t = Dev(x)
+    pool = t["pool"].clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_replay(w, t, pool, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.ERRBIT_ACCEPT_LEN
+    ph = host(pool)
+    for b in (0, 1, 2):
+        assert np.array_equal(ph[x["indices"][b]], x["pool"][x["indices"][b]])
+    _, cache = run_verify(w, t, cache=True)
+    ch = host(cache)
+    for b, L in ((3, 2), (4, w.T)):
+        assert np.array_equal(ph[x["indices"][b]], ch[b, L - 1])

@@ -45,6 +45,8 @@ MUTANTS = [
     ("commit_first_token", "(((int64_t)b * d->T) + (L - 1)) * per_lane", "(((int64_t)b * d->T) + 0) * per_lane"),
     ("padding_not_skipped", "if (slot == -1) return -1;", "if (slot == -1) return 0;"),
     ("accept_len_unchecked", "if (L < 0 || L > d->T) {", "if (0) {"),
+    ("replay_ignores_accept_len", "const int n_tok = steps ? steps[b] : T;", "const int n_tok = T;"),
+    ("replay_off_by_one", "const int n_tok = steps ? steps[b] : T;", "const int n_tok = steps ? steps[b] - (steps[b] > 1) : T;"),
 ]
 
 
