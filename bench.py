@@ -36,6 +36,7 @@ import gdn_workloads as W  # noqa: E402
 METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
+                  "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent_launch.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_commit.cu"]
 
@@ -236,13 +237,21 @@ class ClockSampler:
 class Step:
     """Device buffers of one workload and the calls of one step, through the public binding."""
 
-    def __init__(self, w: W.Workload, device):
+    def __init__(self, w: W.Workload, device, pool_cache=None):
         import torch
 
         import gated_deltanet_linear_mtp_gb300 as gdn
 
         self.gdn, self.torch, self.w = gdn, torch, w
-        x = w.arrays()
+        x = w.small_arrays()
+        key = (w.state_dtype, w.seed if w.pool_seed is None else w.pool_seed, w.num_slots, w.HV, w.DV, w.DK)
+        if pool_cache is not None and key in pool_cache:
+            x["pool"] = pool_cache[key]
+        else:
+            x["pool"] = w.pool()
+            if pool_cache is not None:  # sweep points of one state dtype share one pool draw
+                pool_cache.clear()
+                pool_cache[key] = x["pool"]
         self.x = x
         active = x["indices"] >= 0
         self.A = int(active.sum())
@@ -297,6 +306,9 @@ class Step:
         return 1 + (1 if self.w.commit else 0)
 
 
+_POOL_CACHE: dict = {}
+
+
 def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, emit=True):
     import torch
 
@@ -304,7 +316,7 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     device = torch.device("cuda", local_rank)
     dist = init_dist(world, "nccl")
     wr = rank_workload(w, rank)
-    st = Step(wr, device)
+    st = Step(wr, device, _POOL_CACHE if args.workload == "sweep" else None)
     props = torch.cuda.get_device_properties(device)
     nflush = max(256 << 20, 2 * props.L2_cache_size) // 4
     flush_w = torch.empty(nflush, dtype=torch.float32, device=device)

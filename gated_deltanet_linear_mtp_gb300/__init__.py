@@ -22,12 +22,14 @@ from typing import Optional
 from .build import LIB_PATH
 
 __all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "GdnError", "GdnDims", "lib", "STATUS",
-           "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "MAX_T", "EXPORTS"]
+           "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT", "MAX_T",
+           "EXPORTS"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_VALUE"}
 ERRBIT_INDEX = 1
 ERRBIT_ACCEPT_LEN = 2
+ERRBIT_TIMEOUT = 4
 MAX_T = 16
 F32, BF16 = 0, 1
 EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_status_string",

@@ -1,6 +1,6 @@
-// gdn_common.cuh -- device building blocks of the decode / verify kernel (sm_103a): storage conversions,
+// gdn_common.cuh -- device building blocks of the decode / verify kernels (sm_103a): storage conversions,
 // 16-byte global accesses, the lane layout of a block of state rows, the per-token row update of the gated
-// delta rule, and the gate and beta scalars.
+// delta rule, the gate and beta scalars, and mbarrier / bulk-copy (TMA) wrappers.
 //
 // The rows of one state S[DV, DK] evolve independently:
 //     u_i = (g s_i) . kh,   s_i <- g s_i + beta (v_i - u_i) kh,   o_i = s_i . qh
@@ -148,6 +148,12 @@ struct Slice8 {
 #pragma unroll
         for (int c = 0; c < NC; ++c) r[c] = ld_state16(src + c * Chunk<StT>::CH);
     }
+    __device__ __forceinline__ static void load_shared(const StT* src, float2 (&s)[4]) {
+        uint4 r[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) r[c] = *reinterpret_cast<const uint4*>(src + c * Chunk<StT>::CH);
+        unpack(r, s);
+    }
     template <bool kStreaming>
     __device__ __forceinline__ static void store_global(StT* dst, const float2 (&s)[4]) {
         float f[8];
@@ -265,5 +271,47 @@ __device__ __forceinline__ float gate(float A_log, float a, float dt_bias) {
 }
 
 __device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+
+// ---- mbarrier and bulk-copy (TMA) wrappers ----------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase with the given parity: false if it did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Global -> shared bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned), completing on
+// the mbarrier `bar` of this CTA.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 
 }  // namespace gdn

@@ -1,17 +1,53 @@
-// gdn_recurrent_launch.cuh -- launches the decode / verify kernel for one (q/k/v type, state type) pair:
-// grid = (ceil(DV / RPC), HV, B), one CTA of Split<DK>::THREADS per (lane, value head, block of RPC rows).
+// gdn_recurrent_launch.cuh -- picks and launches the decode / verify / replay-commit kernel for one
+// (q/k/v type, state type) pair.
+//
+//   gdn_recurrent_staged_kernel, grid = (ceil(DV / (NSUB * RPC)), HV, B), when a CTA has little work per
+//       state byte (T * sizeof(state) <= 8: bf16 with T <= 4, fp32 with T <= 2), so that the state's load
+//       latency dominates and bulk copies keep more bytes in flight, and when that grid still gives every
+//       SM at least two CTAs;
+//   gdn_recurrent_kernel, grid = (ceil(DV / RPC), HV, B), otherwise.
+// The rule follows a B x T x state-dtype sweep of both kernels on the GB300 (the staged kernel was 15-40%
+// faster inside the rule, and 4-80% slower outside it).  Both run Split<DK>::THREADS threads per CTA.
 #pragma once
+
+#include <algorithm>
 
 #include "gdn_recurrent.cuh"
 
 namespace gdn {
 
+constexpr int kStagedMaxTokenBytes = 8;  // T * sizeof(state element) at or below which staging pays
+constexpr int kStagedMinCtasPerSm = 2;
+
+template <typename StT, int DK>
+bool use_staged(const RecurrentParams& p, int B) {
+    if (p.T * (int)sizeof(StT) > kStagedMaxTokenBytes) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const int64_t ctas = (int64_t)B * p.HV * ((p.DV + Staged<DK, StT>::ROWS - 1) / Staged<DK, StT>::ROWS);
+    return ctas >= (int64_t)kStagedMinCtasPerSm * sms;
+}
+
 template <typename InT, typename StT, int DK>
 cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
+    constexpr int NT = Split<DK>::THREADS;
+    if (use_staged<StT, DK>(p, B)) {
+        using ST = Staged<DK, StT>;
+        const uint32_t smem = ST::smem_bytes(p.T);
+        auto kernel = gdn_recurrent_staged_kernel<DK, InT, StT>;
+        if (smem > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        const dim3 grid((p.DV + ST::ROWS - 1) / ST::ROWS, p.HV, B);
+        kernel<<<grid, NT, smem, s>>>(p);
+        return cudaGetLastError();
+    }
     constexpr int RPC = Split<DK>::RPC;
-    const size_t smem = sizeof(float) * general_smem_floats(DK, RPC, p.T);
+    const size_t smem = direct_smem_bytes<DK>(p.T);
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
-    gdn_recurrent_kernel<DK, InT, StT><<<grid, Split<DK>::THREADS, smem, s>>>(p);
+    gdn_recurrent_kernel<DK, InT, StT><<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 

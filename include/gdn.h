@@ -38,8 +38,10 @@
  *   - Errors the host can see are returned as a status before anything is enqueued.  Errors that depend on
  *     device data are defined, never a fault: a lane whose index is < -1 or >= num_slots, or (commit) whose
  *     accept length is outside 0..T, is skipped and a bit is OR-ed into *err_word (if err_word is not NULL):
- *     GDN_ERRBIT_INDEX, GDN_ERRBIT_ACCEPT_LEN.  The kernels never wait on other CTAs or on flags, so
- *     they cannot hang.  The caller zeroes *err_word and reads it when it wants.
+ *     GDN_ERRBIT_INDEX, GDN_ERRBIT_ACCEPT_LEN.  No kernel waits on another CTA or on a flag; the only waits
+ *     are on the CTA's own bulk copies of state into shared memory, and they are bounded: one that runs
+ *     out sets GDN_ERRBIT_TIMEOUT and that part of the state is left unprocessed.  The caller zeroes
+ *     *err_word and reads it when it wants.
  *   - Padded lanes (index -1, the padding index guard of FlashInfer #2810, same page, Requirements) are
  *     skipped: their o, intermediate states and pool slots are left untouched, bit for bit.
  *   - Distinct active lanes must use distinct slots in gdn_decode and gdn_commit (they write the pool);
@@ -72,7 +74,7 @@ typedef enum gdn_status {
 
 typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
-enum { GDN_ERRBIT_INDEX = 1, GDN_ERRBIT_ACCEPT_LEN = 2 };
+enum { GDN_ERRBIT_INDEX = 1, GDN_ERRBIT_ACCEPT_LEN = 2, GDN_ERRBIT_TIMEOUT = 4 };
 
 enum { GDN_MAX_T = 16 }; /* tokens per call: decode (T >= 1), verify up to 16 (the page's MTP beyond T > 4) */
 

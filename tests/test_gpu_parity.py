@@ -222,6 +222,15 @@ EDGE = [
     small("scale_half_f32out", DK=128, DV=64, out="f32", scale=0.5),
     small("b1", B=1, DK=128, DV=128),
     small("padded_half", B=8, num_slots=12, DK=128, DV=72, pad=0.5),
+    # few tokens per state byte and >= 2 CTAs per SM: the bulk-copy staged kernel (several row blocks per
+    # CTA), with ragged last blocks
+    small("staged_dk128_dv100_T2", B=8, HK=16, HV=48, DK=128, DV=100, T=2, num_slots=10),
+    small("staged_dk64_dv200_T1", B=8, HK=16, HV=48, DK=64, DV=200, T=1, num_slots=10),
+    small("staged_dk256_dv24_T2_f32", B=8, HK=16, HV=48, DK=256, DV=24, T=2, state="f32", out="f32", num_slots=10),
+    small("staged_dk16_dv200_T1_f32in", B=8, HK=16, HV=48, DK=16, DV=200, T=1, qkv="f32", num_slots=10),
+    small("staged_dk32_dv96_T2_f32state", B=8, HK=16, HV=48, DK=32, DV=96, T=2, state="f32", num_slots=10),
+    small("staged_bf16_T4", B=8, HK=16, HV=48, DK=128, DV=136, T=4, num_slots=10),
+    small("staged_padded", B=16, HK=16, HV=48, num_slots=20, DK=128, DV=136, T=2, pad=0.5),
 ]
 
 
@@ -239,8 +248,8 @@ def test_edge_verify(w):
 
 
 @pytest.mark.parametrize("w", [e for e in EDGE if e.name in ("dk16_dv200_ragged", "dk128_dv100_ragged_T16",
-                                                                 "dk256_dv24_ragged", "padded_half")],
-                         ids=lambda w: w.name)
+                                                                 "dk256_dv24_ragged", "padded_half")
+                               or e.name.startswith("staged")], ids=lambda w: w.name)
 def test_edge_decode(w):
     w = w.replace(mode="decode")
     x = w.arrays()
@@ -395,7 +404,7 @@ def run_replay(w, t: Dev, pool, accept_len, err=None):
 
 REPLAY = [W.tiny(), W.verify_t4(), W.verify_t8()] + [e for e in EDGE if e.name in (
     "dk16_dv200_ragged", "dk32_dv33_f32state", "dk128_dv100_ragged_T16", "dk256_dv24_ragged", "hv_8x_hk",
-    "padded_half", "scale_half_f32out")]
+    "padded_half", "scale_half_f32out", "staged_dk128_dv100_T2", "staged_padded")]
 
 
 @pytest.mark.parametrize("w", REPLAY, ids=lambda w: w.name)
