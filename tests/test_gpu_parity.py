@@ -451,3 +451,58 @@ def test_commit_replay_accept_lengths():
     ch = host(cache)
     for b, L in ((3, 2), (4, w.T)):
         assert np.array_equal(ph[x["indices"][b]], ch[b, L - 1])
+
+
+# ---- degenerate cases of the method and maximum sizes ------------------------------------------------------
+def _degenerate_case(kind, state="f32", qkv="f32", out="f32"):
+    w = small(f"degenerate_{kind}", B=2, T=4, HK=1, HV=2, DK=128, DV=64, num_slots=4, qkv=qkv, state=state, out=out)
+    x = w.arrays()
+    rng = np.random.default_rng(8)
+    as_store = (lambda a: np.asarray(a, np.float32)) if qkv == "f32" else W.to_bf16_bits
+    if kind == "orthonormal":  # g = 1, beta = 1, keys orthonormal, q = k: the delta rule writes v exactly
+        Q, _ = np.linalg.qr(rng.standard_normal((128, 128)))
+        keys = Q[:, :w.T].T.astype(np.float32)
+        k = np.broadcast_to(keys[None, :, None, :], x["k"].shape).copy()
+        x["k"] = as_store(k)
+        x["q"] = as_store(k)
+        x["a"] = as_store(np.full(x["a"].shape, -np.inf, np.float32))
+        x["b"] = as_store(np.full(x["b"].shape, np.inf, np.float32))
+    elif kind == "beta0":  # beta = 0: pure decay
+        x["b"] = as_store(np.full(x["b"].shape, -np.inf, np.float32))
+    elif kind == "zero_keys":  # k = 0: kh = 0, no write, pure decay
+        x["k"] = as_store(np.zeros(x["k"].shape, np.float32))
+    return w, x
+
+
+@pytest.mark.parametrize("kind", ["orthonormal", "beta0", "zero_keys"])
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_degenerate_cases(kind, state):
+    w, x = _degenerate_case(kind, state=state, qkv="f32" if state == "f32" else "bf16",
+                            out="f32" if state == "f32" else "bf16")
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    oh, ch = host(o), host(cache)
+    assert np.all(np.isfinite(storage_to_f64(oh))) and np.all(np.isfinite(storage_to_f64(ch)))
+    compare_verify(w, x, oh, ch)
+    if kind == "orthonormal" and state == "f32":
+        v = storage_to_f64(x["v"])
+        assert np.abs(storage_to_f64(oh) - v).max() <= 1e-5 * np.abs(v).max() + 1e-6
+
+
+def test_maximum_batch():
+    """B = 65535 lanes (the grid's z limit), tiny heads; sampled lanes against the oracle."""
+    w = W.Workload("max_B", B=65535, T=2, HK=1, HV=1, DK=16, DV=16, num_slots=65535, qkv_dtype="bf16",
+                   state_dtype="bf16", out_dtype="bf16", mode="verify", cache=True, commit=True, seed=11,
+                   pool_std=0.1, pad_fraction=0.05)
+    x = w.arrays()
+    t = Dev(x)
+    o, cache = run_verify(w, t, cache=True)
+    torch.cuda.synchronize()
+    oh, ch = host(o), host(cache)
+    lanes = np.sort(np.random.default_rng(3).choice(w.B, 48, replace=False))
+    lanes = np.unique(np.concatenate([lanes, [0, w.B - 1]]))
+    compare_verify(w, x, oh, ch, lanes=lanes)
+    pool_before = host(t["pool"])
+    gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
+    check_commit(w, x, pool_before, host(t["pool"]), ch)
