@@ -37,8 +37,27 @@ METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent_launch.cuh",
+                  "gated_deltanet_linear_mtp_gb300/csrc/gdn_verify_chunked.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_commit.cu"]
+
+
+def kernel_name(w, role: str, sms: int) -> str:
+    """Name of the kernel the library launches for one call of the step: the rule of the launcher
+    (gdn_recurrent_launch.cuh) restated for the report."""
+    if role == "commit":
+        return "gdn_commit_kernel"
+    if w.state_dtype == "bf16" and w.T <= 8 and ((role == "verify" and not w.cache) or role == "commit_replay"):
+        return "gdn_verify_chunked_kernel"
+    st = 2 if w.state_dtype == "bf16" else 4
+    p = w.DK // 8
+    rpc = (32 // p) * min(p, 4) * 4  # rows per CTA of the token-by-token kernels
+    block = rpc * w.DK * st
+    nsub = 1 if block >= 32768 else min(8, 32768 // block)
+    ctas = w.B * w.HV * -(-w.DV // (nsub * rpc))
+    if w.T * st <= 8 and ctas >= 2 * sms:
+        return "gdn_recurrent_staged_kernel"
+    return "gdn_recurrent_kernel"
 
 
 # ---------------------------------------------------------------------------------------------------------
@@ -388,11 +407,12 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     cb = commit_bytes(wr, st.A, st.accepted) if wr.commit else 0
     com_ms = [e[1].elapsed_time(e[2]) for e in evs]
     role = "decode" if w.mode == "decode" else "verify"
-    kernels = [{"role": role, "kernel": "gdn_recurrent_kernel", "avg_us": statistics.mean(rec_ms) * 1e3,
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    kernels = [{"role": role, "kernel": kernel_name(wr, role, sms), "avg_us": statistics.mean(rec_ms) * 1e3,
                 "algorithmic_bytes": rb}]
     if wr.commit:
-        kernels.append({"role": "commit_replay" if wr.commit_mode == "replay" else "commit",
-                        "kernel": "gdn_recurrent_kernel" if wr.commit_mode == "replay" else "gdn_commit_kernel",
+        crole = "commit_replay" if wr.commit_mode == "replay" else "commit"
+        kernels.append({"role": crole, "kernel": kernel_name(wr, crole, sms),
                         "avg_us": statistics.mean(com_ms) * 1e3, "algorithmic_bytes": cb})
     for k in kernels:
         k["achieved_gbs"] = k["algorithmic_bytes"] / (k["avg_us"] * 1e-6) / 1e9

@@ -8,11 +8,16 @@
 //   gdn_recurrent_kernel, grid = (ceil(DV / RPC), HV, B), otherwise.
 // The rule follows a B x T x state-dtype sweep of both kernels on the GB300 (the staged kernel was 15-40%
 // faster inside the rule, and 4-80% slower outside it).  Both run Split<DK>::THREADS threads per CTA.
+// On a bf16 pool with T <= 8, a verify that stores neither intermediate states nor a write-back, and a
+// replay commit, run the persistent chunked tensor-core kernel (gdn_verify_chunked.cuh) instead, one CTA
+// per resident slot of the GPU.
 #pragma once
 
 #include <algorithm>
+#include <type_traits>
 
 #include "gdn_recurrent.cuh"
+#include "gdn_verify_chunked.cuh"
 
 namespace gdn {
 
@@ -32,6 +37,12 @@ bool use_staged(const RecurrentParams& p, int B) {
 template <typename InT, typename StT, int DK>
 cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int NT = Split<DK>::THREADS;
+    if constexpr (std::is_same<StT, __nv_bfloat16>::value) {
+        const bool verify_only = p.cache == nullptr && p.pool_out == nullptr && p.steps == nullptr;
+        const bool replay_commit = p.cache == nullptr && p.pool_out != nullptr && p.steps != nullptr && p.o == nullptr;
+        if ((verify_only || replay_commit) && p.T <= kChunkMaxT)
+            return replay_commit ? launch_chunked<DK, InT, true>(p, B, s) : launch_chunked<DK, InT, false>(p, B, s);
+    }
     if (use_staged<StT, DK>(p, B)) {
         using ST = Staged<DK, StT>;
         const uint32_t smem = ST::smem_bytes(p.T);

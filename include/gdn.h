@@ -106,9 +106,11 @@ gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const 
 /*
  * gdn_mtp_verify -- T draft tokens from state_pool[state_indices[b]] (read only: the pool is never
  * written).  If intermediate_states is not NULL, the state after token t is stored, rounded to
- * state_dtype, in intermediate_states[b, t].  MTP verify through the pool API (initial_state_indices) of
- * sglang PR #23273, Summary; bf16 state, T beyond 4 and intermediate caching from its Requirements
- * (FlashInfer #2679).
+ * state_dtype, in intermediate_states[b, t].  Without intermediate_states, bf16 state and T <= 8, the
+ * outputs come from the chunked form of the same recurrence (S_0 [k q] on the tensor cores, k and q split
+ * into bf16 hi + lo parts, about 16 significant bits), within fp32-level error of the token-by-token
+ * outputs.  MTP verify through the pool API (initial_state_indices) of sglang PR #23273, Summary; bf16
+ * state, T beyond 4 and intermediate caching from its Requirements (FlashInfer #2679).
  */
 gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
                           const void* b, const float* A_log, const float* dt_bias, const void* state_pool,
@@ -130,8 +132,11 @@ gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* sta
  * gdn_commit_replay -- the same pool update as gdn_commit, without intermediate states: for every active
  * lane with accept_len[b] >= 1, the first accept_len[b] tokens are run again from state_pool[slot] (which
  * gdn_mtp_verify left unchanged) and the final state is written back into that slot, rounded to
- * state_dtype.  Same arithmetic as gdn_mtp_verify, so the slot receives exactly the bits gdn_commit would
- * copy from intermediate_states[b, accept_len[b] - 1].  q, k, v, a, b, A_log, dt_bias, scale and l2_eps
+ * state_dtype.  fp32 state, or T > 8: the token-by-token arithmetic of gdn_mtp_verify, so the slot receives
+ * exactly the bits gdn_commit would copy from intermediate_states[b, accept_len[b] - 1].  bf16 state with
+ * T <= 8: the same state in chunked form (S_L = gamma S_0 + a sum of rank-1 terms, S_0 k on the tensor
+ * cores with k split into bf16 hi + lo parts), within fp32-level error of that copy before the final bf16
+ * rounding, so the two may differ in the last bf16 bit.  q, k, v, a, b, A_log, dt_bias, scale and l2_eps
  * must be those the verify call used; no outputs are written; accept_len 0 leaves the slot as it is,
  * lengths outside 0..T set GDN_ERRBIT_ACCEPT_LEN.  Verify then moves 1 state instead of 1 + T, at the cost
  * of reading each state once more here: the cached replay with in-kernel commit of TensorRT-LLM PR #20937

@@ -36,6 +36,19 @@ def test_algorithmic_bytes_replay_and_decode():
         + 32 * 8 + 64 * 4
 
 
+def test_kernel_names_follow_the_launcher_rule():
+    sms = 152
+    v4, v8, d1 = W.verify_t4(), W.verify_t8(), W.decode_t1()
+    assert bench.kernel_name(v4, "verify", sms) == "gdn_recurrent_staged_kernel"  # bf16, T=4: 8 bytes per row elt
+    assert bench.kernel_name(v4, "commit", sms) == "gdn_commit_kernel"
+    assert bench.kernel_name(v8, "verify", sms) == "gdn_recurrent_kernel"  # T * 2 bytes > 8
+    r4 = W.verify_t4_replay()
+    assert bench.kernel_name(r4, "verify", sms) == "gdn_verify_chunked_kernel"  # no cache, bf16 pool, T <= 8
+    assert bench.kernel_name(r4, "commit_replay", sms) == "gdn_verify_chunked_kernel"
+    assert bench.kernel_name(d1, "decode", sms) in ("gdn_recurrent_staged_kernel", "gdn_recurrent_kernel")
+    assert bench.kernel_name(W.tiny(), "verify", sms) == "gdn_recurrent_kernel"  # a handful of CTAs: never staged
+
+
 def test_rank_workloads_differ_only_in_seed():
     w = W.verify_t4()
     w1 = bench.rank_workload(w, 1)

@@ -13,8 +13,8 @@ import torch
 import gated_deltanet_linear_mtp_gb300 as gdn
 import gdn_workloads as W
 import oracle
-from gpu_util import (Dev, assert_f32_close, canary, check_o, check_state, dev, host, is_canary, run_decode,
-                      run_verify, storage_to_f64)
+from gpu_util import (Dev, assert_bf16_stored_close, assert_f32_close, canary, check_o, check_state, dev, host,
+                      is_canary, run_decode, run_verify, storage_to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -201,6 +201,11 @@ def test_sweep_point(w):
 
 
 # ---- edge cases: several row tiles, ragged tails, every DK, dtype mixes -----------------------------
+def verify_is_chunked(w) -> bool:
+    """Verify without intermediate states on a bf16 pool with T <= 8 runs the chunked tensor-core kernel."""
+    return w.state_dtype == "bf16" and w.T <= 8
+
+
 def small(name, B=3, T=3, HK=2, HV=4, DK=64, DV=40, num_slots=7, qkv="bf16", state="bf16", out="bf16",
           seed=0, scale=1.0, pad=0.0):
     return W.Workload(name, B=B, T=T, HK=HK, HV=HV, DK=DK, DV=DV, num_slots=num_slots, qkv_dtype=qkv,
@@ -241,10 +246,13 @@ def test_edge_verify(w):
     o, cache = run_verify(w, t, cache=True)
     torch.cuda.synchronize()
     compare_verify(w, x, host(o), host(cache))
-    # the same call without the cache gives the same o, bit for bit
     o2, _ = run_verify(w, t, cache=False)
-    assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o.view(torch.int32),
-                       o2.view(torch.int16) if o2.dtype == torch.bfloat16 else o2.view(torch.int32))
+    if verify_is_chunked(w):  # without the cache a bf16 pool with T <= 8 takes the chunked form: same tolerance
+        torch.cuda.synchronize()
+        compare_verify(w, x, host(o2), None)
+    else:  # the same kernel without the cache gives the same o, bit for bit
+        assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o.view(torch.int32),
+                           o2.view(torch.int16) if o2.dtype == torch.bfloat16 else o2.view(torch.int32))
 
 
 @pytest.mark.parametrize("w", [e for e in EDGE if e.name in ("dk16_dv200_ragged", "dk128_dv100_ragged_T16",
@@ -396,15 +404,109 @@ def test_side_stream_and_graph_replay():
         check_commit(w, xr, host(pool0), host(t["pool"]), c_eager)
 
 
-# ---- replay commit: the same pool bits as the cached commit, without caching ----------------------------
+# ---- verify without intermediate states: the chunked tensor-core form for bf16 pools --------------------
+NOCACHE = [small(f"nocache_dk{dk}_dv{dv}_T{T}_{qkv}", B=5, T=T, HK=2, HV=4, DK=dk, DV=dv, num_slots=9, qkv=qkv,
+                 out=out, pad=0.2)
+           for dk, dv, T, qkv, out in [(128, 128, 4, "bf16", "bf16"), (128, 200, 8, "bf16", "f32"),
+                                       (128, 100, 1, "bf16", "bf16"), (64, 64, 3, "f32", "f32"),
+                                       (256, 72, 5, "bf16", "bf16"), (32, 40, 2, "bf16", "bf16"),
+                                       (16, 16, 7, "f32", "bf16"), (128, 128, 16, "bf16", "bf16")]]
+# several items per CTA, key heads shared by 4 value heads, several row blocks per head, padded lanes
+NOCACHE += [small("nocache_persistent_dk128_dv300_T4", B=64, T=4, HK=2, HV=8, DK=128, DV=300, num_slots=80,
+                  pad=0.25),
+            small("nocache_persistent_dk64_dv64_T6", B=96, T=6, HK=4, HV=16, DK=64, DV=64, num_slots=100, pad=0.1)]
+
+
+@pytest.mark.parametrize("w", NOCACHE + [W.verify_t4_replay()], ids=lambda w: w.name)
+def test_verify_without_cache(w):
+    x = w.arrays()
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, _ = run_verify(w, t, cache=False, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    oh = host(o)
+    idx = x["indices"]
+    act = np.flatnonzero(idx >= 0)
+    lanes = act if len(act) <= 24 else np.sort(np.random.default_rng(4).choice(act, 24, replace=False))
+    compare_verify(w, x, oh, None, lanes=np.concatenate([lanes, np.flatnonzero(idx < 0)]))
+    # and the states it read are untouched
+    assert np.array_equal(host(t["pool"]), x["pool"])
+
+
+def test_chunked_bad_indices_set_error_bits():
+    w = small("bad_chunked", B=6, T=4, DK=128, DV=160, num_slots=8)
+    x = w.arrays()
+    x["indices"][:] = [0, -1, 8, -2, 3, 5]         # 8 and -2 are out of range
+    x["accept_len"][:] = [1, 1, 1, 1, 0, w.T + 1]  # lane 4: no-op; lane 5: out of range
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, _ = run_verify(w, t, cache=False, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.ERRBIT_INDEX
+    oh = host(o)
+    for b in (1, 2, 3):
+        assert is_canary(oh[b]).all()
+    compare_verify(w, x, oh, None, lanes=[0, 4, 5])
+    err.zero_()
+    pool = t["pool"].clone()
+    run_replay(w, t, pool, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.ERRBIT_INDEX | gdn.ERRBIT_ACCEPT_LEN
+    after = host(pool)
+    keep = [s for s in range(8) if s != 0]
+    assert np.array_equal(after[keep], x["pool"][keep])  # lanes 4 (L=0) and 5 (L>T) left slots 3, 5 alone
+    xs = take_lanes(x, [0])
+    ref = x["pool"].copy()
+    assert oracle.default().commit_replay(oracle.dims_of(w), xs, ref, xs["accept_len"]) == 0
+    check_state(w, after[0], ref[0], "replayed slot 0")
+
+
+def test_chunked_verify_and_replay_in_a_graph():
+    """The chunked kernels' per-call host set-up (tensor map, grid) captured once and replayed."""
+    w = small("graph_chunked", B=24, T=4, HK=2, HV=8, DK=128, DV=128, num_slots=40, pad=0.1)
+    x = w.arrays()
+    t = Dev(x)
+    pool0 = t["pool"].clone()
+    o = canary((w.B, w.T, w.HV, w.DV), w.out_dtype)
+    run_verify(w, t, cache=False, o=o)
+    run_replay(w, t, t["pool"], t["accept_len"])
+    torch.cuda.synchronize()
+    o_eager, p_eager = host(o), host(t["pool"])
+    compare_verify(w, x, o_eager, None)
+    g = torch.cuda.CUDAGraph()
+    t["pool"].copy_(pool0)
+    with torch.cuda.graph(g):
+        run_verify(w, t, cache=False, o=o)
+        run_replay(w, t, t["pool"], t["accept_len"])
+    for _ in range(3):
+        o.copy_(canary(o.shape, w.out_dtype))
+        t["pool"].copy_(pool0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host(o), o_eager) and np.array_equal(host(t["pool"]), p_eager)
+
+
+# ---- replay commit: the pool state of the cached commit, without caching ------------------------------
 def run_replay(w, t: Dev, pool, accept_len, err=None):
     gdn.gdn_commit_replay(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], pool, t["indices"],
                           accept_len, err, scale=w.scale, l2_eps=w.l2_eps)
 
 
-REPLAY = [W.tiny(), W.verify_t4(), W.verify_t8()] + [e for e in EDGE if e.name in (
-    "dk16_dv200_ragged", "dk32_dv33_f32state", "dk128_dv100_ragged_T16", "dk256_dv24_ragged", "hv_8x_hk",
-    "padded_half", "scale_half_f32out", "staged_dk128_dv100_T2", "staged_padded")]
+def assert_replay_matches_copy(w, rep, copy, what):
+    """Token-by-token replay: the cached commit's bits.  Chunked replay (bf16 pool, T <= 8): within 1 bf16 ulp
+    (+1e-4 max) of them and almost all bits equal, since both round an fp32 value of the same state to bf16."""
+    if verify_is_chunked(w):
+        assert_bf16_stored_close(rep, copy, what, min_exact=0.97)
+    else:
+        assert np.array_equal(rep, copy), what
+
+
+REPLAY = [W.tiny(), W.verify_t4(), W.verify_t8(), W.verify_t4_replay(), W.verify_t8_replay()] + [
+    e for e in EDGE if e.name in (
+        "dk16_dv200_ragged", "dk32_dv33_f32state", "dk128_dv100_ragged_T16", "dk256_dv24_ragged", "hv_8x_hk",
+        "padded_half", "scale_half_f32out", "staged_dk128_dv100_T2", "staged_padded", "dk128_dv128_T1",
+        "dk256_dv64_bf16")] + [w for w in NOCACHE if w.T <= 8]
 
 
 @pytest.mark.parametrize("w", REPLAY, ids=lambda w: w.name)
@@ -420,7 +522,7 @@ def test_commit_replay_equals_cached_commit(w):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     rep = host(pool_rep)
-    assert np.array_equal(rep, host(pool_copy)), "replay commit differs from the cached commit"
+    assert_replay_matches_copy(w, rep, host(pool_copy), "replay commit vs the cached commit")
     # and against the oracle's replay, on sampled lanes
     idx = x["indices"]
     act = np.flatnonzero(idx >= 0)
@@ -450,7 +552,7 @@ def test_commit_replay_accept_lengths():
     _, cache = run_verify(w, t, cache=True)
     ch = host(cache)
     for b, L in ((3, 2), (4, w.T)):
-        assert np.array_equal(ph[x["indices"][b]], ch[b, L - 1])
+        assert_replay_matches_copy(w, ph[x["indices"][b]], ch[b, L - 1], f"lane {b}, accept_len {L}")
 
 
 # ---- degenerate cases of the method and maximum sizes ------------------------------------------------------
@@ -488,6 +590,16 @@ def test_degenerate_cases(kind, state):
     if kind == "orthonormal" and state == "f32":
         v = storage_to_f64(x["v"])
         assert np.abs(storage_to_f64(oh) - v).max() <= 1e-5 * np.abs(v).max() + 1e-6
+    if verify_is_chunked(w):  # the chunked forms of verify and of the replay commit on the same inputs
+        o2, _ = run_verify(w, t, cache=False)
+        pool = t["pool"].clone()
+        run_replay(w, t, pool, t["accept_len"])
+        torch.cuda.synchronize()
+        assert np.all(np.isfinite(storage_to_f64(host(o2))))
+        compare_verify(w, x, host(o2), None)
+        ref = x["pool"].copy()
+        assert oracle.default().commit_replay(oracle.dims_of(w), x, ref, x["accept_len"]) == 0
+        check_state(w, host(pool), ref, "replayed pool")
 
 
 def test_maximum_batch():
