@@ -62,7 +62,6 @@ struct ChunkPlan {
         return !kCommit && (uint32_t)kChunkRows * p_stride(T) * 4 <= STAGE_BYTES;
     }
     __host__ __device__ static uint32_t b_off() { return NS * STAGE_BYTES; }
-    __host__ __device__ static uint32_t qk_off(int T) { return b_off() + (uint32_t)b_rows(T) * ROW_BYTES; }
     // replay commit: the coefficient tile A2 = [c hi | c lo | c hi | 0] (bf16, rows padded by 16 bytes)
     __host__ __device__ static int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
     __host__ __device__ static uint32_t a2_stride(int T) { return (uint32_t)a2_cols(T) * 2 + 16; }
@@ -71,14 +70,9 @@ struct ChunkPlan {
         const uint32_t pw = 32u * p_stride(T) * 4, aw = 32u * a2_stride(T);
         return pw > aw ? pw : aw;
     }
-    // fp32 normalised vectors: q_0..q_{T-1}, k_0..k_{T-1} (the replay commit keeps the k rows only, and once
-    // the Gram matrix is formed lays P and A2 over them)
-    __host__ __device__ static uint32_t p_off(int T) { return kCommit ? qk_off(T) : qk_off(T) + 2u * T * DK * 4; }
+    __host__ __device__ static uint32_t p_off(int T) { return b_off() + (uint32_t)b_rows(T) * ROW_BYTES; }
     __host__ __device__ static uint32_t s_off(int T) {
-        if (kCommit) {
-            const uint32_t qk = (uint32_t)T * DK * 4, pa = 4u * warp_region(T);
-            return qk_off(T) + (qk > pa ? qk : pa);
-        }
+        if (kCommit) return p_off(T) + 4u * warp_region(T);
         return p_off(T) + (p_in_stage(T) ? 0u : (uint32_t)kChunkRows * p_stride(T) * 4);
     }
     // NS mbarriers, then per stage the pool slot (-1: nothing loaded) and the token count of its item
@@ -299,8 +293,6 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
     const uint32_t ctl = base + CS::ctl_off(T);  // mbarrier of stage s at ctl + 8 s
     int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(T) + NS * 8);
     int* st_len = st_slot + NS;
-    // [2T][DK]: q_0..q_{T-1}, k_0..k_{T-1}; in the replay commit the region starts at k_0
-    float* qkn = reinterpret_cast<float*>(sm + CS::qk_off(T)) - (kCommit ? T * DK : 0);
     unsigned char* Bs = sm + CS::b_off();  // rows: k hi (T) | k lo (T) | q hi (T) | q lo (T) | zeros
     float* gs = reinterpret_cast<float*>(sm + CS::s_off(T));
     float* bs = gs + T;
@@ -423,7 +415,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
         if (it + 1 < end) load_regs(npos, !(npos.b == b && npos.h / R == hk), nxt);
 
         if (active && !reuse) {
-            // token prologue: normalise q and k (fp32 copies for the Gram matrices; bf16 hi + lo rows of B)
+            // token prologue: normalise q and k into bf16 hi + lo rows of B
 #pragma unroll
             for (int pass = 0; pass < IR::NPASS; ++pass) {
                 if (j0 + pass * VPASS >= 2 * T) break;
@@ -443,9 +435,6 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                         f[2 * e] = x[e].x * rn;
                         f[2 * e + 1] = x[e].y * rn;
                     }
-                    float* dst = qkn + j * DK + 8 * vc;
-                    *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -478,29 +467,45 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
             issue_ahead();
         }
 
-        if (active && !reuse) {
-            // Gram matrices (kh.kh, and kh.qh in verify mode): 8 lanes per dot product, 4 per warp pass
-            const int ndots = kCommit ? T * T : 2 * T * T;
-            for (int d0 = warp * 4; d0 < ndots; d0 += 16) {
-                const int idx = d0 + (lane >> 3);
-                const int g8 = lane & 7;
-                float acc = 0.f;
-                if (idx < ndots) {
-                    const int which = idx / (T * T), st2 = idx - which * T * T;
-                    const int s = st2 / T, t = st2 - s * T;
-                    const float* xs = qkn + (T + s) * DK;                  // kh_s
-                    const float* ys = qkn + (which == 0 ? T + t : t) * DK;  // kh_t or qh_t
-                    for (int e = 4 * g8; e < DK; e += 32) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(xs + e);
-                        const float4 b4 = *reinterpret_cast<const float4*>(ys + e);
-                        acc = fmaf(a4.x, b4.x, fmaf(a4.y, b4.y, fmaf(a4.z, b4.z, fmaf(a4.w, b4.w, acc))));
-                    }
-                }
+        if (active && !reuse && warp == 1) {
+            // Gram matrices kh.kh (and kh.qh in verify mode) on the tensor cores, from the hi + lo rows of B:
+            // A rows 0..7 address kh_0..kh_7 and rows 8..15 kl_0..kl_7, B columns 8 nb .. 8 nb + 7 address
+            // block nb of B (kh, kl, qh, ql); rows past T point at row 0 and their products are dropped.  The
+            // four products of a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.
+            constexpr int NB = kCommit ? 2 : 4;
+            const int m = lane & 15;
+            const int arow = m < 8 ? (m < T ? m : 0) : (m - 8 < T ? T + m - 8 : 0);
+            const uint32_t a_addr = base + CS::b_off() + (uint32_t)arow * CS::ROW_BYTES + (lane >> 4) * 16;
+            uint32_t b_addr[NB];
 #pragma unroll
-                for (int m = 1; m < 8; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-                if (g8 == 0 && idx < ndots) {
-                    const int which = idx / (T * T);
-                    (which == 0 ? KK : KQ)[idx - which * T * T] = acc;
+            for (int nb = 0; nb < NB; ++nb) {
+                const int jr = lane & 7;
+                const int brow = jr < T ? nb * T + jr : 0;
+                b_addr[nb] = base + CS::b_off() + (uint32_t)brow * CS::ROW_BYTES + ((lane >> 3) & 1) * 16;
+            }
+            float g[NB][4];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) g[nb][c] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(a_addr + ks * 32, a0, a1, a2, a3);
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    uint32_t b0, b1;
+                    ldsm_x2(b_addr[nb] + ks * 32, b0, b1);
+                    mma_bf16_16816(g[nb], a0, a1, a2, a3, b0, b1);
+                }
+            }
+            const int s_ = lane >> 2;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t_ = 2 * (lane & 3) + e;
+                if (s_ < T && t_ < T) {
+                    KK[s_ * T + t_] = (g[0][e] + g[1][e]) + (g[0][2 + e] + g[1][2 + e]);
+                    if (!kCommit) KQ[s_ * T + t_] = (g[2 % NB][e] + g[3 % NB][e]) + (g[2 % NB][2 + e] + g[3 % NB][2 + e]);
                 }
             }
         }
@@ -691,7 +696,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                 if (CS::p_in_stage(T)) fence_proxy_async_smem();  // generic writes, then a TMA load refills it
             }
         }
-        __syncthreads();  // the stage, B, qkn, P and the gates are free for the next item
+        __syncthreads();  // the stage, B, P and the gates are free for the next item
         if (it + 1 < end) cur = nxt;
         pos = npos;
     }
