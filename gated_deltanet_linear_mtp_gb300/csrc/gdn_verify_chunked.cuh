@@ -61,6 +61,8 @@ struct ChunkPlan {
     __host__ __device__ static bool p_in_stage(int T) {
         return !kCommit && (uint32_t)kChunkRows * p_stride(T) * 4 <= STAGE_BYTES;
     }
+    // verify: better still, each warp's P over its own 32 rows of the stage's first box (no CTA barrier)
+    __host__ __device__ static bool p_in_warp_rows(int T) { return !kCommit && (uint32_t)p_stride(T) * 4 <= SWZ; }
     __host__ __device__ static uint32_t b_off() { return NS * STAGE_BYTES; }
     // replay commit: the coefficient tile A2 = [c hi | c lo | c hi | 0] (bf16, rows padded by 16 bytes)
     __host__ __device__ static int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
@@ -263,7 +265,7 @@ struct ItemPos {
 };
 
 template <int DK, typename InT, bool kCommit, int NS>
-__global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const RecurrentParams p,
+__global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(const RecurrentParams p,
                                                                           const __grid_constant__ CUtensorMap tmap,
                                                                           int n_items, int per_cta) {
     using CS = ChunkPlan<DK, kCommit, NS>;
@@ -282,8 +284,10 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
     const int beg = blockIdx.x * per_cta;
     const int end = min(n_items, beg + per_cta);
     if (beg >= end) return;
-    constexpr int GATE_T0 = ROWS - 32;  // the last warp computes the gates: its lanes have no q/k work in
-                                        // the replay commit, and the least in verify
+    // roles besides the shared work: warp 1 forms the Gram matrices, thread PT of warp 2 issues the TMA
+    // loads and stores (and alone waits on its bulk groups), warp 3 computes the gates
+    constexpr int PT = 64;
+    constexpr int GATE_T0 = ROWS - 32;
 
     extern __shared__ unsigned char ch_smem[];
     const uint32_t raw_base = smem_u32(ch_smem);
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
     ItemPos pos = item_pos(beg);  // the current item
     ItemPos ipos = pos;           // thread 0: the next item to issue, with its slot and token count
     int islot = 0, ilen = 0;
-    if (tid == 0) {
+    if (tid == PT) {
         for (int s = 0; s < NS; ++s) mbar_init(ctl + 8 * s, 1);
         fence_mbar_init();
         islot = p.indices[ipos.b];
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
         const int row0 = rb * ROWS;
         const int nrows = min(ROWS, p.DV - row0);
         const bool refill = it + NS - 1 < end;
-        auto issue_ahead = [&] {  // thread 0: item it + NS - 1, then look up the slot of the one after it
+        auto issue_ahead = [&] {  // thread PT: item it + NS - 1, then look up the slot of the one after it
             issue(ipos, islot, ilen, (i + NS - 1) % NS);
             ipos.next(NRB, p.HV);
             if (it + NS < end) {
@@ -403,7 +407,6 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                 ilen = kCommit ? p.steps[ipos.b] : T;
             }
         };
-        if (!kCommit && refill && tid == 0) issue_ahead();
         const int slot = st_slot[st];
         const int L = st_len[st];
         const bool active = slot >= 0;
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
 #pragma unroll
                 for (int m = 1; m < LPV; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
                 if (j < 2 * T) {
-                    const float rn = 1.f / sqrtf(ss + p.l2_eps);
+                    const float rn = rsqrtf(ss + p.l2_eps);
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -456,15 +459,16 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                 *reinterpret_cast<uint4*>(Bs + r * CS::ROW_BYTES + 16 * c) = make_uint4(0, 0, 0, 0);
             }
         }
+        __syncthreads();
+        // the refill of the stage the last item used (the replay commit first waits for its store to have read
+        // it) and the gates (needed only after the tile's wait) go in parallel with the Gram matrices
+        if (refill && tid == PT) {
+            if (kCommit) bulk_wait_read_all();
+            issue_ahead();
+        }
         if (active && tid >= GATE_T0 && tid - GATE_T0 < T) {
             gs[tid - GATE_T0] = gate(cur.A_log, to_f32(cur.a), cur.dt_bias);
             bs[tid - GATE_T0] = sigmoid(to_f32(cur.b));
-        }
-        __syncthreads();
-        // the replay commit refills here: the stage it reuses was stored from at the end of the last item
-        if (kCommit && refill && tid == 0) {
-            bulk_wait_read_all();
-            issue_ahead();
         }
 
         if (active && !reuse && warp == 1) {
@@ -516,7 +520,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
             phase ^= 1u << st;
         }
         if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
+            if (tid == PT) {
                 if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
                 // drain every tile still in flight (this one and the ones issued ahead) before leaving
                 mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
@@ -532,11 +536,13 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
         if (active) {
             const uint32_t stage = base + st * CS::STAGE_BYTES;
             const int ra_row = warp * 32 + (lane & 15);  // the row this lane addresses in ldmatrix / stmatrix
-            float* P = CS::p_in_stage(T) ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES)
-                                         : reinterpret_cast<float*>(sm + CS::p_off(T));
+            float* P = CS::p_in_warp_rows(T) ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES + warp * 32 * CS::SWZ)
+                       : CS::p_in_stage(T)   ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES)
+                                             : reinterpret_cast<float*>(sm + CS::p_off(T));
             // this warp's 32 rows of P
-            float* Pw = kCommit ? reinterpret_cast<float*>(sm + CS::p_off(T) + warp * CS::warp_region(T))
-                                : P + warp * 32 * CS::p_stride(T);
+            float* Pw = kCommit                  ? reinterpret_cast<float*>(sm + CS::p_off(T) + warp * CS::warp_region(T))
+                        : CS::p_in_warp_rows(T) ? P
+                                                : P + warp * 32 * CS::p_stride(T);
             // P = S_0 [kh hi | kh lo | qh hi | qh lo]^T on the tensor cores: warp w, rows [32w, 32w + 32)
             {
                 const int NT8 = CS::b_rows(T) / 8;
@@ -568,7 +574,10 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                         }
                     }
                 }
-                if (CS::p_in_stage(T)) __syncthreads();  // every warp's A reads are done before P covers the stage
+                if (CS::p_in_warp_rows(T))
+                    __syncwarp();  // the warp's A reads are done before P covers its rows
+                else if (CS::p_in_stage(T))
+                    __syncthreads();  // every warp's A reads are done before P covers the stage
                 const int ps = CS::p_stride(T), ncol = CS::ncols(T);
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
@@ -671,7 +680,7 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                 }
                 fence_proxy_async_smem();  // the stmatrix writes above, then the TMA store reads them
                 __syncthreads();
-                if (tid == 0) {
+                if (tid == PT) {
 #pragma unroll
                     for (int j = 0; j < CS::NBOX; ++j)
                         tma_store_3d(&tmap, j * CS::BOX_COLS, row0, slot * p.HV + h, stage + j * CS::BOX_BYTES);
@@ -693,14 +702,15 @@ __global__ void __launch_bounds__(kChunkThreads) gdn_verify_chunked_kernel(const
                 case 7: row_recurrence<7>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
                 default: row_recurrence<8>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
                 }
-                if (CS::p_in_stage(T)) fence_proxy_async_smem();  // generic writes, then a TMA load refills it
+                if (CS::p_in_warp_rows(T) || CS::p_in_stage(T))
+                    fence_proxy_async_smem();  // generic writes, then a TMA load refills the stage
             }
         }
         __syncthreads();  // the stage, B, P and the gates are free for the next item
         if (it + 1 < end) cur = nxt;
         pos = npos;
     }
-    if (kCommit && tid == 0) bulk_wait_all();
+    if (kCommit && tid == PT) bulk_wait_all();
 }
 
 // ---- host side ------------------------------------------------------------------------------------------------
