@@ -287,38 +287,129 @@ class Step:
         self.cache = (torch.empty((w.B, w.T, w.HV, w.DV, w.DK), dtype=td[w.state_dtype], device=device)
                       if w.cache else None)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
-        # pinned host copies of the per-step inputs (end-to-end leg)
-        self.step_keys = ["q", "k", "v", "a", "b", "indices"] + (["accept_len"] if w.commit else [])
-        self.h_in = {k: self.d[k].cpu().pin_memory() for k in self.step_keys}
-        self.h_out = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
-        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.h_in.values())
-        self.d2h_bytes = self.o.numel() * self.o.element_size()
+        self._init_e2e(x, device)
 
-    def recurrent(self):
-        d, w = self.d, self.w
+    def _init_e2e(self, x, device):
+        """End-to-end leg: each step's inputs packed in one pinned host buffer (one copy in), o copied back;
+        two device slots of inputs and outputs so that a step's copies overlap its neighbours' compute.
+        The steps rotate over disjoint sets of pool slots (same padding positions), so consecutive steps
+        touch different states."""
+        torch, w = self.torch, self.w
+        self.step_keys = ["q", "k", "v", "a", "b", "indices"] + (["accept_len"] if w.commit else [])
+        host = {k: self.d[k].cpu() for k in self.step_keys}
+        self.layout, off = {}, 0
+        for k in self.step_keys:
+            nb = host[k].numel() * host[k].element_size()
+            self.layout[k] = (off, nb, host[k].dtype, tuple(host[k].shape))
+            off = (off + nb + 255) // 256 * 256
+        self.packed_bytes = off
+        idx = x["indices"]
+        act = np.flatnonzero(idx >= 0)
+        used = set(idx[act].tolist())
+        free = np.random.default_rng([w.seed, 99]).permutation([s for s in range(w.num_slots) if s not in used])
+        nsets = 1 + (min(3, len(free) // len(act)) if len(act) else 0)
+        self.h_sets = []
+        for j in range(nsets):
+            buf = torch.empty(self.packed_bytes, dtype=torch.uint8).pin_memory()
+            for k in self.step_keys:
+                o, nb, dt, shape = self.layout[k]
+                src = host[k]
+                if k == "indices" and j > 0:
+                    src = src.clone()
+                    src[torch.from_numpy(act)] = torch.from_numpy(free[(j - 1) * len(act):j * len(act)].astype(np.int32))
+                buf[o:o + nb].copy_(src.reshape(-1).view(torch.uint8))
+            self.h_sets.append(buf)
+        self.dev_slots = [torch.empty(self.packed_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        self.slot_views = []
+        for buf in self.dev_slots:
+            v = dict(self.d)
+            for k in self.step_keys:
+                o, nb, dt, shape = self.layout[k]
+                v[k] = buf[o:o + nb].view(dt).view(shape)
+            self.slot_views.append(v)
+        self.o_slots = [torch.empty_like(self.o) for _ in range(2)]
+        self.h_out = [torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory() for _ in range(2)]
+        self.h2d_bytes = sum(self.layout[k][1] for k in self.step_keys)
+        self.d2h_bytes = self.o.numel() * self.o.element_size()
+        self.e2e_sets = nsets
+
+    def recurrent(self, d=None, o=None):
+        d, w, o = d or self.d, self.w, self.o if o is None else o
         if w.mode == "decode":
             self.gdn.gdn_decode(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
-                                d["indices"], self.o, self.err, scale=w.scale, l2_eps=w.l2_eps)
+                                d["indices"], o, self.err, scale=w.scale, l2_eps=w.l2_eps)
         else:
             self.gdn.gdn_mtp_verify(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
-                                    d["indices"], self.o, self.cache, self.err, scale=w.scale, l2_eps=w.l2_eps)
+                                    d["indices"], o, self.cache, self.err, scale=w.scale, l2_eps=w.l2_eps)
 
-    def commit(self):
+    def commit(self, d=None):
         if not self.w.commit:
             return
-        d, w = self.d, self.w
+        d, w = d or self.d, self.w
         if w.commit_mode == "replay":
             self.gdn.gdn_commit_replay(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
                                        d["indices"], d["accept_len"], self.err, scale=w.scale, l2_eps=w.l2_eps)
         else:
             self.gdn.gdn_commit(d["pool"], d["indices"], self.cache, d["accept_len"], self.err)
 
-    def upload(self):
-        for k in self.step_keys:
-            self.d[k].copy_(self.h_in[k], non_blocking=True)
+    E2E_GRAPH_STEPS = 32
 
-    def download(self):
-        self.h_out.copy_(self.o, non_blocking=True)
+    def run_e2e(self, K: int, warmup: int, comp) -> float:
+        """Pipelined steps through the public calls, captured once as a CUDA graph of E2E_GRAPH_STEPS steps and
+        replayed; returns the device time per step (ms), from before the first copy in to after the last copy
+        out.  Step i: copy in (H2D stream) -> verify/decode + commit (compute stream) -> copy o out (D2H
+        stream); step i+1's copy in runs during step i's compute."""
+        torch = self.torch
+        G = self.E2E_GRAPH_STEPS
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        down = [torch.cuda.Event() for _ in range(2)]
+
+        def steps(cs):
+            h2d.wait_stream(cs)
+            d2h.wait_stream(cs)
+            for i in range(G):
+                s = i % 2
+                if i >= 2:
+                    h2d.wait_event(done[s])  # step i-2 has finished reading this input slot
+                with torch.cuda.stream(h2d):
+                    self.dev_slots[s].copy_(self.h_sets[i % len(self.h_sets)], non_blocking=True)
+                    up[s].record(h2d)
+                cs.wait_event(up[s])
+                if i >= 2:
+                    cs.wait_event(down[s])  # step i-2's o has been copied out of this output slot
+                with torch.cuda.stream(cs):
+                    self.recurrent(self.slot_views[s], self.o_slots[s])
+                    self.commit(self.slot_views[s])
+                    done[s].record(cs)
+                d2h.wait_event(done[s])
+                with torch.cuda.stream(d2h):
+                    self.h_out[s].copy_(self.o_slots[s], non_blocking=True)
+                    down[s].record(d2h)
+            cs.wait_stream(h2d)
+            cs.wait_stream(d2h)
+
+        for _ in range(max(1, warmup // G)):  # eager warm-up
+            steps(comp)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(comp)
+        with torch.cuda.graph(graph, stream=cap):
+            steps(cap)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, -(-K // G))
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(comp):
+            t0.record(comp)
+            for _ in range(reps):
+                graph.replay()
+            t1.record(comp)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (reps * G)
 
     @property
     def launches_per_step(self) -> int:
@@ -348,18 +439,14 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
         flush_w.fill_(1.0)
         flush_r.sum()
 
-    def one(ev=None, e2e=False):
+    def one(ev=None):
         flush_l2()
         if ev is not None:
             ev[0].record(stream)
-        if e2e:
-            st.upload()
         st.recurrent()
         if ev is not None:
             ev[1].record(stream)
         st.commit()
-        if e2e:
-            st.download()
         if ev is not None:
             ev[2].record(stream)
 
@@ -390,17 +477,13 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     tokens_rank = st.A * wr.T * K
     tokens_all = sum_over_ranks(tokens_rank, dist, device)
 
-    # end-to-end: host->device inputs, the two calls, device->host o, every step
-    for _ in range(max(1, args.warmup)):
-        one(e2e=True)
-    torch.cuda.synchronize()
-    evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # end-to-end: every step's inputs copied in from pinned host memory and its o copied back, pipelined
     if dist is not None:
         dist.barrier()
-    for i in range(K):
-        one(evs2[i], e2e=True)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in evs2), dist, device)
+    e2e_ms_step = max_over_ranks(st.run_e2e(K, args.warmup, stream), dist, device)
+    tokens_step_all = sum_over_ranks(st.A * wr.T, dist, device)
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error word {st.err.item()} after the end-to-end leg")
 
     peak, peak_src = hbm_peak()
     rb = recurrent_bytes(wr, st.A)
@@ -442,6 +525,10 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
             "l2": "flushed before every step outside its CUDA events (256 MiB write, then 256 MiB read: clean lines)",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
             "timing": "CUDA events per step on the launch stream, summed; max over ranks",
+            "e2e": (f"pipelined: each step's inputs copied in from pinned host memory (one packed copy) and its o "
+                    f"copied back, on H2D / D2H streams beside the compute stream, {st.E2E_GRAPH_STEPS} steps captured "
+                    f"as one CUDA graph and replayed; no L2 flush: steps rotate over {st.e2e_sets} disjoint sets of "
+                    f"pool slots"),
         },
         "verify_steps_per_s": K * world / (total_ms * 1e-3),
         "hbm_gbs_step": step_bytes * world * K / (total_ms * 1e-3) / 1e9,
@@ -458,8 +545,8 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
             "traffic": recorded_traffic(dom["role"], w.name),
         },
         "kernels": kernels,
-        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": st.h2d_bytes,
-                "d2h_bytes_per_step": st.d2h_bytes},
+        "e2e": {"value": tokens_step_all / (e2e_ms_step * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": st.h2d_bytes,
+                "d2h_bytes_per_step": st.d2h_bytes, "ms_per_step": e2e_ms_step},
         "gpu_launches": st.launches_per_step * K,
         "clocks": clocks,
         "device": props.name,

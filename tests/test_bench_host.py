@@ -49,6 +49,38 @@ def test_kernel_names_follow_the_launcher_rule():
     assert bench.kernel_name(W.tiny(), "verify", sms) == "gdn_recurrent_kernel"  # a handful of CTAs: never staged
 
 
+def test_e2e_inputs_pack_and_rotate_over_disjoint_slots(monkeypatch):
+    """The end-to-end leg's packed host buffers hold each step input byte for byte (16-byte aligned views), and
+    its slot sets keep the padding positions and are pairwise disjoint."""
+    import numpy as np
+    import torch
+
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)  # no GPU here
+    w = W.Workload("e2e_small", B=6, T=3, HK=2, HV=4, DK=32, DV=24, num_slots=40, qkv_dtype="bf16",
+                   state_dtype="bf16", out_dtype="bf16", mode="verify", cache=False, commit=True, seed=5,
+                   pad_fraction=0.34, commit_mode="replay")
+    st = bench.Step(w, torch.device("cpu"))
+    assert st.e2e_sets == 4
+    idx0 = st.d["indices"].numpy()
+    seen = []
+    for j, hb in enumerate(st.h_sets):
+        st.dev_slots[1].copy_(hb)
+        v = st.slot_views[1]
+        for k in st.step_keys:
+            assert v[k].data_ptr() % 16 == 0 and v[k].shape == st.d[k].shape and v[k].dtype == st.d[k].dtype
+            if k != "indices":
+                assert torch.equal(v[k].view(torch.uint8), st.d[k].view(torch.uint8)), k
+        idx = v["indices"].numpy()
+        assert np.array_equal(idx < 0, idx0 < 0)
+        if j == 0:
+            assert np.array_equal(idx, idx0)
+        act = set(idx[idx >= 0].tolist())
+        assert len(act) == int((idx >= 0).sum()) and max(act) < w.num_slots
+        assert all(not (act & other) for other in seen)
+        seen.append(act)
+    assert st.h2d_bytes == sum(st.d[k].numel() * st.d[k].element_size() for k in st.step_keys)
+
+
 def test_rank_workloads_differ_only_in_seed():
     w = W.verify_t4()
     w1 = bench.rank_workload(w, 1)
