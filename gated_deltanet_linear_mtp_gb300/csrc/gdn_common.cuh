@@ -314,4 +314,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  : "memory");
 }
 
+// Position of a work item of the persistent kernels: items are numbered row block fastest, then value head,
+// then lane, and a CTA walks a contiguous range of them without dividing.
+struct ItemPos {
+    int b, h, rb;  // lane, value head, row block
+    __device__ __forceinline__ static ItemPos of(int it, int NRB, int HV) {
+        ItemPos q;
+        q.rb = it % NRB;
+        const int bh = it / NRB;
+        q.h = bh % HV;
+        q.b = bh / HV;
+        return q;
+    }
+    __device__ __forceinline__ void next(int NRB, int HV) {
+        if (++rb == NRB) {
+            rb = 0;
+            if (++h == HV) {
+                h = 0;
+                ++b;
+            }
+        }
+    }
+};
+
 }  // namespace gdn

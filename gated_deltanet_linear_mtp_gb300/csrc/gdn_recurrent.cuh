@@ -38,7 +38,8 @@ struct TokenPrologue {
     __host__ __device__ static size_t smem_floats(int T) { return (size_t)2 * T * DK + (size_t)T * ROWS + 3 * (size_t)T; }
 
     uint4 qraw[QK::NC], kraw[QK::NC], vpre;
-    float a_raw, b_raw, A_h, dt_h;
+    InT a_raw, b_raw;  // converted in finish(): a conversion here would wait for the load
+    float A_h, dt_h;
     int t0, tj, hk;
 
     __device__ __forceinline__ void prefetch(const RecurrentParams& p, int b, int h, int row0, int tid) {
@@ -47,7 +48,7 @@ struct TokenPrologue {
         tj = lane % LPT;
         t0 = warp * TPW + lane / LPT;
         hk = h / (p.HV / p.HK);
-        a_raw = b_raw = 0.f;
+        a_raw = b_raw = InT(0.f);
 #pragma unroll
         for (int c = 0; c < QK::NC; ++c) qraw[c] = kraw[c] = make_uint4(0, 0, 0, 0);
         if (t0 < T) {
@@ -56,8 +57,8 @@ struct TokenPrologue {
             QK::load_global(static_cast<const InT*>(p.k) + off, kraw);
             if (tj == 0) {
                 const int64_t ab = ((int64_t)b * T + t0) * p.HV + h;
-                a_raw = to_f32(static_cast<const InT*>(p.a)[ab]);
-                b_raw = to_f32(static_cast<const InT*>(p.b)[ab]);
+                a_raw = static_cast<const InT*>(p.a)[ab];
+                b_raw = static_cast<const InT*>(p.b)[ab];
             }
         }
         A_h = p.A_log[h];
@@ -85,8 +86,8 @@ struct TokenPrologue {
                     QK::load_global(static_cast<const InT*>(p.k) + off, kraw);
                     if (tj == 0) {
                         const int64_t ab = ((int64_t)b * T + t) * p.HV + h;
-                        a_raw = to_f32(static_cast<const InT*>(p.a)[ab]);
-                        b_raw = to_f32(static_cast<const InT*>(p.b)[ab]);
+                        a_raw = static_cast<const InT*>(p.a)[ab];
+                        b_raw = static_cast<const InT*>(p.b)[ab];
                     }
                 }
             }
@@ -120,8 +121,8 @@ struct TokenPrologue {
                     make_float4(k2[2].x * rk, k2[2].y * rk, k2[3].x * rk, k2[3].y * rk);
                 if (tj == 0) {
                     kqs[t] = sqk * rq * rk;
-                    gs[t] = gate(A_h, a_raw, dt_h);
-                    bs[t] = sigmoid(b_raw);
+                    gs[t] = gate(A_h, to_f32(a_raw), dt_h);
+                    bs[t] = sigmoid(to_f32(b_raw));
                 }
             }
         }

@@ -24,12 +24,16 @@ namespace gdn {
 constexpr int kStagedMaxTokenBytes = 8;  // T * sizeof(state element) at or below which staging pays
 constexpr int kStagedMinCtasPerSm = 2;
 
-template <typename StT, int DK>
-bool use_staged(const RecurrentParams& p, int B) {
-    if (p.T * (int)sizeof(StT) > kStagedMaxTokenBytes) return false;
+inline int sm_count() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return false;
+        return 0;
+    return sms;
+}
+
+template <typename StT, int DK>
+bool use_staged(const RecurrentParams& p, int B, int sms) {
+    if (sms <= 0 || p.T * (int)sizeof(StT) > kStagedMaxTokenBytes) return false;
     const int64_t ctas = (int64_t)B * p.HV * ((p.DV + Staged<DK, StT>::ROWS - 1) / Staged<DK, StT>::ROWS);
     return ctas >= (int64_t)kStagedMinCtasPerSm * sms;
 }
@@ -43,7 +47,8 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
         if ((verify_only || replay_commit) && p.T <= kChunkMaxT)
             return replay_commit ? launch_chunked<DK, InT, true>(p, B, s) : launch_chunked<DK, InT, false>(p, B, s);
     }
-    if (use_staged<StT, DK>(p, B)) {
+    const int sms = sm_count();
+    if (use_staged<StT, DK>(p, B, sms)) {
         using ST = Staged<DK, StT>;
         const uint32_t smem = ST::smem_bytes(p.T);
         auto kernel = gdn_recurrent_staged_kernel<DK, InT, StT>;

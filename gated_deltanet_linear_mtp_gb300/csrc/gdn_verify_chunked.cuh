@@ -251,18 +251,6 @@ struct ItemRegs {
     float A_log, dt_bias;
 };
 
-struct ItemPos {
-    int b, h, rb;  // lane, value head, 128-row block
-    __device__ __forceinline__ void next(int NRB, int HV) {
-        if (++rb == NRB) {
-            rb = 0;
-            if (++h == HV) {
-                h = 0;
-                ++b;
-            }
-        }
-    }
-};
 
 template <int DK, typename InT, bool kCommit, int NS>
 __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(const RecurrentParams p,
@@ -303,15 +291,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     float* KK = bs + T;      // [T][T] kh_s . kh_t
     float* KQ = KK + T * T;  // [T][T] kh_s . qh_t
 
-    auto item_pos = [&](int it) {
-        ItemPos q;
-        q.rb = it % NRB;
-        const int bh = it / NRB;
-        q.h = bh % p.HV;
-        q.b = bh / p.HV;
-        return q;
-    };
-    // thread 0: start the tile of the item at `ip` (pool slot and token count loaded one issue earlier) into
+    // thread PT: start the tile of the item at `ip` (pool slot and token count loaded one issue earlier) into
     // stage s
     auto issue = [&](const ItemPos& ip, int slot, int L, int s) {
         const int h = ip.h, rb = ip.rb;
@@ -369,7 +349,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         }
     };
 
-    ItemPos pos = item_pos(beg);  // the current item
+    ItemPos pos = ItemPos::of(beg, NRB, p.HV);  // the current item
     ItemPos ipos = pos;           // thread 0: the next item to issue, with its slot and token count
     int islot = 0, ilen = 0;
     if (tid == PT) {
