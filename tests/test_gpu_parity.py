@@ -618,3 +618,30 @@ def test_maximum_batch():
     pool_before = host(t["pool"])
     gdn.gdn_commit(t["pool"], t["indices"], cache, t["accept_len"])
     check_commit(w, x, pool_before, host(t["pool"]), ch)
+
+
+def test_maximum_batch_chunked():
+    """B = 65535 lanes through the chunked verify and replay commit: thousands of items per persistent CTA;
+    sampled lanes against the oracle, every other slot untouched."""
+    w = W.Workload("max_B_chunked", B=65535, T=3, HK=1, HV=2, DK=32, DV=40, num_slots=65535, qkv_dtype="bf16",
+                   state_dtype="bf16", out_dtype="bf16", mode="verify", cache=False, commit=True, seed=12,
+                   pool_std=0.1, pad_fraction=0.05, commit_mode="replay")
+    x = w.arrays()
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, _ = run_verify(w, t, cache=False, err=err)
+    run_replay(w, t, t["pool"], t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lanes = np.sort(np.random.default_rng(5).choice(w.B, 48, replace=False))
+    lanes = np.unique(np.concatenate([lanes, [0, w.B - 1]]))
+    compare_verify(w, x, host(o), None, lanes=lanes)
+    after = host(t["pool"])
+    xs = take_lanes(x, lanes)
+    ref = x["pool"].copy()
+    assert oracle.default().commit_replay(oracle.dims_of(w), xs, ref, xs["accept_len"]) == 0
+    sl = xs["indices"][(xs["indices"] >= 0) & (xs["accept_len"] > 0)]
+    check_state(w, after[sl], ref[sl], "replayed slots")
+    idx = x["indices"]
+    untouched = np.setdiff1d(np.arange(w.num_slots), idx[(idx >= 0) & (x["accept_len"] > 0)])
+    assert np.array_equal(after[untouched], x["pool"][untouched])
