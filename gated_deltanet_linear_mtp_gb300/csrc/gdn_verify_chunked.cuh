@@ -56,7 +56,10 @@ struct ChunkPlan {
     // columns of P: kh hi, kh lo (and qh hi, qh lo in verify mode), T each
     __host__ __device__ static int ncols(int T) { return kCommit ? 2 * T : 4 * T; }
     __host__ __device__ static int b_rows(int T) { return ((ncols(T) + 7) / 8) * 8; }  // whole n8 tiles
-    __host__ __device__ static int p_stride(int T) { return ncols(T) + 1; }            // fp32 row stride of P
+    // fp32 row stride of P: verify with even T pads rows to 4T + 4 floats, so that a thread reads its row with
+    // float4 loads (T + 1 odd keeps 8 consecutive rows on 8 distinct 16-byte bank groups); otherwise + 1
+    __host__ __device__ static int p_stride(int T) { return (!kCommit && T % 2 == 0) ? 4 * T + 4 : ncols(T) + 1; }
+    __host__ __device__ static int gram_stride(int T) { return (T + 3) & ~3; }  // padded row of the Gram matrices
     // verify: P goes over the item's own stage once every warp has finished its MMAs, when it fits
     __host__ __device__ static bool p_in_stage(int T) {
         return !kCommit && (uint32_t)kChunkRows * p_stride(T) * 4 <= STAGE_BYTES;
@@ -77,8 +80,10 @@ struct ChunkPlan {
         if (kCommit) return p_off(T) + 4u * warp_region(T);
         return p_off(T) + (p_in_stage(T) ? 0u : (uint32_t)kChunkRows * p_stride(T) * 4);
     }
+    // g, beta (T each), then the Gram matrices, transposed (row t holds kh_s . kh_t, kh_s . qh_t over s)
+    __host__ __device__ static uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
     // NS mbarriers, then per stage the pool slot (-1: nothing loaded) and the token count of its item
-    __host__ __device__ static uint32_t ctl_off(int T) { return (s_off(T) + (2u * T + 2u * T * T) * 4 + 15u) & ~15u; }
+    __host__ __device__ static uint32_t ctl_off(int T) { return gram_off(T) + 2u * T * gram_stride(T) * 4; }
     __host__ __device__ static uint32_t bytes(int T) { return ctl_off(T) + NS * 16 + 1024; }  // + alignment slack
 };
 
@@ -153,28 +158,56 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// T floats from shared memory: float4 loads when the address is 16-byte aligned by construction
+template <int N, bool kVec>
+__device__ __forceinline__ void load_row(const float* src, float (&dst)[N]) {
+    if constexpr (kVec && N % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < N / 4; ++j) {
+            const float4 f = reinterpret_cast<const float4*>(src)[j];
+            dst[4 * j] = f.x;
+            dst[4 * j + 1] = f.y;
+            dst[4 * j + 2] = f.z;
+            dst[4 * j + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) dst[j] = src[j];
+    }
+}
+
 // One row's T x T recurrence (T fixed at compile time, so delta stays in registers).  Pr: the row of P,
-// [S_0 kh hi | S_0 kh lo | S_0 qh hi | S_0 qh lo]; v: the row's v per token.
+// [S_0 kh hi | S_0 kh lo | S_0 qh hi | S_0 qh lo]; v: the row's v per token; KKt, KQt: the transposed Gram
+// matrices, rows of TP = gram_stride(T) floats.
 template <int T>
 __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const float* Pr, const float (&v)[kChunkMaxT],
-                                               const float* gs, const float* bs, const float* KK, const float* KQ,
+                                               const float* gs, const float* bs, const float* KKt, const float* KQt,
                                                bool live, int64_t o0, int64_t tok_out) {
+    constexpr int TP = (T + 3) & ~3;
+    float pr[4 * T];
+    load_row<4 * T, T % 2 == 0>(Pr, pr);
+    float g[T], be[T];
+    load_row<T, false>(gs, g);
+    load_row<T, false>(bs, be);
     float delta[T];
     float gamma = 1.f;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        gamma *= gs[t];
-        float u = gamma * (Pr[t] + Pr[T + t]);            // gamma_t S_0 kh_t
-        float o = gamma * (Pr[2 * T + t] + Pr[3 * T + t]);  // gamma_t S_0 qh_t
+        float kk[TP], kq[TP];  // kh_s . kh_t and kh_s . qh_t over s
+        load_row<TP, true>(KKt + t * TP, kk);
+        load_row<TP, true>(KQt + t * TP, kq);
+        gamma *= g[t];
+        float u = gamma * (pr[t] + pr[T + t]);            // gamma_t S_0 kh_t
+        float o = gamma * (pr[2 * T + t] + pr[3 * T + t]);  // gamma_t S_0 qh_t
         float G = 1.f;
 #pragma unroll
         for (int s = t - 1; s >= 0; --s) {  // G(s, t) = g_{s+1} ... g_t
-            G *= gs[s + 1];
-            u = fmaf(G * KK[s * T + t], delta[s], u);
-            o = fmaf(G * KQ[s * T + t], delta[s], o);
+            G *= g[s + 1];
+            u = fmaf(G * kk[s], delta[s], u);
+            o = fmaf(G * kq[s], delta[s], o);
         }
-        delta[t] = bs[t] * (v[t] - u);
-        o = fmaf(KQ[t * T + t], delta[t], o);
+        delta[t] = be[t] * (v[t] - u);
+        o = fmaf(kq[t], delta[t], o);
         if (live) {
             const float ov = p.scale * o;
             if (p.out_bf16)
@@ -190,7 +223,8 @@ __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const f
 // lo = c - hi rounded), to be multiplied by [kh hi; kh hi; kh lo].
 template <int T>
 __device__ __forceinline__ void row_coefficients(const float* Pr, const float (&v)[kChunkMaxT], const float* gs,
-                                                 const float* bs, const float* KK, int L, unsigned char* a2row) {
+                                                 const float* bs, const float* KKt, int L, unsigned char* a2row) {
+    constexpr int TP = (T + 3) & ~3;
     float delta[T];
     float gamma = 1.f;
     float a[T];
@@ -206,7 +240,7 @@ __device__ __forceinline__ void row_coefficients(const float* Pr, const float (&
 #pragma unroll
             for (int s = t - 1; s >= 0; --s) {
                 G *= gs[s + 1];
-                u = fmaf(G * KK[s * T + t], delta[s], u);
+                u = fmaf(G * KKt[t * TP + s], delta[s], u);
             }
             delta[t] = bs[t] * (v[t] - u);
         }
@@ -288,8 +322,9 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     unsigned char* Bs = sm + CS::b_off();  // rows: k hi (T) | k lo (T) | q hi (T) | q lo (T) | zeros
     float* gs = reinterpret_cast<float*>(sm + CS::s_off(T));
     float* bs = gs + T;
-    float* KK = bs + T;      // [T][T] kh_s . kh_t
-    float* KQ = KK + T * T;  // [T][T] kh_s . qh_t
+    const int TP = CS::gram_stride(T);
+    float* KK = reinterpret_cast<float*>(sm + CS::gram_off(T));  // transposed: KK[t * TP + s] = kh_s . kh_t
+    float* KQ = KK + T * TP;                                     // transposed: KQ[t * TP + s] = kh_s . qh_t
 
     // thread PT: start the tile of the item at `ip` (pool slot and token count loaded one issue earlier) into
     // stage s
@@ -451,12 +486,14 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
             bs[tid - GATE_T0] = sigmoid(to_f32(cur.b));
         }
 
-        if (active && !reuse && warp == 1) {
+        if (active && !reuse && (warp == 1 || (!kCommit && warp == 0))) {
             // Gram matrices kh.kh (and kh.qh in verify mode) on the tensor cores, from the hi + lo rows of B:
             // A rows 0..7 address kh_0..kh_7 and rows 8..15 kl_0..kl_7, B columns 8 nb .. 8 nb + 7 address
             // block nb of B (kh, kl, qh, ql); rows past T point at row 0 and their products are dropped.  The
-            // four products of a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.
-            constexpr int NB = kCommit ? 2 : 4;
+            // four products of a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.  Warp 1 forms kh.kh from
+            // blocks 0, 1; in verify, warp 0 forms kh.qh from blocks 2, 3 at the same time.
+            constexpr int NB = 2;
+            const int nb0 = warp == 1 ? 0 : 2;
             const int m = lane & 15;
             const int arow = m < 8 ? (m < T ? m : 0) : (m - 8 < T ? T + m - 8 : 0);
             const uint32_t a_addr = base + CS::b_off() + (uint32_t)arow * CS::ROW_BYTES + (lane >> 4) * 16;
@@ -464,7 +501,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
                 const int jr = lane & 7;
-                const int brow = jr < T ? nb * T + jr : 0;
+                const int brow = jr < T ? (nb0 + nb) * T + jr : 0;
                 b_addr[nb] = base + CS::b_off() + (uint32_t)brow * CS::ROW_BYTES + ((lane >> 3) & 1) * 16;
             }
             float g[NB][4];
@@ -487,10 +524,8 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int t_ = 2 * (lane & 3) + e;
-                if (s_ < T && t_ < T) {
-                    KK[s_ * T + t_] = (g[0][e] + g[1][e]) + (g[0][2 + e] + g[1][2 + e]);
-                    if (!kCommit) KQ[s_ * T + t_] = (g[2 % NB][e] + g[3 % NB][e]) + (g[2 % NB][2 + e] + g[3 % NB][2 + e]);
-                }
+                if (s_ < T && t_ < T)
+                    (warp == 1 ? KK : KQ)[t_ * TP + s_] = (g[0][e] + g[1][e]) + (g[0][2 + e] + g[1][2 + e]);
             }
         }
         // the state tile: bounded wait (uniform: every thread takes the same branch)
