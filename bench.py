@@ -53,7 +53,8 @@ def kernel_name(w, role: str, sms: int) -> str:
     p = w.DK // 8
     rpc = (32 // p) * min(p, 4) * 4  # rows per CTA of the token-by-token kernels
     block = rpc * w.DK * st
-    nsub = 1 if block >= 32768 else min(8, 32768 // block)
+    cap = (16 if (st == 4 or w.T >= 4) else 32) * 1024  # state staged per CTA
+    nsub = 1 if block >= cap else min(8, cap // block)
     ctas = w.B * w.HV * -(-w.DV // (nsub * rpc))
     if w.T * st <= 8 and ctas >= 2 * sms:
         return "gdn_recurrent_staged_kernel"

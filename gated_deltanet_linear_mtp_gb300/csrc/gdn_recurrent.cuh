@@ -6,7 +6,7 @@
 //   gdn_recurrent_kernel         one block of rows per CTA; the state comes straight from global memory
 //                                with 16-byte loads into registers.  Many CTAs per SM overlap one CTA's
 //                                prologue with the others' token loops.
-//   gdn_recurrent_staged_kernel  NSUB consecutive blocks per CTA; the CTA's state rows are bulk-copied
+//   gdn_recurrent_staged_kernel  NSUB consecutive blocks per CTA (16 or 32 KiB of state); the CTA's rows are bulk-copied
 //                                (TMA) into shared memory at once, one copy and one mbarrier per block, so
 //                                the bytes in flight per SM are not bounded by registers; the token
 //                                prologue is formed once for all the blocks.  Used where a CTA has little
@@ -277,12 +277,13 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
 // ---- TMA-staged kernel ------------------------------------------------------------------------------------
 constexpr uint32_t kMbarPollLimit = 1u << 22;  // polls of one mbarrier wait before it is declared failed
 
-template <int DK, typename StT>
+template <int DK, typename StT, int KIB>
 struct Staged {
     static constexpr int RPC = Split<DK>::RPC;
     static constexpr int BLOCK_BYTES = RPC * DK * (int)sizeof(StT);
-    // up to 32 KiB of state per CTA, in NSUB blocks of RPC rows
-    static constexpr int NSUB = BLOCK_BYTES >= 32768 ? 1 : (32768 / BLOCK_BYTES > 8 ? 8 : 32768 / BLOCK_BYTES);
+    // up to KIB KiB of state per CTA, in NSUB blocks of RPC rows
+    static constexpr int CAP = KIB * 1024;
+    static constexpr int NSUB = BLOCK_BYTES >= CAP ? 1 : (CAP / BLOCK_BYTES > 8 ? 8 : CAP / BLOCK_BYTES);
     static constexpr int ROWS = NSUB * RPC;
     __host__ __device__ static uint32_t prologue_offset() { return (uint32_t)NSUB * BLOCK_BYTES; }
     __host__ __device__ static uint32_t mbar_offset(int T) {
@@ -294,12 +295,12 @@ struct Staged {
     __host__ __device__ static uint32_t smem_bytes(int T) { return mbar_offset(T) + 8u * NSUB; }
 };
 
-template <int DK, typename InT, typename StT>
+template <int DK, typename InT, typename StT, int KIB>
 __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM)
     gdn_recurrent_staged_kernel(const RecurrentParams p) {
     using SP = Split<DK>;
     using SL = Slice8<StT>;
-    using ST = Staged<DK, StT>;
+    using ST = Staged<DK, StT, KIB>;
     constexpr int RL = SP::RL;
     constexpr int RPC = SP::RPC;
     constexpr int NT = SP::THREADS;

@@ -4,10 +4,12 @@
 //   gdn_recurrent_staged_kernel, grid = (ceil(DV / (NSUB * RPC)), HV, B), when a CTA has little work per
 //       state byte (T * sizeof(state) <= 8: bf16 with T <= 4, fp32 with T <= 2), so that the state's load
 //       latency dominates and bulk copies keep more bytes in flight, and when that grid still gives every
-//       SM at least two CTAs;
+//       SM at least two CTAs.  A CTA stages 16 KiB of state for an fp32 pool or T >= 4, 32 KiB otherwise;
 //   gdn_recurrent_kernel, grid = (ceil(DV / RPC), HV, B), otherwise.
-// The rule follows a B x T x state-dtype sweep of both kernels on the GB300 (the staged kernel was 15-40%
-// faster inside the rule, and 4-80% slower outside it).  Both run Split<DK>::THREADS threads per CTA.
+// The rules follow B x T x state-dtype sweeps on the GB300: the staged kernel was 15-40% faster than the
+// direct one inside its rule and 4-80% slower outside it; 16 KiB stages were up to 15% faster than 32 KiB
+// for fp32 pools and bf16 with T = 4, and up to 12% slower for bf16 with T <= 2.  Both kernels run
+// Split<DK>::THREADS threads per CTA.
 // On a bf16 pool with T <= 8, a verify that stores neither intermediate states nor a write-back, and a
 // replay commit, run the persistent chunked tensor-core kernel (gdn_verify_chunked.cuh) instead, one CTA
 // per resident slot of the GPU.
@@ -31,11 +33,29 @@ inline int sm_count() {
     return sms;
 }
 
-template <typename StT, int DK>
+template <typename StT, int DK, int KIB>
 bool use_staged(const RecurrentParams& p, int B, int sms) {
+    using ST = Staged<DK, StT, KIB>;
     if (sms <= 0 || p.T * (int)sizeof(StT) > kStagedMaxTokenBytes) return false;
-    const int64_t ctas = (int64_t)B * p.HV * ((p.DV + Staged<DK, StT>::ROWS - 1) / Staged<DK, StT>::ROWS);
+    const int64_t ctas = (int64_t)B * p.HV * ((p.DV + ST::ROWS - 1) / ST::ROWS);
     return ctas >= (int64_t)kStagedMinCtasPerSm * sms;
+}
+
+// the staged kernel with KIB KiB per CTA, if the rule above picks it; false: use the direct kernel
+template <typename InT, typename StT, int DK, int KIB>
+bool launch_staged(const RecurrentParams& p, int B, int sms, cudaStream_t s, cudaError_t& err) {
+    if (!use_staged<StT, DK, KIB>(p, B, sms)) return false;
+    using ST = Staged<DK, StT, KIB>;
+    const uint32_t smem = ST::smem_bytes(p.T);
+    auto kernel = gdn_recurrent_staged_kernel<DK, InT, StT, KIB>;
+    if (smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return true;
+    }
+    const dim3 grid((p.DV + ST::ROWS - 1) / ST::ROWS, p.HV, B);
+    kernel<<<grid, Split<DK>::THREADS, smem, s>>>(p);
+    err = cudaGetLastError();
+    return true;
 }
 
 template <typename InT, typename StT, int DK>
@@ -48,18 +68,10 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
             return replay_commit ? launch_chunked<DK, InT, true>(p, B, s) : launch_chunked<DK, InT, false>(p, B, s);
     }
     const int sms = sm_count();
-    if (use_staged<StT, DK>(p, B, sms)) {
-        using ST = Staged<DK, StT>;
-        const uint32_t smem = ST::smem_bytes(p.T);
-        auto kernel = gdn_recurrent_staged_kernel<DK, InT, StT>;
-        if (smem > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
-        const dim3 grid((p.DV + ST::ROWS - 1) / ST::ROWS, p.HV, B);
-        kernel<<<grid, NT, smem, s>>>(p);
-        return cudaGetLastError();
-    }
+    cudaError_t err = cudaSuccess;
+    const bool small_stage = std::is_same<StT, float>::value || p.T >= 4;
+    if (small_stage ? launch_staged<InT, StT, DK, 16>(p, B, sms, s, err) : launch_staged<InT, StT, DK, 32>(p, B, sms, s, err))
+        return err;
     constexpr int RPC = Split<DK>::RPC;
     const size_t smem = direct_smem_bytes<DK>(p.T);
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
