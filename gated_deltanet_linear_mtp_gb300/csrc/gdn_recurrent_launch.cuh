@@ -4,7 +4,8 @@
 //   gdn_recurrent_staged_kernel, grid = (ceil(DV / (NSUB * RPC)), HV, B), when a CTA has little work per
 //       state byte (T * sizeof(state) <= 8: bf16 with T <= 4, fp32 with T <= 2), so that the state's load
 //       latency dominates and bulk copies keep more bytes in flight, and when that grid still gives every
-//       SM at least two CTAs.  A CTA stages 16 KiB of state for an fp32 pool or T >= 4, 32 KiB otherwise;
+//       SM at least two CTAs.  A CTA stages 16 KiB of state for an fp32 pool or T >= 4, 32 KiB otherwise
+//       (and the fp32 16 KiB kernel at DK = 128 budgets registers for 7 CTAs per SM instead of 6);
 //   gdn_recurrent_kernel, grid = (ceil(DV / RPC), HV, B), otherwise.
 // The rules follow B x T x state-dtype sweeps on the GB300: the staged kernel was 15-40% faster than the
 // direct one inside its rule and 4-80% slower outside it; 16 KiB stages were up to 15% faster than 32 KiB
@@ -69,9 +70,13 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     }
     const int sms = sm_count();
     cudaError_t err = cudaSuccess;
-    const bool small_stage = std::is_same<StT, float>::value || p.T >= 4;
-    if (small_stage ? launch_staged<InT, StT, DK, 16>(p, B, sms, s, err) : launch_staged<InT, StT, DK, 32>(p, B, sms, s, err))
-        return err;
+    bool staged;
+    if constexpr (std::is_same<StT, float>::value)
+        staged = launch_staged<InT, StT, DK, 16>(p, B, sms, s, err);
+    else
+        staged = p.T >= 4 ? launch_staged<InT, StT, DK, 16>(p, B, sms, s, err)
+                          : launch_staged<InT, StT, DK, 32>(p, B, sms, s, err);
+    if (staged) return err;
     constexpr int RPC = Split<DK>::RPC;
     const size_t smem = direct_smem_bytes<DK>(p.T);
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
