@@ -47,7 +47,9 @@ def kernel_name(w, role: str, sms: int) -> str:
     (gdn_recurrent_launch.cuh) restated for the report."""
     if role == "commit":
         return "gdn_commit_kernel"
-    if w.state_dtype == "bf16" and w.T <= 8 and ((role == "verify" and not w.cache) or role == "commit_replay"):
+    in_range = w.num_slots * w.HV <= 2**31 - 1 and w.B * w.HV * -(-w.DV // 128) <= 2**31 - 1
+    if (w.state_dtype == "bf16" and w.T <= 8 and in_range
+            and ((role == "verify" and not w.cache) or role == "commit_replay")):
         return "gdn_verify_chunked_kernel"
     st = 2 if w.state_dtype == "bf16" else 4
     p = w.DK // 8

@@ -17,6 +17,8 @@
 #pragma once
 
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <type_traits>
 
 #include "gdn_recurrent.cuh"
@@ -65,7 +67,11 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     if constexpr (std::is_same<StT, __nv_bfloat16>::value) {
         const bool verify_only = p.cache == nullptr && p.pool_out == nullptr && p.steps == nullptr;
         const bool replay_commit = p.cache == nullptr && p.pool_out != nullptr && p.steps != nullptr && p.o == nullptr;
-        if ((verify_only || replay_commit) && p.T <= kChunkMaxT)
+        // the chunked kernel addresses num_slots * HV heads with a signed 32-bit TMA coordinate and counts its
+        // items in int; beyond either range, the token-by-token kernels below serve the call
+        const uint64_t heads = (uint64_t)p.num_slots * (uint64_t)p.HV;
+        const uint64_t items = (uint64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
+        if ((verify_only || replay_commit) && p.T <= kChunkMaxT && heads <= INT32_MAX && items <= INT32_MAX)
             return replay_commit ? launch_chunked<DK, InT, true>(p, B, s) : launch_chunked<DK, InT, false>(p, B, s);
     }
     const int sms = sm_count();
