@@ -7,7 +7,7 @@ verify step of sglang PR #23273 "[GDN] Enable FlashInfer MTP verify on SM100+ (B
 L2 (129 MB) is flushed between steps, outside each step's CUDA events: a 256 MiB write, then a 256 MiB read
 so that the lines left in L2 are clean.
 
-    python bench.py [--steps K] [--warmup W] [--workload verify4|verify8|decode|sweep] [--impl reference]
+    python bench.py [--steps K] [--warmup W] [--workload verify4|verify8|decode|...|sweep|sweep_replay] [--impl reference]
 
 Prints one JSON line (``--workload sweep``: one per point).  ``value`` = verified tokens/s (A x T per step,
 A = non-padded lanes, summed over ranks, divided by the slowest rank's device time).
@@ -429,7 +429,7 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     device = torch.device("cuda", local_rank)
     dist = init_dist(world, "nccl")
     wr = rank_workload(w, rank)
-    st = Step(wr, device, _POOL_CACHE if args.workload == "sweep" else None)
+    st = Step(wr, device, _POOL_CACHE if args.workload.startswith("sweep") else None)
     props = torch.cuda.get_device_properties(device)
     nflush = max(256 << 20, 2 * props.L2_cache_size) // 4
     flush_w = torch.empty(nflush, dtype=torch.float32, device=device)
@@ -666,7 +666,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep"], default="verify4")
+    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay"], default="verify4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
@@ -676,6 +676,8 @@ def main(argv=None):
     rank, world, local_rank = dist_env()
     if args.workload == "sweep":
         pts = W.sweep()
+    elif args.workload == "sweep_replay":
+        pts = W.sweep_replay()
     else:
         pts = [W.NAMED[args.workload]()]
     for w in pts:

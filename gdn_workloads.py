@@ -224,5 +224,19 @@ def sweep() -> List[Workload]:
     return pts
 
 
+def sweep_replay() -> List[Workload]:
+    """The verify + replay-commit path (no intermediate states) over B x T, bf16 state, pool 1024 slots:
+    point i draws its inputs from seed 3000 + i; all points share the bf16 pool of the sweep (seed 2001)."""
+    pts = []
+    i = 0
+    for T in (2, 4, 8):
+        for B in (16, 64, 128, 256):
+            pts.append(Workload(f"sweep_replay_B{B}_T{T}", B=B, T=T, HK=16, HV=32, DK=128, DV=128, num_slots=1024,
+                                qkv_dtype=BF16, state_dtype=BF16, out_dtype=BF16, mode="verify", cache=False,
+                                commit=True, seed=3000 + i, pool_seed=2001, commit_mode="replay"))
+            i += 1
+    return pts
+
+
 NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8,
          "verify4_replay": verify_t4_replay, "verify8_replay": verify_t8_replay}
