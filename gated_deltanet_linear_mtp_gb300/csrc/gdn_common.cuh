@@ -318,19 +318,26 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // then lane, and a CTA walks a contiguous range of them without dividing.
 struct ItemPos {
     int b, h, rb;  // lane, value head, row block
-    __device__ __forceinline__ static ItemPos of(int it, int NRB, int HV) {
+    int hk, hr;    // key head h / R and h % R, R = value heads per key head
+    __device__ __forceinline__ static ItemPos of(int it, int NRB, int HV, int R) {
         ItemPos q;
         q.rb = it % NRB;
         const int bh = it / NRB;
         q.h = bh % HV;
         q.b = bh / HV;
+        q.hk = q.h / R;
+        q.hr = q.h - q.hk * R;
         return q;
     }
-    __device__ __forceinline__ void next(int NRB, int HV) {
+    __device__ __forceinline__ void next(int NRB, int HV, int R) {
         if (++rb == NRB) {
             rb = 0;
+            if (++hr == R) {
+                hr = 0;
+                ++hk;
+            }
             if (++h == HV) {
-                h = 0;
+                h = hk = hr = 0;
                 ++b;
             }
         }

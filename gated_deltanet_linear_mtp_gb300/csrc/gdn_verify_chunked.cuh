@@ -60,12 +60,19 @@ struct ChunkPlan {
     // float4 loads (T + 1 odd keeps 8 consecutive rows on 8 distinct 16-byte bank groups); otherwise + 1
     __host__ __device__ static int p_stride(int T) { return (!kCommit && T % 2 == 0) ? 4 * T + 4 : ncols(T) + 1; }
     __host__ __device__ static int gram_stride(int T) { return (T + 3) & ~3; }  // padded row of the Gram matrices
-    // verify: P goes over the item's own stage once every warp has finished its MMAs, when it fits
-    __host__ __device__ static bool p_in_stage(int T) {
-        return !kCommit && (uint32_t)kChunkRows * p_stride(T) * 4 <= STAGE_BYTES;
+    // Where a warp's 32 rows of P go (verify; the replay commit has a region of its own):
+    //   0  over the warp's own 32 rows of the stage's first box, once its MMAs are done (no CTA barrier);
+    //   1  likewise over its own rows of the first two boxes, 16 P rows in each (rows too long for one box);
+    //   2  over the whole stage, after a CTA barrier (every warp's MMAs done);
+    //   3  a region of its own.
+    __host__ __device__ static int p_mode(int T) {
+        if (kCommit) return 3;
+        const uint32_t row = (uint32_t)p_stride(T) * 4;
+        if (row <= SWZ) return 0;
+        if (NBOX >= 2 && 16u * row <= 32u * SWZ) return 1;
+        if ((uint32_t)kChunkRows * row <= STAGE_BYTES) return 2;
+        return 3;
     }
-    // verify: better still, each warp's P over its own 32 rows of the stage's first box (no CTA barrier)
-    __host__ __device__ static bool p_in_warp_rows(int T) { return !kCommit && (uint32_t)p_stride(T) * 4 <= SWZ; }
     __host__ __device__ static uint32_t b_off() { return NS * STAGE_BYTES; }
     // replay commit: the coefficient tile A2 = [c hi | c lo | c hi | 0] (bf16, rows padded by 16 bytes)
     __host__ __device__ static int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
@@ -78,7 +85,7 @@ struct ChunkPlan {
     __host__ __device__ static uint32_t p_off(int T) { return b_off() + (uint32_t)b_rows(T) * ROW_BYTES; }
     __host__ __device__ static uint32_t s_off(int T) {
         if (kCommit) return p_off(T) + 4u * warp_region(T);
-        return p_off(T) + (p_in_stage(T) ? 0u : (uint32_t)kChunkRows * p_stride(T) * 4);
+        return p_off(T) + (p_mode(T) < 3 ? 0u : (uint32_t)kChunkRows * p_stride(T) * 4);
     }
     // g, beta (T each), then the Gram matrices, transposed (row t holds kh_s . kh_t, kh_s . qh_t over s)
     __host__ __device__ static uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T;
     const int NRB = (p.DV + ROWS - 1) / ROWS;
-    const int R = p.HV / p.HK;
+    const int R = p.HV / p.HK;  // value heads per key head
     const int beg = blockIdx.x * per_cta;
     const int end = min(n_items, beg + per_cta);
     if (beg >= end) return;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
             const int j = j0 + vj0 + ps * VPASS;
 #pragma unroll
             for (int c = 0; c < QK::NC; ++c) r.raw[ps][c] = make_uint4(0, 0, 0, 0);
-            if (need_qk && j < 2 * T) QK::load_global(vec_ptr(ip.b, ip.h / R, j), r.raw[ps]);
+            if (need_qk && j < 2 * T) QK::load_global(vec_ptr(ip.b, ip.hk, j), r.raw[ps]);
         }
         const int row = ip.rb * ROWS + tid;
         const InT* vsrc = static_cast<const InT*>(p.v) + ((int64_t)ip.b * T * p.HV + ip.h) * p.DV + row;
@@ -384,7 +391,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         }
     };
 
-    ItemPos pos = ItemPos::of(beg, NRB, p.HV);  // the current item
+    ItemPos pos = ItemPos::of(beg, NRB, p.HV, R);  // the current item
     ItemPos ipos = pos;           // thread 0: the next item to issue, with its slot and token count
     int islot = 0, ilen = 0;
     if (tid == PT) {
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         ilen = kCommit ? p.steps[ipos.b] : T;
         for (int j = 0; j < NS - 1 && beg + j < end; ++j) {
             issue(ipos, islot, ilen, j);
-            ipos.next(NRB, p.HV);
+            ipos.next(NRB, p.HV, R);
             if (beg + j + 1 < end) {
                 islot = p.indices[ipos.b];
                 ilen = kCommit ? p.steps[ipos.b] : T;
@@ -410,13 +417,13 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     for (int i = 0, it = beg; it < end; ++i, ++it) {
         const int st = i % NS;
         const int b = pos.b, h = pos.h, rb = pos.rb;
-        const int hk = h / R;
+        const int hk = pos.hk;
         const int row0 = rb * ROWS;
         const int nrows = min(ROWS, p.DV - row0);
         const bool refill = it + NS - 1 < end;
         auto issue_ahead = [&] {  // thread PT: item it + NS - 1, then look up the slot of the one after it
             issue(ipos, islot, ilen, (i + NS - 1) % NS);
-            ipos.next(NRB, p.HV);
+            ipos.next(NRB, p.HV, R);
             if (it + NS < end) {
                 islot = p.indices[ipos.b];
                 ilen = kCommit ? p.steps[ipos.b] : T;
@@ -429,8 +436,8 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         prev_b = b;
         prev_hk = hk;
         ItemPos npos = pos;
-        npos.next(NRB, p.HV);
-        if (it + 1 < end) load_regs(npos, !(npos.b == b && npos.h / R == hk), nxt);
+        npos.next(NRB, p.HV, R);
+        if (it + 1 < end) load_regs(npos, !(npos.b == b && npos.hk == hk), nxt);
 
         if (active && !reuse) {
             // token prologue: normalise q and k into bf16 hi + lo rows of B
@@ -551,13 +558,18 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         if (active) {
             const uint32_t stage = base + st * CS::STAGE_BYTES;
             const int ra_row = warp * 32 + (lane & 15);  // the row this lane addresses in ldmatrix / stmatrix
-            float* P = CS::p_in_warp_rows(T) ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES + warp * 32 * CS::SWZ)
-                       : CS::p_in_stage(T)   ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES)
-                                             : reinterpret_cast<float*>(sm + CS::p_off(T));
-            // this warp's 32 rows of P
-            float* Pw = kCommit                  ? reinterpret_cast<float*>(sm + CS::p_off(T) + warp * CS::warp_region(T))
-                        : CS::p_in_warp_rows(T) ? P
-                                                : P + warp * 32 * CS::p_stride(T);
+            // this warp's P rows 0..15 and 16..31 (pbase[m] + r * p_stride, r < 16)
+            float* pbase[2];
+            {
+                const int ps = CS::p_stride(T);
+                unsigned char* own = sm + st * CS::STAGE_BYTES + warp * 32 * CS::SWZ;  // its rows in box 0
+                float* Pw = kCommit              ? reinterpret_cast<float*>(sm + CS::p_off(T) + warp * CS::warp_region(T))
+                            : CS::p_mode(T) <= 1 ? reinterpret_cast<float*>(own)
+                            : CS::p_mode(T) == 2 ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES) + warp * 32 * ps
+                                                 : reinterpret_cast<float*>(sm + CS::p_off(T)) + warp * 32 * ps;
+                pbase[0] = Pw;
+                pbase[1] = CS::p_mode(T) == 1 ? reinterpret_cast<float*>(own + CS::BOX_BYTES) : Pw + 16 * ps;
+            }
             // P = S_0 [kh hi | kh lo | qh hi | qh lo]^T on the tensor cores: warp w, rows [32w, 32w + 32)
             {
                 const int NT8 = CS::b_rows(T) / 8;
@@ -589,32 +601,32 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
                         }
                     }
                 }
-                if (CS::p_in_warp_rows(T))
-                    __syncwarp();  // the warp's A reads are done before P covers its rows
-                else if (CS::p_in_stage(T))
+                if (CS::p_mode(T) == 2)
                     __syncthreads();  // every warp's A reads are done before P covers the stage
+                else
+                    __syncwarp();  // the warp's A reads are done before P covers its rows
                 const int ps = CS::p_stride(T), ncol = CS::ncols(T);
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    const int r = mt * 16 + (lane >> 2);
+                    const int r = lane >> 2;  // row within the m tile; pbase[mt] holds the tile's first row
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt) {
                         const int c = nt * 8 + (lane & 3) * 2;
                         if (nt < NT8) {
                             if (c < ncol) {
-                                Pw[r * ps + c] = acc[mt][nt][0];
-                                Pw[(r + 8) * ps + c] = acc[mt][nt][2];
+                                pbase[mt][r * ps + c] = acc[mt][nt][0];
+                                pbase[mt][(r + 8) * ps + c] = acc[mt][nt][2];
                             }
                             if (c + 1 < ncol) {
-                                Pw[r * ps + c + 1] = acc[mt][nt][1];
-                                Pw[(r + 8) * ps + c + 1] = acc[mt][nt][3];
+                                pbase[mt][r * ps + c + 1] = acc[mt][nt][1];
+                                pbase[mt][(r + 8) * ps + c + 1] = acc[mt][nt][3];
                             }
                         }
                     }
                 }
             }
             __syncwarp();
-            float* Pr = Pw + lane * CS::p_stride(T);
+            float* Pr = pbase[lane >> 4] + (lane & 15) * CS::p_stride(T);
             float vr[kChunkMaxT];
 #pragma unroll
             for (int t = 0; t < kChunkMaxT; ++t) vr[t] = to_f32(cur.v[t]);
@@ -717,7 +729,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
                 case 7: row_recurrence<7>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
                 default: row_recurrence<8>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
                 }
-                if (CS::p_in_warp_rows(T) || CS::p_in_stage(T))
+                if (CS::p_mode(T) <= 2)
                     fence_proxy_async_smem();  // generic writes, then a TMA load refills the stage
             }
         }
