@@ -11,19 +11,20 @@
 // The only per-element work is the contraction S_0 [kh_1..kh_T qh_1..qh_T], a (rows x DK) x (DK x 2T)
 // product: it runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with S_0 exact in
 // bf16 and kh, qh split into bf16 hi + lo parts (4T columns), which keeps about 16 significant bits of
-// kh and qh.  The T x T Gram matrices kh.kh and kh.qh come from the fp32 normalised vectors, and each row's
-// small triangular recurrence runs in fp32 registers, one thread per row.
+// kh and qh.  The T x T Gram matrices kh.kh and kh.qh are formed on the tensor cores from the same hi + lo
+// rows, and each row's small triangular recurrence runs in fp32 registers, one thread per row.
 //
 // Two modes, for bf16 state pools and T <= 8 (the launcher's choice):
 //   verify (kCommit = false)   outputs o only: no intermediate states, no write-back;
 //   replay commit (kCommit)    the first L = steps[b] tokens, no outputs, and the state after them,
 //                              S_L = gamma_L S_0 + sum_{s<L} G(s, L-1) delta_s kh_s^T, written back into the
-//                              slot (kh only: 2T columns, one Gram matrix).
+//                              slot (kh only: 2T columns, one Gram matrix); the rank-L update runs on the
+//                              tensor cores too.
 //
 // Work item = 128 state rows of one (lane, value head); items are numbered row block fastest, then value
 // head, then lane, and each CTA (4 warps, warp w owning rows [32w, 32w + 32)) takes a contiguous range of
-// them.  Thread 0 keeps NS - 1 state tiles in flight ahead of the item being computed: one 3-D TMA tensor
-// load per 64-column box into a 1024-byte aligned stage, rows past DV filled with zeros, 16-byte chunks
+// them.  One thread (PT) keeps NS - 1 state tiles in flight ahead of the item being computed: one 3-D TMA
+// tensor load per 64-column box into a 1024-byte aligned stage, rows past DV filled with zeros, 16-byte chunks
 // swizzled within each 128-byte line so that the ldmatrix reads of the MMA are conflict-free.  q, k, v, a
 // and b of the next item are loaded into registers while the current one is computed, and consecutive
 // items of one key head reuse its normalised q, k and Gram matrices.  The replay commit rewrites the tile
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     };
 
     ItemPos pos = ItemPos::of(beg, NRB, p.HV, R);  // the current item
-    ItemPos ipos = pos;           // thread 0: the next item to issue, with its slot and token count
+    ItemPos ipos = pos;           // thread PT: the next item to issue, with its slot and token count
     int islot = 0, ilen = 0;
     if (tid == PT) {
         for (int s = 0; s < NS; ++s) mbar_init(ctl + 8 * s, 1);
