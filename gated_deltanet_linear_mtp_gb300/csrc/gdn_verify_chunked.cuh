@@ -34,6 +34,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "gdn_common.cuh"
@@ -787,20 +788,21 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     using CS = ChunkPlan<DK, kCommit, NS>;
     auto kernel = gdn_verify_chunked_kernel<DK, InT, kCommit, NS>;
     const uint32_t smem = CS::bytes(p.T);
-    static int attr_bytes = 0;  // dynamic shared memory this instantiation has been opened for
-    if ((int)smem > attr_bytes) {
+    // launch caches shared by every calling thread (a repeated first call only repeats the same queries)
+    static std::atomic<int> attr_bytes{0};  // dynamic shared memory this instantiation has been opened for
+    if ((int)smem > attr_bytes.load(std::memory_order_relaxed)) {
         const int most = (int)CS::bytes(kChunkMaxT);
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e != cudaSuccess) return e;
-        attr_bytes = most;
+        attr_bytes.store(most, std::memory_order_relaxed);
     }
-    static int occ_cache[kChunkMaxT + 1] = {0};
-    int occ = occ_cache[p.T];
+    static std::atomic<int> occ_cache[kChunkMaxT + 1];  // zero-initialised (static storage)
+    int occ = occ_cache[p.T].load(std::memory_order_relaxed);
     if (occ == 0) {
         const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkThreads, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) return cudaErrorInvalidConfiguration;
-        occ_cache[p.T] = occ;
+        occ_cache[p.T].store(occ, std::memory_order_relaxed);
     }
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);

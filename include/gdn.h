@@ -30,9 +30,10 @@
  *     accept_len              [B]                     int32
  *
  * Common rules.
- *   - Every pointer is DEVICE memory owned by the caller.  The library allocates nothing, holds no mutable
- *     global state, never synchronises, and enqueues its work asynchronously on `stream` (0 = legacy
- *     default stream).  Calls are thread-safe.  A call with B == 0 enqueues nothing and returns GDN_OK.
+ *   - Every pointer is DEVICE memory owned by the caller.  The library allocates nothing, keeps no state
+ *     between calls besides launch-configuration caches (atomic, filled on first use), never synchronises,
+ *     and enqueues its work asynchronously on `stream` (0 = legacy default stream).  Calls are thread-safe.
+ *     A call with B == 0 enqueues nothing and returns GDN_OK.
  *   - Alignment: q, k, state_pool and intermediate_states start on 16 bytes; the other arrays on their
  *     element size.  Outputs must not overlap inputs (decode updates state_pool in place by design).
  *   - Errors the host can see are returned as a status before anything is enqueued.  Errors that depend on
