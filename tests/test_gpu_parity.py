@@ -487,6 +487,51 @@ def test_chunked_verify_and_replay_in_a_graph():
         assert np.array_equal(host(o), o_eager) and np.array_equal(host(t["pool"]), p_eager)
 
 
+def test_calls_from_two_host_threads():
+    """Two host threads, each on its own stream, call verify (with and without the cache, i.e. the rank-1 and the
+    chunked kernels) and the replay commit over and over; every result equals the single-threaded one bit for
+    bit."""
+    import threading
+
+    cases = [small("thr_bf16", B=8, T=4, HK=2, HV=4, DK=128, DV=160, num_slots=12),
+             small("thr_f32", B=6, T=3, HK=2, HV=4, DK=64, DV=72, num_slots=10, state="f32", out="f32")]
+    prepared = []
+    for w in cases:
+        x = w.arrays()
+        t = Dev(x)
+        o_c, cache = run_verify(w, t, cache=True)
+        o_n, _ = run_verify(w, t, cache=False)
+        pool = t["pool"].clone()
+        run_replay(w, t, pool, t["accept_len"])
+        torch.cuda.synchronize()
+        prepared.append((w, t, host(o_c), host(cache), host(o_n), host(pool)))
+    failures = []
+
+    def worker(w, t, o_c_ref, c_ref, o_n_ref, pool_ref):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    o_c, cache = run_verify(w, t, cache=True, stream=stream)
+                    o_n, _ = run_verify(w, t, cache=False, stream=stream)
+                    pool = t["pool"].clone()
+                    run_replay(w, t, pool, t["accept_len"])
+                stream.synchronize()
+                for got, ref, what in ((host(o_c), o_c_ref, "o"), (host(cache), c_ref, "cache"),
+                                       (host(o_n), o_n_ref, "o without cache"), (host(pool), pool_ref, "replay")):
+                    if not np.array_equal(got, ref):
+                        failures.append(f"{w.name}: {what} differs")
+        except Exception as e:  # surfaced below
+            failures.append(f"{w.name}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=a) for a in prepared]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not failures, failures
+
+
 # ---- replay commit: the pool state of the cached commit, without caching ------------------------------
 def run_replay(w, t: Dev, pool, accept_len, err=None):
     gdn.gdn_commit_replay(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], pool, t["indices"],
