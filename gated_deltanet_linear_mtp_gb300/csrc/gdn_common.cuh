@@ -314,6 +314,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  : "memory");
 }
 
+// Polls of one mbarrier wait before the wait is declared failed (the kernel then sets GDN_ERRBIT_TIMEOUT and
+// leaves the work it waited for undone).  A test build lowers it, together with GDN_TEST_MISSING_COPY, which
+// leaves one copy unissued so that its wait runs out (tests/test_gpu_timeout.py).
+#ifndef GDN_WAIT_POLLS
+#define GDN_WAIT_POLLS (1u << 22)
+#endif
+
 // Position of a work item of the persistent kernels: items are numbered row block fastest, then value head,
 // then lane, and a CTA walks a contiguous range of them without dividing.
 struct ItemPos {

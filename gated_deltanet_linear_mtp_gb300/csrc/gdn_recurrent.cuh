@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
 }
 
 // ---- TMA-staged kernel ------------------------------------------------------------------------------------
-constexpr uint32_t kMbarPollLimit = 1u << 22;  // polls of one mbarrier wait before it is declared failed
+constexpr uint32_t kMbarPollLimit = GDN_WAIT_POLLS;  // polls of one mbarrier wait before it is declared failed
 
 template <int DK, typename StT, int KIB>
 struct Staged {
@@ -334,7 +334,12 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
     if (tid < NSUB) {
         const int r = row0 + tid * RPC;
         const int nrows = min(RPC, p.DV - r);
-        if (nrows > 0) {
+        bool issue_copy = nrows > 0;
+#ifdef GDN_TEST_MISSING_COPY
+        // test build: block 0 of the first CTA is never copied (and never arrived on), so its wait runs out
+        if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) issue_copy = false;
+#endif
+        if (issue_copy) {
             const uint32_t bytes = (uint32_t)nrows * DK * sizeof(StT);
             mbar_arrive_expect_tx(mbar0 + 8 * tid, bytes);
             bulk_g2s(sbase + (uint32_t)tid * ST::BLOCK_BYTES, static_cast<const StT*>(p.pool_in) + (head_row0 + r) * DK,

@@ -55,6 +55,13 @@
 
 #include <stdint.h>
 
+/* The library exports these functions and nothing else (it is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -100,7 +107,7 @@ typedef struct gdn_dims {
  * stays fp32 between the tokens of one call.  Defines the SM100+ decode path of sglang PR #23273,
  * Summary, with the padding index guard of its Requirements.
  */
-gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+GDN_API gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
                       const void* b, const float* A_log, const float* dt_bias, void* state_pool,
                       const int32_t* state_indices, void* o, int32_t* err_word, gdn_stream_t stream);
 
@@ -113,7 +120,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k, const 
  * outputs.  MTP verify through the pool API (initial_state_indices) of sglang PR #23273, Summary; bf16
  * state, T beyond 4 and intermediate caching from its Requirements (FlashInfer #2679).
  */
-gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+GDN_API gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
                           const void* b, const float* A_log, const float* dt_bias, const void* state_pool,
                           const int32_t* state_indices, void* o, void* intermediate_states,
                           int32_t* err_word, gdn_stream_t stream);
@@ -125,7 +132,7 @@ gdn_status gdn_mtp_verify(const gdn_dims* dims, const void* q, const void* k, co
  * the commit contract in TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), "Moved out of this PR"
  * (the manager's all-layer commit) and its commit message, MTP > Verify (checkpoint-commit contract).
  */
-gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* state_indices,
+GDN_API gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* state_indices,
                       const void* intermediate_states, const int32_t* accept_len, int32_t* err_word,
                       gdn_stream_t stream);
 
@@ -143,19 +150,19 @@ gdn_status gdn_commit(const gdn_dims* dims, void* state_pool, const int32_t* sta
  * of reading each state once more here: the cached replay with in-kernel commit of TensorRT-LLM PR #20937
  * (GB300 Qwen3.8-Flash-Next NVFP4), "MTP > Verify" and "Moved out of this PR".
  */
-gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+GDN_API gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
                              const void* b, const float* A_log, const float* dt_bias, void* state_pool,
                              const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
                              gdn_stream_t stream);
 
 /* Static string naming a status; never NULL. */
-const char* gdn_status_string(gdn_status status);
+GDN_API const char* gdn_status_string(gdn_status status);
 
 /* cudaError_t of the calling thread's last GDN_ERR_CUDA (0 if none). */
-int32_t gdn_last_cuda_error(void);
+GDN_API int32_t gdn_last_cuda_error(void);
 
 /* ABI version of this header: 1. */
-int32_t gdn_abi_version(void);
+GDN_API int32_t gdn_abi_version(void);
 
 #ifdef __cplusplus
 }

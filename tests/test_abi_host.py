@@ -34,6 +34,20 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_library_exports_only_the_declared_functions(L):
+    """Hidden visibility: internal symbols (template statics among them) must not bind across two copies of
+    the library in one process."""
+    import shutil
+    import subprocess
+
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", gbuild.LIB_PATH], capture_output=True, text=True, check=True)
+    names = {line.split()[-1] for line in out.stdout.splitlines() if line.strip()}
+    assert names == set(declared_functions())
+
+
 def test_status_strings_and_version(L):
     for code, name in gdn.STATUS.items():
         assert L.gdn_status_string(code).decode().startswith(name)

@@ -1,0 +1,77 @@
+"""The bounded waits of the copy-fed kernels, made to run out without a fault.
+
+A test build of the library (flags GDN_TEST_MISSING_COPY and a short GDN_WAIT_POLLS) leaves one bulk / TMA
+copy unissued and never arrives on its mbarrier, so the wait for it can only run out.  That is the same path
+a copy that never lands would take: the kernel sets GDN_ERRBIT_TIMEOUT, gives up the work it waited for,
+drains the copies it did issue and ends.  Nothing is left in flight, so the GPU context stays usable: the
+product library then runs a normal call in the same process and matches the oracle."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_mtp_gb300 as gdn
+import gdn_workloads as W
+from gated_deltanet_linear_mtp_gb300 import build as gbuild
+from gpu_util import Dev, host, run_verify
+from test_gpu_parity import compare_verify
+
+pytestmark = pytest.mark.gpu
+
+TEST_BUILD = os.path.join(gbuild.PKG, "_build", "wait_timeout_test")
+
+
+@pytest.fixture(scope="module")
+def timeout_lib():
+    return gbuild.build(["-DGDN_TEST_MISSING_COPY", "-DGDN_WAIT_POLLS=65536u"], out_dir=TEST_BUILD)
+
+
+def workload(name, T, cache, **kw):
+    # lane 0 active (the missing copy belongs to lane 0, head 0, rows 0..); enough CTAs for the staged kernel
+    base = dict(B=8, HK=16, HV=48, DK=128, DV=128, num_slots=10, qkv_dtype="bf16", state_dtype="bf16",
+                out_dtype="bf16", mode="verify", cache=cache, commit=True, seed=21, pool_std=0.1)
+    base.update(kw)
+    return W.Workload(name, T=T, **base)
+
+
+def run_with(lib_path, monkeypatch, fn):
+    monkeypatch.setattr(gdn, "_lib_handle", None)
+    monkeypatch.setattr(gdn, "LIB_PATH", lib_path)
+    try:
+        return fn()
+    finally:
+        monkeypatch.setattr(gdn, "_lib_handle", None)
+        monkeypatch.setattr(gdn, "LIB_PATH", gbuild.LIB_PATH)
+
+
+@pytest.mark.parametrize("case", ["chunked_verify", "chunked_replay", "staged_verify"])
+def test_wait_that_runs_out_sets_the_timeout_bit(timeout_lib, monkeypatch, case):
+    if case == "staged_verify":  # bf16, T = 2, with the cache: the staged (bulk-copy) kernel
+        w = workload("timeout_staged", T=2, cache=True)
+    else:  # bf16, T = 4, no cache: the chunked (TMA) kernel
+        w = workload("timeout_chunked", T=4, cache=False)
+    x = w.arrays()
+    x["indices"][0] = 0 if x["indices"][0] < 0 else x["indices"][0]
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call():
+        if case == "chunked_replay":  # into a copy: the pool itself must stay as the oracle has it
+            pool = t["pool"].clone()
+            gdn.gdn_commit_replay(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], pool,
+                                  t["indices"], t["accept_len"], err, scale=w.scale, l2_eps=w.l2_eps)
+        else:
+            run_verify(w, t, cache=w.cache, err=err)
+        torch.cuda.synchronize()
+
+    run_with(timeout_lib, monkeypatch, call)
+    assert int(err.item()) & gdn.ERRBIT_TIMEOUT, "the wait did not report running out"
+
+    # the context is usable: the product library verifies the same batch correctly afterwards
+    err.zero_()
+    o, cache = run_verify(w, t, cache=w.cache, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lanes = np.flatnonzero(x["indices"] >= 0)[:4]
+    compare_verify(w, x, host(o), host(cache) if cache is not None else None, lanes=lanes)
