@@ -600,6 +600,60 @@ def test_commit_replay_accept_lengths():
         assert_replay_matches_copy(w, ph[x["indices"][b]], ch[b, L - 1], f"lane {b}, accept_len {L}")
 
 
+# ---- seeded random shapes through every call ---------------------------------------------------------------
+def _random_case(i):
+    r = np.random.default_rng([77, i])
+    DK = int(r.choice([16, 32, 64, 128, 256]))
+    HK = int(r.integers(1, 4))
+    HV = HK * int(r.integers(1, 5))
+    T = int(r.choice([1, 2, 3, 4, 5, 7, 8, 12, 16]))
+    B = int(r.integers(1, 12))
+    state = str(r.choice(["bf16", "f32"]))
+    qkv = str(r.choice(["bf16", "f32"]))
+    out = str(r.choice(["bf16", "f32"]))
+    DV = int(r.integers(1, 300))
+    return small(f"random{i}_dk{DK}_dv{DV}_h{HK}x{HV}_T{T}_B{B}_{state}", B=B, T=T, HK=HK, HV=HV, DK=DK, DV=DV,
+                 num_slots=B + int(r.integers(0, 6)), qkv=qkv, state=state, out=out, seed=100 + i,
+                 pad=float(r.choice([0.0, 0.3])))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_shapes_every_call(i):
+    """verify with and without the cache (the rank-1 and, for bf16 T <= 8, the chunked kernels), the copy and
+    the replay commits, and decode, on one seeded random shape, against the oracle."""
+    w = _random_case(i)
+    x = w.arrays()
+    t = Dev(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, cache = run_verify(w, t, cache=True, err=err)
+    o2, _ = run_verify(w, t, cache=False, err=err)
+    pool_rep = t["pool"].clone()
+    run_replay(w, t, pool_rep, t["accept_len"], err)
+    pool_copy = t["pool"].clone()
+    gdn.gdn_commit(pool_copy, t["indices"], cache, t["accept_len"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    compare_verify(w, x, host(o), host(cache))
+    compare_verify(w, x, host(o2), None)
+    check_commit(w, x, x["pool"], host(pool_copy), host(cache))
+    ref = x["pool"].copy()
+    assert oracle.default().commit_replay(oracle.dims_of(w), x, ref, x["accept_len"]) == 0
+    check_state(w, host(pool_rep), ref, "replayed pool")
+    # decode of the same shape (T tokens, written back)
+    wd = w.replace(mode="decode")
+    t_d = Dev(x)
+    od = run_decode(wd, t_d, t_d["pool"], err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    pool_ref = x["pool"].copy()
+    od_ref, _ = oracle.default().decode(oracle.dims_of(wd), x, pool_ref)
+    act = (x["indices"] >= 0)
+    if act.any():
+        check_o(wd, host(od)[act], od_ref[act], "decode o")
+        sl = x["indices"][act]
+        check_state(wd, host(t_d["pool"])[sl], pool_ref[sl], "decode write-back")
+
+
 # ---- degenerate cases of the method and maximum sizes ------------------------------------------------------
 def _degenerate_case(kind, state="f32", qkv="f32", out="f32"):
     w = small(f"degenerate_{kind}", B=2, T=4, HK=1, HV=2, DK=128, DV=64, num_slots=4, qkv=qkv, state=state, out=out)
