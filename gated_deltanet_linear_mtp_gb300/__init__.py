@@ -205,7 +205,9 @@ def gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_w
 def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, *,
                       scale=1.0, l2_eps=1e-6, stream=None) -> None:
     """The first ``accept_len[b]`` tokens again from ``state_pool[state_indices[b]]``, final state written back
-    (the verify call's inputs; no outputs).  Same pool bits as ``gdn_commit`` after a caching verify."""
+    (the verify call's inputs; no outputs).  The pool state ``gdn_commit`` leaves after a caching verify: the
+    same bits for an fp32 pool or T > 8, within one bf16 ulp (the chunked tensor-core form) for a bf16 pool
+    with T <= 8."""
     import torch
 
     L = lib()
