@@ -1,4 +1,4 @@
-"""CPU oracle for the Gated DeltaNet decode / MTP-verify / commit path.
+"""CPU oracle for the Gated DeltaNet decode / MTP-verify / commit / prefill path and its gated RMSNorm.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline`` leg
 and ``--impl reference`` arm may import this package.  It shares no code with the CUDA library in
@@ -57,7 +57,11 @@ class Oracle:
         self.lib.orc_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp]
         self.lib.orc_commit.argtypes = [dp, vp, ip, vp, ip]
         self.lib.orc_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip]
-        for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit, self.lib.orc_commit_replay):
+        self.lib.orc_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp]
+        self.lib.orc_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, vp, ctypes.c_int32, vp,
+                                               ctypes.c_int32, vp, ctypes.c_double, vp]
+        for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit, self.lib.orc_commit_replay,
+                  self.lib.orc_prefill, self.lib.orc_gated_rmsnorm):
             f.restype = ctypes.c_int
         for name in ("orc_round_bf16", "orc_softplus", "orc_sigmoid"):
             getattr(self.lib, name).argtypes = [ctypes.c_double]
@@ -159,6 +163,59 @@ class Oracle:
         if flags < 0:
             raise ValueError(f"oracle rejected dims ({flags})")
         return flags
+
+    def prefill(self, d: Dict, x: Dict[str, np.ndarray], cu_seqlens: np.ndarray, pool: np.ndarray,
+                has_initial_state: Optional[np.ndarray] = None, o: Optional[np.ndarray] = None):
+        """Prefill of len(cu_seqlens) - 1 packed sequences; ``x`` holds q, k [N, HK, DK], v [N, HV, DV],
+        a, b [N, HV], A_log, dt_bias, indices [B].  Updates ``pool`` in place (the slots of active
+        sequences); returns (o [N, HV, DV] fp64, flag word).  ``o`` may be passed pre-filled (canaries)."""
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        B = cu.shape[0] - 1
+        N = x["q"].shape[0]
+        HK, HV, DK, DV = d["HK"], d["HV"], d["DK"], d["DV"]
+        qd = d["qkv_dtype"]
+        q = self._check(x["q"], qd, (N, HK, DK), "q")
+        k = self._check(x["k"], qd, (N, HK, DK), "k")
+        v = self._check(x["v"], qd, (N, HV, DV), "v")
+        a = self._check(x["a"], qd, (N, HV), "a")
+        b = self._check(x["b"], qd, (N, HV), "b")
+        A_log = self._check(x["A_log"], "f32", (HV,), "A_log")
+        dt_bias = self._check(x["dt_bias"], "f32", (HV,), "dt_bias")
+        idx = np.ascontiguousarray(x["indices"], dtype=np.int32)
+        if B < 0 or idx.shape != (B,):
+            raise ValueError("indices / cu_seqlens shapes")
+        assert pool.flags["C_CONTIGUOUS"]
+        self._check(pool, d["state_dtype"], (d["num_slots"], HV, DV, DK), "pool")
+        init = None
+        if has_initial_state is not None:
+            init = np.ascontiguousarray(has_initial_state, dtype=np.int32)
+            if init.shape != (B,):
+                raise ValueError("has_initial_state shape")
+        if o is None:
+            o = np.zeros((N, HV, DV), np.float64)
+        if N == 0 or B == 0:
+            return o, 0
+        dims = self._dims(dict(d, T=N), B)
+        flags = self.lib.orc_prefill(ctypes.byref(dims), _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                     _ptr(A_log), _ptr(dt_bias), _ptr(pool), _ptr(idx), _ptr(init), _ptr(o))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return o, flags
+
+    def gated_rmsnorm(self, o: np.ndarray, o_dtype: str, z: np.ndarray, z_dtype: str, w: np.ndarray,
+                      eps: float) -> np.ndarray:
+        """y = o / sqrt(mean(o^2) + eps) * w * silu(z) over the last axis (length DV); fp64 result."""
+        o = self._check(o, o_dtype, o.shape, "o")
+        z = self._check(z, z_dtype, o.shape, "z")
+        DV = o.shape[-1]
+        w = self._check(w, "f32", (DV,), "w")
+        y = np.zeros(o.shape, np.float64)
+        rows = int(np.prod(o.shape[:-1]))
+        rc = self.lib.orc_gated_rmsnorm(rows, DV, _ptr(o), DTYPE_CODE[o_dtype], _ptr(z), DTYPE_CODE[z_dtype],
+                                        _ptr(w), float(eps), _ptr(y))
+        if rc < 0:
+            raise ValueError(f"oracle rejected sizes ({rc})")
+        return y
 
     def commit(self, d: Dict, pool: np.ndarray, indices: np.ndarray, cache: np.ndarray,
                accept_len: np.ndarray) -> int:

@@ -1,4 +1,5 @@
-"""Independent NumPy restatement of the gated delta rule in product form, float64, dense matrices.
+"""Independent NumPy restatement of the gated delta rule in product form, float64, dense matrices (decode /
+verify lanes: ``lane_head``; prefill sequences: ``sequence_head``).
 
 TEST INFRASTRUCTURE (see ``oracle/__init__.py``).  It shares nothing with ``gdn_oracle.c`` beyond the
 definition both restate: the loop oracle scales, projects and updates row by row; this module multiplies
@@ -59,3 +60,30 @@ def lane_head(d: Dict, x: Dict[str, np.ndarray], b: int, h: int) -> Tuple[np.nda
         outs.append(scale * (S @ qh))
         states.append(S.copy())
     return np.stack(outs), states
+
+
+def sequence_head(d: Dict, x: Dict[str, np.ndarray], cu_seqlens, has_initial_state, b: int,
+                  h: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Prefill of sequence b, value head h, in product form: outputs (L x DV) at token positions
+    cu_seqlens[b] .. cu_seqlens[b+1]-1 of the packed arrays and the final state (DV x DK).  The start is the
+    pool slot's state, or the zero matrix where has_initial_state[b] == 0."""
+    HK, HV, DK, DV = d["HK"], d["HV"], d["DK"], d["DV"]
+    qd, sd = d["qkv_dtype"], d["state_dtype"]
+    eps, scale = float(d.get("l2_eps", 1e-6)), float(d.get("scale", 1.0))
+    hk = h // (HV // HK)
+    fresh = has_initial_state is not None and int(has_initial_state[b]) == 0
+    S = np.zeros((DV, DK)) if fresh else decode_storage(x["pool"][int(x["indices"][b]), h], sd).reshape(DV, DK)
+    I = np.eye(DK)
+    outs = []
+    for n in range(int(cu_seqlens[b]), int(cu_seqlens[b + 1])):
+        q = decode_storage(x["q"][n, hk], qd)
+        k = decode_storage(x["k"][n, hk], qd)
+        v = decode_storage(x["v"][n, h], qd)
+        qh = q / np.sqrt(q @ q + eps)
+        kh = k / np.sqrt(k @ k + eps)
+        g = np.exp(-np.exp(float(x["A_log"][h])) *
+                   np.logaddexp(0.0, decode_storage(x["a"][n, h], qd) + float(x["dt_bias"][h])))
+        beta = _sigmoid(decode_storage(x["b"][n, h], qd))
+        S = g * S @ (I - beta * np.outer(kh, kh)) + beta * np.outer(v, kh)
+        outs.append(scale * (S @ qh))
+    return (np.stack(outs) if outs else np.zeros((0, DV))), S

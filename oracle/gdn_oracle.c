@@ -27,6 +27,20 @@
  *   replay commit: the first L_b tokens again from pool[idx[b], h], then pool[idx[b], h] = R(S): the
  *     same value as the commit above, without caching every intermediate state.
  *
+ *   prefill: B variable-length sequences packed along one token axis of length N (= dims T): sequence b
+ *     runs tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 from S = pool[idx[b], h] if has_initial_state[b] is
+ *     non-zero, else from S = 0 (the pool slot is then not read at all: fresh-state zeroing), writes o at
+ *     those token positions and pool[idx[b], h] = R(S) after its last token.  The chunked gated delta
+ *     rule with a bf16 state pool and an initial-state mask of TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-
+ *     Next NVFP4), Per-File QA Perspective, Source files and Test-code files (flashinfer_chunk_gated_delta_
+ *     rule: "fresh-state zeroing", bf16 pools); the chunking there is an evaluation order of this same
+ *     recurrence, so the definition is the token loop.
+ *   gated RMSNorm of the outputs (the "decode rows gated norm" of the same page and section), per row r of
+ *     DV outputs:  y[r, i] = o[r, i] / sqrt(mean_i(o[r, i]^2) + eps) * w[i] * silu(z[r, i]),
+ *     silu(x) = x * sigmoid(x).  The page names the fusion, not its formula: this is the plain reading
+ *     (RMS over the value dimension of one head, one weight vector of length DV shared by all heads, the
+ *     gate applied after the norm).
+ *
  * Padded lanes (index -1) are skipped: the page's padding index guard (sglang PR #23273, Requirements,
  * FlashInfer #2810).  bf16 state with intermediate caching beyond T > 4: same page, Requirements
  * (FlashInfer #2679).  A_log is fp32: same page, Summary (A_log.detach().float()).
@@ -35,8 +49,9 @@
  * (each cache write, the decode write-back): round-to-nearest-even, directly from fp64 (no double
  * rounding).  The running state of one call is never rounded between tokens.
  *
- * Out-of-range data (index < -1 or >= num_slots, accept length outside 0..T) skips the lane and sets a
- * bit in the returned flag word: bit 0 = index, bit 1 = accept length.
+ * Out-of-range data (index < -1 or >= num_slots, accept length outside 0..T, a prefill sequence whose
+ * bounds are negative, decreasing or beyond N) skips the lane and sets a bit in the returned flag word:
+ * bit 0 = index, bit 1 = accept length, bit 3 = sequence bounds.
  */
 #include <math.h>
 #include <stdint.h>
@@ -126,12 +141,15 @@ static int lane_slot(const orc_dims* d, const int32_t* idx, int b, int* flags) {
 }
 
 /* Runs the tokens of every active lane: all T, or steps[b] of them if steps != NULL (a count outside 0..T
- * sets flag bit 1 and skips the lane).  If o != NULL, stores the outputs.  If cache != NULL, stores R(S)
- * after every token (verify).  If write_back, stores R(S) of the last token run into the lane's pool slot
- * (decode; replay commit). */
+ * sets flag bit 1 and skips the lane), or, if seq != NULL (prefill), tokens seq[b] .. seq[b+1]-1 of the
+ * token axis (bounds outside 0..T set flag bit 3 and skip the lane).  A lane with has_init != NULL and
+ * has_init[b] == 0 starts from the zero state.  If o != NULL, stores the outputs.  If cache != NULL,
+ * stores R(S) after every token (verify).  If write_back, stores R(S) of the last token run into the
+ * lane's pool slot (decode; replay commit; prefill). */
 static int run(const orc_dims* d, const void* q, const void* k, const void* v, const void* a,
                const void* bb, const float* A_log, const float* dt_bias, void* pool, const int32_t* idx,
-               double* o, void* cache, int write_back, const int32_t* steps) {
+               double* o, void* cache, int write_back, const int32_t* steps, const int32_t* seq,
+               const int32_t* has_init) {
     const int B = d->B, T = d->T, HK = d->HK, HV = d->HV, DK = d->DK, DV = d->DV;
     const int r = HV / HK;
     int flags = 0;
@@ -146,22 +164,34 @@ static int run(const orc_dims* d, const void* q, const void* k, const void* v, c
     for (int b = 0; b < B; ++b) {
         int slot = lane_slot(d, idx, b, &flags);
         if (slot < 0) continue;
-        const int n_tok = steps ? steps[b] : T;
+        /* the lane's tokens are positions tok0 .. tok0 + n_tok - 1 of the token axis of q, k, v, a, b, o */
+        int64_t tok0 = (int64_t)b * T;
+        int n_tok = steps ? steps[b] : T;
+        if (seq) {
+            if (seq[b] < 0 || seq[b + 1] < seq[b] || seq[b + 1] > T) {
+                flags |= 8;
+                continue;
+            }
+            tok0 = seq[b];
+            n_tok = seq[b + 1] - seq[b];
+        }
         if (n_tok < 0 || n_tok > T) {
             flags |= 2;
             continue;
         }
         if (n_tok == 0) continue;
+        const int fresh = has_init && !has_init[b];
         for (int h = 0; h < HV; ++h) {
             const int hk = h / r;
             const int64_t state_off = ((int64_t)slot * HV + h) * DV * DK;
             for (int i = 0; i < DV; ++i)
-                for (int j = 0; j < DK; ++j) S[i * DK + j] = load(pool, d->state_dtype, state_off + i * DK + j);
+                for (int j = 0; j < DK; ++j)
+                    S[i * DK + j] = fresh ? 0.0 : load(pool, d->state_dtype, state_off + i * DK + j);
 
             for (int t = 0; t < n_tok; ++t) {
-                const int64_t qk_off = (((int64_t)b * T + t) * HK + hk) * DK;
-                const int64_t ab_off = ((int64_t)b * T + t) * HV + h;
-                const int64_t v_off = (((int64_t)b * T + t) * HV + h) * DV;
+                const int64_t qk_off = ((tok0 + t) * HK + hk) * DK;
+                const int64_t ab_off = (tok0 + t) * HV + h;
+                const int64_t v_off = ((tok0 + t) * HV + h) * DV;
 
                 double qq = 0.0, kk = 0.0;
                 for (int j = 0; j < DK; ++j) {
@@ -215,14 +245,14 @@ int orc_verify(const orc_dims* d, const void* q, const void* k, const void* v, c
                const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, double* o,
                void* cache) {
     if (!dims_ok(d)) return -2;
-    return run(d, q, k, v, a, b, A_log, dt_bias, (void*)pool, idx, o, cache, 0, NULL);
+    return run(d, q, k, v, a, b, A_log, dt_bias, (void*)pool, idx, o, cache, 0, NULL, NULL, NULL);
 }
 
 /* T tokens from pool[idx[b]], final state written back into the same slot. */
 int orc_decode(const orc_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
                const float* A_log, const float* dt_bias, void* pool, const int32_t* idx, double* o) {
     if (!dims_ok(d)) return -2;
-    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1, NULL);
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1, NULL, NULL, NULL);
 }
 
 /* Replay commit: the first accept_len[b] tokens of every active lane from pool[idx[b]], the final state
@@ -231,7 +261,39 @@ int orc_commit_replay(const orc_dims* d, const void* q, const void* k, const voi
                       const void* b, const float* A_log, const float* dt_bias, void* pool, const int32_t* idx,
                       const int32_t* accept_len) {
     if (!dims_ok(d)) return -2;
-    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, NULL, NULL, 1, accept_len);
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, NULL, NULL, 1, accept_len, NULL, NULL);
+}
+
+/* Prefill: d->B sequences over a token axis of d->T tokens (q, k [T, HK, DK]; v [T, HV, DV]; a, b [T, HV];
+ * o [T, HV, DV]); has_init (nullable: every sequence has one) selects the pool state or zero as the start;
+ * the final state goes into pool[idx[b]].  Positions outside every sequence, and those of skipped lanes,
+ * keep their o. */
+int orc_prefill(const orc_dims* d, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,
+                const void* a, const void* b, const float* A_log, const float* dt_bias, void* pool,
+                const int32_t* idx, const int32_t* has_init, double* o) {
+    if (!dims_ok(d)) return -2;
+    return run(d, q, k, v, a, b, A_log, dt_bias, pool, idx, o, NULL, 1, NULL, cu_seqlens, has_init);
+}
+
+/* Gated RMSNorm of `rows` rows of DV values: o and z in their storage types, w fp32 [DV], y fp64. */
+int orc_gated_rmsnorm(int64_t rows, int32_t DV, const void* o, int32_t o_dtype, const void* z, int32_t z_dtype,
+                      const float* w, double eps, double* y) {
+    if (rows < 0 || DV < 1 || eps < 0.0) return -2;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ms = 0.0;
+        for (int i = 0; i < DV; ++i) {
+            const double x = load(o, o_dtype, r * DV + i);
+            ms += x * x;
+        }
+        ms /= DV;
+        const double inv_rms = 1.0 / sqrt(ms + eps);
+        for (int i = 0; i < DV; ++i) {
+            const double zi = load(z, z_dtype, r * DV + i);
+            const double silu = zi * orc_sigmoid(zi);
+            y[r * DV + i] = load(o, o_dtype, r * DV + i) * inv_rms * (double)w[i] * silu;
+        }
+    }
+    return 0;
 }
 
 /* pool[idx[b], :] = cache[b, L_b - 1, :] (all heads), bit for bit, for active lanes with L_b >= 1. */

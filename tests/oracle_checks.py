@@ -358,7 +358,167 @@ def check_commit_replay(orc):
     assert np.array_equal(p_bad, x["pool"])
 
 
+def _prefill_case(lengths, HK=2, HV=4, DK=8, DV=6, seed=61, qkv="f64", state="f64"):
+    """Packed prefill inputs for sequences of the given lengths (random q, k, v, a, b, gates, pool)."""
+    N = int(sum(lengths))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    B = len(lengths)
+    rng = np.random.default_rng(seed)
+    st = {"f64": np.float64, "f32": np.float32}
+    num_slots = B + 3
+    d = dict(T=N, HK=HK, HV=HV, DK=DK, DV=DV, num_slots=num_slots, qkv_dtype=qkv, state_dtype=state,
+             scale=1.0, l2_eps=1e-6)
+    x = dict(q=rng.standard_normal((N, HK, DK)).astype(st[qkv]), k=rng.standard_normal((N, HK, DK)).astype(st[qkv]),
+             v=rng.standard_normal((N, HV, DV)).astype(st[qkv]), a=rng.standard_normal((N, HV)).astype(st[qkv]),
+             b=rng.standard_normal((N, HV)).astype(st[qkv]),
+             A_log=np.log(rng.uniform(1, 16, HV)).astype(np.float32),
+             dt_bias=rng.standard_normal(HV).astype(np.float32),
+             pool=(rng.standard_normal((num_slots, HV, DV, DK)) * 0.3).astype(st[state]),
+             indices=rng.permutation(num_slots)[:B].astype(np.int32))
+    return d, x, cu
+
+
+def check_prefill_product_form(orc):
+    """Variable-length sequences, with and without an initial state, against the product form
+    (brute.sequence_head); a padded sequence and an empty one leave o and the pool as they were."""
+    lengths = [5, 1, 0, 7, 3, 4]
+    d, x, cu = _prefill_case(lengths)
+    x["indices"][4] = -1
+    init = np.array([1, 0, 1, 0, 1, 1], np.int32)
+    pool = x["pool"].copy()
+    o0 = np.full((cu[-1], d["HV"], d["DV"]), CANARY)
+    o, fl = orc.prefill(d, x, cu, pool, init, o=o0.copy())
+    assert fl == 0
+    for b in range(len(lengths)):
+        lo, hi = cu[b], cu[b + 1]
+        slot = x["indices"][b]
+        if slot < 0:
+            assert np.all(o[lo:hi] == CANARY)
+            continue
+        if lengths[b] == 0:
+            assert np.array_equal(pool[slot], x["pool"][slot])
+            continue
+        for h in range(d["HV"]):
+            ob, S = brute.sequence_head(d, x, cu, init, b, h)
+            assert rel_err(o[lo:hi, h], ob) < 1e-12, (b, h)
+            assert rel_err(pool[slot, h], S) < 1e-12, (b, h)
+    touched = x["indices"][[0, 1, 3, 5]]
+    untouched = np.setdiff1d(np.arange(d["num_slots"]), touched)
+    assert np.array_equal(pool[untouched], x["pool"][untouched])
+
+
+def check_prefill_fresh_state(orc):
+    """A sequence without an initial state never reads its slot (NaN there changes nothing) and starts from
+    zero: after one token S = beta v kh^T, so o = beta v (kh . qh)."""
+    from scipy.special import expit
+
+    d, x, cu = _prefill_case([1, 3], HK=1, HV=2, DK=4, DV=3, seed=62)
+    init = np.array([0, 0], np.int32)
+    pool = x["pool"].copy()
+    pool[x["indices"]] = np.nan
+    o, fl = orc.prefill(d, x, cu, pool, init)
+    assert fl == 0 and np.all(np.isfinite(o)) and np.all(np.isfinite(pool[x["indices"]]))
+    pool_zero = x["pool"].copy()
+    pool_zero[x["indices"]] = 0.0
+    o2, _ = orc.prefill(d, x, cu, pool_zero, np.array([1, 1], np.int32))
+    assert np.array_equal(o, o2) and np.array_equal(pool[x["indices"]], pool_zero[x["indices"]])
+    for h in range(2):
+        q, k, v = x["q"][0, 0], x["k"][0, 0], x["v"][0, h]
+        kq = (k @ q) / math.sqrt((k @ k + 1e-6) * (q @ q + 1e-6))
+        want = expit(float(x["b"][0, h])) * v * kq
+        assert rel_err(o[0, h], want) < 1e-12, h
+
+
+def check_prefill_matches_verify_and_decode(orc):
+    """Equal lengths T packed lane after lane are the [B, T] layout of verify: same outputs as verify, and
+    the final state written back is the one decode(T) writes."""
+    T, B = 3, 3
+    d, x, cu = _prefill_case([T] * B, HK=2, HV=4, DK=8, DV=5, seed=63)
+    x["indices"][1] = -1
+    pool = x["pool"].copy()
+    o, fl = orc.prefill(d, x, cu, pool)
+    assert fl == 0
+    dv = dict(d, T=T)
+    xv = dict(x)
+    for n, shape in (("q", (B, T, d["HK"], d["DK"])), ("k", (B, T, d["HK"], d["DK"])),
+                     ("v", (B, T, d["HV"], d["DV"])), ("a", (B, T, d["HV"])), ("b", (B, T, d["HV"]))):
+        xv[n] = np.ascontiguousarray(x[n].reshape(shape))
+    o_v, _, _ = orc.verify(dv, xv, cache=False)
+    pool_d = x["pool"].copy()
+    orc.decode(dv, xv, pool_d)
+    for b in (0, 2):
+        assert np.array_equal(o[b * T:(b + 1) * T], o_v[b])
+    assert np.array_equal(pool, pool_d)
+
+
+def check_prefill_chained(orc):
+    """A sequence split in two prefill calls (the second from the state the first wrote) equals one call."""
+    d, x, cu = _prefill_case([9], HK=1, HV=2, DK=8, DV=4, seed=64)
+    pool_one = x["pool"].copy()
+    o_one, _ = orc.prefill(d, x, cu, pool_one)
+    for L1 in (1, 4, 8):
+        pool = x["pool"].copy()
+        x1 = dict(x, **{n: np.ascontiguousarray(x[n][:L1]) for n in ("q", "k", "v", "a", "b")})
+        x2 = dict(x, **{n: np.ascontiguousarray(x[n][L1:]) for n in ("q", "k", "v", "a", "b")})
+        o1, _ = orc.prefill(dict(d, T=L1), x1, np.array([0, L1], np.int32), pool, np.ones(1, np.int32))
+        o2, _ = orc.prefill(dict(d, T=9 - L1), x2, np.array([0, 9 - L1], np.int32), pool)
+        assert rel_err(np.concatenate([o1, o2]), o_one) < 1e-13, L1
+        assert rel_err(pool, pool_one) < 1e-13, L1
+
+
+def check_prefill_bad_bounds(orc):
+    """Decreasing, negative or too-long sequence bounds skip the sequence and set flag 8; an out-of-range
+    index flag 1; nothing is written for them."""
+    d, x, cu = _prefill_case([2, 3], HK=1, HV=1, DK=4, DV=4, seed=65)
+    for bad in ([0, 3, 2], [-1, 2, 5], [0, 2, 6]):
+        pool = x["pool"].copy()
+        o, fl = orc.prefill(d, x, np.array(bad, np.int32), pool, o=np.full((5, 1, 4), CANARY))
+        assert fl == 8, (bad, fl)
+        ok = [b for b in range(2) if 0 <= bad[b] <= bad[b + 1] <= 5]
+        for b in range(2):
+            if b not in ok:
+                assert np.array_equal(pool[x["indices"][b]], x["pool"][x["indices"][b]]), bad
+    x["indices"][0] = d["num_slots"]
+    pool = x["pool"].copy()
+    o, fl = orc.prefill(d, x, cu, pool, o=np.full((5, 1, 4), CANARY))
+    assert fl == 1 and np.all(o[0:2] == CANARY) and not np.any(o[2:5] == CANARY)
+
+
+def check_gated_rmsnorm_closed_forms(orc):
+    """Rows with a closed-form RMS (one-hot, constant, a 3-4-5 pair, zero) and gates z = ln r, where
+    silu(ln r) = ln r * r / (1 + r) exactly; weights differ per column, gates per row and column."""
+    DV = 4
+    w = np.array([0.5, -2.0, 1.25, 3.0], np.float32)
+    r = np.array([[3.0, 0.25, 7.0, 1.5], [2.0, 9.0, 0.5, 4.0], [5.0, 0.2, 1.0, 6.0], [1.25, 3.0, 8.0, 0.75],
+                  [4.0, 4.0, 0.1, 2.5]])
+    z = np.log(r)
+    silu = np.log(r) * r / (1.0 + r)
+    for eps in (0.0, 1e-6, 0.75):
+        o = np.array([[0.0, 2.5, 0.0, 0.0],       # one-hot: mean = c^2 / DV
+                      [-1.5, -1.5, -1.5, -1.5],   # constant
+                      [3.0, 0.0, 4.0, 0.0],       # mean = 25 / 4
+                      [0.0, 0.0, 0.0, 0.0],       # zero row
+                      [1.0, -1.0, 1.0, -1.0]])
+        rms = np.sqrt(np.array([2.5 ** 2 / DV, 2.25, 25.0 / 4, 0.0, 1.0]) + eps)
+        y = orc.gated_rmsnorm(o, "f64", z, "f64", w, eps)
+        for i in range(5):
+            if i == 3 and eps == 0.0:
+                continue                          # 0 / 0: no closed form
+            want = o[i] / rms[i] * w.astype(np.float64) * silu[i]
+            assert np.abs(y[i] - want).max() <= 1e-14 * max(1.0, np.abs(want).max()), (eps, i, y[i], want)
+    # storage types are read exactly: bf16 o and z (bit patterns), fp32 rows
+    from gdn_workloads import to_bf16_bits
+    ob = to_bf16_bits(np.array([[3.0, 0.0, 4.0, 0.0]], np.float32))
+    zb = to_bf16_bits(np.array([[1.0, 2.0, -1.0, 0.5]], np.float32))
+    y = orc.gated_rmsnorm(ob, "bf16", zb, "bf16", w, 0.0)
+    zz = np.array([1.0, 2.0, -1.0, 0.5])
+    want = np.array([3.0, 0.0, 4.0, 0.0]) / 2.5 * w * (zz / (1 + np.exp(-zz)))
+    assert np.abs(y[0] - want).max() < 1e-14
+
+
 ALL_CHECKS = [check_bf16_rounding, check_scalar_functions, check_gate_closed_form, check_beta_sigmoid,
               check_beta_zero_pure_decay, check_orthonormal_keys_write_v, check_l2norm_eps, check_scale,
               check_head_mapping, check_product_form, check_chained_calls, check_padding_and_bad_data,
-              check_commit_replay]
+              check_commit_replay, check_prefill_product_form, check_prefill_fresh_state,
+              check_prefill_matches_verify_and_decode, check_prefill_chained, check_prefill_bad_bounds,
+              check_gated_rmsnorm_closed_forms]

@@ -45,8 +45,23 @@ MUTANTS = [
     ("commit_first_token", "(((int64_t)b * d->T) + (L - 1)) * per_lane", "(((int64_t)b * d->T) + 0) * per_lane"),
     ("padding_not_skipped", "if (slot == -1) return -1;", "if (slot == -1) return 0;"),
     ("accept_len_unchecked", "if (L < 0 || L > d->T) {", "if (0) {"),
-    ("replay_ignores_accept_len", "const int n_tok = steps ? steps[b] : T;", "const int n_tok = T;"),
-    ("replay_off_by_one", "const int n_tok = steps ? steps[b] : T;", "const int n_tok = steps ? steps[b] - (steps[b] > 1) : T;"),
+    ("replay_ignores_accept_len", "int n_tok = steps ? steps[b] : T;", "int n_tok = T;"),
+    ("replay_off_by_one", "int n_tok = steps ? steps[b] : T;", "int n_tok = steps ? steps[b] - (steps[b] > 1) : T;"),
+    ("prefill_fresh_reads_pool", "const int fresh = has_init && !has_init[b];", "const int fresh = 0;"),
+    ("prefill_fresh_inverted", "const int fresh = has_init && !has_init[b];",
+     "const int fresh = has_init && has_init[b];"),
+    ("prefill_token_base", "tok0 = seq[b];", "tok0 = seq[0];"),
+    ("prefill_length_one_short", "n_tok = seq[b + 1] - seq[b];", "n_tok = seq[b + 1] - seq[b] - (seq[b + 1] > seq[b]);"),
+    ("prefill_bad_bounds_flag", "flags |= 8;", "flags |= 2;"),
+    ("norm_sum_not_mean", "ms /= DV;", ""),
+    ("norm_eps_outside_root", "const double inv_rms = 1.0 / sqrt(ms + eps);",
+     "const double inv_rms = 1.0 / (sqrt(ms) + eps);"),
+    ("norm_gate_sigmoid_only", "const double silu = zi * orc_sigmoid(zi);", "const double silu = orc_sigmoid(zi);"),
+    ("norm_gate_sign", "const double silu = zi * orc_sigmoid(zi);", "const double silu = zi * orc_sigmoid(-zi);"),
+    ("norm_weight_index", "* (double)w[i] * silu;", "* (double)w[0] * silu;"),
+    ("norm_gate_row", "const double zi = load(z, z_dtype, r * DV + i);", "const double zi = load(z, z_dtype, i);"),
+    ("norm_output_unnormalised", "y[r * DV + i] = load(o, o_dtype, r * DV + i) * inv_rms * (double)w[i] * silu;",
+     "y[r * DV + i] = load(o, o_dtype, r * DV + i) * (double)w[i] * silu;"),
 ]
 
 
