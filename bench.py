@@ -8,6 +8,7 @@ L2 (129 MB) is flushed between steps, outside each step's CUDA events: a 256 MiB
 so that the lines left in L2 are clean.
 
     python bench.py [--steps K] [--warmup W] [--workload verify4|verify8|decode|...|sweep|sweep_replay] [--impl reference]
+    python bench.py --workload prefill8k|prefill_mix|gated_norm     (the prefill and gated-norm calls, own lines)
 
 Prints one JSON line (``--workload sweep``: one per point).  ``value`` = verified tokens/s (A x T per step,
 A = non-padded lanes, summed over ranks, divided by the slowest rank's device time).
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 import gdn_workloads as W  # noqa: E402
 
 METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8"
+PREFILL_NAMED = {"prefill8k": W.prefill_8k, "prefill_mix": W.prefill_mix}
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent_launch.cuh",
@@ -563,6 +565,228 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     return result
 
 
+# ---- prefill and the gated RMSNorm ----------------------------------------------------------------------
+PREFILL_METRIC = "GDN prefill tokens/s (variable-length prompts into the state pool)"
+NORM_METRIC = "GDN gated RMSNorm rows/s and achieved HBM GB/s"
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per Blackwell SM
+PREFILL_FLOPS_PER_ELEM = 7  # per state element and token: decay 1, S.kh 2, rank-1 update 2, S.qh 2
+
+
+def alu_peak_tflops(sms: int, mhz: float) -> float:
+    """FP32 FMA peak of the CUDA cores (not the tensor cores): SMs x 128 lanes x 2 flops x clock."""
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def _timed_calls(call, K: int, warmup: int, stream, sampler):
+    import torch
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    sampler.stop()
+    return [e[0].elapsed_time(e[1]) for e in evs], t_wall
+
+
+def _prefill_cpu_baseline(pw, x, seconds: float):
+    """The oracle as it stands (one thread, fp64 C loops) on (prompt, head) pairs in order -- each a whole
+    prompt for one value head -- until about `seconds` of CPU work; tokens/s of the layer = pair tokens / HV
+    / time (a token's work is HV such pairs)."""
+    import oracle
+
+    orc = oracle.default()
+    r = pw.HV // pw.HK
+    d = dict(T=0, HK=1, HV=1, DK=pw.DK, DV=pw.DV, num_slots=1, qkv_dtype=pw.qkv_dtype, state_dtype=pw.state_dtype,
+             scale=pw.scale, l2_eps=pw.l2_eps)
+    cu = x["cu_seqlens"]
+    pairs = [(b, h) for b in range(pw.B) if x["indices"][b] >= 0 for h in range(pw.HV)]
+    done_tokens, n_pairs, t0 = 0, 0, time.perf_counter()
+    for b, h in pairs:
+        lo, hi, hk, slot = int(cu[b]), int(cu[b + 1]), h // r, int(x["indices"][b])
+        y = dict(q=np.ascontiguousarray(x["q"][lo:hi, hk:hk + 1]), k=np.ascontiguousarray(x["k"][lo:hi, hk:hk + 1]),
+                 v=np.ascontiguousarray(x["v"][lo:hi, h:h + 1]), a=np.ascontiguousarray(x["a"][lo:hi, h:h + 1]),
+                 b=np.ascontiguousarray(x["b"][lo:hi, h:h + 1]), A_log=np.ascontiguousarray(x["A_log"][h:h + 1]),
+                 dt_bias=np.ascontiguousarray(x["dt_bias"][h:h + 1]), indices=np.zeros(1, np.int32))
+        pool = np.ascontiguousarray(x["pool"][slot:slot + 1, h:h + 1])
+        orc.prefill(d, y, np.array([0, hi - lo], np.int32), pool, np.array([x["has_initial_state"][b]], np.int32))
+        done_tokens += hi - lo
+        n_pairs += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_tokens / pw.HV / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle prefill of the first {n_pairs} of {len(pairs)} (prompt, value head) pairs of "
+                      f"{pw.name} ({done_tokens} pair-tokens), fp64 C loops, one thread, {dt:.1f} s; "
+                      f"tokens/s = pair-tokens / HV / time"}
+
+
+def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
+    import torch
+
+    import gated_deltanet_linear_mtp_gb300 as gdn
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(world, "nccl")
+    pr = pw if rank == 0 else pw.replace(seed=pw.seed + 7919 * rank)
+    x = pr.arrays()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    t = {k: to_dev(v) for k, v in x.items()}
+    N = int(x["cu_seqlens"][-1])
+    odt = torch.bfloat16 if pw.out_dtype == "bf16" else torch.float32
+    o = torch.empty((N, pw.HV, pw.DV), dtype=odt, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    names = ("q", "k", "v", "a", "b")
+
+    def call(src=t, out=o):
+        gdn.gdn_prefill(src["q"], src["k"], src["v"], src["a"], src["b"], t["A_log"], t["dt_bias"], t["pool"],
+                        t["indices"], t["cu_seqlens"], out, t["has_initial_state"], err, scale=pw.scale,
+                        l2_eps=pw.l2_eps)
+
+    sampler = ClockSampler(local_rank)
+    if dist is not None:
+        dist.barrier()
+    ms, t_wall = _timed_calls(call, args.steps, args.warmup, stream, sampler)
+    if err.item() != 0:
+        raise RuntimeError(f"device error word {err.item()}")
+    total_ms = max_over_ranks(sum(ms), dist, device)
+    lens = np.diff(x["cu_seqlens"])
+    active_tokens = int(lens[x["indices"] >= 0].sum())
+    tokens_all = sum_over_ranks(active_tokens * args.steps, dist, device)
+
+    # end to end through the binding: each step's q, k, v, a, b copied in from pinned host memory and o
+    # copied back, on the compute stream
+    host_in = {k: t[k].cpu().pin_memory() for k in names}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = o.numel() * o.element_size()
+
+    def e2e_step():
+        for k in names:
+            t[k].copy_(host_in[k], non_blocking=True)
+        call()
+        o_host.copy_(o, non_blocking=True)
+
+    K_e2e = max(3, min(args.steps, 20))
+    e2e_ms, _ = _timed_calls(e2e_step, K_e2e, 2, stream, ClockSampler(local_rank))
+    e2e_ms_step = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+
+    props = torch.cuda.get_device_properties(device)
+    clocks = sampler.summary()
+    max_mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = alu_peak_tflops(props.multi_processor_count, max_mhz)
+    avg_us = statistics.mean(ms) * 1e3
+    flops = PREFILL_FLOPS_PER_ELEM * pw.DV * pw.DK * pw.HV * active_tokens
+    achieved = flops / (avg_us * 1e-6) / 1e12
+    result = {
+        "metric": PREFILL_METRIC, "value": tokens_all / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy draws; shapes and distributions of the named workload)",
+        "config": {"workload": pw.name, "B": pw.B, "tokens": N, "active_tokens": active_tokens, "HK": pw.HK,
+                   "HV": pw.HV, "DK": pw.DK, "DV": pw.DV, "state_dtype": pw.state_dtype, "qkv_dtype": pw.qkv_dtype,
+                   "fresh_sequences": int((x["has_initial_state"] == 0).sum()),
+                   "step": "gdn_prefill (every prompt from its slot or from zero; final state into the slot)",
+                   "l2": f"not flushed: the step reads {h2d / 1e9:.2f} GB of token inputs, more than L2",
+                   "parallelism": f"replicas x{world} (independent prompts, no collective)",
+                   "timing": "CUDA events per call on the launch stream, summed; max over ranks",
+                   "e2e": "inputs copied in from pinned host memory and o copied back on the compute stream, "
+                          "per step, not overlapped"},
+        "roofline": {"kernel": "gdn_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"derived: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                                    f"flops x {max_mhz:.0f} MHz (maximum SM clock)",
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us, "traffic": None},
+        "e2e": {"value": sum_over_ranks(active_tokens, dist, device) / (e2e_ms_step * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
+        "gpu_launches": args.steps, "clocks": clocks, "device": props.name,
+        "sm_count": props.multi_processor_count, "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = _prefill_cpu_baseline(pw, x, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
+def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536 * 32, DV: int = 128):
+    """The gated RMSNorm over the outputs of the ISL-8K prefill (65,536 tokens x 32 heads of 128, bf16)."""
+    import torch
+
+    import gated_deltanet_linear_mtp_gb300 as gdn
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(world, "nccl")
+    g = W.gated_norm_inputs(rows, DV, "bf16", "bf16", seed=17 + 7919 * rank)
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+    o, z = bf(g["o"]), bf(g["z"])
+    wt = torch.from_numpy(g["w"]).to(device)
+    y = torch.empty_like(o)
+    stream = torch.cuda.current_stream(device)
+    sampler = ClockSampler(local_rank)
+    if dist is not None:
+        dist.barrier()
+    ms, t_wall = _timed_calls(lambda: gdn.gdn_gated_rmsnorm(o, z, wt, y), args.steps, args.warmup, stream, sampler)
+    total_ms = max_over_ranks(sum(ms), dist, device)
+    nbytes = rows * DV * 2 * 3 + DV * 4
+    avg_us = statistics.mean(ms) * 1e3
+    peak, peak_src = hbm_peak()
+    achieved = nbytes / (avg_us * 1e-6) / 1e9
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    z_host = torch.empty(z.shape, dtype=z.dtype).pin_memory()
+    o_host.copy_(o)
+    z_host.copy_(z)
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e_step():
+        o.copy_(o_host, non_blocking=True)
+        z.copy_(z_host, non_blocking=True)
+        gdn.gdn_gated_rmsnorm(o, z, wt, y)
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_ms, _ = _timed_calls(e2e_step, max(3, min(args.steps, 20)), 2, stream, ClockSampler(local_rank))
+    e2e_ms_step = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    props = torch.cuda.get_device_properties(device)
+    result = {
+        "metric": NORM_METRIC, "value": rows * args.steps * world / (total_ms * 1e-3), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy draws)",
+        "config": {"workload": f"gated_rmsnorm_rows{rows}_DV{DV}_bf16", "rows": rows, "DV": DV,
+                   "o_dtype": "bf16", "z_dtype": "bf16",
+                   "l2": f"not flushed: each call moves {nbytes / 1e9:.2f} GB, more than L2",
+                   "parallelism": f"replicas x{world}", "timing": "CUDA events per call, summed; max over ranks",
+                   "e2e": "o and z copied in from pinned host memory and y copied back per step"},
+        "roofline": {"kernel": "gdn_gated_rmsnorm_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_us": avg_us, "traffic": None},
+        "e2e": {"value": rows * world / (e2e_ms_step * 1e-3), "unit": "rows/s",
+                "h2d_bytes_per_step": 2 * rows * DV * 2, "d2h_bytes_per_step": rows * DV * 2,
+                "ms_per_step": e2e_ms_step},
+        "gpu_launches": args.steps, "clocks": sampler.summary(), "device": props.name,
+        "sm_count": props.multi_processor_count, "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
 # ---- the oracle as CPU baseline / reference arm -----------------------------------------------------------
 def oracle_pairs(w: W.Workload, x: dict, pairs):
     """Per (lane, value head) inputs for the oracle: one lane, one head, its own one-slot pool copy."""
@@ -666,7 +890,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay"], default="verify4")
+    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay"] + sorted(PREFILL_NAMED)
+                    + ["gated_norm"], default="verify4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
@@ -674,6 +899,17 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_env()
+    if args.workload in PREFILL_NAMED or args.workload == "gated_norm":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the verify "
+                                  "workloads; prefill and the gated norm report the oracle as cpu_baseline"}))
+            return 0
+        if args.workload == "gated_norm":
+            run_norm_arm(args, rank, world, local_rank)
+        else:
+            run_prefill_arm(args, PREFILL_NAMED[args.workload](), rank, world, local_rank)
+        return 0
     if args.workload == "sweep":
         pts = W.sweep()
     elif args.workload == "sweep_replay":

@@ -8,10 +8,15 @@ library has not been built, every call raises.
     gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
     gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
     gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, ...)
+    gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o,
+                has_initial_state=None, err_word=None, ...)
+    gdn_gated_rmsnorm(o, z, norm_weight, y=None, eps=1e-6)
 
 Shapes and semantics are those of ``include/gdn.h``: q, k ``[B,T,HK,DK]``; v, o ``[B,T,HV,DV]``; a, b
 ``[B,T,HV]``; A_log, dt_bias ``[HV]`` fp32; state_pool ``[num_slots,HV,DV,DK]``; state_indices, accept_len
-``[B]`` int32; intermediate_states ``[B,T,HV,DV,DK]``; err_word a 1-element int32 device tensor.
+``[B]`` int32; intermediate_states ``[B,T,HV,DV,DK]``; err_word a 1-element int32 device tensor.  Prefill takes
+packed tokens: q, k ``[N,HK,DK]``; v, o ``[N,HV,DV]``; a, b ``[N,HV]``; cu_seqlens ``[B+1]`` and
+has_initial_state ``[B]`` int32.
 """
 from __future__ import annotations
 
@@ -21,19 +26,20 @@ from typing import Optional
 
 from .build import LIB_PATH
 
-__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "GdnError", "GdnDims", "lib", "STATUS",
-           "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT", "MAX_T",
-           "EXPORTS"]
+__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_prefill", "gdn_gated_rmsnorm",
+           "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
+           "ERRBIT_SEQLEN", "MAX_T", "EXPORTS"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_VALUE"}
 ERRBIT_INDEX = 1
 ERRBIT_ACCEPT_LEN = 2
 ERRBIT_TIMEOUT = 4
+ERRBIT_SEQLEN = 8
 MAX_T = 16
 F32, BF16 = 0, 1
-EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_status_string",
-           "gdn_last_cuda_error", "gdn_abi_version")
+EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_prefill", "gdn_gated_rmsnorm",
+           "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
 
 
 class GdnDims(ctypes.Structure):
@@ -68,7 +74,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
         L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
         L.gdn_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip, ip, vp]
-        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay):
+        L.gdn_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp, ip, vp]
+        L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
+                                        ctypes.c_float, vp, vp]
+        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_prefill,
+                  L.gdn_gated_rmsnorm):
             f.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -219,3 +229,60 @@ def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
                               _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
                               _dev(state_indices, "state_indices"), _dev(accept_len, "accept_len"),
                               _dev(err_word, "err_word"), _stream(stream)), "gdn_commit_replay")
+
+
+def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o, has_initial_state=None,
+                err_word=None, *, scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """Prefill of ``len(cu_seqlens) - 1`` packed sequences: sequence b (tokens ``cu_seqlens[b]`` ..
+    ``cu_seqlens[b+1]-1``) starts from ``state_pool[state_indices[b]]`` (or zero where
+    ``has_initial_state[b] == 0``), writes o at its tokens and its final state into that slot."""
+    import torch
+
+    L = lib()
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("prefill takes packed tokens: q, k [N,HK,DK], v, o [N,HV,DV], a, b [N,HV]")
+    N = q.shape[0]
+    B = cu_seqlens.shape[0] - 1
+    if cu_seqlens.dim() != 1 or B < 0:
+        raise ValueError("cu_seqlens is [B+1]")
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    # the [B, T] checks of the other calls, with the token axis as T and one "lane"
+    d = _io_dims(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), a.unsqueeze(0), b.unsqueeze(0), A_log, dt_bias,
+                 state_pool, state_indices[:1] if B > 0 else torch.zeros(1, dtype=torch.int32, device=q.device),
+                 o.unsqueeze(0), scale, l2_eps)
+    _shape(state_indices, (B,), "state_indices")
+    if has_initial_state is not None:
+        _shape(has_initial_state, (B,), "has_initial_state")
+        if has_initial_state.dtype != torch.int32:
+            raise TypeError("has_initial_state must be int32")
+    d.B, d.T = B, N
+    _call(L.gdn_prefill(ctypes.byref(d), _dev(cu_seqlens, "cu_seqlens"), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"),
+                        _dev(a, "a"), _dev(b, "b"), _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"),
+                        _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
+                        _dev(has_initial_state, "has_initial_state"), _dev(o, "o"), _dev(err_word, "err_word"),
+                        _stream(stream)), "gdn_prefill")
+
+
+def gdn_gated_rmsnorm(o, z, norm_weight, y=None, *, eps=1e-6, stream=None):
+    """``y = o / sqrt(mean(o^2) + eps) * norm_weight * silu(z)`` over the last axis (DV) of o; returns y
+    (a new tensor of o's shape and dtype unless given; ``y`` may be ``o`` itself)."""
+    import torch
+
+    L = lib()
+    if o.dim() < 1 or tuple(z.shape) != tuple(o.shape):
+        raise ValueError("z must have o's shape")
+    DV = o.shape[-1]
+    _shape(norm_weight, (DV,), "norm_weight")
+    if norm_weight.dtype != torch.float32:
+        raise TypeError("norm_weight must be fp32")
+    if y is None:
+        y = torch.empty_like(o)
+    _shape(y, o.shape, "y")
+    if y.dtype != o.dtype:
+        raise TypeError("y must have o's dtype")
+    rows = o.numel() // DV if DV > 0 else 0
+    _call(L.gdn_gated_rmsnorm(rows, DV, _code(o, "o"), _code(z, "z"), _dev(o, "o"), _dev(z, "z"),
+                              _dev(norm_weight, "norm_weight"), float(eps), _dev(y, "y"), _stream(stream)),
+          "gdn_gated_rmsnorm")
+    return y

@@ -25,10 +25,11 @@ size_t dtype_bytes(int32_t d) { return d == GDN_F32 ? 4 : 2; }
 bool supported_dk(int32_t dk) { return dk == 16 || dk == 32 || dk == 64 || dk == 128 || dk == 256; }
 
 // Sizes common to every call.  `need_io`: q/k/v/o dtypes and the scalars matter (decode, verify).
-gdn_status check_dims(const gdn_dims* d, bool need_io) {
+// `prefill`: T is the total token count of the packed sequences (0 .. INT32_MAX), not tokens per lane.
+gdn_status check_dims(const gdn_dims* d, bool need_io, bool prefill = false) {
     if (d == nullptr) return GDN_ERR_NULL;
     if (d->B < 0 || d->B > 65535) return GDN_ERR_SHAPE;
-    if (d->T < 1 || d->T > GDN_MAX_T) return GDN_ERR_SHAPE;
+    if (prefill ? d->T < 0 : (d->T < 1 || d->T > GDN_MAX_T)) return GDN_ERR_SHAPE;
     if (d->HV < 1 || d->HV > 65535 || d->DV < 1 || d->num_slots < 1) return GDN_ERR_SHAPE;
     if (!valid_dtype(d->state_dtype)) return GDN_ERR_DTYPE;
     if (need_io) {
@@ -39,7 +40,8 @@ gdn_status check_dims(const gdn_dims* d, bool need_io) {
     if (d->DK < 1) return GDN_ERR_SHAPE;
     if (!supported_dk(d->DK)) return GDN_ERR_UNSUPPORTED;
     // every element offset is formed in int64: bound the largest array (the cache) well inside it
-    const double cache_elems = (double)d->B * d->T * d->HV * (double)d->DV * d->DK;
+    const double cache_elems = prefill ? (double)d->T * d->HV * (double)d->DV
+                                       : (double)d->B * d->T * d->HV * (double)d->DV * d->DK;
     const double pool_elems = (double)d->num_slots * d->HV * (double)d->DV * d->DK;
     if (cache_elems > 4.0e18 || pool_elems > 4.0e18) return GDN_ERR_SHAPE;
     return GDN_OK;
@@ -65,10 +67,10 @@ gdn_status finish(cudaError_t e) {
     return GDN_ERR_CUDA;
 }
 
-gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a,
-                         const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
-                         void* pool_out, const int32_t* idx, const int32_t* steps, void* o, void* cache,
-                         int32_t* err, cudaStream_t stream) {
+RecurrentParams make_params(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a,
+                            const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
+                            void* pool_out, const int32_t* idx, const int32_t* steps, void* o, void* cache,
+                            int32_t* err) {
     RecurrentParams p;
     p.q = q;
     p.k = k;
@@ -93,6 +95,15 @@ gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const 
     p.v_vec = aligned(v, 16) && ((int64_t)d->DV * (int64_t)dtype_bytes(d->qkv_dtype)) % 16 == 0;
     p.scale = d->scale;
     p.l2_eps = d->l2_eps;
+    return p;
+}
+
+gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a,
+                         const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
+                         void* pool_out, const int32_t* idx, const int32_t* steps, void* o, void* cache,
+                         int32_t* err, cudaStream_t stream) {
+    const RecurrentParams p =
+        make_params(d, q, k, v, a, b, A_log, dt_bias, pool_in, pool_out, idx, steps, o, cache, err);
     const bool qkv_bf16 = d->qkv_dtype == GDN_BF16;
     if (d->state_dtype == GDN_F32) return finish(launch_recurrent_f32state(p, d->B, d->DK, qkv_bf16, stream));
     return finish(launch_recurrent_bf16state(p, d->B, d->DK, qkv_bf16, stream));
@@ -168,6 +179,48 @@ gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k,
                          nullptr, nullptr, err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
+gdn_status gdn_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                       const int32_t* state_indices, const int32_t* has_initial_state, void* o, int32_t* err_word,
+                       gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0 || dims->T == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    if (!cu_seqlens) return GDN_ERR_NULL;
+    if (!aligned(cu_seqlens, 4) || (has_initial_state && !aligned(has_initial_state, 4))) return GDN_ERR_ALIGN;
+    const RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices,
+                                          nullptr, o, nullptr, err_word);
+    return finish(launch_prefill(p, cu_seqlens, has_initial_state, dims->B, dims->T, dims->DK,
+                                 dims->qkv_dtype == GDN_BF16, dims->state_dtype == GDN_BF16,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t DV, int32_t o_dtype, int32_t z_dtype, const void* o, const void* z,
+                             const float* norm_weight, float eps, void* y, gdn_stream_t stream) {
+    if (rows < 0 || DV < 1 || rows > gated_norm_max_rows()) return GDN_ERR_SHAPE;
+    if ((double)rows * DV > 4.0e18) return GDN_ERR_SHAPE;
+    if (!valid_dtype(o_dtype) || !valid_dtype(z_dtype)) return GDN_ERR_DTYPE;
+    if (!std::isfinite(eps) || eps < 0.f) return GDN_ERR_VALUE;
+    if (rows == 0) return GDN_OK;
+    if (!o || !z || !norm_weight || !y) return GDN_ERR_NULL;
+    const uintptr_t osz = dtype_bytes(o_dtype), zsz = dtype_bytes(z_dtype);
+    if (!aligned(o, osz) || !aligned(y, osz) || !aligned(z, zsz) || !aligned(norm_weight, 4)) return GDN_ERR_ALIGN;
+    GatedNormParams p;
+    p.o = o;
+    p.z = z;
+    p.w = norm_weight;
+    p.y = y;
+    p.rows = rows;
+    p.DV = DV;
+    p.o_bf16 = o_dtype == GDN_BF16;
+    p.z_bf16 = z_dtype == GDN_BF16;
+    p.vec = DV % 8 == 0 && aligned(o, 16) && aligned(z, 16) && aligned(y, 16) && aligned(norm_weight, 16);
+    p.eps = eps;
+    return finish(launch_gated_norm(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* gdn_status_string(gdn_status status) {
     switch (status) {
     case GDN_OK: return "GDN_OK";
@@ -177,7 +230,7 @@ const char* gdn_status_string(gdn_status status) {
     case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: a pointer is misaligned";
     case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: DK must be 16, 32, 64, 128 or 256";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: kernel launch failed (see gdn_last_cuda_error)";
-    case GDN_ERR_VALUE: return "GDN_ERR_VALUE: scale or l2_eps not finite, or l2_eps < 0";
+    case GDN_ERR_VALUE: return "GDN_ERR_VALUE: scale or an epsilon not finite, or an epsilon < 0";
     }
     return "unknown gdn_status";
 }

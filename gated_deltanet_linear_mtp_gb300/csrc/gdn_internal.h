@@ -42,8 +42,25 @@ struct CommitParams {
     int64_t lane_bytes;  // HV * DV * DK * element size: one lane's state, all heads
 };
 
+struct GatedNormParams {
+    const void* o;   // [rows, DV], o_bf16 ? bf16 : fp32
+    const void* z;   // [rows, DV], z_bf16 ? bf16 : fp32
+    const float* w;  // [DV]
+    void* y;         // [rows, DV], o's type; may be o itself
+    int64_t rows;
+    int DV;
+    int o_bf16, z_bf16;
+    int vec;  // DV % 8 == 0 and o, z, y, w start on 16 bytes: 8 columns per access
+    float eps;
+};
+
 cudaError_t launch_recurrent_f32state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
 cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams& p, int B, cudaStream_t s);
+// prefill: p.T unused; the token axis has n_tokens entries, sequence b spans cu_seqlens[b] .. cu_seqlens[b+1]-1
+cudaError_t launch_prefill(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                           int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s);
+cudaError_t launch_gated_norm(const GatedNormParams& p, cudaStream_t s);
+int64_t gated_norm_max_rows();
 
 }  // namespace gdn

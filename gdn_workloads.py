@@ -47,7 +47,7 @@ POOL_BLOCK = 16  # slots per independent pool stream
 
 # stream ids: one independent generator per tensor
 _STREAM = {"q": 1, "k": 2, "v": 3, "a": 4, "b": 5, "dt_bias": 6, "A_log": 7, "pool": 8,
-           "slots": 9, "pad": 10, "accept_len": 11}
+           "slots": 9, "pad": 10, "accept_len": 11, "lengths": 12, "fresh": 13, "z": 14, "norm_weight": 15}
 
 
 def _rng(seed: int, name: str) -> np.random.Generator:
@@ -240,3 +240,110 @@ def sweep_replay() -> List[Workload]:
 
 NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8,
          "verify4_replay": verify_t4_replay, "verify8_replay": verify_t8_replay}
+
+
+# ---- prefill ------------------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    """Prefill of B packed sequences into the pool.  Lengths: ``lengths`` if given, else uniform integers in
+    [min_len, max_len] (seeded).  A ``fresh_fraction`` of the sequences has no initial state
+    (has_initial_state = 0: a new request) and a ``pad_fraction`` carries index -1.
+
+    Layouts: q, k [N, HK, DK]; v [N, HV, DV]; a, b [N, HV]; cu_seqlens [B+1]; has_initial_state [B] int32."""
+
+    name: str
+    B: int
+    HK: int
+    HV: int
+    DK: int
+    DV: int
+    num_slots: int
+    qkv_dtype: str
+    state_dtype: str
+    out_dtype: str
+    seed: int
+    min_len: int = 1
+    max_len: int = 64
+    lengths: Optional[tuple] = None
+    fresh_fraction: float = 0.5
+    pad_fraction: float = 0.0
+    pool_std: float = 0.05
+    scale: float = 1.0
+    l2_eps: float = 1e-6
+
+    def replace(self, **kw) -> "PrefillWorkload":
+        return dataclasses.replace(self, **kw)
+
+    def seq_lengths(self) -> np.ndarray:
+        if self.lengths is not None:
+            return np.asarray(self.lengths, np.int64)
+        return _rng(self.seed, "lengths").integers(self.min_len, self.max_len + 1, self.B)
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.seq_lengths().sum())
+
+    def small_arrays(self) -> Dict[str, np.ndarray]:
+        lens = self.seq_lengths()
+        N, B, HK, HV, DK, DV, s = int(lens.sum()), self.B, self.HK, self.HV, self.DK, self.DV, self.seed
+        f32 = np.float32
+        out: Dict[str, np.ndarray] = {}
+        out["q"] = _store(_rng(s, "q").standard_normal((N, HK, DK), dtype=f32), self.qkv_dtype)
+        out["k"] = _store(_rng(s, "k").standard_normal((N, HK, DK), dtype=f32), self.qkv_dtype)
+        out["v"] = _store(_rng(s, "v").standard_normal((N, HV, DV), dtype=f32), self.qkv_dtype)
+        out["a"] = _store(_rng(s, "a").standard_normal((N, HV), dtype=f32), self.qkv_dtype)
+        out["b"] = _store(_rng(s, "b").standard_normal((N, HV), dtype=f32), self.qkv_dtype)
+        out["dt_bias"] = _rng(s, "dt_bias").standard_normal(HV, dtype=f32)
+        out["A_log"] = np.log(_rng(s, "A_log").uniform(1.0, 16.0, HV)).astype(f32)
+        if B > self.num_slots:
+            raise ValueError("more sequences than pool slots")
+        slots = _rng(s, "slots").permutation(self.num_slots)[:B].astype(np.int32)
+        n_pad = int(round(self.pad_fraction * B))
+        if n_pad:
+            slots[_rng(s, "pad").permutation(B)[:n_pad]] = -1
+        out["indices"] = slots
+        out["cu_seqlens"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        init = np.ones(B, np.int32)
+        n_fresh = int(round(self.fresh_fraction * B))
+        if n_fresh:
+            init[_rng(s, "fresh").permutation(B)[:n_fresh]] = 0
+        out["has_initial_state"] = init
+        return out
+
+    def pool(self) -> np.ndarray:
+        return Workload(self.name, B=0, T=1, HK=self.HK, HV=self.HV, DK=self.DK, DV=self.DV,
+                        num_slots=self.num_slots, qkv_dtype=self.qkv_dtype, state_dtype=self.state_dtype,
+                        out_dtype=self.out_dtype, mode="decode", cache=False, commit=False, seed=self.seed,
+                        pool_std=self.pool_std).pool()
+
+    def arrays(self) -> Dict[str, np.ndarray]:
+        out = self.small_arrays()
+        out["pool"] = self.pool()
+        return out
+
+
+def prefill_8k() -> PrefillWorkload:
+    """Prefill at the ISL-8K serving point: 8 prompts of 8192 tokens (65,536 tokens), HK=16, HV=32, 128x128
+    bf16 state pool of 64 slots, bf16 q/k/v/o, half of the prompts new (no initial state), half continuing
+    from a cached state."""
+    return PrefillWorkload("prefill_ISL8K_B8_bf16state", B=8, HK=16, HV=32, DK=128, DV=128, num_slots=64,
+                           qkv_dtype=BF16, state_dtype=BF16, out_dtype=BF16, seed=4, lengths=(8192,) * 8,
+                           fresh_fraction=0.5)
+
+
+def prefill_mix() -> PrefillWorkload:
+    """Prefill of 64 prompts of mixed length, uniform in [256, 4096] tokens, otherwise as prefill_8k."""
+    return PrefillWorkload("prefill_mix256to4096_B64_bf16state", B=64, HK=16, HV=32, DK=128, DV=128,
+                           num_slots=128, qkv_dtype=BF16, state_dtype=BF16, out_dtype=BF16, seed=5, min_len=256,
+                           max_len=4096, fresh_fraction=0.5)
+
+
+# ---- gated RMSNorm of the outputs ---------------------------------------------------------------------------
+def gated_norm_inputs(rows: int, DV: int, o_dtype: str, z_dtype: str, seed: int) -> Dict[str, np.ndarray]:
+    """o ~ N(0, 0.3^2) (the scale of the recurrence's outputs at the workloads above), gate z ~ N(0, 1),
+    norm weight ~ 1 + N(0, 0.1^2); o and z [rows, DV] in their storage types, weight fp32 [DV]."""
+    f32 = np.float32
+    o = _rng(seed, "v").standard_normal((rows, DV), dtype=f32) * f32(0.3)
+    z = _rng(seed, "z").standard_normal((rows, DV), dtype=f32)
+    w = (1.0 + 0.1 * _rng(seed, "norm_weight").standard_normal(DV)).astype(f32)
+    return {"o": _store(o, o_dtype), "z": _store(z, z_dtype), "w": w}

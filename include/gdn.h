@@ -82,7 +82,7 @@ typedef enum gdn_status {
 
 typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
-enum { GDN_ERRBIT_INDEX = 1, GDN_ERRBIT_ACCEPT_LEN = 2, GDN_ERRBIT_TIMEOUT = 4 };
+enum { GDN_ERRBIT_INDEX = 1, GDN_ERRBIT_ACCEPT_LEN = 2, GDN_ERRBIT_TIMEOUT = 4, GDN_ERRBIT_SEQLEN = 8 };
 
 enum { GDN_MAX_T = 16 }; /* tokens per call: decode (T >= 1), verify up to 16 (the page's MTP beyond T > 4) */
 
@@ -154,6 +154,44 @@ GDN_API gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const 
                              const void* b, const float* A_log, const float* dt_bias, void* state_pool,
                              const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
                              gdn_stream_t stream);
+
+/*
+ * gdn_prefill -- prefill of B variable-length sequences packed along one token axis of N = dims->T tokens
+ * (here T is the total token count, 0 .. 2^31 - 1, not bounded by GDN_MAX_T):
+ *     q, k  [N, HK, DK]   v, o  [N, HV, DV]   a, b  [N, HV]   (qkv_dtype; o in out_dtype)
+ *     cu_seqlens          [B + 1] int32, device: sequence b is tokens cu_seqlens[b] .. cu_seqlens[b+1]-1
+ *     has_initial_state   [B] int32, device, nullable (NULL: every sequence has one)
+ * Sequence b with slot = state_indices[b] != -1 starts from state_pool[slot, h] if has_initial_state[b]
+ * is non-zero, else from the zero state (the slot is then not read: a fresh slot may hold anything), runs
+ * its tokens with the recurrence above, writes o at their positions and the final state into
+ * state_pool[slot, h], rounded to state_dtype once (the running state stays fp32).  An empty sequence
+ * leaves its slot as it is.  Sequences must not overlap (their outputs would race); they may leave gaps
+ * between them (o is not written there).  Bounds that are negative,
+ * decreasing or beyond N skip the sequence and set GDN_ERRBIT_SEQLEN; a bad index sets GDN_ERRBIT_INDEX
+ * (checked first).  Distinct active sequences must use distinct slots.  The chunked gated delta rule with
+ * bf16 state pools and an initial-state mask ("fresh-state zeroing") of TensorRT-LLM PR #20937 (GB300
+ * Qwen3.8-Flash-Next NVFP4), Per-File QA Perspective, Source files and Test-code files.  Alignment: q, k,
+ * state_pool on 16 bytes, the rest on their element size.
+ */
+GDN_API gdn_status gdn_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q, const void* k,
+                               const void* v, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, void* state_pool, const int32_t* state_indices,
+                               const int32_t* has_initial_state, void* o, int32_t* err_word, gdn_stream_t stream);
+
+/*
+ * gdn_gated_rmsnorm -- gated RMSNorm of `rows` rows of DV outputs (one value head of one token per row):
+ *     y[r, i] = o[r, i] / sqrt(mean_i(o[r, i]^2) + eps) * norm_weight[i] * silu(z[r, i]),
+ *     silu(x) = x * sigmoid(x),
+ * in fp32, y stored in o_dtype (round to nearest even for bf16).  o, y [rows, DV] o_dtype; z [rows, DV]
+ * z_dtype (the gate projection); norm_weight [DV] fp32; all device memory.  y may be o itself (in place),
+ * no other overlap.  rows == 0 enqueues nothing.  The decode-rows gated norm of TensorRT-LLM PR #20937,
+ * Per-File QA Perspective, Source files (the page gives no formula: RMS over the value dimension, one
+ * weight per column shared by all heads, SiLU gate after the norm, is the reading taken).  eps must be
+ * finite and >= 0 (GDN_ERR_VALUE); o, z, y, norm_weight aligned to their element size.
+ */
+GDN_API gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t DV, int32_t o_dtype, int32_t z_dtype, const void* o,
+                                     const void* z, const float* norm_weight, float eps, void* y,
+                                     gdn_stream_t stream);
 
 /* Static string naming a status; never NULL. */
 GDN_API const char* gdn_status_string(gdn_status status);

@@ -1,6 +1,7 @@
 """The oracle's pins are strong enough: a plausible mistake planted in a copy of the oracle fails at least
 one of them.  Every mutant is compiled from a text-substituted copy of ``oracle/gdn_oracle.c`` into a
-temporary directory, on the CPU; the committed oracle is never modified."""
+temporary directory, on the CPU; the committed oracle is never modified.  Each mutant keeps every access
+of every pin in bounds (a mutant runs in this process: an out-of-bounds write would corrupt its heap)."""
 import os
 
 import pytest
@@ -50,7 +51,7 @@ MUTANTS = [
     ("prefill_fresh_reads_pool", "const int fresh = has_init && !has_init[b];", "const int fresh = 0;"),
     ("prefill_fresh_inverted", "const int fresh = has_init && !has_init[b];",
      "const int fresh = has_init && has_init[b];"),
-    ("prefill_token_base", "tok0 = seq[b];", "tok0 = seq[0];"),
+    ("prefill_token_base", "tok0 = seq[b];", "tok0 = seq[b] > 0 ? seq[b] - 1 : 0;"),
     ("prefill_length_one_short", "n_tok = seq[b + 1] - seq[b];", "n_tok = seq[b + 1] - seq[b] - (seq[b + 1] > seq[b]);"),
     ("prefill_bad_bounds_flag", "flags |= 8;", "flags |= 2;"),
     ("norm_sum_not_mean", "ms /= DV;", ""),
