@@ -143,25 +143,31 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def kernel_source_hash() -> str:
+PREFILL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_prefill.cu",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh"]
+NORM_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_gated_norm.cu"]
+
+
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(role: str, workload_name: str):
+def recorded_traffic(role: str, workload_name: str, sources=None):
     """DRAM bytes per launch of the kernel in `role` from the committed ncu summary
     ``profiles/<role>_<workload>.md``, if it was taken on the current kernel sources
-    (``kernel_source_sha256`` line); else None."""
+    (``kernel_source_sha256`` line, over `sources`); else None."""
     p = os.path.join(ROOT, "profiles", f"{role}_{workload_name}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
     m_tr = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash(sources):
         return None
     return float(m_tr.group(1))
 
@@ -710,7 +716,8 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"derived: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
                                     f"flops x {max_mhz:.0f} MHz (maximum SM clock)",
-                     "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us, "traffic": None},
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us,
+                     "traffic": recorded_traffic("prefill", pw.name, PREFILL_SOURCES)},
         "e2e": {"value": sum_over_ranks(active_tokens, dist, device) / (e2e_ms_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "gpu_launches": args.steps, "clocks": clocks, "device": props.name,
@@ -775,7 +782,8 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
         "roofline": {"kernel": "gdn_gated_rmsnorm_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
-                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_us": avg_us, "traffic": None},
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_us": avg_us,
+                     "traffic": recorded_traffic("gated_norm", f"gated_rmsnorm_rows{rows}_DV{DV}_bf16", NORM_SOURCES)},
         "e2e": {"value": rows * world / (e2e_ms_step * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": 2 * rows * DV * 2, "d2h_bytes_per_step": rows * DV * 2,
                 "ms_per_step": e2e_ms_step},

@@ -179,3 +179,44 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         gdn.lib()
+
+
+# ---- prefill and the gated norm: host-side checks (status before any CUDA call) --------------------------
+def prefill(L, d, **ptrs):
+    a = dict(cu=P, q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, init=None, o=P, err=None)
+    a.update(ptrs)
+    return L.gdn_prefill(ctypes.byref(d) if d is not None else None, a["cu"], a["q"], a["k"], a["v"], a["a"],
+                         a["b"], a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["init"], a["o"], a["err"], None)
+
+
+def test_prefill_host_validation(L):
+    assert prefill(L, None) == 1
+    assert prefill(L, dims(T=-1)) == 2                      # T is the total token count: >= 0
+    assert prefill(L, dims(B=0, T=100)) == 0                # no sequences: nothing enqueued
+    assert prefill(L, dims(B=4, T=0)) == 0                  # no tokens: nothing enqueued
+    assert prefill(L, dims(T=100), cu=None) == 1
+    assert prefill(L, dims(T=100), o=None) == 1
+    assert prefill(L, dims(T=100), init=ODD) == 4
+    assert prefill(L, dims(T=100), cu=ODD) == 4
+    assert prefill(L, dims(T=100), q=ODD) == 4
+    assert prefill(L, dims(T=100, HV=3)) == 2               # HV % HK
+    assert prefill(L, dims(T=100, DK=48)) == 5
+    assert prefill(L, dims(T=100, qkv_dtype=7)) == 3
+    assert prefill(L, dims(T=100, l2_eps=-1.0)) == 7
+
+
+def norm(L, rows=16, DV=128, od=1, zd=1, o=P, z=P, w=P, eps=1e-6, y=P2):
+    return L.gdn_gated_rmsnorm(rows, DV, od, zd, o, z, w, ctypes.c_float(eps), y, None)
+
+
+def test_gated_rmsnorm_host_validation(L):
+    assert norm(L, rows=-1) == 2
+    assert norm(L, DV=0) == 2
+    assert norm(L, rows=1 << 60) == 2                       # beyond the launchable row count
+    assert norm(L, od=2) == 3 and norm(L, zd=-1) == 3
+    assert norm(L, eps=-1e-3) == 7 and norm(L, eps=float("inf")) == 7 and norm(L, eps=float("nan")) == 7
+    assert norm(L, rows=0, o=None, z=None, w=None, y=None) == 0
+    assert norm(L, o=None) == 1 and norm(L, z=None) == 1 and norm(L, w=None) == 1 and norm(L, y=None) == 1
+    assert norm(L, o=ctypes.c_void_p(0x10001)) == 4         # bf16 o on an odd address
+    assert norm(L, od=0, o=ODD) == 4                        # fp32 o on 2 bytes
+    assert norm(L, w=ODD) == 4
