@@ -33,16 +33,17 @@
  *   - Every pointer is DEVICE memory owned by the caller.  The library allocates nothing, keeps no state
  *     between calls besides launch-configuration caches (atomic, filled on first use), never synchronises,
  *     and enqueues its work asynchronously on `stream` (0 = legacy default stream).  Calls are thread-safe.
- *     A call with B == 0 enqueues nothing and returns GDN_OK.
+ *     A call with B == 0 (prefill: or no tokens; gated norm: rows == 0) enqueues nothing and returns GDN_OK.
  *   - Alignment: q, k, state_pool and intermediate_states start on 16 bytes; the other arrays on their
  *     element size.  Outputs must not overlap inputs (decode updates state_pool in place by design).
  *   - Errors the host can see are returned as a status before anything is enqueued.  Errors that depend on
- *     device data are defined, never a fault: a lane whose index is < -1 or >= num_slots, or (commit) whose
- *     accept length is outside 0..T, is skipped and a bit is OR-ed into *err_word (if err_word is not NULL):
- *     GDN_ERRBIT_INDEX, GDN_ERRBIT_ACCEPT_LEN.  No kernel waits on another CTA or on a flag; the only waits
- *     are on the CTA's own bulk copies of state into shared memory, and they are bounded: one that runs
- *     out sets GDN_ERRBIT_TIMEOUT and that part of the state is left unprocessed.  The caller zeroes
- *     *err_word and reads it when it wants.
+ *     device data are defined, never a fault: a lane whose index is < -1 or >= num_slots, (commit) whose
+ *     accept length is outside 0..T, or (prefill) whose token bounds are negative, decreasing or beyond the
+ *     token count, is skipped and a bit is OR-ed into *err_word (if err_word is not NULL):
+ *     GDN_ERRBIT_INDEX, GDN_ERRBIT_ACCEPT_LEN, GDN_ERRBIT_SEQLEN.  No kernel waits on another CTA or on a
+ *     flag; the only waits are on the CTA's own bulk copies of state into shared memory, and they are
+ *     bounded: one that runs out sets GDN_ERRBIT_TIMEOUT and that part of the state is left unprocessed.
+ *     The caller zeroes *err_word and reads it when it wants.
  *   - Padded lanes (index -1, the padding index guard of FlashInfer #2810, same page, Requirements) are
  *     skipped: their o, intermediate states and pool slots are left untouched, bit for bit.
  *   - Distinct active lanes must use distinct slots in gdn_decode and gdn_commit (they write the pool);

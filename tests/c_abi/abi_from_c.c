@@ -36,6 +36,21 @@ int main(void) {
     EXPECT(gdn_commit(&d, p, p, (void*)(uintptr_t)0x10002, p, NULL, NULL) == GDN_ERR_ALIGN);
     d.B = 0;
     EXPECT(gdn_commit(&d, NULL, NULL, NULL, NULL, NULL, NULL) == GDN_OK);
+    /* prefill: T is the packed token count (beyond GDN_MAX_T); the device-side arrays are plain int32 */
+    d.B = 4; d.T = 4096;
+    EXPECT(gdn_prefill(&d, NULL, p, p, p, p, p, p, p, p, p, NULL, p, NULL, NULL) == GDN_ERR_NULL);
+    EXPECT(gdn_prefill(&d, p, p, p, p, p, p, p, p, p, p, (const int32_t*)(uintptr_t)0x10002, p, NULL, NULL) ==
+           GDN_ERR_ALIGN);
+    d.T = -1;
+    EXPECT(gdn_prefill(&d, p, p, p, p, p, p, p, p, p, p, NULL, p, NULL, NULL) == GDN_ERR_SHAPE);
+    d.T = 0;
+    EXPECT(gdn_prefill(&d, p, p, p, p, p, p, p, p, p, p, NULL, p, NULL, NULL) == GDN_OK);
+    /* gated norm: explicit sizes and dtypes */
+    EXPECT(gdn_gated_rmsnorm(0, 128, GDN_BF16, GDN_BF16, NULL, NULL, NULL, 1e-6f, NULL, NULL) == GDN_OK);
+    EXPECT(gdn_gated_rmsnorm(16, 128, GDN_BF16, GDN_BF16, p, p, p, -1.0f, p, NULL) == GDN_ERR_VALUE);
+    EXPECT(gdn_gated_rmsnorm(16, 0, GDN_BF16, GDN_BF16, p, p, p, 1e-6f, p, NULL) == GDN_ERR_SHAPE);
+    EXPECT(gdn_gated_rmsnorm(16, 128, 5, GDN_BF16, p, p, p, 1e-6f, p, NULL) == GDN_ERR_DTYPE);
+    EXPECT(gdn_gated_rmsnorm(16, 128, GDN_BF16, GDN_BF16, p, NULL, p, 1e-6f, p, NULL) == GDN_ERR_NULL);
     EXPECT(gdn_last_cuda_error() == 0);
     if (failures == 0) printf("abi_from_c: ok\n");
     return failures == 0 ? 0 : 1;
