@@ -139,7 +139,8 @@ def _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale,
     _shape(b, (B, T, HV), "b")
     _shape(A_log, (HV,), "A_log")
     _shape(dt_bias, (HV,), "dt_bias")
-    _shape(state_indices, (B,), "state_indices")
+    if state_indices is not None:  # None: the caller checks the indices (prefill: one per prompt)
+        _shape(state_indices, (B,), "state_indices")
     num_slots = state_pool.shape[0]
     _shape(state_pool, (num_slots, HV, DV, DK), "state_pool")
     qkv = _code(q, "q")
@@ -149,7 +150,7 @@ def _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale,
     for t, n in ((A_log, "A_log"), (dt_bias, "dt_bias")):
         if t.dtype != torch.float32:
             raise TypeError(f"{n} must be fp32")
-    if state_indices.dtype != torch.int32:
+    if state_indices is not None and state_indices.dtype != torch.int32:
         raise TypeError("state_indices must be int32")
     out = _code(o, "o") if o is not None else _code(state_pool, "state_pool")
     return GdnDims(B, T, HK, HV, DK, DV, num_slots, qkv, _code(state_pool, "state_pool"), out, float(scale),
@@ -247,11 +248,12 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seq
         raise ValueError("cu_seqlens is [B+1]")
     if cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
-    # the [B, T] checks of the other calls, with the token axis as T and one "lane"
+    # the [B, T] checks of the other calls, with the token axis as T of one "lane"; the indices are per prompt
     d = _io_dims(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), a.unsqueeze(0), b.unsqueeze(0), A_log, dt_bias,
-                 state_pool, state_indices[:1] if B > 0 else torch.zeros(1, dtype=torch.int32, device=q.device),
-                 o.unsqueeze(0), scale, l2_eps)
+                 state_pool, None, o.unsqueeze(0), scale, l2_eps)
     _shape(state_indices, (B,), "state_indices")
+    if state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
     if has_initial_state is not None:
         _shape(has_initial_state, (B,), "has_initial_state")
         if has_initial_state.dtype != torch.int32:

@@ -220,3 +220,36 @@ def test_gated_rmsnorm_host_validation(L):
     assert norm(L, o=ctypes.c_void_p(0x10001)) == 4         # bf16 o on an odd address
     assert norm(L, od=0, o=ODD) == 4                        # fp32 o on 2 bytes
     assert norm(L, w=ODD) == 4
+
+
+# ---- the Python binding rejects bad shapes and dtypes before taking any pointer (CPU tensors suffice) -----
+def test_binding_prefill_and_norm_argument_checks():
+    import torch
+
+    N, HK, HV, DK, DV = 10, 2, 4, 16, 8
+    bf = torch.bfloat16
+    q, v, ab = torch.zeros(N, HK, DK, dtype=bf), torch.zeros(N, HV, DV, dtype=bf), torch.zeros(N, HV, dtype=bf)
+    A, pool = torch.zeros(HV), torch.zeros(3, HV, DV, DK, dtype=bf)
+    o, cu = torch.zeros(N, HV, DV, dtype=bf), torch.tensor([0, 4, 10], dtype=torch.int32)
+    idx = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        gdn.gdn_prefill(q, q, v, ab, ab, A, A, pool, idx.long(), cu, o)
+    with pytest.raises(ValueError):
+        gdn.gdn_prefill(q, q, v, ab, ab, A, A, pool, torch.zeros(3, dtype=torch.int32), cu, o)
+    with pytest.raises(TypeError):
+        gdn.gdn_prefill(q, q, v, ab, ab, A, A, pool, idx, cu.long(), o)
+    with pytest.raises(ValueError):
+        gdn.gdn_prefill(q.unsqueeze(0), q, v, ab, ab, A, A, pool, idx, cu, o)  # [B, T, ...] layout: not packed
+    with pytest.raises(ValueError):
+        gdn.gdn_prefill(q, q, v, ab, ab, A, A, pool, idx, cu, o[:5])
+    with pytest.raises(TypeError):
+        gdn.gdn_prefill(q, q, v, ab, ab, A, A, pool, idx, cu, o, torch.ones(2, dtype=torch.bool))
+    z = torch.zeros(N * HV, DV, dtype=bf)
+    with pytest.raises(ValueError):
+        gdn.gdn_gated_rmsnorm(z, z[:3], torch.ones(DV))
+    with pytest.raises(TypeError):
+        gdn.gdn_gated_rmsnorm(z, z, torch.ones(DV, dtype=bf))
+    with pytest.raises(ValueError):
+        gdn.gdn_gated_rmsnorm(z, z, torch.ones(DV + 1))
+    with pytest.raises(TypeError):
+        gdn.gdn_gated_rmsnorm(z, z, torch.ones(DV), torch.zeros(N * HV, DV))
