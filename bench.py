@@ -602,6 +602,29 @@ def _timed_calls(call, K: int, warmup: int, stream, sampler):
     return [e[0].elapsed_time(e[1]) for e in evs], t_wall
 
 
+def _prefill_pairs(pw, x):
+    """(prompt, value head) pairs of the active prompts, in order."""
+    return [(b, h) for b in range(pw.B) if x["indices"][b] >= 0 for h in range(pw.HV)]
+
+
+def _prefill_pair(orc, pw, x, b: int, h: int, max_tokens=None):
+    """The oracle's prefill of prompt b, value head h alone (its first max_tokens tokens if given), on a copy
+    of its slot; returns the tokens run."""
+    cu = x["cu_seqlens"]
+    lo, hi, hk, slot = int(cu[b]), int(cu[b + 1]), h // (pw.HV // pw.HK), int(x["indices"][b])
+    if max_tokens is not None:
+        hi = min(hi, lo + max_tokens)
+    d = dict(T=0, HK=1, HV=1, DK=pw.DK, DV=pw.DV, num_slots=1, qkv_dtype=pw.qkv_dtype, state_dtype=pw.state_dtype,
+             scale=pw.scale, l2_eps=pw.l2_eps)
+    y = dict(q=np.ascontiguousarray(x["q"][lo:hi, hk:hk + 1]), k=np.ascontiguousarray(x["k"][lo:hi, hk:hk + 1]),
+             v=np.ascontiguousarray(x["v"][lo:hi, h:h + 1]), a=np.ascontiguousarray(x["a"][lo:hi, h:h + 1]),
+             b=np.ascontiguousarray(x["b"][lo:hi, h:h + 1]), A_log=np.ascontiguousarray(x["A_log"][h:h + 1]),
+             dt_bias=np.ascontiguousarray(x["dt_bias"][h:h + 1]), indices=np.zeros(1, np.int32))
+    pool = np.ascontiguousarray(x["pool"][slot:slot + 1, h:h + 1])
+    orc.prefill(d, y, np.array([0, hi - lo], np.int32), pool, np.array([x["has_initial_state"][b]], np.int32))
+    return hi - lo
+
+
 def _prefill_cpu_baseline(pw, x, seconds: float):
     """The oracle as it stands (one thread, fp64 C loops) on (prompt, head) pairs in order -- each a whole
     prompt for one value head -- until about `seconds` of CPU work; tokens/s of the layer = pair tokens / HV
@@ -609,21 +632,10 @@ def _prefill_cpu_baseline(pw, x, seconds: float):
     import oracle
 
     orc = oracle.default()
-    r = pw.HV // pw.HK
-    d = dict(T=0, HK=1, HV=1, DK=pw.DK, DV=pw.DV, num_slots=1, qkv_dtype=pw.qkv_dtype, state_dtype=pw.state_dtype,
-             scale=pw.scale, l2_eps=pw.l2_eps)
-    cu = x["cu_seqlens"]
-    pairs = [(b, h) for b in range(pw.B) if x["indices"][b] >= 0 for h in range(pw.HV)]
+    pairs = _prefill_pairs(pw, x)
     done_tokens, n_pairs, t0 = 0, 0, time.perf_counter()
     for b, h in pairs:
-        lo, hi, hk, slot = int(cu[b]), int(cu[b + 1]), h // r, int(x["indices"][b])
-        y = dict(q=np.ascontiguousarray(x["q"][lo:hi, hk:hk + 1]), k=np.ascontiguousarray(x["k"][lo:hi, hk:hk + 1]),
-                 v=np.ascontiguousarray(x["v"][lo:hi, h:h + 1]), a=np.ascontiguousarray(x["a"][lo:hi, h:h + 1]),
-                 b=np.ascontiguousarray(x["b"][lo:hi, h:h + 1]), A_log=np.ascontiguousarray(x["A_log"][h:h + 1]),
-                 dt_bias=np.ascontiguousarray(x["dt_bias"][h:h + 1]), indices=np.zeros(1, np.int32))
-        pool = np.ascontiguousarray(x["pool"][slot:slot + 1, h:h + 1])
-        orc.prefill(d, y, np.array([0, hi - lo], np.int32), pool, np.array([x["has_initial_state"][b]], np.int32))
-        done_tokens += hi - lo
+        done_tokens += _prefill_pair(orc, pw, x, b, h)
         n_pairs += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -795,6 +807,75 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
     return result
 
 
+def run_prefill_reference_arm(args, pw, rank: int, world: int):
+    """The reference arm of a prefill workload: the oracle, each step the first L tokens of prompt 0 for one
+    value head, L sized so that warm-up + steps take about --ref-seconds.  tokens/s = L / HV / step time."""
+    if rank != 0:
+        return
+    import oracle
+
+    orc = oracle.default()
+    x = pw.arrays()
+    b, h = _prefill_pairs(pw, x)[0]
+    n_seq = int(x["cu_seqlens"][b + 1] - x["cu_seqlens"][b])
+    probe = min(64, n_seq)
+    t0 = time.perf_counter()
+    _prefill_pair(orc, pw, x, b, h, probe)
+    t_tok = max((time.perf_counter() - t0) / probe, 1e-9)
+    L = int(max(1, min(n_seq, args.ref_seconds / (args.steps + args.warmup) / t_tok)))
+    for _ in range(args.warmup):
+        _prefill_pair(orc, pw, x, b, h, L)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _prefill_pair(orc, pw, x, b, h, L)
+    dt = time.perf_counter() - t0
+    v = L / pw.HV * args.steps / dt
+    desc = (f"each step: oracle prefill of the first {L} tokens of prompt {b}, value head {h} of {pw.name} (1 of "
+            f"{pw.HV} heads), fp64 C loops, one thread; tokens/s = L / HV / time")
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": pw.name},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_norm_reference_arm(args, rank: int, world: int, rows: int = 65536 * 32, DV: int = 128):
+    """The reference arm of the gated norm: the oracle on the first n rows each step, n sized so that
+    warm-up + steps take about --ref-seconds."""
+    if rank != 0:
+        return
+    import oracle
+
+    orc = oracle.default()
+    g = W.gated_norm_inputs(rows, DV, "bf16", "bf16", seed=17)
+
+    def run(n):
+        orc.gated_rmsnorm(g["o"][:n], "bf16", g["z"][:n], "bf16", g["w"], 1e-6)
+
+    t0 = time.perf_counter()
+    run(256)
+    t_row = max((time.perf_counter() - t0) / 256, 1e-9)
+    n = int(max(1, min(rows, args.ref_seconds / (args.steps + args.warmup) / t_row)))
+    for _ in range(args.warmup):
+        run(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(n)
+    dt = time.perf_counter() - t0
+    v = n * args.steps / dt
+    desc = f"each step: oracle gated norm of the first {n} of {rows} rows of DV={DV}, fp64 C loops, one thread"
+    print(json.dumps({
+        "impl": "reference", "metric": NORM_METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"gated_rmsnorm_rows{rows}_DV{DV}_bf16"},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 # ---- the oracle as CPU baseline / reference arm -----------------------------------------------------------
 def oracle_pairs(w: W.Workload, x: dict, pairs):
     """Per (lane, value head) inputs for the oracle: one lane, one head, its own one-slot pool copy."""
@@ -909,9 +990,10 @@ def main(argv=None):
     rank, world, local_rank = dist_env()
     if args.workload in PREFILL_NAMED or args.workload == "gated_norm":
         if args.impl == "reference":
-            if rank == 0:
-                print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the verify "
-                                  "workloads; prefill and the gated norm report the oracle as cpu_baseline"}))
+            if args.workload == "gated_norm":
+                run_norm_reference_arm(args, rank, world)
+            else:
+                run_prefill_reference_arm(args, PREFILL_NAMED[args.workload](), rank, world)
             return 0
         if args.workload == "gated_norm":
             run_norm_arm(args, rank, world, local_rank)

@@ -136,3 +136,38 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     with redirect_stdout(buf):
         assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"]) == 0
     assert buf.getvalue() == ""
+
+
+def test_prefill_and_norm_reference_arms_small():
+    """The oracle arms of the prefill and gated-norm lines, on small inputs: one JSON line each, the oracle as
+    the reference, nothing copied."""
+    import argparse
+
+    args = argparse.Namespace(steps=3, warmup=3, ref_seconds=1.0)
+    pw = W.PrefillWorkload("prefill_small", B=3, HK=2, HV=4, DK=16, DV=16, num_slots=5, qkv_dtype="bf16",
+                           state_dtype="bf16", out_dtype="bf16", seed=9, lengths=(20, 0, 7), pad_fraction=0.0)
+    for run, unit, name in ((lambda: bench.run_prefill_reference_arm(args, pw, 0, 1), "tokens/s", pw.name),
+                            (lambda: bench.run_norm_reference_arm(args, 0, 1, rows=512, DV=64), "rows/s",
+                             "gated_rmsnorm_rows512_DV64_bf16")):
+        buf = io.StringIO()
+        with redirect_stdout(buf):
+            run()
+        j = json.loads(buf.getvalue().strip().splitlines()[-1])
+        assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == unit
+        assert j["config"]["workload"] == name and j["cpu_baseline"]["kind"] == "oracle"
+        assert j["e2e"]["h2d_bytes_per_step"] == 0
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_prefill_reference_arm(args, pw, 1, 2)  # other ranks do no work
+    assert buf.getvalue() == ""
+
+
+def test_prefill_cpu_baseline_small():
+    pw = W.PrefillWorkload("prefill_small", B=2, HK=1, HV=2, DK=16, DV=16, num_slots=4, qkv_dtype="f32",
+                           state_dtype="f32", out_dtype="f32", seed=10, lengths=(5, 9))
+    cb = bench._prefill_cpu_baseline(pw, pw.arrays(), 0.01)
+    assert cb["value"] > 0 and cb["kind"] == "oracle" and cb["cores"] == 1
+
+
+def test_alu_peak_derivation():
+    assert abs(bench.alu_peak_tflops(152, 2070) - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
