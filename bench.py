@@ -19,6 +19,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -213,15 +214,19 @@ class ClockSampler:
             self.source = "nvidia-smi"
             self._bus = None
 
+    class _Util(ctypes.Structure):
+        _fields_ = [("gpu", ctypes.c_uint), ("memory", ctypes.c_uint)]
+
     def _sample_nvml(self):
         nv, h = self._nvml, self._handle
-        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        clk, pw, rs, ut = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), self._Util()
         while not self._stop.is_set():
             ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
             nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
             self._reasons_fn(h, ctypes.byref(rs))
+            util = ut.gpu if nv.nvmlDeviceGetUtilizationRates(h, ctypes.byref(ut)) == 0 else -1
             if ok:
-                self.samples.append((clk.value, pw.value / 1000.0, int(rs.value)))
+                self.samples.append((clk.value, pw.value / 1000.0, int(rs.value), util))
             time.sleep(self.period)
 
     def start(self):
@@ -231,8 +236,9 @@ class ClockSampler:
         else:
             try:
                 self._proc = subprocess.Popen(
-                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
-                     "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE, text=True)
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                     "utilization.gpu", "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE,
+                    text=True)
             except Exception:
                 self._proc = None
 
@@ -245,22 +251,29 @@ class ClockSampler:
             out, _ = self._proc.communicate()
             for line in out.splitlines():
                 try:
-                    c, m, p, r = [x.strip() for x in line.split(",")]
-                    self.samples.append((float(c), float(p), int(r, 16)))
+                    c, m, p, r, u = [x.strip() for x in line.split(",")]
+                    self.samples.append((float(c), float(p), int(r, 16), float(u)))
                     self.max_mhz = float(m)
                 except Exception:
                     pass
 
     def summary(self):
+        """Median SM clock over the samples taken while the GPU was busy (all samples if utilisation is not
+        readable), the clock-event reasons seen in any sample, and the sample counts."""
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.source}
-        clocks = [s[0] for s in self.samples]
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "samples_under_load": 0, "source": self.source}
+        loaded = [s for s in self.samples if s[3] > 0]
+        readable = any(s[3] >= 0 for s in self.samples)
+        basis = loaded if loaded else self.samples
         bits = 0
         for s in self.samples:
             bits |= s[2]
         reasons = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(clocks), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                "samples": len(self.samples), "power_w_max": max(s[1] for s in self.samples), "source": self.source}
+        return {"sm_mhz": statistics.median(s[0] for s in basis), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "samples_under_load": len(loaded) if readable else None,
+                "sm_mhz_min": min(s[0] for s in basis), "power_w_max": max(s[1] for s in self.samples),
+                "period_ms": self.period * 1e3, "source": self.source}
 
 
 # ---- the CUDA arm -----------------------------------------------------------------------------------------
@@ -365,11 +378,12 @@ class Step:
 
     E2E_GRAPH_STEPS = 32
 
-    def run_e2e(self, K: int, warmup: int, comp) -> float:
+    def run_e2e(self, K: int, warmup: int, comp, min_seconds: float = 0.0):
         """Pipelined steps through the public calls, captured once as a CUDA graph of E2E_GRAPH_STEPS steps and
-        replayed; returns the device time per step (ms), from before the first copy in to after the last copy
-        out.  Step i: copy in (H2D stream) -> verify/decode + commit (compute stream) -> copy o out (D2H
-        stream); step i+1's copy in runs during step i's compute."""
+        replayed at least K steps and at least `min_seconds`; returns (device time per step in ms, from before
+        the first copy in to after the last copy out; steps timed).  Step i: copy in (H2D stream) ->
+        verify/decode + commit (compute stream) -> copy o out (D2H stream); step i+1's copy in runs during
+        step i's compute."""
         torch = self.torch
         G = self.E2E_GRAPH_STEPS
         h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
@@ -410,17 +424,21 @@ class Step:
         with torch.cuda.graph(graph, stream=cap):
             steps(cap)
         torch.cuda.synchronize()
-        graph.replay()
-        torch.cuda.synchronize()
-        reps = max(1, -(-K // G))
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(comp):
+            t0.record(comp)
+            graph.replay()
+            t1.record(comp)
+        torch.cuda.synchronize()
+        one_ms = max(t0.elapsed_time(t1), 1e-3)
+        reps = max(1, -(-K // G), int(math.ceil(min_seconds * 1e3 / one_ms)))
         with torch.cuda.stream(comp):
             t0.record(comp)
             for _ in range(reps):
                 graph.replay()
             t1.record(comp)
         torch.cuda.synchronize()
-        return t0.elapsed_time(t1) / (reps * G)
+        return t0.elapsed_time(t1) / (reps * G), reps * G
 
     @property
     def launches_per_step(self) -> int:
@@ -428,30 +446,64 @@ class Step:
 
 
 _POOL_CACHE: dict = {}
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal (~8 TB/s); the specification's >= 70 % target is against it
+MIN_WINDOW_S = 1.0        # each point's timed region covers at least this much device time
 
 
-def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, emit=True):
+def roofline_block(kernel: dict, peak: float, peak_src: str, traffic) -> dict:
+    """Roofline of the dominant kernel: against the measured copy peak (frac) and the nominal 8 TB/s
+    (frac_nominal, the basis of the >= 0.70 target)."""
+    return {
+        "kernel": f"{kernel['kernel']} ({kernel['role']})",
+        "bound": "hbm",
+        "achieved": kernel["achieved_gbs"],
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": kernel["frac"],
+        "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
+        "nominal_peak": NOMINAL_HBM_GBS,
+        "frac_nominal": kernel["achieved_gbs"] / NOMINAL_HBM_GBS,
+        "target_basis": "frac_nominal (>= 0.70 of the nominal ~8 TB/s on verify T=4 B=128 bf16 state)",
+        "algorithmic_bytes_per_launch": kernel["algorithmic_bytes"],
+        "avg_launch_us": kernel["avg_us"],
+        "traffic": traffic,
+    }
+
+
+class _Flush:
+    """Write a buffer larger than L2 (evicts everything), then read another one so that the lines left in L2
+    are clean and the timed step does not pay for writing the flush's dirty lines back."""
+
+    def __init__(self, device):
+        import torch
+
+        props = torch.cuda.get_device_properties(device)
+        n = max(256 << 20, 2 * props.L2_cache_size) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        self.r = torch.zeros(n, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        self.r.sum()
+
+
+def measure_point(args, w: W.Workload, rank: int, world: int, local_rank: int, dist, min_seconds: float,
+                  e2e: bool = True, steps: int = None) -> dict:
+    """One workload on this rank's GPU: W warm-up steps, then R x K timed steps (R chosen from the warm-up
+    so that the timed region covers at least `min_seconds` of device time; the same R on every rank), each
+    step bracketed by CUDA events with an L2 flush before it, outside the events.  Then the end-to-end leg
+    (`e2e`).  Returns the result record (no CPU baseline)."""
     import torch
 
-    torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    dist = init_dist(world, "nccl")
+    K = args.steps if steps is None else steps
     wr = rank_workload(w, rank)
-    st = Step(wr, device, _POOL_CACHE if args.workload.startswith("sweep") else None)
-    props = torch.cuda.get_device_properties(device)
-    nflush = max(256 << 20, 2 * props.L2_cache_size) // 4
-    flush_w = torch.empty(nflush, dtype=torch.float32, device=device)
-    flush_r = torch.zeros(nflush, dtype=torch.float32, device=device)
+    st = Step(wr, device, _POOL_CACHE if w.pool_seed is not None else None)
+    flush = _Flush(device)
     stream = torch.cuda.current_stream(device)
 
-    def flush_l2():
-        # write a buffer larger than L2 (evicts everything), then read another one so that the lines left
-        # in L2 are clean and the timed step does not pay for writing the flush's dirty lines back
-        flush_w.fill_(1.0)
-        flush_r.sum()
-
     def one(ev=None):
-        flush_l2()
+        flush()
         if ev is not None:
             ev[0].record(stream)
         st.recurrent()
@@ -461,45 +513,53 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
         if ev is not None:
             ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        one()
+    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.warmup)]
+    for i in range(args.warmup):
+        one(wev[i])
     torch.cuda.synchronize()
     if st.err.item() != 0:
-        raise RuntimeError(f"device error word {st.err.item()} after warm-up")
-
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        raise RuntimeError(f"device error word {st.err.item()} after warm-up ({w.name})")
+    warm_ms = statistics.median(e[0].elapsed_time(e[2]) for e in wev)
+    R = max(1, int(math.ceil(min_seconds * 1e3 / max(K * warm_ms, 1e-6))))
+    R = int(max_over_ranks(R, dist, device))
+    n = R * K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     sampler = ClockSampler(local_rank)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
     t_wall = time.perf_counter()
-    for i in range(K):
+    for i in range(n):
         one(evs[i])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     sampler.stop()
     if dist is not None:
         dist.barrier()
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error word {st.err.item()} after the timed steps ({w.name})")
     rec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    com_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), dist, device)
-    tokens_rank = st.A * wr.T * K
-    tokens_all = sum_over_ranks(tokens_rank, dist, device)
+    tokens_all = sum_over_ranks(st.A * wr.T * n, dist, device)
 
-    # end-to-end: every step's inputs copied in from pinned host memory and its o copied back, pipelined
-    if dist is not None:
-        dist.barrier()
-    e2e_ms_step = max_over_ranks(st.run_e2e(K, args.warmup, stream), dist, device)
-    tokens_step_all = sum_over_ranks(st.A * wr.T, dist, device)
-    if st.err.item() != 0:
-        raise RuntimeError(f"device error word {st.err.item()} after the end-to-end leg")
+    e2e_rec = None
+    if e2e:
+        if dist is not None:
+            dist.barrier()
+        e2e_ms, e2e_steps = st.run_e2e(K, args.warmup, stream, min_seconds)
+        e2e_ms_step = max_over_ranks(e2e_ms, dist, device)
+        if st.err.item() != 0:
+            raise RuntimeError(f"device error word {st.err.item()} after the end-to-end leg ({w.name})")
+        e2e_rec = {"value": sum_over_ranks(st.A * wr.T, dist, device) / (e2e_ms_step * 1e-3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes,
+                   "ms_per_step": e2e_ms_step, "timed_steps": e2e_steps}
 
     peak, peak_src = hbm_peak()
     rb = recurrent_bytes(wr, st.A)
     cb = commit_bytes(wr, st.A, st.accepted) if wr.commit else 0
-    com_ms = [e[1].elapsed_time(e[2]) for e in evs]
     role = "decode" if w.mode == "decode" else "verify"
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     kernels = [{"role": role, "kernel": kernel_name(wr, role, sms), "avg_us": statistics.mean(rec_ms) * 1e3,
@@ -511,17 +571,19 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
     for k in kernels:
         k["achieved_gbs"] = k["algorithmic_bytes"] / (k["avg_us"] * 1e-6) / 1e9
         k["frac"] = k["achieved_gbs"] / peak
+        k["frac_nominal"] = k["achieved_gbs"] / NOMINAL_HBM_GBS
     dom = max(kernels, key=lambda k: k["avg_us"])
-    step_bytes = rb + cb
-    clocks = sampler.summary()
+    props = torch.cuda.get_device_properties(device)
     result = {
         "metric": METRIC,
         "value": tokens_all / (total_ms * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
+        "repeats": R,
+        "timed_steps": n,
         "warmup": args.warmup,
-        "ms_per_step": total_ms / K,
+        "ms_per_step": total_ms / n,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -535,35 +597,71 @@ def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, em
                 (" + gdn_commit_replay" if w.commit_mode == "replay" else " + gdn_commit") if w.commit else "")),
             "l2": "flushed before every step outside its CUDA events (256 MiB write, then 256 MiB read: clean lines)",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
-            "timing": "CUDA events per step on the launch stream, summed; max over ranks",
+            "timing": (f"CUDA events per step on the launch stream, summed over {R} x {K} steps (the timed region "
+                       f"covers >= {min_seconds:g} s of device time); max over ranks"),
             "e2e": (f"pipelined: each step's inputs copied in from pinned host memory (one packed copy) and its o "
                     f"copied back, on H2D / D2H streams beside the compute stream, {st.E2E_GRAPH_STEPS} steps captured "
-                    f"as one CUDA graph and replayed; no L2 flush: steps rotate over {st.e2e_sets} disjoint sets of "
-                    f"pool slots"),
+                    f"as one CUDA graph and replayed for >= {min_seconds:g} s; no L2 flush: steps rotate over "
+                    f"{st.e2e_sets} disjoint sets of pool slots") if e2e else None,
         },
-        "verify_steps_per_s": K * world / (total_ms * 1e-3),
-        "hbm_gbs_step": step_bytes * world * K / (total_ms * 1e-3) / 1e9,
-        "roofline": {
-            "kernel": f"{dom['kernel']} ({dom['role']})",
-            "bound": "hbm",
-            "achieved": dom["achieved_gbs"],
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": dom["frac"],
-            "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
-            "algorithmic_bytes_per_launch": dom["algorithmic_bytes"],
-            "avg_launch_us": dom["avg_us"],
-            "traffic": recorded_traffic(dom["role"], w.name),
-        },
+        "verify_steps_per_s": n * world / (total_ms * 1e-3),
+        "hbm_gbs_step": (rb + cb) * world * n / (total_ms * 1e-3) / 1e9,
+        "roofline": roofline_block(dom, peak, peak_src, recorded_traffic(dom["role"], w.name)),
         "kernels": kernels,
-        "e2e": {"value": tokens_step_all / (e2e_ms_step * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": st.h2d_bytes,
-                "d2h_bytes_per_step": st.d2h_bytes, "ms_per_step": e2e_ms_step},
-        "gpu_launches": st.launches_per_step * K,
-        "clocks": clocks,
+        "e2e": e2e_rec,
+        "gpu_launches": st.launches_per_step * n,
+        "clocks": sampler.summary(),
         "device": props.name,
         "sm_count": props.multi_processor_count,
         "wall_s_timed_region": t_wall,
     }
+    del st, flush
+    torch.cuda.empty_cache()
+    return result
+
+
+POINT_KEYS = ("value", "unit", "ms_per_step", "repeats", "timed_steps", "verify_steps_per_s", "hbm_gbs_step",
+              "roofline", "kernels", "e2e", "gpu_launches", "clocks", "wall_s_timed_region")
+# the metric's T = 1 and T = 8 points and the verify + replay-commit steps, each measured like the main line
+POINTS = ("decode", "verify8", "verify4_replay", "verify8_replay")
+
+
+def point_record(r: dict) -> dict:
+    rec = {k: r[k] for k in POINT_KEYS}
+    rec["config"] = {k: r["config"][k] for k in ("workload", "B", "active_lanes", "T", "state_dtype",
+                                                   "intermediate_cache", "step")}
+    return rec
+
+
+def sweep_summary(args, rank, world, local_rank, dist, pts, steps: int) -> list:
+    """Tokens/s and the dominant kernel's fraction of the measured peak per point (fixed step count, no
+    end-to-end leg)."""
+    out = []
+    for w in pts:
+        r = measure_point(args, w, rank, world, local_rank, dist, 0.0, e2e=False, steps=steps)
+        out.append({"workload": w.name, "B": w.B, "T": w.T, "state_dtype": w.state_dtype,
+                    "tokens_per_s": r["value"], "ms_per_step": r["ms_per_step"],
+                    "kernel": r["roofline"]["kernel"], "frac": r["roofline"]["frac"],
+                    "frac_nominal": r["roofline"]["frac_nominal"], "sm_mhz": r["clocks"]["sm_mhz"]})
+    return out
+
+
+def run_cuda_arm(args, w: W.Workload, rank: int, world: int, local_rank: int, emit=True, points=(),
+                 sweep_steps: int = 0):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dist = init_dist(world, "nccl")
+    result = measure_point(args, w, rank, world, local_rank, dist, args.min_seconds)
+    if points:
+        result["points"] = {}
+        for name in points:
+            pw = W.NAMED[name]()
+            result["points"][pw.name] = point_record(
+                measure_point(args, pw, rank, world, local_rank, dist, args.min_seconds))
+    if sweep_steps > 0:
+        result["sweep"] = {"steps_per_point": sweep_steps,
+                           "points": sweep_summary(args, rank, world, local_rank, dist, W.sweep(), sweep_steps)}
     if rank == 0 and not args.no_cpu_baseline and emit:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0 and emit:
@@ -583,12 +681,19 @@ def alu_peak_tflops(sms: int, mhz: float) -> float:
     return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
 
 
-def _timed_calls(call, K: int, warmup: int, stream, sampler):
+def _timed_calls(call, K: int, warmup: int, stream, sampler, min_seconds: float = 0.0):
+    """W warm-up calls, then R x K timed calls (R from the warm-up, so that the timed calls cover at least
+    `min_seconds` of device time), each bracketed by CUDA events; returns (per-call ms, wall seconds)."""
     import torch
 
-    for _ in range(warmup):
+    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(warmup)]
+    for i in range(warmup):
+        wev[i][0].record(stream)
         call()
+        wev[i][1].record(stream)
     torch.cuda.synchronize()
+    warm_ms = statistics.median(e[0].elapsed_time(e[1]) for e in wev) if wev else 0.0
+    K = K * max(1, int(math.ceil(min_seconds * 1e3 / max(K * warm_ms, 1e-6)))) if min_seconds > 0 else K
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler.start()
     t_wall = time.perf_counter()
@@ -626,24 +731,25 @@ def _prefill_pair(orc, pw, x, b: int, h: int, max_tokens=None):
 
 
 def _prefill_cpu_baseline(pw, x, seconds: float):
-    """The oracle as it stands (one thread, fp64 C loops) on (prompt, head) pairs in order -- each a whole
-    prompt for one value head -- until about `seconds` of CPU work; tokens/s of the layer = pair tokens / HV
-    / time (a token's work is HV such pairs)."""
+    """The oracle as it stands (fp64 C loops) on (prompt, head) pairs in order -- each a whole prompt for one
+    value head -- on every host core until about `seconds` have passed (and on one thread beside it);
+    tokens/s of the layer = pair tokens / HV / time (a token's work is HV such pairs)."""
     import oracle
 
     orc = oracle.default()
     pairs = _prefill_pairs(pw, x)
-    done_tokens, n_pairs, t0 = 0, 0, time.perf_counter()
-    for b, h in pairs:
-        done_tokens += _prefill_pair(orc, pw, x, b, h)
-        n_pairs += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": done_tokens / pw.HV / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle prefill of the first {n_pairs} of {len(pairs)} (prompt, value head) pairs of "
-                      f"{pw.name} ({done_tokens} pair-tokens), fp64 C loops, one thread, {dt:.1f} s; "
-                      f"tokens/s = pair-tokens / HV / time"}
+    cores = host_cores()
+    cu = x["cu_seqlens"]
+    ntok = [int(cu[b + 1] - cu[b]) for b, _ in pairs]
+    work = [(lambda b=b, h=h: _prefill_pair(orc, pw, x, b, h)) for b, h in pairs]
+    n1, dt1 = oracle_throughput(work, seconds / 3.0, 1)
+    n, dt = oracle_throughput(work, seconds * 2.0 / 3.0, cores)
+    tok1, tok = sum(ntok[:n1]), sum(ntok[:n])
+    return {"value": tok / pw.HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+            "one_thread": {"value": tok1 / pw.HV / dt1, "unit": "tokens/s", "pairs": n1, "seconds": dt1},
+            "sample": f"oracle prefill of the first {n} of {len(pairs)} (prompt, value head) pairs of {pw.name} "
+                      f"({tok} pair-tokens), fp64 C loops on {cores} threads, {dt:.1f} s; tokens/s = pair-tokens / "
+                      f"HV / time; one thread: {n1} pairs in {dt1:.1f} s"}
 
 
 def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
@@ -678,13 +784,14 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
     sampler = ClockSampler(local_rank)
     if dist is not None:
         dist.barrier()
-    ms, t_wall = _timed_calls(call, args.steps, args.warmup, stream, sampler)
+    ms, t_wall = _timed_calls(call, args.steps, args.warmup, stream, sampler, args.min_seconds)
     if err.item() != 0:
         raise RuntimeError(f"device error word {err.item()}")
     total_ms = max_over_ranks(sum(ms), dist, device)
+    n_timed = len(ms)
     lens = np.diff(x["cu_seqlens"])
     active_tokens = int(lens[x["indices"] >= 0].sum())
-    tokens_all = sum_over_ranks(active_tokens * args.steps, dist, device)
+    tokens_all = sum_over_ranks(active_tokens * n_timed, dist, device)
 
     # end to end through the binding: each step's q, k, v, a, b copied in from pinned host memory and o
     # copied back, on the compute stream
@@ -712,7 +819,8 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
     achieved = flops / (avg_us * 1e-6) / 1e12
     result = {
         "metric": PREFILL_METRIC, "value": tokens_all / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "steps": args.steps, "timed_steps": n_timed, "warmup": args.warmup, "ms_per_step": total_ms / n_timed,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded numpy draws; shapes and distributions of the named workload)",
         "config": {"workload": pw.name, "B": pw.B, "tokens": N, "active_tokens": active_tokens, "HK": pw.HK,
@@ -721,7 +829,8 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
                    "step": "gdn_prefill (every prompt from its slot or from zero; final state into the slot)",
                    "l2": f"not flushed: the step reads {h2d / 1e9:.2f} GB of token inputs, more than L2",
                    "parallelism": f"replicas x{world} (independent prompts, no collective)",
-                   "timing": "CUDA events per call on the launch stream, summed; max over ranks",
+                   "timing": f"CUDA events per call on the launch stream, summed over {n_timed} calls (>= "
+                             f"{args.min_seconds:g} s of device time); max over ranks",
                    "e2e": "inputs copied in from pinned host memory and o copied back on the compute stream, "
                           "per step, not overlapped"},
         "roofline": {"kernel": "gdn_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
@@ -732,7 +841,7 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
                      "traffic": recorded_traffic("prefill", pw.name, PREFILL_SOURCES)},
         "e2e": {"value": sum_over_ranks(active_tokens, dist, device) / (e2e_ms_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
-        "gpu_launches": args.steps, "clocks": clocks, "device": props.name,
+        "gpu_launches": n_timed, "clocks": clocks, "device": props.name,
         "sm_count": props.multi_processor_count, "wall_s_timed_region": t_wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -760,8 +869,10 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
     sampler = ClockSampler(local_rank)
     if dist is not None:
         dist.barrier()
-    ms, t_wall = _timed_calls(lambda: gdn.gdn_gated_rmsnorm(o, z, wt, y), args.steps, args.warmup, stream, sampler)
+    ms, t_wall = _timed_calls(lambda: gdn.gdn_gated_rmsnorm(o, z, wt, y), args.steps, args.warmup, stream, sampler,
+                              args.min_seconds)
     total_ms = max_over_ranks(sum(ms), dist, device)
+    n_timed = len(ms)
     nbytes = rows * DV * 2 * 3 + DV * 4
     avg_us = statistics.mean(ms) * 1e3
     peak, peak_src = hbm_peak()
@@ -782,8 +893,9 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
     e2e_ms_step = max_over_ranks(statistics.mean(e2e_ms), dist, device)
     props = torch.cuda.get_device_properties(device)
     result = {
-        "metric": NORM_METRIC, "value": rows * args.steps * world / (total_ms * 1e-3), "unit": "rows/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "metric": NORM_METRIC, "value": rows * n_timed * world / (total_ms * 1e-3), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "timed_steps": n_timed, "warmup": args.warmup,
+        "ms_per_step": total_ms / n_timed,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded numpy draws)",
         "config": {"workload": f"gated_rmsnorm_rows{rows}_DV{DV}_bf16", "rows": rows, "DV": DV,
@@ -794,12 +906,13 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
         "roofline": {"kernel": "gdn_gated_rmsnorm_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_us": avg_us,
                      "traffic": recorded_traffic("gated_norm", f"gated_rmsnorm_rows{rows}_DV{DV}_bf16", NORM_SOURCES)},
         "e2e": {"value": rows * world / (e2e_ms_step * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": 2 * rows * DV * 2, "d2h_bytes_per_step": rows * DV * 2,
                 "ms_per_step": e2e_ms_step},
-        "gpu_launches": args.steps, "clocks": sampler.summary(), "device": props.name,
+        "gpu_launches": n_timed, "clocks": sampler.summary(), "device": props.name,
         "sm_count": props.multi_processor_count, "wall_s_timed_region": t_wall,
     }
     if rank == 0:
@@ -808,70 +921,83 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
 
 
 def run_prefill_reference_arm(args, pw, rank: int, world: int):
-    """The reference arm of a prefill workload: the oracle, each step the first L tokens of prompt 0 for one
-    value head, L sized so that warm-up + steps take about --ref-seconds.  tokens/s = L / HV / step time."""
+    """The reference arm of a prefill workload: the oracle on every host core, each step the first L tokens of
+    one (prompt, value head) pair per core, L sized so that warm-up + steps take about --ref-seconds.
+    tokens/s = pairs x L / HV / step time."""
     if rank != 0:
         return
     import oracle
 
     orc = oracle.default()
     x = pw.arrays()
-    b, h = _prefill_pairs(pw, x)[0]
-    n_seq = int(x["cu_seqlens"][b + 1] - x["cu_seqlens"][b])
+    cores = host_cores()
+    pairs = _prefill_pairs(pw, x)
+    cu = x["cu_seqlens"]
+    b, h = pairs[0]
+    n_seq = int(cu[b + 1] - cu[b])
     probe = min(64, n_seq)
     t0 = time.perf_counter()
     _prefill_pair(orc, pw, x, b, h, probe)
     t_tok = max((time.perf_counter() - t0) / probe, 1e-9)
-    L = int(max(1, min(n_seq, args.ref_seconds / (args.steps + args.warmup) / t_tok)))
+    use = pairs[:cores]
+    L = int(max(1, min(min(int(cu[bb + 1] - cu[bb]) for bb, _ in use),
+                       args.ref_seconds / (args.steps + args.warmup) / t_tok)))
+    work = [(lambda bb=bb, hh=hh: _prefill_pair(orc, pw, x, bb, hh, L)) for bb, hh in use]
     for _ in range(args.warmup):
-        _prefill_pair(orc, pw, x, b, h, L)
+        oracle_throughput(work, 1e9, len(use))
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _prefill_pair(orc, pw, x, b, h, L)
+        oracle_throughput(work, 1e9, len(use))
     dt = time.perf_counter() - t0
-    v = L / pw.HV * args.steps / dt
-    desc = (f"each step: oracle prefill of the first {L} tokens of prompt {b}, value head {h} of {pw.name} (1 of "
-            f"{pw.HV} heads), fp64 C loops, one thread; tokens/s = L / HV / time")
+    v = len(use) * L / pw.HV * args.steps / dt
+    desc = (f"each step: oracle prefill of the first {L} tokens of {len(use)} (prompt, value head) pairs of "
+            f"{pw.name}, one per thread on {len(use)} threads, fp64 C loops; tokens/s = pairs x L / HV / time")
     print(json.dumps({
         "impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": pw.name},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": len(use), "kind": "oracle",
+                         "cpu_model": cpu_model(), "sample": desc},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 def run_norm_reference_arm(args, rank: int, world: int, rows: int = 65536 * 32, DV: int = 128):
-    """The reference arm of the gated norm: the oracle on the first n rows each step, n sized so that
-    warm-up + steps take about --ref-seconds."""
+    """The reference arm of the gated norm: the oracle on the first n rows each step, split over every host
+    core, n sized so that warm-up + steps take about --ref-seconds."""
     if rank != 0:
         return
     import oracle
 
     orc = oracle.default()
     g = W.gated_norm_inputs(rows, DV, "bf16", "bf16", seed=17)
+    cores = host_cores()
 
-    def run(n):
-        orc.gated_rmsnorm(g["o"][:n], "bf16", g["z"][:n], "bf16", g["w"], 1e-6)
+    def run(lo, hi):
+        orc.gated_rmsnorm(g["o"][lo:hi], "bf16", g["z"][lo:hi], "bf16", g["w"], 1e-6)
 
     t0 = time.perf_counter()
-    run(256)
+    run(0, 256)
     t_row = max((time.perf_counter() - t0) / 256, 1e-9)
-    n = int(max(1, min(rows, args.ref_seconds / (args.steps + args.warmup) / t_row)))
+    n = int(max(cores, min(rows, cores * args.ref_seconds / (args.steps + args.warmup) / t_row)))
+    cuts = [n * j // cores for j in range(cores + 1)]
+    work = [(lambda lo=cuts[j], hi=cuts[j + 1]: run(lo, hi)) for j in range(cores)]
     for _ in range(args.warmup):
-        run(n)
+        oracle_throughput(work, 1e9, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        run(n)
+        oracle_throughput(work, 1e9, cores)
     dt = time.perf_counter() - t0
     v = n * args.steps / dt
-    desc = f"each step: oracle gated norm of the first {n} of {rows} rows of DV={DV}, fp64 C loops, one thread"
+    desc = (f"each step: oracle gated norm of the first {n} of {rows} rows of DV={DV}, split over {cores} threads, "
+            f"fp64 C loops")
     print(json.dumps({
         "impl": "reference", "metric": NORM_METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"gated_rmsnorm_rows{rows}_DV{DV}_bf16"},
-        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": desc},
         "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -923,52 +1049,118 @@ def _pair_setup(w: W.Workload):
     return orc, x, d, pairs
 
 
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, else lscpu, else the machine type)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+
+    return platform.machine()
+
+
+def oracle_throughput(work, seconds: float, threads: int):
+    """Runs `work` (callables, one oracle call each) in order on `threads` threads -- each thread takes the next
+    item -- until all are done or `seconds` have passed; returns (items done, elapsed s).  The oracle's ctypes
+    calls release the GIL, so the threads run on separate cores."""
+    import itertools
+
+    nxt = itertools.count()
+    done = [0] * threads
+    t0 = time.perf_counter()
+    deadline = t0 + seconds
+
+    def worker(j):
+        while time.perf_counter() < deadline:
+            i = next(nxt)
+            if i >= len(work):
+                return
+            work[i]()
+            done[j] += 1
+
+    ts = [threading.Thread(target=worker, args=(j,)) for j in range(threads)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return sum(done), time.perf_counter() - t0
+
+
+def _pair_work(orc, w, d, x, pairs):
+    return [(lambda y=y: oracle_pair_step(orc, w, d, y)) for y in oracle_pairs(w, x, pairs)]
+
+
 def cpu_baseline(w: W.Workload, seconds: float):
-    """The oracle as it stands (one thread, fp64 C loops) on a bounded sample of the workload: (lane, head)
-    pairs in order until `seconds` of CPU work; tokens/s = pairs * T / HV / time."""
+    """The oracle as it stands (fp64 C loops) on a bounded sample of the workload -- (lane, head) pairs in order
+    -- on every host core (the reported value), and on one thread beside it; tokens/s = pairs * T / HV /
+    time.  The pairs' inputs are sliced out before the clock starts."""
     orc, x, d, pairs = _pair_setup(w)
-    done, t0 = 0, time.perf_counter()
-    for chunk in range(0, len(pairs), 32):
-        for y in oracle_pairs(w, x, pairs[chunk:chunk + 32]):
-            oracle_pair_step(orc, w, d, y)
-            done += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": done * w.T / w.HV / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle step (verify+commit) of the first {done} of {len(pairs)} (lane, head) pairs of "
-                      f"{w.name}, fp64 C loops, one thread, {dt:.1f} s"}
+    cores = host_cores()
+    probe = _pair_work(orc, w, d, x, pairs[:1])[0]
+    t0 = time.perf_counter()
+    probe()
+    t_pair = max(time.perf_counter() - t0, 1e-6)
+    one_s, all_s = seconds / 3.0, seconds * 2.0 / 3.0
+    n_need = int(min(len(pairs), 1.5 * cores * all_s / t_pair + 1))
+    work = _pair_work(orc, w, d, x, pairs[:n_need])
+    n1, dt1 = oracle_throughput(work, one_s, 1)
+    n, dt = oracle_throughput(work, all_s, cores)
+    return {"value": n * w.T / w.HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "one_thread": {"value": n1 * w.T / w.HV / dt1, "unit": "tokens/s", "pairs": n1, "seconds": dt1},
+            "sample": f"oracle step ({'decode' if w.mode == 'decode' else 'verify+commit'}) of the first {n} of "
+                      f"{len(pairs)} (lane, head) pairs of {w.name}, fp64 C loops on {cores} threads (one per "
+                      f"core), {dt:.1f} s; one thread: {n1} pairs in {dt1:.1f} s"}
 
 
 def run_reference_arm(args, w: W.Workload, rank: int, world: int):
-    """The reference arm is the oracle: each step runs a bounded sample of (lane, head) pairs, sized so that
-    warm-up + steps take about --ref-seconds in total.  Only rank 0 works."""
+    """The reference arm is the oracle on every host core: each step runs a bounded sample of (lane, head)
+    pairs, sized so that warm-up + steps take about --ref-seconds in total.  Only rank 0 works."""
     if rank != 0:
         return
     orc, x, d, pairs = _pair_setup(w)
-    probe = oracle_pairs(w, x, pairs[:1])[0]
+    cores = host_cores()
+    probe = _pair_work(orc, w, d, x, pairs[:1])[0]
     t0 = time.perf_counter()
-    oracle_pair_step(orc, w, d, probe)
+    probe()
     t_pair = max(time.perf_counter() - t0, 1e-6)
     per_step = args.ref_seconds / (args.steps + args.warmup)
-    n = int(max(1, min(len(pairs), per_step // t_pair)))
-    sample = oracle_pairs(w, x, pairs[:n])
+    n = int(max(1, min(len(pairs), cores * per_step // t_pair)))
+    work = _pair_work(orc, w, d, x, pairs[:n])
     for _ in range(args.warmup):
-        for y in sample:
-            oracle_pair_step(orc, w, d, y)
+        oracle_throughput(work, 1e9, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        for y in sample:
-            oracle_pair_step(orc, w, d, y)
+        oracle_throughput(work, 1e9, cores)
     dt = time.perf_counter() - t0
     v = n * w.T / w.HV * args.steps / dt
-    desc = (f"each step: oracle verify+commit of {n} of {len(pairs)} (lane, head) pairs of {w.name}, "
-            f"fp64 C loops, one thread; tokens/s = pairs * T / HV / time")
+    desc = (f"each step: oracle {'decode' if w.mode == 'decode' else 'verify+commit'} of {n} of {len(pairs)} "
+            f"(lane, head) pairs of {w.name}, fp64 C loops on {cores} threads; tokens/s = pairs * T / HV / time")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w.name},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": desc},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -984,6 +1176,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--min-seconds", type=float, default=MIN_WINDOW_S,
+                    help="minimum device time of each point's timed region (the K steps are repeated to reach it)")
+    ap.add_argument("--no-points", action="store_true",
+                    help="verify4 line only: leave out the T=1 / T=8 / replay-commit points and the sweep summary")
+    ap.add_argument("--sweep-steps", type=int, default=40, help="steps per point of the verify4 line's sweep summary")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1006,11 +1203,13 @@ def main(argv=None):
         pts = W.sweep_replay()
     else:
         pts = [W.NAMED[args.workload]()]
+    headline = args.workload == "verify4" and not args.no_points
     for w in pts:
         if args.impl == "reference":
             run_reference_arm(args, w, rank, world)
         else:
-            run_cuda_arm(args, w, rank, world, local_rank)
+            run_cuda_arm(args, w, rank, world, local_rank, points=POINTS if headline else (),
+                         sweep_steps=args.sweep_steps if headline else 0)
     return 0
 
 

@@ -117,10 +117,34 @@ def _shape(t, want, name: str):
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(want)}")
 
 
-def _stream(stream):
+def _common_device(named):
+    """The one CUDA device that every given tensor (``(name, tensor)`` pairs, None skipped) lives on.
+
+    A call launches its kernels on one GPU with raw pointers: a tensor on another GPU would be read through
+    peer access or fault, so mixed devices are rejected before anything is launched."""
+    dev, first = None, None
+    for name, t in named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev, first = t.device, name
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device} but {first} is on {dev}: every tensor of one call must be "
+                             "on the same GPU")
+    if dev is None:
+        raise ValueError("no CUDA tensor given")
+    return dev
+
+
+def _stream(stream, device):
+    """The launch stream: the given one (which must belong to `device`) or `device`'s current stream."""
     import torch
 
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if s.device != device:
+        raise ValueError(f"stream is on {s.device}, the tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -162,16 +186,32 @@ def _call(status: int, what: str) -> None:
         raise GdnError(status, what)
 
 
-# ---- the three calls -----------------------------------------------------------------------------------
+def _launch(device, stream, fn, args, what: str) -> None:
+    """One library call with `device` current, on `stream` (default: `device`'s current stream)."""
+    import torch
+
+    s = _stream(stream, device)
+    with torch.cuda.device(device):
+        _call(fn(*args, s), what)
+
+
+def _io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices):
+    return [("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias),
+            ("state_pool", state_pool), ("state_indices", state_indices)]
+
+
+# ---- the calls -------------------------------------------------------------------------------------------
 def gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, *, scale=1.0,
                l2_eps=1e-6, stream=None) -> None:
     """T tokens (normally 1) from ``state_pool[state_indices[b]]``; the final state is written back in place."""
     L = lib()
     d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
-    _call(L.gdn_decode(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
-                       _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
-                       _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word"),
-                       _stream(stream)), "gdn_decode")
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("o", o), ("err_word", err_word)])
+    _launch(device, stream, L.gdn_decode,
+            (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+             _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word")), "gdn_decode")
 
 
 def gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None,
@@ -183,11 +223,13 @@ def gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, 
         _shape(intermediate_states, (d.B, d.T, d.HV, d.DV, d.DK), "intermediate_states")
         if intermediate_states.dtype != state_pool.dtype:
             raise TypeError("intermediate_states must have state_pool's dtype")
-    _call(L.gdn_mtp_verify(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
-                           _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
-                           _dev(state_indices, "state_indices"), _dev(o, "o"),
-                           _dev(intermediate_states, "intermediate_states"), _dev(err_word, "err_word"),
-                           _stream(stream)), "gdn_mtp_verify")
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("o", o), ("intermediate_states", intermediate_states), ("err_word", err_word)])
+    _launch(device, stream, L.gdn_mtp_verify,
+            (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+             _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(intermediate_states, "intermediate_states"),
+             _dev(err_word, "err_word")), "gdn_mtp_verify")
 
 
 def gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None, *, stream=None) -> None:
@@ -208,9 +250,13 @@ def gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_w
         raise TypeError("intermediate_states must have state_pool's dtype")
     sd = _code(state_pool, "state_pool")
     d = GdnDims(B, T, 1, HV, DK, DV, num_slots, sd, sd, sd, 1.0, 0.0)
-    _call(L.gdn_commit(ctypes.byref(d), _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
-                       _dev(intermediate_states, "intermediate_states"), _dev(accept_len, "accept_len"),
-                       _dev(err_word, "err_word"), _stream(stream)), "gdn_commit")
+    device = _common_device([("state_pool", state_pool), ("state_indices", state_indices),
+                             ("intermediate_states", intermediate_states), ("accept_len", accept_len),
+                             ("err_word", err_word)])
+    _launch(device, stream, L.gdn_commit,
+            (ctypes.byref(d), _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
+             _dev(intermediate_states, "intermediate_states"), _dev(accept_len, "accept_len"),
+             _dev(err_word, "err_word")), "gdn_commit")
 
 
 def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, *,
@@ -226,10 +272,13 @@ def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
     _shape(accept_len, (d.B,), "accept_len")
     if accept_len.dtype != torch.int32:
         raise TypeError("accept_len must be int32")
-    _call(L.gdn_commit_replay(ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
-                              _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
-                              _dev(state_indices, "state_indices"), _dev(accept_len, "accept_len"),
-                              _dev(err_word, "err_word"), _stream(stream)), "gdn_commit_replay")
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("accept_len", accept_len), ("err_word", err_word)])
+    _launch(device, stream, L.gdn_commit_replay,
+            (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+             _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(accept_len, "accept_len"), _dev(err_word, "err_word")),
+            "gdn_commit_replay")
 
 
 def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o, has_initial_state=None,
@@ -259,11 +308,14 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seq
         if has_initial_state.dtype != torch.int32:
             raise TypeError("has_initial_state must be int32")
     d.B, d.T = B, N
-    _call(L.gdn_prefill(ctypes.byref(d), _dev(cu_seqlens, "cu_seqlens"), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"),
-                        _dev(a, "a"), _dev(b, "b"), _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"),
-                        _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
-                        _dev(has_initial_state, "has_initial_state"), _dev(o, "o"), _dev(err_word, "err_word"),
-                        _stream(stream)), "gdn_prefill")
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("cu_seqlens", cu_seqlens), ("o", o), ("has_initial_state", has_initial_state),
+                               ("err_word", err_word)])
+    _launch(device, stream, L.gdn_prefill,
+            (ctypes.byref(d), _dev(cu_seqlens, "cu_seqlens"), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"),
+             _dev(a, "a"), _dev(b, "b"), _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"),
+             _dev(state_pool, "state_pool"), _dev(state_indices, "state_indices"),
+             _dev(has_initial_state, "has_initial_state"), _dev(o, "o"), _dev(err_word, "err_word")), "gdn_prefill")
 
 
 def gdn_gated_rmsnorm(o, z, norm_weight, y=None, *, eps=1e-6, stream=None):
@@ -284,7 +336,8 @@ def gdn_gated_rmsnorm(o, z, norm_weight, y=None, *, eps=1e-6, stream=None):
     if y.dtype != o.dtype:
         raise TypeError("y must have o's dtype")
     rows = o.numel() // DV if DV > 0 else 0
-    _call(L.gdn_gated_rmsnorm(rows, DV, _code(o, "o"), _code(z, "z"), _dev(o, "o"), _dev(z, "z"),
-                              _dev(norm_weight, "norm_weight"), float(eps), _dev(y, "y"), _stream(stream)),
-          "gdn_gated_rmsnorm")
+    device = _common_device([("o", o), ("z", z), ("norm_weight", norm_weight), ("y", y)])
+    _launch(device, stream, L.gdn_gated_rmsnorm,
+            (rows, DV, _code(o, "o"), _code(z, "z"), _dev(o, "o"), _dev(z, "z"), _dev(norm_weight, "norm_weight"),
+             float(eps), _dev(y, "y")), "gdn_gated_rmsnorm")
     return y

@@ -785,6 +785,7 @@ cudaError_t encode_pool_map(CUtensorMap* map, void* pool, const RecurrentParams&
 }
 
 constexpr int kChunkStages = 2;
+constexpr int kChunkCachedDevices = 64;  // devices whose launch settings are cached
 
 // grid = min(items, SMs x resident CTAs), each CTA a contiguous range of items
 template <int DK, typename InT, bool kCommit>
@@ -793,26 +794,29 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     using CS = ChunkPlan<DK, kCommit, NS>;
     auto kernel = gdn_verify_chunked_kernel<DK, InT, kCommit, NS>;
     const uint32_t smem = CS::bytes(p.T);
-    // launch caches shared by every calling thread (a repeated first call only repeats the same queries)
-    static std::atomic<int> attr_bytes{0};  // dynamic shared memory this instantiation has been opened for
-    if ((int)smem > attr_bytes.load(std::memory_order_relaxed)) {
-        const int most = (int)CS::bytes(kChunkMaxT);
-        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-        if (e != cudaSuccess) return e;
-        attr_bytes.store(most, std::memory_order_relaxed);
-    }
-    static std::atomic<int> occ_cache[kChunkMaxT + 1];  // zero-initialised (static storage)
-    int occ = occ_cache[p.T].load(std::memory_order_relaxed);
-    if (occ == 0) {
-        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (occ < 1) return cudaErrorInvalidConfiguration;
-        occ_cache[p.T].store(occ, std::memory_order_relaxed);
-    }
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    // Launch caches shared by every calling thread, one entry per device: the shared-memory opening is a
+    // per-device attribute of the function, and occupancy may differ between devices.  A repeated first call
+    // only repeats the same queries; devices beyond the table are queried on every call.
+    static std::atomic<int> attr_bytes[kChunkCachedDevices];               // bytes opened on each device
+    static std::atomic<int> occ_cache[kChunkCachedDevices][kChunkMaxT + 1];  // zero-initialised (static)
+    const bool cached = dev >= 0 && dev < kChunkCachedDevices;
+    if (!cached || (int)smem > attr_bytes[dev].load(std::memory_order_relaxed)) {
+        const int most = (int)CS::bytes(kChunkMaxT);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        if (e != cudaSuccess) return e;
+        if (cached) attr_bytes[dev].store(most, std::memory_order_relaxed);
+    }
+    int occ = cached ? occ_cache[dev][p.T].load(std::memory_order_relaxed) : 0;
+    if (occ == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        if (cached) occ_cache[dev][p.T].store(occ, std::memory_order_relaxed);
+    }
     CUtensorMap map;
     e = encode_pool_map<DK>(&map, kCommit ? p.pool_out : const_cast<void*>(p.pool_in), p);
     if (e != cudaSuccess) return e;

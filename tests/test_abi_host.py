@@ -253,3 +253,72 @@ def test_binding_prefill_and_norm_argument_checks():
         gdn.gdn_gated_rmsnorm(z, z, torch.ones(DV + 1))
     with pytest.raises(TypeError):
         gdn.gdn_gated_rmsnorm(z, z, torch.ones(DV), torch.zeros(N * HV, DV))
+
+
+# ---- every tensor of a call on one GPU (checked before anything is launched; fakes stand in for GPUs) ------
+class _OnDevice:
+    """A CPU tensor that reports itself as living on the given CUDA device (never dereferenced: the check
+    under test rejects the call first)."""
+
+    is_cuda = True
+
+    def __init__(self, t, device):
+        import torch
+
+        self._t, self.device = t, torch.device(device)
+
+    def __getattr__(self, name):
+        return getattr(self._t, name)
+
+
+class _FakeStream:
+    def __init__(self, device):
+        import torch
+
+        self.device, self.cuda_stream = torch.device(device), 0
+
+
+def _verify_args(dev_of):
+    import torch
+
+    B, T, HK, HV, DK, DV = 2, 3, 1, 2, 16, 16
+    bf = torch.bfloat16
+    t = dict(q=torch.zeros(B, T, HK, DK, dtype=bf), k=torch.zeros(B, T, HK, DK, dtype=bf),
+             v=torch.zeros(B, T, HV, DV, dtype=bf), a=torch.zeros(B, T, HV, dtype=bf),
+             b=torch.zeros(B, T, HV, dtype=bf), A_log=torch.zeros(HV), dt_bias=torch.zeros(HV),
+             pool=torch.zeros(4, HV, DV, DK, dtype=bf), idx=torch.zeros(B, dtype=torch.int32),
+             o=torch.zeros(B, T, HV, DV, dtype=bf), acc=torch.ones(B, dtype=torch.int32),
+             cache=torch.zeros(B, T, HV, DV, DK, dtype=bf))
+    return {k: _OnDevice(x, dev_of(k)) for k, x in t.items()}
+
+
+def test_binding_common_device_helper():
+    import torch
+
+    a, b = _OnDevice(torch.zeros(1), "cuda:0"), _OnDevice(torch.zeros(1), "cuda:1")
+    assert gdn._common_device([("a", a), ("skipped", None), ("a2", a)]) == torch.device("cuda:0")
+    with pytest.raises(ValueError, match="same GPU"):
+        gdn._common_device([("a", a), ("b", b)])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gdn._common_device([("a", a), ("cpu", torch.zeros(1))])
+
+
+@pytest.mark.parametrize("odd", ["q", "v", "pool", "idx", "o", "cache", "acc"])
+def test_binding_rejects_tensors_on_two_gpus(odd):
+    x = _verify_args(lambda k: "cuda:1" if k == odd else "cuda:0")
+    with pytest.raises(ValueError, match="same GPU"):
+        if odd == "acc":
+            gdn.gdn_commit(x["pool"], x["idx"], x["cache"], x["acc"])
+        else:
+            gdn.gdn_mtp_verify(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"], x["pool"],
+                               x["idx"], x["o"], x["cache"])
+    if odd in ("pool", "idx", "acc", "cache"):
+        with pytest.raises(ValueError, match="same GPU"):
+            gdn.gdn_commit(x["pool"], x["idx"], x["cache"], x["acc"])
+
+
+def test_binding_rejects_a_stream_of_another_gpu():
+    x = _verify_args(lambda k: "cuda:0")
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        gdn.gdn_mtp_verify(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"], x["pool"], x["idx"],
+                           x["o"], None, stream=_FakeStream("cuda:1"))

@@ -165,9 +165,53 @@ def test_prefill_and_norm_reference_arms_small():
 def test_prefill_cpu_baseline_small():
     pw = W.PrefillWorkload("prefill_small", B=2, HK=1, HV=2, DK=16, DV=16, num_slots=4, qkv_dtype="f32",
                            state_dtype="f32", out_dtype="f32", seed=10, lengths=(5, 9))
-    cb = bench._prefill_cpu_baseline(pw, pw.arrays(), 0.01)
-    assert cb["value"] > 0 and cb["kind"] == "oracle" and cb["cores"] == 1
+    cb = bench._prefill_cpu_baseline(pw, pw.arrays(), 0.05)
+    assert cb["value"] > 0 and cb["kind"] == "oracle" and cb["cores"] == bench.host_cores()
+    assert cb["one_thread"]["value"] > 0 and cb["cpu_model"]
 
 
 def test_alu_peak_derivation():
     assert abs(bench.alu_peak_tflops(152, 2070) - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+
+
+def test_cpu_baseline_uses_every_core_and_reports_one_thread():
+    cb = bench.cpu_baseline(W.tiny(), 0.3)
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() >= 1
+    assert cb["value"] > 0 and cb["one_thread"]["value"] > 0 and cb["one_thread"]["pairs"] >= 1
+    assert cb["cpu_model"] and str(cb["cores"]) in cb["sample"]
+
+
+def test_oracle_throughput_runs_items_in_order_until_done_or_deadline():
+    import threading
+
+    seen, lock = [], threading.Lock()
+
+    def item(i):
+        def f():
+            with lock:
+                seen.append(i)
+        return f
+
+    n, dt = bench.oracle_throughput([item(i) for i in range(50)], 1e9, 4)
+    assert n == 50 and sorted(seen) == list(range(50)) and dt >= 0
+    n, _ = bench.oracle_throughput([item(i) for i in range(50)], -1.0, 4)  # deadline already passed
+    assert n == 0
+
+
+def test_clock_summary_takes_the_median_under_load():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.max_mhz, cs.source, cs.period = 2070, "test", 0.01
+    # (sm MHz, W, reason bits, utilisation %): two idle samples at a low clock, three busy ones
+    cs.samples = [(900, 100.0, 0x1, 0), (2070, 900.0, 0, 100), (2000, 950.0, 0x4, 100), (2070, 910.0, 0, 90),
+                  (900, 100.0, 0x1, 0)]
+    s = cs.summary()
+    assert s["sm_mhz"] == 2070 and s["samples"] == 5 and s["samples_under_load"] == 3 and s["sm_mhz_min"] == 2000
+    assert s["reasons"] == ["sw_power_cap"]  # gpu_idle is not a throttle reason
+
+
+def test_roofline_block_reports_both_peaks():
+    k = {"kernel": "k", "role": "verify", "achieved_gbs": 6400.0, "frac": 6400.0 / 6790.0, "algorithmic_bytes": 1,
+         "avg_us": 1.0}
+    r = bench.roofline_block(k, 6790.0, "measured (x)", None)
+    assert abs(r["frac"] - 6400 / 6790) < 1e-12 and abs(r["frac_nominal"] - 0.8) < 1e-12
+    assert r["nominal_peak"] == 8000.0 and r["peak"] == 6790.0 and "of measured" in r["peak_source"]
