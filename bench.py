@@ -51,7 +51,7 @@ def kernel_name(w, role: str, sms: int) -> str:
     if role == "commit":
         return "gdn_commit_kernel"
     in_range = w.num_slots * w.HV <= 2**31 - 1 and w.B * w.HV * -(-w.DV // 128) <= 2**31 - 1
-    if (w.state_dtype == "bf16" and w.T <= 8 and in_range
+    if (w.state_dtype == "bf16" and w.T <= 8 and w.DK >= 64 and in_range
             and ((role == "verify" and not w.cache) or role == "commit_replay")):
         return "gdn_verify_chunked_kernel"
     st = 2 if w.state_dtype == "bf16" else 4
@@ -1078,10 +1078,10 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def oracle_throughput(work, seconds: float, threads: int):
+def oracle_throughput(work, seconds: float, threads: int, cycle: bool = False):
     """Runs `work` (callables, one oracle call each) in order on `threads` threads -- each thread takes the next
-    item -- until all are done or `seconds` have passed; returns (items done, elapsed s).  The oracle's ctypes
-    calls release the GIL, so the threads run on separate cores."""
+    item -- until all are done (`cycle`: over and over) or `seconds` have passed; returns (items done,
+    elapsed s).  The oracle's ctypes calls release the GIL, so the threads run on separate cores."""
     import itertools
 
     nxt = itertools.count()
@@ -1092,9 +1092,9 @@ def oracle_throughput(work, seconds: float, threads: int):
     def worker(j):
         while time.perf_counter() < deadline:
             i = next(nxt)
-            if i >= len(work):
+            if i >= len(work) and not cycle:
                 return
-            work[i]()
+            work[i % len(work)]()
             done[j] += 1
 
     ts = [threading.Thread(target=worker, args=(j,)) for j in range(threads)]
@@ -1120,16 +1120,17 @@ def cpu_baseline(w: W.Workload, seconds: float):
     probe()
     t_pair = max(time.perf_counter() - t0, 1e-6)
     one_s, all_s = seconds / 3.0, seconds * 2.0 / 3.0
-    n_need = int(min(len(pairs), 1.5 * cores * all_s / t_pair + 1))
+    n_need = int(min(len(pairs), 1.5 * cores * all_s / t_pair + 1))  # about the work the time allows
     work = _pair_work(orc, w, d, x, pairs[:n_need])
-    n1, dt1 = oracle_throughput(work, one_s, 1)
-    n, dt = oracle_throughput(work, all_s, cores)
+    n1, dt1 = oracle_throughput(work, one_s, 1, cycle=True)
+    n, dt = oracle_throughput(work, all_s, cores, cycle=True)
     return {"value": n * w.T / w.HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "cpu_model": cpu_model(),
             "one_thread": {"value": n1 * w.T / w.HV / dt1, "unit": "tokens/s", "pairs": n1, "seconds": dt1},
-            "sample": f"oracle step ({'decode' if w.mode == 'decode' else 'verify+commit'}) of the first {n} of "
-                      f"{len(pairs)} (lane, head) pairs of {w.name}, fp64 C loops on {cores} threads (one per "
-                      f"core), {dt:.1f} s; one thread: {n1} pairs in {dt1:.1f} s"}
+            "sample": f"oracle step ({'decode' if w.mode == 'decode' else 'verify+commit'}) of {n} (lane, head) "
+                      f"pairs of {w.name} (its first {len(work)} of {len(pairs)} pairs, in order and again), fp64 "
+                      f"C loops on {cores} threads (one per core), {dt:.1f} s; one thread: {n1} pairs in "
+                      f"{dt1:.1f} s"}
 
 
 def run_reference_arm(args, w: W.Workload, rank: int, world: int):

@@ -11,8 +11,8 @@
 // direct one inside its rule and 4-80% slower outside it; 16 KiB stages were up to 15% faster than 32 KiB
 // for fp32 pools and bf16 with T = 4, and up to 12% slower for bf16 with T <= 2.  Both kernels run
 // Split<DK>::THREADS threads per CTA.
-// On a bf16 pool with T <= 8, a verify that stores neither intermediate states nor a write-back, and a
-// replay commit, run the persistent chunked tensor-core kernel (gdn_verify_chunked.cuh) instead, one CTA
+// On a bf16 pool with T <= 8 and DK >= 64, a verify that stores neither intermediate states nor a write-back,
+// and a replay commit, run the persistent chunked tensor-core kernel (gdn_verify_chunked.cuh) instead, one CTA
 // per resident slot of the GPU.
 #pragma once
 
@@ -64,7 +64,7 @@ bool launch_staged(const RecurrentParams& p, int B, int sms, cudaStream_t s, cud
 template <typename InT, typename StT, int DK>
 cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int NT = Split<DK>::THREADS;
-    if constexpr (std::is_same<StT, __nv_bfloat16>::value) {
+    if constexpr (std::is_same<StT, __nv_bfloat16>::value && DK >= kChunkMinDK) {
         const bool verify_only = p.cache == nullptr && p.pool_out == nullptr && p.steps == nullptr;
         const bool replay_commit = p.cache == nullptr && p.pool_out != nullptr && p.steps != nullptr && p.o == nullptr;
         // the chunked kernel addresses num_slots * HV heads with a signed 32-bit TMA coordinate and counts its

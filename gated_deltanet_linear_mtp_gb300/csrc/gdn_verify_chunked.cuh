@@ -1,5 +1,6 @@
 // gdn_verify_chunked.cuh -- MTP verify without intermediate states, and the replay commit, in chunked form on
-// the tensor cores; persistent CTAs stream the state tiles through a ring of TMA stages.
+// the tensor cores (tcgen05, accumulators in tensor memory); persistent CTAs stream the state tiles through a
+// ring of TMA stages.
 //
 // When nothing needs the states S_1..S_T themselves, the recurrence can be unrolled.  Writing
 // gamma_t = g_1 ... g_t, G(s,t) = g_{s+1} ... g_t (G(t,t) = 1) and delta_t = beta_t (v_t - u_t),
@@ -8,27 +9,30 @@
 // so for every state row
 //     u_t = g_t S_{t-1} kh_t = gamma_t (S_0 kh_t) + sum_{s<t}  G(s,t) (kh_s . kh_t) delta_s
 //     o_t = S_t qh_t         = gamma_t (S_0 qh_t) + sum_{s<=t} G(s,t) (kh_s . qh_t) delta_s .
-// The only per-element work is the contraction S_0 [kh_1..kh_T qh_1..qh_T], a (rows x DK) x (DK x 2T)
-// product: it runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with S_0 exact in
-// bf16 and kh, qh split into bf16 hi + lo parts (4T columns), which keeps about 16 significant bits of
-// kh and qh.  The T x T Gram matrices kh.kh and kh.qh are formed on the tensor cores from the same hi + lo
-// rows, and each row's small triangular recurrence runs in fp32 registers, one thread per row.
+// The only per-element work is the contraction P = S_0 [kh_1..kh_T qh_1..qh_T], a (128 x DK) x (DK x 2T)
+// product per item.  One thread issues it as DK/16 tcgen05.mma instructions (M = 128, N = 16 or 32, bf16 in,
+// fp32 accumulate in tensor memory) straight from the TMA stage, with S_0 exact in bf16 and kh, qh split into
+// bf16 hi + lo parts (4T columns), which keeps about 16 significant bits of kh and qh; every thread then reads
+// the P row of its own state row out of tensor memory (tcgen05.ld, lane = row).  The T x T Gram matrices
+// kh.kh and kh.qh are formed with mma.sync from the same hi + lo rows, and each row's small triangular
+// recurrence runs in fp32 registers, one thread per row.
 //
-// Two modes, for bf16 state pools and T <= 8 (the launcher's choice):
-//   verify (kCommit = false)   outputs o only: no intermediate states, no write-back;
+// Two modes, for bf16 state pools, T <= 8 and DK in {64, 128, 256} (the launcher's choice):
+//   verify (kCommit = false)   outputs o only: no intermediate states, no write-back.  A stage is refilled as
+//                              soon as the MMA that reads it has completed, before the row recurrence runs;
 //   replay commit (kCommit)    the first L = steps[b] tokens, no outputs, and the state after them,
 //                              S_L = gamma_L S_0 + sum_{s<L} G(s, L-1) delta_s kh_s^T, written back into the
-//                              slot (kh only: 2T columns, one Gram matrix); the rank-L update runs on the
-//                              tensor cores too.
+//                              slot (kh only: 2T columns, one Gram matrix); the rank-L update runs on mma.sync
+//                              over the stage in place, which a TMA tensor store then writes back.
 //
 // Work item = 128 state rows of one (lane, value head); items are numbered row block fastest, then value
 // head, then lane, and each CTA (4 warps, warp w owning rows [32w, 32w + 32)) takes a contiguous range of
-// them.  One thread (PT) keeps NS - 1 state tiles in flight ahead of the item being computed: one 3-D TMA
-// tensor load per 64-column box into a 1024-byte aligned stage, rows past DV filled with zeros, 16-byte chunks
-// swizzled within each 128-byte line so that the ldmatrix reads of the MMA are conflict-free.  q, k, v, a
-// and b of the next item are loaded into registers while the current one is computed, and consecutive
-// items of one key head reuse its normalised q, k and Gram matrices.  The replay commit rewrites the tile
-// in place and stores it with a TMA tensor store (rows past DV are not written).
+// them.  One thread (PT) keeps the next state tiles in flight: one 3-D TMA tensor load per 64-column box into
+// a 1024-byte aligned stage, rows past DV filled with zeros, 16-byte chunks swizzled within each 128-byte row
+// (the 128-byte swizzle, which is also the K-major operand layout of tcgen05.mma and keeps the ldmatrix reads
+// conflict-free).  The same thread issues the tile's MMAs.  q, k, v, a and b of the next item are loaded into
+// registers while the current one is computed, and consecutive items of one key head reuse its normalised q, k
+// and Gram matrices.
 #pragma once
 
 #include <cuda.h>
@@ -41,69 +45,71 @@
 
 namespace gdn {
 
-constexpr int kChunkRows = 128;  // state rows per item: 4 warps x 32
-constexpr int kChunkThreads = 128;
+constexpr int kChunkRows = 128;  // state rows per item: 4 warps x 32 = the MMA's M
+constexpr int kChunkGroupThreads = 128;  // one group of 4 warps works on one item at a time
 constexpr int kChunkMaxT = 8;
+constexpr int kChunkMinDK = 64;  // rows of 64 bf16 at least: whole 128-byte swizzle spans
 constexpr uint32_t kChunkWaitPolls = GDN_WAIT_POLLS;
+constexpr uint32_t kChunkTmemCols = 32;  // tensor-memory columns per group: P has at most 4 T = 32 columns
+constexpr int kChunkMaxGroups = 3;
 
-// Shared-memory plan of one CTA, as byte offsets from a 1024-byte aligned base.
+// Shared-memory plan of one group, as byte offsets from its 1024-byte aligned base; the groups of a CTA sit
+// one after another, then a word for the tensor-memory address.
 template <int DK, bool kCommit, int NS>
 struct ChunkPlan {
-    static constexpr uint32_t SWZ = DK * 2 < 128 ? DK * 2 : 128;  // swizzle span = bytes of one box row
-    static constexpr int BOX_COLS = SWZ / 2;
-    static constexpr int NBOX = DK / BOX_COLS;
-    static constexpr uint32_t BOX_BYTES = kChunkRows * SWZ;
+    static_assert(DK % 64 == 0, "the chunked kernel takes whole 128-byte rows");
+    static constexpr int NBOX = DK / 64;                      // 64-column (128-byte) boxes per row
+    static constexpr uint32_t BOX_BYTES = kChunkRows * 128;   // one box of a stage
     static constexpr uint32_t STAGE_BYTES = kChunkRows * DK * 2;
-    static constexpr uint32_t ROW_BYTES = DK * 2 + 16;  // padded bf16 row of B
     // columns of P: kh hi, kh lo (and qh hi, qh lo in verify mode), T each
-    __host__ __device__ static int ncols(int T) { return kCommit ? 2 * T : 4 * T; }
-    __host__ __device__ static int b_rows(int T) { return ((ncols(T) + 7) / 8) * 8; }  // whole n8 tiles
-    // fp32 row stride of P: verify with even T pads rows to 4T + 4 floats, so that a thread reads its row with
-    // float4 loads (T + 1 odd keeps 8 consecutive rows on 8 distinct 16-byte bank groups); otherwise + 1
-    __host__ __device__ static int p_stride(int T) { return (!kCommit && T % 2 == 0) ? 4 * T + 4 : ncols(T) + 1; }
-    __host__ __device__ static int gram_stride(int T) { return (T + 3) & ~3; }  // padded row of the Gram matrices
-    // Where a warp's 32 rows of P go (verify; the replay commit has a region of its own):
-    //   0  over the warp's own 32 rows of the stage's first box, once its MMAs are done (no CTA barrier);
-    //   1  likewise over its own rows of the first two boxes, 16 P rows in each (rows too long for one box);
-    //   2  over the whole stage, after a CTA barrier (every warp's MMAs done);
-    //   3  a region of its own.
-    __host__ __device__ static int p_mode(int T) {
-        if (kCommit) return 3;
-        const uint32_t row = (uint32_t)p_stride(T) * 4;
-        if (row <= SWZ) return 0;
-        if (NBOX >= 2 && 16u * row <= 32u * SWZ) return 1;
-        if ((uint32_t)kChunkRows * row <= STAGE_BYTES) return 2;
-        return 3;
-    }
-    __host__ __device__ static uint32_t b_off() { return NS * STAGE_BYTES; }
+    __host__ __device__ static constexpr int ncols(int T) { return kCommit ? 2 * T : 4 * T; }
+    // rows of B (one per column of P), padded to the MMA's N: a multiple of 16
+    __host__ __device__ static constexpr int nb(int T) { return (ncols(T) + 15) / 16 * 16; }
+    __host__ __device__ static constexpr uint32_t b_off() { return NS * STAGE_BYTES; }
+    __host__ __device__ static constexpr uint32_t b_bytes(int T) { return (uint32_t)nb(T) * DK * 2; }
     // replay commit: the coefficient tile A2 = [c hi | c lo | c hi | 0] (bf16, rows padded by 16 bytes)
-    __host__ __device__ static int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
-    __host__ __device__ static uint32_t a2_stride(int T) { return (uint32_t)a2_cols(T) * 2 + 16; }
-    // replay commit: bytes of one warp's P rows, later covered by its A2 rows
-    __host__ __device__ static uint32_t warp_region(int T) {
-        const uint32_t pw = 32u * p_stride(T) * 4, aw = 32u * a2_stride(T);
-        return pw > aw ? pw : aw;
-    }
-    __host__ __device__ static uint32_t p_off(int T) { return b_off() + (uint32_t)b_rows(T) * ROW_BYTES; }
-    __host__ __device__ static uint32_t s_off(int T) {
-        if (kCommit) return p_off(T) + 4u * warp_region(T);
-        return p_off(T) + (p_mode(T) < 3 ? 0u : (uint32_t)kChunkRows * p_stride(T) * 4);
-    }
+    __host__ __device__ static constexpr int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
+    __host__ __device__ static constexpr uint32_t a2_stride(int T) { return (uint32_t)a2_cols(T) * 2 + 16; }
+    __host__ __device__ static constexpr uint32_t a2_off(int T) { return b_off() + b_bytes(T); }
     // g, beta (T each), then the Gram matrices, transposed (row t holds kh_s . kh_t, kh_s . qh_t over s)
-    __host__ __device__ static uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
-    // NS mbarriers, then per stage the pool slot (-1: nothing loaded) and the token count of its item
-    __host__ __device__ static uint32_t ctl_off(int T) { return gram_off(T) + 2u * T * gram_stride(T) * 4; }
-    __host__ __device__ static uint32_t bytes(int T) { return ctl_off(T) + NS * 16 + 1024; }  // + alignment slack
+    __host__ __device__ static constexpr uint32_t s_off(int T) {
+        return a2_off(T) + (kCommit ? (uint32_t)kChunkRows * a2_stride(T) : 0u);
+    }
+    __host__ __device__ static constexpr int gram_stride(int T) { return (T + 3) & ~3; }
+    __host__ __device__ static constexpr uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
+    // NS tile mbarriers and the MMA mbarrier, the tensor-memory address and a failure flag, then per stage the
+    // pool slot (-1: nothing loaded) and the token count of its item
+    __host__ __device__ static constexpr uint32_t ctl_off(int T) {
+        return gram_off(T) + 2u * T * gram_stride(T) * 4;
+    }
+    __host__ __device__ static constexpr uint32_t group_bytes(int T) {
+        return (ctl_off(T) + 8u * (NS + 1) + 8u + 8u * NS + 1023u) & ~1023u;
+    }
+    __host__ __device__ static constexpr uint32_t bytes(int T, int G) {
+        return (uint32_t)G * group_bytes(T) + 16u + 1024u;  // + the tensor-memory address, + alignment slack
+    }
 };
 
-// Byte offset of the 16-byte chunk c of row r in a stage: box c / CPB, and inside the box the chunk index
-// XORed with bits 7.. of its linear offset (the TMA 32 / 64 / 128-byte swizzle patterns).
-template <int DK>
-__device__ __forceinline__ uint32_t swz_off(int r, int c) {
-    constexpr uint32_t SWZ = DK * 2 < 128 ? DK * 2 : 128;
-    constexpr int CPB = SWZ / 16;
-    const uint32_t lin = (uint32_t)r * SWZ + (uint32_t)(c % CPB) * 16;
-    return (uint32_t)(c / CPB) * (kChunkRows * SWZ) + (lin ^ (((lin >> 7) & (CPB - 1)) << 4));
+// One group's barrier (named barrier `id`, its 128 threads), and the same with an OR over a predicate.
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kChunkGroupThreads) : "memory");
+}
+__device__ __forceinline__ bool group_sync_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "n"(kChunkGroupThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Byte offset of the 16-byte chunk c (columns 8c .. 8c+7) of row r in a bf16 tile of `rows` rows kept as
+// 64-column boxes of rows x 128 bytes, each 16-byte chunk XORed with bits 7..9 of its linear offset: the layout
+// of a TMA load with the 128-byte swizzle, and the K-major SWIZZLE_128B operand layout of tcgen05.mma.
+__device__ __forceinline__ uint32_t sw128(int rows, int r, int c) {
+    const uint32_t lin = (uint32_t)r * 128 + (uint32_t)(c & 7) * 16;
+    return (uint32_t)(c >> 3) * ((uint32_t)rows * 128) + (lin ^ (((lin >> 7) & 7) << 4));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -167,6 +173,66 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// ---- tcgen05: tensor-memory allocation, MMA issue and completion, loads ------------------------------------
+// Shared-memory matrix descriptor of a K-major bf16 operand in the 128-byte swizzled layout (sw128): start
+// address, stride between 8-row groups 1024 bytes (the leading offset is unused for this layout), descriptor
+// version 1, swizzle mode 2 (128 bytes).  Advancing K by 16 elements inside a 128-byte span adds 32 bytes to
+// the start address; the next 64 columns start one box further.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T, issued by one thread; `accumulate` 0 overwrites D
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// the mbarrier `bar` receives one arrival once every MMA this thread issued before has completed
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {  // one whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t tmem, uint32_t ncols) {  // one whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane (warp w reads lanes 32w .. 32w + 31)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* f) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // T floats from shared memory: float4 loads when the address is 16-byte aligned by construction
 template <int N, bool kVec>
 __device__ __forceinline__ void load_row(const float* src, float (&dst)[N]) {
@@ -185,16 +251,15 @@ __device__ __forceinline__ void load_row(const float* src, float (&dst)[N]) {
     }
 }
 
-// One row's T x T recurrence (T fixed at compile time, so delta stays in registers).  Pr: the row of P,
+// One row's T x T recurrence (T fixed at compile time, so delta stays in registers).  pr: the row of P,
 // [S_0 kh hi | S_0 kh lo | S_0 qh hi | S_0 qh lo]; v: the row's v per token; KKt, KQt: the transposed Gram
 // matrices, rows of TP = gram_stride(T) floats.
-template <int T>
-__device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const float* Pr, const float (&v)[kChunkMaxT],
-                                               const float* gs, const float* bs, const float* KKt, const float* KQt,
-                                               bool live, int64_t o0, int64_t tok_out) {
+template <int T, int NP>
+__device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const float (&pr)[NP],
+                                               const float (&v)[kChunkMaxT], const float* gs, const float* bs,
+                                               const float* KKt, const float* KQt, bool live, int64_t o0,
+                                               int64_t tok_out) {
     constexpr int TP = (T + 3) & ~3;
-    float pr[4 * T];
-    load_row<4 * T, T % 2 == 0>(Pr, pr);
     float g[T], be[T];
     load_row<T, false>(gs, g);
     load_row<T, false>(bs, be);
@@ -227,24 +292,21 @@ __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const f
     }
 }
 
-// Replay commit: one row's coefficients c_s = G(s, L-1) delta_s (s < L, 0 beyond), read from its P row and,
-// after the warp's __syncwarp, written as its row of A2 = [c hi | c lo | c hi | 0] in bf16 (hi = c rounded,
-// lo = c - hi rounded), to be multiplied by [kh hi; kh hi; kh lo].
-template <int T>
-__device__ __forceinline__ void row_coefficients(const float* Pr, const float (&v)[kChunkMaxT], const float* gs,
+// Replay commit: one row's coefficients c_s = G(s, L-1) delta_s (s < L, 0 beyond) from its P row, written as
+// its row of A2 = [c hi | c lo | c hi | 0] in bf16 (hi = c rounded, lo = c - hi rounded), to be multiplied by
+// [kh hi; kh hi; kh lo].
+template <int T, int NP>
+__device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const float (&v)[kChunkMaxT], const float* gs,
                                                  const float* bs, const float* KKt, int L, unsigned char* a2row) {
     constexpr int TP = (T + 3) & ~3;
     float delta[T];
     float gamma = 1.f;
-    float a[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) a[t] = Pr[t] + Pr[T + t];  // S_0 kh_t
 #pragma unroll
     for (int t = 0; t < T; ++t) {
         delta[t] = 0.f;
         if (t < L) {
             gamma *= gs[t];
-            float u = gamma * a[t];
+            float u = gamma * (pr[t] + pr[T + t]);  // gamma_t S_0 kh_t
             float G = 1.f;
 #pragma unroll
             for (int s = t - 1; s >= 0; --s) {
@@ -272,7 +334,6 @@ __device__ __forceinline__ void row_coefficients(const float* Pr, const float (&
     }
     constexpr int W = 3 * T <= 16 ? 16 : 32;
     auto col = [&](int i) -> float { return i < T ? hi[i] : (i < 2 * T ? lo[i - T] : (i < 3 * T ? hi[i - 2 * T] : 0.f)); };
-    __syncwarp();  // every lane of the warp has read its P row
     uint32_t w[W / 2];
 #pragma unroll
     for (int i = 0; i < W; i += 2) w[i / 2] = bf16x2_bits(col(i), col(i + 1));
@@ -281,9 +342,11 @@ __device__ __forceinline__ void row_coefficients(const float* Pr, const float (&
         *reinterpret_cast<uint4*>(a2row + 16 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
-// Per-item registers loaded one item ahead, kept in their storage type until used (a conversion right after
-// the load would wait for it): q / k (this lane's 16-byte pieces of every vector pass), v of row tid, and, on
-// the last warp, a and b of token tid - (128 - 32) with the head's A_log and dt_bias.
+// Per-item inputs in registers, kept in their storage type until used (a conversion right after the load would
+// wait for it): q / k (this lane's 16-byte pieces of every vector pass), v of row tid, and, on the last warp, a
+// and b of token tid - (128 - 32) with the head's A_log and dt_bias.  Each field is loaded for the next item
+// right after its last use in the current one, so every load has about one item of lead time and none is
+// waited for by a register copy.
 template <int DK, typename InT, bool kCommit>
 struct ItemRegs {
     static constexpr int VPASS = 4 * (32 / (DK / 8));
@@ -294,11 +357,111 @@ struct ItemRegs {
     float A_log, dt_bias;
 };
 
+// After the tile's MMA: every thread reads the P row of its state row from tensor memory, then runs the row's
+// recurrence (verify: o), or forms its coefficients and the CTA rewrites the tile and stores it (replay commit).
+template <int T, int DK, typename InT, bool kCommit, int NS>
+__device__ __forceinline__ void chunk_rows(const RecurrentParams& p, const CUtensorMap* tmap, uint32_t tmem,
+                                           unsigned char* sm, uint32_t base, uint32_t stage,
+                                           const float (&vr)[kChunkMaxT], int b, int h, int row0, int nrows, int slot,
+                                           int L, int bar_id) {
+    using CS = ChunkPlan<DK, kCommit, NS>;
+    constexpr int NP = CS::nb(T);  // columns of P in tensor memory
+    constexpr int TP = (T + 3) & ~3;
+    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5, lane = tid & 31;
+    const float* gs = reinterpret_cast<const float*>(sm + CS::s_off(T));
+    const float* bs = gs + T;
+    const float* KK = reinterpret_cast<const float*>(sm + CS::gram_off(T));
+    const float* KQ = KK + T * TP;
+    float pr[NP];
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < NP; c += 16) tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c, pr + c);
+    tmem_wait_ld();
+    if constexpr (!kCommit) {
+        const bool live = tid < nrows;
+        const int64_t o0 = ((int64_t)b * T * p.HV + h) * p.DV + row0 + tid;
+        row_recurrence<T, NP>(p, pr, vr, gs, bs, KK, KQ, live, o0, (int64_t)p.HV * p.DV);
+    } else {
+        constexpr int PT = 64;
+        constexpr int NB = CS::nb(T);
+        constexpr uint32_t A2S = CS::a2_stride(T);
+        unsigned char* a2w = sm + CS::a2_off(T) + warp * 32 * A2S;  // this warp's 32 rows of A2
+        row_coefficients<T, NP>(pr, vr, gs, bs, KK, L, a2w + lane * A2S);
+        float gamma = 1.f;
+        for (int t = 0; t < L; ++t) gamma *= gs[t];
+        __syncwarp();
+        // S_L = gamma S_0 + A2 [kh hi; kh hi; kh lo] on mma.sync, 16 columns at a time: S_0 comes in as the
+        // accumulator (ldmatrix gives the m16n8 accumulator layout of each 8 x 8 block) and goes back over itself
+        // (stmatrix), each warp on its own rows
+        constexpr int KS2 = CS::a2_cols(T) / 16;
+        const uint32_t bbase = base + CS::b_off();
+        const uint32_t a2b = base + CS::a2_off(T) + warp * 32 * A2S + (uint32_t)(lane & 15) * A2S + (lane >> 4) * 16;
+        const int ra_row = warp * 32 + (lane & 15);
+        uint32_t af[KS2][2][4];  // [k step][m tile]
+#pragma unroll
+        for (int ks = 0; ks < KS2; ++ks)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                ldsm_x4(a2b + mt * 16 * A2S + ks * 32, af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3]);
+        int brow[KS2];  // row of B2 (a row of B) that this lane addresses, per k step
+#pragma unroll
+        for (int ks = 0; ks < KS2; ++ks) {
+            const int kidx = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            brow[ks] = kidx < T ? kidx : (kidx < 2 * T ? kidx - T : (kidx < 3 * T ? kidx - T : 0));
+        }
+#pragma unroll 2
+        for (int np = 0; np < DK / 16; ++np) {
+            float d[2][2][4];
+            uint32_t sa[2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                sa[mt] = stage + sw128(kChunkRows, ra_row + mt * 16, 2 * np + (lane >> 4));
+                uint32_t s0, s1, s2, s3;
+                ldsm_x4(sa[mt], s0, s1, s2, s3);
+                const float2 f0 = bf16x2_to_float2(s0), f1 = bf16x2_to_float2(s1);
+                const float2 f2 = bf16x2_to_float2(s2), f3 = bf16x2_to_float2(s3);
+                d[mt][0][0] = gamma * f0.x;
+                d[mt][0][1] = gamma * f0.y;
+                d[mt][0][2] = gamma * f1.x;
+                d[mt][0][3] = gamma * f1.y;
+                d[mt][1][0] = gamma * f2.x;
+                d[mt][1][1] = gamma * f2.y;
+                d[mt][1][2] = gamma * f3.x;
+                d[mt][1][3] = gamma * f3.y;
+            }
+#pragma unroll
+            for (int ks = 0; ks < KS2; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4_trans(bbase + sw128(NB, brow[ks], 2 * np + (lane >> 4)), b00, b01, b10, b11);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mma_bf16_16816(d[mt][0], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b00, b01);
+                    mma_bf16_16816(d[mt][1], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b10, b11);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                stsm_x4(sa[mt], bf16x2_bits(d[mt][0][0], d[mt][0][1]), bf16x2_bits(d[mt][0][2], d[mt][0][3]),
+                        bf16x2_bits(d[mt][1][0], d[mt][1][1]), bf16x2_bits(d[mt][1][2], d[mt][1][3]));
+        }
+        fence_proxy_async_smem();  // the stmatrix writes above, then the TMA store reads them
+        group_sync(bar_id);
+        if (tid == PT) {
+#pragma unroll
+            for (int j = 0; j < CS::NBOX; ++j)
+                tma_store_3d(tmap, j * 64, row0, slot * p.HV + h, stage + j * CS::BOX_BYTES);
+            bulk_commit_group();
+        }
+    }
+}
 
-template <int DK, typename InT, bool kCommit, int NS>
-__global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(const RecurrentParams p,
-                                                                          const __grid_constant__ CUtensorMap tmap,
-                                                                          int n_items, int per_cta) {
+// A kernel that allocates tensor memory runs one CTA per SM, so the CTA holds G groups of 4 warps, each an
+// independent item pipeline (its own stages, B, Gram matrices, mbarriers, named barrier 1 + g and 32 columns
+// of tensor memory); group g of CTA c walks the items of virtual CTA c G + g.
+template <int DK, typename InT, bool kCommit, int NS, int G>
+__global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
+    gdn_verify_chunked_kernel(const RecurrentParams p, const __grid_constant__ CUtensorMap tmap, int n_items,
+                              int per_cta) {
     using CS = ChunkPlan<DK, kCommit, NS>;
     using QK = Slice8<InT>;
     constexpr int ROWS = kChunkRows;
@@ -306,29 +469,37 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     constexpr int LPV = DK / 8;       // lanes per q or k vector (8 columns each)
     constexpr int VPW = 32 / LPV;     // vectors per warp per pass
     constexpr int VPASS = 4 * VPW;    // vectors per CTA pass
-    constexpr int CPR = DK / 8;       // 16-byte chunks per state row
-    static_assert(DK % 16 == 0 && LPV <= 32 && ROWS % CPR == 0, "DK");
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr bool kEarly = !kCommit;  // verify: a stage is refilled as soon as its MMA has completed
+    static_assert(LPV <= 32, "DK");
+    const int grp = threadIdx.x / kChunkGroupThreads;
+    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5, lane = tid & 31;
+    const int bar_id = 1 + grp;  // named barrier 0 is the whole CTA's
     const int T = p.T;
     const int NRB = (p.DV + ROWS - 1) / ROWS;
     const int R = p.HV / p.HK;  // value heads per key head
-    const int beg = blockIdx.x * per_cta;
+    // virtual CTA grp * gridDim.x + blockIdx.x: with few items, group 0 of every CTA gets them first
+    const int beg = (int)min((int64_t)n_items, ((int64_t)grp * gridDim.x + blockIdx.x) * per_cta);
     const int end = min(n_items, beg + per_cta);
-    if (beg >= end) return;
-    // roles besides the shared work: warp 1 forms the Gram matrices, thread PT of warp 2 issues the TMA
-    // loads and stores (and alone waits on its bulk groups), warp 3 computes the gates
+    // roles in a group besides the shared work: warp 1 forms the Gram matrices (warp 0 too in verify), thread PT
+    // of warp 2 issues the TMA loads and stores and the tile's MMAs (and alone waits on the tiles and its bulk
+    // groups), warp 3 computes the gates; warp 0 of the CTA allocates the tensor memory for every group
     constexpr int PT = 64;
     constexpr int GATE_T0 = ROWS - 32;
 
     extern __shared__ unsigned char ch_smem[];
     const uint32_t raw_base = smem_u32(ch_smem);
     const uint32_t pad = ((raw_base + 1023u) & ~1023u) - raw_base;
-    unsigned char* sm = ch_smem + pad;
-    const uint32_t base = raw_base + pad;
-    const uint32_t ctl = base + CS::ctl_off(T);  // mbarrier of stage s at ctl + 8 s
-    int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(T) + NS * 8);
+    unsigned char* sm = ch_smem + pad + grp * CS::group_bytes(T);  // this group's part
+    const uint32_t base = raw_base + pad + grp * CS::group_bytes(T);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ch_smem + pad + G * CS::group_bytes(T));
+    const uint32_t ctl = base + CS::ctl_off(T);  // mbarrier of stage s at ctl + 8 s; the MMA's at ctl + 8 NS
+    const uint32_t mma_bar = ctl + 8 * NS;
+    volatile int* fail_flag = reinterpret_cast<volatile int*>(sm + CS::ctl_off(T) + 8 * (NS + 1));
+    int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(T) + 8 * (NS + 1) + 8);
     int* st_len = st_slot + NS;
-    unsigned char* Bs = sm + CS::b_off();  // rows: k hi (T) | k lo (T) | q hi (T) | q lo (T) | zeros
+    unsigned char* Bs = sm + CS::b_off();  // rows: k hi (T) | k lo (T) | q hi (T) | q lo (T) | padding, swizzled
+    const uint32_t bbase = base + CS::b_off();
+    const int NB = CS::nb(T);
     float* gs = reinterpret_cast<float*>(sm + CS::s_off(T));
     float* bs = gs + T;
     const int TP = CS::gram_stride(T);
@@ -360,19 +531,19 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
             mbar_arrive_expect_tx(bar, CS::STAGE_BYTES);
 #pragma unroll
             for (int j = 0; j < CS::NBOX; ++j)
-                tma_load_3d(base + s * CS::STAGE_BYTES + j * CS::BOX_BYTES, &tmap, j * CS::BOX_COLS, rb * ROWS,
-                            slot * p.HV + h, bar);
+                tma_load_3d(base + s * CS::STAGE_BYTES + j * CS::BOX_BYTES, &tmap, j * 64, rb * ROWS, slot * p.HV + h,
+                            bar);
         }
     };
     const int vj0 = warp * VPW + lane / LPV;  // this lane's vector in the first pass (before the j0 offset)
-    const int vc = lane % LPV;                // its columns [8 vc, 8 vc + 8)
+    const int vc = lane % LPV;                // its columns [8 vc, 8 vc + 8): chunk vc of the row
     const int j0 = kCommit ? T : 0;           // vectors j in [j0, 2T): q_j for j < T, k_{j-T} otherwise
     auto vec_ptr = [&](int b, int hk, int j) -> const InT* {
         const int t = j < T ? j : j - T;
         return static_cast<const InT*>(j < T ? p.q : p.k) + (((int64_t)b * T + t) * p.HK + hk) * DK + 8 * vc;
     };
     using IR = ItemRegs<DK, InT, kCommit>;
-    auto load_regs = [&](const ItemPos& ip, bool need_qk, IR& r) {
+    auto load_qk = [&](const ItemPos& ip, bool need_qk, IR& r) {
 #pragma unroll
         for (int ps = 0; ps < IR::NPASS; ++ps) {
             const int j = j0 + vj0 + ps * VPASS;
@@ -380,6 +551,8 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
             for (int c = 0; c < QK::NC; ++c) r.raw[ps][c] = make_uint4(0, 0, 0, 0);
             if (need_qk && j < 2 * T) QK::load_global(vec_ptr(ip.b, ip.hk, j), r.raw[ps]);
         }
+    };
+    auto load_v = [&](const ItemPos& ip, IR& r) {
         const int row = ip.rb * ROWS + tid;
         const InT* vsrc = static_cast<const InT*>(p.v) + ((int64_t)ip.b * T * p.HV + ip.h) * p.DV + row;
 #pragma unroll
@@ -387,6 +560,8 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
             r.v[t] = InT(0.f);
             if (t < T && row < p.DV) r.v[t] = vsrc[(int64_t)t * p.HV * p.DV];
         }
+    };
+    auto load_ab = [&](const ItemPos& ip, IR& r) {
         r.a = r.b = InT(0.f);
         r.A_log = r.dt_bias = 0.f;
         if (tid >= GATE_T0 && tid - GATE_T0 < T) {
@@ -399,43 +574,53 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
     };
 
     ItemPos pos = ItemPos::of(beg, NRB, p.HV, R);  // the current item
-    ItemPos ipos = pos;           // thread PT: the next item to issue, with its slot and token count
+    ItemPos ipos = pos;  // thread PT: the next item to issue (number nis), with its slot and token count
+    int nis = beg;
     int islot = 0, ilen = 0;
-    if (tid == PT) {
-        for (int s = 0; s < NS; ++s) mbar_init(ctl + 8 * s, 1);
+    auto issue_next = [&](int s) {  // thread PT: issue item nis into stage s, then look up the one after it
+        issue(ipos, islot, ilen, s);
+        ipos.next(NRB, p.HV, R);
+        if (++nis < end) {
+            islot = p.indices[ipos.b];
+            ilen = kCommit ? p.steps[ipos.b] : T;
+        }
+    };
+    constexpr uint32_t kCols = G == 1 ? 32u : (G == 2 ? 64u : 128u);  // a power of 2, at least 32
+    if (threadIdx.x < 32) tmem_alloc(smem_u32(tmem_slot), kCols);
+    if (tid == PT && beg < end) {
+        for (int s = 0; s <= NS; ++s) mbar_init(ctl + 8 * s, 1);
         fence_mbar_init();
+        *fail_flag = 0;
         islot = p.indices[ipos.b];
         ilen = kCommit ? p.steps[ipos.b] : T;
-        for (int j = 0; j < NS - 1 && beg + j < end; ++j) {
-            issue(ipos, islot, ilen, j);
-            ipos.next(NRB, p.HV, R);
-            if (beg + j + 1 < end) {
-                islot = p.indices[ipos.b];
-                ilen = kCommit ? p.steps[ipos.b] : T;
-            }
-        }
+        for (int j = 0; j < (kEarly ? NS : NS - 1) && nis < end; ++j) issue_next(j);
     }
-    IR cur, nxt;
-    load_regs(pos, true, cur);
+    // B's padding rows stay zero (their columns of P are never read)
+    for (int i2 = CS::ncols(T) * (DK / 8) + tid; i2 < NB * (DK / 8); i2 += ROWS)
+        *reinterpret_cast<uint4*>(Bs + sw128(NB, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();  // the padding rows are read by the tensor cores too
+    IR in;  // the current item's inputs (each field refilled for the next item after its last use)
+    if (beg < end) {
+        load_qk(pos, true, in);
+        load_v(pos, in);
+        load_ab(pos, in);
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem = tmem_base + kChunkTmemCols * grp;  // this group's columns
 
-    uint32_t phase = 0;  // bit s: parity of the next completion of stage s
+    uint32_t phase = 0;   // bit s: parity of the next completion of stage s
+    uint32_t mphase = 0;  // parity of the next completion of the MMA barrier
     int prev_b = -1, prev_hk = -1;
+    bool failed = false;
     for (int i = 0, it = beg; it < end; ++i, ++it) {
         const int st = i % NS;
         const int b = pos.b, h = pos.h, rb = pos.rb;
         const int hk = pos.hk;
         const int row0 = rb * ROWS;
         const int nrows = min(ROWS, p.DV - row0);
-        const bool refill = it + NS - 1 < end;
-        auto issue_ahead = [&] {  // thread PT: item it + NS - 1, then look up the slot of the one after it
-            issue(ipos, islot, ilen, (i + NS - 1) % NS);
-            ipos.next(NRB, p.HV, R);
-            if (it + NS < end) {
-                islot = p.indices[ipos.b];
-                ilen = kCommit ? p.steps[ipos.b] : T;
-            }
-        };
         const int slot = st_slot[st];
         const int L = st_len[st];
         const bool active = slot >= 0;
@@ -444,7 +629,6 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
         prev_hk = hk;
         ItemPos npos = pos;
         npos.next(NRB, p.HV, R);
-        if (it + 1 < end) load_regs(npos, !(npos.b == b && npos.hk == hk), nxt);
 
         if (active && !reuse) {
             // token prologue: normalise q and k into bf16 hi + lo rows of B
@@ -453,7 +637,7 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
                 if (j0 + pass * VPASS >= 2 * T) break;
                 const int j = j0 + vj0 + pass * VPASS;
                 float2 x[4];
-                QK::unpack(cur.raw[pass], x);
+                QK::unpack(in.raw[pass], x);
                 float ss = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ss = fmaf(x[e].x, x[e].x, fmaf(x[e].y, x[e].y, ss));
@@ -461,76 +645,65 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
                 for (int m = 1; m < LPV; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
                 if (j < 2 * T) {
                     const float rn = rsqrtf(ss + p.l2_eps);
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[2 * e] = x[e].x * rn;
-                        f[2 * e + 1] = x[e].y * rn;
-                    }
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(f[2 * e] - __low2float(hi2),
-                                                                         f[2 * e + 1] - __high2float(hi2));
+                        const float f0 = x[e].x * rn, f1 = x[e].y * rn;
+                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(f0, f1);
+                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(f0 - __low2float(hi2), f1 - __high2float(hi2));
                         hw[e] = *reinterpret_cast<const uint32_t*>(&hi2);
                         lw[e] = *reinterpret_cast<const uint32_t*>(&lo2);
                     }
                     const int t = j < T ? j : j - T;
                     const int hi_row = j < T ? 2 * T + t : t;  // q hi rows start at 2T, k hi rows at 0
-                    *reinterpret_cast<uint4*>(Bs + hi_row * CS::ROW_BYTES + 16 * vc) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Bs + (hi_row + T) * CS::ROW_BYTES + 16 * vc) =
-                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    *reinterpret_cast<uint4*>(Bs + sw128(NB, hi_row, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Bs + sw128(NB, hi_row + T, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
-            for (int i2 = CS::ncols(T) * (DK / 8) + tid; i2 < CS::b_rows(T) * (DK / 8); i2 += ROWS) {  // B padding
-                const int r = i2 / (DK / 8), c = i2 - r * (DK / 8);
-                *reinterpret_cast<uint4*>(Bs + r * CS::ROW_BYTES + 16 * c) = make_uint4(0, 0, 0, 0);
-            }
+            fence_proxy_async_smem();  // B is written here and read by the tensor cores' MMA
         }
-        __syncthreads();
-        // the refill of the stage the last item used (the replay commit first waits for its store to have read
-        // it) and the gates (needed only after the tile's wait) go in parallel with the Gram matrices
-        if (refill && tid == PT) {
-            if (kCommit) bulk_wait_read_all();
-            issue_ahead();
+        if (it + 1 < end) load_qk(npos, !(npos.b == b && npos.hk == hk), in);
+        tc_fence_before();
+        group_sync(bar_id);
+        // replay commit: the refill of the stage the last item used, once its store has read it
+        if (!kEarly && tid == PT && nis < end && nis == it + NS - 1) {
+            bulk_wait_read_all();
+            issue_next((i + NS - 1) % NS);
         }
         if (active && tid >= GATE_T0 && tid - GATE_T0 < T) {
-            gs[tid - GATE_T0] = gate(cur.A_log, to_f32(cur.a), cur.dt_bias);
-            bs[tid - GATE_T0] = sigmoid(to_f32(cur.b));
+            gs[tid - GATE_T0] = gate(in.A_log, to_f32(in.a), in.dt_bias);
+            bs[tid - GATE_T0] = sigmoid(to_f32(in.b));
         }
-
+        if (it + 1 < end) load_ab(npos, in);
         if (active && !reuse && (warp == 1 || (!kCommit && warp == 0))) {
-            // Gram matrices kh.kh (and kh.qh in verify mode) on the tensor cores, from the hi + lo rows of B:
-            // A rows 0..7 address kh_0..kh_7 and rows 8..15 kl_0..kl_7, B columns 8 nb .. 8 nb + 7 address
-            // block nb of B (kh, kl, qh, ql); rows past T point at row 0 and their products are dropped.  The
-            // four products of a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.  Warp 1 forms kh.kh from
-            // blocks 0, 1; in verify, warp 0 forms kh.qh from blocks 2, 3 at the same time.
-            constexpr int NB = 2;
+            // Gram matrices kh.kh (and kh.qh in verify mode) on mma.sync, from the hi + lo rows of B: A rows
+            // 0..7 address kh_0..kh_7 and rows 8..15 kl_0..kl_7, B columns 8 nb .. 8 nb + 7 address block nb of B
+            // (kh, kl, qh, ql); rows past T point at row 0 and their products are dropped.  The four products of
+            // a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.  Warp 1 forms kh.kh from blocks 0, 1; in
+            // verify, warp 0 forms kh.qh from blocks 2, 3 at the same time.
+            constexpr int NBLK = 2;
             const int nb0 = warp == 1 ? 0 : 2;
             const int m = lane & 15;
             const int arow = m < 8 ? (m < T ? m : 0) : (m - 8 < T ? T + m - 8 : 0);
-            const uint32_t a_addr = base + CS::b_off() + (uint32_t)arow * CS::ROW_BYTES + (lane >> 4) * 16;
-            uint32_t b_addr[NB];
+            int brow[NBLK];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
+            for (int nb = 0; nb < NBLK; ++nb) {
                 const int jr = lane & 7;
-                const int brow = jr < T ? (nb0 + nb) * T + jr : 0;
-                b_addr[nb] = base + CS::b_off() + (uint32_t)brow * CS::ROW_BYTES + ((lane >> 3) & 1) * 16;
+                brow[nb] = jr < T ? (nb0 + nb) * T + jr : 0;
             }
-            float g[NB][4];
+            float g[NBLK][4];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
+            for (int nb = 0; nb < NBLK; ++nb)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) g[nb][c] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(a_addr + ks * 32, a0, a1, a2, a3);
+                ldsm_x4(bbase + sw128(NB, arow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
+                for (int nb = 0; nb < NBLK; ++nb) {
                     uint32_t b0, b1;
-                    ldsm_x2(b_addr[nb] + ks * 32, b0, b1);
+                    ldsm_x2(bbase + sw128(NB, brow[nb], 2 * ks + ((lane >> 3) & 1)), b0, b1);
                     mma_bf16_16816(g[nb], a0, a1, a2, a3, b0, b1);
                 }
             }
@@ -542,209 +715,81 @@ __global__ void __launch_bounds__(kChunkThreads, 3) gdn_verify_chunked_kernel(co
                     (warp == 1 ? KK : KQ)[t_ * TP + s_] = (g[0][e] + g[1][e]) + (g[0][2 + e] + g[1][2 + e]);
             }
         }
-        // the state tile: bounded wait (uniform: every thread takes the same branch)
-        bool ok = true;
-        if (active) {
-            ok = mbar_wait_bounded(ctl + 8 * st, (phase >> st) & 1u, kChunkWaitPolls);
-            phase ^= 1u << st;
+        // P = S_0 [kh hi | kh lo | qh hi | qh lo]^T on the tensor cores, issued by PT once the tile has landed
+        if (active && tid == PT) {
+            if (mbar_wait_bounded(ctl + 8 * st, (phase >> st) & 1u, kChunkWaitPolls)) {
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(ROWS, NB);
+                const uint32_t stage = base + st * CS::STAGE_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const uint32_t koff = (uint32_t)((ks & 3) * 32);  // 16 columns further inside the 128-byte span
+                    const uint64_t ad = umma_desc_sw128(stage + (uint32_t)(ks >> 2) * CS::BOX_BYTES + koff);
+                    const uint64_t bd = umma_desc_sw128(bbase + (uint32_t)(ks >> 2) * (uint32_t)NB * 128u + koff);
+                    umma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(mma_bar);
+            } else {
+                *fail_flag = 1;
+                mbar_arrive(mma_bar);  // releases the other threads' wait on the MMA; they see the flag
+            }
         }
-        if (__syncthreads_or(!ok)) {
+        if (active) phase ^= 1u << st;
+        bool mok = true;
+        if (active) {
+            mok = mbar_wait_bounded(mma_bar, mphase, kChunkWaitPolls);
+            mphase ^= 1u;
+        }
+        // every thread has seen the MMA complete (so the stage and B are read); the Gram matrices and the gates
+        // are in place
+        if (group_sync_or(bar_id, !mok || (active && *fail_flag != 0))) {
+            failed = true;
             if (tid == PT) {
                 if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
-                // drain every tile still in flight (this one and the ones issued ahead) before leaving
-                mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
-                for (int j = 1; j < NS && it + j < end; ++j) {
+                // drain what is in flight before leaving: this item's tile and MMA, and the tiles issued ahead
+                if (active) {
+                    mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
+                    mbar_wait_bounded(mma_bar, mphase ^ 1u, kChunkWaitPolls);
+                }
+                for (int j = 1; j < NS && it + j < nis; ++j) {
                     const int s2 = (i + j) % NS;
                     if (st_slot[s2] >= 0) mbar_wait_bounded(ctl + 8 * s2, (phase >> s2) & 1u, kChunkWaitPolls);
                 }
                 if (kCommit) bulk_wait_all();
             }
-            return;
+            break;
         }
+        // verify: the stage is free as soon as its MMA has completed
+        if (kEarly && tid == PT && nis < end) issue_next(st);
 
+        float vr[kChunkMaxT];
+#pragma unroll
+        for (int t = 0; t < kChunkMaxT; ++t) vr[t] = to_f32(in.v[t]);
+        if (it + 1 < end) load_v(npos, in);
         if (active) {
             const uint32_t stage = base + st * CS::STAGE_BYTES;
-            const int ra_row = warp * 32 + (lane & 15);  // the row this lane addresses in ldmatrix / stmatrix
-            // this warp's P rows 0..15 and 16..31 (pbase[m] + r * p_stride, r < 16)
-            float* pbase[2];
-            {
-                const int ps = CS::p_stride(T);
-                unsigned char* own = sm + st * CS::STAGE_BYTES + warp * 32 * CS::SWZ;  // its rows in box 0
-                float* Pw = kCommit              ? reinterpret_cast<float*>(sm + CS::p_off(T) + warp * CS::warp_region(T))
-                            : CS::p_mode(T) <= 1 ? reinterpret_cast<float*>(own)
-                            : CS::p_mode(T) == 2 ? reinterpret_cast<float*>(sm + st * CS::STAGE_BYTES) + warp * 32 * ps
-                                                 : reinterpret_cast<float*>(sm + CS::p_off(T)) + warp * 32 * ps;
-                pbase[0] = Pw;
-                pbase[1] = CS::p_mode(T) == 1 ? reinterpret_cast<float*>(own + CS::BOX_BYTES) : Pw + 16 * ps;
-            }
-            // P = S_0 [kh hi | kh lo | qh hi | qh lo]^T on the tensor cores: warp w, rows [32w, 32w + 32)
-            {
-                const int NT8 = CS::b_rows(T) / 8;
-                float acc[2][4][4];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[mt][nt][c] = 0.f;
-                const int ra = ra_row;
-                const uint32_t b_base =
-                    base + CS::b_off() + (uint32_t)(lane & 7) * CS::ROW_BYTES + ((lane >> 3) & 1) * 16;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    uint32_t a[2][4];
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-                        ldsm_x4(stage + swz_off<DK>(ra + mt * 16, 2 * ks + (lane >> 4)), a[mt][0], a[mt][1], a[mt][2],
-                                a[mt][3]);
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        if (nt < NT8) {
-                            uint32_t b0, b1;
-                            ldsm_x2(b_base + nt * 8 * CS::ROW_BYTES + ks * 32, b0, b1);
-#pragma unroll
-                            for (int mt = 0; mt < 2; ++mt)
-                                mma_bf16_16816(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], b0, b1);
-                        }
-                    }
-                }
-                if (CS::p_mode(T) == 2)
-                    __syncthreads();  // every warp's A reads are done before P covers the stage
-                else
-                    __syncwarp();  // the warp's A reads are done before P covers its rows
-                const int ps = CS::p_stride(T), ncol = CS::ncols(T);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int r = lane >> 2;  // row within the m tile; pbase[mt] holds the tile's first row
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        const int c = nt * 8 + (lane & 3) * 2;
-                        if (nt < NT8) {
-                            if (c < ncol) {
-                                pbase[mt][r * ps + c] = acc[mt][nt][0];
-                                pbase[mt][(r + 8) * ps + c] = acc[mt][nt][2];
-                            }
-                            if (c + 1 < ncol) {
-                                pbase[mt][r * ps + c + 1] = acc[mt][nt][1];
-                                pbase[mt][(r + 8) * ps + c + 1] = acc[mt][nt][3];
-                            }
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            float* Pr = pbase[lane >> 4] + (lane & 15) * CS::p_stride(T);
-            float vr[kChunkMaxT];
-#pragma unroll
-            for (int t = 0; t < kChunkMaxT; ++t) vr[t] = to_f32(cur.v[t]);
-
-            if constexpr (kCommit) {
-                // per row: the coefficients of the final state, as this warp's rows of A2
-                unsigned char* a2w = sm + CS::p_off(T) + warp * CS::warp_region(T);
-                switch (T) {
-                case 1: row_coefficients<1>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 2: row_coefficients<2>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 3: row_coefficients<3>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 4: row_coefficients<4>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 5: row_coefficients<5>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 6: row_coefficients<6>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                case 7: row_coefficients<7>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                default: row_coefficients<8>(Pr, vr, gs, bs, KK, L, a2w + lane * CS::a2_stride(T)); break;
-                }
-                float gamma = 1.f;
-                for (int t = 0; t < L; ++t) gamma *= gs[t];
-                __syncwarp();
-                // S_L = gamma S_0 + A2 [kh hi; kh hi; kh lo] on the tensor cores, 16 columns at a time: S_0 comes
-                // in as the accumulator (ldmatrix gives the m16n8 accumulator layout of each 8 x 8 block) and
-                // goes back over itself (stmatrix), each warp on its own rows
-                const int KS2 = CS::a2_cols(T) / 16;
-                const uint32_t a2b = base + CS::p_off(T) + warp * CS::warp_region(T) +
-                                     (uint32_t)(lane & 15) * CS::a2_stride(T) + (lane >> 4) * 16;
-                uint32_t af[2][2][4];  // [k step][m tile]
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-                        if (ks < KS2)
-                            ldsm_x4(a2b + mt * 16 * CS::a2_stride(T) + ks * 32, af[ks][mt][0], af[ks][mt][1],
-                                    af[ks][mt][2], af[ks][mt][3]);
-                uint32_t brow[2];  // row of B2 (a row of B) that this lane addresses, per k step
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int kidx = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int r = kidx < T ? kidx : (kidx < 2 * T ? kidx - T : (kidx < 3 * T ? kidx - T : 0));
-                    brow[ks] = base + CS::b_off() + (uint32_t)r * CS::ROW_BYTES + (lane >> 4) * 16;
-                }
-#pragma unroll 2
-                for (int np = 0; np < DK / 16; ++np) {
-                    float d[2][2][4];
-                    uint32_t sa[2];
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        sa[mt] = stage + swz_off<DK>(ra_row + mt * 16, 2 * np + (lane >> 4));
-                        uint32_t s0, s1, s2, s3;
-                        ldsm_x4(sa[mt], s0, s1, s2, s3);
-                        const float2 f0 = bf16x2_to_float2(s0), f1 = bf16x2_to_float2(s1);
-                        const float2 f2 = bf16x2_to_float2(s2), f3 = bf16x2_to_float2(s3);
-                        d[mt][0][0] = gamma * f0.x;
-                        d[mt][0][1] = gamma * f0.y;
-                        d[mt][0][2] = gamma * f1.x;
-                        d[mt][0][3] = gamma * f1.y;
-                        d[mt][1][0] = gamma * f2.x;
-                        d[mt][1][1] = gamma * f2.y;
-                        d[mt][1][2] = gamma * f3.x;
-                        d[mt][1][3] = gamma * f3.y;
-                    }
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        if (ks < KS2) {
-                            uint32_t b00, b01, b10, b11;
-                            ldsm_x4_trans(brow[ks] + np * 32, b00, b01, b10, b11);
-#pragma unroll
-                            for (int mt = 0; mt < 2; ++mt) {
-                                mma_bf16_16816(d[mt][0], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b00, b01);
-                                mma_bf16_16816(d[mt][1], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b10, b11);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-                        stsm_x4(sa[mt], bf16x2_bits(d[mt][0][0], d[mt][0][1]), bf16x2_bits(d[mt][0][2], d[mt][0][3]),
-                                bf16x2_bits(d[mt][1][0], d[mt][1][1]), bf16x2_bits(d[mt][1][2], d[mt][1][3]));
-                }
-                fence_proxy_async_smem();  // the stmatrix writes above, then the TMA store reads them
-                __syncthreads();
-                if (tid == PT) {
-#pragma unroll
-                    for (int j = 0; j < CS::NBOX; ++j)
-                        tma_store_3d(&tmap, j * CS::BOX_COLS, row0, slot * p.HV + h, stage + j * CS::BOX_BYTES);
-                    bulk_commit_group();
-                }
-            } else {
-                // per row (one thread each, in the warp that computed it): the recurrence and the outputs
-                const int r = warp * 32 + lane;
-                const bool live = r < nrows;
-                const int64_t o0 = ((int64_t)b * T * p.HV + h) * p.DV + row0 + r;
-                const int64_t tok_out = (int64_t)p.HV * p.DV;
-                switch (T) {
-                case 1: row_recurrence<1>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 2: row_recurrence<2>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 3: row_recurrence<3>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 4: row_recurrence<4>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 5: row_recurrence<5>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 6: row_recurrence<6>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                case 7: row_recurrence<7>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                default: row_recurrence<8>(p, Pr, vr, gs, bs, KK, KQ, live, o0, tok_out); break;
-                }
-                if (CS::p_mode(T) <= 2)
-                    fence_proxy_async_smem();  // generic writes, then a TMA load refills the stage
+            // replay commit: the write-back reads the tile itself; each thread acquires the landed copy (its wait
+            // ends at once: PT saw the phase complete)
+            if (kCommit) mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
+            switch (T) {
+            case 1: chunk_rows<1, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 2: chunk_rows<2, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 3: chunk_rows<3, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 4: chunk_rows<4, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 5: chunk_rows<5, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 6: chunk_rows<6, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 7: chunk_rows<7, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            default: chunk_rows<8, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
             }
         }
-        __syncthreads();  // the stage, B, P and the gates are free for the next item
-        if (it + 1 < end) cur = nxt;
         pos = npos;
     }
-    if (kCommit && tid == PT) bulk_wait_all();
+    if (kCommit && !failed && tid == PT) bulk_wait_all();
+    // every group's tensor-memory reads are complete before the allocation is released
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x < 32) tmem_dealloc(tmem_base, kCols);
 }
 
 // ---- host side ------------------------------------------------------------------------------------------------
@@ -766,34 +811,47 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// The bf16 pool as a 3-D tensor [num_slots * HV][DV][DK]; box = (one swizzle span of columns, 128 rows, 1).
+// The bf16 pool as a 3-D tensor [num_slots * HV][DV][DK]; box = (64 columns, 128 rows, 1), 128-byte swizzle.
 template <int DK>
 cudaError_t encode_pool_map(CUtensorMap* map, void* pool, const RecurrentParams& p) {
     const EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr) return cudaErrorNotSupported;
-    constexpr uint32_t SWZ = DK * 2 < 128 ? DK * 2 : 128;
     const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)p.DV, (cuuint64_t)p.num_slots * (cuuint64_t)p.HV};
     const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)p.DV * DK * 2};
-    const cuuint32_t box[3] = {SWZ / 2, (cuuint32_t)kChunkRows, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kChunkRows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw =
-        SWZ == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (SWZ == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr int kChunkStages = 2;
+// TMA stages per CTA (state tiles in flight or being read by the MMA)
+#ifndef GDN_CHUNK_STAGES
+#define GDN_CHUNK_STAGES 2
+#endif
+constexpr int kChunkStages = GDN_CHUNK_STAGES;
 constexpr int kChunkCachedDevices = 64;  // devices whose launch settings are cached
+constexpr uint32_t kChunkMaxSmem = 227 * 1024;  // dynamic shared memory a CTA may open
 
-// grid = min(items, SMs x resident CTAs), each CTA a contiguous range of items
+// groups per CTA: as many as the shared memory of T = 8 allows, up to kChunkMaxGroups
+template <int DK, bool kCommit, int NS>
+constexpr int chunk_groups() {
+    using CS = ChunkPlan<DK, kCommit, NS>;
+    for (int g = kChunkMaxGroups; g > 1; --g)
+        if (CS::bytes(kChunkMaxT, g) <= kChunkMaxSmem) return g;
+    return 1;
+}
+
+// grid = min(items, SMs x resident CTAs) CTAs of G groups, each group a contiguous range of items
 template <int DK, typename InT, bool kCommit>
 cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int NS = kChunkStages;
+    constexpr int G = chunk_groups<DK, kCommit, NS>();
     using CS = ChunkPlan<DK, kCommit, NS>;
-    auto kernel = gdn_verify_chunked_kernel<DK, InT, kCommit, NS>;
-    const uint32_t smem = CS::bytes(p.T);
+    static_assert(CS::bytes(kChunkMaxT, G) <= kChunkMaxSmem, "shared memory of one group");
+    auto kernel = gdn_verify_chunked_kernel<DK, InT, kCommit, NS, G>;
+    const uint32_t smem = CS::bytes(p.T, G);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -801,18 +859,18 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     // Launch caches shared by every calling thread, one entry per device: the shared-memory opening is a
     // per-device attribute of the function, and occupancy may differ between devices.  A repeated first call
     // only repeats the same queries; devices beyond the table are queried on every call.
-    static std::atomic<int> attr_bytes[kChunkCachedDevices];               // bytes opened on each device
+    static std::atomic<int> attr_bytes[kChunkCachedDevices];                 // bytes opened on each device
     static std::atomic<int> occ_cache[kChunkCachedDevices][kChunkMaxT + 1];  // zero-initialised (static)
     const bool cached = dev >= 0 && dev < kChunkCachedDevices;
     if (!cached || (int)smem > attr_bytes[dev].load(std::memory_order_relaxed)) {
-        const int most = (int)CS::bytes(kChunkMaxT);
+        const int most = (int)CS::bytes(kChunkMaxT, G);
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e != cudaSuccess) return e;
         if (cached) attr_bytes[dev].store(most, std::memory_order_relaxed);
     }
     int occ = cached ? occ_cache[dev][p.T].load(std::memory_order_relaxed) : 0;
     if (occ == 0) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkGroupThreads * G, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) return cudaErrorInvalidConfiguration;
         if (cached) occ_cache[dev][p.T].store(occ, std::memory_order_relaxed);
@@ -822,10 +880,10 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
     if (items > INT32_MAX) return cudaErrorInvalidValue;
-    const int64_t want = std::min<int64_t>(items, (int64_t)sms * occ);
-    const int per_cta = (int)((items + want - 1) / want);
-    const int grid = (int)((items + per_cta - 1) / per_cta);
-    kernel<<<grid, kChunkThreads, smem, s>>>(p, map, (int)items, per_cta);
+    const int64_t ctas = std::min<int64_t>(items, (int64_t)sms * occ);
+    const int64_t vctas = std::min<int64_t>(items, ctas * G);
+    const int per_cta = (int)((items + vctas - 1) / vctas);
+    kernel<<<(int)ctas, kChunkGroupThreads * G, smem, s>>>(p, map, (int)items, per_cta);
     return cudaGetLastError();
 }
 

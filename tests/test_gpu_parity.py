@@ -220,8 +220,9 @@ def test_sweep_point(w):
 
 # ---- edge cases: several row tiles, ragged tails, every DK, dtype mixes -----------------------------
 def verify_is_chunked(w) -> bool:
-    """Verify without intermediate states on a bf16 pool with T <= 8 runs the chunked tensor-core kernel."""
-    return w.state_dtype == "bf16" and w.T <= 8
+    """Verify without intermediate states on a bf16 pool with T <= 8 and DK >= 64 runs the chunked tensor-core
+    kernel."""
+    return w.state_dtype == "bf16" and w.T <= 8 and w.DK >= 64
 
 
 def small(name, B=3, T=3, HK=2, HV=4, DK=64, DV=40, num_slots=7, qkv="bf16", state="bf16", out="bf16",
@@ -740,7 +741,7 @@ def test_maximum_batch():
 def test_maximum_batch_chunked():
     """B = 65535 lanes through the chunked verify and replay commit: thousands of items per persistent CTA;
     sampled lanes against the oracle, every other slot untouched."""
-    w = W.Workload("max_B_chunked", B=65535, T=3, HK=1, HV=2, DK=32, DV=40, num_slots=65535, qkv_dtype="bf16",
+    w = W.Workload("max_B_chunked", B=65535, T=3, HK=1, HV=2, DK=64, DV=40, num_slots=65535, qkv_dtype="bf16",
                    state_dtype="bf16", out_dtype="bf16", mode="verify", cache=False, commit=True, seed=12,
                    pool_std=0.1, pad_fraction=0.05, commit_mode="replay")
     x = w.arrays()
