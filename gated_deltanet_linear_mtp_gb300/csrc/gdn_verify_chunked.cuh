@@ -22,8 +22,10 @@
 //                              soon as the MMA that reads it has completed, before the row recurrence runs;
 //   replay commit (kCommit)    the first L = steps[b] tokens, no outputs, and the state after them,
 //                              S_L = gamma_L S_0 + sum_{s<L} G(s, L-1) delta_s kh_s^T, written back into the
-//                              slot (kh only: 2T columns, one Gram matrix); the rank-L update runs on mma.sync
-//                              over the stage in place, which a TMA tensor store then writes back.
+//                              slot (kh only: 2T columns, one Gram matrix).  The rank-L update is one more
+//                              tcgen05.mma: the per-row coefficients go to tensor memory (tcgen05.st, A operand),
+//                              B is the kh hi / lo rows read MN-major; each thread adds gamma_L S_0 to its row
+//                              of the product and writes the row over the stage, which a TMA store writes back.
 //
 // Work item = 128 state rows of one (lane, value head); items are numbered row block fastest, then value
 // head, then lane, and each CTA (4 warps, warp w owning rows [32w, 32w + 32)) takes a contiguous range of
@@ -50,7 +52,6 @@ constexpr int kChunkGroupThreads = 128;  // one group of 4 warps works on one it
 constexpr int kChunkMaxT = 8;
 constexpr int kChunkMinDK = 64;  // rows of 64 bf16 at least: whole 128-byte swizzle spans
 constexpr uint32_t kChunkWaitPolls = GDN_WAIT_POLLS;
-constexpr uint32_t kChunkTmemCols = 32;  // tensor-memory columns per group: P has at most 4 T = 32 columns
 constexpr int kChunkMaxGroups = 3;
 
 // Shared-memory plan of one group, as byte offsets from its 1024-byte aligned base; the groups of a CTA sit
@@ -63,18 +64,21 @@ struct ChunkPlan {
     static constexpr uint32_t STAGE_BYTES = kChunkRows * DK * 2;
     // columns of P: kh hi, kh lo (and qh hi, qh lo in verify mode), T each
     __host__ __device__ static constexpr int ncols(int T) { return kCommit ? 2 * T : 4 * T; }
-    // rows of B (one per column of P), padded to the MMA's N: a multiple of 16
+    // the MMA's N for P: a multiple of 16
     __host__ __device__ static constexpr int nb(int T) { return (ncols(T) + 15) / 16 * 16; }
+    // replay commit: the K of the write-back, coefficients [c hi | c hi | c lo] against B rows [kh hi; kh lo; kh hi]
+    __host__ __device__ static constexpr int a2_cols(int T) { return (3 * T + 15) / 16 * 16; }
+    // rows of B: verify [kh hi | kh lo | qh hi | qh lo], replay [kh hi | kh lo | kh hi], zero rows to a multiple
+    // of 16
+    __host__ __device__ static constexpr int brows(int T) { return kCommit ? a2_cols(T) : nb(T); }
     __host__ __device__ static constexpr uint32_t b_off() { return NS * STAGE_BYTES; }
-    __host__ __device__ static constexpr uint32_t b_bytes(int T) { return (uint32_t)nb(T) * DK * 2; }
-    // replay commit: the coefficient tile A2 = [c hi | c lo | c hi | 0] (bf16, rows padded by 16 bytes)
-    __host__ __device__ static constexpr int a2_cols(int T) { return 3 * T <= 16 ? 16 : 32; }
-    __host__ __device__ static constexpr uint32_t a2_stride(int T) { return (uint32_t)a2_cols(T) * 2 + 16; }
-    __host__ __device__ static constexpr uint32_t a2_off(int T) { return b_off() + b_bytes(T); }
+    __host__ __device__ static constexpr uint32_t b_bytes(int T) { return (uint32_t)brows(T) * DK * 2; }
+    // tensor-memory columns of one group: P (verify); the product D (DK columns, P overlaps its first ones), then
+    // the coefficients, two bf16 per column (replay)
+    __host__ __device__ static constexpr uint32_t a2_col() { return DK; }
+    __host__ __device__ static constexpr uint32_t tmem_cols() { return kCommit ? (DK + 16 + 31) / 32 * 32 : 32; }
     // g, beta (T each), then the Gram matrices, transposed (row t holds kh_s . kh_t, kh_s . qh_t over s)
-    __host__ __device__ static constexpr uint32_t s_off(int T) {
-        return a2_off(T) + (kCommit ? (uint32_t)kChunkRows * a2_stride(T) : 0u);
-    }
+    __host__ __device__ static constexpr uint32_t s_off(int T) { return b_off() + b_bytes(T); }
     __host__ __device__ static constexpr int gram_stride(int T) { return (T + 3) & ~3; }
     __host__ __device__ static constexpr uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
     // NS tile mbarriers and the MMA mbarrier, the tensor-memory address and a failure flag, then per stage the
@@ -120,18 +124,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 
 __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
-                 "r"(r2), "r"(r3)
-                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
@@ -207,6 +199,23 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// MN-major bf16 operand in the 128-byte swizzled layout (rows = K, 64 columns of N per box): the leading offset
+// is the stride between 64-column boxes, the stride offset the one between 8-row groups.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t addr, uint32_t box_stride) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((box_stride >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// D[tmem] (+)= A[tmem] * B: A in tensor memory (lane = row, two bf16 per column), B from its descriptor
+__device__ __forceinline__ void umma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {  // one whole warp
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -232,6 +241,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* f) {
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 8 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* w) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // T floats from shared memory: float4 loads when the address is 16-byte aligned by construction
 template <int N, bool kVec>
@@ -292,12 +310,12 @@ __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const f
     }
 }
 
-// Replay commit: one row's coefficients c_s = G(s, L-1) delta_s (s < L, 0 beyond) from its P row, written as
-// its row of A2 = [c hi | c lo | c hi | 0] in bf16 (hi = c rounded, lo = c - hi rounded), to be multiplied by
-// [kh hi; kh hi; kh lo].
-template <int T, int NP>
+// Replay commit: one row's coefficients c_s = G(s, L-1) delta_s (s < L, 0 beyond) from its P row, as its row of
+// A2 = [c hi | c hi | c lo | 0] in bf16 pairs (hi = c rounded, lo = c - hi rounded; element 2j in the low half),
+// to be multiplied by the B rows [kh hi; kh lo; kh hi].
+template <int T, int NP, int K2>
 __device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const float (&v)[kChunkMaxT], const float* gs,
-                                                 const float* bs, const float* KKt, int L, unsigned char* a2row) {
+                                                 const float* bs, const float* KKt, int L, uint32_t (&a2)[K2 / 2]) {
     constexpr int TP = (T + 3) & ~3;
     float delta[T];
     float gamma = 1.f;
@@ -332,14 +350,9 @@ __device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const fl
         hi[s] = __bfloat162float(__float2bfloat16_rn(c[s]));
         lo[s] = c[s] - hi[s];
     }
-    constexpr int W = 3 * T <= 16 ? 16 : 32;
-    auto col = [&](int i) -> float { return i < T ? hi[i] : (i < 2 * T ? lo[i - T] : (i < 3 * T ? hi[i - 2 * T] : 0.f)); };
-    uint32_t w[W / 2];
+    auto col = [&](int i) -> float { return i < T ? hi[i] : (i < 2 * T ? hi[i - T] : (i < 3 * T ? lo[i - 2 * T] : 0.f)); };
 #pragma unroll
-    for (int i = 0; i < W; i += 2) w[i / 2] = bf16x2_bits(col(i), col(i + 1));
-#pragma unroll
-    for (int q = 0; q < W / 8; ++q)
-        *reinterpret_cast<uint4*>(a2row + 16 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int i = 0; i < K2; i += 2) a2[i / 2] = bf16x2_bits(col(i), col(i + 1));
 }
 
 // Per-item inputs in registers, kept in their storage type until used (a conversion right after the load would
@@ -358,16 +371,17 @@ struct ItemRegs {
 };
 
 // After the tile's MMA: every thread reads the P row of its state row from tensor memory, then runs the row's
-// recurrence (verify: o), or forms its coefficients and the CTA rewrites the tile and stores it (replay commit).
+// recurrence (verify: o), or forms its coefficients and the group rewrites the tile and stores it (replay
+// commit).  False: a wait ran out (nothing was written).
 template <int T, int DK, typename InT, bool kCommit, int NS>
-__device__ __forceinline__ void chunk_rows(const RecurrentParams& p, const CUtensorMap* tmap, uint32_t tmem,
+__device__ __forceinline__ bool chunk_rows(const RecurrentParams& p, const CUtensorMap* tmap, uint32_t tmem,
                                            unsigned char* sm, uint32_t base, uint32_t stage,
                                            const float (&vr)[kChunkMaxT], int b, int h, int row0, int nrows, int slot,
-                                           int L, int bar_id) {
+                                           int L, int bar_id, uint32_t mma_bar, uint32_t& mphase) {
     using CS = ChunkPlan<DK, kCommit, NS>;
     constexpr int NP = CS::nb(T);  // columns of P in tensor memory
     constexpr int TP = (T + 3) & ~3;
-    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5;
     const float* gs = reinterpret_cast<const float*>(sm + CS::s_off(T));
     const float* bs = gs + T;
     const float* KK = reinterpret_cast<const float*>(sm + CS::gram_off(T));
@@ -383,68 +397,59 @@ __device__ __forceinline__ void chunk_rows(const RecurrentParams& p, const CUten
         row_recurrence<T, NP>(p, pr, vr, gs, bs, KK, KQ, live, o0, (int64_t)p.HV * p.DV);
     } else {
         constexpr int PT = 64;
-        constexpr int NB = CS::nb(T);
-        constexpr uint32_t A2S = CS::a2_stride(T);
-        unsigned char* a2w = sm + CS::a2_off(T) + warp * 32 * A2S;  // this warp's 32 rows of A2
-        row_coefficients<T, NP>(pr, vr, gs, bs, KK, L, a2w + lane * A2S);
+        constexpr int K2 = CS::a2_cols(T);
+        constexpr int BR = CS::brows(T);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        uint32_t a2[K2 / 2];
+        row_coefficients<T, NP, K2>(pr, vr, gs, bs, KK, L, a2);
+#pragma unroll
+        for (int c = 0; c < K2 / 2; c += 8) tmem_st8(lane_base + CS::a2_col() + c, a2 + c);
+        tmem_wait_st();
         float gamma = 1.f;
         for (int t = 0; t < L; ++t) gamma *= gs[t];
-        __syncwarp();
-        // S_L = gamma S_0 + A2 [kh hi; kh hi; kh lo] on mma.sync, 16 columns at a time: S_0 comes in as the
-        // accumulator (ldmatrix gives the m16n8 accumulator layout of each 8 x 8 block) and goes back over itself
-        // (stmatrix), each warp on its own rows
-        constexpr int KS2 = CS::a2_cols(T) / 16;
-        const uint32_t bbase = base + CS::b_off();
-        const uint32_t a2b = base + CS::a2_off(T) + warp * 32 * A2S + (uint32_t)(lane & 15) * A2S + (lane >> 4) * 16;
-        const int ra_row = warp * 32 + (lane & 15);
-        uint32_t af[KS2][2][4];  // [k step][m tile]
+        tc_fence_before();
+        group_sync(bar_id);  // every row's coefficients are in tensor memory, every P row has been read
+        // D = A2 [kh hi; kh lo; kh hi] on the tensor cores: A2 from tensor memory, B = B's rows read MN-major
+        if (tid == PT) {
+            tc_fence_after();
+            const uint32_t idesc = umma_idesc_bf16(kChunkRows, DK) | (1u << 16);  // B MN-major
+            const uint32_t bbase = base + CS::b_off();
 #pragma unroll
-        for (int ks = 0; ks < KS2; ++ks)
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-                ldsm_x4(a2b + mt * 16 * A2S + ks * 32, af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3]);
-        int brow[KS2];  // row of B2 (a row of B) that this lane addresses, per k step
-#pragma unroll
-        for (int ks = 0; ks < KS2; ++ks) {
-            const int kidx = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            brow[ks] = kidx < T ? kidx : (kidx < 2 * T ? kidx - T : (kidx < 3 * T ? kidx - T : 0));
+            for (int ks = 0; ks < K2 / 16; ++ks)
+                umma_bf16_ta(tmem, tmem + CS::a2_col() + 8 * ks, umma_desc_sw128_mn(bbase + 2048u * ks, BR * 128u),
+                             idesc, ks > 0 ? 1u : 0u);
+            umma_commit(mma_bar);
         }
-#pragma unroll 2
-        for (int np = 0; np < DK / 16; ++np) {
-            float d[2][2][4];
-            uint32_t sa[2];
+        const bool mok = mbar_wait_bounded(mma_bar, mphase, kChunkWaitPolls);
+        mphase ^= 1u;
+        if (group_sync_or(bar_id, !mok)) {  // the product never completed: leave the slot as it is
+            if (tid == PT) mbar_wait_bounded(mma_bar, mphase ^ 1u, kChunkWaitPolls);
+            return false;
+        }
+        tc_fence_after();
+        // S_L = gamma S_0 + D, this thread's row, 32 columns at a time, rounded to bf16 over the stage
+        unsigned char* srow = sm + (stage - base);
+#pragma unroll 1
+        for (int c32 = 0; c32 < DK / 32; ++c32) {
+            float d[32];
+            tmem_ld16(lane_base + 32 * c32, d);
+            tmem_ld16(lane_base + 32 * c32 + 16, d + 16);
+            tmem_wait_ld();
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                sa[mt] = stage + sw128(kChunkRows, ra_row + mt * 16, 2 * np + (lane >> 4));
-                uint32_t s0, s1, s2, s3;
-                ldsm_x4(sa[mt], s0, s1, s2, s3);
-                const float2 f0 = bf16x2_to_float2(s0), f1 = bf16x2_to_float2(s1);
-                const float2 f2 = bf16x2_to_float2(s2), f3 = bf16x2_to_float2(s3);
-                d[mt][0][0] = gamma * f0.x;
-                d[mt][0][1] = gamma * f0.y;
-                d[mt][0][2] = gamma * f1.x;
-                d[mt][0][3] = gamma * f1.y;
-                d[mt][1][0] = gamma * f2.x;
-                d[mt][1][1] = gamma * f2.y;
-                d[mt][1][2] = gamma * f3.x;
-                d[mt][1][3] = gamma * f3.y;
-            }
+            for (int q = 0; q < 4; ++q) {
+                uint4* cp = reinterpret_cast<uint4*>(srow + sw128(kChunkRows, tid, 4 * c32 + q));
+                const uint4 s0 = *cp;
+                const uint32_t w[4] = {s0.x, s0.y, s0.z, s0.w};
+                uint32_t o[4];
 #pragma unroll
-            for (int ks = 0; ks < KS2; ++ks) {
-                uint32_t b00, b01, b10, b11;
-                ldsm_x4_trans(bbase + sw128(NB, brow[ks], 2 * np + (lane >> 4)), b00, b01, b10, b11);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    mma_bf16_16816(d[mt][0], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b00, b01);
-                    mma_bf16_16816(d[mt][1], af[ks][mt][0], af[ks][mt][1], af[ks][mt][2], af[ks][mt][3], b10, b11);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = bf16x2_to_float2(w[e]);
+                    o[e] = bf16x2_bits(fmaf(gamma, f.x, d[8 * q + 2 * e]), fmaf(gamma, f.y, d[8 * q + 2 * e + 1]));
                 }
+                *cp = make_uint4(o[0], o[1], o[2], o[3]);
             }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-                stsm_x4(sa[mt], bf16x2_bits(d[mt][0][0], d[mt][0][1]), bf16x2_bits(d[mt][0][2], d[mt][0][3]),
-                        bf16x2_bits(d[mt][1][0], d[mt][1][1]), bf16x2_bits(d[mt][1][2], d[mt][1][3]));
         }
-        fence_proxy_async_smem();  // the stmatrix writes above, then the TMA store reads them
+        fence_proxy_async_smem();  // the rows written above, then the TMA store reads them
         group_sync(bar_id);
         if (tid == PT) {
 #pragma unroll
@@ -453,6 +458,7 @@ __device__ __forceinline__ void chunk_rows(const RecurrentParams& p, const CUten
             bulk_commit_group();
         }
     }
+    return true;
 }
 
 // A kernel that allocates tensor memory runs one CTA per SM, so the CTA holds G groups of 4 warps, each an
@@ -497,9 +503,11 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
     volatile int* fail_flag = reinterpret_cast<volatile int*>(sm + CS::ctl_off(T) + 8 * (NS + 1));
     int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(T) + 8 * (NS + 1) + 8);
     int* st_len = st_slot + NS;
-    unsigned char* Bs = sm + CS::b_off();  // rows: k hi (T) | k lo (T) | q hi (T) | q lo (T) | padding, swizzled
+    // B's rows, swizzled: verify k hi (T) | k lo (T) | q hi (T) | q lo (T); replay k hi | k lo | k hi; zero padding
+    unsigned char* Bs = sm + CS::b_off();
     const uint32_t bbase = base + CS::b_off();
-    const int NB = CS::nb(T);
+    const int NB = CS::nb(T);     // the P MMA's N
+    const int BR = CS::brows(T);  // rows of B
     float* gs = reinterpret_cast<float*>(sm + CS::s_off(T));
     float* bs = gs + T;
     const int TP = CS::gram_stride(T);
@@ -585,7 +593,13 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
             ilen = kCommit ? p.steps[ipos.b] : T;
         }
     };
-    constexpr uint32_t kCols = G == 1 ? 32u : (G == 2 ? 64u : 128u);  // a power of 2, at least 32
+    // tensor-memory columns of the CTA: a power of 2 covering every group's share
+    constexpr uint32_t kCols = G * CS::tmem_cols() <= 32    ? 32u
+                               : G * CS::tmem_cols() <= 64  ? 64u
+                               : G * CS::tmem_cols() <= 128 ? 128u
+                               : G * CS::tmem_cols() <= 256 ? 256u
+                                                            : 512u;
+    static_assert(G * CS::tmem_cols() <= 512, "tensor memory of the groups");
     if (threadIdx.x < 32) tmem_alloc(smem_u32(tmem_slot), kCols);
     if (tid == PT && beg < end) {
         for (int s = 0; s <= NS; ++s) mbar_init(ctl + 8 * s, 1);
@@ -595,9 +609,9 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         ilen = kCommit ? p.steps[ipos.b] : T;
         for (int j = 0; j < (kEarly ? NS : NS - 1) && nis < end; ++j) issue_next(j);
     }
-    // B's padding rows stay zero (their columns of P are never read)
-    for (int i2 = CS::ncols(T) * (DK / 8) + tid; i2 < NB * (DK / 8); i2 += ROWS)
-        *reinterpret_cast<uint4*>(Bs + sw128(NB, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
+    // B's padding rows stay zero (the products with them are never used, and must be finite)
+    for (int i2 = (kCommit ? 3 : 4) * T * (DK / 8) + tid; i2 < BR * (DK / 8); i2 += ROWS)
+        *reinterpret_cast<uint4*>(Bs + sw128(BR, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();  // the padding rows are read by the tensor cores too
     IR in;  // the current item's inputs (each field refilled for the next item after its last use)
     if (beg < end) {
@@ -609,7 +623,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem = tmem_base + kChunkTmemCols * grp;  // this group's columns
+    const uint32_t tmem = tmem_base + CS::tmem_cols() * grp;  // this group's columns
 
     uint32_t phase = 0;   // bit s: parity of the next completion of stage s
     uint32_t mphase = 0;  // parity of the next completion of the MMA barrier
@@ -656,8 +670,11 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                     }
                     const int t = j < T ? j : j - T;
                     const int hi_row = j < T ? 2 * T + t : t;  // q hi rows start at 2T, k hi rows at 0
-                    *reinterpret_cast<uint4*>(Bs + sw128(NB, hi_row, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Bs + sw128(NB, hi_row + T, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row + T, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    if (kCommit)  // the write-back's third block of B: kh hi again
+                        *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row + 2 * T, vc)) =
+                            make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 }
             }
             fence_proxy_async_smem();  // B is written here and read by the tensor cores' MMA
@@ -691,22 +708,26 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                 const int jr = lane & 7;
                 brow[nb] = jr < T ? (nb0 + nb) * T + jr : 0;
             }
-            float g[NBLK][4];
+            float g[NBLK][4], g2[NBLK][4];  // two accumulation chains (even and odd k steps): half the latency
 #pragma unroll
             for (int nb = 0; nb < NBLK; ++nb)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) g[nb][c] = 0.f;
+                for (int c = 0; c < 4; ++c) g[nb][c] = g2[nb][c] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(bbase + sw128(NB, arow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+                ldsm_x4(bbase + sw128(BR, arow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
                 for (int nb = 0; nb < NBLK; ++nb) {
                     uint32_t b0, b1;
-                    ldsm_x2(bbase + sw128(NB, brow[nb], 2 * ks + ((lane >> 3) & 1)), b0, b1);
-                    mma_bf16_16816(g[nb], a0, a1, a2, a3, b0, b1);
+                    ldsm_x2(bbase + sw128(BR, brow[nb], 2 * ks + ((lane >> 3) & 1)), b0, b1);
+                    mma_bf16_16816((ks & 1) ? g2[nb] : g[nb], a0, a1, a2, a3, b0, b1);
                 }
             }
+#pragma unroll
+            for (int nb = 0; nb < NBLK; ++nb)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) g[nb][c] += g2[nb][c];
             const int s_ = lane >> 2;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -725,7 +746,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     const uint32_t koff = (uint32_t)((ks & 3) * 32);  // 16 columns further inside the 128-byte span
                     const uint64_t ad = umma_desc_sw128(stage + (uint32_t)(ks >> 2) * CS::BOX_BYTES + koff);
-                    const uint64_t bd = umma_desc_sw128(bbase + (uint32_t)(ks >> 2) * (uint32_t)NB * 128u + koff);
+                    const uint64_t bd = umma_desc_sw128(bbase + (uint32_t)(ks >> 2) * (uint32_t)BR * 128u + koff);
                     umma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(mma_bar);
@@ -771,15 +792,28 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
             // replay commit: the write-back reads the tile itself; each thread acquires the landed copy (its wait
             // ends at once: PT saw the phase complete)
             if (kCommit) mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
+            bool rows_ok = true;
             switch (T) {
-            case 1: chunk_rows<1, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 2: chunk_rows<2, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 3: chunk_rows<3, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 4: chunk_rows<4, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 5: chunk_rows<5, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 6: chunk_rows<6, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            case 7: chunk_rows<7, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
-            default: chunk_rows<8, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id); break;
+            case 1: rows_ok = chunk_rows<1, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 2: rows_ok = chunk_rows<2, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 3: rows_ok = chunk_rows<3, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 4: rows_ok = chunk_rows<4, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 5: rows_ok = chunk_rows<5, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 6: rows_ok = chunk_rows<6, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            case 7: rows_ok = chunk_rows<7, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            default: rows_ok = chunk_rows<8, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            }
+            if (!rows_ok) {  // a wait ran out inside: report it and drain the tiles issued ahead
+                failed = true;
+                if (tid == PT) {
+                    if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+                    for (int j = 1; j < NS && it + j < nis; ++j) {
+                        const int s2 = (i + j) % NS;
+                        if (st_slot[s2] >= 0) mbar_wait_bounded(ctl + 8 * s2, (phase >> s2) & 1u, kChunkWaitPolls);
+                    }
+                    bulk_wait_all();
+                }
+                break;
             }
         }
         pos = npos;
