@@ -52,8 +52,10 @@ def kernel_name(w, role: str, sms: int) -> str:
         return "gdn_commit_kernel"
     in_range = w.num_slots * w.HV <= 2**31 - 1 and w.B * w.HV * -(-w.DV // 128) <= 2**31 - 1
     if (w.state_dtype == "bf16" and w.T <= 8 and w.DK >= 64 and in_range
-            and ((role == "verify" and not w.cache) or role == "commit_replay")):
+            and ((role == "verify" and not w.cache) or role in ("commit_replay", "verify_commit"))):
         return "gdn_verify_chunked_kernel"
+    if role == "verify_commit":  # outside the one-pass kernel: the replay commit and the verify, two launches
+        return "gdn_recurrent_kernel + gdn_recurrent_kernel"
     st = 2 if w.state_dtype == "bf16" else 4
     p = w.DK // 8
     rpc = (32 // p) * min(p, 4) * 4  # rows per CTA of the token-by-token kernels
@@ -121,6 +123,16 @@ def recurrent_bytes(w: W.Workload, A: int) -> int:
         state_write = A * w.HV * E * s
     per_tok = 2 * w.HK * w.DK * i + w.HV * w.DV * i + w.HV * w.DV * ob + 2 * w.HV * i
     return state_read + state_write + A * w.T * per_tok + w.HV * 8 + w.B * 4
+
+
+def fused_bytes(w: W.Workload, A: int, prev_accepted: int) -> int:
+    """One-pass step (gdn_mtp_verify_commit): every active state read once and written once, the previous step's
+    accepted tokens' k, v, a, b, and this step's q, k, v, a, b and o."""
+    s, i, ob = esize(w.state_dtype), esize(w.qkv_dtype), esize(w.out_dtype)
+    state = 2 * A * w.HV * w.DV * w.DK * s
+    per_tok = 2 * w.HK * w.DK * i + w.HV * w.DV * i + w.HV * w.DV * ob + 2 * w.HV * i
+    prev_tok = w.HK * w.DK * i + w.HV * w.DV * i + 2 * w.HV * i
+    return state + A * w.T * per_tok + prev_accepted * prev_tok + w.HV * 8 + 2 * w.B * 4
 
 
 def commit_bytes(w: W.Workload, A: int, accepted_tokens: int = 0) -> int:
@@ -306,6 +318,12 @@ class Step:
             return torch.from_numpy(a).to(device)
 
         self.d = {k: t(v) for k, v in x.items()}
+        # one-pass steps: the tokens of the previous step (its k, v, a, b, accept lengths), committed first
+        self.prev, self.prev_accepted = None, 0
+        if w.commit_mode == "fused":
+            xp = W.previous_step(w)
+            self.prev = {k: t(v) for k, v in xp.items()}
+            self.prev_accepted = int(xp["accept_len"][active].sum())
         td = {"f32": torch.float32, "bf16": torch.bfloat16}
         self.o = torch.empty((w.B, w.T, w.HV, w.DV), dtype=td[w.out_dtype], device=device)
         self.cache = (torch.empty((w.B, w.T, w.HV, w.DV, w.DK), dtype=td[w.state_dtype], device=device)
@@ -343,7 +361,12 @@ class Step:
                     src[torch.from_numpy(act)] = torch.from_numpy(free[(j - 1) * len(act):j * len(act)].astype(np.int32))
                 buf[o:o + nb].copy_(src.reshape(-1).view(torch.uint8))
             self.h_sets.append(buf)
-        self.dev_slots = [torch.empty(self.packed_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        # input / output slots in flight: 2; a one-pass step also reads the previous step's inputs, so 3
+        self.nslots = 3 if w.commit_mode == "fused" else 2
+        self.dev_slots = [torch.empty(self.packed_bytes, dtype=torch.uint8, device=device)
+                          for _ in range(self.nslots)]
+        for buf in self.dev_slots:  # every slot holds a valid step (the first one-pass step reads the last slot)
+            buf.copy_(self.h_sets[0].to(device))
         self.slot_views = []
         for buf in self.dev_slots:
             v = dict(self.d)
@@ -351,15 +374,21 @@ class Step:
                 o, nb, dt, shape = self.layout[k]
                 v[k] = buf[o:o + nb].view(dt).view(shape)
             self.slot_views.append(v)
-        self.o_slots = [torch.empty_like(self.o) for _ in range(2)]
-        self.h_out = [torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory() for _ in range(2)]
+        self.o_slots = [torch.empty_like(self.o) for _ in range(self.nslots)]
+        self.h_out = [torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory() for _ in range(self.nslots)]
         self.h2d_bytes = sum(self.layout[k][1] for k in self.step_keys)
         self.d2h_bytes = self.o.numel() * self.o.element_size()
         self.e2e_sets = nsets
 
-    def recurrent(self, d=None, o=None):
+    def recurrent(self, d=None, o=None, prev=None):
         d, w, o = d or self.d, self.w, self.o if o is None else o
-        if w.mode == "decode":
+        if w.commit_mode == "fused":
+            pv = prev or self.prev
+            self.gdn.gdn_mtp_verify_commit(
+                self.gdn.ReplayTokens(pv["k"], pv["v"], pv["a"], pv["b"], pv["accept_len"]), d["q"], d["k"], d["v"],
+                d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"], d["indices"], o, self.err, scale=w.scale,
+                l2_eps=w.l2_eps)
+        elif w.mode == "decode":
             self.gdn.gdn_decode(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
                                 d["indices"], o, self.err, scale=w.scale, l2_eps=w.l2_eps)
         else:
@@ -367,7 +396,7 @@ class Step:
                                     d["indices"], o, self.cache, self.err, scale=w.scale, l2_eps=w.l2_eps)
 
     def commit(self, d=None):
-        if not self.w.commit:
+        if not self.w.commit or self.w.commit_mode == "fused":  # a one-pass step commits inside recurrent()
             return
         d, w = d or self.d, self.w
         if w.commit_mode == "replay":
@@ -387,25 +416,28 @@ class Step:
         torch = self.torch
         G = self.E2E_GRAPH_STEPS
         h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        up = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
-        down = [torch.cuda.Event() for _ in range(2)]
+        NSL = self.nslots
+        fused = self.w.commit_mode == "fused"
+        up = [torch.cuda.Event() for _ in range(NSL)]
+        done = [torch.cuda.Event() for _ in range(NSL)]
+        down = [torch.cuda.Event() for _ in range(NSL)]
 
         def steps(cs):
             h2d.wait_stream(cs)
             d2h.wait_stream(cs)
             for i in range(G):
-                s = i % 2
-                if i >= 2:
-                    h2d.wait_event(done[s])  # step i-2 has finished reading this input slot
+                s = i % NSL
+                last_reader = i - NSL + (1 if fused else 0)  # the last step reading this input slot
+                if last_reader >= 0:
+                    h2d.wait_event(done[last_reader % NSL])
                 with torch.cuda.stream(h2d):
                     self.dev_slots[s].copy_(self.h_sets[i % len(self.h_sets)], non_blocking=True)
                     up[s].record(h2d)
                 cs.wait_event(up[s])
-                if i >= 2:
-                    cs.wait_event(down[s])  # step i-2's o has been copied out of this output slot
+                if i >= NSL:
+                    cs.wait_event(down[s])  # the o of step i - NSL has been copied out of this output slot
                 with torch.cuda.stream(cs):
-                    self.recurrent(self.slot_views[s], self.o_slots[s])
+                    self.recurrent(self.slot_views[s], self.o_slots[s], self.slot_views[(i - 1) % NSL])
                     self.commit(self.slot_views[s])
                     done[s].record(cs)
                 d2h.wait_event(done[s])
@@ -442,7 +474,7 @@ class Step:
 
     @property
     def launches_per_step(self) -> int:
-        return 1 + (1 if self.w.commit else 0)
+        return 1 + (1 if self.w.commit and self.w.commit_mode != "fused" else 0)
 
 
 _POOL_CACHE: dict = {}
@@ -558,13 +590,14 @@ def measure_point(args, w: W.Workload, rank: int, world: int, local_rank: int, d
                    "ms_per_step": e2e_ms_step, "timed_steps": e2e_steps}
 
     peak, peak_src = hbm_peak()
-    rb = recurrent_bytes(wr, st.A)
-    cb = commit_bytes(wr, st.A, st.accepted) if wr.commit else 0
-    role = "decode" if w.mode == "decode" else "verify"
+    fused = wr.commit_mode == "fused"
+    rb = fused_bytes(wr, st.A, st.prev_accepted) if fused else recurrent_bytes(wr, st.A)
+    cb = commit_bytes(wr, st.A, st.accepted) if wr.commit and not fused else 0
+    role = "decode" if w.mode == "decode" else ("verify_commit" if fused else "verify")
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     kernels = [{"role": role, "kernel": kernel_name(wr, role, sms), "avg_us": statistics.mean(rec_ms) * 1e3,
                 "algorithmic_bytes": rb}]
-    if wr.commit:
+    if wr.commit and not fused:
         crole = "commit_replay" if wr.commit_mode == "replay" else "commit"
         kernels.append({"role": crole, "kernel": kernel_name(wr, crole, sms),
                         "avg_us": statistics.mean(com_ms) * 1e3, "algorithmic_bytes": cb})
@@ -593,8 +626,10 @@ def measure_point(args, w: W.Workload, rank: int, world: int, local_rank: int, d
             "workload": w.name, "B": w.B, "active_lanes": st.A, "T": w.T, "HK": w.HK, "HV": w.HV, "DK": w.DK,
             "DV": w.DV, "num_slots": w.num_slots, "state_dtype": w.state_dtype, "qkv_dtype": w.qkv_dtype,
             "out_dtype": w.out_dtype, "intermediate_cache": w.cache, "commit_per_step": w.commit,
-            "step": ("gdn_decode" if w.mode == "decode" else "gdn_mtp_verify" + (
-                (" + gdn_commit_replay" if w.commit_mode == "replay" else " + gdn_commit") if w.commit else "")),
+            "step": ("gdn_decode" if w.mode == "decode" else
+                     "gdn_mtp_verify_commit (the previous step's accepted prefix committed, then verify)" if fused else
+                     "gdn_mtp_verify" + ((" + gdn_commit_replay" if w.commit_mode == "replay" else " + gdn_commit")
+                                         if w.commit else "")),
             "l2": "flushed before every step outside its CUDA events (256 MiB write, then 256 MiB read: clean lines)",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
             "timing": (f"CUDA events per step on the launch stream, summed over {R} x {K} steps (the timed region "
@@ -622,8 +657,9 @@ def measure_point(args, w: W.Workload, rank: int, world: int, local_rank: int, d
 
 POINT_KEYS = ("value", "unit", "ms_per_step", "repeats", "timed_steps", "verify_steps_per_s", "hbm_gbs_step",
               "roofline", "kernels", "e2e", "gpu_launches", "clocks", "wall_s_timed_region")
-# the metric's T = 1 and T = 8 points and the verify + replay-commit steps, each measured like the main line
-POINTS = ("decode", "verify8", "verify4_replay", "verify8_replay")
+# the metric's T = 1 and T = 8 points and the verify + replay-commit and one-pass steps, each measured like the
+# main line
+POINTS = ("decode", "verify8", "verify4_replay", "verify8_replay", "verify4_fused", "verify8_fused")
 
 
 def point_record(r: dict) -> dict:
@@ -1172,7 +1208,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay"] + sorted(PREFILL_NAMED)
+    ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay", "sweep_fused"] + sorted(PREFILL_NAMED)
                     + ["gated_norm"], default="verify4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -1202,6 +1238,8 @@ def main(argv=None):
         pts = W.sweep()
     elif args.workload == "sweep_replay":
         pts = W.sweep_replay()
+    elif args.workload == "sweep_fused":
+        pts = W.sweep_fused()
     else:
         pts = [W.NAMED[args.workload]()]
     headline = args.workload == "verify4" and not args.no_points

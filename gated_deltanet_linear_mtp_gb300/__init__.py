@@ -8,6 +8,7 @@ library has not been built, every call raises.
     gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
     gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
     gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, ...)
+    gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, ...)
     gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o,
                 has_initial_state=None, err_word=None, ...)
     gdn_gated_rmsnorm(o, z, norm_weight, y=None, eps=1e-6)
@@ -26,8 +27,8 @@ from typing import Optional
 
 from .build import LIB_PATH
 
-__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_prefill", "gdn_gated_rmsnorm",
-           "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
+__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "ReplayTokens",
+           "gdn_prefill", "gdn_gated_rmsnorm", "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
            "ERRBIT_SEQLEN", "MAX_T", "EXPORTS"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
@@ -38,8 +39,8 @@ ERRBIT_TIMEOUT = 4
 ERRBIT_SEQLEN = 8
 MAX_T = 16
 F32, BF16 = 0, 1
-EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_prefill", "gdn_gated_rmsnorm",
-           "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
+EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "gdn_prefill",
+           "gdn_gated_rmsnorm", "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
 
 
 class GdnDims(ctypes.Structure):
@@ -47,6 +48,19 @@ class GdnDims(ctypes.Structure):
                 ("DK", ctypes.c_int32), ("DV", ctypes.c_int32), ("num_slots", ctypes.c_int32),
                 ("qkv_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+
+
+class _ReplayTokensC(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("a", ctypes.c_void_p),
+                ("b", ctypes.c_void_p), ("accept_len", ctypes.c_void_p)]
+
+
+class ReplayTokens:
+    """The k, v, a, b of an earlier ``gdn_mtp_verify`` on the same lanes (``[B, T', ...]``, T' its token count)
+    and ``accept_len`` ``[B]`` int32: the tokens ``gdn_mtp_verify_commit`` commits before it verifies."""
+
+    def __init__(self, k, v, a, b, accept_len):
+        self.k, self.v, self.a, self.b, self.accept_len = k, v, a, b, accept_len
 
 
 class GdnError(RuntimeError):
@@ -74,11 +88,12 @@ def lib() -> ctypes.CDLL:
         L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
         L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
         L.gdn_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip, ip, vp]
+        L.gdn_mtp_verify_commit.argtypes = [dp, ctypes.POINTER(_ReplayTokensC)] + [vp] * 5 + [vp, vp, vp, ip, vp, ip, vp]
         L.gdn_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp, ip, vp]
         L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
                                         ctypes.c_float, vp, vp]
-        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_prefill,
-                  L.gdn_gated_rmsnorm):
+        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_mtp_verify_commit,
+                  L.gdn_prefill, L.gdn_gated_rmsnorm):
             f.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -279,6 +294,40 @@ def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
              _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
              _dev(state_indices, "state_indices"), _dev(accept_len, "accept_len"), _dev(err_word, "err_word")),
             "gdn_commit_replay")
+
+
+def gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, *,
+                          scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """One speculative step in one pass: commit ``prev``'s accepted prefix (``prev``: a ``ReplayTokens``, exactly
+    ``gdn_commit_replay`` of those tokens) into the slots, then verify these T tokens from the committed states
+    (exactly ``gdn_mtp_verify`` without intermediate states).  ``prev`` may have another token count."""
+    import torch
+
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
+    if prev.k.dim() != 4:
+        raise ValueError("prev.k is [B, T', HK, DK]")
+    Tp = prev.k.shape[1]
+    _shape(prev.k, (d.B, Tp, d.HK, d.DK), "prev.k")
+    _shape(prev.v, (d.B, Tp, d.HV, d.DV), "prev.v")
+    _shape(prev.a, (d.B, Tp, d.HV), "prev.a")
+    _shape(prev.b, (d.B, Tp, d.HV), "prev.b")
+    _shape(prev.accept_len, (d.B,), "prev.accept_len")
+    for t, n in ((prev.k, "prev.k"), (prev.v, "prev.v"), (prev.a, "prev.a"), (prev.b, "prev.b")):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{n} must have q's dtype")
+    if prev.accept_len.dtype != torch.int32:
+        raise TypeError("prev.accept_len must be int32")
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("o", o), ("err_word", err_word), ("prev.k", prev.k), ("prev.v", prev.v),
+                               ("prev.a", prev.a), ("prev.b", prev.b), ("prev.accept_len", prev.accept_len)])
+    rt = _ReplayTokensC(Tp, _dev(prev.k, "prev.k"), _dev(prev.v, "prev.v"), _dev(prev.a, "prev.a"),
+                        _dev(prev.b, "prev.b"), _dev(prev.accept_len, "prev.accept_len"))
+    _launch(device, stream, L.gdn_mtp_verify_commit,
+            (ctypes.byref(d), ctypes.byref(rt), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"),
+             _dev(b, "b"), _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word")),
+            "gdn_mtp_verify_commit")
 
 
 def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o, has_initial_state=None,

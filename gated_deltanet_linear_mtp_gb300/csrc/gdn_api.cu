@@ -71,7 +71,7 @@ RecurrentParams make_params(const gdn_dims* d, const void* q, const void* k, con
                             const void* b, const float* A_log, const float* dt_bias, const void* pool_in,
                             void* pool_out, const int32_t* idx, const int32_t* steps, void* o, void* cache,
                             int32_t* err) {
-    RecurrentParams p;
+    RecurrentParams p{};  // the replay-commit + verify fields stay null unless set by that call
     p.q = q;
     p.k = k;
     p.v = v;
@@ -177,6 +177,48 @@ gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k,
     if (!aligned(accept_len, 4)) return GDN_ERR_ALIGN;
     return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, accept_len,
                          nullptr, nullptr, err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q, const void* k,
+                                 const void* v, const void* a, const void* b, const float* A_log, const float* dt_bias,
+                                 void* state_pool, const int32_t* state_indices, void* o, int32_t* err_word,
+                                 gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (prev == nullptr) return GDN_ERR_NULL;
+    if (prev->T < 1 || prev->T > GDN_MAX_T) return GDN_ERR_SHAPE;
+    gdn_dims pd = *dims;  // the earlier call's shape: its own token count
+    pd.T = prev->T;
+    s = check_dims(&pd, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    // the earlier tokens have the layouts of k, v, a, b (no q: the replay writes no outputs)
+    s = check_io(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_indices, nullptr,
+                 err_word, false);
+    if (s != GDN_OK) return s;
+    if (!prev->accept_len) return GDN_ERR_NULL;
+    if (!aligned(prev->accept_len, 4)) return GDN_ERR_ALIGN;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dims->state_dtype == GDN_BF16) {
+        RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices,
+                                        prev->accept_len, o, nullptr, err_word);
+        p.rk = prev->k;
+        p.rv = prev->v;
+        p.ra = prev->a;
+        p.rb = prev->b;
+        p.rT = prev->T;
+        cudaError_t e = cudaSuccess;
+        if (launch_replay_verify_bf16state(p, dims->B, dims->DK, dims->qkv_dtype == GDN_BF16, st, e)) return finish(e);
+    }
+    // outside the one-pass kernel's range: the same two steps as two launches, the replay commit (q is not read
+    // for outputs; the earlier k stands in for it) and then the verify from the committed slots
+    s = run_recurrent(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_pool,
+                      state_indices, prev->accept_len, nullptr, nullptr, err_word, st);
+    if (s != GDN_OK) return s;
+    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o, nullptr,
+                         err_word, st);
 }
 
 gdn_status gdn_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,

@@ -26,6 +26,13 @@ struct RecurrentParams {
     void* o;               // nullptr: no outputs (replay commit)
     void* cache;           // nullptr: no intermediate states
     int32_t* err;    // nullable
+    // replay commit + verify: the earlier call's tokens to commit first (rT per lane; steps[b] of them), with
+    // q .. b above the tokens to verify; nullptr / 0 otherwise
+    const void* rk;
+    const void* rv;
+    const void* ra;
+    const void* rb;
+    int rT;
     int T, HK, HV, DV, num_slots;
     int out_bf16;
     int v_vec;  // v starts on 16 bytes and DV * sizeof(v) % 16 == 0: v is read in 16-byte chunks
@@ -56,6 +63,11 @@ struct GatedNormParams {
 
 cudaError_t launch_recurrent_f32state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
 cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
+// Replay commit of p.rk .. p.rb (p.rT tokens per lane, p.steps[b] of them) and then verify of p.q .. p.b (p.T
+// tokens) in one pass of the chunked kernel; false (nothing launched) when the call is outside that kernel's
+// range (T or rT above 8, DK below 64, too many heads or items), else `err` is the launch's status.
+bool launch_replay_verify_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s,
+                                    cudaError_t& err);
 cudaError_t launch_commit(const CommitParams& p, int B, cudaStream_t s);
 // prefill: p.T unused; the token axis has n_tokens entries, sequence b spans cu_seqlens[b] .. cu_seqlens[b+1]-1
 cudaError_t launch_prefill(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,

@@ -8,4 +8,9 @@ cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, 
                     : launch_recurrent<float, __nv_bfloat16>(p, B, DK, s);
 }
 
+bool launch_replay_verify_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s,
+                                    cudaError_t& err) {
+    return qkv_bf16 ? launch_replay_verify<__nv_bfloat16>(p, B, DK, s, err) : launch_replay_verify<float>(p, B, DK, s, err);
+}
+
 }  // namespace gdn

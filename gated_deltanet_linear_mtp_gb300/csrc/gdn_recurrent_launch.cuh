@@ -72,7 +72,8 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
         const uint64_t heads = (uint64_t)p.num_slots * (uint64_t)p.HV;
         const uint64_t items = (uint64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
         if ((verify_only || replay_commit) && p.T <= kChunkMaxT && heads <= INT32_MAX && items <= INT32_MAX)
-            return replay_commit ? launch_chunked<DK, InT, true>(p, B, s) : launch_chunked<DK, InT, false>(p, B, s);
+            return replay_commit ? launch_chunked<DK, InT, kModeReplay>(p, B, s)
+                                 : launch_chunked<DK, InT, kModeVerify>(p, B, s);
     }
     const int sms = sm_count();
     cudaError_t err = cudaSuccess;
@@ -88,6 +89,30 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
     gdn_recurrent_kernel<DK, InT, StT><<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+// the chunked kernel's replay commit + verify mode, if the call is in its range
+template <typename InT, int DK>
+bool launch_replay_verify_dk(const RecurrentParams& p, int B, cudaStream_t s, cudaError_t& err) {
+    if constexpr (DK >= kChunkMinDK) {
+        const uint64_t heads = (uint64_t)p.num_slots * (uint64_t)p.HV;
+        const uint64_t items = (uint64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
+        if (p.T <= kChunkMaxT && p.rT >= 1 && p.rT <= kChunkMaxT && heads <= INT32_MAX && items <= INT32_MAX) {
+            err = launch_chunked<DK, InT, kModeReplayVerify>(p, B, s);
+            return true;
+        }
+    }
+    return false;
+}
+
+template <typename InT>
+bool launch_replay_verify(const RecurrentParams& p, int B, int DK, cudaStream_t s, cudaError_t& err) {
+    switch (DK) {
+    case 64: return launch_replay_verify_dk<InT, 64>(p, B, s, err);
+    case 128: return launch_replay_verify_dk<InT, 128>(p, B, s, err);
+    case 256: return launch_replay_verify_dk<InT, 256>(p, B, s, err);
+    default: return false;
+    }
 }
 
 template <typename InT, typename StT>

@@ -17,15 +17,18 @@
 // kh.kh and kh.qh are formed with mma.sync from the same hi + lo rows, and each row's small triangular
 // recurrence runs in fp32 registers, one thread per row.
 //
-// Two modes, for bf16 state pools, T <= 8 and DK in {64, 128, 256} (the launcher's choice):
-//   verify (kCommit = false)   outputs o only: no intermediate states, no write-back.  A stage is refilled as
+// Three modes, for bf16 state pools, T <= 8 and DK in {64, 128, 256} (the launcher's choice):
+//   verify                     outputs o only: no intermediate states, no write-back.  A stage is refilled as
 //                              soon as the MMA that reads it has completed, before the row recurrence runs;
-//   replay commit (kCommit)    the first L = steps[b] tokens, no outputs, and the state after them,
+//   replay commit              the first L = steps[b] tokens, no outputs, and the state after them,
 //                              S_L = gamma_L S_0 + sum_{s<L} G(s, L-1) delta_s kh_s^T, written back into the
 //                              slot (kh only: 2T columns, one Gram matrix).  The rank-L update is one more
 //                              tcgen05.mma: the per-row coefficients go to tensor memory (tcgen05.st, A operand),
 //                              B is the kh hi / lo rows read MN-major; each thread adds gamma_L S_0 to its row
-//                              of the product and writes the row over the stage, which a TMA store writes back.
+//                              of the product and writes the row over the stage, which a TMA store writes back;
+//   replay commit + verify     the replay commit of an earlier call's accepted tokens, then verify of this
+//                              call's tokens from the committed state as written (the rows over the stage): one
+//                              read and one write of every state for a whole speculative step.
 //
 // Work item = 128 state rows of one (lane, value head); items are numbered row block fastest, then value
 // head, then lane, and each CTA (4 warps, warp w owning rows [32w, 32w + 32)) takes a contiguous range of
@@ -54,44 +57,57 @@ constexpr int kChunkMinDK = 64;  // rows of 64 bf16 at least: whole 128-byte swi
 constexpr uint32_t kChunkWaitPolls = GDN_WAIT_POLLS;
 constexpr int kChunkMaxGroups = 3;
 
+// The chunked kernel's modes: verify only, replay commit only, and replay commit then verify in one pass.
+enum ChunkMode { kModeVerify = 0, kModeReplay = 1, kModeReplayVerify = 2 };
+
 // Shared-memory plan of one group, as byte offsets from its 1024-byte aligned base; the groups of a CTA sit
-// one after another, then a word for the tensor-memory address.
-template <int DK, bool kCommit, int NS>
+// one after another, then a word for the tensor-memory address.  Tr = tokens of the replay set (0 in verify
+// mode), Tv = tokens of the verify set (0 in replay mode).
+template <int DK, int kMode, int NS>
 struct ChunkPlan {
     static_assert(DK % 64 == 0, "the chunked kernel takes whole 128-byte rows");
+    static constexpr bool kReplay = kMode != kModeVerify;
+    static constexpr bool kVerify = kMode != kModeReplay;
     static constexpr int NBOX = DK / 64;                      // 64-column (128-byte) boxes per row
     static constexpr uint32_t BOX_BYTES = kChunkRows * 128;   // one box of a stage
     static constexpr uint32_t STAGE_BYTES = kChunkRows * DK * 2;
-    // columns of P: kh hi, kh lo (and qh hi, qh lo in verify mode), T each
-    __host__ __device__ static constexpr int ncols(int T) { return kCommit ? 2 * T : 4 * T; }
-    // the MMA's N for P: a multiple of 16
-    __host__ __device__ static constexpr int nb(int T) { return (ncols(T) + 15) / 16 * 16; }
-    // replay commit: the K of the write-back, coefficients [c hi | c hi | c lo] against B rows [kh hi; kh lo; kh hi]
-    __host__ __device__ static constexpr int a2_cols(int T) { return (3 * T + 15) / 16 * 16; }
-    // rows of B: verify [kh hi | kh lo | qh hi | qh lo], replay [kh hi | kh lo | kh hi], zero rows to a multiple
-    // of 16
-    __host__ __device__ static constexpr int brows(int T) { return kCommit ? a2_cols(T) : nb(T); }
-    __host__ __device__ static constexpr uint32_t b_off() { return NS * STAGE_BYTES; }
-    __host__ __device__ static constexpr uint32_t b_bytes(int T) { return (uint32_t)brows(T) * DK * 2; }
-    // tensor-memory columns of one group: P (verify); the product D (DK columns, P overlaps its first ones), then
-    // the coefficients, two bf16 per column (replay)
+    // replay set: P columns kh hi | kh lo (2 Tr), the MMA's N a multiple of 16; B rows kh hi | kh lo | kh hi
+    // (3 Tr, the write-back's K, against coefficients [c hi | c hi | c lo]) padded with zero rows to 16
+    __host__ __device__ static constexpr int nr(int Tr) { return (2 * Tr + 15) / 16 * 16; }
+    __host__ __device__ static constexpr int rrows(int Tr) { return kReplay ? (3 * Tr + 15) / 16 * 16 : 0; }
+    // verify set: B rows kh hi | kh lo | qh hi | qh lo (4 Tv) padded to 16, also the MMA's N
+    __host__ __device__ static constexpr int vrows(int Tv) { return kVerify ? (4 * Tv + 15) / 16 * 16 : 0; }
+    __host__ __device__ static constexpr uint32_t br_off() { return NS * STAGE_BYTES; }
+    __host__ __device__ static constexpr uint32_t bv_off(int Tr) { return br_off() + (uint32_t)rrows(Tr) * DK * 2; }
+    // g, beta of the replay set (Tr each), then of the verify set (Tv each)
+    __host__ __device__ static constexpr uint32_t s_off(int Tr, int Tv) {
+        return bv_off(Tr) + (uint32_t)vrows(Tv) * DK * 2;
+    }
+    // the Gram matrices, transposed (row t holds kh_s . kh_t or kh_s . qh_t over s, padded to tp(T) floats):
+    // replay kh.kh (Tr rows), then verify kh.kh and kh.qh (Tv rows each)
+    __host__ __device__ static constexpr int tp(int T) { return (T + 3) & ~3; }
+    __host__ __device__ static constexpr uint32_t gram_off(int Tr, int Tv) {
+        return s_off(Tr, Tv) + ((8u * (Tr + Tv) + 15u) & ~15u);
+    }
+    // NS tile mbarriers and the MMA mbarrier, a failure flag, then per stage the pool slot (-1: nothing loaded)
+    // and the token count of its item
+    __host__ __device__ static constexpr uint32_t ctl_off(int Tr, int Tv) {
+        return gram_off(Tr, Tv) + 4u * (uint32_t)(Tr * tp(Tr) + 2 * Tv * tp(Tv));
+    }
+    __host__ __device__ static constexpr uint32_t group_bytes(int Tr, int Tv) {
+        return (ctl_off(Tr, Tv) + 8u * (NS + 1) + 8u + 8u * NS + 1023u) & ~1023u;
+    }
+    __host__ __device__ static constexpr uint32_t bytes(int Tr, int Tv, int G) {
+        return (uint32_t)G * group_bytes(Tr, Tv) + 16u + 1024u;  // + the tensor-memory address, + alignment slack
+    }
+    // the largest plan: T = kChunkMaxT in each set the mode has
+    __host__ __device__ static constexpr uint32_t max_bytes(int G) {
+        return bytes(kReplay ? kChunkMaxT : 0, kVerify ? kChunkMaxT : 0, G);
+    }
+    // tensor-memory columns of one group: P; in the replay modes also the product D (DK columns, P overlaps its
+    // first ones), then the coefficients, two bf16 per column
     __host__ __device__ static constexpr uint32_t a2_col() { return DK; }
-    __host__ __device__ static constexpr uint32_t tmem_cols() { return kCommit ? (DK + 16 + 31) / 32 * 32 : 32; }
-    // g, beta (T each), then the Gram matrices, transposed (row t holds kh_s . kh_t, kh_s . qh_t over s)
-    __host__ __device__ static constexpr uint32_t s_off(int T) { return b_off() + b_bytes(T); }
-    __host__ __device__ static constexpr int gram_stride(int T) { return (T + 3) & ~3; }
-    __host__ __device__ static constexpr uint32_t gram_off(int T) { return s_off(T) + ((8u * T + 15u) & ~15u); }
-    // NS tile mbarriers and the MMA mbarrier, the tensor-memory address and a failure flag, then per stage the
-    // pool slot (-1: nothing loaded) and the token count of its item
-    __host__ __device__ static constexpr uint32_t ctl_off(int T) {
-        return gram_off(T) + 2u * T * gram_stride(T) * 4;
-    }
-    __host__ __device__ static constexpr uint32_t group_bytes(int T) {
-        return (ctl_off(T) + 8u * (NS + 1) + 8u + 8u * NS + 1023u) & ~1023u;
-    }
-    __host__ __device__ static constexpr uint32_t bytes(int T, int G) {
-        return (uint32_t)G * group_bytes(T) + 16u + 1024u;  // + the tensor-memory address, + alignment slack
-    }
+    __host__ __device__ static constexpr uint32_t tmem_cols() { return kReplay ? (DK + 16 + 31) / 32 * 32 : 32; }
 };
 
 // One group's barrier (named barrier `id`, its 128 threads), and the same with an OR over a predicate.
@@ -356,179 +372,234 @@ __device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const fl
 }
 
 // Per-item inputs in registers, kept in their storage type until used (a conversion right after the load would
-// wait for it): q / k (this lane's 16-byte pieces of every vector pass), v of row tid, and, on the last warp, a
-// and b of token tid - (128 - 32) with the head's A_log and dt_bias.  Each field is loaded for the next item
-// right after its last use in the current one, so every load has about one item of lead time and none is
-// waited for by a register copy.
-template <int DK, typename InT, bool kCommit>
+// wait for it): the q / k pieces of this lane (16 bytes of one vector per pass), v of row tid for the replay set
+// and the verify set, and, on the last warp, a and b of one token (lanes 0..15: replay set, 16..31: verify set)
+// with the head's A_log and dt_bias.  Each field is loaded for the next item right after its last use in the
+// current one, so every load has about one item of lead time and none is waited for by a register copy.
+template <int DK, typename InT, int kMode>
 struct ItemRegs {
-    static constexpr int VPASS = 4 * (32 / (DK / 8));
-    static constexpr int NPASS = ((kCommit ? 1 : 2) * kChunkMaxT + VPASS - 1) / VPASS;
+    static constexpr int VPASS = 4 * (32 / (DK / 8));  // vectors per pass of the group
+    static constexpr int NVEC = (kMode != kModeVerify ? kChunkMaxT : 0) + (kMode != kModeReplay ? 2 * kChunkMaxT : 0);
+    static constexpr int NPASS = (NVEC + VPASS - 1) / VPASS;
     uint4 raw[NPASS][Slice8<InT>::NC];
-    InT v[kChunkMaxT];
+    InT vr[kMode != kModeVerify ? kChunkMaxT : 1];
+    InT vv[kMode != kModeReplay ? kChunkMaxT : 1];
     InT a, b;
     float A_log, dt_bias;
 };
 
-// After the tile's MMA: every thread reads the P row of its state row from tensor memory, then runs the row's
-// recurrence (verify: o), or forms its coefficients and the group rewrites the tile and stores it (replay
-// commit).  False: a wait ran out (nothing was written).
-template <int T, int DK, typename InT, bool kCommit, int NS>
-__device__ __forceinline__ bool chunk_rows(const RecurrentParams& p, const CUtensorMap* tmap, uint32_t tmem,
-                                           unsigned char* sm, uint32_t base, uint32_t stage,
-                                           const float (&vr)[kChunkMaxT], int b, int h, int row0, int nrows, int slot,
-                                           int L, int bar_id, uint32_t mma_bar, uint32_t& mphase) {
-    using CS = ChunkPlan<DK, kCommit, NS>;
-    constexpr int NP = CS::nb(T);  // columns of P in tensor memory
-    constexpr int TP = (T + 3) & ~3;
+// Gram matrix X[t][s] = x_s . y_t (x_s: rows s and T + s of the region, hi and lo; y_t: rows (yb) T + t and
+// (yb + 1) T + t, hi and lo) on mma.sync, one warp: A rows 0..7 address x hi 0..7 and rows 8..15 x lo 0..7, B
+// columns 8 nb .. 8 nb + 7 address block yb + nb; rows past T point at row 0 and their products are dropped.  The
+// four products of a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane; two accumulation chains (even and
+// odd k steps) halve the latency.  Stored transposed in rows of TP floats.
+template <int DK>
+__device__ __forceinline__ void gram_warp(uint32_t bbase, int BR, int T, int yb, float* out, int TP, int lane) {
+    constexpr int KSTEPS = DK / 16;
+    const int m = lane & 15;
+    const int arow = m < 8 ? (m < T ? m : 0) : (m - 8 < T ? T + m - 8 : 0);
+    const int jr = lane & 7;
+    const int brow0 = jr < T ? yb * T + jr : 0, brow1 = jr < T ? (yb + 1) * T + jr : 0;
+    float g[2][4], g2[2][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) g[0][c] = g[1][c] = g2[0][c] = g2[1][c] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1, c0, c1;
+        ldsm_x4(bbase + sw128(BR, arow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+        ldsm_x2(bbase + sw128(BR, brow0, 2 * ks + ((lane >> 3) & 1)), b0, b1);
+        ldsm_x2(bbase + sw128(BR, brow1, 2 * ks + ((lane >> 3) & 1)), c0, c1);
+        mma_bf16_16816((ks & 1) ? g2[0] : g[0], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816((ks & 1) ? g2[1] : g[1], a0, a1, a2, a3, c0, c1);
+    }
+    const int s_ = lane >> 2;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t_ = 2 * (lane & 3) + e;
+        if (s_ < T && t_ < T)
+            out[t_ * TP + s_] = ((g[0][e] + g2[0][e]) + (g[1][e] + g2[1][e])) +
+                                ((g[0][2 + e] + g2[0][2 + e]) + (g[1][2 + e] + g2[1][2 + e]));
+    }
+}
+
+// Replay set, after its P MMA: every thread reads the P row of its state row from tensor memory and forms the
+// row's coefficients; the group multiplies them into the tile on the tensor cores, each thread adds gamma_L S_0
+// to its row and writes it over the stage, and PT stores the tile into the slot.  False: a wait ran out (the
+// stage and the slot are left as they are).
+template <int T, int DK, typename InT, int kMode, int NS>
+__device__ __forceinline__ bool replay_rows(const CUtensorMap* tmap, uint32_t tmem, unsigned char* sm, uint32_t base,
+                                            uint32_t stage, const float (&v)[kChunkMaxT], const float* gs,
+                                            const float* bs, const float* KK, int h, int HV, int row0, int slot, int L,
+                                            int bar_id, uint32_t mma_bar, uint32_t& mphase) {
+    using CS = ChunkPlan<DK, kMode, NS>;
+    constexpr int PT = 64;
+    constexpr int NP = CS::nr(T);
+    constexpr int K2 = CS::rrows(T);
     const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5;
-    const float* gs = reinterpret_cast<const float*>(sm + CS::s_off(T));
-    const float* bs = gs + T;
-    const float* KK = reinterpret_cast<const float*>(sm + CS::gram_off(T));
-    const float* KQ = KK + T * TP;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    float pr[NP];
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < NP; c += 16) tmem_ld16(lane_base + c, pr + c);
+    tmem_wait_ld();
+    uint32_t a2[K2 / 2];
+    row_coefficients<T, NP, K2>(pr, v, gs, bs, KK, L, a2);
+#pragma unroll
+    for (int c = 0; c < K2 / 2; c += 8) tmem_st8(lane_base + CS::a2_col() + c, a2 + c);
+    tmem_wait_st();
+    float gamma = 1.f;
+    for (int t = 0; t < L; ++t) gamma *= gs[t];
+    tc_fence_before();
+    group_sync(bar_id);  // every row's coefficients are in tensor memory, every P row has been read
+    // D = A2 [kh hi; kh lo; kh hi] on the tensor cores: A2 from tensor memory, B = the replay rows read MN-major
+    if (tid == PT) {
+        tc_fence_after();
+        const uint32_t idesc = umma_idesc_bf16(kChunkRows, DK) | (1u << 16);  // B MN-major
+        const uint32_t brb = base + CS::br_off();
+#pragma unroll
+        for (int ks = 0; ks < K2 / 16; ++ks)
+            umma_bf16_ta(tmem, tmem + CS::a2_col() + 8 * ks, umma_desc_sw128_mn(brb + 2048u * ks, K2 * 128u), idesc,
+                         ks > 0 ? 1u : 0u);
+        umma_commit(mma_bar);
+    }
+    const bool mok = mbar_wait_bounded(mma_bar, mphase, kChunkWaitPolls);
+    mphase ^= 1u;
+    if (group_sync_or(bar_id, !mok)) {  // the product never completed: leave the slot as it is
+        if (tid == PT) mbar_wait_bounded(mma_bar, mphase ^ 1u, kChunkWaitPolls);
+        return false;
+    }
+    tc_fence_after();
+    // S_L = gamma S_0 + D, this thread's row, 32 columns at a time, rounded to bf16 over the stage
+    unsigned char* srow = sm + (stage - base);
+#pragma unroll 1
+    for (int c32 = 0; c32 < DK / 32; ++c32) {
+        float d[32];
+        tmem_ld16(lane_base + 32 * c32, d);
+        tmem_ld16(lane_base + 32 * c32 + 16, d + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4* cp = reinterpret_cast<uint4*>(srow + sw128(kChunkRows, tid, 4 * c32 + q));
+            const uint4 s0 = *cp;
+            const uint32_t w[4] = {s0.x, s0.y, s0.z, s0.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = bf16x2_to_float2(w[e]);
+                o[e] = bf16x2_bits(fmaf(gamma, f.x, d[8 * q + 2 * e]), fmaf(gamma, f.y, d[8 * q + 2 * e + 1]));
+            }
+            *cp = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    fence_proxy_async_smem();  // the rows written above, then the TMA store (and a verify MMA) read them
+    tc_fence_before();
+    group_sync(bar_id);
+    if (tid == PT) {
+#pragma unroll
+        for (int j = 0; j < CS::NBOX; ++j) tma_store_3d(tmap, j * 64, row0, slot * HV + h, stage + j * CS::BOX_BYTES);
+        bulk_commit_group();
+    }
+    return true;
+}
+
+// Verify set, after its P MMA: every thread reads the P row of its state row from tensor memory and runs the
+// row's T x T recurrence, writing o.
+template <int T, int DK, typename InT, int kMode, int NS>
+__device__ __forceinline__ void verify_rows(const RecurrentParams& p, uint32_t tmem, const float (&v)[kChunkMaxT],
+                                            const float* gs, const float* bs, const float* KK, const float* KQ, int b,
+                                            int h, int row0, int nrows) {
+    using CS = ChunkPlan<DK, kMode, NS>;
+    constexpr int NP = CS::vrows(T);
+    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5;
     float pr[NP];
     tc_fence_after();
 #pragma unroll
     for (int c = 0; c < NP; c += 16) tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c, pr + c);
     tmem_wait_ld();
-    if constexpr (!kCommit) {
-        const bool live = tid < nrows;
-        const int64_t o0 = ((int64_t)b * T * p.HV + h) * p.DV + row0 + tid;
-        row_recurrence<T, NP>(p, pr, vr, gs, bs, KK, KQ, live, o0, (int64_t)p.HV * p.DV);
-    } else {
-        constexpr int PT = 64;
-        constexpr int K2 = CS::a2_cols(T);
-        constexpr int BR = CS::brows(T);
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-        uint32_t a2[K2 / 2];
-        row_coefficients<T, NP, K2>(pr, vr, gs, bs, KK, L, a2);
-#pragma unroll
-        for (int c = 0; c < K2 / 2; c += 8) tmem_st8(lane_base + CS::a2_col() + c, a2 + c);
-        tmem_wait_st();
-        float gamma = 1.f;
-        for (int t = 0; t < L; ++t) gamma *= gs[t];
-        tc_fence_before();
-        group_sync(bar_id);  // every row's coefficients are in tensor memory, every P row has been read
-        // D = A2 [kh hi; kh lo; kh hi] on the tensor cores: A2 from tensor memory, B = B's rows read MN-major
-        if (tid == PT) {
-            tc_fence_after();
-            const uint32_t idesc = umma_idesc_bf16(kChunkRows, DK) | (1u << 16);  // B MN-major
-            const uint32_t bbase = base + CS::b_off();
-#pragma unroll
-            for (int ks = 0; ks < K2 / 16; ++ks)
-                umma_bf16_ta(tmem, tmem + CS::a2_col() + 8 * ks, umma_desc_sw128_mn(bbase + 2048u * ks, BR * 128u),
-                             idesc, ks > 0 ? 1u : 0u);
-            umma_commit(mma_bar);
-        }
-        const bool mok = mbar_wait_bounded(mma_bar, mphase, kChunkWaitPolls);
-        mphase ^= 1u;
-        if (group_sync_or(bar_id, !mok)) {  // the product never completed: leave the slot as it is
-            if (tid == PT) mbar_wait_bounded(mma_bar, mphase ^ 1u, kChunkWaitPolls);
-            return false;
-        }
-        tc_fence_after();
-        // S_L = gamma S_0 + D, this thread's row, 32 columns at a time, rounded to bf16 over the stage
-        unsigned char* srow = sm + (stage - base);
-#pragma unroll 1
-        for (int c32 = 0; c32 < DK / 32; ++c32) {
-            float d[32];
-            tmem_ld16(lane_base + 32 * c32, d);
-            tmem_ld16(lane_base + 32 * c32 + 16, d + 16);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4* cp = reinterpret_cast<uint4*>(srow + sw128(kChunkRows, tid, 4 * c32 + q));
-                const uint4 s0 = *cp;
-                const uint32_t w[4] = {s0.x, s0.y, s0.z, s0.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = bf16x2_to_float2(w[e]);
-                    o[e] = bf16x2_bits(fmaf(gamma, f.x, d[8 * q + 2 * e]), fmaf(gamma, f.y, d[8 * q + 2 * e + 1]));
-                }
-                *cp = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        }
-        fence_proxy_async_smem();  // the rows written above, then the TMA store reads them
-        group_sync(bar_id);
-        if (tid == PT) {
-#pragma unroll
-            for (int j = 0; j < CS::NBOX; ++j)
-                tma_store_3d(tmap, j * 64, row0, slot * p.HV + h, stage + j * CS::BOX_BYTES);
-            bulk_commit_group();
-        }
-    }
-    return true;
+    const bool live = tid < nrows;
+    const int64_t o0 = ((int64_t)b * T * p.HV + h) * p.DV + row0 + tid;
+    row_recurrence<T, NP>(p, pr, v, gs, bs, KK, KQ, live, o0, (int64_t)p.HV * p.DV);
 }
 
 // A kernel that allocates tensor memory runs one CTA per SM, so the CTA holds G groups of 4 warps, each an
-// independent item pipeline (its own stages, B, Gram matrices, mbarriers, named barrier 1 + g and 32 columns
-// of tensor memory); group g of CTA c walks the items of virtual CTA c G + g.
-template <int DK, typename InT, bool kCommit, int NS, int G>
+// independent item pipeline (its own stages, B rows, Gram matrices, mbarriers, named barrier 1 + g and share of
+// the tensor memory); group g of CTA c walks the items of virtual CTA g gridDim + c.
+//   kModeVerify          p.q, p.k, p.v, p.a, p.b: T verify tokens; outputs o.
+//   kModeReplay          p.k, p.v, p.a, p.b: the first steps[b] of T tokens, committed into the slot.
+//   kModeReplayVerify    p.rk, p.rv, p.ra, p.rb: the first steps[b] of rT tokens committed into the slot, then
+//                        p.q .. p.b: T verify tokens from the committed state (as stored, rounded to bf16).
+template <int DK, typename InT, int kMode, int NS, int G>
 __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
     gdn_verify_chunked_kernel(const RecurrentParams p, const __grid_constant__ CUtensorMap tmap, int n_items,
                               int per_cta) {
-    using CS = ChunkPlan<DK, kCommit, NS>;
+    using CS = ChunkPlan<DK, kMode, NS>;
     using QK = Slice8<InT>;
+    using IR = ItemRegs<DK, InT, kMode>;
+    constexpr bool kReplay = CS::kReplay, kVerify = CS::kVerify;
     constexpr int ROWS = kChunkRows;
     constexpr int KSTEPS = DK / 16;
-    constexpr int LPV = DK / 8;       // lanes per q or k vector (8 columns each)
-    constexpr int VPW = 32 / LPV;     // vectors per warp per pass
-    constexpr int VPASS = 4 * VPW;    // vectors per CTA pass
-    constexpr bool kEarly = !kCommit;  // verify: a stage is refilled as soon as its MMA has completed
+    constexpr int LPV = DK / 8;        // lanes per q or k vector (8 columns each)
+    constexpr int VPW = 32 / LPV;      // vectors per warp per pass
+    constexpr int VPASS = 4 * VPW;     // vectors per group pass
+    constexpr bool kEarly = !kReplay;  // verify only: a stage is refilled as soon as its MMA has completed
     static_assert(LPV <= 32, "DK");
     const int grp = threadIdx.x / kChunkGroupThreads;
     const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5, lane = tid & 31;
     const int bar_id = 1 + grp;  // named barrier 0 is the whole CTA's
-    const int T = p.T;
+    const int Tv = kVerify ? p.T : 0;                                       // verify tokens
+    const int Tr = kMode == kModeReplay ? p.T : (kReplay ? p.rT : 0);       // replay tokens
     const int NRB = (p.DV + ROWS - 1) / ROWS;
     const int R = p.HV / p.HK;  // value heads per key head
     // virtual CTA grp * gridDim.x + blockIdx.x: with few items, group 0 of every CTA gets them first
     const int beg = (int)min((int64_t)n_items, ((int64_t)grp * gridDim.x + blockIdx.x) * per_cta);
     const int end = min(n_items, beg + per_cta);
-    // roles in a group besides the shared work: warp 1 forms the Gram matrices (warp 0 too in verify), thread PT
-    // of warp 2 issues the TMA loads and stores and the tile's MMAs (and alone waits on the tiles and its bulk
-    // groups), warp 3 computes the gates; warp 0 of the CTA allocates the tensor memory for every group
+    // roles in a group besides the shared work: warp 1 (and 0, and 3 in the combined mode) form the Gram
+    // matrices, thread PT of warp 2 issues the TMA loads and stores and the MMAs (and alone waits on the tiles and
+    // its bulk groups), warp 3 computes the gates; warp 0 of the CTA allocates the tensor memory for every group
     constexpr int PT = 64;
     constexpr int GATE_T0 = ROWS - 32;
 
     extern __shared__ unsigned char ch_smem[];
     const uint32_t raw_base = smem_u32(ch_smem);
     const uint32_t pad = ((raw_base + 1023u) & ~1023u) - raw_base;
-    unsigned char* sm = ch_smem + pad + grp * CS::group_bytes(T);  // this group's part
-    const uint32_t base = raw_base + pad + grp * CS::group_bytes(T);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ch_smem + pad + G * CS::group_bytes(T));
-    const uint32_t ctl = base + CS::ctl_off(T);  // mbarrier of stage s at ctl + 8 s; the MMA's at ctl + 8 NS
+    const uint32_t gbytes = CS::group_bytes(Tr, Tv);
+    unsigned char* sm = ch_smem + pad + grp * gbytes;  // this group's part
+    const uint32_t base = raw_base + pad + grp * gbytes;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ch_smem + pad + G * gbytes);
+    const uint32_t ctl = base + CS::ctl_off(Tr, Tv);  // mbarrier of stage s at ctl + 8 s; the MMA's at ctl + 8 NS
     const uint32_t mma_bar = ctl + 8 * NS;
-    volatile int* fail_flag = reinterpret_cast<volatile int*>(sm + CS::ctl_off(T) + 8 * (NS + 1));
-    int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(T) + 8 * (NS + 1) + 8);
+    volatile int* fail_flag = reinterpret_cast<volatile int*>(sm + CS::ctl_off(Tr, Tv) + 8 * (NS + 1));
+    int* st_slot = reinterpret_cast<int*>(sm + CS::ctl_off(Tr, Tv) + 8 * (NS + 1) + 8);
     int* st_len = st_slot + NS;
-    // B's rows, swizzled: verify k hi (T) | k lo (T) | q hi (T) | q lo (T); replay k hi | k lo | k hi; zero padding
-    unsigned char* Bs = sm + CS::b_off();
-    const uint32_t bbase = base + CS::b_off();
-    const int NB = CS::nb(T);     // the P MMA's N
-    const int BR = CS::brows(T);  // rows of B
-    float* gs = reinterpret_cast<float*>(sm + CS::s_off(T));
-    float* bs = gs + T;
-    const int TP = CS::gram_stride(T);
-    float* KK = reinterpret_cast<float*>(sm + CS::gram_off(T));  // transposed: KK[t * TP + s] = kh_s . kh_t
-    float* KQ = KK + T * TP;                                     // transposed: KQ[t * TP + s] = kh_s . qh_t
+    // B rows, swizzled: replay kh hi | kh lo | kh hi, then verify kh hi | kh lo | qh hi | qh lo; zero padding
+    unsigned char* Br = sm + CS::br_off();
+    unsigned char* Bv = sm + CS::bv_off(Tr);
+    const uint32_t brb = base + CS::br_off(), bvb = base + CS::bv_off(Tr);
+    const int RR = CS::rrows(Tr), VR = CS::vrows(Tv);
+    float* gr = reinterpret_cast<float*>(sm + CS::s_off(Tr, Tv));  // replay g, beta
+    float* br_ = gr + Tr;
+    float* gv = br_ + Tr;  // verify g, beta
+    float* bv_ = gv + Tv;
+    float* KKr = reinterpret_cast<float*>(sm + CS::gram_off(Tr, Tv));
+    float* KKv = KKr + Tr * CS::tp(Tr);
+    float* KQv = KKv + Tv * CS::tp(Tv);
 
     // thread PT: start the tile of the item at `ip` (pool slot and token count loaded one issue earlier) into
     // stage s
     auto issue = [&](const ItemPos& ip, int slot, int L, int s) {
         const int h = ip.h, rb = ip.rb;
         const bool slot_ok = slot >= 0 && slot < p.num_slots;
-        const bool len_ok = L >= 0 && L <= T;
+        const bool len_ok = L >= 0 && L <= Tr;
         if (p.err != nullptr && h == 0 && rb == 0) {  // once per lane
             if (slot != -1 && !slot_ok)
                 atomicOr(p.err, GDN_ERRBIT_INDEX);
-            else if (slot_ok && !len_ok)
+            else if (kReplay && slot_ok && !len_ok)
                 atomicOr(p.err, GDN_ERRBIT_ACCEPT_LEN);
         }
-        const bool active = slot_ok && len_ok && L > 0;
+        // replay only: nothing to do for a lane without tokens to commit; combined: a bad length commits nothing
+        const bool active = kMode == kModeReplay ? slot_ok && len_ok && L > 0 : slot_ok;
         st_slot[s] = active ? slot : -1;
-        st_len[s] = L;
+        st_len[s] = kReplay && len_ok ? L : 0;
         bool issue_copy = active;
 #ifdef GDN_TEST_MISSING_COPY
         // test build: the first item (lane 0, head 0, rows 0..) is never copied nor arrived on: its wait runs out
@@ -543,39 +614,60 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                             bar);
         }
     };
-    const int vj0 = warp * VPW + lane / LPV;  // this lane's vector in the first pass (before the j0 offset)
+    // vectors of one item, numbered: replay k_0 .. k_{Tr-1}, then verify q_0 .. q_{Tv-1}, k_0 .. k_{Tv-1}
+    const int NV = Tr + 2 * Tv;
+    const int vj0 = warp * VPW + lane / LPV;  // this lane's vector in the first pass
     const int vc = lane % LPV;                // its columns [8 vc, 8 vc + 8): chunk vc of the row
-    const int j0 = kCommit ? T : 0;           // vectors j in [j0, 2T): q_j for j < T, k_{j-T} otherwise
+    const InT* rk = static_cast<const InT*>(kMode == kModeReplay ? p.k : p.rk);
+    const InT* rv = static_cast<const InT*>(kMode == kModeReplay ? p.v : p.rv);
+    const InT* ra = static_cast<const InT*>(kMode == kModeReplay ? p.a : p.ra);
+    const InT* rbp = static_cast<const InT*>(kMode == kModeReplay ? p.b : p.rb);
     auto vec_ptr = [&](int b, int hk, int j) -> const InT* {
-        const int t = j < T ? j : j - T;
-        return static_cast<const InT*>(j < T ? p.q : p.k) + (((int64_t)b * T + t) * p.HK + hk) * DK + 8 * vc;
+        if (j < Tr) return rk + (((int64_t)b * Tr + j) * p.HK + hk) * DK + 8 * vc;
+        j -= Tr;
+        const int t = j < Tv ? j : j - Tv;
+        return static_cast<const InT*>(j < Tv ? p.q : p.k) + (((int64_t)b * Tv + t) * p.HK + hk) * DK + 8 * vc;
     };
-    using IR = ItemRegs<DK, InT, kCommit>;
     auto load_qk = [&](const ItemPos& ip, bool need_qk, IR& r) {
 #pragma unroll
         for (int ps = 0; ps < IR::NPASS; ++ps) {
-            const int j = j0 + vj0 + ps * VPASS;
+            const int j = vj0 + ps * VPASS;
 #pragma unroll
             for (int c = 0; c < QK::NC; ++c) r.raw[ps][c] = make_uint4(0, 0, 0, 0);
-            if (need_qk && j < 2 * T) QK::load_global(vec_ptr(ip.b, ip.hk, j), r.raw[ps]);
+            if (need_qk && j < NV) QK::load_global(vec_ptr(ip.b, ip.hk, j), r.raw[ps]);
         }
     };
     auto load_v = [&](const ItemPos& ip, IR& r) {
         const int row = ip.rb * ROWS + tid;
-        const InT* vsrc = static_cast<const InT*>(p.v) + ((int64_t)ip.b * T * p.HV + ip.h) * p.DV + row;
+        if constexpr (kReplay) {
+            const InT* src = rv + ((int64_t)ip.b * Tr * p.HV + ip.h) * p.DV + row;
 #pragma unroll
-        for (int t = 0; t < kChunkMaxT; ++t) {
-            r.v[t] = InT(0.f);
-            if (t < T && row < p.DV) r.v[t] = vsrc[(int64_t)t * p.HV * p.DV];
+            for (int t = 0; t < kChunkMaxT; ++t) {
+                r.vr[t] = InT(0.f);
+                if (t < Tr && row < p.DV) r.vr[t] = src[(int64_t)t * p.HV * p.DV];
+            }
+        }
+        if constexpr (kVerify) {
+            const InT* src = static_cast<const InT*>(p.v) + ((int64_t)ip.b * Tv * p.HV + ip.h) * p.DV + row;
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t) {
+                r.vv[t] = InT(0.f);
+                if (t < Tv && row < p.DV) r.vv[t] = src[(int64_t)t * p.HV * p.DV];
+            }
         }
     };
+    // gate lanes of warp 3: 0..15 the replay set, 16..31 the verify set
+    const int gt = tid - GATE_T0;
+    const bool gate_r = kReplay && gt >= 0 && gt < Tr;
+    const bool gate_v = kVerify && gt >= 16 && gt - 16 < Tv;
     auto load_ab = [&](const ItemPos& ip, IR& r) {
         r.a = r.b = InT(0.f);
         r.A_log = r.dt_bias = 0.f;
-        if (tid >= GATE_T0 && tid - GATE_T0 < T) {
-            const int64_t ab = ((int64_t)ip.b * T + (tid - GATE_T0)) * p.HV + ip.h;
-            r.a = static_cast<const InT*>(p.a)[ab];
-            r.b = static_cast<const InT*>(p.b)[ab];
+        if (gate_r || gate_v) {
+            const int t = gate_r ? gt : gt - 16;
+            const int64_t ab = ((int64_t)ip.b * (gate_r ? Tr : Tv) + t) * p.HV + ip.h;
+            r.a = (gate_r ? ra : static_cast<const InT*>(p.a))[ab];
+            r.b = (gate_r ? rbp : static_cast<const InT*>(p.b))[ab];
             r.A_log = p.A_log[ip.h];
             r.dt_bias = p.dt_bias[ip.h];
         }
@@ -590,7 +682,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         ipos.next(NRB, p.HV, R);
         if (++nis < end) {
             islot = p.indices[ipos.b];
-            ilen = kCommit ? p.steps[ipos.b] : T;
+            ilen = kReplay ? p.steps[ipos.b] : 0;
         }
     };
     // tensor-memory columns of the CTA: a power of 2 covering every group's share
@@ -606,12 +698,14 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         fence_mbar_init();
         *fail_flag = 0;
         islot = p.indices[ipos.b];
-        ilen = kCommit ? p.steps[ipos.b] : T;
+        ilen = kReplay ? p.steps[ipos.b] : 0;
         for (int j = 0; j < (kEarly ? NS : NS - 1) && nis < end; ++j) issue_next(j);
     }
-    // B's padding rows stay zero (the products with them are never used, and must be finite)
-    for (int i2 = (kCommit ? 3 : 4) * T * (DK / 8) + tid; i2 < BR * (DK / 8); i2 += ROWS)
-        *reinterpret_cast<uint4*>(Bs + sw128(BR, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
+    // the padding rows of B stay zero (the products with them are never used, and must be finite)
+    for (int i2 = 3 * Tr * (DK / 8) + tid; i2 < RR * (DK / 8); i2 += ROWS)
+        *reinterpret_cast<uint4*>(Br + sw128(RR, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
+    for (int i2 = 4 * Tv * (DK / 8) + tid; i2 < VR * (DK / 8); i2 += ROWS)
+        *reinterpret_cast<uint4*>(Bv + sw128(VR, i2 / (DK / 8), i2 % (DK / 8))) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();  // the padding rows are read by the tensor cores too
     IR in;  // the current item's inputs (each field refilled for the next item after its last use)
     if (beg < end) {
@@ -638,6 +732,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         const int slot = st_slot[st];
         const int L = st_len[st];
         const bool active = slot >= 0;
+        const bool replay_now = kReplay && active && L > 0;
         const bool reuse = b == prev_b && hk == prev_hk;  // same lane and key head: q, k, Gram still in place
         prev_b = b;
         prev_hk = hk;
@@ -648,8 +743,8 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
             // token prologue: normalise q and k into bf16 hi + lo rows of B
 #pragma unroll
             for (int pass = 0; pass < IR::NPASS; ++pass) {
-                if (j0 + pass * VPASS >= 2 * T) break;
-                const int j = j0 + vj0 + pass * VPASS;
+                if (pass * VPASS >= NV) break;
+                const int j = vj0 + pass * VPASS;
                 float2 x[4];
                 QK::unpack(in.raw[pass], x);
                 float ss = 0.f;
@@ -657,7 +752,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                 for (int e = 0; e < 4; ++e) ss = fmaf(x[e].x, x[e].x, fmaf(x[e].y, x[e].y, ss));
 #pragma unroll
                 for (int m = 1; m < LPV; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-                if (j < 2 * T) {
+                if (j < NV) {
                     const float rn = rsqrtf(ss + p.l2_eps);
                     uint32_t hw[4], lw[4];
 #pragma unroll
@@ -668,13 +763,18 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                         hw[e] = *reinterpret_cast<const uint32_t*>(&hi2);
                         lw[e] = *reinterpret_cast<const uint32_t*>(&lo2);
                     }
-                    const int t = j < T ? j : j - T;
-                    const int hi_row = j < T ? 2 * T + t : t;  // q hi rows start at 2T, k hi rows at 0
-                    *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row + T, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    if (kCommit)  // the write-back's third block of B: kh hi again
-                        *reinterpret_cast<uint4*>(Bs + sw128(BR, hi_row + 2 * T, vc)) =
-                            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    const uint4 hv = make_uint4(hw[0], hw[1], hw[2], hw[3]), lv = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    if (j < Tr) {  // replay k_j: rows j (hi), Tr + j (lo), 2 Tr + j (hi again)
+                        *reinterpret_cast<uint4*>(Br + sw128(RR, j, vc)) = hv;
+                        *reinterpret_cast<uint4*>(Br + sw128(RR, Tr + j, vc)) = lv;
+                        *reinterpret_cast<uint4*>(Br + sw128(RR, 2 * Tr + j, vc)) = hv;
+                    } else {  // verify q_t: rows 2 Tv + t, 3 Tv + t; k_t: rows t, Tv + t
+                        const int jj = j - Tr;
+                        const int t = jj < Tv ? jj : jj - Tv;
+                        const int hi_row = jj < Tv ? 2 * Tv + t : t;
+                        *reinterpret_cast<uint4*>(Bv + sw128(VR, hi_row, vc)) = hv;
+                        *reinterpret_cast<uint4*>(Bv + sw128(VR, hi_row + Tv, vc)) = lv;
+                    }
                 }
             }
             fence_proxy_async_smem();  // B is written here and read by the tensor cores' MMA
@@ -682,72 +782,43 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         if (it + 1 < end) load_qk(npos, !(npos.b == b && npos.hk == hk), in);
         tc_fence_before();
         group_sync(bar_id);
-        // replay commit: the refill of the stage the last item used, once its store has read it
+        // replay modes: the refill of the stage the last item used, once its store has read it
         if (!kEarly && tid == PT && nis < end && nis == it + NS - 1) {
             bulk_wait_read_all();
             issue_next((i + NS - 1) % NS);
         }
-        if (active && tid >= GATE_T0 && tid - GATE_T0 < T) {
-            gs[tid - GATE_T0] = gate(in.A_log, to_f32(in.a), in.dt_bias);
-            bs[tid - GATE_T0] = sigmoid(to_f32(in.b));
+        if (active && (gate_r || gate_v)) {
+            float* gd = gate_r ? gr + gt : gv + (gt - 16);
+            gd[0] = gate(in.A_log, to_f32(in.a), in.dt_bias);
+            gd[gate_r ? Tr : Tv] = sigmoid(to_f32(in.b));
         }
         if (it + 1 < end) load_ab(npos, in);
-        if (active && !reuse && (warp == 1 || (!kCommit && warp == 0))) {
-            // Gram matrices kh.kh (and kh.qh in verify mode) on mma.sync, from the hi + lo rows of B: A rows
-            // 0..7 address kh_0..kh_7 and rows 8..15 kl_0..kl_7, B columns 8 nb .. 8 nb + 7 address block nb of B
-            // (kh, kl, qh, ql); rows past T point at row 0 and their products are dropped.  The four products of
-            // a pair (hi.hi, hi.lo, lo.hi, lo.lo) then sit in one lane.  Warp 1 forms kh.kh from blocks 0, 1; in
-            // verify, warp 0 forms kh.qh from blocks 2, 3 at the same time.
-            constexpr int NBLK = 2;
-            const int nb0 = warp == 1 ? 0 : 2;
-            const int m = lane & 15;
-            const int arow = m < 8 ? (m < T ? m : 0) : (m - 8 < T ? T + m - 8 : 0);
-            int brow[NBLK];
-#pragma unroll
-            for (int nb = 0; nb < NBLK; ++nb) {
-                const int jr = lane & 7;
-                brow[nb] = jr < T ? (nb0 + nb) * T + jr : 0;
-            }
-            float g[NBLK][4], g2[NBLK][4];  // two accumulation chains (even and odd k steps): half the latency
-#pragma unroll
-            for (int nb = 0; nb < NBLK; ++nb)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) g[nb][c] = g2[nb][c] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(bbase + sw128(BR, arow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-                for (int nb = 0; nb < NBLK; ++nb) {
-                    uint32_t b0, b1;
-                    ldsm_x2(bbase + sw128(BR, brow[nb], 2 * ks + ((lane >> 3) & 1)), b0, b1);
-                    mma_bf16_16816((ks & 1) ? g2[nb] : g[nb], a0, a1, a2, a3, b0, b1);
-                }
-            }
-#pragma unroll
-            for (int nb = 0; nb < NBLK; ++nb)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) g[nb][c] += g2[nb][c];
-            const int s_ = lane >> 2;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t_ = 2 * (lane & 3) + e;
-                if (s_ < T && t_ < T)
-                    (warp == 1 ? KK : KQ)[t_ * TP + s_] = (g[0][e] + g[1][e]) + (g[0][2 + e] + g[1][2 + e]);
+        if (active && !reuse) {
+            if (kMode == kModeVerify) {
+                if (warp == 1) gram_warp<DK>(bvb, VR, Tv, 0, KKv, CS::tp(Tv), lane);
+                if (warp == 0) gram_warp<DK>(bvb, VR, Tv, 2, KQv, CS::tp(Tv), lane);
+            } else if (kMode == kModeReplay) {
+                if (warp == 1) gram_warp<DK>(brb, RR, Tr, 0, KKr, CS::tp(Tr), lane);
+            } else {
+                if (warp == 1) gram_warp<DK>(brb, RR, Tr, 0, KKr, CS::tp(Tr), lane);
+                if (warp == 0) gram_warp<DK>(bvb, VR, Tv, 2, KQv, CS::tp(Tv), lane);
+                if (warp == 3) gram_warp<DK>(bvb, VR, Tv, 0, KKv, CS::tp(Tv), lane);
             }
         }
-        // P = S_0 [kh hi | kh lo | qh hi | qh lo]^T on the tensor cores, issued by PT once the tile has landed
+        // the first MMA, issued by PT once the tile has landed: S_0 [kh hi | kh lo] of the replay set, or (nothing
+        // to commit) S_0 [kh hi | kh lo | qh hi | qh lo] of the verify set
         if (active && tid == PT) {
             if (mbar_wait_bounded(ctl + 8 * st, (phase >> st) & 1u, kChunkWaitPolls)) {
                 tc_fence_after();
-                const uint32_t idesc = umma_idesc_bf16(ROWS, NB);
+                const uint32_t bb = replay_now ? brb : bvb;
+                const uint32_t box = (uint32_t)(replay_now ? RR : VR) * 128u;
+                const uint32_t idesc = umma_idesc_bf16(ROWS, replay_now ? CS::nr(Tr) : VR);
                 const uint32_t stage = base + st * CS::STAGE_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     const uint32_t koff = (uint32_t)((ks & 3) * 32);  // 16 columns further inside the 128-byte span
-                    const uint64_t ad = umma_desc_sw128(stage + (uint32_t)(ks >> 2) * CS::BOX_BYTES + koff);
-                    const uint64_t bd = umma_desc_sw128(bbase + (uint32_t)(ks >> 2) * (uint32_t)BR * 128u + koff);
-                    umma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                    umma_bf16(tmem, umma_desc_sw128(stage + (uint32_t)(ks >> 2) * CS::BOX_BYTES + koff),
+                              umma_desc_sw128(bb + (uint32_t)(ks >> 2) * box + koff), idesc, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(mma_bar);
             } else {
@@ -776,34 +847,78 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                     const int s2 = (i + j) % NS;
                     if (st_slot[s2] >= 0) mbar_wait_bounded(ctl + 8 * s2, (phase >> s2) & 1u, kChunkWaitPolls);
                 }
-                if (kCommit) bulk_wait_all();
+                if (kReplay) bulk_wait_all();
             }
             break;
         }
-        // verify: the stage is free as soon as its MMA has completed
+        // verify only: the stage is free as soon as its MMA has completed
         if (kEarly && tid == PT && nis < end) issue_next(st);
 
-        float vr[kChunkMaxT];
+        float vrr[kChunkMaxT], vrv[kChunkMaxT];
 #pragma unroll
-        for (int t = 0; t < kChunkMaxT; ++t) vr[t] = to_f32(in.v[t]);
+        for (int t = 0; t < kChunkMaxT; ++t) {
+            vrr[t] = kReplay ? to_f32(in.vr[kReplay ? t : 0]) : 0.f;
+            vrv[t] = kVerify ? to_f32(in.vv[kVerify ? t : 0]) : 0.f;
+        }
         if (it + 1 < end) load_v(npos, in);
         if (active) {
             const uint32_t stage = base + st * CS::STAGE_BYTES;
-            // replay commit: the write-back reads the tile itself; each thread acquires the landed copy (its wait
-            // ends at once: PT saw the phase complete)
-            if (kCommit) mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
-            bool rows_ok = true;
-            switch (T) {
-            case 1: rows_ok = chunk_rows<1, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 2: rows_ok = chunk_rows<2, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 3: rows_ok = chunk_rows<3, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 4: rows_ok = chunk_rows<4, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 5: rows_ok = chunk_rows<5, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 6: rows_ok = chunk_rows<6, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            case 7: rows_ok = chunk_rows<7, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
-            default: rows_ok = chunk_rows<8, DK, InT, kCommit, NS>(p, &tmap, tmem, sm, base, stage, vr, b, h, row0, nrows, slot, L, bar_id, mma_bar, mphase); break;
+            bool ok = true;
+            if constexpr (kReplay) if (replay_now) {
+                // the write-back reads the tile itself: each thread acquires the landed copy (its wait ends at
+                // once: PT saw the phase complete)
+                mbar_wait_bounded(ctl + 8 * st, ((phase >> st) & 1u) ^ 1u, kChunkWaitPolls);
+#define GDN_REPLAY_ROWS(TT)                                                                                      \
+    ok = replay_rows<TT, DK, InT, kMode, NS>(&tmap, tmem, sm, base, stage, vrr, gr, br_, KKr, h, p.HV, row0, slot, L, \
+                                             bar_id, mma_bar, mphase)
+                switch (Tr) {
+                case 1: GDN_REPLAY_ROWS(1); break;
+                case 2: GDN_REPLAY_ROWS(2); break;
+                case 3: GDN_REPLAY_ROWS(3); break;
+                case 4: GDN_REPLAY_ROWS(4); break;
+                case 5: GDN_REPLAY_ROWS(5); break;
+                case 6: GDN_REPLAY_ROWS(6); break;
+                case 7: GDN_REPLAY_ROWS(7); break;
+                default: GDN_REPLAY_ROWS(8); break;
+                }
+#undef GDN_REPLAY_ROWS
+                if (kVerify && ok) {
+                    // the verify set's MMA on the committed state, from the rows just written over the stage
+                    if (tid == PT) {
+                        tc_fence_after();
+                        const uint32_t idesc = umma_idesc_bf16(ROWS, VR);
+#pragma unroll
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                            const uint32_t koff = (uint32_t)((ks & 3) * 32);
+                            umma_bf16(tmem, umma_desc_sw128(stage + (uint32_t)(ks >> 2) * CS::BOX_BYTES + koff),
+                                      umma_desc_sw128(bvb + (uint32_t)(ks >> 2) * (uint32_t)VR * 128u + koff), idesc,
+                                      ks > 0 ? 1u : 0u);
+                        }
+                        umma_commit(mma_bar);
+                    }
+                    const bool vok = mbar_wait_bounded(mma_bar, mphase, kChunkWaitPolls);
+                    mphase ^= 1u;
+                    if (group_sync_or(bar_id, !vok)) {
+                        if (tid == PT) mbar_wait_bounded(mma_bar, mphase ^ 1u, kChunkWaitPolls);
+                        ok = false;
+                    }
+                }
             }
-            if (!rows_ok) {  // a wait ran out inside: report it and drain the tiles issued ahead
+            if constexpr (kVerify) if (ok) {
+#define GDN_VERIFY_ROWS(TT) verify_rows<TT, DK, InT, kMode, NS>(p, tmem, vrv, gv, bv_, KKv, KQv, b, h, row0, nrows)
+                switch (Tv) {
+                case 1: GDN_VERIFY_ROWS(1); break;
+                case 2: GDN_VERIFY_ROWS(2); break;
+                case 3: GDN_VERIFY_ROWS(3); break;
+                case 4: GDN_VERIFY_ROWS(4); break;
+                case 5: GDN_VERIFY_ROWS(5); break;
+                case 6: GDN_VERIFY_ROWS(6); break;
+                case 7: GDN_VERIFY_ROWS(7); break;
+                default: GDN_VERIFY_ROWS(8); break;
+                }
+#undef GDN_VERIFY_ROWS
+            }
+            if (!ok) {  // a wait ran out inside: report it and drain the tiles issued ahead
                 failed = true;
                 if (tid == PT) {
                     if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
@@ -818,7 +933,7 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         }
         pos = npos;
     }
-    if (kCommit && !failed && tid == PT) bulk_wait_all();
+    if (kReplay && !failed && tid == PT) bulk_wait_all();
     // every group's tensor-memory reads are complete before the allocation is released
     tc_fence_before();
     __syncthreads();
@@ -868,24 +983,27 @@ constexpr int kChunkStages = GDN_CHUNK_STAGES;
 constexpr int kChunkCachedDevices = 64;  // devices whose launch settings are cached
 constexpr uint32_t kChunkMaxSmem = 227 * 1024;  // dynamic shared memory a CTA may open
 
-// groups per CTA: as many as the shared memory of T = 8 allows, up to kChunkMaxGroups
-template <int DK, bool kCommit, int NS>
+// groups per CTA: as many as the shared memory of T = 8 (in every token set of the mode) allows, up to
+// kChunkMaxGroups
+template <int DK, int kMode, int NS>
 constexpr int chunk_groups() {
-    using CS = ChunkPlan<DK, kCommit, NS>;
+    using CS = ChunkPlan<DK, kMode, NS>;
     for (int g = kChunkMaxGroups; g > 1; --g)
-        if (CS::bytes(kChunkMaxT, g) <= kChunkMaxSmem) return g;
+        if (CS::max_bytes(g) <= kChunkMaxSmem) return g;
     return 1;
 }
 
 // grid = min(items, SMs x resident CTAs) CTAs of G groups, each group a contiguous range of items
-template <int DK, typename InT, bool kCommit>
+template <int DK, typename InT, int kMode>
 cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int NS = kChunkStages;
-    constexpr int G = chunk_groups<DK, kCommit, NS>();
-    using CS = ChunkPlan<DK, kCommit, NS>;
-    static_assert(CS::bytes(kChunkMaxT, G) <= kChunkMaxSmem, "shared memory of one group");
-    auto kernel = gdn_verify_chunked_kernel<DK, InT, kCommit, NS, G>;
-    const uint32_t smem = CS::bytes(p.T, G);
+    constexpr int G = chunk_groups<DK, kMode, NS>();
+    using CS = ChunkPlan<DK, kMode, NS>;
+    static_assert(CS::max_bytes(G) <= kChunkMaxSmem, "shared memory of one group");
+    auto kernel = gdn_verify_chunked_kernel<DK, InT, kMode, NS, G>;
+    const int Tv = kMode == kModeReplay ? 0 : p.T;
+    const int Tr = kMode == kModeVerify ? 0 : (kMode == kModeReplay ? p.T : p.rT);
+    const uint32_t smem = CS::bytes(Tr, Tv, G);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -894,23 +1012,24 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     // per-device attribute of the function, and occupancy may differ between devices.  A repeated first call
     // only repeats the same queries; devices beyond the table are queried on every call.
     static std::atomic<int> attr_bytes[kChunkCachedDevices];                 // bytes opened on each device
-    static std::atomic<int> occ_cache[kChunkCachedDevices][kChunkMaxT + 1];  // zero-initialised (static)
+    static std::atomic<int> occ_cache[kChunkCachedDevices][(kChunkMaxT + 1) * (kChunkMaxT + 1)];  // zero (static)
     const bool cached = dev >= 0 && dev < kChunkCachedDevices;
     if (!cached || (int)smem > attr_bytes[dev].load(std::memory_order_relaxed)) {
-        const int most = (int)CS::bytes(kChunkMaxT, G);
+        const int most = (int)CS::max_bytes(G);
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e != cudaSuccess) return e;
         if (cached) attr_bytes[dev].store(most, std::memory_order_relaxed);
     }
-    int occ = cached ? occ_cache[dev][p.T].load(std::memory_order_relaxed) : 0;
+    const int okey = Tr * (kChunkMaxT + 1) + Tv;
+    int occ = cached ? occ_cache[dev][okey].load(std::memory_order_relaxed) : 0;
     if (occ == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kChunkGroupThreads * G, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) return cudaErrorInvalidConfiguration;
-        if (cached) occ_cache[dev][p.T].store(occ, std::memory_order_relaxed);
+        if (cached) occ_cache[dev][okey].store(occ, std::memory_order_relaxed);
     }
     CUtensorMap map;
-    e = encode_pool_map<DK>(&map, kCommit ? p.pool_out : const_cast<void*>(p.pool_in), p);
+    e = encode_pool_map<DK>(&map, kMode == kModeVerify ? const_cast<void*>(p.pool_in) : p.pool_out, p);
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
     if (items > INT32_MAX) return cudaErrorInvalidValue;

@@ -99,7 +99,8 @@ class Workload:
     scale: float = 1.0
     l2_eps: float = 1e-6
     pool_seed: Optional[int] = None  # None: the pool is drawn from `seed`
-    commit_mode: str = "copy"        # "copy": from the cached states; "replay": re-run the accepted tokens
+    commit_mode: str = "copy"        # "copy": from the cached states; "replay": re-run the accepted tokens;
+    #                                  "fused": commit the previous step's accepted tokens inside this step's verify
 
     @property
     def n_padded(self) -> int:
@@ -200,6 +201,25 @@ def verify_t8_replay() -> Workload:
                                commit_mode="replay")
 
 
+def verify_t4_fused() -> Workload:
+    """verify_t4 as one-pass steps: each verify first commits the previous step's accepted prefix
+    (gdn_mtp_verify_commit); no intermediate states."""
+    return verify_t4().replace(name="mtp_verify_T4_B128_bf16state_fused_commit", cache=False, commit_mode="fused")
+
+
+def verify_t8_fused() -> Workload:
+    """verify_t8 as one-pass steps (gdn_mtp_verify_commit); no intermediate states."""
+    return verify_t8().replace(name="mtp_verify_T8_B256_pad10_bf16state_fused_commit", cache=False,
+                               commit_mode="fused")
+
+
+def previous_step(w: Workload) -> Dict[str, np.ndarray]:
+    """The earlier verify of a one-pass step on the same lanes: its k, v, a, b (draws of seed + 1, same shapes)
+    and accept lengths U{1..T} of its own stream."""
+    x = w.replace(seed=w.seed + 1).small_arrays()
+    return {k: x[k] for k in ("k", "v", "a", "b", "accept_len")}
+
+
 SWEEP_B = (1, 4, 16, 64, 128, 256)
 SWEEP_T = (1, 2, 4, 8)
 SWEEP_STATE = (F32, BF16)
@@ -238,8 +258,14 @@ def sweep_replay() -> List[Workload]:
     return pts
 
 
+def sweep_fused() -> List[Workload]:
+    """The one-pass step (gdn_mtp_verify_commit) over the grid of sweep_replay, same seeds and pool."""
+    return [w.replace(name=w.name.replace("sweep_replay", "sweep_fused"), commit_mode="fused") for w in sweep_replay()]
+
+
 NAMED = {"tiny": tiny, "decode": decode_t1, "verify4": verify_t4, "verify8": verify_t8,
-         "verify4_replay": verify_t4_replay, "verify8_replay": verify_t8_replay}
+         "verify4_replay": verify_t4_replay, "verify8_replay": verify_t8_replay,
+         "verify4_fused": verify_t4_fused, "verify8_fused": verify_t8_fused}
 
 
 # ---- prefill ------------------------------------------------------------------------------------------------

@@ -30,8 +30,9 @@
  *     accept_len              [B]                     int32
  *
  * Common rules.
- *   - Every pointer is DEVICE memory owned by the caller.  The library allocates nothing, keeps no state
- *     between calls besides launch-configuration caches (atomic, filled on first use), never synchronises,
+ *   - Every pointer is DEVICE memory owned by the caller, on the device that is current when the call is made
+ *     (the one `stream` belongs to).  The library allocates nothing, keeps no state between calls besides
+ *     launch-configuration caches (atomic, one entry per device, filled on first use), never synchronises,
  *     and enqueues its work asynchronously on `stream` (0 = legacy default stream).  Calls are thread-safe.
  *     A call with B == 0 (prefill: or no tokens; gated norm: rows == 0) enqueues nothing and returns GDN_OK.
  *   - Alignment: q, k, state_pool and intermediate_states start on 16 bytes; the other arrays on their
@@ -115,8 +116,8 @@ GDN_API gdn_status gdn_decode(const gdn_dims* dims, const void* q, const void* k
 /*
  * gdn_mtp_verify -- T draft tokens from state_pool[state_indices[b]] (read only: the pool is never
  * written).  If intermediate_states is not NULL, the state after token t is stored, rounded to
- * state_dtype, in intermediate_states[b, t].  Without intermediate_states, bf16 state and T <= 8, the
- * outputs come from the chunked form of the same recurrence (S_0 [k q] on the tensor cores, k and q split
+ * state_dtype, in intermediate_states[b, t].  Without intermediate_states, bf16 state, T <= 8 and DK >= 64,
+ * the outputs come from the chunked form of the same recurrence (S_0 [k q] on the tensor cores, k and q split
  * into bf16 hi + lo parts, about 16 significant bits), within fp32-level error of the token-by-token
  * outputs.  MTP verify through the pool API (initial_state_indices) of sglang PR #23273, Summary; bf16
  * state, T beyond 4 and intermediate caching from its Requirements (FlashInfer #2679).
@@ -155,6 +156,37 @@ GDN_API gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const 
                              const void* b, const float* A_log, const float* dt_bias, void* state_pool,
                              const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
                              gdn_stream_t stream);
+
+/* The tokens of an earlier gdn_mtp_verify call on the same lanes, whose accepted prefix gdn_mtp_verify_commit
+ * commits before it verifies: the compact recovery record of a speculative step (its k, v, a, b and accept
+ * lengths; q is not needed, the replay writes no outputs).  All device memory, layouts as in the header. */
+typedef struct gdn_replay_tokens {
+    int32_t T;                 /* tokens per lane of that call, 1 .. GDN_MAX_T */
+    const void* k;             /* [B, T, HK, DK] qkv_dtype, 16-byte aligned */
+    const void* v;             /* [B, T, HV, DV] qkv_dtype */
+    const void* a;             /* [B, T, HV] qkv_dtype */
+    const void* b;             /* [B, T, HV] qkv_dtype */
+    const int32_t* accept_len; /* [B] int32: lane b commits its first accept_len[b] tokens (0: none) */
+} gdn_replay_tokens;
+
+/*
+ * gdn_mtp_verify_commit -- one speculative step in one pass over the state pool: for every active lane, first
+ * the commit of the earlier call's accepted prefix, exactly gdn_commit_replay(prev) (the state after
+ * prev->accept_len[b] of prev's tokens written into state_pool[slot], rounded to state_dtype), then verify of
+ * this call's T tokens from the slot as just written, exactly gdn_mtp_verify without intermediate states (o).
+ * dims describes this call (dims->T tokens); prev->T may differ from it (the draft width may change between
+ * steps).  With a bf16 pool, both token counts <= 8 and DK >= 64, one kernel reads each state once and writes it
+ * once; otherwise the two calls run back to back.  An accept length outside 0 .. prev->T sets
+ * GDN_ERRBIT_ACCEPT_LEN and commits nothing for that lane (its verify still runs from the slot as it is).  The
+ * in-kernel commit of TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), "Moved out of this PR" (commits
+ * in-kernel below 16 decode requests), fed by the compact GDN recovery records of the issue "Proposal: native
+ * BF16 MTP speculative decoding for dense Qwen3.8-27B".
+ */
+GDN_API gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q,
+                                         const void* k, const void* v, const void* a, const void* b,
+                                         const float* A_log, const float* dt_bias, void* state_pool,
+                                         const int32_t* state_indices, void* o, int32_t* err_word,
+                                         gdn_stream_t stream);
 
 /*
  * gdn_prefill -- prefill of B variable-length sequences packed along one token axis of N = dims->T tokens

@@ -322,3 +322,34 @@ def test_binding_rejects_a_stream_of_another_gpu():
     with pytest.raises(ValueError, match="stream is on cuda:1"):
         gdn.gdn_mtp_verify(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"], x["pool"], x["idx"],
                            x["o"], None, stream=_FakeStream("cuda:1"))
+
+
+# ---- gdn_mtp_verify_commit: the earlier call's tokens are checked like the others ---------------------------
+def verify_commit(L, d, prev_T=4, prev=True, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, o=P, err=None, pk=P, pv=P, pa=P, pb=P, acc=P)
+    a.update(ptrs)
+    rt = gdn._ReplayTokensC(prev_T, a["pk"], a["pv"], a["pa"], a["pb"], a["acc"])
+    return L.gdn_mtp_verify_commit(ctypes.byref(d) if d is not None else None, ctypes.byref(rt) if prev else None,
+                                   a["q"], a["k"], a["v"], a["a"], a["b"], a["A_log"], a["dt_bias"], a["pool"],
+                                   a["idx"], a["o"], a["err"], None)
+
+
+@pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "pk", "pv", "pa",
+                                 "pb", "acc"])
+def test_verify_commit_null_pointer(L, ptr):
+    assert verify_commit(L, dims(), **{ptr: None}) == 1
+
+
+def test_verify_commit_checks(L):
+    assert verify_commit(L, None) == 1
+    assert verify_commit(L, dims(), prev=False) == 1
+    assert verify_commit(L, dims(), prev_T=0) == 2
+    assert verify_commit(L, dims(), prev_T=17) == 2
+    assert verify_commit(L, dims(T=0)) == 2
+    assert verify_commit(L, dims(DK=48)) == 5
+    assert verify_commit(L, dims(), pk=ODD) == 4          # the earlier k starts on 16 bytes
+    assert verify_commit(L, dims(), acc=ODD) == 4
+    assert verify_commit(L, dims(qkv_dtype=0), pv=ctypes.c_void_p(0x10002)) == 4  # fp32 v on 2 bytes
+    z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "pk", "pv", "pa", "pb",
+                           "acc")}
+    assert verify_commit(L, dims(B=0), **z) == 0

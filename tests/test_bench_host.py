@@ -215,3 +215,16 @@ def test_roofline_block_reports_both_peaks():
     r = bench.roofline_block(k, 6790.0, "measured (x)", None)
     assert abs(r["frac"] - 6400 / 6790) < 1e-12 and abs(r["frac_nominal"] - 0.8) < 1e-12
     assert r["nominal_peak"] == 8000.0 and r["peak"] == 6790.0 and "of measured" in r["peak_source"]
+
+
+def test_fused_step_bytes_and_kernel():
+    w = W.verify_t4_fused()
+    state = 128 * 32 * 128 * 128 * 2
+    per_tok = 2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 2
+    prev_tok = 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 2
+    assert bench.fused_bytes(w, 128, 300) == 2 * state + 128 * 4 * per_tok + 300 * prev_tok + 32 * 8 + 2 * 128 * 4
+    assert bench.kernel_name(w, "verify_commit", 152) == "gdn_verify_chunked_kernel"
+    assert bench.kernel_name(w.replace(state_dtype="f32"), "verify_commit", 152).count("gdn_recurrent_kernel") == 2
+    p = W.previous_step(w)
+    assert p["k"].shape == (128, 4, 16, 128) and p["accept_len"].min() >= 1 and p["accept_len"].max() <= 4
+    assert not (p["k"] == w.small_arrays()["k"]).all()  # its own draws
