@@ -26,17 +26,17 @@ struct RecurrentParams {
     void* o;               // nullptr: no outputs (replay commit)
     void* cache;           // nullptr: no intermediate states
     int32_t* err;    // nullable
-    // replay commit + verify: the earlier call's tokens to commit first (rT per lane; steps[b] of them), with
-    // q .. b above the tokens to verify; nullptr / 0 otherwise
-    const void* rk;
-    const void* rv;
-    const void* ra;
-    const void* rb;
-    int rT;
     int T, HK, HV, DV, num_slots;
     int out_bf16;
     int v_vec;  // v starts on 16 bytes and DV * sizeof(v) % 16 == 0: v is read in 16-byte chunks
     float scale, l2_eps;
+    // replay commit + verify: the earlier call's tokens to commit first (rT per lane; steps[b] of them), with
+    // q .. b above the tokens to verify; nullptr / 0 otherwise
+    int rT;
+    const void* rk;
+    const void* rv;
+    const void* ra;
+    const void* rb;
 };
 
 struct CommitParams {

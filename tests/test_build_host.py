@@ -17,8 +17,9 @@ TIMED = [
     ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li16E", 4),   # verify T=4
     ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li32E", 0),   # bf16 T <= 2
     ("gdn_recurrent_bf16.cu", "gdn_recurrent_kernelILi128E13__nv_bfloat16S1_E", 0),               # verify T=8
-    ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Lb0E", 0),          # verify, no cache
-    ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Lb1E", 0),          # replay commit
+    ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li0E", 0),          # verify, no cache
+    ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li1E", 0),          # replay commit
+    ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li2E", 0),          # one-pass step
     ("gdn_recurrent_f32.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16fLi16E", 0),       # decode fp32
     ("gdn_prefill.cu", "gdn_prefill_kernelILi128E13__nv_bfloat16S1_E", 0),                        # prefill
     ("gdn_gated_norm.cu", "gdn_gated_rmsnorm_reg_kernel", 0),                                    # gated norm
