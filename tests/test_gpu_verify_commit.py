@@ -89,6 +89,10 @@ def run_two_calls(w, x, xp, t, tp):
     return o, pool
 
 
+def bits(a: np.ndarray) -> np.ndarray:
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
 def one_pass(w, Tp) -> bool:
     return w.state_dtype == "bf16" and w.T <= 8 and Tp <= 8 and w.DK >= 64
 
@@ -145,8 +149,9 @@ def test_verify_commit_against_the_oracle_and_the_two_calls(w, Tp, zero):
     check_step(w, Tp, x, xp, o_h, pool_h)
     o2, pool2 = run_two_calls(w, x, xp, t, tp)
     torch.cuda.synchronize()
-    assert np.array_equal(host(o2), o_h), "o differs from gdn_commit_replay + gdn_mtp_verify"
-    assert np.array_equal(host(pool2), pool_h), "the pool differs from gdn_commit_replay + gdn_mtp_verify"
+    # bit patterns: the padded lanes hold NaN canaries
+    assert np.array_equal(bits(host(o2)), bits(o_h)), "o differs from gdn_commit_replay + gdn_mtp_verify"
+    assert np.array_equal(bits(host(pool2)), bits(pool_h)), "the pool differs from gdn_commit_replay + gdn_mtp_verify"
 
 
 @pytest.mark.parametrize("w", [W.verify_t4(), W.verify_t8()], ids=lambda w: w.name)
