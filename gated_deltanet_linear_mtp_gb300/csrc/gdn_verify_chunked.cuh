@@ -994,15 +994,11 @@ constexpr int chunk_groups() {
 }
 
 // grid = min(items, SMs x resident CTAs) CTAs of G groups, each group a contiguous range of items
-template <int DK, typename InT, int kMode>
-cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
+template <int DK, typename InT, int kMode, int G>
+cudaError_t launch_chunked_groups(const RecurrentParams& p, int B, int Tr, int Tv, cudaStream_t s) {
     constexpr int NS = kChunkStages;
-    constexpr int G = chunk_groups<DK, kMode, NS>();
     using CS = ChunkPlan<DK, kMode, NS>;
-    static_assert(CS::max_bytes(G) <= kChunkMaxSmem, "shared memory of one group");
     auto kernel = gdn_verify_chunked_kernel<DK, InT, kMode, NS, G>;
-    const int Tv = kMode == kModeReplay ? 0 : p.T;
-    const int Tr = kMode == kModeVerify ? 0 : (kMode == kModeReplay ? p.T : p.rT);
     const uint32_t smem = CS::bytes(Tr, Tv, G);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1015,7 +1011,7 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     static std::atomic<int> occ_cache[kChunkCachedDevices][(kChunkMaxT + 1) * (kChunkMaxT + 1)];  // zero (static)
     const bool cached = dev >= 0 && dev < kChunkCachedDevices;
     if (!cached || (int)smem > attr_bytes[dev].load(std::memory_order_relaxed)) {
-        const int most = (int)CS::max_bytes(G);
+        const int most = (int)std::min<uint32_t>(CS::max_bytes(G), kChunkMaxSmem);
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e != cudaSuccess) return e;
         if (cached) attr_bytes[dev].store(most, std::memory_order_relaxed);
@@ -1038,6 +1034,23 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     const int per_cta = (int)((items + vctas - 1) / vctas);
     kernel<<<(int)ctas, kChunkGroupThreads * G, smem, s>>>(p, map, (int)items, per_cta);
     return cudaGetLastError();
+}
+
+// The group count: as many as the largest token counts of the mode allow; the one-pass mode, which holds both
+// token sets' rows, takes one group more when its actual token counts leave room for it.
+template <int DK, typename InT, int kMode>
+cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
+    constexpr int NS = kChunkStages;
+    constexpr int G = chunk_groups<DK, kMode, NS>();
+    using CS = ChunkPlan<DK, kMode, NS>;
+    static_assert(CS::max_bytes(G) <= kChunkMaxSmem, "shared memory of one group");
+    const int Tv = kMode == kModeReplay ? 0 : p.T;
+    const int Tr = kMode == kModeVerify ? 0 : (kMode == kModeReplay ? p.T : p.rT);
+    if constexpr (kMode == kModeReplayVerify && G < kChunkMaxGroups && (G + 1) * CS::tmem_cols() <= 512) {
+        if (CS::bytes(Tr, Tv, G + 1) <= kChunkMaxSmem)
+            return launch_chunked_groups<DK, InT, kMode, G + 1>(p, B, Tr, Tv, s);
+    }
+    return launch_chunked_groups<DK, InT, kMode, G>(p, B, Tr, Tv, s);
 }
 
 }  // namespace gdn
