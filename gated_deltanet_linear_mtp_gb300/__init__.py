@@ -8,7 +8,10 @@ library has not been built, every call raises.
     gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
     gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
     gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, ...)
-    gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, ...)
+    gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None,
+                          norm=None, ...)
+    gdn_mtp_verify_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, norm,
+                         intermediate_states=None, err_word=None, ...)
     gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o,
                 has_initial_state=None, err_word=None, ...)
     gdn_gated_rmsnorm(o, z, norm_weight, y=None, eps=1e-6)
@@ -28,6 +31,7 @@ from typing import Optional
 from .build import LIB_PATH
 
 __all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "ReplayTokens",
+           "gdn_mtp_verify_gated", "GatedNorm",
            "gdn_prefill", "gdn_gated_rmsnorm", "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
            "ERRBIT_SEQLEN", "MAX_T", "EXPORTS"]
 
@@ -39,7 +43,8 @@ ERRBIT_TIMEOUT = 4
 ERRBIT_SEQLEN = 8
 MAX_T = 16
 F32, BF16 = 0, 1
-EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "gdn_prefill",
+EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit",
+           "gdn_mtp_verify_gated", "gdn_prefill",
            "gdn_gated_rmsnorm", "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
 
 
@@ -61,6 +66,19 @@ class ReplayTokens:
 
     def __init__(self, k, v, a, b, accept_len):
         self.k, self.v, self.a, self.b, self.accept_len = k, v, a, b, accept_len
+
+
+class _GatedNormC(ctypes.Structure):
+    _fields_ = [("z", ctypes.c_void_p), ("z_dtype", ctypes.c_int32), ("norm_weight", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("y", ctypes.c_void_p)]
+
+
+class GatedNorm:
+    """The gated RMSNorm of a verify's outputs into ``y``: ``z`` (the gate, o's shape, fp32 or bf16),
+    ``norm_weight`` ``[DV]`` fp32, ``y`` (o's shape and dtype; may be o itself)."""
+
+    def __init__(self, z, norm_weight, y, eps=1e-6):
+        self.z, self.norm_weight, self.y, self.eps = z, norm_weight, y, eps
 
 
 class GdnError(RuntimeError):
@@ -88,12 +106,14 @@ def lib() -> ctypes.CDLL:
         L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
         L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
         L.gdn_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip, ip, vp]
-        L.gdn_mtp_verify_commit.argtypes = [dp, ctypes.POINTER(_ReplayTokensC)] + [vp] * 5 + [vp, vp, vp, ip, vp, ip, vp]
+        L.gdn_mtp_verify_commit.argtypes = ([dp, ctypes.POINTER(_ReplayTokensC)] + [vp] * 5 +
+                                            [vp, vp, vp, ip, vp, ctypes.POINTER(_GatedNormC), ip, vp])
+        L.gdn_mtp_verify_gated.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ctypes.POINTER(_GatedNormC), ip, vp]
         L.gdn_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp, ip, vp]
         L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
                                         ctypes.c_float, vp, vp]
         for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_mtp_verify_commit,
-                  L.gdn_prefill, L.gdn_gated_rmsnorm):
+                  L.gdn_mtp_verify_gated, L.gdn_prefill, L.gdn_gated_rmsnorm):
             f.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -296,8 +316,50 @@ def gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
             "gdn_commit_replay")
 
 
+def _norm_c(norm, o):
+    """The C record of a GatedNorm for outputs o (checked: shapes, dtypes)."""
+    import torch
+
+    if norm is None:
+        return None
+    _shape(norm.z, o.shape, "norm.z")
+    _shape(norm.y, o.shape, "norm.y")
+    _shape(norm.norm_weight, (o.shape[-1],), "norm.norm_weight")
+    if norm.y.dtype != o.dtype:
+        raise TypeError("norm.y must have o's dtype")
+    if norm.norm_weight.dtype != torch.float32:
+        raise TypeError("norm.norm_weight must be fp32")
+    return _GatedNormC(_dev(norm.z, "norm.z"), _code(norm.z, "norm.z"), _dev(norm.norm_weight, "norm.norm_weight"),
+                       float(norm.eps), _dev(norm.y, "norm.y"))
+
+
+def _norm_named(norm):
+    return [] if norm is None else [("norm.z", norm.z), ("norm.norm_weight", norm.norm_weight), ("norm.y", norm.y)]
+
+
+def gdn_mtp_verify_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, norm, intermediate_states=None,
+                         err_word=None, *, scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """``gdn_mtp_verify`` (o, optional intermediate states) and the gated RMSNorm of o into ``norm.y``
+    (``norm``: a GatedNorm), inside the verify kernel where one item holds a whole head."""
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
+    if intermediate_states is not None:
+        _shape(intermediate_states, (d.B, d.T, d.HV, d.DV, d.DK), "intermediate_states")
+        if intermediate_states.dtype != state_pool.dtype:
+            raise TypeError("intermediate_states must have state_pool's dtype")
+    nc = _norm_c(norm, o)
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("o", o), ("intermediate_states", intermediate_states), ("err_word", err_word)]
+                            + _norm_named(norm))
+    _launch(device, stream, L.gdn_mtp_verify_gated,
+            (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+             _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(intermediate_states, "intermediate_states"),
+             ctypes.byref(nc), _dev(err_word, "err_word")), "gdn_mtp_verify_gated")
+
+
 def gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, *,
-                          scale=1.0, l2_eps=1e-6, stream=None) -> None:
+                          norm=None, scale=1.0, l2_eps=1e-6, stream=None) -> None:
     """One speculative step in one pass: commit ``prev``'s accepted prefix (``prev``: a ``ReplayTokens``, exactly
     ``gdn_commit_replay`` of those tokens) into the slots, then verify these T tokens from the committed states
     (exactly ``gdn_mtp_verify`` without intermediate states).  ``prev`` may have another token count."""
@@ -318,15 +380,18 @@ def gdn_mtp_verify_commit(prev, q, k, v, a, b, A_log, dt_bias, state_pool, state
             raise TypeError(f"{n} must have q's dtype")
     if prev.accept_len.dtype != torch.int32:
         raise TypeError("prev.accept_len must be int32")
+    nc = _norm_c(norm, o)
     device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
                             + [("o", o), ("err_word", err_word), ("prev.k", prev.k), ("prev.v", prev.v),
-                               ("prev.a", prev.a), ("prev.b", prev.b), ("prev.accept_len", prev.accept_len)])
+                               ("prev.a", prev.a), ("prev.b", prev.b), ("prev.accept_len", prev.accept_len)]
+                            + _norm_named(norm))
     rt = _ReplayTokensC(Tp, _dev(prev.k, "prev.k"), _dev(prev.v, "prev.v"), _dev(prev.a, "prev.a"),
                         _dev(prev.b, "prev.b"), _dev(prev.accept_len, "prev.accept_len"))
     _launch(device, stream, L.gdn_mtp_verify_commit,
             (ctypes.byref(d), ctypes.byref(rt), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"),
              _dev(b, "b"), _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
-             _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word")),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), ctypes.byref(nc) if nc is not None else None,
+             _dev(err_word, "err_word")),
             "gdn_mtp_verify_commit")
 
 

@@ -109,6 +109,102 @@ gdn_status run_recurrent(const gdn_dims* d, const void* q, const void* k, const 
     return finish(launch_recurrent_bf16state(p, d->B, d->DK, qkv_bf16, stream));
 }
 
+// The gated norm of a verify's outputs: its record checked; `fused` is set when the chunked kernel applies it
+// (a bf16 pool without intermediate states, the kernel's range, DV <= 128: one item holds a whole head).
+gdn_status check_norm(const gdn_dims* d, const gdn_gated_norm_out* n, const void* o) {
+    if (n == nullptr) return GDN_OK;
+    if (!n->z || !n->norm_weight || !n->y) return GDN_ERR_NULL;
+    if (!valid_dtype(n->z_dtype)) return GDN_ERR_DTYPE;
+    if (!std::isfinite(n->eps) || n->eps < 0.f) return GDN_ERR_VALUE;
+    if (!aligned(n->z, dtype_bytes(n->z_dtype)) || !aligned(n->y, dtype_bytes(d->out_dtype)) ||
+        !aligned(n->norm_weight, 4))
+        return GDN_ERR_ALIGN;
+    (void)o;
+    return GDN_OK;
+}
+
+bool norm_fused(const gdn_dims* d, bool cache) {
+    return d->state_dtype == GDN_BF16 && !cache && d->DV <= 128 &&
+           chunked_verify_eligible(d->B, d->T, d->DK, d->DV, d->HV, d->num_slots);
+}
+
+void set_norm(RecurrentParams& p, const gdn_gated_norm_out* n) {
+    p.nz = n->z;
+    p.nz_bf16 = n->z_dtype == GDN_BF16;
+    p.nw = n->norm_weight;
+    p.ny = n->y;
+    p.neps = n->eps;
+}
+
+// the standalone norm of the stored o, rows of padded or invalid lanes left untouched
+gdn_status run_norm(const gdn_dims* d, const gdn_gated_norm_out* n, const void* o, const int32_t* idx,
+                    cudaStream_t st) {
+    GatedNormParams g{};
+    g.o = o;
+    g.z = n->z;
+    g.w = n->norm_weight;
+    g.y = n->y;
+    g.rows = (int64_t)d->B * d->T * d->HV;
+    g.DV = d->DV;
+    g.o_bf16 = d->out_dtype == GDN_BF16;
+    g.z_bf16 = n->z_dtype == GDN_BF16;
+    g.vec = d->DV % 8 == 0 && aligned(o, 16) && aligned(n->z, 16) && aligned(n->y, 16) && aligned(n->norm_weight, 16);
+    g.eps = n->eps;
+    g.lane_slot = idx;
+    g.rows_per_lane = (int64_t)d->T * d->HV;
+    g.num_slots = d->num_slots;
+    return finish(launch_gated_norm(g, st));
+}
+
+gdn_status verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q, const void* k,
+                         const void* v, const void* a, const void* b, const float* A_log, const float* dt_bias,
+                         void* state_pool, const int32_t* state_indices, void* o, const gdn_gated_norm_out* norm,
+                         int32_t* err_word, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (prev == nullptr) return GDN_ERR_NULL;
+    if (prev->T < 1 || prev->T > GDN_MAX_T) return GDN_ERR_SHAPE;
+    gdn_dims pd = *dims;  // the earlier call's shape: its own token count
+    pd.T = prev->T;
+    s = check_dims(&pd, true);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    // the earlier tokens have the layouts of k, v, a, b (no q: the replay writes no outputs)
+    s = check_io(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_indices, nullptr,
+                 err_word, false);
+    if (s != GDN_OK) return s;
+    if (!prev->accept_len) return GDN_ERR_NULL;
+    if (!aligned(prev->accept_len, 4)) return GDN_ERR_ALIGN;
+    s = check_norm(dims, norm, o);
+    if (s != GDN_OK) return s;
+    if (norm && (double)dims->B * dims->T * dims->HV > (double)gated_norm_max_rows()) return GDN_ERR_SHAPE;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dims->state_dtype == GDN_BF16 && (norm == nullptr || norm_fused(dims, false))) {
+        RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices,
+                                        prev->accept_len, o, nullptr, err_word);
+        p.rk = prev->k;
+        p.rv = prev->v;
+        p.ra = prev->a;
+        p.rb = prev->b;
+        p.rT = prev->T;
+        if (norm) set_norm(p, norm);
+        cudaError_t e = cudaSuccess;
+        if (launch_replay_verify_bf16state(p, dims->B, dims->DK, dims->qkv_dtype == GDN_BF16, st, e)) return finish(e);
+    }
+    // outside the one-pass kernel's range: the same two steps as two launches, the replay commit (q is not read
+    // for outputs; the earlier k stands in for it) and then the verify from the committed slots
+    s = run_recurrent(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_pool,
+                      state_indices, prev->accept_len, nullptr, nullptr, err_word, st);
+    if (s != GDN_OK) return s;
+    if (norm == nullptr)
+        return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o,
+                             nullptr, err_word, st);
+    return gdn_mtp_verify_gated(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, nullptr, norm,
+                                err_word, stream);
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -179,46 +275,38 @@ gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const void* k,
                          nullptr, nullptr, err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
-gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q, const void* k,
-                                 const void* v, const void* a, const void* b, const float* A_log, const float* dt_bias,
-                                 void* state_pool, const int32_t* state_indices, void* o, int32_t* err_word,
-                                 gdn_stream_t stream) {
+gdn_status gdn_mtp_verify_gated(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                                const void* b, const float* A_log, const float* dt_bias, const void* state_pool,
+                                const int32_t* state_indices, void* o, void* intermediate_states,
+                                const gdn_gated_norm_out* norm, int32_t* err_word, gdn_stream_t stream) {
     gdn_status s = check_dims(dims, true);
     if (s != GDN_OK) return s;
-    if (prev == nullptr) return GDN_ERR_NULL;
-    if (prev->T < 1 || prev->T > GDN_MAX_T) return GDN_ERR_SHAPE;
-    gdn_dims pd = *dims;  // the earlier call's shape: its own token count
-    pd.T = prev->T;
-    s = check_dims(&pd, true);
+    if (norm == nullptr) return GDN_ERR_NULL;
+    s = check_norm(dims, norm, o);
     if (s != GDN_OK) return s;
     if (dims->B == 0) return GDN_OK;
+    if ((double)dims->B * dims->T * dims->HV > (double)gated_norm_max_rows()) return GDN_ERR_SHAPE;
     s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
     if (s != GDN_OK) return s;
-    // the earlier tokens have the layouts of k, v, a, b (no q: the replay writes no outputs)
-    s = check_io(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_indices, nullptr,
-                 err_word, false);
-    if (s != GDN_OK) return s;
-    if (!prev->accept_len) return GDN_ERR_NULL;
-    if (!aligned(prev->accept_len, 4)) return GDN_ERR_ALIGN;
+    if (intermediate_states && !aligned(intermediate_states, 16)) return GDN_ERR_ALIGN;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dims->state_dtype == GDN_BF16) {
-        RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices,
-                                        prev->accept_len, o, nullptr, err_word);
-        p.rk = prev->k;
-        p.rv = prev->v;
-        p.ra = prev->a;
-        p.rb = prev->b;
-        p.rT = prev->T;
-        cudaError_t e = cudaSuccess;
-        if (launch_replay_verify_bf16state(p, dims->B, dims->DK, dims->qkv_dtype == GDN_BF16, st, e)) return finish(e);
-    }
-    // outside the one-pass kernel's range: the same two steps as two launches, the replay commit (q is not read
-    // for outputs; the earlier k stands in for it) and then the verify from the committed slots
-    s = run_recurrent(&pd, prev->k, prev->k, prev->v, prev->a, prev->b, A_log, dt_bias, state_pool, state_pool,
-                      state_indices, prev->accept_len, nullptr, nullptr, err_word, st);
-    if (s != GDN_OK) return s;
-    return run_recurrent(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o, nullptr,
-                         err_word, st);
+    RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o,
+                                    intermediate_states, err_word);
+    const bool fused = norm_fused(dims, intermediate_states != nullptr);
+    if (fused) set_norm(p, norm);
+    const bool qkv_bf16 = dims->qkv_dtype == GDN_BF16;
+    s = finish(dims->state_dtype == GDN_F32 ? launch_recurrent_f32state(p, dims->B, dims->DK, qkv_bf16, st)
+                                            : launch_recurrent_bf16state(p, dims->B, dims->DK, qkv_bf16, st));
+    if (s != GDN_OK || fused) return s;
+    return run_norm(dims, norm, o, state_indices, st);
+}
+
+gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q, const void* k,
+                                 const void* v, const void* a, const void* b, const float* A_log, const float* dt_bias,
+                                 void* state_pool, const int32_t* state_indices, void* o,
+                                 const gdn_gated_norm_out* norm, int32_t* err_word, gdn_stream_t stream) {
+    return verify_commit(dims, prev, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, norm, err_word,
+                         stream);
 }
 
 gdn_status gdn_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,
@@ -249,7 +337,7 @@ gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t DV, int32_t o_dtype, int32_t 
     if (!o || !z || !norm_weight || !y) return GDN_ERR_NULL;
     const uintptr_t osz = dtype_bytes(o_dtype), zsz = dtype_bytes(z_dtype);
     if (!aligned(o, osz) || !aligned(y, osz) || !aligned(z, zsz) || !aligned(norm_weight, 4)) return GDN_ERR_ALIGN;
-    GatedNormParams p;
+    GatedNormParams p{};
     p.o = o;
     p.z = z;
     p.w = norm_weight;

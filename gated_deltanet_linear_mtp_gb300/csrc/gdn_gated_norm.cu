@@ -60,12 +60,20 @@ __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 constexpr int kNormThreads = 256;
 
 // Rows of at most 8 * GS * NCH columns (DV % 8 == 0, 16-byte aligned): everything from registers.
+// A row of a padded or invalid lane (when the call names the lanes' slots): left untouched.
+__device__ __forceinline__ bool skipped_row(const GatedNormParams& q, int64_t row) {
+    if (q.lane_slot == nullptr) return false;
+    const int s = q.lane_slot[row / q.rows_per_lane];
+    return s < 0 || s >= q.num_slots;
+}
+
 template <typename OT, typename ZT, int GS, int NCH>
 __global__ void __launch_bounds__(kNormThreads) gdn_gated_rmsnorm_reg_kernel(const OT* o, const ZT* z, const float* w,
-                                                                             OT* y, int64_t rows, int DV, float eps) {
+                                                                             OT* y, int64_t rows, int DV, float eps,
+                                                                             const GatedNormParams q) {
     const int64_t row = ((int64_t)blockIdx.x * kNormThreads + threadIdx.x) / GS;
     const int gl = threadIdx.x % GS;
-    if (row >= rows) return;  // whole groups leave together: a group shares its row
+    if (row >= rows || skipped_row(q, row)) return;  // whole groups leave together: a group shares its row
     const unsigned mask = GS == 32 ? 0xffffffffu : (((1u << GS) - 1u) << ((threadIdx.x & 31) & ~(GS - 1)));
     const OT* orow = o + row * DV;
     const ZT* zrow = z + row * DV;
@@ -103,10 +111,11 @@ __global__ void __launch_bounds__(kNormThreads) gdn_gated_rmsnorm_reg_kernel(con
 // Any row: a loop over 8-column chunks (kVec) or single columns, re-reading o for y.
 template <typename OT, typename ZT, int GS, bool kVec>
 __global__ void __launch_bounds__(kNormThreads) gdn_gated_rmsnorm_kernel(const OT* o, const ZT* z, const float* w,
-                                                                         OT* y, int64_t rows, int DV, float eps) {
+                                                                         OT* y, int64_t rows, int DV, float eps,
+                                                                         const GatedNormParams q) {
     const int64_t row = ((int64_t)blockIdx.x * kNormThreads + threadIdx.x) / GS;
     const int gl = threadIdx.x % GS;
-    if (row >= rows) return;  // whole groups leave together: a group shares its row
+    if (row >= rows || skipped_row(q, row)) return;  // whole groups leave together: a group shares its row
     const unsigned mask = GS == 32 ? 0xffffffffu : (((1u << GS) - 1u) << ((threadIdx.x & 31) & ~(GS - 1)));
     const OT* orow = o + row * DV;
     const ZT* zrow = z + row * DV;
@@ -148,7 +157,7 @@ cudaError_t launch_norm_gs(const GatedNormParams& p, cudaStream_t s) {
     const int64_t threads = p.rows * GS;
     const int64_t blocks = (threads + kNormThreads - 1) / kNormThreads;
     gdn_gated_rmsnorm_kernel<OT, ZT, GS, kVec><<<(unsigned)blocks, kNormThreads, 0, s>>>(
-        static_cast<const OT*>(p.o), static_cast<const ZT*>(p.z), p.w, static_cast<OT*>(p.y), p.rows, p.DV, p.eps);
+        static_cast<const OT*>(p.o), static_cast<const ZT*>(p.z), p.w, static_cast<OT*>(p.y), p.rows, p.DV, p.eps, p);
     return cudaGetLastError();
 }
 
@@ -157,7 +166,7 @@ cudaError_t launch_norm_reg(const GatedNormParams& p, cudaStream_t s) {
     const int64_t threads = p.rows * GS;
     const int64_t blocks = (threads + kNormThreads - 1) / kNormThreads;
     gdn_gated_rmsnorm_reg_kernel<OT, ZT, GS, NCH><<<(unsigned)blocks, kNormThreads, 0, s>>>(
-        static_cast<const OT*>(p.o), static_cast<const ZT*>(p.z), p.w, static_cast<OT*>(p.y), p.rows, p.DV, p.eps);
+        static_cast<const OT*>(p.o), static_cast<const ZT*>(p.z), p.w, static_cast<OT*>(p.y), p.rows, p.DV, p.eps, p);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,13 @@ struct RecurrentParams {
     const void* rv;
     const void* ra;
     const void* rb;
+    // gated RMSNorm of the stored o (chunked verify with DV <= 128): y = o / sqrt(mean(o^2) + neps) * nw * silu(nz)
+    // per (token, head) row of DV, y in o's type; nz == nullptr: none
+    const void* nz;
+    const float* nw;
+    void* ny;
+    float neps;
+    int nz_bf16;
 };
 
 struct CommitParams {
@@ -59,9 +66,17 @@ struct GatedNormParams {
     int o_bf16, z_bf16;
     int vec;  // DV % 8 == 0 and o, z, y, w start on 16 bytes: 8 columns per access
     float eps;
+    // rows of padded or invalid lanes left untouched: row r belongs to lane r / rows_per_lane, skipped when
+    // lane_slot[lane] is outside 0 .. num_slots - 1; nullptr: every row
+    const int32_t* lane_slot;
+    int64_t rows_per_lane;
+    int num_slots;
 };
 
 cudaError_t launch_recurrent_f32state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
+// A verify without intermediate states on a bf16 pool runs the chunked tensor-core kernel (which can also apply
+// the gated norm when DV <= 128) when this holds.
+bool chunked_verify_eligible(int B, int T, int DK, int DV, int HV, int num_slots);
 cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
 // Replay commit of p.rk .. p.rb (p.rT tokens per lane, p.steps[b] of them) and then verify of p.q .. p.b (p.T
 // tokens) in one pass of the chunked kernel; false (nothing launched) when the call is outside that kernel's

@@ -26,6 +26,14 @@
 
 namespace gdn {
 
+// The chunked kernel takes T <= 8 tokens and DK >= 64; it addresses num_slots * HV heads with a signed 32-bit
+// TMA coordinate and counts its items in int.  Beyond these, the token-by-token kernels serve the call.
+inline bool chunked_range(int B, int T, int DK, int DV, int HV, int num_slots) {
+    const uint64_t heads = (uint64_t)num_slots * (uint64_t)HV;
+    const uint64_t items = (uint64_t)B * HV * (((uint64_t)DV + kChunkRows - 1) / kChunkRows);
+    return T >= 1 && T <= kChunkMaxT && DK >= kChunkMinDK && heads <= INT32_MAX && items <= INT32_MAX;
+}
+
 constexpr int kStagedMaxTokenBytes = 8;  // T * sizeof(state element) at or below which staging pays
 constexpr int kStagedMinCtasPerSm = 2;
 
@@ -67,11 +75,7 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     if constexpr (std::is_same<StT, __nv_bfloat16>::value && DK >= kChunkMinDK) {
         const bool verify_only = p.cache == nullptr && p.pool_out == nullptr && p.steps == nullptr;
         const bool replay_commit = p.cache == nullptr && p.pool_out != nullptr && p.steps != nullptr && p.o == nullptr;
-        // the chunked kernel addresses num_slots * HV heads with a signed 32-bit TMA coordinate and counts its
-        // items in int; beyond either range, the token-by-token kernels below serve the call
-        const uint64_t heads = (uint64_t)p.num_slots * (uint64_t)p.HV;
-        const uint64_t items = (uint64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
-        if ((verify_only || replay_commit) && p.T <= kChunkMaxT && heads <= INT32_MAX && items <= INT32_MAX)
+        if ((verify_only || replay_commit) && chunked_range(B, p.T, DK, p.DV, p.HV, p.num_slots))
             return replay_commit ? launch_chunked<DK, InT, kModeReplay>(p, B, s)
                                  : launch_chunked<DK, InT, kModeVerify>(p, B, s);
     }
@@ -95,9 +99,8 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
 template <typename InT, int DK>
 bool launch_replay_verify_dk(const RecurrentParams& p, int B, cudaStream_t s, cudaError_t& err) {
     if constexpr (DK >= kChunkMinDK) {
-        const uint64_t heads = (uint64_t)p.num_slots * (uint64_t)p.HV;
-        const uint64_t items = (uint64_t)B * p.HV * ((p.DV + kChunkRows - 1) / kChunkRows);
-        if (p.T <= kChunkMaxT && p.rT >= 1 && p.rT <= kChunkMaxT && heads <= INT32_MAX && items <= INT32_MAX) {
+        if (chunked_range(B, p.T, DK, p.DV, p.HV, p.num_slots) && p.T <= kFusedMaxT && p.rT >= 1 &&
+            p.rT <= kFusedMaxT) {
             err = launch_chunked<DK, InT, kModeReplayVerify>(p, B, s);
             return true;
         }

@@ -56,6 +56,9 @@ constexpr int kChunkMaxT = 8;
 constexpr int kChunkMinDK = 64;  // rows of 64 bf16 at least: whole 128-byte swizzle spans
 constexpr uint32_t kChunkWaitPolls = GDN_WAIT_POLLS;
 constexpr int kChunkMaxGroups = 3;
+// the one-pass mode (replay commit + verify) holds both token sets: it takes at most 4 tokens in each, where three
+// groups fit; with more, the two calls measured faster as separate launches of three groups each
+constexpr int kFusedMaxT = 4;
 
 // The chunked kernel's modes: verify only, replay commit only, and replay commit then verify in one pass.
 enum ChunkMode { kModeVerify = 0, kModeReplay = 1, kModeReplayVerify = 2 };
@@ -94,15 +97,21 @@ struct ChunkPlan {
     __host__ __device__ static constexpr uint32_t ctl_off(int Tr, int Tv) {
         return gram_off(Tr, Tv) + 4u * (uint32_t)(Tr * tp(Tr) + 2 * Tv * tp(Tv));
     }
+    // verify with the gated norm: each warp's partial sums of squares, 8 tokens x 4 warps
+    __host__ __device__ static constexpr uint32_t red_off(int Tr, int Tv) {
+        return (ctl_off(Tr, Tv) + 8u * (NS + 1) + 8u + 8u * NS + 15u) & ~15u;
+    }
     __host__ __device__ static constexpr uint32_t group_bytes(int Tr, int Tv) {
-        return (ctl_off(Tr, Tv) + 8u * (NS + 1) + 8u + 8u * NS + 1023u) & ~1023u;
+        return (red_off(Tr, Tv) + (kVerify ? 4u * 4 * kChunkMaxT : 0u) + 1023u) & ~1023u;
     }
     __host__ __device__ static constexpr uint32_t bytes(int Tr, int Tv, int G) {
         return (uint32_t)G * group_bytes(Tr, Tv) + 16u + 1024u;  // + the tensor-memory address, + alignment slack
     }
-    // the largest plan: T = kChunkMaxT in each set the mode has
+    // tokens of a set at most: kChunkMaxT, kFusedMaxT in the one-pass mode
+    static constexpr int MAXT = kMode == kModeReplayVerify ? kFusedMaxT : kChunkMaxT;
+    // the largest plan: MAXT tokens in each set the mode has
     __host__ __device__ static constexpr uint32_t max_bytes(int G) {
-        return bytes(kReplay ? kChunkMaxT : 0, kVerify ? kChunkMaxT : 0, G);
+        return bytes(kReplay ? MAXT : 0, kVerify ? MAXT : 0, G);
     }
     // tensor-memory columns of one group: P; in the replay modes also the product D (DK columns, P overlaps its
     // first ones), then the coefficients, two bf16 per column
@@ -287,12 +296,12 @@ __device__ __forceinline__ void load_row(const float* src, float (&dst)[N]) {
 
 // One row's T x T recurrence (T fixed at compile time, so delta stays in registers).  pr: the row of P,
 // [S_0 kh hi | S_0 kh lo | S_0 qh hi | S_0 qh lo]; v: the row's v per token; KKt, KQt: the transposed Gram
-// matrices, rows of TP = gram_stride(T) floats.
+// matrices, rows of TP = gram_stride(T) floats.  ost: the values stored into o (after rounding to its type).
 template <int T, int NP>
-__device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const float (&pr)[NP],
-                                               const float (&v)[kChunkMaxT], const float* gs, const float* bs,
+__device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const float (&pr)[NP], const float* v,
+                                               const float* gs, const float* bs,
                                                const float* KKt, const float* KQt, bool live, int64_t o0,
-                                               int64_t tok_out) {
+                                               int64_t tok_out, float (&ost)[T]) {
     constexpr int TP = (T + 3) & ~3;
     float g[T], be[T];
     load_row<T, false>(gs, g);
@@ -316,12 +325,14 @@ __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const f
         }
         delta[t] = be[t] * (v[t] - u);
         o = fmaf(kq[t], delta[t], o);
-        if (live) {
-            const float ov = p.scale * o;
-            if (p.out_bf16)
-                static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = __float2bfloat16_rn(ov);
-            else
-                static_cast<float*>(p.o)[o0 + t * tok_out] = ov;
+        const float ov = p.scale * o;
+        if (p.out_bf16) {
+            const __nv_bfloat16 ob = __float2bfloat16_rn(ov);
+            ost[t] = __bfloat162float(ob);
+            if (live) static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = ob;
+        } else {
+            ost[t] = ov;
+            if (live) static_cast<float*>(p.o)[o0 + t * tok_out] = ov;
         }
     }
 }
@@ -330,7 +341,7 @@ __device__ __forceinline__ void row_recurrence(const RecurrentParams& p, const f
 // A2 = [c hi | c hi | c lo | 0] in bf16 pairs (hi = c rounded, lo = c - hi rounded; element 2j in the low half),
 // to be multiplied by the B rows [kh hi; kh lo; kh hi].
 template <int T, int NP, int K2>
-__device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const float (&v)[kChunkMaxT], const float* gs,
+__device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const float* v, const float* gs,
                                                  const float* bs, const float* KKt, int L, uint32_t (&a2)[K2 / 2]) {
     constexpr int TP = (T + 3) & ~3;
     float delta[T];
@@ -378,12 +389,14 @@ __device__ __forceinline__ void row_coefficients(const float (&pr)[NP], const fl
 // current one, so every load has about one item of lead time and none is waited for by a register copy.
 template <int DK, typename InT, int kMode>
 struct ItemRegs {
+    static constexpr int MAXT = kMode == kModeReplayVerify ? kFusedMaxT : kChunkMaxT;
     static constexpr int VPASS = 4 * (32 / (DK / 8));  // vectors per pass of the group
-    static constexpr int NVEC = (kMode != kModeVerify ? kChunkMaxT : 0) + (kMode != kModeReplay ? 2 * kChunkMaxT : 0);
+    static constexpr int NVEC = (kMode != kModeVerify ? MAXT : 0) + (kMode != kModeReplay ? 2 * MAXT : 0);
     static constexpr int NPASS = (NVEC + VPASS - 1) / VPASS;
     uint4 raw[NPASS][Slice8<InT>::NC];
-    InT vr[kMode != kModeVerify ? kChunkMaxT : 1];
-    InT vv[kMode != kModeReplay ? kChunkMaxT : 1];
+    InT vr[kMode != kModeVerify ? MAXT : 1];
+    InT vv[kMode != kModeReplay ? MAXT : 1];
+    uint32_t vz[kMode != kModeReplay ? MAXT : 1];  // z of the gated norm, raw (fp32 bits, or bf16 bits)
     InT a, b;
     float A_log, dt_bias;
 };
@@ -428,7 +441,7 @@ __device__ __forceinline__ void gram_warp(uint32_t bbase, int BR, int T, int yb,
 // stage and the slot are left as they are).
 template <int T, int DK, typename InT, int kMode, int NS>
 __device__ __forceinline__ bool replay_rows(const CUtensorMap* tmap, uint32_t tmem, unsigned char* sm, uint32_t base,
-                                            uint32_t stage, const float (&v)[kChunkMaxT], const float* gs,
+                                            uint32_t stage, const float* v, const float* gs,
                                             const float* bs, const float* KK, int h, int HV, int row0, int slot, int L,
                                             int bar_id, uint32_t mma_bar, uint32_t& mphase) {
     using CS = ChunkPlan<DK, kMode, NS>;
@@ -505,12 +518,13 @@ __device__ __forceinline__ bool replay_rows(const CUtensorMap* tmap, uint32_t tm
 // Verify set, after its P MMA: every thread reads the P row of its state row from tensor memory and runs the
 // row's T x T recurrence, writing o.
 template <int T, int DK, typename InT, int kMode, int NS>
-__device__ __forceinline__ void verify_rows(const RecurrentParams& p, uint32_t tmem, const float (&v)[kChunkMaxT],
+__device__ __forceinline__ void verify_rows(const RecurrentParams& p, uint32_t tmem, const float* v,
+                                            const uint32_t* z, float wrow, float* red, int bar_id,
                                             const float* gs, const float* bs, const float* KK, const float* KQ, int b,
                                             int h, int row0, int nrows) {
     using CS = ChunkPlan<DK, kMode, NS>;
     constexpr int NP = CS::vrows(T);
-    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5;
+    const int tid = threadIdx.x & (kChunkGroupThreads - 1), warp = tid >> 5, lane = tid & 31;
     float pr[NP];
     tc_fence_after();
 #pragma unroll
@@ -518,7 +532,38 @@ __device__ __forceinline__ void verify_rows(const RecurrentParams& p, uint32_t t
     tmem_wait_ld();
     const bool live = tid < nrows;
     const int64_t o0 = ((int64_t)b * T * p.HV + h) * p.DV + row0 + tid;
-    row_recurrence<T, NP>(p, pr, v, gs, bs, KK, KQ, live, o0, (int64_t)p.HV * p.DV);
+    const int64_t tok_out = (int64_t)p.HV * p.DV;
+    float ost[T];
+    row_recurrence<T, NP>(p, pr, v, gs, bs, KK, KQ, live, o0, tok_out, ost);
+    if (p.nz != nullptr) {
+        // gated RMSNorm of the stored o over the DV rows of the head (this item holds all of them): sums of
+        // squares per token over the warp (shuffles), then over the 4 warps (shared memory), in one order for
+        // every thread
+        float ss[T];
+#pragma unroll
+        for (int t = 0; t < T; ++t) ss[t] = live ? ost[t] * ost[t] : 0.f;
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+            for (int t = 0; t < T; ++t) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], m);
+        if (lane == 0)
+#pragma unroll
+            for (int t = 0; t < T; ++t) red[warp * kChunkMaxT + t] = ss[t];
+        group_sync(bar_id);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            const float tot = (red[t] + red[kChunkMaxT + t]) + (red[2 * kChunkMaxT + t] + red[3 * kChunkMaxT + t]);
+            const float inv_rms = 1.f / sqrtf(tot / (float)p.DV + p.neps);
+            const float zt = p.nz_bf16 ? __uint_as_float(z[t] << 16) : __uint_as_float(z[t]);
+            const float y = ost[t] * inv_rms * wrow * (zt / (1.f + expf(-zt)));
+            if (live) {
+                if (p.out_bf16)
+                    static_cast<__nv_bfloat16*>(p.ny)[o0 + t * tok_out] = __float2bfloat16_rn(y);
+                else
+                    static_cast<float*>(p.ny)[o0 + t * tok_out] = y;
+            }
+        }
+    }
 }
 
 // A kernel that allocates tensor memory runs one CTA per SM, so the CTA holds G groups of 4 warps, each an
@@ -583,6 +628,9 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
     float* KKr = reinterpret_cast<float*>(sm + CS::gram_off(Tr, Tv));
     float* KKv = KKr + Tr * CS::tp(Tr);
     float* KQv = KKv + Tv * CS::tp(Tv);
+    float* red = reinterpret_cast<float*>(sm + CS::red_off(Tr, Tv));  // the gated norm's partial sums
+    // the gated norm's weight of this thread's row (the norm is fused only when one item holds a whole head)
+    const float wrow = (kVerify && p.nz != nullptr && tid < p.DV) ? p.nw[tid] : 0.f;
 
     // thread PT: start the tile of the item at `ip` (pool slot and token count loaded one issue earlier) into
     // stage s
@@ -642,17 +690,24 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         if constexpr (kReplay) {
             const InT* src = rv + ((int64_t)ip.b * Tr * p.HV + ip.h) * p.DV + row;
 #pragma unroll
-            for (int t = 0; t < kChunkMaxT; ++t) {
+            for (int t = 0; t < IR::MAXT; ++t) {
                 r.vr[t] = InT(0.f);
                 if (t < Tr && row < p.DV) r.vr[t] = src[(int64_t)t * p.HV * p.DV];
             }
         }
         if constexpr (kVerify) {
-            const InT* src = static_cast<const InT*>(p.v) + ((int64_t)ip.b * Tv * p.HV + ip.h) * p.DV + row;
+            const int64_t off = ((int64_t)ip.b * Tv * p.HV + ip.h) * p.DV + row;
+            const InT* src = static_cast<const InT*>(p.v) + off;
 #pragma unroll
-            for (int t = 0; t < kChunkMaxT; ++t) {
+            for (int t = 0; t < IR::MAXT; ++t) {
                 r.vv[t] = InT(0.f);
-                if (t < Tv && row < p.DV) r.vv[t] = src[(int64_t)t * p.HV * p.DV];
+                r.vz[t] = 0u;
+                if (t < Tv && row < p.DV) {
+                    r.vv[t] = src[(int64_t)t * p.HV * p.DV];
+                    if (p.nz != nullptr)
+                        r.vz[t] = p.nz_bf16 ? (uint32_t)static_cast<const uint16_t*>(p.nz)[off + (int64_t)t * p.HV * p.DV]
+                                            : static_cast<const uint32_t*>(p.nz)[off + (int64_t)t * p.HV * p.DV];
+                }
             }
         }
     };
@@ -854,11 +909,13 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
         // verify only: the stage is free as soon as its MMA has completed
         if (kEarly && tid == PT && nis < end) issue_next(st);
 
-        float vrr[kChunkMaxT], vrv[kChunkMaxT];
+        float vrr[IR::MAXT], vrv[IR::MAXT];
+        uint32_t zr[IR::MAXT];  // this item's z before the next item's loads replace it
 #pragma unroll
-        for (int t = 0; t < kChunkMaxT; ++t) {
+        for (int t = 0; t < IR::MAXT; ++t) {
             vrr[t] = kReplay ? to_f32(in.vr[kReplay ? t : 0]) : 0.f;
             vrv[t] = kVerify ? to_f32(in.vv[kVerify ? t : 0]) : 0.f;
+            zr[t] = kVerify ? in.vz[kVerify ? t : 0] : 0u;
         }
         if (it + 1 < end) load_v(npos, in);
         if (active) {
@@ -871,15 +928,16 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
 #define GDN_REPLAY_ROWS(TT)                                                                                      \
     ok = replay_rows<TT, DK, InT, kMode, NS>(&tmap, tmem, sm, base, stage, vrr, gr, br_, KKr, h, p.HV, row0, slot, L, \
                                              bar_id, mma_bar, mphase)
+                // token counts above MAXT never reach this kernel (the launcher's range)
                 switch (Tr) {
                 case 1: GDN_REPLAY_ROWS(1); break;
                 case 2: GDN_REPLAY_ROWS(2); break;
                 case 3: GDN_REPLAY_ROWS(3); break;
                 case 4: GDN_REPLAY_ROWS(4); break;
-                case 5: GDN_REPLAY_ROWS(5); break;
-                case 6: GDN_REPLAY_ROWS(6); break;
-                case 7: GDN_REPLAY_ROWS(7); break;
-                default: GDN_REPLAY_ROWS(8); break;
+                case 5: GDN_REPLAY_ROWS(IR::MAXT < 5 ? IR::MAXT : 5); break;
+                case 6: GDN_REPLAY_ROWS(IR::MAXT < 6 ? IR::MAXT : 6); break;
+                case 7: GDN_REPLAY_ROWS(IR::MAXT < 7 ? IR::MAXT : 7); break;
+                default: GDN_REPLAY_ROWS(IR::MAXT); break;
                 }
 #undef GDN_REPLAY_ROWS
                 if (kVerify && ok) {
@@ -905,16 +963,17 @@ __global__ void __launch_bounds__(kChunkGroupThreads * G, 1)
                 }
             }
             if constexpr (kVerify) if (ok) {
-#define GDN_VERIFY_ROWS(TT) verify_rows<TT, DK, InT, kMode, NS>(p, tmem, vrv, gv, bv_, KKv, KQv, b, h, row0, nrows)
+#define GDN_VERIFY_ROWS(TT) \
+    verify_rows<TT, DK, InT, kMode, NS>(p, tmem, vrv, zr, wrow, red, bar_id, gv, bv_, KKv, KQv, b, h, row0, nrows)
                 switch (Tv) {
                 case 1: GDN_VERIFY_ROWS(1); break;
                 case 2: GDN_VERIFY_ROWS(2); break;
                 case 3: GDN_VERIFY_ROWS(3); break;
                 case 4: GDN_VERIFY_ROWS(4); break;
-                case 5: GDN_VERIFY_ROWS(5); break;
-                case 6: GDN_VERIFY_ROWS(6); break;
-                case 7: GDN_VERIFY_ROWS(7); break;
-                default: GDN_VERIFY_ROWS(8); break;
+                case 5: GDN_VERIFY_ROWS(IR::MAXT < 5 ? IR::MAXT : 5); break;
+                case 6: GDN_VERIFY_ROWS(IR::MAXT < 6 ? IR::MAXT : 6); break;
+                case 7: GDN_VERIFY_ROWS(IR::MAXT < 7 ? IR::MAXT : 7); break;
+                default: GDN_VERIFY_ROWS(IR::MAXT); break;
                 }
 #undef GDN_VERIFY_ROWS
             }
@@ -1036,8 +1095,7 @@ cudaError_t launch_chunked_groups(const RecurrentParams& p, int B, int Tr, int T
     return cudaGetLastError();
 }
 
-// The group count: as many as the largest token counts of the mode allow; the one-pass mode, which holds both
-// token sets' rows, takes one group more when its actual token counts leave room for it.
+// The group count: as many as the largest token counts of the mode allow.
 template <int DK, typename InT, int kMode>
 cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int NS = kChunkStages;
@@ -1046,10 +1104,6 @@ cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
     static_assert(CS::max_bytes(G) <= kChunkMaxSmem, "shared memory of one group");
     const int Tv = kMode == kModeReplay ? 0 : p.T;
     const int Tr = kMode == kModeVerify ? 0 : (kMode == kModeReplay ? p.T : p.rT);
-    if constexpr (kMode == kModeReplayVerify && G < kChunkMaxGroups && (G + 1) * CS::tmem_cols() <= 512) {
-        if (CS::bytes(Tr, Tv, G + 1) <= kChunkMaxSmem)
-            return launch_chunked_groups<DK, InT, kMode, G + 1>(p, B, Tr, Tv, s);
-    }
     return launch_chunked_groups<DK, InT, kMode, G>(p, B, Tr, Tv, s);
 }
 

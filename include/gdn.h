@@ -157,6 +157,32 @@ GDN_API gdn_status gdn_commit_replay(const gdn_dims* dims, const void* q, const 
                              const int32_t* state_indices, const int32_t* accept_len, int32_t* err_word,
                              gdn_stream_t stream);
 
+/* The gated RMSNorm applied to a verify's outputs (gdn_mtp_verify_gated, gdn_mtp_verify_commit): exactly
+ * gdn_gated_rmsnorm of the o the call stores,
+ *     y[b,t,h,i] = o[b,t,h,i] / sqrt(mean_i(o[b,t,h,:]^2) + eps) * norm_weight[i] * silu(z[b,t,h,i]),
+ * computed in fp32 and stored in out_dtype; rows of padded lanes are left untouched.  Device memory. */
+typedef struct gdn_gated_norm_out {
+    const void* z;             /* [B, T, HV, DV] z_dtype: the gate projection */
+    int32_t z_dtype;           /* gdn_dtype of z */
+    const float* norm_weight;  /* [DV] fp32 */
+    float eps;                 /* finite, >= 0 */
+    void* y;                   /* [B, T, HV, DV] out_dtype; may be o itself (then o is replaced by y) */
+} gdn_gated_norm_out;
+
+/*
+ * gdn_mtp_verify_gated -- gdn_mtp_verify (o and, if given, intermediate_states, as that call writes them)
+ * followed by the gated RMSNorm of o into norm->y.  Without intermediate states, with a bf16 pool in the chunked
+ * kernel's range (T <= 8, DK >= 64) and DV <= 128, the norm runs inside the verify kernel (one item holds a whole
+ * head: the sum of squares is a reduction across its rows); otherwise gdn_gated_rmsnorm runs after it.  The
+ * decode-rows gated norm of TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), Per-File QA Perspective,
+ * Source files, fused into the recurrence's output.
+ */
+GDN_API gdn_status gdn_mtp_verify_gated(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                                        const void* a, const void* b, const float* A_log, const float* dt_bias,
+                                        const void* state_pool, const int32_t* state_indices, void* o,
+                                        void* intermediate_states, const gdn_gated_norm_out* norm, int32_t* err_word,
+                                        gdn_stream_t stream);
+
 /* The tokens of an earlier gdn_mtp_verify call on the same lanes, whose accepted prefix gdn_mtp_verify_commit
  * commits before it verifies: the compact recovery record of a speculative step (its k, v, a, b and accept
  * lengths; q is not needed, the replay writes no outputs).  All device memory, layouts as in the header. */
@@ -175,8 +201,9 @@ typedef struct gdn_replay_tokens {
  * prev->accept_len[b] of prev's tokens written into state_pool[slot], rounded to state_dtype), then verify of
  * this call's T tokens from the slot as just written, exactly gdn_mtp_verify without intermediate states (o).
  * dims describes this call (dims->T tokens); prev->T may differ from it (the draft width may change between
- * steps).  With a bf16 pool, both token counts <= 8 and DK >= 64, one kernel reads each state once and writes it
- * once; otherwise the two calls run back to back.  An accept length outside 0 .. prev->T sets
+ * steps).  With a bf16 pool, both token counts <= 4 and DK >= 64, one kernel reads each state once and writes it
+ * once; otherwise the two calls run back to back (with more tokens they measured faster as two launches).  With
+ * norm != NULL, the verify is gdn_mtp_verify_gated's (o and the gated norm into norm->y).  An accept length outside 0 .. prev->T sets
  * GDN_ERRBIT_ACCEPT_LEN and commits nothing for that lane (its verify still runs from the slot as it is).  The
  * in-kernel commit of TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), "Moved out of this PR" (commits
  * in-kernel below 16 decode requests), fed by the compact GDN recovery records of the issue "Proposal: native
@@ -185,8 +212,8 @@ typedef struct gdn_replay_tokens {
 GDN_API gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q,
                                          const void* k, const void* v, const void* a, const void* b,
                                          const float* A_log, const float* dt_bias, void* state_pool,
-                                         const int32_t* state_indices, void* o, int32_t* err_word,
-                                         gdn_stream_t stream);
+                                         const int32_t* state_indices, void* o, const gdn_gated_norm_out* norm,
+                                         int32_t* err_word, gdn_stream_t stream);
 
 /*
  * gdn_prefill -- prefill of B variable-length sequences packed along one token axis of N = dims->T tokens

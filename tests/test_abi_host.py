@@ -331,7 +331,7 @@ def verify_commit(L, d, prev_T=4, prev=True, **ptrs):
     rt = gdn._ReplayTokensC(prev_T, a["pk"], a["pv"], a["pa"], a["pb"], a["acc"])
     return L.gdn_mtp_verify_commit(ctypes.byref(d) if d is not None else None, ctypes.byref(rt) if prev else None,
                                    a["q"], a["k"], a["v"], a["a"], a["b"], a["A_log"], a["dt_bias"], a["pool"],
-                                   a["idx"], a["o"], a["err"], None)
+                                   a["idx"], a["o"], None, a["err"], None)
 
 
 @pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "pk", "pv", "pa",
@@ -353,3 +353,32 @@ def test_verify_commit_checks(L):
     z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "pk", "pv", "pa", "pb",
                            "acc")}
     assert verify_commit(L, dims(B=0), **z) == 0
+
+
+# ---- gdn_mtp_verify_gated: the verify's checks plus the norm record's ------------------------------------
+def verify_gated(L, d, norm=True, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, o=P, cache=None, err=None, z=P, w=P, y=P,
+             zd=1, eps=1e-6)
+    a.update(ptrs)
+    n = gdn._GatedNormC(a["z"], a["zd"], a["w"], a["eps"], a["y"])
+    return L.gdn_mtp_verify_gated(ctypes.byref(d) if d is not None else None, a["q"], a["k"], a["v"], a["a"], a["b"],
+                                  a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["o"], a["cache"],
+                                  ctypes.byref(n) if norm else None, a["err"], None)
+
+
+@pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "z", "w", "y"])
+def test_verify_gated_null_pointer(L, ptr):
+    assert verify_gated(L, dims(), **{ptr: None}) == 1
+
+
+def test_verify_gated_checks(L):
+    assert verify_gated(L, dims(), norm=False) == 1
+    assert verify_gated(L, dims(), zd=7) == 3
+    assert verify_gated(L, dims(), eps=-1.0) == 7
+    assert verify_gated(L, dims(), eps=float("nan")) == 7
+    assert verify_gated(L, dims(), y=ctypes.c_void_p(0x10001)) == 4  # bf16 y on an odd address
+    assert verify_gated(L, dims(), w=ctypes.c_void_p(0x10002)) == 4
+    assert verify_gated(L, dims(), zd=0, z=ctypes.c_void_p(0x10002)) == 4  # fp32 z on 2 bytes
+    assert verify_gated(L, dims(T=0)) == 2
+    z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o")}
+    assert verify_gated(L, dims(B=0), **z) == 0
