@@ -170,15 +170,21 @@ cudaError_t launch_norm_reg(const GatedNormParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// 8-column chunks a lane loads at once for rows of up to 32 chunks (more bytes in flight per thread)
+#ifndef GDN_NORM_LANE_CHUNKS
+#define GDN_NORM_LANE_CHUNKS 1
+#endif
+constexpr int kLaneChunks = GDN_NORM_LANE_CHUNKS;
+
 template <typename OT, typename ZT>
 cudaError_t launch_norm_t(const GatedNormParams& p, cudaStream_t s) {
     if (!p.vec) return launch_norm_gs<OT, ZT, 32, false>(p, s);
-    const int chunks = p.DV / 8;  // lanes per row: the chunks of a row, rounded up to a power of two, <= 32
-    if (chunks <= 1) return launch_norm_reg<OT, ZT, 1, 1>(p, s);
-    if (chunks <= 2) return launch_norm_reg<OT, ZT, 2, 1>(p, s);
-    if (chunks <= 4) return launch_norm_reg<OT, ZT, 4, 1>(p, s);
-    if (chunks <= 8) return launch_norm_reg<OT, ZT, 8, 1>(p, s);
-    if (chunks <= 16) return launch_norm_reg<OT, ZT, 16, 1>(p, s);
+    const int chunks = p.DV / 8;  // lanes per row: the chunks of a row over kLaneChunks, a power of two, <= 32
+    if (chunks <= kLaneChunks) return launch_norm_reg<OT, ZT, 1, kLaneChunks>(p, s);
+    if (chunks <= 2 * kLaneChunks) return launch_norm_reg<OT, ZT, 2, kLaneChunks>(p, s);
+    if (chunks <= 4 * kLaneChunks) return launch_norm_reg<OT, ZT, 4, kLaneChunks>(p, s);
+    if (chunks <= 8 * kLaneChunks) return launch_norm_reg<OT, ZT, 8, kLaneChunks>(p, s);
+    if (chunks <= 16 * kLaneChunks) return launch_norm_reg<OT, ZT, 16, kLaneChunks>(p, s);
     if (chunks <= 32) return launch_norm_reg<OT, ZT, 32, 1>(p, s);
     if (chunks <= 64) return launch_norm_reg<OT, ZT, 32, 2>(p, s);
     if (chunks <= 128) return launch_norm_reg<OT, ZT, 32, 4>(p, s);

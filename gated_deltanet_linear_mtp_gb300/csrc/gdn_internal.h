@@ -77,6 +77,7 @@ cudaError_t launch_recurrent_f32state(const RecurrentParams& p, int B, int DK, b
 // A verify without intermediate states on a bf16 pool runs the chunked tensor-core kernel (which can also apply
 // the gated norm when DV <= 128) when this holds.
 bool chunked_verify_eligible(int B, int T, int DK, int DV, int HV, int num_slots);
+constexpr int kChunkGroupsPerSm = 3;  // item pipelines of the chunked verify kernel per SM (DK <= 128)
 cudaError_t launch_recurrent_bf16state(const RecurrentParams& p, int B, int DK, bool qkv_bf16, cudaStream_t s);
 // Replay commit of p.rk .. p.rb (p.rT tokens per lane, p.steps[b] of them) and then verify of p.q .. p.b (p.T
 // tokens) in one pass of the chunked kernel; false (nothing launched) when the call is outside that kernel's
