@@ -88,6 +88,10 @@ cudaError_t launch_commit(const CommitParams& p, int B, cudaStream_t s);
 // prefill: p.T unused; the token axis has n_tokens entries, sequence b spans cu_seqlens[b] .. cu_seqlens[b+1]-1
 cudaError_t launch_prefill(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
                            int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s);
+// prefill in chunked form on the tensor cores (gdn_prefill_chunked.cu): DK = 64 or 128
+bool prefill_chunked_eligible(int DK);
+cudaError_t launch_prefill_chunked(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                                   int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s);
 cudaError_t launch_gated_norm(const GatedNormParams& p, cudaStream_t s);
 int64_t gated_norm_max_rows();
 

@@ -163,6 +163,10 @@ cudaError_t launch_prefill_t(const RecurrentParams& p, const int32_t* cu, const 
 
 cudaError_t launch_prefill(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
                            int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s) {
+#ifndef GDN_PREFILL_TOKEN_LOOP  // a comparison build keeps every DK on the token loop
+    if (prefill_chunked_eligible(DK))
+        return launch_prefill_chunked(p, cu_seqlens, has_init, B, n_tokens, DK, qkv_bf16, state_bf16, s);
+#endif
     if (state_bf16)
         return qkv_bf16 ? launch_prefill_t<__nv_bfloat16, __nv_bfloat16>(p, cu_seqlens, has_init, B, n_tokens, DK, s)
                         : launch_prefill_t<float, __nv_bfloat16>(p, cu_seqlens, has_init, B, n_tokens, DK, s);

@@ -1,0 +1,595 @@
+// gdn_prefill_chunked.cu -- prefill in chunked form on the tensor cores (sm_103a, tcgen05 with the state held in
+// tensor memory), for DK in {64, 128}.  The call's definition is the one of gdn_prefill.cu: sequence b owns tokens
+// cu_seqlens[b] .. cu_seqlens[b+1]-1, starts from its pool slot (or from zero when has_initial_state[b] == 0),
+// writes o at every token and its final state back into the slot.  The chunked gated delta rule with bf16 state
+// pools and the initial-state mask of TensorRT-LLM PR #20937 (Per-File QA Perspective, Source files and
+// Test-code files: the chunked prefill kernel and its fresh-state zeroing).
+//
+// Chunked form.  Within a chunk of C = 32 tokens t = 0 .. C-1 starting from state S_0, with
+// gamma_t = g_0 ... g_t, G(s,t) = g_{s+1} ... g_t (G(t,t) = 1) and delta_t = beta_t (v_t - g_t S_{t-1} kh_t),
+// the recurrence unrolls to (the same algebra as the chunked verify):
+//     u_t   = g_t S_{t-1} kh_t = gamma_t (S_0 kh_t) + sum_{s<t}  G(s,t) (kh_s . kh_t) delta_s,   delta_t = beta_t (v_t - u_t)
+//     o_t   = scale S_t qh_t   = scale (gamma_t (S_0 qh_t) + sum_{s<=t} G(s,t) (kh_s . qh_t) delta_s)
+//     S_C-1 = gamma_{C-1} S_0 + sum_s G(s, C-1) delta_s kh_s^T .
+// Per chunk the dense work is three products on the tensor cores, each in bf16 hi + lo parts (x = hi + lo, hi =
+// bf16(x), lo = bf16(x - hi): about 16 significant bits, and all four part products are taken, so the only error
+// besides fp32 accumulation is that of the split itself):
+//   Gram   [kh; qh] kh^T     (M = 128 rows of the stacked token buffer, N = C; A and B from shared memory),
+//   P      S_0 [kh; qh]^T    (M = 128 state rows, N = 4C; A = S_0 hi / lo written into tensor memory),
+//   update S += c kh         (M = 128, N = DK; A = c_s = G(s, C-1) delta_s hi / lo in tensor memory, B = the kh
+//                             rows read MN-major), onto gamma_{C-1} S_0 written in place beforehand;
+// what is left per state row is the C x C triangular recurrence above, in fp32 registers, one thread per row.
+// The state stays in fp32 in tensor memory for the whole sequence and is rounded to the pool's type once, at the
+// final write-back, like the token loop's registers.
+//
+// CTA = one item = (sequence, value head, block of 128 state rows); a kernel that allocates tensor memory runs one
+// CTA per SM.  Warps 0-3 (the row group, thread = state row = tensor-memory lane) run the state chain: S_0 into
+// hi / lo, the P product, the row recurrence and the o stores, the coefficients, the update product.  Warps 4-7
+// (the token group) prepare the next chunk meanwhile, into the other of two buffers: q, k normalised into the
+// stacked bf16 rows [kh hi | qh hi | kh lo | qh lo] (the 128-byte swizzled operand layout), v of the block's rows,
+// the gates and their prefix and suffix products, and the decay-weighted Gram matrices
+// KKw[t][s] = G(s,t) kh_s . kh_t (s < t) and KQw[t][s] = G(s,t) kh_s . qh_t (s <= t).  mbarriers hand the
+// buffers back and forth (every wait bounded: a wait that runs out sets GDN_ERRBIT_TIMEOUT and the CTA leaves).
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "gdn_tcgen05.cuh"
+
+#include <atomic>
+
+namespace gdn {
+namespace {
+
+constexpr int kPC = 32;          // tokens per chunk
+constexpr int kPRows = 128;      // state rows per item: the MMA's M, the tensor-memory lanes
+constexpr int kPThreads = 256;   // the row group (warps 0-3) and the token group (warps 4-7)
+constexpr int kBarRow = 1, kBarTok = 2;  // named barriers of the two groups (0 is the CTA's)
+constexpr uint32_t kPWaitPolls = GDN_WAIT_POLLS;
+constexpr uint32_t kPCols = 512;  // tensor memory of the CTA (a power of two covering the plan)
+
+template <int DK>
+struct PrefillChunkPlan {
+    static_assert(DK == 64 || DK == 128, "the chunked prefill takes DK = 64 or 128");
+    // shared memory, bytes from the 1024-byte aligned base: two stacked token buffers (128 rows x DK bf16 in
+    // 64-column boxes of 128 rows), two float buffers, the partial Gram rows, the mbarriers
+    static constexpr uint32_t BOX = 128u * 128u;
+    static constexpr uint32_t KQ_BYTES = 128u * DK * 2u;
+    static constexpr int KKW = 0, KQW = kPC * kPC, VB = 2 * kPC * kPC, GG = VB + kPC * kPRows, BET = GG + kPC,
+                         GAM = BET + kPC, CEND = GAM + kPC, F_FLOATS = CEND + kPC;
+    static constexpr int SCR_STRIDE = kPC + 1;  // partial Gram rows, padded against bank conflicts
+    static constexpr uint32_t F_OFF = 2u * KQ_BYTES;
+    static constexpr uint32_t SCR_OFF = F_OFF + 2u * F_FLOATS * 4u;
+    static constexpr uint32_t BAR_OFF = (SCR_OFF + 64u * SCR_STRIDE * 4u + 15u) & ~15u;
+    static constexpr uint32_t BYTES = BAR_OFF + 128u + 1024u;  // + the alignment slack of the base
+    // tensor-memory columns: S (fp32), S_0 hi and lo (bf16 pairs), P, the two Gram products, c hi and lo
+    static constexpr uint32_t S_COL = 0, SH_COL = DK, SL_COL = DK + DK / 2, P_COL = 2 * DK, G1_COL = P_COL + 4 * kPC,
+                              G2_COL = G1_COL + kPC, CH_COL = G2_COL + kPC, CL_COL = CH_COL + kPC / 2,
+                              COLS = CL_COL + kPC / 2;
+    static_assert(COLS <= kPCols, "tensor memory of the plan");
+};
+
+// mbarriers, 8 bytes each from the plan's BAR_OFF
+enum { kFull0 = 0, kFull1, kEmpty0, kEmpty1, kPBar, kUpdBar, kGramBar, kDrainRow, kDrainTok, kNumBars };
+
+template <typename T>
+__device__ __forceinline__ void load16(const T* src, float (&f)[16]);
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* src, float (&f)[16]) {
+    const uint4 a = reinterpret_cast<const uint4*>(src)[0], b = reinterpret_cast<const uint4*>(src)[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float2 x = bf16x2_to_float2(w[e]);
+        f[2 * e] = x.x;
+        f[2 * e + 1] = x.y;
+    }
+}
+template <>
+__device__ __forceinline__ void load16<float>(const float* src, float (&f)[16]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float4 x = reinterpret_cast<const float4*>(src)[e];
+        f[4 * e] = x.x;
+        f[4 * e + 1] = x.y;
+        f[4 * e + 2] = x.z;
+        f[4 * e + 3] = x.w;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(T* dst, const float (&f)[16]);
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float (&f)[16]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = bf16x2_bits(f[2 * e], f[2 * e + 1]);
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+template <>
+__device__ __forceinline__ void store16<float>(float* dst, const float (&f)[16]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        reinterpret_cast<float4*>(dst)[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+}
+
+// x = hi + lo in bf16 pairs (element 2e in the low half): hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<const uint32_t*>(&h2);
+    lo = bf16x2_bits(x0 - __low2float(h2), x1 - __high2float(h2));
+}
+
+template <int DK, typename InT, typename StT>
+__global__ void __launch_bounds__(kPThreads, 1)
+    gdn_prefill_chunked_kernel(const RecurrentParams p, const int32_t* __restrict__ cu_seqlens,
+                               const int32_t* __restrict__ has_init, int n_tokens) {
+    using PL = PrefillChunkPlan<DK>;
+    constexpr int C = kPC;
+    const int NRB = (p.DV + kPRows - 1) / kPRows;
+    const int item = blockIdx.x;  // row block fastest, then value head, then sequence
+    const int rb = item % NRB, h = (item / NRB) % p.HV, b = item / (NRB * p.HV);
+    const int hk = h / (p.HV / p.HK);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int lt = tid & (kPRows - 1);  // index in the group = tensor-memory lane
+    const bool row_group = tid < kPRows;
+    const int row = rb * kPRows + lt;   // row group: the state row; token group: the row of v it loads
+
+    // lane gather, then the sequence's bounds, checked like the token loop (index first)
+    const int slot = p.indices[b];
+    const bool reporter = p.err != nullptr && tid == 0 && rb == 0 && h == 0;  // once per sequence
+    if (slot < 0 || slot >= p.num_slots) {
+        if (slot != -1 && reporter) atomicOr(p.err, GDN_ERRBIT_INDEX);
+        return;
+    }
+    const int lo = cu_seqlens[b], hi = cu_seqlens[b + 1];
+    if (lo < 0 || hi < lo || hi > n_tokens) {
+        if (reporter) atomicOr(p.err, GDN_ERRBIT_SEQLEN);
+        return;
+    }
+    const int n = hi - lo;
+    if (n == 0) return;
+    const bool fresh = has_init != nullptr && has_init[b] == 0;
+    const int nch = (n + C - 1) / C;
+
+    extern __shared__ unsigned char pc_smem[];
+    const uint32_t raw_base = smem_u32(pc_smem);
+    const uint32_t pad = ((raw_base + 1023u) & ~1023u) - raw_base;
+    unsigned char* sm = pc_smem + pad;
+    const uint32_t base = raw_base + pad;
+    const uint32_t bars = base + PL::BAR_OFF;
+    auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+    volatile int* fail = reinterpret_cast<volatile int*>(sm + PL::BAR_OFF + 8 * kNumBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PL::BAR_OFF + 8 * kNumBars + 8);
+    float* scr = reinterpret_cast<float*>(sm + PL::SCR_OFF);
+
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kPCols);
+    if (tid == 0) {
+        mbar_init(bar(kFull0), kPRows);
+        mbar_init(bar(kFull1), kPRows);
+        for (int i = kEmpty0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    auto fbuf = [&](int buf) -> float* { return reinterpret_cast<float*>(sm + PL::F_OFF) + buf * PL::F_FLOATS; };
+    auto kq_addr = [&](int buf) -> uint32_t { return base + (uint32_t)buf * PL::KQ_BYTES; };
+
+    if (row_group) {
+        // ================================ row group: the state chain ================================
+        const bool live = row < p.DV;
+        bool issued = false;  // thread 0: an MMA was issued (drained before leaving)
+        // initial state: the pool row in fp32 tensor memory, zero for a fresh sequence
+        {
+            const StT* src = static_cast<const StT*>(p.pool_in) + (((int64_t)slot * p.HV + h) * p.DV + row) * DK;
+#pragma unroll
+            for (int c0 = 0; c0 < DK; c0 += 16) {
+                float f[16];
+                if (live && !fresh) {
+                    load16<StT>(src + c0, f);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) f[e] = 0.f;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(f[e]);
+                tmem_st8(lane_base + PL::S_COL + c0, w);
+                tmem_st8(lane_base + PL::S_COL + c0 + 8, w + 8);
+            }
+            tmem_wait_st();
+        }
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int buf = c & 1;
+            const float* F = fbuf(buf);
+            const uint32_t kq = kq_addr(buf);
+            bool w = mbar_wait_bounded(bar(kFull0 + buf), (uint32_t)(c >> 1) & 1u, kPWaitPolls);
+            if (w && c > 0) w = mbar_wait_bounded(bar(kUpdBar), (uint32_t)(c - 1) & 1u, kPWaitPolls);
+            if (named_sync_or(kBarRow, kPRows, !w || *fail != 0)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // S_0 -> bf16 hi / lo (the A operand of P), and gamma_{C-1} S_0 back in place for the update
+            const float gend = F[PL::GAM + C - 1];
+#pragma unroll
+            for (int c0 = 0; c0 < DK; c0 += 32) {
+                float f[32];
+                tmem_ld16(lane_base + PL::S_COL + c0, f);
+                tmem_ld16(lane_base + PL::S_COL + c0 + 16, f + 16);
+                tmem_wait_ld();
+                uint32_t hw[16], lw[16], sw[32];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) split_pair(f[2 * e], f[2 * e + 1], hw[e], lw[e]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sw[e] = __float_as_uint(gend * f[e]);
+                tmem_st8(lane_base + PL::SH_COL + c0 / 2, hw);
+                tmem_st8(lane_base + PL::SH_COL + c0 / 2 + 8, hw + 8);
+                tmem_st8(lane_base + PL::SL_COL + c0 / 2, lw);
+                tmem_st8(lane_base + PL::SL_COL + c0 / 2 + 8, lw + 8);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_st8(lane_base + PL::S_COL + c0 + 8 * j, sw + 8 * j);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_sync(kBarRow, kPRows);
+            // P = S_0 [kh hi | qh hi | kh lo | qh lo]^T, both parts of S_0 into one accumulator
+            if (lt == 0) {
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(kPRows, 4 * C);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < DK / 16; ++ks)
+                        umma_bf16_ta(tmem + PL::P_COL, tmem + (part ? PL::SL_COL : PL::SH_COL) + 8 * ks,
+                                     umma_desc_sw128(kq + (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u),
+                                     idesc, (part | ks) ? 1u : 0u);
+                umma_commit(bar(kPBar));
+                issued = true;
+            }
+            const bool pw = mbar_wait_bounded(bar(kPBar), (uint32_t)c & 1u, kPWaitPolls);
+            if (named_sync_or(kBarRow, kPRows, !pw)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // this row of P: S_0 kh_t = P[t] + P[2C + t], S_0 qh_t = P[C + t] + P[3C + t]
+            float pk[C], pq[C];
+            {
+                float x[C];
+                tmem_ld16(lane_base + PL::P_COL, pk);
+                tmem_ld16(lane_base + PL::P_COL + 16, pk + 16);
+                tmem_ld16(lane_base + PL::P_COL + 2 * C, x);
+                tmem_ld16(lane_base + PL::P_COL + 2 * C + 16, x + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < C; ++t) pk[t] += x[t];
+                tmem_ld16(lane_base + PL::P_COL + C, pq);
+                tmem_ld16(lane_base + PL::P_COL + C + 16, pq + 16);
+                tmem_ld16(lane_base + PL::P_COL + 3 * C, x);
+                tmem_ld16(lane_base + PL::P_COL + 3 * C + 16, x + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < C; ++t) pq[t] += x[t];
+            }
+            // the row's recurrence; KKw / KQw rows are zero beyond s < t / s <= t, and d[s] is zero until set
+            const float* KKw = F + PL::KKW;
+            const float* KQw = F + PL::KQW;
+            const int len = min(C, n - c * C);
+            const int64_t o0 = ((int64_t)(lo + c * C) * p.HV + h) * p.DV + row;
+            const int64_t tok_out = (int64_t)p.HV * p.DV;
+            float d[C];
+#pragma unroll
+            for (int t = 0; t < C; ++t) d[t] = 0.f;
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                const float gm = F[PL::GAM + t];
+                float u0 = gm * pk[t], u1 = 0.f;
+#pragma unroll
+                for (int s = 0; s < t; s += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(KKw + t * C + s);
+                    u0 = fmaf(a4.x, d[s], u0);
+                    u1 = fmaf(a4.y, d[s + 1], u1);
+                    u0 = fmaf(a4.z, d[s + 2], u0);
+                    u1 = fmaf(a4.w, d[s + 3], u1);
+                }
+                d[t] = F[PL::BET + t] * (F[PL::VB + t * kPRows + lt] - (u0 + u1));
+                float o0v = gm * pq[t], o1v = 0.f;
+#pragma unroll
+                for (int s = 0; s <= t; s += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(KQw + t * C + s);
+                    o0v = fmaf(a4.x, d[s], o0v);
+                    o1v = fmaf(a4.y, d[s + 1], o1v);
+                    o0v = fmaf(a4.z, d[s + 2], o0v);
+                    o1v = fmaf(a4.w, d[s + 3], o1v);
+                }
+                const float ov = p.scale * (o0v + o1v);
+                if (live && t < len) {
+                    if (p.out_bf16)
+                        static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = __float2bfloat16_rn(ov);
+                    else
+                        static_cast<float*>(p.o)[o0 + t * tok_out] = ov;
+                }
+            }
+            // coefficients c_s = G(s, C-1) delta_s in hi / lo, the A operand of the update
+            {
+                uint32_t chw[C / 2], clw[C / 2];
+#pragma unroll
+                for (int s = 0; s < C; s += 2)
+                    split_pair(F[PL::CEND + s] * d[s], F[PL::CEND + s + 1] * d[s + 1], chw[s / 2], clw[s / 2]);
+#pragma unroll
+                for (int j = 0; j < C / 2; j += 8) {
+                    tmem_st8(lane_base + PL::CH_COL + j, chw + j);
+                    tmem_st8(lane_base + PL::CL_COL + j, clw + j);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            named_sync(kBarRow, kPRows);  // every row's coefficients are in place; every read of buffer buf is done
+            // S += (c hi + c lo)(kh hi + kh lo): B = rows 0..C-1 (kh hi) and 2C..3C-1 (kh lo), read MN-major
+            if (lt == 0) {
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(kPRows, DK) | (1u << 16);
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int bh = 0; bh < 2; ++bh)
+#pragma unroll
+                        for (int ks = 0; ks < C / 16; ++ks) {
+                            const uint32_t brow = (uint32_t)(bh * 2 * C + 16 * ks);
+                            umma_bf16_ta(tmem + PL::S_COL, tmem + (a ? PL::CL_COL : PL::CH_COL) + 8 * ks,
+                                         umma_desc_sw128_mn(kq + brow * 128u, PL::BOX), idesc, 1u);
+                        }
+                umma_commit(bar(kUpdBar));
+                umma_commit(bar(kEmpty0 + buf));  // the token group may refill buffer buf
+            }
+        }
+        if (ok) {  // the final state into the slot, rounded to the pool's type
+            const bool uw = mbar_wait_bounded(bar(kUpdBar), (uint32_t)(nch - 1) & 1u, kPWaitPolls);
+            if (named_sync_or(kBarRow, kPRows, !uw)) {
+                ok = false;
+            } else {
+                tc_fence_after();
+                StT* dst = static_cast<StT*>(p.pool_out) + (((int64_t)slot * p.HV + h) * p.DV + row) * DK;
+#pragma unroll
+                for (int c0 = 0; c0 < DK; c0 += 16) {
+                    float f[16];
+                    tmem_ld16(lane_base + PL::S_COL + c0, f);
+                    tmem_wait_ld();
+                    if (live) store16<StT>(dst + c0, f);
+                }
+            }
+        }
+        if (!ok && lt == 0) {
+            *fail = 1;
+            if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+        }
+        if (lt == 0 && issued) {  // every MMA of this group has completed before the tensor memory is released
+            umma_commit(bar(kDrainRow));
+            mbar_wait_bounded(bar(kDrainRow), 0u, kPWaitPolls);
+        }
+    } else {
+        // ============================ token group: the next chunk's inputs ============================
+        using QK = Slice8<InT>;
+        constexpr int LPV = DK / 8;          // threads per q or k vector, 8 columns each
+        constexpr int VPP = kPRows / LPV;    // vectors per pass of the group
+        constexpr int NPASS = 2 * C / VPP;   // k_0 .. k_{C-1}, q_0 .. q_{C-1}
+        const int vj0 = lt / LPV, vc = lt % LPV;
+        const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+        const InT* qp = static_cast<const InT*>(p.q);
+        const InT* kp = static_cast<const InT*>(p.k);
+        const InT* vp = static_cast<const InT*>(p.v);
+        const InT* ap = static_cast<const InT*>(p.a);
+        const InT* bp = static_cast<const InT*>(p.b);
+        uint4 raw[NPASS][QK::NC];
+        InT vraw[C];
+        InT araw = InT(0.f), braw = InT(0.f);
+        auto load_chunk = [&](int c) {
+            const int t0 = c * C;
+#pragma unroll
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const int j = vj0 + ps * VPP;
+                const int t = j < C ? j : j - C;
+#pragma unroll
+                for (int e = 0; e < QK::NC; ++e) raw[ps][e] = make_uint4(0, 0, 0, 0);
+                if (t0 + t < n)
+                    QK::load_global((j < C ? kp : qp) + ((int64_t)(lo + t0 + t) * p.HK + hk) * DK + 8 * vc, raw[ps]);
+            }
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                vraw[t] = InT(0.f);
+                if (t0 + t < n && row < p.DV) vraw[t] = vp[((int64_t)(lo + t0 + t) * p.HV + h) * p.DV + row];
+            }
+            if (lt < C && t0 + lt < n) {
+                araw = ap[(int64_t)(lo + t0 + lt) * p.HV + h];
+                braw = bp[(int64_t)(lo + t0 + lt) * p.HV + h];
+            }
+        };
+        bool issued = false;
+        bool ok = true;
+        load_chunk(0);
+        for (int c = 0; c < nch; ++c) {
+            const int buf = c & 1;
+            float* F = fbuf(buf);
+            unsigned char* KQ = sm + (size_t)buf * PL::KQ_BYTES;
+            const uint32_t kq = kq_addr(buf);
+            // buffer buf is free once the update of chunk c - 2 (which read it last) has completed
+            const bool w = c < 2 || mbar_wait_bounded(bar(kEmpty0 + buf), (uint32_t)((c - 2) >> 1) & 1u, kPWaitPolls);
+            if (named_sync_or(kBarTok, kPRows, !w || *fail != 0)) {
+                ok = w;
+                break;
+            }
+            // gates (lane = token of the chunk), with gamma_t = g_0 .. g_t and G(s, C-1) = g_{s+1} .. g_{C-1}
+            if (lt < C) {
+                const bool valid = c * C + lt < n;  // tokens past the sequence: g = 1, beta = 0, zero q and k
+                const float g = valid ? gate(A_log, to_f32(araw), dt_bias) : 1.f;
+                const float be = valid ? sigmoid(to_f32(braw)) : 0.f;
+                float gm = g, sf = g;
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gm, m);
+                    if (lt >= m) gm *= y;
+                    const float z = __shfl_down_sync(0xffffffffu, sf, m);
+                    if (lt + m < 32) sf *= z;
+                }
+                float ce = __shfl_down_sync(0xffffffffu, sf, 1);
+                if (lt == C - 1) ce = 1.f;
+                F[PL::GG + lt] = g;
+                F[PL::BET + lt] = be;
+                F[PL::GAM + lt] = gm;
+                F[PL::CEND + lt] = ce;
+            }
+            // v of this thread's row, per token
+#pragma unroll
+            for (int t = 0; t < C; ++t) F[PL::VB + t * kPRows + lt] = to_f32(vraw[t]);
+            // q, k normalised, into the stacked rows: kh hi at t, qh hi at C + t, kh lo at 2C + t, qh lo at 3C + t
+#pragma unroll
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const int j = vj0 + ps * VPP;
+                float2 x[4];
+                QK::unpack(raw[ps], x);
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ss = fmaf(x[e].x, x[e].x, fmaf(x[e].y, x[e].y, ss));
+#pragma unroll
+                for (int m = 1; m < LPV; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                const int t = j < C ? j : j - C;
+                const float rn = c * C + t < n ? rsqrtf(ss + p.l2_eps) : 0.f;  // rows past the sequence: zero
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_pair(x[e].x * rn, x[e].y * rn, hw[e], lw[e]);
+                const int hrow = j;  // k_t: row t; q_t: row C + t (j = C + t)
+                *reinterpret_cast<uint4*>(KQ + sw128(kPRows, hrow, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(KQ + sw128(kPRows, hrow + 2 * C, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            fence_proxy_async_smem();  // the rows are read by the tensor cores
+            named_sync(kBarTok, kPRows);
+            // Gram products [kh; qh] kh hi^T and [kh; qh] kh lo^T over all four parts of the stacked rows
+            if (lt == 0) {
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(kPRows, C);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < DK / 16; ++ks) {
+                        const uint32_t koff = (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u;
+                        umma_bf16(tmem + (part ? PL::G2_COL : PL::G1_COL), umma_desc_sw128(kq + koff),
+                                  umma_desc_sw128(kq + (uint32_t)(part * 2 * C) * 128u + koff), idesc,
+                                  ks > 0 ? 1u : 0u);
+                    }
+                umma_commit(bar(kGramBar));
+                issued = true;
+            }
+            if (c + 1 < nch) load_chunk(c + 1);  // in flight meanwhile
+            const bool gw = mbar_wait_bounded(bar(kGramBar), (uint32_t)c & 1u, kPWaitPolls);
+            if (named_sync_or(kBarTok, kPRows, !gw)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // lane m of the products holds stacked row m against kh_s: rows 2C.. (the lo parts) hand their sums
+            // to rows 0..2C-1 through shared memory
+            float gr[C];
+            {
+                float x[C];
+                tmem_ld16(lane_base + PL::G1_COL, gr);
+                tmem_ld16(lane_base + PL::G1_COL + 16, gr + 16);
+                tmem_ld16(lane_base + PL::G2_COL, x);
+                tmem_ld16(lane_base + PL::G2_COL + 16, x + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int s = 0; s < C; ++s) gr[s] += x[s];
+            }
+            if (lt >= 2 * C) {
+#pragma unroll
+                for (int s = 0; s < C; ++s) scr[(lt - 2 * C) * PL::SCR_STRIDE + s] = gr[s];
+            }
+            tc_fence_before();
+            named_sync(kBarTok, kPRows);
+            if (lt < 2 * C) {
+                const int t = lt & (C - 1);
+                const bool isq = lt >= C;  // rows C..2C-1: qh_t . kh_s
+                float wv[C];
+                float G = 1.f;  // G(s, t), built downwards from s = t
+#pragma unroll
+                for (int s = C - 1; s >= 0; --s) {
+                    if (s < t) G *= F[PL::GG + s + 1];
+                    const float full = gr[s] + scr[lt * PL::SCR_STRIDE + s];
+                    wv[s] = (isq ? s <= t : s < t) ? G * full : 0.f;
+                }
+                float* dst = F + (isq ? PL::KQW : PL::KKW) + t * C;
+#pragma unroll
+                for (int s = 0; s < C; s += 4)
+                    *reinterpret_cast<float4*>(dst + s) = make_float4(wv[s], wv[s + 1], wv[s + 2], wv[s + 3]);
+            }
+            mbar_arrive(bar(kFull0 + buf));  // after this thread's writes of the chunk
+        }
+        if (!ok && lt == 0) {
+            *fail = 1;
+            if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+        }
+        if (lt == 0 && issued) {
+            umma_commit(bar(kDrainTok));
+            mbar_wait_bounded(bar(kDrainTok), 0u, kPWaitPolls);
+        }
+    }
+    // every tensor-memory access of both groups is complete before the allocation is released
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kPCols);
+}
+
+template <int DK, typename InT, typename StT>
+cudaError_t launch_dk(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                      int n_tokens, cudaStream_t s) {
+    using PL = PrefillChunkPlan<DK>;
+    auto kernel = gdn_prefill_chunked_kernel<DK, InT, StT>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // the shared-memory attribute is per device: set once for each
+    static std::atomic<uint64_t> ready{0};
+    if (dev < 64 && !(ready.load(std::memory_order_acquire) >> dev & 1u)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::BYTES);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(1ull << dev, std::memory_order_acq_rel);
+    } else if (dev >= 64) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::BYTES);
+        if (e != cudaSuccess) return e;
+    }
+    const int NRB = (p.DV + kPRows - 1) / kPRows;
+    const int64_t items = (int64_t)B * p.HV * NRB;
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
+    kernel<<<(unsigned)items, kPThreads, PL::BYTES, s>>>(p, cu_seqlens, has_init, n_tokens);
+    return cudaGetLastError();
+}
+
+template <typename InT, typename StT>
+cudaError_t launch_t(const RecurrentParams& p, const int32_t* cu, const int32_t* init, int B, int N, int DK,
+                     cudaStream_t s) {
+    switch (DK) {
+    case 64: return launch_dk<64, InT, StT>(p, cu, init, B, N, s);
+    case 128: return launch_dk<128, InT, StT>(p, cu, init, B, N, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool prefill_chunked_eligible(int DK) { return DK == 64 || DK == 128; }
+
+cudaError_t launch_prefill_chunked(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                                   int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s) {
+    if (state_bf16)
+        return qkv_bf16 ? launch_t<__nv_bfloat16, __nv_bfloat16>(p, cu_seqlens, has_init, B, n_tokens, DK, s)
+                        : launch_t<float, __nv_bfloat16>(p, cu_seqlens, has_init, B, n_tokens, DK, s);
+    return qkv_bf16 ? launch_t<__nv_bfloat16, float>(p, cu_seqlens, has_init, B, n_tokens, DK, s)
+                    : launch_t<float, float>(p, cu_seqlens, has_init, B, n_tokens, DK, s);
+}
+
+}  // namespace gdn
