@@ -35,6 +35,7 @@
 #include "gdn_tcgen05.cuh"
 
 #include <atomic>
+#include <cstring>
 
 namespace gdn {
 namespace {
@@ -53,17 +54,25 @@ struct PrefillChunkPlan {
     // 64-column boxes of 128 rows), two float buffers, the partial Gram rows, the mbarriers
     static constexpr uint32_t BOX = 128u * 128u;
     static constexpr uint32_t KQ_BYTES = 128u * DK * 2u;
-    static constexpr int KKW = 0, KQW = kPC * kPC, VB = 2 * kPC * kPC, GG = VB + kPC * kPRows, BET = GG + kPC,
-                         GAM = BET + kPC, CEND = GAM + kPC, F_FLOATS = CEND + kPC;
+    // KQw in bf16 hi then lo, the B operand of the O product: C rows of 128 bytes each (K = C of 64 columns used)
+    static constexpr uint32_t KQB_BYTES = 2u * kPC * 128u;
+    static constexpr uint32_t KQB_OFF = 2u * KQ_BYTES;
+    // float buffer: KKwT, v of the block's rows per token, g, beta, gamma, G(s, C-1)
+    static constexpr int KKW = 0, VB = kPC * kPC, GG = VB + kPC * kPRows, BET = GG + kPC, GAM = BET + kPC,
+                         CEND = GAM + kPC, F_FLOATS = CEND + kPC;
     static constexpr int SCR_STRIDE = kPC + 1;  // partial Gram rows, padded against bank conflicts
-    static constexpr uint32_t F_OFF = 2u * KQ_BYTES;
+    static constexpr uint32_t F_OFF = KQB_OFF + 2u * KQB_BYTES;
     static constexpr uint32_t SCR_OFF = F_OFF + 2u * F_FLOATS * 4u;
-    static constexpr uint32_t BAR_OFF = (SCR_OFF + 64u * SCR_STRIDE * 4u + 15u) & ~15u;
+    // two chunks of o staged for the bulk stores: [token][128 rows] in o's type (fp32 at most)
+    static constexpr uint32_t OB_BYTES = kPC * kPRows * 4u;
+    static constexpr uint32_t OB_OFF = (SCR_OFF + 64u * SCR_STRIDE * 4u + 1023u) & ~1023u;
+    static constexpr uint32_t BAR_OFF = OB_OFF + 2u * OB_BYTES;
     static constexpr uint32_t BYTES = BAR_OFF + 128u + 1024u;  // + the alignment slack of the base
-    // tensor-memory columns: S (fp32), S_0 hi and lo (bf16 pairs), P, the two Gram products, c hi and lo
+    // tensor-memory columns: S (fp32), S_0 hi and lo (bf16 pairs; delta hi and lo after the P product), P, the two
+    // Gram products, c hi and lo, O
     static constexpr uint32_t S_COL = 0, SH_COL = DK, SL_COL = DK + DK / 2, P_COL = 2 * DK, G1_COL = P_COL + 4 * kPC,
                               G2_COL = G1_COL + kPC, CH_COL = G2_COL + kPC, CL_COL = CH_COL + kPC / 2,
-                              COLS = CL_COL + kPC / 2;
+                              O_COL = CL_COL + kPC / 2, COLS = O_COL + kPC;
     static_assert(COLS <= kPCols, "tensor memory of the plan");
 };
 
@@ -122,7 +131,8 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 template <int DK, typename InT, typename StT>
 __global__ void __launch_bounds__(kPThreads, 1)
     gdn_prefill_chunked_kernel(const RecurrentParams p, const int32_t* __restrict__ cu_seqlens,
-                               const int32_t* __restrict__ has_init, int n_tokens) {
+                               const int32_t* __restrict__ has_init, int n_tokens,
+                               const __grid_constant__ CUtensorMap omap, int o_tma) {
     using PL = PrefillChunkPlan<DK>;
     constexpr int C = kPC;
     const int NRB = (p.DV + kPRows - 1) / kPRows;
@@ -202,6 +212,59 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             tmem_wait_st();
         }
+        // o: o_t = scale O_t, O = gamma_t S_0 qh_t + sum_s KQw[t][s] delta_s formed on the tensor cores in its own
+        // columns (read back in the next chunk while its P product runs); staged in shared memory and written by one
+        // TMA tensor store per whole chunk (o as [tokens][HV][DV], box 32 x 1 x 128), or by bulk copies of the
+        // block's rows per token, or, when o allows neither, stored directly
+        const uint32_t osz = p.out_bf16 ? 2u : 4u;
+        const bool o_bulk = (reinterpret_cast<uintptr_t>(p.o) & 15u) == 0 && ((int64_t)p.DV * osz) % 16 == 0;
+        const uint32_t blk_bytes = (uint32_t)min(kPRows, p.DV - rb * kPRows) * osz;
+        const int64_t tok_out = (int64_t)p.HV * p.DV;
+        auto emit_o = [&](int cc) {
+            float ov[C];
+            tmem_ld16(lane_base + PL::O_COL, ov);
+            tmem_ld16(lane_base + PL::O_COL + 16, ov + 16);
+            tmem_wait_ld();
+            if (o_bulk) {
+                unsigned char* ob = sm + PL::OB_OFF + (cc & 1) * PL::OB_BYTES;
+                if (p.out_bf16) {
+#pragma unroll
+                    for (int t = 0; t < C; ++t)
+                        reinterpret_cast<__nv_bfloat16*>(ob)[t * kPRows + lt] = __float2bfloat16_rn(p.scale * ov[t]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < C; ++t) reinterpret_cast<float*>(ob)[t * kPRows + lt] = p.scale * ov[t];
+                }
+                fence_proxy_async_smem();  // read by the bulk copies
+            } else if (live) {
+                const int len = min(C, n - cc * C);
+                const int64_t o0 = ((int64_t)(lo + cc * C) * p.HV + h) * p.DV + row;
+                if (p.out_bf16) {
+#pragma unroll
+                    for (int t = 0; t < C; ++t)
+                        if (t < len)
+                            static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = __float2bfloat16_rn(p.scale * ov[t]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < C; ++t)
+                        if (t < len) static_cast<float*>(p.o)[o0 + t * tok_out] = p.scale * ov[t];
+                }
+            }
+        };
+        constexpr int kOT = 96;  // the thread that issues and waits for the o copies (not the MMA issuer)
+        auto issue_o = [&](int cc) {  // thread kOT, after a barrier behind every row's emit_o(cc)
+            const int len = min(C, n - cc * C);
+            const uint32_t ob = base + PL::OB_OFF + (uint32_t)(cc & 1) * PL::OB_BYTES;
+            if (o_tma && len == C) {
+                tma_store_3d(&omap, rb * kPRows, h, lo + cc * C, ob);
+            } else {  // the sequence's last, partial chunk: the box would run into the next sequence
+                for (int t = 0; t < len; ++t)
+                    bulk_s2g(static_cast<unsigned char*>(p.o) +
+                                 (((int64_t)(lo + cc * C + t) * p.HV + h) * p.DV + rb * kPRows) * osz,
+                             ob + (uint32_t)t * kPRows * osz, blk_bytes);
+            }
+            bulk_commit_group();
+        };
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int buf = c & 1;
@@ -209,53 +272,75 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t kq = kq_addr(buf);
             bool w = mbar_wait_bounded(bar(kFull0 + buf), (uint32_t)(c >> 1) & 1u, kPWaitPolls);
             if (w && c > 0) w = mbar_wait_bounded(bar(kUpdBar), (uint32_t)(c - 1) & 1u, kPWaitPolls);
+            // the staging buffer of chunk c-1's o was last copied from for chunk c-3, two groups ago
+            if (lt == kOT && o_bulk && c >= 3) bulk_wait_read_but_one();
             if (named_sync_or(kBarRow, kPRows, !w || *fail != 0)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // S_0 -> bf16 hi / lo (the A operand of P), and gamma_{C-1} S_0 back in place for the update
+            // S_0 -> bf16 hi / lo (the A operand of P), and gamma_{C-1} S_0 back in place for the update, 32 columns
+            // at a time with the next block's load in flight
             const float gend = F[PL::GAM + C - 1];
-#pragma unroll
-            for (int c0 = 0; c0 < DK; c0 += 32) {
-                float f[32];
-                tmem_ld16(lane_base + PL::S_COL + c0, f);
-                tmem_ld16(lane_base + PL::S_COL + c0 + 16, f + 16);
+            {
+                float f[2][32];
+                tmem_ld16(lane_base + PL::S_COL, f[0]);
+                tmem_ld16(lane_base + PL::S_COL + 16, f[0] + 16);
                 tmem_wait_ld();
-                uint32_t hw[16], lw[16], sw[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) split_pair(f[2 * e], f[2 * e + 1], hw[e], lw[e]);
+                for (int jb = 0; jb < DK / 32; ++jb) {
+                    const int c0 = 32 * jb;
+                    float(&x)[32] = f[jb & 1];
+                    if (jb + 1 < DK / 32) {
+                        tmem_ld16(lane_base + PL::S_COL + c0 + 32, f[(jb + 1) & 1]);
+                        tmem_ld16(lane_base + PL::S_COL + c0 + 48, f[(jb + 1) & 1] + 16);
+                    }
+                    uint32_t hw[16], lw[16], sw[32];
+                    const float2 g2 = make_float2(gend, gend), m1 = make_float2(-1.f, -1.f);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sw[e] = __float_as_uint(gend * f[e]);
-                tmem_st8(lane_base + PL::SH_COL + c0 / 2, hw);
-                tmem_st8(lane_base + PL::SH_COL + c0 / 2 + 8, hw + 8);
-                tmem_st8(lane_base + PL::SL_COL + c0 / 2, lw);
-                tmem_st8(lane_base + PL::SL_COL + c0 / 2 + 8, lw + 8);
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 x2 = make_float2(x[2 * e], x[2 * e + 1]);
+                        const __nv_bfloat162 h2 = __float22bfloat162_rn(x2);
+                        hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        const float2 r2 = __ffma2_rn(bf16x2_to_float2(hw[e]), m1, x2);  // x - hi, exact
+                        lw[e] = bf16x2_bits(r2.x, r2.y);
+                        const float2 s2 = __fmul2_rn(g2, x2);
+                        sw[2 * e] = __float_as_uint(s2.x);
+                        sw[2 * e + 1] = __float_as_uint(s2.y);
+                    }
+                    tmem_st8(lane_base + PL::SH_COL + c0 / 2, hw);
+                    tmem_st8(lane_base + PL::SH_COL + c0 / 2 + 8, hw + 8);
+                    tmem_st8(lane_base + PL::SL_COL + c0 / 2, lw);
+                    tmem_st8(lane_base + PL::SL_COL + c0 / 2 + 8, lw + 8);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tmem_st8(lane_base + PL::S_COL + c0 + 8 * j, sw + 8 * j);
+                    for (int q = 0; q < 4; ++q) tmem_st8(lane_base + PL::S_COL + c0 + 8 * q, sw + 8 * q);
+                    if (jb + 1 < DK / 32) tmem_wait_ld();
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             named_sync(kBarRow, kPRows);
-            // P = S_0 [kh hi | qh hi | kh lo | qh lo]^T, both parts of S_0 into one accumulator
+            // P = S_0 [kh hi | qh hi | kh lo | qh lo]^T: S_0 hi against all 128 stacked rows, S_0 lo against the hi
+            // rows only (the lo.lo part, about 2^-18 relative, is left out); then chunk c-1's o to global memory
             if (lt == 0) {
                 tc_fence_after();
-                const uint32_t idesc = umma_idesc_bf16(kPRows, 4 * C);
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < DK / 16; ++ks)
-                        umma_bf16_ta(tmem + PL::P_COL, tmem + (part ? PL::SL_COL : PL::SH_COL) + 8 * ks,
-                                     umma_desc_sw128(kq + (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u),
-                                     idesc, (part | ks) ? 1u : 0u);
+                for (int ks = 0; ks < DK / 16; ++ks) {
+                    const uint64_t bd = umma_desc_sw128(kq + (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u);
+                    umma_bf16_ta(tmem + PL::P_COL, tmem + PL::SH_COL + 8 * ks, bd, umma_idesc_bf16(kPRows, 4 * C),
+                                 ks > 0 ? 1u : 0u);
+                    umma_bf16_ta(tmem + PL::P_COL, tmem + PL::SL_COL + 8 * ks, bd, umma_idesc_bf16(kPRows, 2 * C), 1u);
+                }
                 umma_commit(bar(kPBar));
                 issued = true;
             }
+            if (c > 0) emit_o(c - 1);  // while the P product runs
             const bool pw = mbar_wait_bounded(bar(kPBar), (uint32_t)c & 1u, kPWaitPolls);
             if (named_sync_or(kBarRow, kPRows, !pw)) {
                 ok = false;
                 break;
             }
+            if (lt == kOT && c > 0 && o_bulk) issue_o(c - 1);
             tc_fence_after();
             // this row of P: S_0 kh_t = P[t] + P[2C + t], S_0 qh_t = P[C + t] + P[3C + t]
             float pk[C], pq[C];
@@ -276,84 +361,89 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int t = 0; t < C; ++t) pq[t] += x[t];
             }
-            // the row's recurrence; KKw / KQw rows are zero beyond s < t / s <= t, and d[s] is zero until set
-            const float* KKw = F + PL::KKW;
-            const float* KQw = F + PL::KQW;
-            const int len = min(C, n - c * C);
-            const int64_t o0 = ((int64_t)(lo + c * C) * p.HV + h) * p.DV + row;
-            const int64_t tok_out = (int64_t)p.HV * p.DV;
-            float d[C];
-#pragma unroll
-            for (int t = 0; t < C; ++t) d[t] = 0.f;
+            // the row's u recurrence, right-looking: once delta_s is known it goes into u_t of every later token
+            // (KKwT[s][t] = KKw[t][s], zero for t <= s), so the dependent chain per token is a few operations and
+            // the rest are independent FMAs
+            const float* KKwT = F + PL::KKW;
+            uint32_t ow[C];  // gamma_t S_0 qh_t, the O product's starting value
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 const float gm = F[PL::GAM + t];
-                float u0 = gm * pk[t], u1 = 0.f;
+                pk[t] *= gm;
+                ow[t] = __float_as_uint(gm * pq[t]);
+            }
+            uint32_t dhw[C / 2], dlw[C / 2], chw[C / 2], clw[C / 2];
+            float dprev = 0.f, cprev = 0.f;
 #pragma unroll
-                for (int s = 0; s < t; s += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(KKw + t * C + s);
-                    u0 = fmaf(a4.x, d[s], u0);
-                    u1 = fmaf(a4.y, d[s + 1], u1);
-                    u0 = fmaf(a4.z, d[s + 2], u0);
-                    u1 = fmaf(a4.w, d[s + 3], u1);
-                }
-                d[t] = F[PL::BET + t] * (F[PL::VB + t * kPRows + lt] - (u0 + u1));
-                float o0v = gm * pq[t], o1v = 0.f;
+            for (int s = 0; s < C; ++s) {
+                const float ds = F[PL::BET + s] * (F[PL::VB + s * kPRows + lt] - pk[s]);
 #pragma unroll
-                for (int s = 0; s <= t; s += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(KQw + t * C + s);
-                    o0v = fmaf(a4.x, d[s], o0v);
-                    o1v = fmaf(a4.y, d[s + 1], o1v);
-                    o0v = fmaf(a4.z, d[s + 2], o0v);
-                    o1v = fmaf(a4.w, d[s + 3], o1v);
+                for (int t4 = (s + 1) & ~3; t4 < C; t4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(KKwT + s * C + t4);
+                    if (t4 > s) pk[t4] = fmaf(a4.x, ds, pk[t4]);
+                    if (t4 + 1 > s) pk[t4 + 1] = fmaf(a4.y, ds, pk[t4 + 1]);
+                    if (t4 + 2 > s) pk[t4 + 2] = fmaf(a4.z, ds, pk[t4 + 2]);
+                    if (t4 + 3 > s) pk[t4 + 3] = fmaf(a4.w, ds, pk[t4 + 3]);
                 }
-                const float ov = p.scale * (o0v + o1v);
-                if (live && t < len) {
-                    if (p.out_bf16)
-                        static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = __float2bfloat16_rn(ov);
-                    else
-                        static_cast<float*>(p.o)[o0 + t * tok_out] = ov;
+                // delta_s (the O product's A) and c_s = G(s, C-1) delta_s (the update's A) in hi / lo pairs
+                const float cs = F[PL::CEND + s] * ds;
+                if (s & 1) {
+                    split_pair(dprev, ds, dhw[s / 2], dlw[s / 2]);
+                    split_pair(cprev, cs, chw[s / 2], clw[s / 2]);
+                } else {
+                    dprev = ds;
+                    cprev = cs;
                 }
             }
-            // coefficients c_s = G(s, C-1) delta_s in hi / lo, the A operand of the update
-            {
-                uint32_t chw[C / 2], clw[C / 2];
 #pragma unroll
-                for (int s = 0; s < C; s += 2)
-                    split_pair(F[PL::CEND + s] * d[s], F[PL::CEND + s + 1] * d[s + 1], chw[s / 2], clw[s / 2]);
-#pragma unroll
-                for (int j = 0; j < C / 2; j += 8) {
-                    tmem_st8(lane_base + PL::CH_COL + j, chw + j);
-                    tmem_st8(lane_base + PL::CL_COL + j, clw + j);
-                }
-                tmem_wait_st();
+            for (int jj = 0; jj < C / 2; jj += 8) {
+                tmem_st8(lane_base + PL::SH_COL + jj, dhw + jj);
+                tmem_st8(lane_base + PL::SL_COL + jj, dlw + jj);
+                tmem_st8(lane_base + PL::CH_COL + jj, chw + jj);
+                tmem_st8(lane_base + PL::CL_COL + jj, clw + jj);
             }
+#pragma unroll
+            for (int jj = 0; jj < C; jj += 8) tmem_st8(lane_base + PL::O_COL + jj, ow + jj);
+            tmem_wait_st();
             tc_fence_before();
-            named_sync(kBarRow, kPRows);  // every row's coefficients are in place; every read of buffer buf is done
-            // S += (c hi + c lo)(kh hi + kh lo): B = rows 0..C-1 (kh hi) and 2C..3C-1 (kh lo), read MN-major
+            named_sync(kBarRow, kPRows);  // every row's operands are in place; every read of buffer buf is done
             if (lt == 0) {
                 tc_fence_after();
+                // O += (delta hi + delta lo)(KQw hi + KQw lo)^T without the lo.lo part: B = the C rows of KQw, K-major
+                const uint32_t kqb = base + PL::KQB_OFF + (uint32_t)buf * PL::KQB_BYTES;
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int bh = 0; bh < 2 - a; ++bh)
+#pragma unroll
+                        for (int ks = 0; ks < C / 16; ++ks)
+                            umma_bf16_ta(tmem + PL::O_COL, tmem + (a ? PL::SL_COL : PL::SH_COL) + 8 * ks,
+                                         umma_desc_sw128(kqb + (uint32_t)bh * (C * 128u) + 32u * ks),
+                                         umma_idesc_bf16(kPRows, C), 1u);
+                // S += c hi (kh hi + kh lo) + c lo kh hi: B = rows 0..C-1 (kh hi) and 2C..3C-1 (kh lo), MN-major
                 const uint32_t idesc = umma_idesc_bf16(kPRows, DK) | (1u << 16);
 #pragma unroll
                 for (int a = 0; a < 2; ++a)
 #pragma unroll
-                    for (int bh = 0; bh < 2; ++bh)
+                    for (int bh = 0; bh < 2 - a; ++bh)
 #pragma unroll
                         for (int ks = 0; ks < C / 16; ++ks) {
                             const uint32_t brow = (uint32_t)(bh * 2 * C + 16 * ks);
                             umma_bf16_ta(tmem + PL::S_COL, tmem + (a ? PL::CL_COL : PL::CH_COL) + 8 * ks,
                                          umma_desc_sw128_mn(kq + brow * 128u, PL::BOX), idesc, 1u);
                         }
-                umma_commit(bar(kUpdBar));
+                umma_commit(bar(kUpdBar));  // also tracks the O product issued before it
                 umma_commit(bar(kEmpty0 + buf));  // the token group may refill buffer buf
             }
         }
-        if (ok) {  // the final state into the slot, rounded to the pool's type
+        if (ok) {  // the last chunk's o, and the final state into the slot, rounded to the pool's type
             const bool uw = mbar_wait_bounded(bar(kUpdBar), (uint32_t)(nch - 1) & 1u, kPWaitPolls);
+            if (lt == kOT && o_bulk && nch >= 3) bulk_wait_read_but_one();
             if (named_sync_or(kBarRow, kPRows, !uw)) {
                 ok = false;
             } else {
                 tc_fence_after();
+                emit_o(nch - 1);
                 StT* dst = static_cast<StT*>(p.pool_out) + (((int64_t)slot * p.HV + h) * p.DV + row) * DK;
 #pragma unroll
                 for (int c0 = 0; c0 < DK; c0 += 16) {
@@ -362,8 +452,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     tmem_wait_ld();
                     if (live) store16<StT>(dst + c0, f);
                 }
+                named_sync(kBarRow, kPRows);
+                if (lt == kOT && o_bulk) issue_o(nch - 1);
             }
         }
+        if (lt == kOT && o_bulk) bulk_wait_all();  // the o copies are complete before the CTA leaves
         if (!ok && lt == 0) {
             *fail = 1;
             if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
@@ -386,7 +479,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const InT* ap = static_cast<const InT*>(p.a);
         const InT* bp = static_cast<const InT*>(p.b);
         uint4 raw[NPASS][QK::NC];
-        InT vraw[C];
+        constexpr int VPASS = C * kPRows / 8 / kPRows;  // 8-row pieces of v per thread and chunk
+        uint4 vraw[VPASS][QK::NC];
+        const int vrow = 8 * (lt % 16), vtok = lt / 16;  // this thread's v piece: rows vrow.., token vtok + 8 pass
+        const int vrows = min(8, p.DV - (row - lt) - vrow);  // rows of the piece inside DV (<= 0: none)
         InT araw = InT(0.f), braw = InT(0.f);
         auto load_chunk = [&](int c) {
             const int t0 = c * C;
@@ -400,9 +496,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     QK::load_global((j < C ? kp : qp) + ((int64_t)(lo + t0 + t) * p.HK + hk) * DK + 8 * vc, raw[ps]);
             }
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                vraw[t] = InT(0.f);
-                if (t0 + t < n && row < p.DV) vraw[t] = vp[((int64_t)(lo + t0 + t) * p.HV + h) * p.DV + row];
+            for (int ps = 0; ps < VPASS; ++ps) {
+                const int t = vtok + 8 * ps;
+#pragma unroll
+                for (int e = 0; e < QK::NC; ++e) vraw[ps][e] = make_uint4(0, 0, 0, 0);
+                if (t0 + t < n && vrows > 0) {
+                    const InT* src = vp + ((int64_t)(lo + t0 + t) * p.HV + h) * p.DV + (row - lt) + vrow;
+                    if (p.v_vec && vrows == 8) {
+                        QK::load_global(src, vraw[ps]);
+                    } else {  // a piece across the end of DV, or v not in 16-byte pieces
+                        InT* dst = reinterpret_cast<InT*>(vraw[ps]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (e < vrows) dst[e] = src[e];
+                    }
+                }
             }
             if (lt < C && t0 + lt < n) {
                 araw = ap[(int64_t)(lo + t0 + lt) * p.HV + h];
@@ -443,9 +551,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 F[PL::GAM + lt] = gm;
                 F[PL::CEND + lt] = ce;
             }
-            // v of this thread's row, per token
+            // v of the block's rows, per token
 #pragma unroll
-            for (int t = 0; t < C; ++t) F[PL::VB + t * kPRows + lt] = to_f32(vraw[t]);
+            for (int ps = 0; ps < VPASS; ++ps) {
+                float2 x[4];
+                QK::unpack(vraw[ps], x);
+                float4* dst = reinterpret_cast<float4*>(F + PL::VB + (vtok + 8 * ps) * kPRows + vrow);
+                dst[0] = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+                dst[1] = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+            }
             // q, k normalised, into the stacked rows: kh hi at t, qh hi at C + t, kh lo at 2C + t, qh lo at 3C + t
 #pragma unroll
             for (int ps = 0; ps < NPASS; ++ps) {
@@ -521,10 +635,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const float full = gr[s] + scr[lt * PL::SCR_STRIDE + s];
                     wv[s] = (isq ? s <= t : s < t) ? G * full : 0.f;
                 }
-                float* dst = F + (isq ? PL::KQW : PL::KKW) + t * C;
+                if (isq) {  // row t of KQw in bf16 hi / lo, K-major rows of 128 bytes (the O product's B)
+                    unsigned char* kb = sm + PL::KQB_OFF + buf * PL::KQB_BYTES;
 #pragma unroll
-                for (int s = 0; s < C; s += 4)
-                    *reinterpret_cast<float4*>(dst + s) = make_float4(wv[s], wv[s + 1], wv[s + 2], wv[s + 3]);
+                    for (int j8 = 0; j8 < C / 8; ++j8) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) split_pair(wv[8 * j8 + 2 * e], wv[8 * j8 + 2 * e + 1], hw[e], lw[e]);
+                        *reinterpret_cast<uint4*>(kb + sw128(C, t, j8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(kb + C * 128 + sw128(C, t, j8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    fence_proxy_async_smem();
+                } else {  // column t of KKwT (fp32, for the row recurrence)
+                    float* dst = F + PL::KKW + t;
+#pragma unroll
+                    for (int s = 0; s < C; ++s) dst[s * C] = wv[s];
+                }
             }
             mbar_arrive(bar(kFull0 + buf));  // after this thread's writes of the chunk
         }
@@ -565,7 +691,26 @@ cudaError_t launch_dk(const RecurrentParams& p, const int32_t* cu_seqlens, const
     const int NRB = (p.DV + kPRows - 1) / kPRows;
     const int64_t items = (int64_t)B * p.HV * NRB;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;
-    kernel<<<(unsigned)items, kPThreads, PL::BYTES, s>>>(p, cu_seqlens, has_init, n_tokens);
+    // o as a 3-D tensor [n_tokens][HV][DV] for the per-chunk TMA store (box: 128 rows of one head, 32 tokens);
+    // when o is not in 16-byte pieces, DV < 128 or the map cannot be made, the kernel copies or stores per token
+    CUtensorMap omap;
+    std::memset(&omap, 0, sizeof omap);
+    int o_tma = 0;
+    const uint64_t osz = p.out_bf16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(p.o) & 15u) == 0 && ((uint64_t)p.DV * osz) % 16 == 0 && p.DV >= kPRows &&
+        n_tokens > 0) {
+        const EncodeTiledFn fn = encode_tiled_fn();
+        if (fn != nullptr) {
+            const cuuint64_t dims[3] = {(cuuint64_t)p.DV, (cuuint64_t)p.HV, (cuuint64_t)n_tokens};
+            const cuuint64_t strides[2] = {(cuuint64_t)p.DV * osz, (cuuint64_t)p.HV * p.DV * osz};
+            const cuuint32_t box[3] = {(cuuint32_t)kPRows, 1, (cuuint32_t)kPC};
+            const cuuint32_t estr[3] = {1, 1, 1};
+            o_tma = fn(&omap, p.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.o,
+                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+    }
+    kernel<<<(unsigned)items, kPThreads, PL::BYTES, s>>>(p, cu_seqlens, has_init, n_tokens, omap, o_tma);
     return cudaGetLastError();
 }
 
