@@ -11,31 +11,39 @@
 //     u_t   = g_t S_{t-1} kh_t = gamma_t (S_0 kh_t) + sum_{s<t}  G(s,t) (kh_s . kh_t) delta_s,   delta_t = beta_t (v_t - u_t)
 //     o_t   = scale S_t qh_t   = scale (gamma_t (S_0 qh_t) + sum_{s<=t} G(s,t) (kh_s . qh_t) delta_s)
 //     S_C-1 = gamma_{C-1} S_0 + sum_s G(s, C-1) delta_s kh_s^T .
-// Per chunk the dense work is three products on the tensor cores, each in bf16 hi + lo parts (x = hi + lo, hi =
-// bf16(x), lo = bf16(x - hi): about 16 significant bits, and all four part products are taken, so the only error
-// besides fp32 accumulation is that of the split itself):
-//   Gram   [kh; qh] kh^T     (M = 128 rows of the stacked token buffer, N = C; A and B from shared memory),
-//   P      S_0 [kh; qh]^T    (M = 128 state rows, N = 4C; A = S_0 hi / lo written into tensor memory),
-//   update S += c kh         (M = 128, N = DK; A = c_s = G(s, C-1) delta_s hi / lo in tensor memory, B = the kh
-//                             rows read MN-major), onto gamma_{C-1} S_0 written in place beforehand;
-// what is left per state row is the C x C triangular recurrence above, in fp32 registers, one thread per row.
-// The state stays in fp32 in tensor memory for the whole sequence and is rounded to the pool's type once, at the
-// final write-back, like the token loop's registers.
+// The dense work is on the tensor cores in bf16 operands with fp32 accumulation, each fp32 operand split into
+// hi = bf16(x) and lo = bf16(x - hi) (about 16 significant bits; the lo.lo part products, about 2^-18 relative,
+// are left out):
+//   Gram   of the chunk's k and q rows (M = 128, N = C or 2C; A and B from shared memory),
+//   P      S_0 [k; q]^T (M = 128 state rows; A = S_0 hi / lo written into tensor memory),
+//   O      delta KQw^T, onto gamma_t S_0 qh_t (A = delta hi / lo in tensor memory, B = KQw hi / lo),
+//   update S += c k (N = DK; A = c_s = G(s, C-1) delta_s hi / lo in tensor memory, B = the k rows read MN-major),
+//          onto gamma_{C-1} S_0 written in place beforehand;
+// what is left per state row is the u recurrence above, in fp32 registers, one thread per row.  The state stays
+// in fp32 in tensor memory for the whole sequence and is rounded to the pool's type once, at the final write-back,
+// like the token loop's registers.
+//
+// Two ways to bring the tokens in.  bf16 q, k, v (with v in whole 16-byte pieces and DV >= 128) arrive by TMA:
+// raw k and q rows straight into the swizzled operand buffer (a bf16 value is its own hi part, its lo part is
+// zero) and v as a bf16 tile; the L2 normalisation is then a factor per token, rk_t = 1 / sqrt(|k_t|^2 + eps)
+// (and rq_t), with |k_t|^2 and |q_t|^2 read off the diagonal of the Gram product [k; q][k; q]^T, applied to P in
+// the row thread, to the weights, and to the update's coefficients.  Otherwise (fp32 inputs, odd layouts) the
+// token group loads and normalises q and k itself into [kh hi | qh hi | kh lo | qh lo] rows and stores v as fp32.
 //
 // CTA = one item = (sequence, value head, block of 128 state rows); a kernel that allocates tensor memory runs one
 // CTA per SM.  Warps 0-3 (the row group, thread = state row = tensor-memory lane) run the state chain: S_0 into
-// hi / lo, the P product, the row recurrence and the o stores, the coefficients, the update product.  Warps 4-7
-// (the token group) prepare the next chunk meanwhile, into the other of two buffers: q, k normalised into the
-// stacked bf16 rows [kh hi | qh hi | kh lo | qh lo] (the 128-byte swizzled operand layout), v of the block's rows,
-// the gates and their prefix and suffix products, and the decay-weighted Gram matrices
-// KKw[t][s] = G(s,t) kh_s . kh_t (s < t) and KQw[t][s] = G(s,t) kh_s . qh_t (s <= t).  mbarriers hand the
-// buffers back and forth (every wait bounded: a wait that runs out sets GDN_ERRBIT_TIMEOUT and the CTA leaves).
+// hi / lo, the P product, the row recurrence, the O and update products, o out.  Warps 4-7 (the token group)
+// prepare the next chunk meanwhile in a ring of buffer stages: the token rows, v, the gates with their prefix and
+// suffix products, the Gram product and from it the decay-weighted matrices KKw[t][s] = G(s,t) kh_s . kh_t (s < t)
+// and KQw[t][s] = G(s,t) kh_s . qh_t (s <= t).  mbarriers hand the stages back and forth (every wait bounded: a
+// wait that runs out sets GDN_ERRBIT_TIMEOUT and the CTA leaves).
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_tcgen05.cuh"
 
 #include <atomic>
 #include <cstring>
+#include <type_traits>
 
 namespace gdn {
 namespace {
@@ -47,37 +55,48 @@ constexpr int kBarRow = 1, kBarTok = 2;  // named barriers of the two groups (0 
 constexpr uint32_t kPWaitPolls = GDN_WAIT_POLLS;
 constexpr uint32_t kPCols = 512;  // tensor memory of the CTA (a power of two covering the plan)
 
-template <int DK>
+template <int DK, bool kTma>
 struct PrefillChunkPlan {
     static_assert(DK == 64 || DK == 128, "the chunked prefill takes DK = 64 or 128");
-    // shared memory, bytes from the 1024-byte aligned base: two stacked token buffers (128 rows x DK bf16 in
-    // 64-column boxes of 128 rows), two float buffers, the partial Gram rows, the mbarriers
-    static constexpr uint32_t BOX = 128u * 128u;
-    static constexpr uint32_t KQ_BYTES = 128u * DK * 2u;
+    static constexpr int NST = kTma ? 3 : 2;  // buffer stages (TMA: one chunk of lead for the loads)
+    // stacked token rows per 64-column box: [k | q] raw bf16 (TMA), or [kh hi | qh hi | kh lo | qh lo]
+    static constexpr int KQR = kTma ? 2 * kPC : 4 * kPC;
+    static constexpr uint32_t BOX = KQR * 128u;
+    static constexpr uint32_t KQ_BYTES = BOX * (DK / 64);
+    // TMA: the Gram product's A spans 128 rows, 64 past the stacked ones, which must still be shared memory
+    static constexpr uint32_t KQ_PAD = kTma ? 64u * 128u : 0u;
     // KQw in bf16 hi then lo, the B operand of the O product: C rows of 128 bytes each (K = C of 64 columns used)
     static constexpr uint32_t KQB_BYTES = 2u * kPC * 128u;
-    static constexpr uint32_t KQB_OFF = 2u * KQ_BYTES;
-    // float buffer: KKwT, v of the block's rows per token, g, beta, gamma, G(s, C-1)
-    static constexpr int KKW = 0, VB = kPC * kPC, GG = VB + kPC * kPRows, BET = GG + kPC, GAM = BET + kPC,
-                         CEND = GAM + kPC, F_FLOATS = CEND + kPC;
-    static constexpr int SCR_STRIDE = kPC + 1;  // partial Gram rows, padded against bank conflicts
-    static constexpr uint32_t F_OFF = KQB_OFF + 2u * KQB_BYTES;
-    static constexpr uint32_t SCR_OFF = F_OFF + 2u * F_FLOATS * 4u;
-    // two chunks of o staged for the bulk stores: [token][128 rows] in o's type (fp32 at most)
+    static constexpr uint32_t KQB_OFF = NST * KQ_BYTES + KQ_PAD;
+    static constexpr uint32_t VT_BYTES = kTma ? kPC * kPRows * 2u : 0u;  // TMA: v as bf16 [token][128 rows]
+    static constexpr uint32_t VT_OFF = KQB_OFF + NST * KQB_BYTES;
+    // floats of a stage: KKwT [s][t]; v [token][row] (no TMA); per token g, beta, gamma, the update's factor
+    // G(s, C-1) rk_s, the P factors gamma_t rk_t and gamma_t rq_t, rk, rq (rk = rq = 1 when normalised beforehand)
+    static constexpr int KKW = 0, VB = kPC * kPC, GG = VB + (kTma ? 0 : kPC * kPRows), BET = GG + kPC,
+                         GAM = BET + kPC, CEND = GAM + kPC, GK = CEND + kPC, GQ = GK + kPC, RK = GQ + kPC,
+                         RQ = RK + kPC, F_FLOATS = RQ + kPC;
+    static constexpr uint32_t F_OFF = VT_OFF + NST * VT_BYTES;
+    static constexpr int SCR_STRIDE = kPC + 1;  // partial Gram rows (no TMA), padded against bank conflicts
+    static constexpr uint32_t SCR_OFF = F_OFF + NST * F_FLOATS * 4u;
+    // two chunks of o staged for the stores: [token][128 rows] in o's type (fp32 at most)
     static constexpr uint32_t OB_BYTES = kPC * kPRows * 4u;
     static constexpr uint32_t OB_OFF = (SCR_OFF + 64u * SCR_STRIDE * 4u + 1023u) & ~1023u;
     static constexpr uint32_t BAR_OFF = OB_OFF + 2u * OB_BYTES;
-    static constexpr uint32_t BYTES = BAR_OFF + 128u + 1024u;  // + the alignment slack of the base
-    // tensor-memory columns: S (fp32), S_0 hi and lo (bf16 pairs; delta hi and lo after the P product), P, the two
-    // Gram products, c hi and lo, O
+    static constexpr uint32_t BYTES = BAR_OFF + 256u + 1024u;  // + the alignment slack of the base
+    static_assert(KQB_OFF % 1024 == 0 && VT_OFF % 1024 == 0 && F_OFF % 16 == 0, "operand alignment");
+    // tensor-memory columns: S (fp32), S_0 hi and lo (bf16 pairs; delta hi and lo after the P product), P, the Gram
+    // product (two of C columns, or one of 2C), c hi and lo, O
     static constexpr uint32_t S_COL = 0, SH_COL = DK, SL_COL = DK + DK / 2, P_COL = 2 * DK, G1_COL = P_COL + 4 * kPC,
                               G2_COL = G1_COL + kPC, CH_COL = G2_COL + kPC, CL_COL = CH_COL + kPC / 2,
                               O_COL = CL_COL + kPC / 2, COLS = O_COL + kPC;
     static_assert(COLS <= kPCols, "tensor memory of the plan");
 };
 
-// mbarriers, 8 bytes each from the plan's BAR_OFF
-enum { kFull0 = 0, kFull1, kEmpty0, kEmpty1, kPBar, kUpdBar, kGramBar, kDrainRow, kDrainTok, kNumBars };
+// mbarriers, 8 bytes each from the plan's BAR_OFF: per stage full (token group -> row group), empty (the update
+// product that read the stage has completed) and TMA (the stage's token rows have landed)
+enum {
+    kFull0 = 0, kEmpty0 = 3, kTmaBar0 = 6, kPBar = 9, kUpdBar, kGramBar, kDrainRow, kDrainTok, kNumBars
+};
 
 template <typename T>
 __device__ __forceinline__ void load16(const T* src, float (&f)[16]);
@@ -128,13 +147,16 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     lo = bf16x2_bits(x0 - __low2float(h2), x1 - __high2float(h2));
 }
 
-template <int DK, typename InT, typename StT>
+template <int DK, typename InT, typename StT, bool kTma>
 __global__ void __launch_bounds__(kPThreads, 1)
     gdn_prefill_chunked_kernel(const RecurrentParams p, const int32_t* __restrict__ cu_seqlens,
                                const int32_t* __restrict__ has_init, int n_tokens,
-                               const __grid_constant__ CUtensorMap omap, int o_tma) {
-    using PL = PrefillChunkPlan<DK>;
+                               const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap kmap,
+                               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap vmap,
+                               int o_tma) {
+    using PL = PrefillChunkPlan<DK, kTma>;
     constexpr int C = kPC;
+    constexpr int NST = PL::NST;
     const int NRB = (p.DV + kPRows - 1) / kPRows;
     const int item = blockIdx.x;  // row block fastest, then value head, then sequence
     const int rb = item % NRB, h = (item / NRB) % p.HV, b = item / (NRB * p.HV);
@@ -174,8 +196,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kPCols);
     if (tid == 0) {
-        mbar_init(bar(kFull0), kPRows);
-        mbar_init(bar(kFull1), kPRows);
+        for (int i = 0; i < NST; ++i) mbar_init(bar(kFull0 + i), kPRows);
         for (int i = kEmpty0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         fence_mbar_init();
         *fail = 0;
@@ -185,8 +206,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    auto fbuf = [&](int buf) -> float* { return reinterpret_cast<float*>(sm + PL::F_OFF) + buf * PL::F_FLOATS; };
-    auto kq_addr = [&](int buf) -> uint32_t { return base + (uint32_t)buf * PL::KQ_BYTES; };
+    auto fbuf = [&](int st) -> float* { return reinterpret_cast<float*>(sm + PL::F_OFF) + st * PL::F_FLOATS; };
+    auto kq_addr = [&](int st) -> uint32_t { return base + (uint32_t)st * PL::KQ_BYTES; };
+    auto kqb_addr = [&](int st) -> uint32_t { return base + PL::KQB_OFF + (uint32_t)st * PL::KQB_BYTES; };
+    auto vtile = [&](int st) -> const __nv_bfloat16* {
+        return reinterpret_cast<const __nv_bfloat16*>(sm + PL::VT_OFF + (size_t)st * PL::VT_BYTES);
+    };
 
     if (row_group) {
         // ================================ row group: the state chain ================================
@@ -267,10 +292,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
-            const int buf = c & 1;
-            const float* F = fbuf(buf);
-            const uint32_t kq = kq_addr(buf);
-            bool w = mbar_wait_bounded(bar(kFull0 + buf), (uint32_t)(c >> 1) & 1u, kPWaitPolls);
+            const int st = c % NST;
+            const float* F = fbuf(st);
+            const uint32_t kq = kq_addr(st);
+            bool w = mbar_wait_bounded(bar(kFull0 + st), (uint32_t)(c / NST) & 1u, kPWaitPolls);
             if (w && c > 0) w = mbar_wait_bounded(bar(kUpdBar), (uint32_t)(c - 1) & 1u, kPWaitPolls);
             // the staging buffer of chunk c-1's o was last copied from for chunk c-3, two groups ago
             if (lt == kOT && o_bulk && c >= 3) bulk_wait_read_but_one();
@@ -320,15 +345,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             named_sync(kBarRow, kPRows);
-            // P = S_0 [kh hi | qh hi | kh lo | qh lo]^T: S_0 hi against all 128 stacked rows, S_0 lo against the hi
-            // rows only (the lo.lo part, about 2^-18 relative, is left out); then chunk c-1's o to global memory
+            // P = S_0 [stacked rows]^T: S_0 hi against every stacked row, S_0 lo against the hi rows (TMA: the raw
+            // k and q rows, N = 2C; otherwise [kh hi | qh hi | kh lo | qh lo], N = 4C and 2C)
             if (lt == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks) {
                     const uint64_t bd = umma_desc_sw128(kq + (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u);
-                    umma_bf16_ta(tmem + PL::P_COL, tmem + PL::SH_COL + 8 * ks, bd, umma_idesc_bf16(kPRows, 4 * C),
-                                 ks > 0 ? 1u : 0u);
+                    umma_bf16_ta(tmem + PL::P_COL, tmem + PL::SH_COL + 8 * ks, bd,
+                                 umma_idesc_bf16(kPRows, kTma ? 2 * C : 4 * C), ks > 0 ? 1u : 0u);
                     umma_bf16_ta(tmem + PL::P_COL, tmem + PL::SL_COL + 8 * ks, bd, umma_idesc_bf16(kPRows, 2 * C), 1u);
                 }
                 umma_commit(bar(kPBar));
@@ -342,24 +367,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             if (lt == kOT && c > 0 && o_bulk) issue_o(c - 1);
             tc_fence_after();
-            // this row of P: S_0 kh_t = P[t] + P[2C + t], S_0 qh_t = P[C + t] + P[3C + t]
+            // this row of P: S_0 k_t = P[t] (+ P[2C + t]), S_0 q_t = P[C + t] (+ P[3C + t])
             float pk[C], pq[C];
             {
-                float x[C];
                 tmem_ld16(lane_base + PL::P_COL, pk);
                 tmem_ld16(lane_base + PL::P_COL + 16, pk + 16);
-                tmem_ld16(lane_base + PL::P_COL + 2 * C, x);
-                tmem_ld16(lane_base + PL::P_COL + 2 * C + 16, x + 16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < C; ++t) pk[t] += x[t];
                 tmem_ld16(lane_base + PL::P_COL + C, pq);
                 tmem_ld16(lane_base + PL::P_COL + C + 16, pq + 16);
-                tmem_ld16(lane_base + PL::P_COL + 3 * C, x);
-                tmem_ld16(lane_base + PL::P_COL + 3 * C + 16, x + 16);
                 tmem_wait_ld();
+                if constexpr (!kTma) {
+                    float x[C];
+                    tmem_ld16(lane_base + PL::P_COL + 2 * C, x);
+                    tmem_ld16(lane_base + PL::P_COL + 2 * C + 16, x + 16);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < C; ++t) pq[t] += x[t];
+                    for (int t = 0; t < C; ++t) pk[t] += x[t];
+                    tmem_ld16(lane_base + PL::P_COL + 3 * C, x);
+                    tmem_ld16(lane_base + PL::P_COL + 3 * C + 16, x + 16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < C; ++t) pq[t] += x[t];
+                }
             }
             // the row's u recurrence, right-looking: once delta_s is known it goes into u_t of every later token
             // (KKwT[s][t] = KKw[t][s], zero for t <= s), so the dependent chain per token is a few operations and
@@ -368,15 +396,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t ow[C];  // gamma_t S_0 qh_t, the O product's starting value
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                const float gm = F[PL::GAM + t];
-                pk[t] *= gm;
-                ow[t] = __float_as_uint(gm * pq[t]);
+                pk[t] *= F[PL::GK + t];  // gamma_t rk_t: gamma_t S_0 kh_t
+                ow[t] = __float_as_uint(F[PL::GQ + t] * pq[t]);
             }
             uint32_t dhw[C / 2], dlw[C / 2], chw[C / 2], clw[C / 2];
             float dprev = 0.f, cprev = 0.f;
+            const __nv_bfloat16* vt = vtile(st);
 #pragma unroll
             for (int s = 0; s < C; ++s) {
-                const float ds = F[PL::BET + s] * (F[PL::VB + s * kPRows + lt] - pk[s]);
+                const float vs = kTma ? __bfloat162float(vt[s * kPRows + lt]) : F[PL::VB + s * kPRows + lt];
+                const float ds = F[PL::BET + s] * (vs - pk[s]);
 #pragma unroll
                 for (int t4 = (s + 1) & ~3; t4 < C; t4 += 4) {
                     const float4 a4 = *reinterpret_cast<const float4*>(KKwT + s * C + t4);
@@ -385,7 +414,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (t4 + 2 > s) pk[t4 + 2] = fmaf(a4.z, ds, pk[t4 + 2]);
                     if (t4 + 3 > s) pk[t4 + 3] = fmaf(a4.w, ds, pk[t4 + 3]);
                 }
-                // delta_s (the O product's A) and c_s = G(s, C-1) delta_s (the update's A) in hi / lo pairs
+                // delta_s (the O product's A) and c_s = G(s, C-1) rk_s delta_s (the update's A) in hi / lo pairs
                 const float cs = F[PL::CEND + s] * ds;
                 if (s & 1) {
                     split_pair(dprev, ds, dhw[s / 2], dlw[s / 2]);
@@ -406,11 +435,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int jj = 0; jj < C; jj += 8) tmem_st8(lane_base + PL::O_COL + jj, ow + jj);
             tmem_wait_st();
             tc_fence_before();
-            named_sync(kBarRow, kPRows);  // every row's operands are in place; every read of buffer buf is done
+            named_sync(kBarRow, kPRows);  // every row's operands are in place; every read of stage st is done
             if (lt == 0) {
                 tc_fence_after();
                 // O += (delta hi + delta lo)(KQw hi + KQw lo)^T without the lo.lo part: B = the C rows of KQw, K-major
-                const uint32_t kqb = base + PL::KQB_OFF + (uint32_t)buf * PL::KQB_BYTES;
+                const uint32_t kqb = kqb_addr(st);
 #pragma unroll
                 for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -420,12 +449,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             umma_bf16_ta(tmem + PL::O_COL, tmem + (a ? PL::SL_COL : PL::SH_COL) + 8 * ks,
                                          umma_desc_sw128(kqb + (uint32_t)bh * (C * 128u) + 32u * ks),
                                          umma_idesc_bf16(kPRows, C), 1u);
-                // S += c hi (kh hi + kh lo) + c lo kh hi: B = rows 0..C-1 (kh hi) and 2C..3C-1 (kh lo), MN-major
+                // S += (c hi + c lo) k: B = the k rows read MN-major (TMA: raw rows 0..C-1; otherwise kh hi rows
+                // 0..C-1 against c hi and lo, and kh lo rows 2C..3C-1 against c hi)
                 const uint32_t idesc = umma_idesc_bf16(kPRows, DK) | (1u << 16);
 #pragma unroll
                 for (int a = 0; a < 2; ++a)
 #pragma unroll
-                    for (int bh = 0; bh < 2 - a; ++bh)
+                    for (int bh = 0; bh < (kTma ? 1 : 2 - a); ++bh)
 #pragma unroll
                         for (int ks = 0; ks < C / 16; ++ks) {
                             const uint32_t brow = (uint32_t)(bh * 2 * C + 16 * ks);
@@ -433,7 +463,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                          umma_desc_sw128_mn(kq + brow * 128u, PL::BOX), idesc, 1u);
                         }
                 umma_commit(bar(kUpdBar));  // also tracks the O product issued before it
-                umma_commit(bar(kEmpty0 + buf));  // the token group may refill buffer buf
+                umma_commit(bar(kEmpty0 + st));  // the token group may refill stage st
             }
         }
         if (ok) {  // the last chunk's o, and the final state into the slot, rounded to the pool's type
@@ -465,8 +495,178 @@ __global__ void __launch_bounds__(kPThreads, 1)
             umma_commit(bar(kDrainRow));
             mbar_wait_bounded(bar(kDrainRow), 0u, kPWaitPolls);
         }
+    } else if constexpr (kTma) {
+        // ================= token group (TMA): raw k, q rows into the operand stage, v as a bf16 tile =================
+        const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+        const __nv_bfloat16* ap = static_cast<const __nv_bfloat16*>(p.a);
+        const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.b);
+        __nv_bfloat16 araw = __float2bfloat16_rn(0.f), braw = araw;
+        auto load_ab = [&](int cc) {  // lane = token of chunk cc
+            if (lt < C && cc * C + lt < n) {
+                araw = ap[(int64_t)(lo + cc * C + lt) * p.HV + h];
+                braw = bp[(int64_t)(lo + cc * C + lt) * p.HV + h];
+            }
+        };
+        constexpr uint32_t kTmaBytes = (2u * DK * C + (uint32_t)C * kPRows) * 2u;  // k, q boxes and the v box
+        int tma_issued = 0;  // thread 0: chunks whose loads have been issued
+        auto issue_tma = [&](int cc) {
+            const int sg = cc % NST;
+            const uint32_t tb = bar(kTmaBar0 + sg), kqs = kq_addr(sg);
+            mbar_arrive_expect_tx(tb, kTmaBytes);
+#pragma unroll
+            for (int j = 0; j < DK / 64; ++j) {
+                tma_load_3d(kqs + (uint32_t)j * PL::BOX, &kmap, 64 * j, hk, lo + cc * C, tb);
+                tma_load_3d(kqs + (uint32_t)j * PL::BOX + C * 128u, &qmap, 64 * j, hk, lo + cc * C, tb);
+            }
+            tma_load_3d(base + PL::VT_OFF + (uint32_t)sg * PL::VT_BYTES, &vmap, rb * kPRows, h, lo + cc * C, tb);
+            tma_issued = cc + 1;
+        };
+        if (lt == 0) {
+            issue_tma(0);
+            if (nch > 1) issue_tma(1);
+        }
+        load_ab(0);
+        bool issued = false, ok = true;
+        int consumed = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int st = c % NST;
+            float* F = fbuf(st);
+            const uint32_t kq = kq_addr(st);
+            const bool w = mbar_wait_bounded(bar(kTmaBar0 + st), (uint32_t)(c / NST) & 1u, kPWaitPolls);
+            if (named_sync_or(kBarTok, kPRows, !w || *fail != 0)) {
+                ok = w;
+                break;
+            }
+            consumed = c + 1;
+            const int len = min(C, n - c * C);
+            if (len < C) {  // the rows past the sequence hold another sequence's tokens (or zeros): clear them
+                unsigned char* KQ = sm + (size_t)st * PL::KQ_BYTES;
+                for (int i = lt; i < (C - len) * (DK / 8); i += kPRows) {
+                    const int r = len + i / (DK / 8), c8 = i % (DK / 8);
+                    *reinterpret_cast<uint4*>(KQ + sw128(PL::KQR, r, c8)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(KQ + sw128(PL::KQR, C + r, c8)) = make_uint4(0, 0, 0, 0);
+                }
+                unsigned char* VT = sm + PL::VT_OFF + (size_t)st * PL::VT_BYTES;
+                for (int i = lt; i < (C - len) * (kPRows / 8); i += kPRows)
+                    *reinterpret_cast<uint4*>(VT + (size_t)(len + i / (kPRows / 8)) * kPRows * 2 + (i % (kPRows / 8)) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();  // the cleared rows are read by the tensor cores
+            }
+            // gates (lane = token), with gamma_t = g_0 .. g_t and G(s, C-1) = g_{s+1} .. g_{C-1}
+            float ce = 1.f;
+            if (lt < C) {
+                const bool valid = lt < len;  // tokens past the sequence: g = 1, beta = 0
+                const float g = valid ? gate(A_log, __bfloat162float(araw), dt_bias) : 1.f;
+                const float be = valid ? sigmoid(__bfloat162float(braw)) : 0.f;
+                float gm = g, sf = g;
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gm, m);
+                    if (lt >= m) gm *= y;
+                    const float z = __shfl_down_sync(0xffffffffu, sf, m);
+                    if (lt + m < 32) sf *= z;
+                }
+                ce = __shfl_down_sync(0xffffffffu, sf, 1);
+                if (lt == C - 1) ce = 1.f;
+                F[PL::GG + lt] = g;
+                F[PL::BET + lt] = be;
+                F[PL::GAM + lt] = gm;
+            }
+            named_sync(kBarTok, kPRows);
+            // Gram product [k; q] [k; q]^T of the raw rows (rows 2C.. of A lie past the stage: their lanes are unused)
+            if (lt == 0) {
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(kPRows, 2 * C);
+#pragma unroll
+                for (int ks = 0; ks < DK / 16; ++ks) {
+                    const uint32_t koff = (uint32_t)(ks >> 2) * PL::BOX + (uint32_t)(ks & 3) * 32u;
+                    umma_bf16(tmem + PL::G1_COL, umma_desc_sw128(kq + koff), umma_desc_sw128(kq + koff), idesc,
+                              ks > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(kGramBar));
+                issued = true;
+            }
+            if (c + 1 < nch) load_ab(c + 1);  // in flight meanwhile
+            const bool gw = mbar_wait_bounded(bar(kGramBar), (uint32_t)c & 1u, kPWaitPolls);
+            if (named_sync_or(kBarTok, kPRows, !gw)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // lane t: k_t . [k; q], lane C + t: q_t . [k; q]; the diagonal gives |k_t|^2 and |q_t|^2
+            float d[2 * C];
+            if (lt < 2 * C) {
+#pragma unroll
+                for (int j = 0; j < 2 * C; j += 16) tmem_ld16(lane_base + PL::G1_COL + j, d + j);
+                tmem_wait_ld();
+                float nrm = 0.f;
+#pragma unroll
+                for (int j = 0; j < C; ++j) {
+                    const float x = lt < C ? d[j] : d[C + j];
+                    if (j == (lt & (C - 1))) nrm = x;
+                }
+                const int t = lt & (C - 1);
+                F[(lt < C ? PL::RK : PL::RQ) + t] = t < len ? rsqrtf(nrm + p.l2_eps) : 0.f;
+            }
+            tc_fence_before();
+            named_sync(kBarTok, kPRows);
+            if (lt < 2 * C) {
+                const int t = lt & (C - 1);
+                const bool isq = lt >= C;  // rows C..2C-1: q_t . k_s
+                const float rt = F[(isq ? PL::RQ : PL::RK) + t];
+                float wv[C];
+                float G = 1.f;  // G(s, t), built downwards from s = t
+#pragma unroll
+                for (int s = C - 1; s >= 0; --s) {
+                    if (s < t) G *= F[PL::GG + s + 1];
+                    wv[s] = (isq ? s <= t : s < t) ? G * (F[PL::RK + s] * rt) * d[s] : 0.f;
+                }
+                if (isq) {  // row t of KQw in bf16 hi / lo, K-major rows of 128 bytes (the O product's B)
+                    unsigned char* kb = sm + PL::KQB_OFF + (size_t)st * PL::KQB_BYTES;
+#pragma unroll
+                    for (int j8 = 0; j8 < C / 8; ++j8) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) split_pair(wv[8 * j8 + 2 * e], wv[8 * j8 + 2 * e + 1], hw[e], lw[e]);
+                        *reinterpret_cast<uint4*>(kb + sw128(C, t, j8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(kb + C * 128 + sw128(C, t, j8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    fence_proxy_async_smem();
+                } else {  // column t of KKwT (fp32, for the row recurrence), and the token's factors
+                    float* dst = F + PL::KKW + t;
+#pragma unroll
+                    for (int s = 0; s < C; ++s) dst[s * C] = wv[s];
+                    const float gm = F[PL::GAM + t];
+                    F[PL::GK + t] = gm * rt;
+                    F[PL::GQ + t] = gm * F[PL::RQ + t];
+                    F[PL::CEND + t] = ce * rt;
+                }
+            }
+            mbar_arrive(bar(kFull0 + st));  // after this thread's writes of the chunk
+            // the loads of chunk c + 2, into the stage of chunk c - 1 once its update product has completed
+            if (lt == 0 && c + 2 < nch) {
+                const bool e = c < 1 || mbar_wait_bounded(bar(kEmpty0 + (c + 2) % NST),
+                                                          (uint32_t)((c - 1) / NST) & 1u, kPWaitPolls);
+                if (e)
+                    issue_tma(c + 2);
+                else
+                    *fail = 1;
+            }
+        }
+        if ((!ok || *fail != 0) && lt == 0) {
+            *fail = 1;
+            if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+        }
+        if (lt == 0) {  // loads issued and not consumed land, and every MMA completes, before the CTA leaves
+            for (int cc = consumed; cc < tma_issued; ++cc)
+                mbar_wait_bounded(bar(kTmaBar0 + cc % NST), (uint32_t)(cc / NST) & 1u, kPWaitPolls);
+            if (issued) {
+                umma_commit(bar(kDrainTok));
+                mbar_wait_bounded(bar(kDrainTok), 0u, kPWaitPolls);
+            }
+        }
     } else {
-        // ============================ token group: the next chunk's inputs ============================
+        // ========== token group (no TMA): q, k loaded and normalised into hi / lo rows, v stored as fp32 ==========
         using QK = Slice8<InT>;
         constexpr int LPV = DK / 8;          // threads per q or k vector, 8 columns each
         constexpr int VPP = kPRows / LPV;    // vectors per pass of the group
@@ -521,12 +721,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         bool ok = true;
         load_chunk(0);
         for (int c = 0; c < nch; ++c) {
-            const int buf = c & 1;
-            float* F = fbuf(buf);
-            unsigned char* KQ = sm + (size_t)buf * PL::KQ_BYTES;
-            const uint32_t kq = kq_addr(buf);
-            // buffer buf is free once the update of chunk c - 2 (which read it last) has completed
-            const bool w = c < 2 || mbar_wait_bounded(bar(kEmpty0 + buf), (uint32_t)((c - 2) >> 1) & 1u, kPWaitPolls);
+            const int st = c % NST;
+            float* F = fbuf(st);
+            unsigned char* KQ = sm + (size_t)st * PL::KQ_BYTES;
+            const uint32_t kq = kq_addr(st);
+            // stage st is free once the update of chunk c - NST (which read it last) has completed
+            const bool w =
+                c < NST || mbar_wait_bounded(bar(kEmpty0 + st), (uint32_t)((c - NST) / NST) & 1u, kPWaitPolls);
             if (named_sync_or(kBarTok, kPRows, !w || *fail != 0)) {
                 ok = w;
                 break;
@@ -549,7 +750,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 F[PL::GG + lt] = g;
                 F[PL::BET + lt] = be;
                 F[PL::GAM + lt] = gm;
-                F[PL::CEND + lt] = ce;
+                F[PL::CEND + lt] = ce;  // q and k are normalised here: the factors rk = rq = 1
+                F[PL::GK + lt] = gm;
+                F[PL::GQ + lt] = gm;
             }
             // v of the block's rows, per token
 #pragma unroll
@@ -577,8 +780,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) split_pair(x[e].x * rn, x[e].y * rn, hw[e], lw[e]);
                 const int hrow = j;  // k_t: row t; q_t: row C + t (j = C + t)
-                *reinterpret_cast<uint4*>(KQ + sw128(kPRows, hrow, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(KQ + sw128(kPRows, hrow + 2 * C, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4*>(KQ + sw128(PL::KQR, hrow, vc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(KQ + sw128(PL::KQR, hrow + 2 * C, vc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             fence_proxy_async_smem();  // the rows are read by the tensor cores
             named_sync(kBarTok, kPRows);
@@ -636,7 +839,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     wv[s] = (isq ? s <= t : s < t) ? G * full : 0.f;
                 }
                 if (isq) {  // row t of KQw in bf16 hi / lo, K-major rows of 128 bytes (the O product's B)
-                    unsigned char* kb = sm + PL::KQB_OFF + buf * PL::KQB_BYTES;
+                    unsigned char* kb = sm + PL::KQB_OFF + (size_t)st * PL::KQB_BYTES;
 #pragma unroll
                     for (int j8 = 0; j8 < C / 8; ++j8) {
                         uint32_t hw[4], lw[4];
@@ -652,7 +855,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int s = 0; s < C; ++s) dst[s * C] = wv[s];
                 }
             }
-            mbar_arrive(bar(kFull0 + buf));  // after this thread's writes of the chunk
+            mbar_arrive(bar(kFull0 + st));  // after this thread's writes of the chunk
         }
         if (!ok && lt == 0) {
             *fail = 1;
@@ -670,48 +873,71 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kPCols);
 }
 
-template <int DK, typename InT, typename StT>
-cudaError_t launch_dk(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
-                      int n_tokens, cudaStream_t s) {
-    using PL = PrefillChunkPlan<DK>;
-    auto kernel = gdn_prefill_chunked_kernel<DK, InT, StT>;
+// A token-major tensor [n_tokens][heads][cols] (bf16 or fp32) as a 3-D tensor map with box (bx, 1, kPC): bx columns
+// of one head for a chunk of tokens; the 128-byte swizzle for operand rows of 64 bf16, none otherwise.  False when
+// the driver's encoder is missing or refuses the layout.
+bool encode_tokens_map(CUtensorMap* map, const void* ptr, bool bf16, int cols, int heads, int n_tokens, int bx,
+                       bool swizzle128) {
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t esz = bf16 ? 2 : 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)n_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * esz, (cuuint64_t)heads * cols * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)bx, 1, (cuuint32_t)kPC};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TokenMaps {
+    CUtensorMap o, k, q, v;
+    int o_tma;
+};
+
+template <int DK, typename InT, typename StT, bool kTma>
+cudaError_t launch_variant(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                           int n_tokens, const TokenMaps& m, cudaStream_t s) {
+    using PL = PrefillChunkPlan<DK, kTma>;
+    auto kernel = gdn_prefill_chunked_kernel<DK, InT, StT, kTma>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     // the shared-memory attribute is per device: set once for each
     static std::atomic<uint64_t> ready{0};
-    if (dev < 64 && !(ready.load(std::memory_order_acquire) >> dev & 1u)) {
+    if (dev >= 64 || !(ready.load(std::memory_order_acquire) >> dev & 1u)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::BYTES);
         if (e != cudaSuccess) return e;
-        ready.fetch_or(1ull << dev, std::memory_order_acq_rel);
-    } else if (dev >= 64) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::BYTES);
-        if (e != cudaSuccess) return e;
+        if (dev < 64) ready.fetch_or(1ull << dev, std::memory_order_acq_rel);
     }
     const int NRB = (p.DV + kPRows - 1) / kPRows;
     const int64_t items = (int64_t)B * p.HV * NRB;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;
-    // o as a 3-D tensor [n_tokens][HV][DV] for the per-chunk TMA store (box: 128 rows of one head, 32 tokens);
-    // when o is not in 16-byte pieces, DV < 128 or the map cannot be made, the kernel copies or stores per token
-    CUtensorMap omap;
-    std::memset(&omap, 0, sizeof omap);
-    int o_tma = 0;
+    kernel<<<(unsigned)items, kPThreads, PL::BYTES, s>>>(p, cu_seqlens, has_init, n_tokens, m.o, m.k, m.q, m.v,
+                                                         m.o_tma);
+    return cudaGetLastError();
+}
+
+template <int DK, typename InT, typename StT>
+cudaError_t launch_dk(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
+                      int n_tokens, cudaStream_t s) {
+    TokenMaps m;
+    std::memset(&m, 0, sizeof m);
+    // o: one TMA store per whole chunk when o is in 16-byte pieces and DV >= 128 (else per-token copies or stores)
     const uint64_t osz = p.out_bf16 ? 2 : 4;
     if ((reinterpret_cast<uintptr_t>(p.o) & 15u) == 0 && ((uint64_t)p.DV * osz) % 16 == 0 && p.DV >= kPRows &&
-        n_tokens > 0) {
-        const EncodeTiledFn fn = encode_tiled_fn();
-        if (fn != nullptr) {
-            const cuuint64_t dims[3] = {(cuuint64_t)p.DV, (cuuint64_t)p.HV, (cuuint64_t)n_tokens};
-            const cuuint64_t strides[2] = {(cuuint64_t)p.DV * osz, (cuuint64_t)p.HV * p.DV * osz};
-            const cuuint32_t box[3] = {(cuuint32_t)kPRows, 1, (cuuint32_t)kPC};
-            const cuuint32_t estr[3] = {1, 1, 1};
-            o_tma = fn(&omap, p.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.o,
-                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-        }
+        n_tokens > 0)
+        m.o_tma = encode_tokens_map(&m.o, p.o, p.out_bf16 != 0, p.DV, p.HV, n_tokens, kPRows, false);
+    // bf16 q, k, v: the loads by TMA (q and k are 16-byte aligned by the interface's rules)
+    if constexpr (std::is_same<InT, __nv_bfloat16>::value) {
+        if (p.v_vec && p.DV >= kPRows && n_tokens > 0 &&
+            encode_tokens_map(&m.k, p.k, true, DK, p.HK, n_tokens, 64, true) &&
+            encode_tokens_map(&m.q, p.q, true, DK, p.HK, n_tokens, 64, true) &&
+            encode_tokens_map(&m.v, p.v, true, p.DV, p.HV, n_tokens, kPRows, false))
+            return launch_variant<DK, InT, StT, true>(p, cu_seqlens, has_init, B, n_tokens, m, s);
     }
-    kernel<<<(unsigned)items, kPThreads, PL::BYTES, s>>>(p, cu_seqlens, has_init, n_tokens, omap, o_tma);
-    return cudaGetLastError();
+    return launch_variant<DK, InT, StT, false>(p, cu_seqlens, has_init, B, n_tokens, m, s);
 }
 
 template <typename InT, typename StT>

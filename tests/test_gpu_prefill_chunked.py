@@ -1,7 +1,9 @@
 """The chunked tensor-core form of gdn_prefill (DK = 64 and 128) against the CPU oracle, through the C ABI.
 
-The form works in chunks of 32 tokens with the state in fp32 for the whole sequence, so the cases aim at what it
-adds over the token loop: lengths on either side of every chunk boundary (1, 31, 32, 33, 63, 64, 65, 97, 130), a
+The form works in chunks of 32 tokens with the state in fp32 for the whole sequence; bf16 q, k, v with DV >= 128
+arrive by TMA (raw rows, normalisation as per-token factors), everything else through the token group's own
+loads (normalised hi / lo rows), and both ways are covered.  The cases aim at what the form adds over the token
+loop: lengths on either side of every chunk boundary (1, 31, 32, 33, 63, 64, 65, 97, 130), a
 second block of state rows that is only partly used (DV = 200), sequences of some thousand tokens (error
 accumulation over a hundred chunks, fp32 state at the 1e-4 bound), and the decay extremes of the gates: g = 0
 (gamma underflows inside the first chunk: every token starts from zero), g = 1 and beta = 0 (pure decay, here no
@@ -30,8 +32,8 @@ def run_and_compare(pw, x, has_init=True):
     return compare_prefill(pw, x, host(o), host(t["pool"]), before, has_init=has_init), host(t["pool"])
 
 
-@pytest.mark.parametrize("DK,qkv,state", [(128, "bf16", "bf16"), (128, "bf16", "f32"), (64, "f32", "bf16"),
-                                          (64, "f32", "f32")])
+@pytest.mark.parametrize("DK,qkv,state", [(128, "bf16", "bf16"), (128, "bf16", "f32"), (64, "bf16", "bf16"),
+                                          (64, "f32", "bf16"), (64, "f32", "f32"), (128, "f32", "bf16")])
 def test_chunk_boundaries(DK, qkv, state):
     lengths = [1, 31, 32, 33, 0, 63, 64, 65, 97, 130]
     pw = small(f"pc_bounds_dk{DK}_{qkv}_{state}", lengths, DK=DK, DV=128, HK=2, HV=4, qkv=qkv, state=state,
