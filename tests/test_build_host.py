@@ -22,8 +22,8 @@ TIMED = [
     ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li2E", 0),          # one-pass step
     ("gdn_recurrent_f32.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16fLi16E", 0),       # decode fp32
     ("gdn_prefill.cu", "gdn_prefill_kernelILi256E13__nv_bfloat16S1_E", 0),                        # prefill token loop (DK 16, 32, 256)
-    ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128E13__nv_bfloat16S2_E", 0),        # prefill
-    ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128EffE", 0),                        # prefill fp32
+    ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128E13__nv_bfloat16S2_Lb1E", 0),     # prefill (TMA)
+    ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128EffLb0E", 0),                     # prefill fp32
     ("gdn_gated_norm.cu", "gdn_gated_rmsnorm_reg_kernel", 0),                                    # gated norm
 ]
 
