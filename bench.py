@@ -38,6 +38,7 @@ import gdn_workloads as W  # noqa: E402
 METRIC = "GDN verify tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/4/8"
 PREFILL_NAMED = {"prefill8k": W.prefill_8k, "prefill_mix": W.prefill_mix}
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent_launch.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_verify_chunked.cuh",
@@ -146,6 +147,17 @@ def commit_bytes(w: W.Workload, A: int, accepted_tokens: int = 0) -> int:
 
 
 # ---- peaks, traffic, clocks -------------------------------------------------------------------------------
+def tensor_peak():
+    """Dense bf16 tensor peak for a kernel timed on its own (the burst figure)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS bf16 GEMM, burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -157,6 +169,8 @@ def hbm_peak():
 
 
 PREFILL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_prefill.cu",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_prefill_chunked.cu",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_tcgen05.cuh",
                    "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
                    "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh"]
 NORM_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_gated_norm.cu"]
@@ -712,6 +726,43 @@ FP32_LANES_PER_SM = 128  # FP32 FMA lanes per Blackwell SM
 PREFILL_FLOPS_PER_ELEM = 7  # per state element and token: decay 1, S.kh 2, rank-1 update 2, S.qh 2
 
 
+PREFILL_CHUNK = 32  # tokens per chunk of the chunked prefill
+
+
+def prefill_is_chunked(pw) -> bool:
+    return pw.DK in (64, 128)
+
+
+def prefill_mma_flops(pw, x):
+    """tcgen05 MMA flops the chunked prefill issues per launch on its TMA path (bf16 q, k, v, DV >= 128), counted
+    from the MMA shapes: per item (sequence, value head, block of 128 state rows) and chunk of 32 tokens,
+    P = S_0 hi and lo against [k; q] (2 x 2*128*64*DK), the Gram product [k; q][k; q]^T (2*128*64*DK, M = 128),
+    O = delta KQw^T in three part products (3 x 2*128*32*32), the update in two (2 x 2*128*DK*32).  None
+    elsewhere (the token loop, or the chunked kernel's other token path)."""
+    if not prefill_is_chunked(pw) or pw.qkv_dtype != "bf16" or pw.DV < 128:
+        return None
+    per = 2 * 2 * 128 * 64 * pw.DK + 2 * 128 * 64 * pw.DK + 3 * 2 * 128 * 32 * 32 + 2 * 2 * 128 * pw.DK * 32
+    lens = np.diff(x["cu_seqlens"])[x["indices"] >= 0]
+    chunks = int(((lens + PREFILL_CHUNK - 1) // PREFILL_CHUNK).sum())
+    return float(per) * chunks * pw.HV * ((pw.DV + 127) // 128)
+
+
+def prefill_bytes(pw, x) -> float:
+    """What the prefill must move: q, k, v, a, b in and o out for every active token, the state read (sequences with
+    an initial state) and written (every active sequence)."""
+    isz = 2 if pw.qkv_dtype == "bf16" else 4
+    osz = 2 if pw.out_dtype == "bf16" else 4
+    ssz = 2 if pw.state_dtype == "bf16" else 4
+    act = x["indices"] >= 0
+    lens = np.diff(x["cu_seqlens"])
+    tokens = int(lens[act].sum())
+    nseq = int((act & (lens > 0)).sum())
+    nread = int((act & (lens > 0) & (x["has_initial_state"] != 0)).sum())
+    per_tok = (2 * pw.HK * pw.DK + pw.HV * pw.DV + 2 * pw.HV) * isz + pw.HV * pw.DV * osz
+    state = pw.HV * pw.DV * pw.DK * ssz
+    return float(tokens * per_tok + (nseq + nread) * state)
+
+
 def alu_peak_tflops(sms: int, mhz: float) -> float:
     """FP32 FMA peak of the CUDA cores (not the tensor cores): SMs x 128 lanes x 2 flops x clock."""
     return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
@@ -849,10 +900,36 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
     props = torch.cuda.get_device_properties(device)
     clocks = sampler.summary()
     max_mhz = clocks.get("sm_max_mhz") or 2070.0
-    peak = alu_peak_tflops(props.multi_processor_count, max_mhz)
     avg_us = statistics.mean(ms) * 1e3
     flops = PREFILL_FLOPS_PER_ELEM * pw.DV * pw.DK * pw.HV * active_tokens
     achieved = flops / (avg_us * 1e-6) / 1e12
+    if prefill_is_chunked(pw):
+        # the chunked kernel: contractions on the tensor cores; the method's flops against the bf16 tensor peak,
+        # with the MMA flops it issues and the HBM fraction of what it must move beside them
+        peak, peak_src = tensor_peak()
+        mma = prefill_mma_flops(pw, x)
+        pb = prefill_bytes(pw, x)
+        hbm, hbm_src = hbm_peak()
+        roof = {"kernel": "gdn_prefill_chunked_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us,
+                "mma_flops_per_launch": mma,
+                "mma_tflops": None if mma is None else mma / (avg_us * 1e-6) / 1e12,
+                "mma_frac": None if mma is None else mma / (avg_us * 1e-6) / 1e12 / peak,
+                "hbm": {"algorithmic_bytes_per_launch": pb, "achieved_gbs": pb / (avg_us * 1e-6) / 1e9,
+                        "peak_gbs": hbm, "frac": pb / (avg_us * 1e-6) / 1e9 / hbm, "peak_source": hbm_src},
+                "limited_by": "the chain of chunks of each (sequence, head): one CTA per SM works through its item's "
+                              "32-token chunks in order, so the per-chunk latency, not a unit's throughput, sets the "
+                              "time",
+                "traffic": recorded_traffic("prefill", pw.name, PREFILL_SOURCES)}
+    else:
+        peak = alu_peak_tflops(props.multi_processor_count, max_mhz)
+        roof = {"kernel": "gdn_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"derived: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                               f"flops x {max_mhz:.0f} MHz (maximum SM clock)",
+                "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us,
+                "traffic": recorded_traffic("prefill", pw.name, PREFILL_SOURCES)}
     result = {
         "metric": PREFILL_METRIC, "value": tokens_all / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "timed_steps": n_timed, "warmup": args.warmup, "ms_per_step": total_ms / n_timed,
@@ -869,12 +946,7 @@ def run_prefill_arm(args, pw, rank: int, world: int, local_rank: int):
                              f"{args.min_seconds:g} s of device time); max over ranks",
                    "e2e": "inputs copied in from pinned host memory and o copied back on the compute stream, "
                           "per step, not overlapped"},
-        "roofline": {"kernel": "gdn_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"derived: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
-                                    f"flops x {max_mhz:.0f} MHz (maximum SM clock)",
-                     "algorithmic_flops_per_launch": flops, "avg_launch_us": avg_us,
-                     "traffic": recorded_traffic("prefill", pw.name, PREFILL_SOURCES)},
+        "roofline": roof,
         "e2e": {"value": sum_over_ranks(active_tokens, dist, device) / (e2e_ms_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "gpu_launches": n_timed, "clocks": clocks, "device": props.name,

@@ -7,6 +7,7 @@ import socket
 import sys
 from contextlib import redirect_stdout
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -228,3 +229,20 @@ def test_fused_step_bytes_and_kernel():
     p = W.previous_step(w)
     assert p["k"].shape == (128, 4, 16, 128) and p["accept_len"].min() >= 1 and p["accept_len"].max() <= 4
     assert not (p["k"] == w.small_arrays()["k"]).all()  # its own draws
+
+
+def test_prefill_roofline_counts():
+    """The chunked prefill's MMA flops and algorithmic bytes, recomputed by hand on two sequences (40 and 0 tokens
+    of an active lane, 33 tokens of a padded one): two chunks of one item per head for the first, none for the
+    others; bytes of the 40 tokens and one state written and read (it has an initial state)."""
+    import bench
+    pw = W.PrefillWorkload("t", B=3, HK=1, HV=2, DK=128, DV=128, num_slots=4, qkv_dtype="bf16", state_dtype="bf16",
+                           out_dtype="bf16", seed=1, lengths=(40, 0, 33), fresh_fraction=0.0)
+    x = pw.small_arrays()
+    x["indices"] = np.array([2, 0, -1], np.int32)
+    per_chunk = 2 * 2 * 128 * 64 * 128 + 2 * 128 * 64 * 128 + 3 * 2 * 128 * 32 * 32 + 2 * 2 * 128 * 128 * 32
+    assert bench.prefill_mma_flops(pw, x) == per_chunk * 2 * 2
+    per_tok = (2 * 128 + 2 * 128 + 2 * 2) * 2 + 2 * 128 * 2
+    assert bench.prefill_bytes(pw, x) == 40 * per_tok + 2 * (2 * 128 * 128 * 2)
+    assert bench.prefill_mma_flops(pw.replace(qkv_dtype="f32"), x) is None  # the other token path: not counted
+    assert not bench.prefill_is_chunked(pw.replace(DK=256))
