@@ -42,6 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_recurrent_launch.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_verify_chunked.cuh",
+                  "gated_deltanet_linear_mtp_gb300/csrc/gdn_tcgen05.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh",
                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_commit.cu"]
 

@@ -512,6 +512,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         auto issue_tma = [&](int cc) {
             const int sg = cc % NST;
             const uint32_t tb = bar(kTmaBar0 + sg), kqs = kq_addr(sg);
+            tma_issued = cc + 1;
+#ifdef GDN_TEST_MISSING_COPY
+            // test build: the first chunk of the first item is never loaded nor arrived on: its wait runs out
+            if (item == 0 && cc == 0) return;
+#endif
             mbar_arrive_expect_tx(tb, kTmaBytes);
 #pragma unroll
             for (int j = 0; j < DK / 64; ++j) {
@@ -519,7 +524,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tma_load_3d(kqs + (uint32_t)j * PL::BOX + C * 128u, &qmap, 64 * j, hk, lo + cc * C, tb);
             }
             tma_load_3d(base + PL::VT_OFF + (uint32_t)sg * PL::VT_BYTES, &vmap, rb * kPRows, h, lo + cc * C, tb);
-            tma_issued = cc + 1;
         };
         if (lt == 0) {
             issue_tma(0);

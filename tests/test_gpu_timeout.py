@@ -75,3 +75,29 @@ def test_wait_that_runs_out_sets_the_timeout_bit(timeout_lib, monkeypatch, case)
     assert int(err.item()) == 0
     lanes = np.flatnonzero(x["indices"] >= 0)[:4]
     compare_verify(w, x, host(o), host(cache) if cache is not None else None, lanes=lanes)
+
+
+def test_chunked_prefill_wait_that_runs_out(timeout_lib, monkeypatch):
+    """The chunked prefill (bf16 tokens by TMA): the first chunk of its first item is never loaded, so the token
+    group's wait for it runs out, and then the row group's wait for that chunk; the bit is set, the CTA drains
+    the loads it did issue and ends, and the product library then prefills the batch correctly."""
+    from test_gpu_prefill import compare_prefill, run_prefill, small
+    pw = small("timeout_prefill", [70, 40], DK=128, DV=128, HK=1, HV=2, seed=23, fresh=0.0)
+    x = pw.arrays()
+    t = Dev(x)
+    before = host(t["pool"])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call():  # into a copy of the pool: the product run below starts from the untouched one
+        tt = {k: t[k] for k in x}
+        tt["pool"] = t["pool"].clone()
+        run_prefill(pw, tt, err)
+        torch.cuda.synchronize()
+
+    run_with(timeout_lib, monkeypatch, call)
+    assert int(err.item()) & gdn.ERRBIT_TIMEOUT, "the wait did not report running out"
+    err.zero_()
+    o = run_prefill(pw, t, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    compare_prefill(pw, x, host(o), host(t["pool"]), before)

@@ -2,10 +2,10 @@
 verifies this call's tokens from the committed states.
 
 Checked against the oracle as the composition the call defines: the oracle's replay commit of the earlier tokens
-into a copy of the pool, then the oracle's verify of the new tokens from that pool.  On the one-pass path (bf16
-pool, both token counts <= 8, DK >= 64) the result must also equal, bit for bit, the two separate GPU calls
-gdn_commit_replay + gdn_mtp_verify (the same arithmetic, the committed rows read from the tile instead of the
-pool).  Outside that path the call runs those two calls itself."""
+into a copy of the pool, then the oracle's verify of the new tokens from that pool.  The result must also equal,
+bit for bit, the two separate GPU calls gdn_commit_replay + gdn_mtp_verify: on the one-pass path (bf16 pool, both
+token counts <= 4, DK >= 64) by the same arithmetic with the committed rows read from the tile instead of the
+pool, and outside it because the call runs those two calls itself."""
 from __future__ import annotations
 
 import os
@@ -93,10 +93,6 @@ def bits(a: np.ndarray) -> np.ndarray:
     return a.view(np.uint32) if a.dtype == np.float32 else a
 
 
-def one_pass(w, Tp) -> bool:
-    return w.state_dtype == "bf16" and w.T <= 8 and Tp <= 8 and w.DK >= 64
-
-
 def oracle_verify_from(w, x, pool, lanes, chunk=16):
     """The oracle's verify of x's tokens from a given pool (the one the GPU committed)."""
     orc = oracle.default()
@@ -140,6 +136,7 @@ def small(name, B=5, T=3, HK=2, HV=4, DK=64, DV=40, num_slots=11, state="bf16", 
                       pool_std=0.1, pad_fraction=pad)
 
 
+# the one-pass kernel takes a bf16 pool, DK >= 64 and both token counts <= 4; the other cases run the two calls
 CASES = [
     (small("vc_dk64_dv40_T3_Tp2"), 2, 0.2),
     (small("vc_dk128_dv200_T4_Tp4", DK=128, DV=200, B=6, T=4, seed=41), 4, 0.3),
@@ -148,7 +145,6 @@ CASES = [
     (small("vc_dk256_dv64_T2_Tp5", DK=256, DV=64, T=2, seed=44), 5, 0.2),
     (small("vc_f32in_dk128_T3_Tp3", DK=128, DV=96, qkv="f32", out="f32", seed=45), 3, 0.2),
     (small("vc_hv_8x_hk", HK=1, HV=8, DK=128, DV=128, T=4, seed=46), 3, 0.0),
-    # outside the one-pass path: the two calls back to back
     (small("vc_f32state_T2_Tp3", state="f32", out="f32", qkv="f32", seed=47), 3, 0.2),
     (small("vc_dk32_bf16", DK=32, DV=33, seed=48), 2, 0.2),
     (small("vc_T12_Tp3", DK=128, DV=64, T=12, seed=49), 3, 0.0),
