@@ -246,22 +246,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t blk_bytes = (uint32_t)min(kPRows, p.DV - rb * kPRows) * osz;
         const int64_t tok_out = (int64_t)p.HV * p.DV;
         auto emit_o = [&](int cc) {
+            if (o_bulk) {  // 16 tokens at a time, not unrolled (less code beside the other warp group's)
+                unsigned char* ob = sm + PL::OB_OFF + (cc & 1) * PL::OB_BYTES;
+#pragma unroll 1
+                for (int t0 = 0; t0 < C; t0 += 16) {
+                    float oh[16];
+                    tmem_ld16(lane_base + PL::O_COL + t0, oh);
+                    tmem_wait_ld();
+                    if (p.out_bf16) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            reinterpret_cast<__nv_bfloat16*>(ob)[(t0 + t) * kPRows + lt] =
+                                __float2bfloat16_rn(p.scale * oh[t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) reinterpret_cast<float*>(ob)[(t0 + t) * kPRows + lt] = p.scale * oh[t];
+                    }
+                }
+                fence_proxy_async_smem();  // read by the bulk copies
+                return;
+            }
             float ov[C];
             tmem_ld16(lane_base + PL::O_COL, ov);
             tmem_ld16(lane_base + PL::O_COL + 16, ov + 16);
             tmem_wait_ld();
-            if (o_bulk) {
-                unsigned char* ob = sm + PL::OB_OFF + (cc & 1) * PL::OB_BYTES;
-                if (p.out_bf16) {
-#pragma unroll
-                    for (int t = 0; t < C; ++t)
-                        reinterpret_cast<__nv_bfloat16*>(ob)[t * kPRows + lt] = __float2bfloat16_rn(p.scale * ov[t]);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < C; ++t) reinterpret_cast<float*>(ob)[t * kPRows + lt] = p.scale * ov[t];
-                }
-                fence_proxy_async_smem();  // read by the bulk copies
-            } else if (live) {
+            if (live) {
                 const int len = min(C, n - cc * C);
                 const int64_t o0 = ((int64_t)(lo + cc * C) * p.HV + h) * p.DV + row;
                 if (p.out_bf16) {
@@ -312,13 +321,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tmem_ld16(lane_base + PL::S_COL, f[0]);
                 tmem_ld16(lane_base + PL::S_COL + 16, f[0] + 16);
                 tmem_wait_ld();
+                // a loop over pairs of blocks, not unrolled: the two warp groups' code shares each scheduler's
+                // instruction cache, and instruction fetch was the leading stall (measured 4% faster)
+#pragma unroll 1
+                for (int jp = 0; jp < DK / 32; jp += 2)
 #pragma unroll
-                for (int jb = 0; jb < DK / 32; ++jb) {
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int jb = jp + jj;
                     const int c0 = 32 * jb;
-                    float(&x)[32] = f[jb & 1];
+                    float(&x)[32] = f[jj];
                     if (jb + 1 < DK / 32) {
-                        tmem_ld16(lane_base + PL::S_COL + c0 + 32, f[(jb + 1) & 1]);
-                        tmem_ld16(lane_base + PL::S_COL + c0 + 48, f[(jb + 1) & 1] + 16);
+                        tmem_ld16(lane_base + PL::S_COL + c0 + 32, f[jj ^ 1]);
+                        tmem_ld16(lane_base + PL::S_COL + c0 + 48, f[jj ^ 1] + 16);
                     }
                     uint32_t hw[16], lw[16], sw[32];
                     const float2 g2 = make_float2(gend, gend), m1 = make_float2(-1.f, -1.f);
