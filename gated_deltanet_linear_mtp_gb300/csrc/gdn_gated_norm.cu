@@ -55,7 +55,10 @@ __device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&f)[8]) {
     *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+// silu on CUDA's fast exponential and division intrinsics: a few ulp of fp32 (about 1e-6 relative for the gates'
+// range), far inside the norm's tolerance, and the limits hold (x -> -inf: e^-x overflows, the quotient is 0).  With
+// the IEEE forms the kernel was bound by issue, not by HBM (344 against 283 us per launch at 2M rows of 128).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 constexpr int kNormThreads = 256;
 
