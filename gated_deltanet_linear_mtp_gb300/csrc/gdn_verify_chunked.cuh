@@ -70,6 +70,9 @@ enum ChunkMode { kModeVerify = 0, kModeReplay = 1, kModeReplayVerify = 2 };
 template <int DK, int kMode, int NS>
 struct ChunkPlan {
     static_assert(DK % 64 == 0, "the chunked kernel takes whole 128-byte rows");
+    // the replay modes read a stage's slot and token count at the top of an item, before that item's refill: the
+    // tile (and its slot) must have been issued an item earlier, so they need two stages at least
+    static_assert(kMode == kModeVerify ? NS >= 1 : NS >= 2, "stages of the chunked kernel");
     static constexpr bool kReplay = kMode != kModeVerify;
     static constexpr bool kVerify = kMode != kModeReplay;
     static constexpr int NBOX = DK / 64;                      // 64-column (128-byte) boxes per row
@@ -899,23 +902,35 @@ cudaError_t encode_pool_map(CUtensorMap* map, void* pool, const RecurrentParams&
 #define GDN_CHUNK_STAGES 2
 #endif
 constexpr int kChunkStages = GDN_CHUNK_STAGES;
+// verify alone may run on other settings (its stage is free once its P product has completed): stages and the most
+// groups per CTA
+#ifndef GDN_VERIFY_STAGES
+#define GDN_VERIFY_STAGES GDN_CHUNK_STAGES
+#endif
+#ifndef GDN_VERIFY_GROUPS
+#define GDN_VERIFY_GROUPS 3
+#endif
+template <int kMode>
+constexpr int chunk_stages() {
+    return kMode == kModeVerify ? GDN_VERIFY_STAGES : kChunkStages;
+}
 constexpr int kChunkCachedDevices = 64;  // devices whose launch settings are cached
 constexpr uint32_t kChunkMaxSmem = 227 * 1024;  // dynamic shared memory a CTA may open
 
-// groups per CTA: as many as the shared memory of T = 8 (in every token set of the mode) allows, up to
-// kChunkMaxGroups
+// groups per CTA: as many as the shared memory of T = 8 (in every token set of the mode) and the tensor memory
+// allow, up to kChunkMaxGroups (verify alone: GDN_VERIFY_GROUPS)
 template <int DK, int kMode, int NS>
 constexpr int chunk_groups() {
     using CS = ChunkPlan<DK, kMode, NS>;
-    for (int g = kChunkMaxGroups; g > 1; --g)
-        if (CS::max_bytes(g) <= kChunkMaxSmem) return g;
+    for (int g = kMode == kModeVerify ? GDN_VERIFY_GROUPS : kChunkMaxGroups; g > 1; --g)
+        if (CS::max_bytes(g) <= kChunkMaxSmem && g * CS::tmem_cols() <= 512) return g;
     return 1;
 }
 
 // grid = min(items, SMs x resident CTAs) CTAs of G groups, each group a contiguous range of items
 template <int DK, typename InT, int kMode, int G>
 cudaError_t launch_chunked_groups(const RecurrentParams& p, int B, int Tr, int Tv, cudaStream_t s) {
-    constexpr int NS = kChunkStages;
+    constexpr int NS = chunk_stages<kMode>();
     using CS = ChunkPlan<DK, kMode, NS>;
     auto kernel = gdn_verify_chunked_kernel<DK, InT, kMode, NS, G>;
     const uint32_t smem = CS::bytes(Tr, Tv, G);
@@ -958,7 +973,7 @@ cudaError_t launch_chunked_groups(const RecurrentParams& p, int B, int Tr, int T
 // The group count: as many as the largest token counts of the mode allow.
 template <int DK, typename InT, int kMode>
 cudaError_t launch_chunked(const RecurrentParams& p, int B, cudaStream_t s) {
-    constexpr int NS = kChunkStages;
+    constexpr int NS = chunk_stages<kMode>();
     constexpr int G = chunk_groups<DK, kMode, NS>();
     using CS = ChunkPlan<DK, kMode, NS>;
     static_assert(CS::max_bytes(G) <= kChunkMaxSmem, "shared memory of one group");
