@@ -5,6 +5,7 @@ Argument marshalling only: every step of the computation runs in the library's C
 library has not been built, every call raises.
 
     gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word=None, scale=1.0, l2_eps=1e-6)
+    gdn_decode_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, norm, err_word=None, ...)
     gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None, ...)
     gdn_commit(state_pool, state_indices, intermediate_states, accept_len, err_word=None)
     gdn_commit_replay(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, accept_len, err_word=None, ...)
@@ -30,7 +31,7 @@ from typing import Optional
 
 from .build import LIB_PATH
 
-__all__ = ["gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "ReplayTokens",
+__all__ = ["gdn_decode", "gdn_decode_gated", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "ReplayTokens",
            "gdn_mtp_verify_gated", "GatedNorm",
            "gdn_prefill", "gdn_gated_rmsnorm", "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
            "ERRBIT_SEQLEN", "MAX_T", "EXPORTS"]
@@ -43,8 +44,8 @@ ERRBIT_TIMEOUT = 4
 ERRBIT_SEQLEN = 8
 MAX_T = 16
 F32, BF16 = 0, 1
-EXPORTS = ("gdn_decode", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit",
-           "gdn_mtp_verify_gated", "gdn_prefill",
+EXPORTS = ("gdn_decode", "gdn_decode_gated", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay",
+           "gdn_mtp_verify_commit", "gdn_mtp_verify_gated", "gdn_prefill",
            "gdn_gated_rmsnorm", "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
 
 
@@ -103,6 +104,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, dp, ip = ctypes.c_void_p, ctypes.POINTER(GdnDims), ctypes.c_void_p
         L.gdn_decode.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, ip, vp]
+        L.gdn_decode_gated.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, ctypes.POINTER(_GatedNormC), ip, vp]
         L.gdn_mtp_verify.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, vp, vp, ip, vp]
         L.gdn_commit.argtypes = [dp, vp, ip, vp, ip, ip, vp]
         L.gdn_commit_replay.argtypes = [dp] + [vp] * 5 + [vp, vp, vp, ip, ip, ip, vp]
@@ -112,7 +114,7 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp, ip, vp]
         L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
                                         ctypes.c_float, vp, vp]
-        for f in (L.gdn_decode, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_mtp_verify_commit,
+        for f in (L.gdn_decode, L.gdn_decode_gated, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_mtp_verify_commit,
                   L.gdn_mtp_verify_gated, L.gdn_prefill, L.gdn_gated_rmsnorm):
             f.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
@@ -247,6 +249,22 @@ def gdn_decode(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_
             (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
              _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
              _dev(state_indices, "state_indices"), _dev(o, "o"), _dev(err_word, "err_word")), "gdn_decode")
+
+
+def gdn_decode_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, norm, err_word=None, *,
+                     scale=1.0, l2_eps=1e-6, stream=None) -> None:
+    """``gdn_decode`` (o and the write-back) and the gated RMSNorm of o into ``norm.y`` (``norm``: a GatedNorm), in
+    the same launch where the CTAs of a head fit one thread-block cluster."""
+    L = lib()
+    d = _io_dims(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, scale, l2_eps)
+    nc = _norm_c(norm, o)
+    device = _common_device(_io_named(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices)
+                            + [("o", o), ("err_word", err_word)] + _norm_named(norm))
+    _launch(device, stream, L.gdn_decode_gated,
+            (ctypes.byref(d), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(a, "a"), _dev(b, "b"),
+             _dev(A_log, "A_log"), _dev(dt_bias, "dt_bias"), _dev(state_pool, "state_pool"),
+             _dev(state_indices, "state_indices"), _dev(o, "o"), ctypes.byref(nc), _dev(err_word, "err_word")),
+            "gdn_decode_gated")
 
 
 def gdn_mtp_verify(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, intermediate_states=None,

@@ -142,6 +142,7 @@ void set_norm(RecurrentParams& p, const gdn_gated_norm_out* n) {
     p.nw = n->norm_weight;
     p.ny = n->y;
     p.neps = n->eps;
+    p.nz_vec = p.DV % 8 == 0 && aligned(n->z, 16);
 }
 
 // the standalone norm of the stored o, rows of padded or invalid lanes left untouched
@@ -300,13 +301,39 @@ gdn_status gdn_mtp_verify_gated(const gdn_dims* dims, const void* q, const void*
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, nullptr, state_indices, nullptr, o,
                                     intermediate_states, err_word);
+    // the chunked kernel takes the norm when norm_fused says so, else a norm launch follows it; the token-by-token
+    // kernels take it themselves (in the same launch, a cluster per head, or with their own norm launch)
+    const bool chunked = dims->state_dtype == GDN_BF16 && intermediate_states == nullptr &&
+                         chunked_verify_eligible(dims->B, dims->T, dims->DK, dims->DV, dims->HV, dims->num_slots);
     const bool fused = norm_fused(dims, intermediate_states != nullptr);
-    if (fused) set_norm(p, norm);
+    if (fused || !chunked) set_norm(p, norm);
     const bool qkv_bf16 = dims->qkv_dtype == GDN_BF16;
     s = finish(dims->state_dtype == GDN_F32 ? launch_recurrent_f32state(p, dims->B, dims->DK, qkv_bf16, st)
                                             : launch_recurrent_bf16state(p, dims->B, dims->DK, qkv_bf16, st));
-    if (s != GDN_OK || fused) return s;
+    if (s != GDN_OK || fused || !chunked) return s;
     return run_norm(dims, norm, o, state_indices, st);
+}
+
+gdn_status gdn_decode_gated(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                            const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                            const int32_t* state_indices, void* o, const gdn_gated_norm_out* norm, int32_t* err_word,
+                            gdn_stream_t stream) {
+    gdn_status s = check_dims(dims, true);
+    if (s != GDN_OK) return s;
+    if (norm == nullptr) return GDN_ERR_NULL;
+    s = check_norm(dims, norm, o);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    if ((double)dims->B * dims->T * dims->HV > (double)gated_norm_max_rows()) return GDN_ERR_SHAPE;
+    s = check_io(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, o, err_word);
+    if (s != GDN_OK) return s;
+    RecurrentParams p = make_params(dims, q, k, v, a, b, A_log, dt_bias, state_pool, state_pool, state_indices, nullptr,
+                                    o, nullptr, err_word);
+    set_norm(p, norm);
+    const bool qkv_bf16 = dims->qkv_dtype == GDN_BF16;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return finish(dims->state_dtype == GDN_F32 ? launch_recurrent_f32state(p, dims->B, dims->DK, qkv_bf16, st)
+                                               : launch_recurrent_bf16state(p, dims->B, dims->DK, qkv_bf16, st));
 }
 
 gdn_status gdn_mtp_verify_commit(const gdn_dims* dims, const gdn_replay_tokens* prev, const void* q, const void* k,

@@ -37,13 +37,14 @@ struct RecurrentParams {
     const void* rv;
     const void* ra;
     const void* rb;
-    // gated RMSNorm of the stored o (chunked verify with DV <= 128): y = o / sqrt(mean(o^2) + neps) * nw * silu(nz)
-    // per (token, head) row of DV, y in o's type; nz == nullptr: none
+    // gated RMSNorm of the stored o (the chunked verify's and the token-by-token kernels' epilogue): y = o /
+    // sqrt(mean(o^2) + neps) * nw * silu(nz) per (token, head) row of DV, y in o's type; nz == nullptr: none
     const void* nz;
     const float* nw;
     void* ny;
     float neps;
     int nz_bf16;
+    int nz_vec;  // z starts on 16 bytes and DV % 8 == 0: z is gathered in 16-byte chunks
 };
 
 struct CommitParams {

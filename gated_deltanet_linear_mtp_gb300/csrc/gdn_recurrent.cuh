@@ -155,11 +155,14 @@ struct TokenPrologue {
 // S holds the block's state in registers; vs_blk points at v of token 0 for the block's first row, with a
 // token stride of vs_stride floats.  Stores the intermediate states, the outputs and the write-back that
 // the call asks for.
+// With the fused gated norm (osm != nullptr) the stored o of every row also goes to osm[t][row - cta_row0], rows of
+// the CTA in a stride of osm_rows.
 template <int DK, typename StT>
 __device__ __forceinline__ void run_tokens(const RecurrentParams& p, float2 (&S)[Split<DK>::RL][4],
                                            const LaneRows<DK>& lr, int b, int h, int r0, int slot, int steps, int pp,
                                            const float* qs, const float* ks, const float* vs_blk, int vs_stride,
-                                           const float* gs, const float* bs, const float* kqs) {
+                                           const float* gs, const float* bs, const float* kqs, float* osm = nullptr,
+                                           int osm_rows = 0, int cta_row0 = 0) {
     using SP = Split<DK>;
     using SL = Slice8<StT>;
     constexpr int RL = SP::RL;
@@ -185,10 +188,15 @@ __device__ __forceinline__ void run_tokens(const RecurrentParams& p, float2 (&S)
         }
         if (writes_o) {
             const float ov = p.scale * orow;
-            if (p.out_bf16)
-                static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = __float2bfloat16_rn(ov);
-            else
+            float stored = ov;
+            if (p.out_bf16) {
+                const __nv_bfloat16 ob = __float2bfloat16_rn(ov);
+                static_cast<__nv_bfloat16*>(p.o)[o0 + t * tok_out] = ob;
+                stored = __bfloat162float(ob);
+            } else {
                 static_cast<float*>(p.o)[o0 + t * tok_out] = ov;
+            }
+            if (osm != nullptr) osm[t * osm_rows + (r0 - cta_row0) + lr.own_row] = stored;
         }
     }
     // decode / replay-commit write-back, in place
@@ -215,13 +223,137 @@ __device__ __forceinline__ bool lane_work(const RecurrentParams& p, int slot, in
     return steps > 0;
 }
 
+// ---- the fused gated norm of the outputs --------------------------------------------------------------------
+// y = o / sqrt(mean over the head's DV rows of o^2 + eps) * w * silu(z) per (token, head), o as stored.  The CTAs
+// of one (lane, head) run as one thread-block cluster (grid.x of them, at most 8).  Every CTA shares the lane and the
+// head, so all of them take the same early exit or none.
+//   norm_begin     (after the lane check) arrives on the cluster barrier's first phase (this CTA has started: its
+//                  shared memory may be written by the others) and gathers the CTA's z rows into shared memory with
+//                  16-byte cp.async copies, which overlap the state load and the token loop;
+//   norm_epilogue  sums o^2 over the CTA's rows per token and stores the sums into every CTA's slot for this rank
+//                  (distributed shared memory), one barrier phase, then every CTA adds the ranks' sums in rank order
+//                  (all see the same value) and writes y for its rows.  No CTA touches another's shared memory after
+//                  that phase, so each may leave when it is done.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+constexpr int kNormMaxCluster = 8;  // CTAs of one head in a cluster at most (the portable cluster size)
+
+// The norm's shared memory after the kernel's own `base` bytes, for T tokens of `rows` rows:
+//   zs    [T][rows] z as given (bf16 or fp32; 4 bytes an element reserved), 16-byte aligned
+//   os    [T][rows] the stored o of the rows, fp32
+//   part  [kNormMaxCluster][GDN_MAX_T] every rank's sums of o^2 per token
+//   inv   [GDN_MAX_T] 1 / rms of the head per token
+struct NormSmem {
+    __host__ __device__ static size_t zs(size_t base) { return (base + 15) & ~(size_t)15; }
+    __host__ __device__ static size_t os(size_t base, int T, int rows) { return zs(base) + sizeof(float) * T * rows; }
+    __host__ __device__ static size_t part(size_t base, int T, int rows) {
+        return os(base, T, rows) + sizeof(float) * T * rows;
+    }
+    __host__ __device__ static size_t end(size_t base, int T, int rows) {
+        return part(base, T, rows) + sizeof(float) * (kNormMaxCluster + 1) * GDN_MAX_T;
+    }
+};
+
+// zs: the CTA's rows row0 .. row0 + rows - 1 of z for T tokens (chunks of rows past DV are not copied)
+__device__ __forceinline__ void norm_begin(const RecurrentParams& p, unsigned char* zs, int rows, int row0, int b,
+                                           int h, int T, int tid, int nt) {
+    cluster_arrive_relaxed();
+    if (!p.nz_vec) return;
+    const int zb = p.nz_bf16 ? 2 : 4;
+    const int zch = 16 / zb;  // elements per chunk; DV % 8 == 0 puts every chunk wholly inside or past DV
+    const int cpt = rows / zch;
+    const unsigned char* z = static_cast<const unsigned char*>(p.nz);
+    for (int i = tid; i < T * cpt; i += nt) {
+        const int t = i / cpt, c = i - t * cpt, row = row0 + c * zch;
+        if (row < p.DV)
+            cp_async16(zs + (size_t)(t * rows + c * zch) * zb,
+                       z + ((((int64_t)b * T + t) * p.HV + h) * p.DV + row) * zb);
+    }
+}
+
+// os: [T][rows] stored o of the CTA's rows row0 .. row0 + rows - 1; zs as norm_begin left it
+template <int NT>
+__device__ __forceinline__ void norm_epilogue(const RecurrentParams& p, const unsigned char* zs, const float* os,
+                                              float* part, int rows, int row0, int b, int h, int T, int tid) {
+    float* inv = part + kNormMaxCluster * GDN_MAX_T;
+    const int warp = tid >> 5, lane = tid & 31;
+    cp_async_commit_wait_all();
+    __syncthreads();      // every row's o and z are in place
+    cluster_wait_acquire();  // every CTA of the cluster has started
+    const uint32_t n = cluster_ctas(), me = cluster_rank();
+    for (int t = warp; t < T; t += NT / 32) {
+        float sq = 0.f;
+        for (int r = lane; r < rows; r += 32)
+            if (row0 + r < p.DV) sq = fmaf(os[t * rows + r], os[t * rows + r], sq);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        if ((uint32_t)lane < n) st_cluster_f32(part + me * GDN_MAX_T + t, (uint32_t)lane, sq);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();  // every rank's sums are in every CTA's part
+    if (tid < T) {
+        float tot = 0.f;
+        for (uint32_t r = 0; r < n; ++r) tot += part[r * GDN_MAX_T + tid];
+        inv[tid] = 1.f / sqrtf(tot / (float)p.DV + p.neps);
+    }
+    __syncthreads();
+    const int64_t tok_out = (int64_t)p.HV * p.DV;
+    for (int i = tid; i < T * rows; i += NT) {
+        const int t = i / rows, r = i - t * rows, row = row0 + r;
+        if (row >= p.DV) continue;
+        const int64_t off = ((int64_t)b * T + t) * tok_out + (int64_t)h * p.DV + row;
+        float zt;
+        if (p.nz_vec)
+            zt = p.nz_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(zs)[i])
+                           : reinterpret_cast<const float*>(zs)[i];
+        else
+            zt = p.nz_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.nz)[off])
+                           : static_cast<const float*>(p.nz)[off];
+        const float y = os[i] * inv[t] * p.nw[row] * (zt / (1.f + expf(-zt)));
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16*>(p.ny)[off] = __float2bfloat16_rn(y);
+        else
+            static_cast<float*>(p.ny)[off] = y;
+    }
+}
+
 template <int DK>
 __host__ __device__ inline size_t direct_smem_bytes(int T) {
     return sizeof(float) * TokenPrologue<DK, float, Split<DK>::RPC, Split<DK>::THREADS>::smem_floats(T);
 }
 
-template <int DK, typename InT, typename StT>
-__global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM)
+// (with the fused norm, one CTA per SM less of register budget: its epilogue's values would spill otherwise)
+template <int DK, typename InT, typename StT, bool kNorm = false>
+__global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM - (kNorm ? 1 : 0))
     gdn_recurrent_kernel(const RecurrentParams p) {
     using SP = Split<DK>;
     using SL = Slice8<StT>;
@@ -241,6 +373,9 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
     TokenPrologue<DK, InT, RPC, NT> pro;
     pro.prefetch(p, b, h, row0, tid);
     if (!lane_work(p, slot, steps, h, tid)) return;
+    extern __shared__ __align__(16) float smem[];
+    unsigned char* const norm_base = reinterpret_cast<unsigned char*>(smem);
+    if constexpr (kNorm) norm_begin(p, norm_base + NormSmem::zs(direct_smem_bytes<DK>(T)), RPC, row0, b, h, T, tid, NT);
 
     // state load, in the lane's register-slot order (LaneRows)
     const LaneRows<DK> lr(warp, rg, pp);
@@ -258,7 +393,6 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
         }
     }
 
-    extern __shared__ float smem[];
     float* qs = smem;          // [T][DK] normalised q, columns permuted by Split::kq_pos
     float* ks = qs + T * DK;   // [T][DK] normalised k, likewise
     float* vs = ks + T * DK;   // [T][RPC] v of this CTA's rows
@@ -271,7 +405,12 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
     float2 S[RL][4];
 #pragma unroll
     for (int s = 0; s < RL; ++s) SL::unpack(raw[s], S[s]);
-    run_tokens<DK, StT>(p, S, lr, b, h, row0, slot, steps, pp, qs, ks, vs, RPC, gs, bs, kqs);
+    const size_t nb = direct_smem_bytes<DK>(T);
+    float* osm = kNorm ? reinterpret_cast<float*>(norm_base + NormSmem::os(nb, T, RPC)) : nullptr;
+    run_tokens<DK, StT>(p, S, lr, b, h, row0, slot, steps, pp, qs, ks, vs, RPC, gs, bs, kqs, osm, RPC, row0);
+    if constexpr (kNorm)
+        norm_epilogue<NT>(p, norm_base + NormSmem::zs(nb), osm,
+                          reinterpret_cast<float*>(norm_base + NormSmem::part(nb, T, RPC)), RPC, row0, b, h, T, tid);
 }
 
 // ---- TMA-staged kernel ------------------------------------------------------------------------------------
@@ -296,10 +435,11 @@ struct Staged {
         return (end + 15u) & ~15u;
     }
     __host__ __device__ static uint32_t smem_bytes(int T) { return mbar_offset(T) + 8u * NSUB; }
+    __host__ __device__ static uint32_t norm_offset(int T) { return (smem_bytes(T) + 15u) & ~15u; }
 };
 
-template <int DK, typename InT, typename StT, int KIB>
-__global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_CTAS)
+template <int DK, typename InT, typename StT, int KIB, bool kNorm = false>
+__global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_CTAS - (kNorm ? 1 : 0))
     gdn_recurrent_staged_kernel(const RecurrentParams p) {
     using SP = Split<DK>;
     using SL = Slice8<StT>;
@@ -322,6 +462,8 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
     if (!lane_work(p, slot, steps, h, tid)) return;
 
     extern __shared__ __align__(16) unsigned char staged_smem[];
+    const size_t nb = ST::norm_offset(T);
+    if constexpr (kNorm) norm_begin(p, staged_smem + NormSmem::zs(nb), ROWS, row0, b, h, T, tid, NT);
     const uint32_t sbase = smem_u32(staged_smem);
     const uint32_t mbar0 = sbase + ST::mbar_offset(T);
     if (tid == 0) {
@@ -357,6 +499,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
     __syncthreads();
 
     const LaneRows<DK> lr(warp, rg, pp);
+    float* osm = kNorm ? reinterpret_cast<float*>(staged_smem + NormSmem::os(nb, T, ROWS)) : nullptr;
     bool failed = false;
     for (int sb = 0; sb < NSUB; ++sb) {
         const int r0 = row0 + sb * RPC;
@@ -372,9 +515,13 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
         float2 S[RL][4];
 #pragma unroll
         for (int s = 0; s < RL; ++s) SL::load_shared(tile + lr.row[s] * DK, S[s]);
-        run_tokens<DK, StT>(p, S, lr, b, h, r0, slot, steps, pp, qs, ks, vs + sb * RPC, ROWS, gs, bs, kqs);
+        run_tokens<DK, StT>(p, S, lr, b, h, r0, slot, steps, pp, qs, ks, vs + sb * RPC, ROWS, gs, bs, kqs, osm, ROWS,
+                            row0);
     }
     if (failed && lane == 0 && p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+    if constexpr (kNorm)
+        norm_epilogue<NT>(p, staged_smem + NormSmem::zs(nb), osm,
+                          reinterpret_cast<float*>(staged_smem + NormSmem::part(nb, T, ROWS)), ROWS, row0, b, h, T, tid);
 }
 
 }  // namespace gdn

@@ -17,6 +17,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <type_traits>
@@ -52,20 +53,102 @@ bool use_staged(const RecurrentParams& p, int B, int sms) {
     return ctas >= (int64_t)kStagedMinCtasPerSm * sms;
 }
 
+// A kernel whose CTAs of one (lane, head) run as a thread-block cluster of grid.x (the fused gated norm).
+template <typename Kernel>
+cudaError_t launch_head_cluster(Kernel kernel, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                                const RecurrentParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// The standalone gated norm of the outputs the kernel just stored (rows of padded or invalid lanes untouched):
+// the fused norm's fallback where a head spans more CTAs than one cluster takes, or the grid more than one wave.
+inline cudaError_t launch_norm_after(const RecurrentParams& p, int B, cudaStream_t s) {
+    auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    GatedNormParams g{};
+    g.o = p.o;
+    g.z = p.nz;
+    g.w = p.nw;
+    g.y = p.ny;
+    g.rows = (int64_t)B * p.T * p.HV;
+    g.DV = p.DV;
+    g.o_bf16 = p.out_bf16;
+    g.z_bf16 = p.nz_bf16;
+    g.vec = p.DV % 8 == 0 && a16(p.o) && a16(p.nz) && a16(p.ny) && a16(p.nw);
+    g.eps = p.neps;
+    g.lane_slot = p.indices;
+    g.rows_per_lane = (int64_t)p.T * p.HV;
+    g.num_slots = p.num_slots;
+    return launch_gated_norm(g, s);
+}
+
+// CTAs of `kernel` (threads, smem bytes each) resident on one SM, from the occupancy calculator; one cached answer
+// per kernel instance (its last smem size), 0 if the query failed
+template <typename Kernel>
+int resident_ctas_per_sm(Kernel kernel, int threads, size_t smem) {
+    static std::atomic<uint64_t> cache{0};  // (smem + 1) << 8 | CTAs
+    const uint64_t c = cache.load(std::memory_order_relaxed);
+    if ((c >> 8) == (uint64_t)smem + 1) return (int)(c & 0xffu);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    n = std::min(n, 255);
+    cache.store(((uint64_t)smem + 1) << 8 | (uint64_t)n, std::memory_order_relaxed);
+    return n;
+}
+
+// A kernel of the rank-1 family with grid `grid`: with the norm fused (p.nz set), or plain and then the standalone
+// norm (p.nz set), or plain.  The norm is fused while a head's CTAs fit one cluster and the whole grid is resident
+// at once (one wave).  Past one wave the two launches measured faster on the GB300 (B x pool-dtype sweeps of
+// decode and T = 4 verify): each CTA keeps its SM slot through the epilogue, waiting on the slowest CTA of its
+// cluster, while the next CTA's state load could use it; inside one wave the fused launch saved 2-3 us of the
+// norm's own launch.
+template <typename KPlain, typename KNorm>
+cudaError_t launch_rank1(KPlain plain, KNorm fused, dim3 grid, int threads, size_t smem, size_t smem_norm,
+                         const RecurrentParams& p, int B, cudaStream_t s) {
+    if (p.nz != nullptr && grid.x <= (unsigned)kNormMaxCluster) {
+        if (smem_norm > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_norm);
+            if (e != cudaSuccess) return e;
+        }
+        const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+        if (ctas <= (int64_t)sm_count() * resident_ctas_per_sm(fused, threads, smem_norm))
+            return launch_head_cluster(fused, grid, threads, smem_norm, s, p);
+    }
+    RecurrentParams q = p;
+    q.nz = nullptr;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(plain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    plain<<<grid, threads, smem, s>>>(q);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && p.nz != nullptr) e = launch_norm_after(p, B, s);
+    return e;
+}
+
 // the staged kernel with KIB KiB per CTA, if the rule above picks it; false: use the direct kernel
 template <typename InT, typename StT, int DK, int KIB>
 bool launch_staged(const RecurrentParams& p, int B, int sms, cudaStream_t s, cudaError_t& err) {
     if (!use_staged<StT, DK, KIB>(p, B, sms)) return false;
     using ST = Staged<DK, StT, KIB>;
-    const uint32_t smem = ST::smem_bytes(p.T);
-    auto kernel = gdn_recurrent_staged_kernel<DK, InT, StT, KIB>;
-    if (smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return true;
-    }
     const dim3 grid((p.DV + ST::ROWS - 1) / ST::ROWS, p.HV, B);
-    kernel<<<grid, Split<DK>::THREADS, smem, s>>>(p);
-    err = cudaGetLastError();
+    err = launch_rank1(gdn_recurrent_staged_kernel<DK, InT, StT, KIB, false>,
+                       gdn_recurrent_staged_kernel<DK, InT, StT, KIB, true>, grid, Split<DK>::THREADS,
+                       ST::smem_bytes(p.T), NormSmem::end(ST::norm_offset(p.T), p.T, ST::ROWS), p, B, s);
     return true;
 }
 
@@ -91,8 +174,8 @@ cudaError_t launch_dk(const RecurrentParams& p, int B, cudaStream_t s) {
     constexpr int RPC = Split<DK>::RPC;
     const size_t smem = direct_smem_bytes<DK>(p.T);
     const dim3 grid((p.DV + RPC - 1) / RPC, p.HV, B);
-    gdn_recurrent_kernel<DK, InT, StT><<<grid, NT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_rank1(gdn_recurrent_kernel<DK, InT, StT, false>, gdn_recurrent_kernel<DK, InT, StT, true>, grid, NT,
+                        smem, NormSmem::end(smem, p.T, RPC), p, B, s);
 }
 
 // the chunked kernel's replay commit + verify mode, if the call is in its range

@@ -171,17 +171,32 @@ typedef struct gdn_gated_norm_out {
 
 /*
  * gdn_mtp_verify_gated -- gdn_mtp_verify (o and, if given, intermediate_states, as that call writes them)
- * followed by the gated RMSNorm of o into norm->y.  Without intermediate states, with a bf16 pool in the chunked
- * kernel's range (T <= 8, DK >= 64) and DV <= 128, the norm runs inside the verify kernel (one item holds a whole
- * head: the sum of squares is a reduction across its rows); otherwise gdn_gated_rmsnorm runs after it.  The
- * decode-rows gated norm of TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), Per-File QA Perspective,
- * Source files, fused into the recurrence's output.
+ * followed by the gated RMSNorm of o into norm->y.  Where the verify runs on the chunked kernel (a bf16 pool
+ * without intermediate states, T <= 8, DK >= 64), the norm runs inside it while DV <= 128 and the batch leaves
+ * each of its item pipelines one item at most, else gdn_gated_rmsnorm runs after it.  Elsewhere the token-by-token
+ * kernels apply it in the same launch: the CTAs that share a head run as one thread-block cluster (at most 8, i.e.
+ * DV <= 256, or DV <= 1024 where one CTA holds 128 rows) and meet their sums of squares in distributed shared
+ * memory.  A wider head, or a grid of more CTAs than the GPU holds at once (where the two launches measured faster),
+ * gets the norm's own launch.  The decode-rows gated norm of TensorRT-LLM PR #20937 (GB300
+ * Qwen3.8-Flash-Next NVFP4), Per-File QA Perspective, Source files, fused into the recurrence's output.
  */
 GDN_API gdn_status gdn_mtp_verify_gated(const gdn_dims* dims, const void* q, const void* k, const void* v,
                                         const void* a, const void* b, const float* A_log, const float* dt_bias,
                                         const void* state_pool, const int32_t* state_indices, void* o,
                                         void* intermediate_states, const gdn_gated_norm_out* norm, int32_t* err_word,
                                         gdn_stream_t stream);
+
+/*
+ * gdn_decode_gated -- gdn_decode (the outputs and the write-back as that call stores them) with the gated RMSNorm of
+ * o into norm->y, in the same launch where the head's CTAs fit one cluster and the grid one wave (as in
+ * gdn_mtp_verify_gated above), else followed by the norm's own launch.  The decode-rows gated norm of TensorRT-LLM PR #20937, Per-File QA
+ * Perspective, Source files (gdn_decode_rows_gated_norm).  Arguments, errors and ownership as gdn_decode and
+ * gdn_gated_norm_out.
+ */
+GDN_API gdn_status gdn_decode_gated(const gdn_dims* dims, const void* q, const void* k, const void* v, const void* a,
+                                    const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                                    const int32_t* state_indices, void* o, const gdn_gated_norm_out* norm,
+                                    int32_t* err_word, gdn_stream_t stream);
 
 /* The tokens of an earlier gdn_mtp_verify call on the same lanes, whose accepted prefix gdn_mtp_verify_commit
  * commits before it verifies: the compact recovery record of a speculative step (its k, v, a, b and accept

@@ -382,3 +382,32 @@ def test_verify_gated_checks(L):
     assert verify_gated(L, dims(T=0)) == 2
     z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o")}
     assert verify_gated(L, dims(B=0), **z) == 0
+
+
+# ---- gdn_decode_gated: the decode's checks plus the norm record's ------------------------------------------
+def decode_gated(L, d, norm=True, **ptrs):
+    a = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=P2, idx=P, o=P, err=None, z=P, w=P, y=P, zd=1,
+             eps=1e-6)
+    a.update(ptrs)
+    n = gdn._GatedNormC(a["z"], a["zd"], a["w"], a["eps"], a["y"])
+    return L.gdn_decode_gated(ctypes.byref(d) if d is not None else None, a["q"], a["k"], a["v"], a["a"], a["b"],
+                              a["A_log"], a["dt_bias"], a["pool"], a["idx"], a["o"],
+                              ctypes.byref(n) if norm else None, a["err"], None)
+
+
+@pytest.mark.parametrize("ptr", ["q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o", "z", "w", "y"])
+def test_decode_gated_null_pointer(L, ptr):
+    assert decode_gated(L, dims(), **{ptr: None}) == 1
+
+
+def test_decode_gated_checks(L):
+    assert decode_gated(L, None) == 1
+    assert decode_gated(L, dims(), norm=False) == 1
+    assert decode_gated(L, dims(), zd=7) == 3
+    assert decode_gated(L, dims(), eps=-1.0) == 7
+    assert decode_gated(L, dims(), y=ctypes.c_void_p(0x10001)) == 4  # bf16 y on an odd address
+    assert decode_gated(L, dims(), w=ctypes.c_void_p(0x10002)) == 4
+    assert decode_gated(L, dims(), pool=ctypes.c_void_p(0x10008)) == 4  # the pool is read in 16-byte pieces
+    assert decode_gated(L, dims(T=0)) == 2
+    z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o")}
+    assert decode_gated(L, dims(B=0), **z) == 0

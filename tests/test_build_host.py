@@ -14,13 +14,15 @@ from gated_deltanet_linear_mtp_gb300 import build as gbuild
 
 # (source, substring of the mangled kernel name, spill-store ceiling in bytes)
 TIMED = [
-    ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li16E", 4),   # verify T=4
-    ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li32E", 0),   # bf16 T <= 2
-    ("gdn_recurrent_bf16.cu", "gdn_recurrent_kernelILi128E13__nv_bfloat16S1_E", 0),               # verify T=8
+    ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li16ELb0E", 4),  # verify T=4
+    ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li32ELb0E", 0),  # bf16 T <= 2
+    ("gdn_recurrent_bf16.cu", "gdn_recurrent_kernelILi128E13__nv_bfloat16S1_Lb0E", 0),              # verify T=8
+    ("gdn_recurrent_bf16.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16S1_Li32ELb1E", 0),  # decode + norm
+    ("gdn_recurrent_bf16.cu", "gdn_recurrent_kernelILi128E13__nv_bfloat16S1_Lb1E", 0),              # small B + norm
     ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li0E", 0),          # verify, no cache
     ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li1E", 0),          # replay commit
     ("gdn_recurrent_bf16.cu", "gdn_verify_chunked_kernelILi128E13__nv_bfloat16Li2E", 0),          # one-pass step
-    ("gdn_recurrent_f32.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16fLi16E", 0),       # decode fp32
+    ("gdn_recurrent_f32.cu", "gdn_recurrent_staged_kernelILi128E13__nv_bfloat16fLi16ELb0E", 0),   # decode fp32
     ("gdn_prefill.cu", "gdn_prefill_kernelILi256E13__nv_bfloat16S1_E", 0),                        # prefill token loop (DK 16, 32, 256)
     ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128E13__nv_bfloat16S2_Lb1E", 0),     # prefill (TMA)
     ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128EffLb0E", 0),                     # prefill fp32

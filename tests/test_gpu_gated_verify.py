@@ -1,10 +1,13 @@
-"""gdn_mtp_verify_gated (and the norm of gdn_mtp_verify_commit) on the GPU: the verify's o exactly as
-gdn_mtp_verify writes it, and y = the gated RMSNorm of that stored o.
+"""gdn_mtp_verify_gated, gdn_decode_gated (and the norm of gdn_mtp_verify_commit) on the GPU: o and the pool exactly
+as the calls without the norm leave them, and y = the gated RMSNorm of that stored o.
 
 o is checked against the oracle's verify as usual; y against the oracle's gated norm of the o the GPU stored
-(the call's definition: the norm of the stored o), with the norm's tolerance.  The fused path (bf16 pool, no
-intermediate states, T <= 8, DK >= 64, DV <= 128: the norm inside the chunked kernel) and the two-launch path
-(everything else) are both covered; rows of padded lanes must be left untouched in y."""
+(the call's definition: the norm of the stored o), with the norm's tolerance.  Three ways to the norm are covered:
+inside the chunked verify kernel (bf16 pool, no intermediate states, T <= 8, DK >= 64, DV <= 128), as the epilogue
+of the token-by-token kernels (every other verify, and decode: the CTAs of one head run as one thread-block cluster
+of at most 8 and meet through distributed shared memory; clusters of 1, 3, 4 and 7 CTAs, direct and staged kernels),
+and the standalone norm launch after the kernel (a head wider than 8 CTAs, or a grid of more than one wave).  Rows of padded lanes must be left
+untouched in y."""
 from __future__ import annotations
 
 import numpy as np
@@ -47,7 +50,7 @@ CASES = [
     (wl("gv_fused_dv96_T3", DV=96, T=3, seed=82), "bf16", False),
     (wl("gv_fused_f32out", qkv="f32", out="f32", seed=83), "f32", False),
     (wl("gv_fused_dk64_T1", DK=64, T=1, seed=84), "bf16", False),
-    # two launches: a cache, DV > 128, an fp32 pool, DK < 64, T > 8
+    # the token-by-token kernels with the norm as their epilogue: a cache, DV > 128, an fp32 pool, DK < 64, T > 8
     (wl("gv_cache_T4", seed=85), "bf16", True),
     (wl("gv_dv200", DV=200, seed=86), "bf16", False),
     (wl("gv_f32state", state="f32", out="f32", qkv="f32", seed=87), "f32", False),
@@ -126,3 +129,74 @@ def test_verify_commit_with_the_norm(T, Tp):
     (o1, p1, y1), (o2, p2, _) = outs
     assert np.array_equal(o1, o2) and np.array_equal(p1, p2), "the norm changed o or the pool"
     check_y(w, x, o1, y1, z, wt, 1e-6, "bf16")
+
+
+def dwl(name, B, HV, HK=2, DK=128, DV=128, state="bf16", qkv="bf16", out="bf16", seed=120, pad=0.2):
+    return W.Workload(name, B=B, T=1, HK=HK, HV=HV, DK=DK, DV=DV, num_slots=B + 5, qkv_dtype=qkv, state_dtype=state,
+                      out_dtype=out, mode="decode", cache=False, commit=False, seed=seed, pool_std=0.1,
+                      pad_fraction=pad)
+
+
+DECODE_CASES = [
+    # staged kernel, a whole head per CTA (a cluster of one): bf16 pool, 384 CTAs
+    (dwl("dg_staged_head", B=12, HV=32, HK=16), "bf16"),
+    # direct kernel (few CTAs): 4 CTAs of 32 rows per head, one cluster of 4
+    (dwl("dg_direct_c4", B=3, HV=4, seed=121), "f32"),
+    # fp32 pool, staged 16 KiB: 32 rows per CTA, clusters of 4 (512 CTAs: one wave)
+    (dwl("dg_f32_staged", B=4, HV=32, HK=16, state="f32", out="f32", qkv="f32", seed=122), "f32"),
+    # clusters of 3 and 7; DK = 32 (128 rows per CTA: a cluster of one in the direct kernel)
+    (dwl("dg_dv96", B=3, HV=4, DV=96, seed=123), "bf16"),
+    (dwl("dg_dv200", B=2, HV=2, HK=1, DV=200, seed=124), "bf16"),
+    (dwl("dg_dk32", B=4, HV=4, DK=32, DV=64, seed=125), "bf16"),
+    # the norm's own launch after the decode: a head of 10 CTAs (wider than one cluster), and a grid of 2048 CTAs
+    # (more than one wave)
+    (dwl("dg_dv300_fallback", B=2, HV=2, HK=1, DV=300, seed=126), "bf16"),
+    (dwl("dg_waves_fallback", B=64, HV=32, HK=16, seed=128), "bf16"),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w,z_dtype", DECODE_CASES, ids=lambda c: c.name if isinstance(c, W.Workload) else str(c))
+def test_decode_gated(w, z_dtype):
+    """gdn_decode_gated: o and the written-back pool bit for bit as gdn_decode leaves them, y the gated norm of that
+    stored o (the oracle's, at the norm's tolerance), rows of padded lanes untouched."""
+    x = w.arrays()
+    z, wt = gate_inputs(w, z_dtype, seed=w.seed + 7)
+    outs = []
+    for gated in (True, False):
+        t = Dev(x)
+        o = canary((w.B, 1, w.HV, w.DV), w.out_dtype)
+        y = canary((w.B, 1, w.HV, w.DV), w.out_dtype)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if gated:
+            gdn.gdn_decode_gated(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["pool"],
+                                 t["indices"], o, gdn.GatedNorm(dev(z), dev(wt), y, eps=1e-6), err, scale=w.scale,
+                                 l2_eps=w.l2_eps)
+        else:
+            gdn.gdn_decode(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["pool"], t["indices"],
+                           o, err, scale=w.scale, l2_eps=w.l2_eps)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append((host(o), host(t["pool"]), host(y)))
+    (o1, p1, y1), (o2, p2, _) = outs
+    bits = lambda a: a.view(np.uint32) if a.dtype == np.float32 else a  # noqa: E731  (padded rows hold NaN canaries)
+    assert np.array_equal(bits(o1), bits(o2)) and np.array_equal(bits(p1), bits(p2)), "the norm changed o or the pool"
+    check_y(w, x, o1, y1, z, wt, 1e-6, z_dtype)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("state", ["bf16", "f32"])
+def test_decode_gated_in_place(state):
+    """y = o: each CTA reads its rows' o from its own shared memory before writing y over them."""
+    w = dwl(f"dg_in_place_{state}", B=3, HV=4, state=state, out=state, qkv=state, seed=127)
+    x = w.arrays()
+    z, wt = gate_inputs(w, "bf16", seed=131)
+    t = Dev(x)
+    o_ref = canary((w.B, 1, w.HV, w.DV), w.out_dtype)
+    gdn.gdn_decode(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], Dev(x)["pool"], t["indices"],
+                   o_ref)
+    o = canary((w.B, 1, w.HV, w.DV), w.out_dtype)
+    gdn.gdn_decode_gated(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["pool"], t["indices"],
+                         o, gdn.GatedNorm(dev(z), dev(wt), o, eps=1e-6))
+    torch.cuda.synchronize()
+    check_y(w, x, host(o_ref), host(o), z, wt, 1e-6, "bf16")
