@@ -93,20 +93,25 @@ inline cudaError_t launch_norm_after(const RecurrentParams& p, int B, cudaStream
     return launch_gated_norm(g, s);
 }
 
-// CTAs of `kernel` (threads, smem bytes each) resident on one SM, from the occupancy calculator; one cached answer
-// per kernel instance (its last smem size), 0 if the query failed
+// CTAs of `kernel` (threads, smem bytes each) resident on one SM of the current device, from the occupancy
+// calculator; one cached answer per kernel instance and device (its last smem size), 0 if a query failed
 template <typename Kernel>
 int resident_ctas_per_sm(Kernel kernel, int threads, size_t smem) {
-    static std::atomic<uint64_t> cache{0};  // (smem + 1) << 8 | CTAs
-    const uint64_t c = cache.load(std::memory_order_relaxed);
-    if ((c >> 8) == (uint64_t)smem + 1) return (int)(c & 0xffu);
+    static std::atomic<uint64_t> cache[kChunkCachedDevices];  // (smem + 1) << 8 | CTAs; zero (static): none
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const bool cached = dev >= 0 && dev < kChunkCachedDevices;
+    if (cached) {
+        const uint64_t c = cache[dev].load(std::memory_order_relaxed);
+        if ((c >> 8) == (uint64_t)smem + 1) return (int)(c & 0xffu);
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     n = std::min(n, 255);
-    cache.store(((uint64_t)smem + 1) << 8 | (uint64_t)n, std::memory_order_relaxed);
+    if (cached) cache[dev].store(((uint64_t)smem + 1) << 8 | (uint64_t)n, std::memory_order_relaxed);
     return n;
 }
 

@@ -178,10 +178,11 @@ def test_prefill_host_checks():
     assert np.array_equal(host(t["pool"]), before) and is_canary(host(o)).all()
 
 
-def test_prefill_full_size_sampled():
-    """ISL 8K x 8 prompts (the timed workload): every prompt's final state and outputs on sampled heads
-    against the oracle run on that (prompt, head) alone."""
-    pw = W.prefill_8k()
+@pytest.mark.parametrize("make", [W.prefill_8k, W.prefill_mix], ids=["isl8k", "mix"])
+def test_prefill_full_size_sampled(make):
+    """The timed workloads at full size (ISL 8K x 8 prompts; 64 prompts of 256..4096 tokens): sampled (prompt,
+    head) pairs' outputs and final states against the oracle run on that (prompt, head) alone."""
+    pw = make()
     x = pw.arrays()
     t = Dev(x)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -192,9 +193,10 @@ def test_prefill_full_size_sampled():
     orc = oracle.default()
     r = pw.HV // pw.HK
     rng = np.random.default_rng(2024)
-    pairs = [(0, 0), (3, pw.HV - 1)] + [(int(b), int(h)) for b, h in zip(rng.integers(0, pw.B, 2),
-                                                                          rng.integers(0, pw.HV, 2))]
     cu = x["cu_seqlens"]
+    lens = np.diff(cu)
+    pairs = [(0, 0), (3, pw.HV - 1), (int(lens.argmax()), 5), (int(lens.argmin()), 7)] + \
+        [(int(b), int(h)) for b, h in zip(rng.integers(0, pw.B, 2), rng.integers(0, pw.HV, 2))]
     for b, h in pairs:
         lo, hi = int(cu[b]), int(cu[b + 1])
         hk = h // r
