@@ -1,4 +1,5 @@
-"""CPU oracle for the Gated DeltaNet decode / MTP-verify / commit / prefill path and its gated RMSNorm.
+"""CPU oracle for the Gated DeltaNet decode / MTP-verify / commit / prefill path, its gated RMSNorm, and the
+in_proj projection with its causal conv1d epilogue (and the convolution state's commit).
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline`` leg
 and ``--impl reference`` arm may import this package.  It shares no code with the CUDA library in
@@ -26,6 +27,29 @@ from . import build as _build
 
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f64": 2}
 NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}
+
+
+class _ConvDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("HK", ctypes.c_int32),
+                ("HV", ctypes.c_int32), ("DK", ctypes.c_int32), ("DV", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32), ("x_dtype", ctypes.c_int32), ("conv_dtype", ctypes.c_int32),
+                ("silu", ctypes.c_int32)]
+
+
+def conv_channels(d: Dict) -> Tuple[int, int]:
+    """(Cc, C): the convolved channels q | k | v and all in_proj channels q | k | v | z | b | a."""
+    Cc = 2 * d["HK"] * d["DK"] + d["HV"] * d["DV"]
+    return Cc, Cc + d["HV"] * d["DV"] + 2 * d["HV"]
+
+
+def split_in_proj(d: Dict, out: np.ndarray) -> Dict[str, np.ndarray]:
+    """The in_proj outputs [B, T, C] split into q, k [B,T,HK,DK], v, z [B,T,HV,DV], b, a [B,T,HV] (views)."""
+    B, T = out.shape[:2]
+    HK, HV, DK, DV = d["HK"], d["HV"], d["DK"], d["DV"]
+    o = np.cumsum([0, HK * DK, HK * DK, HV * DV, HV * DV, HV, HV])
+    return dict(q=out[..., o[0]:o[1]].reshape(B, T, HK, DK), k=out[..., o[1]:o[2]].reshape(B, T, HK, DK),
+                v=out[..., o[2]:o[3]].reshape(B, T, HV, DV), z=out[..., o[3]:o[4]].reshape(B, T, HV, DV),
+                b=out[..., o[4]:o[5]], a=out[..., o[5]:o[6]])
 
 
 class _Dims(ctypes.Structure):
@@ -60,8 +84,12 @@ class Oracle:
         self.lib.orc_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp]
         self.lib.orc_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, vp, ctypes.c_int32, vp,
                                                ctypes.c_int32, vp, ctypes.c_double, vp]
+        cdp = ctypes.POINTER(_ConvDims)
+        self.lib.orc_in_proj_conv.argtypes = [cdp, vp, vp, vp, vp, vp, ip, ctypes.c_int32, vp, vp]
+        self.lib.orc_conv_commit.argtypes = [cdp, vp, ip, vp, ip]
         for f in (self.lib.orc_verify, self.lib.orc_decode, self.lib.orc_commit, self.lib.orc_commit_replay,
-                  self.lib.orc_prefill, self.lib.orc_gated_rmsnorm):
+                  self.lib.orc_prefill, self.lib.orc_gated_rmsnorm, self.lib.orc_in_proj_conv,
+                  self.lib.orc_conv_commit):
             f.restype = ctypes.c_int
         for name in ("orc_round_bf16", "orc_softplus", "orc_sigmoid"):
             getattr(self.lib, name).argtypes = [ctypes.c_double]
@@ -227,6 +255,56 @@ class Oracle:
         L = np.ascontiguousarray(accept_len, dtype=np.int32)
         dims = self._dims(d, B)
         flags = self.lib.orc_commit(ctypes.byref(dims), _ptr(pool), _ptr(idx), _ptr(cache), _ptr(L))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return flags
+
+
+    # -- the in_proj projection with its causal conv1d epilogue ----------------------------------------------
+    @staticmethod
+    def _conv_dims(d: Dict, B: int) -> _ConvDims:
+        return _ConvDims(B, d["T"], d["H"], d["HK"], d["HV"], d["DK"], d["DV"], d["K"], d["num_slots"],
+                         DTYPE_CODE[d["x_dtype"]], DTYPE_CODE[d["conv_dtype"]], int(bool(d.get("silu", 1))))
+
+    def in_proj_conv(self, d: Dict, x: np.ndarray, W: np.ndarray, conv_w: np.ndarray, conv_b: Optional[np.ndarray],
+                     pool: np.ndarray, indices: np.ndarray, write_pool: bool, records: bool = True,
+                     out: Optional[np.ndarray] = None):
+        """x [B,T,H], W [C,H] (``x_dtype``), conv_w [Cc,K] / conv_b [Cc] fp32, pool [slots,K-1,Cc] (``conv_dtype``,
+        updated in place when ``write_pool``).  Returns (out [B,T,C] fp64 in W's channel order, the recovery
+        records [B,T,Cc] in ``conv_dtype`` or None, flag word).  ``out`` may be passed pre-filled (canaries):
+        rows of skipped lanes are left as given."""
+        B = indices.shape[0]
+        T, H, K = d["T"], d["H"], d["K"]
+        Cc, C = conv_channels(d)
+        x = self._check(x, d["x_dtype"], (B, T, H), "x")
+        W = self._check(W, d["x_dtype"], (C, H), "W")
+        conv_w = self._check(conv_w, "f32", (Cc, K), "conv_w")
+        if conv_b is not None:
+            conv_b = self._check(conv_b, "f32", (Cc,), "conv_b")
+        self._check(pool, d["conv_dtype"], (d["num_slots"], K - 1, Cc), "pool")
+        assert pool.flags["C_CONTIGUOUS"]
+        idx = np.ascontiguousarray(indices, dtype=np.int32)
+        if out is None:
+            out = np.zeros((B, T, C), np.float64)
+        rec = np.zeros((B, T, Cc), NP_STORAGE[d["conv_dtype"]]) if records else None
+        dims = self._conv_dims(d, B)
+        flags = self.lib.orc_in_proj_conv(ctypes.byref(dims), _ptr(x), _ptr(W), _ptr(conv_w), _ptr(conv_b),
+                                          _ptr(pool), _ptr(idx), int(bool(write_pool)), _ptr(out), _ptr(rec))
+        if flags < 0:
+            raise ValueError(f"oracle rejected dims ({flags})")
+        return out, rec, flags
+
+    def conv_commit(self, d: Dict, pool: np.ndarray, indices: np.ndarray, records: np.ndarray,
+                    accept_len: np.ndarray) -> int:
+        """The convolution state after each lane's first L_b rows, from its recovery records, in place."""
+        B = indices.shape[0]
+        Cc, _ = conv_channels(d)
+        self._check(pool, d["conv_dtype"], (d["num_slots"], d["K"] - 1, Cc), "pool")
+        records = self._check(records, d["conv_dtype"], (B, d["T"], Cc), "records")
+        idx = np.ascontiguousarray(indices, dtype=np.int32)
+        L = np.ascontiguousarray(accept_len, dtype=np.int32)
+        dims = self._conv_dims(d, B)
+        flags = self.lib.orc_conv_commit(ctypes.byref(dims), _ptr(pool), _ptr(idx), _ptr(records), _ptr(L))
         if flags < 0:
             raise ValueError(f"oracle rejected dims ({flags})")
         return flags

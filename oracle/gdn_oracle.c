@@ -318,3 +318,131 @@ int orc_commit(const orc_dims* d, void* pool, const int32_t* idx, const void* ca
     }
     return flags;
 }
+
+/* ---- the in_proj projection with its causal conv1d epilogue ------------------------------------------------
+ *
+ * The GDN input projection of the decode and verify rows with the short causal convolution fused after it:
+ * TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), What changes, Decode at small batch ("the in_proj
+ * GEMV with a fused conv1d epilogue, for 2..16 verify rows and up to 8 decode rows"); the convolution state is
+ * committed with the accepted prefix (issue "Proposal: native BF16 MTP speculative decoding for dense
+ * Qwen3.8-27B", What: the compact GDN recovery records and their commit, with the convolution's).  The pages give
+ * no formula; the plain reading written out here:
+ *
+ *   rows: lane b owns rows b*T .. b*T+T-1 of x [B*T, H]; W [C, H] with its C output channels in the order
+ *     q (HK*DK) | k (HK*DK) | v (HV*DV) | z (HV*DV) | b (HV) | a (HV); the first Cc = 2*HK*DK + HV*DV channels
+ *     (q, k, v) go through the convolution.
+ *   p[t, c]  = sum_h W[c, h] * x[b*T + t, h]
+ *   u[t, c]  = R_conv(p[t, c])                  (c < Cc: the pre-convolution value as the state stores it)
+ *   seq      = pool[slot, 0 .. K-2, c] (oldest first), then u[0 .. T-1, c]
+ *   y[t, c]  = bias[c] + sum_{j < K} w[c, j] * seq[t + j, c]    (tap K-1 weighs the current row)
+ *   y        = y * sigmoid(y) when silu is set
+ *   out[b, t, c] = y[t, c] for c < Cc, p[t, c] otherwise (fp64; the caller rounds to its output type)
+ *   u_rec[b, t, c] = u[t, c]  (the verify rows' recovery records, if asked for)
+ *   write_pool (decode): pool[slot, j, c] = seq[T + j, c] for j < K-1 (the last K-1 entries)
+ *   conv commit of L accepted rows: pool[slot, j, c] = seq[L + j, c] with seq built from u_rec (bit copies);
+ *     L = 0 leaves the slot, L outside 0..T sets flag bit 1.
+ * Padded lanes (index -1) are skipped entirely; other out-of-range indices set flag bit 0.
+ */
+typedef struct {
+    int32_t B, T, H;        /* lanes, rows per lane, hidden size */
+    int32_t HK, HV, DK, DV; /* head layout of the outputs */
+    int32_t K;              /* convolution taps */
+    int32_t num_slots;
+    int32_t x_dtype;        /* storage type of x and W */
+    int32_t conv_dtype;     /* storage type of the convolution-state pool and of the recovery records */
+    int32_t silu;           /* 1: SiLU after the convolution */
+} orc_conv_dims;
+
+static double round_to(int dtype, double x) {
+    switch (dtype) {
+    case ORC_F32: return (double)(float)x;
+    case ORC_BF16: return orc_round_bf16(x);
+    }
+    return x;
+}
+
+static int conv_dims_ok(const orc_conv_dims* d) {
+    return d->B >= 0 && d->T >= 1 && d->H >= 1 && d->HK >= 1 && d->HV >= 1 && d->DK >= 1 && d->DV >= 1 &&
+           d->K >= 1 && d->K <= 8 && d->num_slots >= 0;
+}
+
+static int conv_lane_slot(const orc_conv_dims* d, const int32_t* idx, int b, int* flags) {
+    const int32_t slot = idx[b];
+    if (slot == -1) return -1;
+    if (slot < 0 || slot >= d->num_slots) {
+        *flags |= 1;
+        return -1;
+    }
+    return slot;
+}
+
+int orc_in_proj_conv(const orc_conv_dims* d, const void* x, const void* W, const float* conv_w, const float* conv_b,
+                     void* conv_pool, const int32_t* idx, int32_t write_pool, double* out, void* u_rec) {
+    if (!conv_dims_ok(d)) return -2;
+    const int T = d->T, H = d->H, K = d->K;
+    const int64_t Cc = 2 * (int64_t)d->HK * d->DK + (int64_t)d->HV * d->DV;
+    const int64_t C = Cc + (int64_t)d->HV * d->DV + 2 * (int64_t)d->HV;
+    int flags = 0;
+    double* seq = (double*)malloc(sizeof(double) * (size_t)(K - 1 + T));
+    if (seq == NULL) return -4;
+    for (int b = 0; b < d->B; ++b) {
+        const int slot = conv_lane_slot(d, idx, b, &flags);
+        if (slot < 0) continue;
+        for (int64_t c = 0; c < C; ++c) {
+            for (int t = 0; t < T; ++t) {
+                double p = 0.0;
+                for (int h = 0; h < H; ++h)
+                    p += load(W, d->x_dtype, c * H + h) * load(x, d->x_dtype, ((int64_t)b * T + t) * H + h);
+                if (c < Cc) {
+                    seq[K - 1 + t] = round_to(d->conv_dtype, p);
+                } else {
+                    out[((int64_t)b * T + t) * C + c] = p;
+                }
+            }
+            if (c >= Cc) continue;
+            for (int j = 0; j < K - 1; ++j)
+                seq[j] = load(conv_pool, d->conv_dtype, ((int64_t)slot * (K - 1) + j) * Cc + c);
+            for (int t = 0; t < T; ++t) {
+                double y = conv_b ? (double)conv_b[c] : 0.0;
+                for (int j = 0; j < K; ++j) y += (double)conv_w[c * K + j] * seq[t + j];
+                if (d->silu) y = y * orc_sigmoid(y);
+                out[((int64_t)b * T + t) * C + c] = y;
+                if (u_rec) store(u_rec, d->conv_dtype, ((int64_t)b * T + t) * Cc + c, seq[K - 1 + t]);
+            }
+            if (write_pool)
+                for (int j = 0; j < K - 1; ++j)
+                    store(conv_pool, d->conv_dtype, ((int64_t)slot * (K - 1) + j) * Cc + c, seq[T + j]);
+        }
+    }
+    free(seq);
+    return flags;
+}
+
+int orc_conv_commit(const orc_conv_dims* d, void* conv_pool, const int32_t* idx, const void* u_rec,
+                    const int32_t* accept_len) {
+    if (!conv_dims_ok(d)) return -2;
+    const int T = d->T, K = d->K;
+    const int64_t Cc = 2 * (int64_t)d->HK * d->DK + (int64_t)d->HV * d->DV;
+    int flags = 0;
+    double* seq = (double*)malloc(sizeof(double) * (size_t)(K - 1 + T));
+    if (seq == NULL) return -4;
+    for (int b = 0; b < d->B; ++b) {
+        const int slot = conv_lane_slot(d, idx, b, &flags);
+        if (slot < 0) continue;
+        const int L = accept_len[b];
+        if (L < 0 || L > T) {
+            flags |= 2;
+            continue;
+        }
+        if (L == 0) continue;
+        for (int64_t c = 0; c < Cc; ++c) {
+            for (int j = 0; j < K - 1; ++j)
+                seq[j] = load(conv_pool, d->conv_dtype, ((int64_t)slot * (K - 1) + j) * Cc + c);
+            for (int t = 0; t < T; ++t) seq[K - 1 + t] = load(u_rec, d->conv_dtype, ((int64_t)b * T + t) * Cc + c);
+            for (int j = 0; j < K - 1; ++j)
+                store(conv_pool, d->conv_dtype, ((int64_t)slot * (K - 1) + j) * Cc + c, seq[L + j]);
+        }
+    }
+    free(seq);
+    return flags;
+}

@@ -516,9 +516,154 @@ def check_gated_rmsnorm_closed_forms(orc):
     assert np.abs(y[0] - want).max() < 1e-14
 
 
+# ---- the in_proj projection with its causal conv1d epilogue -------------------------------------------------
+def _conv_case(B=2, T=3, H=5, HK=1, HV=2, DK=2, DV=3, K=4, x="f64", conv="f64", silu=1, seed=70, identity=False):
+    """Dims and fp64-exact arrays: x ~ N(0,1), W ~ N(0, 1/H) (or the identity with H = C), conv taps U(-1, 1)
+    and biases in fp32, a random convolution-state pool, distinct random slots."""
+    import oracle
+
+    num_slots = B + 2
+    rng = np.random.default_rng(seed)
+    d = dict(T=T, H=H, HK=HK, HV=HV, DK=DK, DV=DV, K=K, num_slots=num_slots, x_dtype=x, conv_dtype=conv, silu=silu)
+    Cc, C = oracle.conv_channels(d)
+    if identity:
+        d["H"] = H = C
+    xs = rng.normal(size=(B, T, H))
+    Wm = np.eye(C) if identity else rng.normal(size=(C, H)) / math.sqrt(H)
+    conv_w = rng.uniform(-1.0, 1.0, (Cc, K)).astype(np.float32)
+    conv_b = rng.normal(0.0, 0.3, Cc).astype(np.float32)
+    pool = rng.normal(size=(num_slots, K - 1, Cc))
+    if conv == "f32":
+        pool = pool.astype(np.float32)
+    idx = rng.permutation(num_slots)[:B].astype(np.int32)
+    if x == "f32":
+        xs, Wm = xs.astype(np.float32), Wm.astype(np.float32)
+    return d, xs, Wm, conv_w, conv_b, pool, idx
+
+
+def check_in_proj_is_the_matrix_product(orc):
+    """With the current-row tap alone (w = e_{K-1}), no bias and no SiLU, every output channel is the product
+    W x of the row (numpy's matmul), the recovery records hold the same for q, k, v, and the pool is read only."""
+    import oracle
+
+    for K in (1, 2, 4):
+        d, xs, Wm, _, _, pool, idx = _conv_case(K=K, silu=0, seed=71 + K)
+        Cc, C = oracle.conv_channels(d)
+        taps = np.zeros((Cc, K), np.float32)
+        taps[:, K - 1] = 1.0
+        before = pool.copy()
+        out, rec, fl = orc.in_proj_conv(d, xs, Wm, taps, None, pool, idx, write_pool=False)
+        want = np.einsum("ch,bth->btc", Wm, xs)
+        assert fl == 0
+        assert np.abs(out - want).max() <= 1e-12 * np.abs(want).max(), K
+        assert np.abs(rec - want[..., :Cc]).max() <= 1e-12 * np.abs(want).max(), K
+        assert np.array_equal(pool, before)
+        parts = oracle.split_in_proj(d, want)
+        assert parts["q"].shape == (2, 3, 1, 2) and parts["z"].shape == (2, 3, 2, 3) and parts["a"].shape == (2, 3, 2)
+        assert np.array_equal(parts["a"], want[..., -2:]) and np.array_equal(parts["v"].reshape(2, 3, 6), want[..., 4:10])
+
+
+def check_conv_is_numpy_convolve(orc):
+    """W = I (p = x): each convolved channel is bias + the 'valid' correlation of [state, x rows] with its taps
+    (numpy.convolve with the taps reversed), SiLU by scipy's expit; the decode write-back keeps the last K-1
+    entries of that sequence; the other channels pass x through."""
+    import oracle
+    from scipy.special import expit
+
+    for K, T, silu in ((4, 3, 0), (4, 1, 1), (2, 5, 1), (3, 2, 0)):
+        d, xs, Wm, taps, bias, pool, idx = _conv_case(K=K, T=T, silu=silu, seed=80 + K + T, identity=True)
+        Cc, C = oracle.conv_channels(d)
+        before = pool.copy()
+        out, _, fl = orc.in_proj_conv(d, xs, Wm, taps, bias, pool, idx, write_pool=True)
+        assert fl == 0
+        for b in range(len(idx)):
+            for c in range(C):
+                if c >= Cc:
+                    assert abs(out[b, :, c] - xs[b, :, c]).max() <= 1e-15, (K, T, b, c)
+                    continue
+                seq = np.concatenate([before[idx[b], :, c], xs[b, :, c]])
+                y = float(bias[c]) + np.convolve(seq, taps[c, ::-1].astype(np.float64), mode="valid")
+                if silu:
+                    y = y * expit(y)
+                assert y.shape == (T,)
+                assert abs(out[b, :, c] - y).max() <= 1e-13 * max(1.0, abs(y).max()), (K, T, b, c)
+                assert np.array_equal(pool[idx[b], :, c], seq[T:]), (K, T, b, c)
+
+
+def check_conv_state_chain_and_commit(orc):
+    """A decode of T rows equals T decodes of one row (outputs and state, exact in fp64); a verify that keeps
+    its recovery records followed by the commit of L rows leaves the state that L one-row decodes leave (L = 0:
+    unchanged); padded lanes touch nothing; a bad index and a bad accept length set their flag bits."""
+    T = 3
+    d, xs, Wm, taps, bias, pool0, idx = _conv_case(B=3, T=T, K=4, silu=1, seed=90)
+    pool_a = pool0.copy()
+    out_a, _, _ = orc.in_proj_conv(d, xs, Wm, taps, bias, pool_a, idx, write_pool=True)
+    d1 = dict(d, T=1)
+    pools = [pool0.copy()]
+    for t in range(T):
+        p = pools[-1].copy()
+        o1, _, _ = orc.in_proj_conv(d1, np.ascontiguousarray(xs[:, t:t + 1]), Wm, taps, bias, p, idx, write_pool=True)
+        assert np.array_equal(o1[:, 0], out_a[:, t]), t
+        pools.append(p)
+    assert np.array_equal(pools[T], pool_a)
+    # verify (read-only) then commit
+    pool_v = pool0.copy()
+    out_v, rec, _ = orc.in_proj_conv(d, xs, Wm, taps, bias, pool_v, idx, write_pool=False)
+    assert np.array_equal(out_v, out_a) and np.array_equal(pool_v, pool0)
+    L = np.array([2, 0, 3], np.int32)
+    assert orc.conv_commit(d, pool_v, idx, rec, L) == 0
+    for b in range(3):
+        assert np.array_equal(pool_v[idx[b]], pools[L[b]][idx[b]]), b
+    # padding and bad data
+    idx2 = idx.copy()
+    idx2[1] = -1
+    pool_p = pool0.copy()
+    canary = np.full(out_a.shape, CANARY)
+    out_p, _, fl = orc.in_proj_conv(d, xs, Wm, taps, bias, pool_p, idx2, write_pool=True, out=canary)
+    assert fl == 0 and np.all(out_p[1] == CANARY) and np.array_equal(pool_p[idx[1]], pool0[idx[1]])
+    assert np.array_equal(out_p[0], out_a[0]) and np.array_equal(pool_p[idx[0]], pool_a[idx[0]])
+    idx2[1] = d["num_slots"]
+    assert orc.in_proj_conv(d, xs, Wm, taps, bias, pool0.copy(), idx2, write_pool=True)[2] == 1
+    pool_c = pool0.copy()
+    assert orc.conv_commit(d, pool_c, idx, rec, np.array([1, T + 1, -1], np.int32)) == 2
+    assert np.array_equal(pool_c[idx[1]], pool0[idx[1]]) and np.array_equal(pool_c[idx[2]], pool0[idx[2]])
+
+
+def check_conv_records_rounded(orc):
+    """A bf16 or fp32 state stores each pre-convolution value rounded once from the exact product (the rounding
+    pinned above), and the convolution reads those stored values; x and W in bf16 or fp32 are read exactly."""
+    import oracle
+    from gdn_workloads import bf16_bits_to_f32, to_bf16_bits
+
+    for conv in ("bf16", "f32"):
+        d, xs, Wm, taps, bias, _, idx = _conv_case(B=2, T=2, K=3, silu=0, conv=conv, seed=95)
+        Cc, C = oracle.conv_channels(d)
+        xb = to_bf16_bits(xs.astype(np.float32))
+        Wb = to_bf16_bits(Wm.astype(np.float32))
+        d["x_dtype"] = "bf16"
+        pool = np.zeros((d["num_slots"], 2, Cc), np.uint16 if conv == "bf16" else np.float32)
+        out, rec, _ = orc.in_proj_conv(d, xb, Wb, taps, bias, pool, idx, write_pool=True)
+        exact = np.einsum("ch,bth->btc", bf16_bits_to_f32(Wb).astype(np.float64), bf16_bits_to_f32(xb).astype(np.float64))
+        if conv == "bf16":
+            want = np.vectorize(orc.round_bf16)(exact[..., :Cc])
+            got = bf16_bits_to_f32(rec).astype(np.float64)
+            stored = bf16_bits_to_f32(pool[idx]).astype(np.float64)
+        else:
+            want = exact[..., :Cc].astype(np.float32).astype(np.float64)
+            got = rec.astype(np.float64)
+            stored = pool[idx].astype(np.float64)
+        assert np.array_equal(got, want), conv
+        assert np.array_equal(stored[:, 0], want[:, 0]) and np.array_equal(stored[:, 1], want[:, 1]), conv
+        # zero state, K = 3: y_t = bias + w2 u_t + w1 u_{t-1}
+        y1 = bias + taps[:, 2].astype(np.float64) * want[:, 1] + taps[:, 1].astype(np.float64) * want[:, 0]
+        assert np.abs(out[:, 1, :Cc] - y1).max() <= 1e-13, conv
+        assert np.abs(out[..., Cc:] - exact[..., Cc:]).max() <= 1e-13, conv
+
+
 ALL_CHECKS = [check_bf16_rounding, check_scalar_functions, check_gate_closed_form, check_beta_sigmoid,
               check_beta_zero_pure_decay, check_orthonormal_keys_write_v, check_l2norm_eps, check_scale,
               check_head_mapping, check_product_form, check_chained_calls, check_padding_and_bad_data,
               check_commit_replay, check_prefill_product_form, check_prefill_fresh_state,
               check_prefill_matches_verify_and_decode, check_prefill_chained, check_prefill_bad_bounds,
-              check_gated_rmsnorm_closed_forms]
+              check_gated_rmsnorm_closed_forms, check_in_proj_is_the_matrix_product, check_conv_is_numpy_convolve,
+              check_conv_state_chain_and_commit, check_conv_records_rounded]

@@ -61,6 +61,23 @@ MUTANTS = [
     ("norm_gate_sign", "const double silu = zi * orc_sigmoid(zi);", "const double silu = zi * orc_sigmoid(-zi);"),
     ("norm_weight_index", "* (double)w[i] * silu;", "* (double)w[0] * silu;"),
     ("norm_gate_row", "const double zi = load(z, z_dtype, r * DV + i);", "const double zi = load(z, z_dtype, i);"),
+    ("in_proj_W_transposed", "load(W, d->x_dtype, c * H + h)", "load(W, d->x_dtype, h * C + c)"),
+    ("in_proj_row_index", "load(x, d->x_dtype, ((int64_t)b * T + t) * H + h)", "load(x, d->x_dtype, ((int64_t)b * T) * H + h)"),
+    ("conv_taps_reversed", "y += (double)conv_w[c * K + j] * seq[t + j];",
+     "y += (double)conv_w[c * K + (K - 1 - j)] * seq[t + j];"),
+    ("conv_bias_dropped", "double y = conv_b ? (double)conv_b[c] : 0.0;", "double y = 0.0;"),
+    ("conv_silu_sigmoid_only", "if (d->silu) y = y * orc_sigmoid(y);", "if (d->silu) y = orc_sigmoid(y);"),
+    ("conv_records_unrounded", "seq[K - 1 + t] = round_to(d->conv_dtype, p);", "seq[K - 1 + t] = p;"),
+    ("conv_state_from_lane", "seq[j] = load(conv_pool, d->conv_dtype, ((int64_t)slot * (K - 1) + j) * Cc + c);",
+     "seq[j] = load(conv_pool, d->conv_dtype, ((int64_t)b * (K - 1) + j) * Cc + c);"),
+    ("conv_write_back_one_early", "((int64_t)slot * (K - 1) + j) * Cc + c, seq[T + j]);",
+     "((int64_t)slot * (K - 1) + j) * Cc + c, seq[T + j - 1]);"),
+    ("conv_commit_one_early", "((int64_t)slot * (K - 1) + j) * Cc + c, seq[L + j]);",
+     "((int64_t)slot * (K - 1) + j) * Cc + c, seq[L + j - 1]);"),
+    ("conv_commit_ignores_accept_len", "((int64_t)slot * (K - 1) + j) * Cc + c, seq[L + j]);",
+     "((int64_t)slot * (K - 1) + j) * Cc + c, seq[T + j]);"),
+    ("conv_padding_not_skipped", "    const int32_t slot = idx[b];\n    if (slot == -1) return -1;\n    if (slot < 0 || slot >= d->num_slots) {",
+     "    const int32_t slot = idx[b] == -1 ? 0 : idx[b];\n    if (slot < 0 || slot >= d->num_slots) {"),
     ("norm_output_unnormalised", "y[r * DV + i] = load(o, o_dtype, r * DV + i) * inv_rms * (double)w[i] * silu;",
      "y[r * DV + i] = load(o, o_dtype, r * DV + i) * (double)w[i] * silu;"),
 ]
