@@ -16,12 +16,17 @@ library has not been built, every call raises.
     gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, o,
                 has_initial_state=None, err_word=None, ...)
     gdn_gated_rmsnorm(o, z, norm_weight, y=None, eps=1e-6)
+    gdn_in_proj_conv(x, W, conv_w, conv_b, conv_state, state_indices, out, write_state, records=None,
+                     err_word=None, silu=True)
+    gdn_conv_commit(conv_state, state_indices, records, accept_len, err_word=None)
 
 Shapes and semantics are those of ``include/gdn.h``: q, k ``[B,T,HK,DK]``; v, o ``[B,T,HV,DV]``; a, b
 ``[B,T,HV]``; A_log, dt_bias ``[HV]`` fp32; state_pool ``[num_slots,HV,DV,DK]``; state_indices, accept_len
 ``[B]`` int32; intermediate_states ``[B,T,HV,DV,DK]``; err_word a 1-element int32 device tensor.  Prefill takes
 packed tokens: q, k ``[N,HK,DK]``; v, o ``[N,HV,DV]``; a, b ``[N,HV]``; cu_seqlens ``[B+1]`` and
-has_initial_state ``[B]`` int32.
+has_initial_state ``[B]`` int32.  The in_proj projection takes x ``[B,T,H]`` bf16, W ``[C,H]`` bf16, conv_w
+``[Cc,K]`` / conv_b ``[Cc]`` fp32, conv_state ``[num_slots,K-1,Cc]`` and records ``[B,T,Cc]``, and writes the q, k,
+v, z, b, a of an ``InProjOut`` (their shapes give HK, DK, HV, DV).
 """
 from __future__ import annotations
 
@@ -33,7 +38,7 @@ from .build import LIB_PATH
 
 __all__ = ["gdn_decode", "gdn_decode_gated", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay", "gdn_mtp_verify_commit", "ReplayTokens",
            "gdn_mtp_verify_gated", "GatedNorm",
-           "gdn_prefill", "gdn_gated_rmsnorm", "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
+           "gdn_prefill", "gdn_gated_rmsnorm", "gdn_in_proj_conv", "gdn_conv_commit", "InProjOut", "GdnError", "GdnDims", "lib", "STATUS", "ERRBIT_INDEX", "ERRBIT_ACCEPT_LEN", "ERRBIT_TIMEOUT",
            "ERRBIT_SEQLEN", "MAX_T", "EXPORTS"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
@@ -46,7 +51,8 @@ MAX_T = 16
 F32, BF16 = 0, 1
 EXPORTS = ("gdn_decode", "gdn_decode_gated", "gdn_mtp_verify", "gdn_commit", "gdn_commit_replay",
            "gdn_mtp_verify_commit", "gdn_mtp_verify_gated", "gdn_prefill",
-           "gdn_gated_rmsnorm", "gdn_status_string", "gdn_last_cuda_error", "gdn_abi_version")
+           "gdn_gated_rmsnorm", "gdn_in_proj_conv", "gdn_conv_commit", "gdn_status_string", "gdn_last_cuda_error",
+           "gdn_abi_version")
 
 
 class GdnDims(ctypes.Structure):
@@ -82,6 +88,25 @@ class GatedNorm:
         self.z, self.norm_weight, self.y, self.eps = z, norm_weight, y, eps
 
 
+class _ConvDimsC(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("HK", ctypes.c_int32),
+                ("HV", ctypes.c_int32), ("DK", ctypes.c_int32), ("DV", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32), ("conv_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("silu", ctypes.c_int32)]
+
+
+class _InProjOutC(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("z", ctypes.c_void_p),
+                ("b", ctypes.c_void_p), ("a", ctypes.c_void_p)]
+
+
+class InProjOut:
+    """The outputs of ``gdn_in_proj_conv``: q, k ``[B,T,HK,DK]``, v, z ``[B,T,HV,DV]``, b, a ``[B,T,HV]``, one dtype."""
+
+    def __init__(self, q, k, v, z, b, a):
+        self.q, self.k, self.v, self.z, self.b, self.a = q, k, v, z, b, a
+
+
 class GdnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -114,6 +139,12 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill.argtypes = [dp, ip] + [vp] * 5 + [vp, vp, vp, ip, ip, vp, ip, vp]
         L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
                                         ctypes.c_float, vp, vp]
+        cdp = ctypes.POINTER(_ConvDimsC)
+        L.gdn_in_proj_conv.argtypes = [cdp, vp, vp, vp, vp, vp, ip, ctypes.c_int32, ctypes.POINTER(_InProjOutC), vp,
+                                       ip, vp]
+        L.gdn_conv_commit.argtypes = [cdp, vp, ip, vp, ip, ip, vp]
+        for f in (L.gdn_in_proj_conv, L.gdn_conv_commit):
+            f.restype = ctypes.c_int
         for f in (L.gdn_decode, L.gdn_decode_gated, L.gdn_mtp_verify, L.gdn_commit, L.gdn_commit_replay, L.gdn_mtp_verify_commit,
                   L.gdn_mtp_verify_gated, L.gdn_prefill, L.gdn_gated_rmsnorm):
             f.restype = ctypes.c_int
@@ -473,3 +504,99 @@ def gdn_gated_rmsnorm(o, z, norm_weight, y=None, *, eps=1e-6, stream=None):
             (rows, DV, _code(o, "o"), _code(z, "z"), _dev(o, "o"), _dev(z, "z"), _dev(norm_weight, "norm_weight"),
              float(eps), _dev(y, "y")), "gdn_gated_rmsnorm")
     return y
+
+
+def _conv_dims(x, W, conv_w, conv_state, out, silu):
+    """gdn_conv_dims from the tensors: x [B,T,H], W [C,H], conv_w [Cc,K], conv_state [num_slots,K-1,Cc] and the
+    outputs' shapes (HK, DK from q; HV, DV from v)."""
+    import torch
+
+    if x.dim() != 3 or W.dim() != 2 or conv_w.dim() != 2 or conv_state.dim() != 3:
+        raise ValueError("x is [B,T,H], W [C,H], conv_w [Cc,K], conv_state [num_slots,K-1,Cc]")
+    B, T, H = x.shape
+    if out.q.dim() != 4 or out.v.dim() != 4:
+        raise ValueError("q and v are 4-D")
+    HK, DK = out.q.shape[2], out.q.shape[3]
+    HV, DV = out.v.shape[2], out.v.shape[3]
+    Cc = 2 * HK * DK + HV * DV
+    C = Cc + HV * DV + 2 * HV
+    K = conv_w.shape[1]
+    _shape(W, (C, H), "W")
+    _shape(conv_w, (Cc, K), "conv_w")
+    _shape(conv_state, (conv_state.shape[0], K - 1, Cc), "conv_state")
+    for t, n, want in ((out.q, "q", (B, T, HK, DK)), (out.k, "k", (B, T, HK, DK)), (out.v, "v", (B, T, HV, DV)),
+                       (out.z, "z", (B, T, HV, DV)), (out.b, "b", (B, T, HV)), (out.a, "a", (B, T, HV))):
+        _shape(t, want, n)
+    for t, n in ((x, "x"), (W, "W")):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{n} must be bf16")
+    if conv_w.dtype != torch.float32:
+        raise TypeError("conv_w must be fp32")
+    od = _code(out.q, "q")
+    for t, n in ((out.k, "k"), (out.v, "v"), (out.z, "z"), (out.b, "b"), (out.a, "a")):
+        if _code(t, n) != od:
+            raise TypeError(f"{n} must have q's dtype")
+    return _ConvDimsC(B, T, H, HK, HV, DK, DV, K, conv_state.shape[0], _code(conv_state, "conv_state"), od,
+                      1 if silu else 0)
+
+
+def gdn_in_proj_conv(x, W, conv_w, conv_b, conv_state, state_indices, out, write_state, records=None,
+                     err_word=None, *, silu=True, stream=None) -> None:
+    """The in_proj projection of x's rows with its causal conv1d epilogue into ``out`` (an ``InProjOut``);
+    ``write_state`` (decode) moves each lane's convolution state on by its T rows, otherwise ``records``
+    (``[B,T,Cc]``, conv_state's dtype) receives the pre-convolution values for ``gdn_conv_commit``."""
+    import torch
+
+    L = lib()
+    d = _conv_dims(x, W, conv_w, conv_state, out, silu)
+    _shape(state_indices, (d.B,), "state_indices")
+    if state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
+    Cc = 2 * d.HK * d.DK + d.HV * d.DV
+    if conv_b is not None:
+        _shape(conv_b, (Cc,), "conv_b")
+        if conv_b.dtype != torch.float32:
+            raise TypeError("conv_b must be fp32")
+    if records is not None:
+        _shape(records, (d.B, d.T, Cc), "records")
+        if _code(records, "records") != d.conv_dtype:
+            raise TypeError("records must have conv_state's dtype")
+    device = _common_device([("x", x), ("W", W), ("conv_w", conv_w), ("conv_b", conv_b), ("conv_state", conv_state),
+                             ("state_indices", state_indices), ("q", out.q), ("k", out.k), ("v", out.v),
+                             ("z", out.z), ("b", out.b), ("a", out.a), ("records", records), ("err_word", err_word)])
+    oc = _InProjOutC(*(_dev(t, n) for t, n in ((out.q, "q"), (out.k, "k"), (out.v, "v"), (out.z, "z"),
+                                                (out.b, "b"), (out.a, "a"))))
+    _launch(device, stream, L.gdn_in_proj_conv,
+            (ctypes.byref(d), _dev(x, "x"), _dev(W, "W"), _dev(conv_w, "conv_w"), _dev(conv_b, "conv_b"),
+             _dev(conv_state, "conv_state"), _dev(state_indices, "state_indices"), 1 if write_state else 0,
+             ctypes.byref(oc), _dev(records, "records"), _dev(err_word, "err_word", torch.int32)),
+            "gdn_in_proj_conv")
+
+
+def gdn_conv_commit(conv_state, state_indices, records, accept_len, err_word=None, *, stream=None) -> None:
+    """The convolution state after each lane's first ``accept_len[b]`` verify rows, from their records."""
+    import torch
+
+    L = lib()
+    if conv_state.dim() != 3 or records.dim() != 3:
+        raise ValueError("conv_state is [num_slots,K-1,Cc], records [B,T,Cc]")
+    B, T, Cc = records.shape
+    K = conv_state.shape[1] + 1
+    _shape(conv_state, (conv_state.shape[0], K - 1, Cc), "conv_state")
+    _shape(state_indices, (B,), "state_indices")
+    _shape(accept_len, (B,), "accept_len")
+    for t, n in ((state_indices, "state_indices"), (accept_len, "accept_len")):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{n} must be int32")
+    if _code(records, "records") != _code(conv_state, "conv_state"):
+        raise TypeError("records must have conv_state's dtype")
+    # the commit needs only the channel count Cc = 2*HK*DK + HV*DV (at least 3): any head layout with that count
+    if Cc < 3:
+        raise ValueError("records: fewer than 3 channels")
+    d = _ConvDimsC(B, T, 8, 1, 1, 1, Cc - 2, K, conv_state.shape[0], _code(conv_state, "conv_state"), BF16, 1)
+    device = _common_device([("conv_state", conv_state), ("state_indices", state_indices), ("records", records),
+                             ("accept_len", accept_len), ("err_word", err_word)])
+    _launch(device, stream, L.gdn_conv_commit,
+            (ctypes.byref(d), _dev(conv_state, "conv_state"), _dev(state_indices, "state_indices"),
+             _dev(records, "records"), _dev(accept_len, "accept_len"), _dev(err_word, "err_word", torch.int32)),
+            "gdn_conv_commit")

@@ -23,7 +23,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgdn.so")
 
 SOURCES = ["gdn_api.cu", "gdn_recurrent_f32.cu", "gdn_recurrent_bf16.cu", "gdn_commit.cu", "gdn_prefill.cu",
-           "gdn_prefill_chunked.cu", "gdn_gated_norm.cu"]
+           "gdn_prefill_chunked.cu", "gdn_gated_norm.cu", "gdn_in_proj_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # hidden visibility: only the GDN_API functions of gdn.h are exported, so that internal symbols (template
 # statics among them) never bind across two libraries loaded in one process

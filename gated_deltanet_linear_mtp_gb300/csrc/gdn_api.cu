@@ -47,6 +47,29 @@ gdn_status check_dims(const gdn_dims* d, bool need_io, bool prefill = false) {
     return GDN_OK;
 }
 
+// Sizes of gdn_in_proj_conv / gdn_conv_commit (`commit`: H, out_dtype and silu are not read).  Cc and C: the
+// convolved and all output channels.  C is bounded so that a grid dimension (C / 128 tiles) and every element
+// offset stay in range.
+gdn_status check_conv_dims(const gdn_conv_dims* d, bool commit, int64_t* Cc, int64_t* C) {
+    if (d == nullptr) return GDN_ERR_NULL;
+    if (d->B < 0 || d->B > 65535 || d->T < 1 || d->T > GDN_MAX_T) return GDN_ERR_SHAPE;
+    if (d->HK < 1 || d->HV < 1 || d->HV > 65535 || d->HV % d->HK != 0 || d->DK < 1 || d->DV < 1) return GDN_ERR_SHAPE;
+    if (d->K < 2 || d->K > 4 || d->num_slots < 1) return GDN_ERR_SHAPE;
+    if (!valid_dtype(d->conv_dtype)) return GDN_ERR_DTYPE;
+    if (!commit) {
+        if (d->H < 8 || d->H > 65536 || d->H % 8 != 0) return GDN_ERR_SHAPE;
+        if (!valid_dtype(d->out_dtype)) return GDN_ERR_DTYPE;
+        if (d->silu != 0 && d->silu != 1) return GDN_ERR_VALUE;
+    }
+    const int64_t qk = (int64_t)d->HK * d->DK, vz = (int64_t)d->HV * d->DV;
+    if (qk > (1 << 22) || vz > (1 << 22)) return GDN_ERR_SHAPE;
+    *Cc = 2 * qk + vz;
+    *C = *Cc + vz + 2 * (int64_t)d->HV;
+    if (*C > (int64_t)65535 * 128) return GDN_ERR_SHAPE;
+    if ((double)d->num_slots * (d->K - 1) * (double)*Cc > 4.0e18) return GDN_ERR_SHAPE;
+    return GDN_OK;
+}
+
 // `o` may be NULL only where the call has no outputs (replay commit: need_o = false).
 gdn_status check_io(const gdn_dims* d, const void* q, const void* k, const void* v, const void* a, const void* b,
                     const float* A_log, const float* dt_bias, const void* pool, const int32_t* idx, const void* o,
@@ -384,6 +407,82 @@ gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t DV, int32_t o_dtype, int32_t 
     p.vec = DV % 8 == 0 && aligned(o, 16) && aligned(z, 16) && aligned(y, 16) && aligned(norm_weight, 16);
     p.eps = eps;
     return finish(launch_gated_norm(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_in_proj_conv(const gdn_conv_dims* dims, const void* x, const void* W, const float* conv_w,
+                            const float* conv_b, void* conv_state, const int32_t* state_indices, int32_t write_state,
+                            const gdn_in_proj_out* out, void* records, int32_t* err_word, gdn_stream_t stream) {
+    int64_t Cc = 0, C = 0;
+    gdn_status s = check_conv_dims(dims, false, &Cc, &C);
+    if (s != GDN_OK) return s;
+    if (write_state != 0 && write_state != 1) return GDN_ERR_VALUE;
+    if (dims->B == 0) return GDN_OK;
+    if (!x || !W || !conv_w || !conv_state || !state_indices || !out) return GDN_ERR_NULL;
+    if (!out->q || !out->k || !out->v || !out->z || !out->b || !out->a) return GDN_ERR_NULL;
+    const uintptr_t ssz = dtype_bytes(dims->conv_dtype), osz = dtype_bytes(dims->out_dtype);
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(conv_w, 4) || (conv_b && !aligned(conv_b, 4))) return GDN_ERR_ALIGN;
+    if (!aligned(conv_state, ssz) || (records && !aligned(records, ssz)) || !aligned(state_indices, 4)) return GDN_ERR_ALIGN;
+    if (!aligned(out->q, osz) || !aligned(out->k, osz) || !aligned(out->v, osz) || !aligned(out->z, osz) ||
+        !aligned(out->b, osz) || !aligned(out->a, osz))
+        return GDN_ERR_ALIGN;
+    if (err_word && !aligned(err_word, 4)) return GDN_ERR_ALIGN;
+    InProjConvParams p{};
+    p.B = dims->B;
+    p.T = dims->T;
+    p.H = dims->H;
+    p.HK = dims->HK;
+    p.HV = dims->HV;
+    p.DK = dims->DK;
+    p.DV = dims->DV;
+    p.K = dims->K;
+    p.num_slots = dims->num_slots;
+    p.Cc = Cc;
+    p.C = C;
+    p.conv_w = conv_w;
+    p.conv_b = conv_b;
+    p.state = conv_state;
+    p.state_bf16 = dims->conv_dtype == GDN_BF16;
+    p.indices = state_indices;
+    p.write_state = write_state;
+    p.q = out->q;
+    p.k = out->k;
+    p.v = out->v;
+    p.z = out->z;
+    p.bo = out->b;
+    p.ao = out->a;
+    p.out_bf16 = dims->out_dtype == GDN_BF16;
+    p.records = records;
+    p.x = x;
+    p.W = W;
+    p.err = err_word;
+    p.silu = dims->silu;
+    return finish(launch_in_proj_conv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_conv_commit(const gdn_conv_dims* dims, void* conv_state, const int32_t* state_indices,
+                           const void* records, const int32_t* accept_len, int32_t* err_word, gdn_stream_t stream) {
+    int64_t Cc = 0, C = 0;
+    gdn_status s = check_conv_dims(dims, true, &Cc, &C);
+    if (s != GDN_OK) return s;
+    if (dims->B == 0) return GDN_OK;
+    if (!conv_state || !state_indices || !records || !accept_len) return GDN_ERR_NULL;
+    const uintptr_t ssz = dtype_bytes(dims->conv_dtype);
+    if (!aligned(conv_state, ssz) || !aligned(records, ssz) || !aligned(state_indices, 4) || !aligned(accept_len, 4))
+        return GDN_ERR_ALIGN;
+    if (err_word && !aligned(err_word, 4)) return GDN_ERR_ALIGN;
+    ConvCommitParams p{};
+    p.state = conv_state;
+    p.indices = state_indices;
+    p.records = records;
+    p.accept_len = accept_len;
+    p.err = err_word;
+    p.B = dims->B;
+    p.T = dims->T;
+    p.K = dims->K;
+    p.num_slots = dims->num_slots;
+    p.state_bf16 = dims->conv_dtype == GDN_BF16;
+    p.Cc = Cc;
+    return finish(launch_conv_commit(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* gdn_status_string(gdn_status status) {

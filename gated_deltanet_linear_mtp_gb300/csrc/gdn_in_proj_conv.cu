@@ -1,0 +1,392 @@
+// gdn_in_proj_conv.cu -- the in_proj projection of the decode / verify rows with its causal conv1d epilogue, and
+// the convolution state's commit (sm_103a).
+//
+// TensorRT-LLM PR #20937 (GB300 Qwen3.8-Flash-Next NVFP4), What changes, Decode at small batch: "the in_proj GEMV
+// with a fused conv1d epilogue, for 2..16 verify rows and up to 8 decode rows"; the convolution state is committed
+// with the accepted prefix from the verify rows' recovery records (issue "Proposal: native BF16 MTP speculative
+// decoding for dense Qwen3.8-27B", What).  For lane b (rows b*T .. b*T+T-1 of x) and output channel c of W:
+//     p[t, c] = sum_h W[c, h] x[b*T + t, h]                         (fp32 accumulation of bf16 products)
+//     channels q | k | v (c < Cc): u[t, c] = R_state(p[t, c]); seq = state[slot, 0 .. K-2, c], u[0 .. T-1, c];
+//         y[t, c] = bias[c] + sum_j w[c, j] seq[t + j, c], SiLU if asked; decode writes the last K-1 of seq back,
+//         verify keeps u as its recovery records
+//     channels z | b | a: the projection itself.
+//
+// gdn_in_proj_conv_kernel: one CTA of 4 warps per (128 output channels, a tile of whole lanes, a slice of the
+// hidden dimension).  W is the dense operand: its 128 x 64 boxes and the rows' N x 64 boxes arrive by TMA (128-byte
+// swizzle) into a ring of stages; one thread issues tcgen05.mma (M = 128 channels, N = the tile's rows padded to 16,
+// K = 16) into a tensor-memory accumulator of 128 lanes x N columns.  The bytes are W's (50 MB for a 12352 x 2048
+// projection), read once, so a small row count is HBM-bound: the grid splits the hidden dimension over a
+// thread-block cluster of up to 8 CTAs so that about two CTAs run per SM, and the partial sums meet through
+// distributed shared memory.  The epilogue moves the accumulator to shared memory (the ring, no longer in use),
+// then each rank of the cluster takes its share of the tile's lanes: thread = channel, so every load and store of
+// the state, the outputs and the records is one coalesced row.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+#include "gdn_tcgen05.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kIpM = 128;                  // output channels per tile: the accumulator's tensor-memory lanes
+constexpr int kIpKC = 64;                  // hidden columns per stage: one 128-byte swizzled box
+constexpr uint32_t kIpWBox = kIpM * kIpKC * 2;  // bytes of W per stage
+constexpr int kIpThreads = 128;
+constexpr int kIpMaxN = 256;               // rows per tile (the MMA's N)
+constexpr int kIpMaxCluster = 8;
+constexpr int kIpMaxStages = 8;
+constexpr uint32_t kIpWaitPolls = GDN_WAIT_POLLS;
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared memory, from a 1024-byte aligned base: `stages` x (W box | rows box), then the mbarriers full[stages],
+// empty[stages], done, then the tensor-memory address.  The epilogue's [N][128] fp32 accumulator copy reuses the
+// ring (N * 512 bytes <= the ring, checked on the host).
+__host__ __device__ inline uint32_t ip_stage_bytes(int N) { return kIpWBox + (uint32_t)N * 128u; }
+__host__ __device__ inline uint32_t ip_bar_offset(int N, int S) { return ip_stage_bytes(N) * (uint32_t)S; }
+__host__ __device__ inline uint32_t ip_smem_bytes(int N, int S) {
+    return ip_bar_offset(N, S) + 8u * (2u * S + 1u) + 16u + 1024u;  // + alignment slack
+}
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+__device__ __forceinline__ void store_elem(void* base, bool bf16, int64_t i, float v) {
+    if (bf16)
+        static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+    else
+        static_cast<float*>(base)[i] = v;
+}
+
+__device__ __forceinline__ float load_elem(const void* base, bool bf16, int64_t i) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
+}
+
+}  // namespace
+
+// The launch's tiling: N rows per tile (whole lanes, padded to 16), `ks` ranks splitting the hidden dimension's
+// `kchunks` 64-column chunks, `stages` ring stages.
+struct IpTiling {
+    int N, lanes_per_tile, ks, kchunks, stages;
+};
+
+// K: convolution taps (2..4)
+template <int K>
+__global__ void __launch_bounds__(kIpThreads, 1)
+    gdn_in_proj_conv_kernel(const InProjConvParams p, const IpTiling g, const __grid_constant__ CUtensorMap wmap,
+                            const __grid_constant__ CUtensorMap xmap) {
+    extern __shared__ __align__(1024) unsigned char ip_smem[];
+    __shared__ int failed;
+    const uint32_t raw = smem_u32(ip_smem);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* const gbase = ip_smem + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int rank = blockIdx.x, ctile = blockIdx.y, rtile = blockIdx.z;
+    const int N = g.N, S = g.stages;
+    const uint32_t stage_b = ip_stage_bytes(N);
+    const uint32_t bars = base + ip_bar_offset(N, S);  // full s: + 8 s; empty s: + 8 (S + s); done: + 16 S
+    const uint32_t done_bar = bars + 16u * S;
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + ip_bar_offset(N, S) + 8u * (2u * S + 1u));
+    const int c0 = rank * g.kchunks / g.ks, nk = (rank + 1) * g.kchunks / g.ks - c0;  // nk >= 1 (host)
+    const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2 * S + 1; ++s) mbar_init(bars + 8u * s, 1);
+        fence_mbar_init();
+        failed = 0;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), ncols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0;  // producer: loads issued
+    if (tid == 0) {
+        // producer: one stage = W's 128 x 64 box and the tile's N x 64 rows box, on the stage's full barrier
+        const int row0 = rtile * g.lanes_per_tile * p.T;
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (i >= S && !mbar_wait_bounded(bars + 8u * (S + s), (uint32_t)((i / S) - 1) & 1u, kIpWaitPolls)) {
+                failed = 1;
+                break;
+            }
+            const uint32_t dst = base + (uint32_t)s * stage_b;
+            mbar_arrive_expect_tx(bars + 8u * s, stage_b);
+            tma_load_2d(dst, &wmap, (c0 + i) * kIpKC, ctile * kIpM, bars + 8u * s);
+            tma_load_2d(dst + kIpWBox, &xmap, (c0 + i) * kIpKC, row0, bars + 8u * s);
+            issued = i + 1;
+        }
+    } else if (tid == 32) {
+        // MMA issuer: D[128 x N] (+)= W box . rows box^T, four K = 16 steps per stage; each stage's completion
+        // frees it for the producer, the last one signals the epilogue
+        const uint32_t idesc = umma_idesc_bf16(kIpM, N);
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (!mbar_wait_bounded(bars + 8u * s, (uint32_t)(i / S) & 1u, kIpWaitPolls)) {
+                failed = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a = base + (uint32_t)s * stage_b, b = a + kIpWBox;
+#pragma unroll
+            for (int kk = 0; kk < kIpKC / 16; ++kk)
+                umma_bf16(tmem, umma_desc_sw128(a + 32u * kk), umma_desc_sw128(b + 32u * kk), idesc,
+                          (i | kk) != 0 ? 1u : 0u);
+            umma_commit(bars + 8u * (S + s));
+        }
+        umma_commit(done_bar);
+    }
+    if (!mbar_wait_bounded(done_bar, 0, kIpWaitPolls)) failed = 1;
+    tc_fence_after();
+    __syncthreads();
+    const bool ok = failed == 0;
+    if (!ok) {
+        // a wait ran out: let the MMAs and the copies already issued finish before the memory is reused or freed
+        if (tid == 0) {
+            mbar_wait_bounded(done_bar, 0, kIpWaitPolls);
+            for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+                mbar_wait_bounded(bars + 8u * (i % S), (uint32_t)(i / S) & 1u, kIpWaitPolls);
+            if (p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
+        }
+        __syncthreads();
+    }
+
+    // the accumulator to shared memory: acc[col][channel], thread = channel (tensor-memory lane 32 warp + lane)
+    float* const acc = reinterpret_cast<float*>(gbase);
+    if (ok) {
+        for (int col = 0; col < N; col += 16) {
+            float f[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)col, f);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[(col + j) * kIpM + tid] = f[j];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (g.ks > 1) cluster_barrier();  // every rank's partial sums are in its shared memory
+
+    // each rank takes lanes rank, rank + ks, ... of the tile; thread = channel c
+    const int64_t c = (int64_t)ctile * kIpM + tid;
+    const int T = p.T;
+    for (int li = rank; ok && li < g.lanes_per_tile; li += g.ks) {
+        const int b = rtile * g.lanes_per_tile + li;
+        if (b >= p.B) break;
+        const int slot = p.indices[b];
+        if (slot < 0 || slot >= p.num_slots) {
+            if (slot != -1 && ctile == 0 && tid == 0 && p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_INDEX);
+            continue;
+        }
+        if (c >= p.C) continue;
+        const bool conv = c < p.Cc;
+        // the full sums over the ranks (in rank order: every rank forms the same value), rounded to the state type
+        // for the convolved channels, back into this rank's copy: only this thread reads them from here on
+        for (int t = 0; t < T; ++t) {
+            float* e = acc + (li * T + t) * kIpM + tid;
+            float v = 0.f;
+            for (int r = 0; r < g.ks; ++r) v += r == rank ? *e : ld_cluster(e, (uint32_t)r);
+            if (conv && p.state_bf16) v = round_bf16(v);
+            *e = v;
+        }
+        const float* u = acc + li * T * kIpM + tid;  // u[t * kIpM]
+        const int64_t row0 = (int64_t)b * T;
+        if (!conv) {
+            const int64_t cz = c - p.Cc, zc = (int64_t)p.HV * p.DV;
+            for (int t = 0; t < T; ++t) {
+                if (cz < zc)
+                    store_elem(p.z, p.out_bf16, (row0 + t) * zc + cz, u[t * kIpM]);
+                else if (cz < zc + p.HV)
+                    store_elem(p.bo, p.out_bf16, (row0 + t) * p.HV + (cz - zc), u[t * kIpM]);
+                else
+                    store_elem(p.ao, p.out_bf16, (row0 + t) * p.HV + (cz - zc - p.HV), u[t * kIpM]);
+            }
+            continue;
+        }
+        // the convolution over seq = state (K - 1 entries, oldest first), u[0 .. T-1]
+        float st[K - 1], w[K];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j)
+            st[j] = load_elem(p.state, p.state_bf16, ((int64_t)slot * (K - 1) + j) * p.Cc + c);
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[j] = p.conv_w[c * K + j];
+        const float bias = p.conv_b != nullptr ? p.conv_b[c] : 0.f;
+        auto seq = [&](int i) -> float {
+            if (i >= K - 1) return u[(i - (K - 1)) * kIpM];
+            float s = st[0];
+#pragma unroll
+            for (int j = 1; j < K - 1; ++j)
+                if (i == j) s = st[j];
+            return s;
+        };
+        // output tensor and offset of channel c: q | k (HK * DK each), then v (HV * DV)
+        const int64_t qc = (int64_t)p.HK * p.DK, vc = (int64_t)p.HV * p.DV;
+        void* const dst = c < qc ? p.q : c < 2 * qc ? p.k : p.v;
+        const int64_t dc = c < qc ? c : c < 2 * qc ? c - qc : c - 2 * qc, dstride = c < 2 * qc ? qc : vc;
+        for (int t = 0; t < T; ++t) {
+            float y = bias;
+#pragma unroll
+            for (int j = 0; j < K; ++j) y = fmaf(w[j], seq(t + j), y);
+            if (p.silu) y = y / (1.f + expf(-y));
+            store_elem(dst, p.out_bf16, (row0 + t) * dstride + dc, y);
+            if (p.records != nullptr) store_elem(p.records, p.state_bf16, (row0 + t) * p.Cc + c, u[t * kIpM]);
+        }
+        if (p.write_state) {
+            float nw[K - 1];
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) nw[j] = seq(T + j);  // every read before the first write
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j)
+                store_elem(p.state, p.state_bf16, ((int64_t)slot * (K - 1) + j) * p.Cc + c, nw[j]);
+        }
+    }
+
+    __syncthreads();
+    if (g.ks > 1) cluster_barrier();  // no rank leaves while another may still read its partial sums
+    if (warp == 1) tmem_dealloc(tmem, ncols);
+}
+
+// The convolution state after each lane's first L accepted rows: pool[slot, j, c] = seq[L + j, c] with seq = the
+// slot's K - 1 entries, then the lane's T recovery records (bit copies: both are stored values of the state type).
+// One thread per (lane, channel); every read comes before the first write.
+template <typename StT>
+__global__ void __launch_bounds__(256) gdn_conv_commit_kernel(const ConvCommitParams p) {
+    const int b = blockIdx.y;
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && p.err != nullptr;
+    const int slot = p.indices[b];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (slot != -1 && reporter) atomicOr(p.err, GDN_ERRBIT_INDEX);
+        return;
+    }
+    const int L = p.accept_len[b];
+    if (L < 0 || L > p.T) {
+        if (reporter) atomicOr(p.err, GDN_ERRBIT_ACCEPT_LEN);
+        return;
+    }
+    if (L == 0 || c >= p.Cc) return;
+    const int K1 = p.K - 1;  // 1 .. 3
+    StT* const st = static_cast<StT*>(p.state) + (int64_t)slot * K1 * p.Cc + c;
+    const StT* const rec = static_cast<const StT*>(p.records) + (int64_t)b * p.T * p.Cc + c;
+    StT nv[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        if (j < K1) nv[j] = L + j < K1 ? st[(int64_t)(L + j) * p.Cc] : rec[(int64_t)(L + j - K1) * p.Cc];
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        if (j < K1) st[(int64_t)j * p.Cc] = nv[j];
+}
+
+namespace {
+
+bool encode_rows_map(CUtensorMap* map, const void* ptr, int cols, int64_t rows, int box_rows) {
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kIpKC, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int ip_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 148;
+    return sms;
+}
+
+}  // namespace
+
+// Tiling: a tile holds whole lanes, all B of them when B * T <= 256 rows, else 256 / T.  The hidden dimension is
+// split over ks ranks (a cluster) so that the grid holds about two CTAs per SM, each rank keeping at least one
+// chunk; the ring takes what two CTAs per SM leave (one for N > 64), 2..8 stages.
+IpTiling in_proj_tiling(int B, int T, int H, int64_t C, int sms) {
+    IpTiling g{};
+    g.lanes_per_tile = (int64_t)B * T <= kIpMaxN ? B : kIpMaxN / T;
+    g.N = (g.lanes_per_tile * T + 15) / 16 * 16;
+    g.kchunks = (H + kIpKC - 1) / kIpKC;
+    const int64_t tiles = ((C + kIpM - 1) / kIpM) * (int64_t)((B + g.lanes_per_tile - 1) / g.lanes_per_tile);
+    int64_t ks = (2 * (int64_t)sms) / std::max<int64_t>(tiles, 1);
+    ks = std::min<int64_t>(std::min<int64_t>(ks, kIpMaxCluster), g.kchunks);
+    g.ks = (int)std::max<int64_t>(ks, 1);
+    const uint32_t budget = g.N <= 64 ? 110u * 1024u : 220u * 1024u;
+    g.stages = (int)std::min<uint32_t>(kIpMaxStages, std::max<uint32_t>(2, budget / ip_stage_bytes(g.N)));
+    return g;
+}
+
+template <int K>
+cudaError_t launch_in_proj_k(const InProjConvParams& p, const IpTiling& g, const CUtensorMap& wmap,
+                             const CUtensorMap& xmap, cudaStream_t s) {
+    auto kernel = gdn_in_proj_conv_kernel<K>;
+    const uint32_t smem = ip_smem_bytes(g.N, g.stages);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g.ks, (unsigned)((p.C + kIpM - 1) / kIpM),
+                       (unsigned)((p.B + g.lanes_per_tile - 1) / g.lanes_per_tile));
+    cfg.blockDim = dim3(kIpThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)g.ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p, g, wmap, xmap);
+}
+
+cudaError_t launch_in_proj_conv(const InProjConvParams& p, cudaStream_t s) {
+    if (p.B == 0) return cudaSuccess;
+    const IpTiling g = in_proj_tiling(p.B, p.T, p.H, p.C, ip_sm_count());
+    if ((uint64_t)g.stages * ip_stage_bytes(g.N) < (uint64_t)g.N * kIpM * 4) return cudaErrorInvalidConfiguration;
+    CUtensorMap wmap, xmap;
+    if (!encode_rows_map(&wmap, p.W, p.H, p.C, kIpM) || !encode_rows_map(&xmap, p.x, p.H, (int64_t)p.B * p.T, g.N))
+        return cudaErrorInvalidValue;
+    switch (p.K) {
+    case 2: return launch_in_proj_k<2>(p, g, wmap, xmap, s);
+    case 3: return launch_in_proj_k<3>(p, g, wmap, xmap, s);
+    case 4: return launch_in_proj_k<4>(p, g, wmap, xmap, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_conv_commit(const ConvCommitParams& p, cudaStream_t s) {
+    if (p.B == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((p.Cc + 255) / 256), (unsigned)p.B);
+    if (p.state_bf16)
+        gdn_conv_commit_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+    else
+        gdn_conv_commit_kernel<float><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

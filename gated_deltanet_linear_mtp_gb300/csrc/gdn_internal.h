@@ -57,6 +57,40 @@ struct CommitParams {
     int64_t lane_bytes;  // HV * DV * DK * element size: one lane's state, all heads
 };
 
+// The in_proj projection with its causal conv1d epilogue (gdn_in_proj_conv), and the convolution state's commit.
+struct InProjConvParams {
+    int B, T, H, HK, HV, DK, DV, K, num_slots;
+    int64_t Cc, C;          // convolved channels (q | k | v), all channels (q | k | v | z | b | a)
+    const float* conv_w;    // [Cc, K]
+    const float* conv_b;    // [Cc] or nullptr
+    void* state;            // [num_slots, K - 1, Cc]
+    int state_bf16;
+    const int32_t* indices;
+    int write_state;        // decode: the last K - 1 entries of each lane's sequence go back to its slot
+    void* q;                // [B, T, HK, DK]
+    void* k;
+    void* v;                // [B, T, HV, DV]
+    void* z;
+    void* bo;               // [B, T, HV]
+    void* ao;
+    int out_bf16;
+    void* records;          // [B, T, Cc] state type, or nullptr
+    const void* x;          // [B * T, H] bf16
+    const void* W;          // [C, H] bf16
+    int32_t* err;
+    int silu;
+};
+
+struct ConvCommitParams {
+    void* state;            // [num_slots, K - 1, Cc]
+    const int32_t* indices;
+    const void* records;    // [B, T, Cc]
+    const int32_t* accept_len;
+    int32_t* err;
+    int B, T, K, num_slots, state_bf16;
+    int64_t Cc;
+};
+
 struct GatedNormParams {
     const void* o;   // [rows, DV], o_bf16 ? bf16 : fp32
     const void* z;   // [rows, DV], z_bf16 ? bf16 : fp32
@@ -94,6 +128,10 @@ bool prefill_chunked_eligible(int DK);
 cudaError_t launch_prefill_chunked(const RecurrentParams& p, const int32_t* cu_seqlens, const int32_t* has_init, int B,
                                    int n_tokens, int DK, bool qkv_bf16, bool state_bf16, cudaStream_t s);
 cudaError_t launch_gated_norm(const GatedNormParams& p, cudaStream_t s);
+
+// gdn_in_proj_conv.cu
+cudaError_t launch_in_proj_conv(const InProjConvParams& p, cudaStream_t s);
+cudaError_t launch_conv_commit(const ConvCommitParams& p, cudaStream_t s);
 int64_t gated_norm_max_rows();
 
 }  // namespace gdn

@@ -47,7 +47,8 @@ POOL_BLOCK = 16  # slots per independent pool stream
 
 # stream ids: one independent generator per tensor
 _STREAM = {"q": 1, "k": 2, "v": 3, "a": 4, "b": 5, "dt_bias": 6, "A_log": 7, "pool": 8,
-           "slots": 9, "pad": 10, "accept_len": 11, "lengths": 12, "fresh": 13, "z": 14, "norm_weight": 15}
+           "slots": 9, "pad": 10, "accept_len": 11, "lengths": 12, "fresh": 13, "z": 14, "norm_weight": 15,
+           "x": 16, "W": 17, "conv_w": 18, "conv_b": 19, "conv_state": 20, "records": 21}
 
 
 def _rng(seed: int, name: str) -> np.random.Generator:
@@ -373,3 +374,84 @@ def gated_norm_inputs(rows: int, DV: int, o_dtype: str, z_dtype: str, seed: int)
     z = _rng(seed, "z").standard_normal((rows, DV), dtype=f32)
     w = (1.0 + 0.1 * _rng(seed, "norm_weight").standard_normal(DV)).astype(f32)
     return {"o": _store(o, o_dtype), "z": _store(z, z_dtype), "w": w}
+
+
+
+@dataclasses.dataclass(frozen=True)
+class InProjWorkload:
+    """Inputs of the in_proj projection with its causal conv1d epilogue (decode or verify rows).
+
+    x ~ N(0, 1) [B, T, H] bf16 (normalised hidden states), W ~ N(0, 1/H) [C, H] bf16 (so that every projection
+    is ~ N(0, 1)), conv taps and biases ~ U(-1/sqrt(K), 1/sqrt(K)) fp32 (the usual depthwise-convolution
+    initialisation, fan-in K), convolution state ~ N(0, 1) [num_slots, K-1, Cc] (earlier projections), distinct
+    slots with ``pad_fraction`` of the lanes at -1, accept lengths in 1..T; C and Cc as the interface defines
+    them (q | k | v | z | b | a, and q | k | v).  No method arithmetic: draws, casts and layout only."""
+
+    name: str
+    B: int
+    T: int
+    H: int
+    HK: int
+    HV: int
+    DK: int
+    DV: int
+    K: int
+    num_slots: int
+    conv_dtype: str
+    out_dtype: str
+    seed: int
+    silu: bool = True
+    pad_fraction: float = 0.0
+
+    def replace(self, **kw) -> "InProjWorkload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def Cc(self) -> int:
+        return 2 * self.HK * self.DK + self.HV * self.DV
+
+    @property
+    def C(self) -> int:
+        return self.Cc + self.HV * self.DV + 2 * self.HV
+
+    def arrays(self) -> Dict[str, np.ndarray]:
+        B, T, H, K, s = self.B, self.T, self.H, self.K, self.seed
+        f32 = np.float32
+        out: Dict[str, np.ndarray] = {}
+        out["x"] = _store(_rng(s, "x").standard_normal((B, T, H), dtype=f32), BF16)
+        w = _rng(s, "W").standard_normal((self.C, H), dtype=f32)
+        w *= f32(1.0 / np.sqrt(H))
+        out["W"] = _store(w, BF16)
+        bound = f32(1.0 / np.sqrt(K))
+        out["conv_w"] = _rng(s, "conv_w").uniform(-bound, bound, (self.Cc, K)).astype(f32)
+        out["conv_b"] = _rng(s, "conv_b").uniform(-bound, bound, self.Cc).astype(f32)
+        out["conv_state"] = _store(_rng(s, "conv_state").standard_normal((self.num_slots, K - 1, self.Cc), dtype=f32),
+                                   self.conv_dtype)
+        if B > self.num_slots:
+            raise ValueError("more lanes than slots: distinct slots are impossible")
+        slots = _rng(s, "slots").permutation(self.num_slots)[:B].astype(np.int32)
+        n_pad = int(round(self.pad_fraction * B))
+        if n_pad:
+            slots[_rng(s, "pad").permutation(B)[:n_pad]] = -1
+        out["indices"] = slots
+        out["accept_len"] = _rng(s, "accept_len").integers(1, T + 1, B).astype(np.int32)
+        # recovery records of an earlier verify (inputs of the commit alone): earlier projections ~ N(0, 1)
+        out["records"] = _store(_rng(s, "records").standard_normal((B, T, self.Cc), dtype=f32), self.conv_dtype)
+        return out
+
+
+def in_proj_verify16() -> InProjWorkload:
+    """16 verify rows (B = 4 lanes x T = 4, the page's largest verify row count): hidden 2048, 16 key heads and 32
+    value heads of 128 (the head layout of every workload above), 4 taps, bf16 state and outputs."""
+    return InProjWorkload("in_proj_conv_verify_B4_T4_H2048", B=4, T=4, H=2048, HK=16, HV=32, DK=128, DV=128, K=4,
+                          num_slots=64, conv_dtype=BF16, out_dtype=BF16, seed=500)
+
+
+def in_proj_decode8() -> InProjWorkload:
+    """8 decode rows (the page's largest decode row count), the rest as in_proj_verify16."""
+    return in_proj_verify16().replace(name="in_proj_conv_decode_B8_T1_H2048", B=8, T=1, seed=501)
+
+
+def in_proj_verify512() -> InProjWorkload:
+    """The verify-T4 batch of 128 lanes (512 rows): the projection becomes a GEMM with two row tiles."""
+    return in_proj_verify16().replace(name="in_proj_conv_verify_B128_T4_H2048", B=128, num_slots=512, seed=502)

@@ -268,6 +268,77 @@ GDN_API gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t DV, int32_t o_dtype, 
                                      const void* z, const float* norm_weight, float eps, void* y,
                                      gdn_stream_t stream);
 
+/*
+ * The in_proj projection of the decode / verify rows with its causal conv1d epilogue: TensorRT-LLM PR #20937
+ * (GB300 Qwen3.8-Flash-Next NVFP4), What changes, Decode at small batch ("the in_proj GEMV with a fused conv1d
+ * epilogue, for 2..16 verify rows and up to 8 decode rows").  The page gives no formula; the reading taken:
+ *
+ *   W [C, H] bf16 holds the C = 2*HK*DK + 2*HV*DV + 2*HV output channels in the order
+ *     q (HK*DK) | k (HK*DK) | v (HV*DV) | z (HV*DV) | b (HV) | a (HV);
+ *   the first Cc = 2*HK*DK + HV*DV channels (q, k, v) pass through a K-tap causal depthwise convolution whose
+ *   state is the K-1 previous inputs of each channel, per pool slot:
+ *     conv_state [num_slots, K-1, Cc] conv_dtype (oldest first),
+ *   For lane b (rows b*T .. b*T+T-1 of x [B*T, H] bf16) with slot = state_indices[b] != -1, channel c, row t:
+ *     p[t, c] = sum_h W[c, h] x[b*T + t, h]                      (fp32 accumulation)
+ *     u[t, c] = p[t, c] rounded to conv_dtype                    (c < Cc: the value the state stores)
+ *     seq     = conv_state[slot, 0 .. K-2, c], u[0 .. T-1, c]
+ *     y[t, c] = conv_b[c] + sum_{j < K} conv_w[c, j] seq[t + j, c], then y * sigmoid(y) if dims->silu
+ *   q, k [B, T, HK, DK], v [B, T, HV, DV] <- y of their channels; z [B, T, HV, DV], b, a [B, T, HV] <- p of theirs
+ *   (all out_dtype).
+ */
+typedef struct gdn_conv_dims {
+    int32_t B;          /* request lanes, 0 .. 65535 */
+    int32_t T;          /* rows per lane, 1 .. GDN_MAX_T */
+    int32_t H;          /* hidden size: a multiple of 8, 8 .. 65536 */
+    int32_t HK;         /* query/key heads of the outputs, >= 1 */
+    int32_t HV;         /* value heads, a multiple of HK */
+    int32_t DK;         /* key dimension, >= 1 */
+    int32_t DV;         /* value dimension, >= 1 */
+    int32_t K;          /* convolution taps, 2 .. 4 */
+    int32_t num_slots;  /* convolution-state slots, >= 1 */
+    int32_t conv_dtype; /* gdn_dtype of conv_state and of the recovery records */
+    int32_t out_dtype;  /* gdn_dtype of q, k, v, z, b, a */
+    int32_t silu;       /* 1: SiLU after the convolution, 0: none */
+} gdn_conv_dims;
+
+/* Outputs of gdn_in_proj_conv: the inputs of gdn_decode / gdn_mtp_verify (q, k, v, a, b) and of the gated norm
+ * (z); device memory, out_dtype, element-aligned, no overlap with anything else. */
+typedef struct gdn_in_proj_out {
+    void* q; /* [B, T, HK, DK] */
+    void* k; /* [B, T, HK, DK] */
+    void* v; /* [B, T, HV, DV] */
+    void* z; /* [B, T, HV, DV] */
+    void* b; /* [B, T, HV] */
+    void* a; /* [B, T, HV] */
+} gdn_in_proj_out;
+
+/*
+ * gdn_in_proj_conv -- the projection and convolution above for every lane whose index is not -1.
+ * write_state = 1 (decode rows): conv_state[slot, j, c] = seq[T + j, c] for j < K-1 (the last K-1 entries).
+ * write_state = 0 (verify rows): conv_state is only read; if records is not NULL it receives u:
+ *     records [B, T, Cc] conv_dtype, the verify rows' recovery records for gdn_conv_commit.
+ * conv_w [Cc, K] fp32, conv_b [Cc] fp32 or NULL (zero).  x and W start on 16 bytes; the rest on their element
+ * size.  Lanes with index -1 are skipped (outputs, records and slot untouched); an index < -1 or >= num_slots
+ * skips the lane and sets GDN_ERRBIT_INDEX.  Distinct active lanes must use distinct slots when write_state = 1.
+ * The waits of the kernel on its own copies are bounded (GDN_ERRBIT_TIMEOUT, outputs of the tile left unwritten).
+ */
+GDN_API gdn_status gdn_in_proj_conv(const gdn_conv_dims* dims, const void* x, const void* W, const float* conv_w,
+                                    const float* conv_b, void* conv_state, const int32_t* state_indices,
+                                    int32_t write_state, const gdn_in_proj_out* out, void* records,
+                                    int32_t* err_word, gdn_stream_t stream);
+
+/*
+ * gdn_conv_commit -- the convolution state after each lane's first L = accept_len[b] verify rows: with seq =
+ * conv_state[slot, 0 .. K-2, c], records[b, 0 .. T-1, c], conv_state[slot, j, c] = seq[L + j, c] (bit copies).
+ * L = 0 leaves the slot; L outside 0 .. T sets GDN_ERRBIT_ACCEPT_LEN, a bad index GDN_ERRBIT_INDEX (the lane is
+ * skipped).  The commit of the convolution state with the accepted prefix (issue "Proposal: native BF16 MTP
+ * speculative decoding for dense Qwen3.8-27B", What: the compact GDN recovery records and their commit).  Only
+ * dims->B, T, HK, HV, DK, DV, K, num_slots and conv_dtype are read.
+ */
+GDN_API gdn_status gdn_conv_commit(const gdn_conv_dims* dims, void* conv_state, const int32_t* state_indices,
+                                   const void* records, const int32_t* accept_len, int32_t* err_word,
+                                   gdn_stream_t stream);
+
 /* Static string naming a status; never NULL. */
 GDN_API const char* gdn_status_string(gdn_status status);
 

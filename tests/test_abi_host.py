@@ -411,3 +411,63 @@ def test_decode_gated_checks(L):
     assert decode_gated(L, dims(T=0)) == 2
     z = {k: None for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "pool", "idx", "o")}
     assert decode_gated(L, dims(B=0), **z) == 0
+
+
+# ---- gdn_in_proj_conv / gdn_conv_commit: host validation (nothing reaches a kernel) ---------------------------
+def conv_dims(**kw):
+    base = dict(B=4, T=4, H=2048, HK=16, HV=32, DK=128, DV=128, K=4, num_slots=8, conv_dtype=1, out_dtype=1, silu=1)
+    base.update(kw)
+    return gdn._ConvDimsC(**base)
+
+
+def in_proj(L, d, out=True, **ptrs):
+    a = dict(x=P2, W=P2, conv_w=P, conv_b=None, state=P, idx=P, write=1, q=P, k=P, v=P, z=P, b=P, a=P, rec=None,
+             err=None)
+    a.update(ptrs)
+    o = gdn._InProjOutC(a["q"], a["k"], a["v"], a["z"], a["b"], a["a"])
+    return L.gdn_in_proj_conv(ctypes.byref(d) if d is not None else None, a["x"], a["W"], a["conv_w"], a["conv_b"],
+                              a["state"], a["idx"], a["write"], ctypes.byref(o) if out else None, a["rec"], a["err"],
+                              None)
+
+
+def conv_commit(L, d, **ptrs):
+    a = dict(state=P, idx=P, rec=P, acc=P, err=None)
+    a.update(ptrs)
+    return L.gdn_conv_commit(ctypes.byref(d) if d is not None else None, a["state"], a["idx"], a["rec"], a["acc"],
+                             a["err"], None)
+
+
+@pytest.mark.parametrize("ptr", ["x", "W", "conv_w", "state", "idx", "q", "k", "v", "z", "b", "a"])
+def test_in_proj_null_pointer(L, ptr):
+    assert in_proj(L, conv_dims(), **{ptr: None}) == 1
+
+
+def test_in_proj_checks(L):
+    assert in_proj(L, None) == 1
+    assert in_proj(L, conv_dims(), out=False) == 1
+    assert in_proj(L, conv_dims(K=1)) == 2 and in_proj(L, conv_dims(K=5)) == 2
+    assert in_proj(L, conv_dims(H=100)) == 2 and in_proj(L, conv_dims(H=0)) == 2  # H % 8 != 0, H < 8
+    assert in_proj(L, conv_dims(T=0)) == 2 and in_proj(L, conv_dims(T=17)) == 2
+    assert in_proj(L, conv_dims(HV=24, HK=16)) == 2                                # HV % HK != 0
+    assert in_proj(L, conv_dims(HK=1, DK=1 << 23)) == 2                            # channels beyond the grid
+    assert in_proj(L, conv_dims(conv_dtype=5)) == 3 and in_proj(L, conv_dims(out_dtype=2)) == 3
+    assert in_proj(L, conv_dims(silu=2)) == 7 and in_proj(L, conv_dims(), write=3) == 7
+    assert in_proj(L, conv_dims(), x=ctypes.c_void_p(0x10008)) == 4               # x and W by TMA: 16 bytes
+    assert in_proj(L, conv_dims(), W=ctypes.c_void_p(0x10004)) == 4
+    assert in_proj(L, conv_dims(), conv_w=ctypes.c_void_p(0x10002)) == 4
+    assert in_proj(L, conv_dims(), state=ctypes.c_void_p(0x10001)) == 4           # bf16 state on an odd address
+    assert in_proj(L, conv_dims(), rec=ctypes.c_void_p(0x10001)) == 4
+    assert in_proj(L, conv_dims(out_dtype=0), v=ctypes.c_void_p(0x10002)) == 4    # fp32 v on 2 bytes
+    z = {k: None for k in ("x", "W", "conv_w", "state", "idx", "q", "k", "v", "z", "b", "a")}
+    assert in_proj(L, conv_dims(B=0), out=False, **z) == 0                        # nothing to do, nothing read
+
+
+def test_conv_commit_checks(L):
+    assert conv_commit(L, None) == 1
+    for p in ("state", "idx", "rec", "acc"):
+        assert conv_commit(L, conv_dims(), **{p: None}) == 1
+    assert conv_commit(L, conv_dims(K=5)) == 2
+    assert conv_commit(L, conv_dims(conv_dtype=9)) == 3
+    assert conv_commit(L, conv_dims(H=3, out_dtype=9, silu=5)) != 2                # the commit reads neither
+    assert conv_commit(L, conv_dims(), acc=ctypes.c_void_p(0x10002)) == 4
+    assert conv_commit(L, conv_dims(B=0), state=None, idx=None, rec=None, acc=None) == 0
