@@ -9,6 +9,7 @@ so that the lines left in L2 are clean.
 
     python bench.py [--steps K] [--warmup W] [--workload verify4|verify8|decode|...|sweep|sweep_replay] [--impl reference]
     python bench.py --workload prefill8k|prefill_mix|gated_norm     (the prefill and gated-norm calls, own lines)
+    python bench.py --workload in_proj16|in_proj8|in_proj512        (the in_proj projection + conv1d, own lines)
 
 Prints one JSON line (``--workload sweep``: one per point).  ``value`` = verified tokens/s (A x T per step,
 A = non-padded lanes, summed over ranks, divided by the slowest rank's device time).
@@ -1029,6 +1030,203 @@ def run_norm_arm(args, rank: int, world: int, local_rank: int, rows: int = 65536
     return result
 
 
+IN_PROJ_METRIC = "GDN in_proj + causal conv1d rows/s and achieved HBM GB/s"
+IN_PROJ_NAMED = {"in_proj16": W.in_proj_verify16, "in_proj8": W.in_proj_decode8, "in_proj512": W.in_proj_verify512}
+IN_PROJ_DECODE = {"in_proj8"}  # decode rows (the state is written back); the others are verify rows (records)
+IN_PROJ_SOURCES = ["gated_deltanet_linear_mtp_gb300/csrc/gdn_in_proj_conv.cu",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_tcgen05.cuh",
+                   "gated_deltanet_linear_mtp_gb300/csrc/gdn_common.cuh"]
+
+
+def in_proj_counts(w: W.InProjWorkload, active: int, decode: bool):
+    """(algorithmic bytes, flops) of one call: W once, the active lanes' x rows, outputs, state read (and
+    written back, or the records), the taps; flops = 2 x rows x C x H of the projection (the convolution's
+    2 K per convolved output is counted too)."""
+    ob = 2 if w.out_dtype == "bf16" else 4
+    sb = 2 if w.conv_dtype == "bf16" else 4
+    rows = active * w.T
+    nbytes = (w.C * w.H * 2 + rows * w.H * 2 + rows * w.C * ob + active * (w.K - 1) * w.Cc * sb
+              + (active * (w.K - 1) * w.Cc * sb if decode else rows * w.Cc * sb) + w.Cc * (w.K + 1) * 4
+              + w.B * 4)
+    flops = 2 * rows * w.C * w.H + 2 * w.K * rows * w.Cc
+    return nbytes, flops
+
+
+def run_in_proj_arm(args, name: str, rank: int, world: int, local_rank: int):
+    """The in_proj projection with its conv1d epilogue on one workload: L2 flushed before every timed call (W, 50
+    MB, would otherwise stay in L2), CUDA events around the call alone."""
+    import torch
+
+    import gated_deltanet_linear_mtp_gb300 as gdn
+
+    w = IN_PROJ_NAMED[name]().replace(seed=IN_PROJ_NAMED[name]().seed + 7919 * rank)
+    decode = name in IN_PROJ_DECODE
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(world, "nccl")
+    x = w.arrays()
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+
+    d = {k: t(v) for k, v in x.items()}
+    odt = torch.bfloat16 if w.out_dtype == "bf16" else torch.float32
+    B, T = w.B, w.T
+    out = gdn.InProjOut(*(torch.empty(s, dtype=odt, device=device) for s in
+                          ((B, T, w.HK, w.DK), (B, T, w.HK, w.DK), (B, T, w.HV, w.DV), (B, T, w.HV, w.DV),
+                           (B, T, w.HV), (B, T, w.HV))))
+    rec = None if decode else torch.empty((B, T, w.Cc), dtype=d["conv_state"].dtype, device=device)
+
+    def call():
+        gdn.gdn_in_proj_conv(d["x"], d["W"], d["conv_w"], d["conv_b"], d["conv_state"], d["indices"], out, decode,
+                             rec, silu=w.silu)
+
+    stream = torch.cuda.current_stream(device)
+    flush = _Flush(device)
+    sampler = ClockSampler(local_rank)
+    for _ in range(args.warmup):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    n_timed = max(args.steps, 1)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_timed)]
+    sampler.start()
+    t_wall = time.perf_counter()
+    for e in evs:
+        flush()
+        e[0].record(stream)
+        call()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    sampler.stop()
+    ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = max_over_ranks(sum(ms), dist, device)
+    active = int((x["indices"] >= 0).sum())
+    nbytes, flops = in_proj_counts(w, active, decode)
+    avg_us = statistics.mean(ms) * 1e3
+    peak, peak_src = hbm_peak()
+    tpeak, tpeak_src = tensor_peak()
+    achieved = nbytes / (avg_us * 1e-6) / 1e9
+    tflops = flops / (avg_us * 1e-6) / 1e12
+    hbm_frac, tensor_frac = achieved / peak, tflops / tpeak
+    bound = "hbm" if hbm_frac >= tensor_frac else "tensor"
+    # end to end: x in from pinned host memory, the six outputs (and the records) back, every step
+    x_host = torch.empty(d["x"].shape, dtype=d["x"].dtype).pin_memory()
+    x_host.copy_(d["x"])
+    outs = [out.q, out.k, out.v, out.z, out.b, out.a] + ([] if rec is None else [rec])
+    back = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+
+    def e2e_step():
+        d["x"].copy_(x_host, non_blocking=True)
+        call()
+        for h, o in zip(back, outs):
+            h.copy_(o, non_blocking=True)
+
+    e2e_ms, _ = _timed_calls(e2e_step, max(3, min(args.steps, 50)), 3, stream, ClockSampler(local_rank))
+    e2e_ms_step = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    h2d = x_host.numel() * 2
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    props = torch.cuda.get_device_properties(device)
+    rows = active * T
+    result = {
+        "metric": IN_PROJ_METRIC, "value": rows * n_timed * world / (total_ms * 1e-3), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "timed_steps": n_timed, "warmup": args.warmup,
+        "ms_per_step": total_ms / n_timed, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x bf16 -> f32", "data": "synthetic (seeded numpy draws, random-init weights)",
+        "config": {"workload": w.name, "B": B, "T": T, "rows": rows, "H": w.H, "C": w.C, "Cc": w.Cc, "K": w.K,
+                   "HK": w.HK, "HV": w.HV, "DK": w.DK, "DV": w.DV, "conv_dtype": w.conv_dtype,
+                   "out_dtype": w.out_dtype, "mode": "decode (state written back)" if decode else
+                   "verify (state read, records written)",
+                   "l2": "flushed before every timed call (256 MiB write + read, outside the events)",
+                   "parallelism": f"replicas x{world}", "timing": "CUDA events per call, summed; max over ranks",
+                   "e2e": "x copied in from pinned host memory and every output copied back per step"},
+        "roofline": {"kernel": "gdn_in_proj_conv_kernel", "bound": bound,
+                     "achieved": achieved if bound == "hbm" else tflops, "peak": peak if bound == "hbm" else tpeak,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": hbm_frac if bound == "hbm" else tensor_frac,
+                     "peak_source": (peak_src if bound == "hbm" else tpeak_src) + ", of measured",
+                     "hbm": {"achieved_gbs": achieved, "frac": hbm_frac, "frac_nominal": achieved / NOMINAL_HBM_GBS},
+                     "tensor": {"achieved_tflops": tflops, "frac": tensor_frac},
+                     "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops, "avg_launch_us": avg_us,
+                     "traffic": recorded_traffic("in_proj_conv", w.name, IN_PROJ_SOURCES)},
+        "e2e": {"value": rows * world / (e2e_ms_step * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
+        "gpu_launches": n_timed, "clocks": sampler.summary(), "device": props.name,
+        "sm_count": props.multi_processor_count, "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = _in_proj_cpu_baseline(w, x, decode, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
+def _in_proj_lane(orc, w, x, b: int, decode: bool):
+    """The oracle's in_proj + convolution of lane b alone (on a copy of the state)."""
+    d = dict(T=w.T, H=w.H, HK=w.HK, HV=w.HV, DK=w.DK, DV=w.DV, K=w.K, num_slots=w.num_slots, x_dtype="bf16",
+             conv_dtype=w.conv_dtype, silu=int(w.silu))
+    orc.in_proj_conv(d, np.ascontiguousarray(x["x"][b:b + 1]), x["W"], x["conv_w"], x["conv_b"],
+                     x["conv_state"].copy() if decode else x["conv_state"], x["indices"][b:b + 1], write_pool=decode,
+                     records=not decode)
+
+
+def _in_proj_cpu_baseline(w, x, decode: bool, seconds: float) -> dict:
+    import oracle
+
+    orc = oracle.default()
+    cores = host_cores()
+    lanes = [b for b in range(w.B) if x["indices"][b] >= 0]
+    work = [(lambda b=b: _in_proj_lane(orc, w, x, b, decode)) for b in lanes]
+    done, dt = oracle_throughput(work, seconds, min(cores, max(1, len(work))), cycle=True)
+    v = done * w.T / dt
+    return {"value": v, "unit": "rows/s", "cores": min(cores, max(1, len(work))), "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"the oracle's in_proj + convolution of single lanes of {w.name} (T = {w.T} rows each) over and "
+                      f"over for {seconds:g} s, one lane per thread, fp64 C loops; rows/s = lanes done x T / time"}
+
+
+def run_in_proj_reference_arm(args, name: str, rank: int, world: int):
+    """The reference arm of an in_proj workload: the oracle, each step every active lane once (one per thread)."""
+    if rank != 0:
+        return
+    import oracle
+
+    w = IN_PROJ_NAMED[name]()
+    decode = name in IN_PROJ_DECODE
+    x = w.arrays()
+    orc = oracle.default()
+    cores = host_cores()
+    lanes = [b for b in range(w.B) if x["indices"][b] >= 0]
+    t0 = time.perf_counter()
+    _in_proj_lane(orc, w, x, lanes[0], decode)
+    t_lane = max(time.perf_counter() - t0, 1e-9)
+    threads = min(cores, len(lanes))
+    n = int(max(1, min(len(lanes), threads * args.ref_seconds / (args.steps + args.warmup) / t_lane)))
+    work = [(lambda b=b: _in_proj_lane(orc, w, x, b, decode)) for b in lanes[:n]]
+    for _ in range(args.warmup):
+        oracle_throughput(work, 1e9, min(threads, n))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_throughput(work, 1e9, min(threads, n))
+    dt = time.perf_counter() - t0
+    v = n * w.T * args.steps / dt
+    desc = (f"each step: the oracle's in_proj + convolution of {n} of the {len(lanes)} active lanes of {w.name}, one "
+            f"lane per thread on {min(threads, n)} threads, fp64 C loops; rows/s = lanes x T / time")
+    print(json.dumps({
+        "impl": "reference", "metric": IN_PROJ_METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w.name},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": min(threads, n), "kind": "oracle",
+                         "cpu_model": cpu_model(), "sample": desc},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_prefill_reference_arm(args, pw, rank: int, world: int):
     """The reference arm of a prefill workload: the oracle on every host core, each step the first L tokens of
     one (prompt, value head) pair per core, L sized so that warm-up + steps take about --ref-seconds.
@@ -1282,7 +1480,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.NAMED) + ["sweep", "sweep_replay", "sweep_fused"] + sorted(PREFILL_NAMED)
-                    + ["gated_norm"], default="verify4")
+                    + ["gated_norm"] + sorted(IN_PROJ_NAMED), default="verify4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
@@ -1295,6 +1493,12 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_env()
+    if args.workload in IN_PROJ_NAMED:
+        if args.impl == "reference":
+            run_in_proj_reference_arm(args, args.workload, rank, world)
+        else:
+            run_in_proj_arm(args, args.workload, rank, world, local_rank)
+        return 0
     if args.workload in PREFILL_NAMED or args.workload == "gated_norm":
         if args.impl == "reference":
             if args.workload == "gated_norm":

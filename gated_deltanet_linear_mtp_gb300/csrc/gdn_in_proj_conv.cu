@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <climits>
 #include <cstdint>
 
 #include "gdn.h"
@@ -38,7 +40,10 @@ namespace {
 constexpr int kIpM = 128;                  // output channels per tile: the accumulator's tensor-memory lanes
 constexpr int kIpKC = 64;                  // hidden columns per stage: one 128-byte swizzled box
 constexpr uint32_t kIpWBox = kIpM * kIpKC * 2;  // bytes of W per stage
-constexpr int kIpThreads = 128;
+constexpr int kIpEpiWarps = 4;            // warps 0-3: one per 32 tensor-memory lanes (channels); the epilogue
+constexpr int kIpProducerWarp = 4;         // lane 0: the TMA loads
+constexpr int kIpMmaWarp = 5;              // lane 0: the MMAs; the warp allocates the tensor memory
+constexpr int kIpThreads = 32 * 6;
 constexpr int kIpMaxN = 256;               // rows per tile (the MMA's N)
 constexpr int kIpMaxCluster = 8;
 constexpr int kIpMaxStages = 8;
@@ -52,12 +57,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+__device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_barrier() {
@@ -65,8 +68,8 @@ __device__ __forceinline__ void cluster_barrier() {
 }
 
 // Shared memory, from a 1024-byte aligned base: `stages` x (W box | rows box), then the mbarriers full[stages],
-// empty[stages], done, then the tensor-memory address.  The epilogue's [N][128] fp32 accumulator copy reuses the
-// ring (N * 512 bytes <= the ring, checked on the host).
+// empty[stages], done, then the tensor-memory address.  The epilogue's partial sums, [ks][lanes a rank owns][T][128]
+// fp32, reuse the ring (ring_holds, checked on the host).
 __host__ __device__ inline uint32_t ip_stage_bytes(int N) { return kIpWBox + (uint32_t)N * 128u; }
 __host__ __device__ inline uint32_t ip_bar_offset(int N, int S) { return ip_stage_bytes(N) * (uint32_t)S; }
 __host__ __device__ inline uint32_t ip_smem_bytes(int N, int S) {
@@ -114,20 +117,42 @@ __global__ void __launch_bounds__(kIpThreads, 1)
     const int c0 = rank * g.kchunks / g.ks, nk = (rank + 1) * g.kchunks / g.ks - c0;  // nk >= 1 (host)
     const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
 
-    if (tid == 0) {
+    const int producer = 32 * kIpProducerWarp;
+    if (tid == producer) {
         for (int s = 0; s < 2 * S + 1; ++s) mbar_init(bars + 8u * s, 1);
         fence_mbar_init();
         failed = 0;
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), ncols);
+    if (warp == kIpMmaWarp) tmem_alloc(smem_u32(tmem_slot), ncols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // The epilogue's inputs do not depend on the product: warps 0-3 (thread = channel c) load the channel's taps and
+    // bias and the first owned lane's index and state entries now, so that their latency hides behind the main loop.
+    const int64_t c = (int64_t)ctile * kIpM + tid;
+    const bool epi = warp < kIpEpiWarps;
+    const bool chan = epi && c < p.C, conv = c < p.Cc;
+    const int T = p.T;
+    const int n_own = rank < g.lanes_per_tile ? (g.lanes_per_tile - rank + g.ks - 1) / g.ks : 0;
+    float w[K], bias = 0.f, st0[K - 1];
+#pragma unroll
+    for (int j = 0; j < K; ++j) w[j] = chan && conv ? p.conv_w[c * K + j] : 0.f;
+    if (chan && conv && p.conv_b != nullptr) bias = p.conv_b[c];
+    const int b0 = rtile * g.lanes_per_tile + rank;
+    const int slot0 = epi && n_own > 0 && b0 < p.B ? p.indices[b0] : -2;  // -2: no lane
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)
+        st0[j] = chan && conv && slot0 >= 0 && slot0 < p.num_slots
+                     ? load_elem(p.state, p.state_bf16, ((int64_t)slot0 * (K - 1) + j) * p.Cc + c)
+                     : 0.f;
+
+    // roles by whole warps: lane 0 of the producer warp loads, lane 0 of the MMA warp issues the MMAs, the other
+    // lanes of those warps wait at __syncwarp (a lane polling beside them would take their issue slots)
     int issued = 0;  // producer: loads issued
-    if (tid == 0) {
-        // producer: one stage = W's 128 x 64 box and the tile's N x 64 rows box, on the stage's full barrier
+    if (tid == producer) {
+        // one stage = W's 128 x 64 box and the tile's N x 64 rows box, on the stage's full barrier
         const int row0 = rtile * g.lanes_per_tile * p.T;
         for (int i = 0; i < nk; ++i) {
             const int s = i % S;
@@ -141,9 +166,9 @@ __global__ void __launch_bounds__(kIpThreads, 1)
             tma_load_2d(dst + kIpWBox, &xmap, (c0 + i) * kIpKC, row0, bars + 8u * s);
             issued = i + 1;
         }
-    } else if (tid == 32) {
-        // MMA issuer: D[128 x N] (+)= W box . rows box^T, four K = 16 steps per stage; each stage's completion
-        // frees it for the producer, the last one signals the epilogue
+    } else if (tid == 32 * kIpMmaWarp) {
+        // D[128 x N] (+)= W box . rows box^T, four K = 16 steps per stage; each stage's completion frees it for the
+        // producer, the last one signals the epilogue
         const uint32_t idesc = umma_idesc_bf16(kIpM, N);
         for (int i = 0; i < nk; ++i) {
             const int s = i % S;
@@ -161,13 +186,14 @@ __global__ void __launch_bounds__(kIpThreads, 1)
         }
         umma_commit(done_bar);
     }
-    if (!mbar_wait_bounded(done_bar, 0, kIpWaitPolls)) failed = 1;
+    if (!epi) __syncwarp();
+    if (epi && !mbar_wait_bounded(done_bar, 0, kIpWaitPolls)) failed = 1;
     tc_fence_after();
     __syncthreads();
     const bool ok = failed == 0;
     if (!ok) {
         // a wait ran out: let the MMAs and the copies already issued finish before the memory is reused or freed
-        if (tid == 0) {
+        if (tid == producer) {
             mbar_wait_bounded(done_bar, 0, kIpWaitPolls);
             for (int i = issued > S ? issued - S : 0; i < issued; ++i)
                 mbar_wait_bounded(bars + 8u * (i % S), (uint32_t)(i / S) & 1u, kIpWaitPolls);
@@ -176,77 +202,105 @@ __global__ void __launch_bounds__(kIpThreads, 1)
         __syncthreads();
     }
 
-    // the accumulator to shared memory: acc[col][channel], thread = channel (tensor-memory lane 32 warp + lane)
-    float* const acc = reinterpret_cast<float*>(gbase);
-    if (ok) {
+    // The partial sums to their owners.  Lane li of the tile belongs to rank li mod ks (as its m = li / ks-th lane);
+    // every rank writes its accumulator column (li, t) into the owner's ring as part[src = rank][m][t][channel]
+    // (thread = channel = tensor-memory lane 32 warp + lane): remote stores for the other ranks, which cost no round
+    // trip.  A first cluster barrier makes sure every rank's main loop is done with its ring, a second that every
+    // partial has arrived; after it all reads are local.
+    const int mmax = (g.lanes_per_tile + g.ks - 1) / g.ks;  // lanes a rank owns at most
+    float* const part = reinterpret_cast<float*>(gbase);     // [ks][mmax][T][128]
+    if (g.ks > 1) cluster_barrier();
+    if (ok && epi) {
+        int li = 0, t = 0, owner = 0, m = 0;  // lane, row, owning rank and its lane index of column col + j
         for (int col = 0; col < N; col += 16) {
             float f[16];
             tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)col, f);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[(col + j) * kIpM + tid] = f[j];
+            for (int j = 0; j < 16; ++j) {
+                if (li < g.lanes_per_tile) {
+                    float* const e = part + (((rank * mmax + m) * T + t) * kIpM + tid);
+                    if (owner == rank)
+                        *e = f[j];
+                    else
+                        st_cluster(e, (uint32_t)owner, f[j]);
+                }
+                if (++t == T) {
+                    t = 0;
+                    ++li;
+                    if (++owner == g.ks) {
+                        owner = 0;
+                        ++m;
+                    }
+                }
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (g.ks > 1) cluster_barrier();  // every rank's partial sums are in its shared memory
+    if (g.ks > 1) cluster_barrier();  // every partial is in its owner's ring
 
-    // each rank takes lanes rank, rank + ks, ... of the tile; thread = channel c
-    const int64_t c = (int64_t)ctile * kIpM + tid;
-    const int T = p.T;
-    for (int li = rank; ok && li < g.lanes_per_tile; li += g.ks) {
-        const int b = rtile * g.lanes_per_tile + li;
-        if (b >= p.B) break;
-        const int slot = p.indices[b];
+    // each rank takes lanes rank, rank + ks, ... of the tile (the first one's loads went out before the main loop);
+    // thread = channel c.  The loops are kept rolled: after an L2 flush the code is fetched from memory too.
+    // where the channel's values go: q | k (HK * DK each), v (HV * DV); z (HV * DV), b, a (HV each)
+    const int64_t qc = (int64_t)p.HK * p.DK, vc = (int64_t)p.HV * p.DV, cz = c - p.Cc;
+    void* dst;
+    int64_t dc, dstride;
+    if (conv) {
+        dst = c < qc ? p.q : c < 2 * qc ? p.k : p.v;
+        dc = c < qc ? c : c < 2 * qc ? c - qc : c - 2 * qc;
+        dstride = c < 2 * qc ? qc : vc;
+    } else {
+        dst = cz < vc ? p.z : cz < vc + p.HV ? p.bo : p.ao;
+        dc = cz < vc ? cz : cz < vc + p.HV ? cz - vc : cz - vc - p.HV;
+        dstride = cz < vc ? vc : p.HV;
+    }
+#pragma unroll 1
+    for (int m = 0; ok && epi && m < n_own; ++m) {
+        const int b = b0 + m * g.ks;
+        int slot = slot0;
+        float st[K - 1];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) st[j] = st0[j];
+        if (m > 0) {
+            slot = b < p.B ? p.indices[b] : -2;
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j)
+                st[j] = chan && conv && slot >= 0 && slot < p.num_slots
+                            ? load_elem(p.state, p.state_bf16, ((int64_t)slot * (K - 1) + j) * p.Cc + c)
+                            : 0.f;
+        }
         if (slot < 0 || slot >= p.num_slots) {
-            if (slot != -1 && ctile == 0 && tid == 0 && p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_INDEX);
+            if (slot != -1 && slot != -2 && ctile == 0 && tid == 0 && p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_INDEX);
             continue;
         }
-        if (c >= p.C) continue;
-        const bool conv = c < p.Cc;
-        // the full sums over the ranks (in rank order: every rank forms the same value), rounded to the state type
-        // for the convolved channels, back into this rank's copy: only this thread reads them from here on
+        if (!chan) continue;
+        // the full sums over the ranks (in rank order), rounded to the state type for the convolved channels, into
+        // the src = 0 slot: only this thread reads them from here on
+        float* const u = part + (m * T) * kIpM + tid;  // u[t * kIpM]
+#pragma unroll 1
         for (int t = 0; t < T; ++t) {
-            float* e = acc + (li * T + t) * kIpM + tid;
-            float v = 0.f;
-            for (int r = 0; r < g.ks; ++r) v += r == rank ? *e : ld_cluster(e, (uint32_t)r);
+            float v = u[t * kIpM];
+            for (int r = 1; r < g.ks; ++r) v += part[((r * mmax + m) * T + t) * kIpM + tid];
             if (conv && p.state_bf16) v = round_bf16(v);
-            *e = v;
+            u[t * kIpM] = v;
         }
-        const float* u = acc + li * T * kIpM + tid;  // u[t * kIpM]
         const int64_t row0 = (int64_t)b * T;
         if (!conv) {
-            const int64_t cz = c - p.Cc, zc = (int64_t)p.HV * p.DV;
-            for (int t = 0; t < T; ++t) {
-                if (cz < zc)
-                    store_elem(p.z, p.out_bf16, (row0 + t) * zc + cz, u[t * kIpM]);
-                else if (cz < zc + p.HV)
-                    store_elem(p.bo, p.out_bf16, (row0 + t) * p.HV + (cz - zc), u[t * kIpM]);
-                else
-                    store_elem(p.ao, p.out_bf16, (row0 + t) * p.HV + (cz - zc - p.HV), u[t * kIpM]);
-            }
+#pragma unroll 1
+            for (int t = 0; t < T; ++t) store_elem(dst, p.out_bf16, (row0 + t) * dstride + dc, u[t * kIpM]);
             continue;
         }
         // the convolution over seq = state (K - 1 entries, oldest first), u[0 .. T-1]
-        float st[K - 1], w[K];
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j)
-            st[j] = load_elem(p.state, p.state_bf16, ((int64_t)slot * (K - 1) + j) * p.Cc + c);
-#pragma unroll
-        for (int j = 0; j < K; ++j) w[j] = p.conv_w[c * K + j];
-        const float bias = p.conv_b != nullptr ? p.conv_b[c] : 0.f;
         auto seq = [&](int i) -> float {
             if (i >= K - 1) return u[(i - (K - 1)) * kIpM];
-            float s = st[0];
+            float x = st[0];
 #pragma unroll
             for (int j = 1; j < K - 1; ++j)
-                if (i == j) s = st[j];
-            return s;
+                if (i == j) x = st[j];
+            return x;
         };
-        // output tensor and offset of channel c: q | k (HK * DK each), then v (HV * DV)
-        const int64_t qc = (int64_t)p.HK * p.DK, vc = (int64_t)p.HV * p.DV;
-        void* const dst = c < qc ? p.q : c < 2 * qc ? p.k : p.v;
-        const int64_t dc = c < qc ? c : c < 2 * qc ? c - qc : c - 2 * qc, dstride = c < 2 * qc ? qc : vc;
+#pragma unroll 1
         for (int t = 0; t < T; ++t) {
             float y = bias;
 #pragma unroll
@@ -267,7 +321,7 @@ __global__ void __launch_bounds__(kIpThreads, 1)
 
     __syncthreads();
     if (g.ks > 1) cluster_barrier();  // no rank leaves while another may still read its partial sums
-    if (warp == 1) tmem_dealloc(tmem, ncols);
+    if (warp == kIpMmaWarp) tmem_dealloc(tmem, ncols);
 }
 
 // The convolution state after each lane's first L accepted rows: pool[slot, j, c] = seq[L + j, c] with seq = the
@@ -315,39 +369,101 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int cols, int64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int ip_sm_count() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 148;
-    return sms;
-}
-
 }  // namespace
 
-// Tiling: a tile holds whole lanes, all B of them when B * T <= 256 rows, else 256 / T.  The hidden dimension is
-// split over ks ranks (a cluster) so that the grid holds about two CTAs per SM, each rank keeping at least one
-// chunk; the ring takes what two CTAs per SM leave (one for N > 64), 2..8 stages.
-IpTiling in_proj_tiling(int B, int T, int H, int64_t C, int sms) {
+// Tiling.  A tile holds whole lanes: all B of them when B * T <= 256 rows, else 256 / T.  The ring takes 2..8
+// stages within what three CTAs per SM leave (N <= 32), two (N <= 64), or one.  The hidden dimension is split
+// over ks ranks (a cluster), ks chosen to minimise waves x chunks per CTA, where a wave is the clusters the GPU
+// holds at once (the occupancy calculator: a cluster's CTAs must share a GPC, so 2 x 152 CTA slots do not take
+// 2 x 152 / ks clusters); ties go to the smaller ks (less reduction).
+// the ring holds the epilogue's partial sums of a split into g.ks ranks
+bool ring_holds(const IpTiling& g, int T) {
+    const uint64_t mmax = (uint64_t)(g.lanes_per_tile + g.ks - 1) / g.ks;
+    return (uint64_t)g.stages * ip_stage_bytes(g.N) >= (uint64_t)g.ks * mmax * T * kIpM * 4;
+}
+
+// everything but the split, from the shape alone
+IpTiling base_tiling(int B, int T, int H) {
     IpTiling g{};
     g.lanes_per_tile = (int64_t)B * T <= kIpMaxN ? B : kIpMaxN / T;
     g.N = (g.lanes_per_tile * T + 15) / 16 * 16;
     g.kchunks = (H + kIpKC - 1) / kIpKC;
-    const int64_t tiles = ((C + kIpM - 1) / kIpM) * (int64_t)((B + g.lanes_per_tile - 1) / g.lanes_per_tile);
-    int64_t ks = (2 * (int64_t)sms) / std::max<int64_t>(tiles, 1);
-    ks = std::min<int64_t>(std::min<int64_t>(ks, kIpMaxCluster), g.kchunks);
-    g.ks = (int)std::max<int64_t>(ks, 1);
-    const uint32_t budget = g.N <= 64 ? 110u * 1024u : 220u * 1024u;
+    const uint32_t budget = g.N <= 32 ? 72u * 1024u : g.N <= 64 ? 110u * 1024u : 220u * 1024u;
     g.stages = (int)std::min<uint32_t>(kIpMaxStages, std::max<uint32_t>(2, budget / ip_stage_bytes(g.N)));
+    g.ks = 1;
     return g;
 }
 
 template <int K>
-cudaError_t launch_in_proj_k(const InProjConvParams& p, const IpTiling& g, const CUtensorMap& wmap,
-                             const CUtensorMap& xmap, cudaStream_t s) {
-    auto kernel = gdn_in_proj_conv_kernel<K>;
+IpTiling in_proj_tiling(int B, int T, int H, int64_t C) {
+    IpTiling g = base_tiling(B, T, H);
+    const int64_t tiles = ((C + kIpM - 1) / kIpM) * (int64_t)((B + g.lanes_per_tile - 1) / g.lanes_per_tile);
     const uint32_t smem = ip_smem_bytes(g.N, g.stages);
+    int64_t best = INT64_MAX;
+    for (int ks = 1; ks <= std::min(kIpMaxCluster, g.kchunks); ++ks) {
+        IpTiling c = g;
+        c.ks = ks;
+        if (!ring_holds(c, T)) continue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ks, (unsigned)((C + kIpM - 1) / kIpM), 1);
+        cfg.blockDim = dim3(kIpThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)ks;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gdn_in_proj_conv_kernel<K>, &cfg) != cudaSuccess ||
+            clusters < 1) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        const int64_t cost = ((tiles + clusters - 1) / clusters) * ((g.kchunks + ks - 1) / ks);
+        if (cost < best) {
+            best = cost;
+            g.ks = ks;
+        }
+    }
+    return g;
+}
+
+// The split last chosen on each device (one cache per K), with a hash of its (B, T, H, C) in the same word: the occupancy
+// queries run once per shape.  Only ks is cached, clamped to the shape's chunks on the way out, so a stale or
+// colliding entry can cost speed but never correctness.
+template <int K>
+IpTiling cached_tiling(int B, int T, int H, int64_t C) {
+    static std::atomic<uint64_t> cache[64];  // hash << 8 | ks; zero (static): empty
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return in_proj_tiling<K>(B, T, H, C);
+    const uint64_t h = (((uint64_t)B * 0x9E3779B97F4A7C15ull) ^ ((uint64_t)T << 40) ^ ((uint64_t)H << 20) ^
+                        (uint64_t)C) & 0x00FFFFFFFFFFFFFFull;
+    const uint64_t c = cache[dev].load(std::memory_order_relaxed);
+    if (c != 0 && (c >> 8) == h) {
+        IpTiling g = base_tiling(B, T, H);
+        g.ks = std::max(1, std::min<int>((int)(c & 0xffu), std::min(kIpMaxCluster, g.kchunks)));
+        while (g.ks > 1 && !ring_holds(g, T)) --g.ks;
+        return g;
+    }
+    const IpTiling g = in_proj_tiling<K>(B, T, H, C);
+    cache[dev].store(h << 8 | (uint64_t)g.ks, std::memory_order_relaxed);
+    return g;
+}
+
+template <int K>
+cudaError_t launch_in_proj_k(const InProjConvParams& p, const CUtensorMap& wmap, cudaStream_t s) {
+    auto kernel = gdn_in_proj_conv_kernel<K>;
+    // the ring of this shape (the split does not change it), opened before the occupancy queries see the kernel
+    const IpTiling b = base_tiling(p.B, p.T, p.H);
+    const uint32_t smem = ip_smem_bytes(b.N, b.stages);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    const IpTiling g = cached_tiling<K>(p.B, p.T, p.H, p.C);
+    if (!ring_holds(g, p.T)) return cudaErrorInvalidConfiguration;  // ks = 1 always fits: lanes x T <= N
+    CUtensorMap xmap;
+    if (!encode_rows_map(&xmap, p.x, p.H, (int64_t)p.B * p.T, g.N)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)g.ks, (unsigned)((p.C + kIpM - 1) / kIpM),
                        (unsigned)((p.B + g.lanes_per_tile - 1) / g.lanes_per_tile));
@@ -366,15 +482,12 @@ cudaError_t launch_in_proj_k(const InProjConvParams& p, const IpTiling& g, const
 
 cudaError_t launch_in_proj_conv(const InProjConvParams& p, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
-    const IpTiling g = in_proj_tiling(p.B, p.T, p.H, p.C, ip_sm_count());
-    if ((uint64_t)g.stages * ip_stage_bytes(g.N) < (uint64_t)g.N * kIpM * 4) return cudaErrorInvalidConfiguration;
-    CUtensorMap wmap, xmap;
-    if (!encode_rows_map(&wmap, p.W, p.H, p.C, kIpM) || !encode_rows_map(&xmap, p.x, p.H, (int64_t)p.B * p.T, g.N))
-        return cudaErrorInvalidValue;
+    CUtensorMap wmap;
+    if (!encode_rows_map(&wmap, p.W, p.H, p.C, kIpM)) return cudaErrorInvalidValue;
     switch (p.K) {
-    case 2: return launch_in_proj_k<2>(p, g, wmap, xmap, s);
-    case 3: return launch_in_proj_k<3>(p, g, wmap, xmap, s);
-    case 4: return launch_in_proj_k<4>(p, g, wmap, xmap, s);
+    case 2: return launch_in_proj_k<2>(p, wmap, s);
+    case 3: return launch_in_proj_k<3>(p, wmap, s);
+    case 4: return launch_in_proj_k<4>(p, wmap, s);
     default: return cudaErrorInvalidValue;
     }
 }
