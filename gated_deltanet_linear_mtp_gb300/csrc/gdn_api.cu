@@ -442,6 +442,7 @@ gdn_status gdn_in_proj_conv(const gdn_conv_dims* dims, const void* x, const void
     p.conv_b = conv_b;
     p.state = conv_state;
     p.state_bf16 = dims->conv_dtype == GDN_BF16;
+    p.state_vec = Cc % 8 == 0 && aligned(conv_state, 16);
     p.indices = state_indices;
     p.write_state = write_state;
     p.q = out->q;

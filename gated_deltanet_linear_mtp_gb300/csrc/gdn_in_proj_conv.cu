@@ -44,7 +44,8 @@ constexpr int kIpEpiWarps = 4;            // warps 0-3: one per 32 tensor-memory
 constexpr int kIpProducerWarp = 4;         // lane 0: the TMA loads
 constexpr int kIpMmaWarp = 5;              // lane 0: the MMAs; the warp allocates the tensor memory
 constexpr int kIpThreads = 32 * 6;
-constexpr int kIpMaxN = 256;               // rows per tile (the MMA's N)
+constexpr int kIpMaxN = 64;                // rows per tile (the MMA's N): more lanes per CTA serialise the epilogue
+constexpr int kIpMaxPf = 16;               // lanes whose indices and state rows the epilogue warps gather in advance
 constexpr int kIpMaxCluster = 8;
 constexpr int kIpMaxStages = 8;
 constexpr uint32_t kIpWaitPolls = GDN_WAIT_POLLS;
@@ -63,6 +64,12 @@ __device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -72,8 +79,13 @@ __device__ __forceinline__ void cluster_barrier() {
 // fp32, reuse the ring (ring_holds, checked on the host).
 __host__ __device__ inline uint32_t ip_stage_bytes(int N) { return kIpWBox + (uint32_t)N * 128u; }
 __host__ __device__ inline uint32_t ip_bar_offset(int N, int S) { return ip_stage_bytes(N) * (uint32_t)S; }
-__host__ __device__ inline uint32_t ip_smem_bytes(int N, int S) {
-    return ip_bar_offset(N, S) + 8u * (2u * S + 1u) + 16u + 1024u;  // + alignment slack
+__host__ __device__ inline uint32_t ip_tslot_offset(int N, int S) { return ip_bar_offset(N, S) + 8u * (2u * S + 1u); }
+// the gathered lane indices [kIpMaxPf] int32, then the gathered state rows [lanes][K - 1][128] (4 bytes a channel)
+__host__ __device__ inline uint32_t ip_slots_offset(int N, int S) { return (ip_tslot_offset(N, S) + 4u + 15u) & ~15u; }
+__host__ __device__ inline uint32_t ip_pf_offset(int N, int S) { return ip_slots_offset(N, S) + 4u * kIpMaxPf; }
+__host__ __device__ inline uint32_t ip_pf_bytes(int lanes, int K) { return (uint32_t)lanes * (K - 1) * kIpM * 4u; }
+__host__ __device__ inline uint32_t ip_smem_bytes(int N, int S, int pf_lanes, int K) {
+    return ip_pf_offset(N, S) + ip_pf_bytes(pf_lanes, K) + 1024u;  // + alignment slack
 }
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -95,6 +107,7 @@ __device__ __forceinline__ float load_elem(const void* base, bool bf16, int64_t 
 // `kchunks` 64-column chunks, `stages` ring stages.
 struct IpTiling {
     int N, lanes_per_tile, ks, kchunks, stages;
+    int pf_lanes;  // lanes whose indices (and, in tiles of convolved channels, state rows) are gathered in advance
 };
 
 // K: convolution taps (2..4)
@@ -113,7 +126,9 @@ __global__ void __launch_bounds__(kIpThreads, 1)
     const uint32_t stage_b = ip_stage_bytes(N);
     const uint32_t bars = base + ip_bar_offset(N, S);  // full s: + 8 s; empty s: + 8 (S + s); done: + 16 S
     const uint32_t done_bar = bars + 16u * S;
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + ip_bar_offset(N, S) + 8u * (2u * S + 1u));
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + ip_tslot_offset(N, S));
+    int* const slots_s = reinterpret_cast<int*>(gbase + ip_slots_offset(N, S));
+    unsigned char* const pf = gbase + ip_pf_offset(N, S);
     const int c0 = rank * g.kchunks / g.ks, nk = (rank + 1) * g.kchunks / g.ks - c0;  // nk >= 1 (host)
     const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
 
@@ -147,6 +162,32 @@ __global__ void __launch_bounds__(kIpThreads, 1)
         st0[j] = chan && conv && slot0 >= 0 && slot0 < p.num_slots
                      ? load_elem(p.state, p.state_bf16, ((int64_t)slot0 * (K - 1) + j) * p.Cc + c)
                      : 0.f;
+    // With more lanes per rank (g.pf_lanes > 0): the first pf_n owned lanes' indices into shared memory, then (tiles
+    // of convolved channels, 16-byte aligned rows) their state rows by 16-byte cp.async copies, all in flight
+    // during the main loop; the epilogue then reads shared memory only.
+    const int pf_n = epi ? min(n_own, g.pf_lanes) : 0;
+    const bool pf_state = pf_n > 0 && p.state_vec && (int64_t)ctile * kIpM < p.Cc;
+    if (pf_n > 0) {
+        if (tid < pf_n) {
+            const int b = b0 + tid * g.ks;
+            slots_s[tid] = b < p.B ? p.indices[b] : -2;
+        }
+        named_sync(1, 32 * kIpEpiWarps);
+        if (pf_state) {
+            const int eb = p.state_bf16 ? 2 : 4;
+            const int cpr = (int)min((int64_t)kIpM, p.Cc - (int64_t)ctile * kIpM) * eb / 16;  // chunks of a row
+            const unsigned char* const src0 =
+                static_cast<const unsigned char*>(p.state) + (int64_t)ctile * kIpM * eb;
+            for (int i = tid; i < pf_n * (K - 1) * cpr; i += 32 * kIpEpiWarps) {
+                const int m = i / ((K - 1) * cpr), r = i - m * ((K - 1) * cpr), j = r / cpr, q = r - j * cpr;
+                const int sl = slots_s[m];
+                if (sl >= 0 && sl < p.num_slots)
+                    cp_async16(smem_u32(pf + ((m * (K - 1) + j) * kIpM) * eb + q * 16),
+                               src0 + (((int64_t)sl * (K - 1) + j) * p.Cc) * eb + q * 16);
+            }
+            cp_async_commit();
+        }
+    }
 
     // roles by whole warps: lane 0 of the producer warp loads, lane 0 of the MMA warp issues the MMAs, the other
     // lanes of those warps wait at __syncwarp (a lane polling beside them would take their issue slots)
@@ -236,6 +277,7 @@ __global__ void __launch_bounds__(kIpThreads, 1)
             }
         }
     }
+    if (pf_state) cp_async_wait_all();  // the gathered state rows, before the barrier publishes them
     tc_fence_before();
     __syncthreads();
     if (g.ks > 1) cluster_barrier();  // every partial is in its owner's ring
@@ -262,7 +304,22 @@ __global__ void __launch_bounds__(kIpThreads, 1)
         float st[K - 1];
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) st[j] = st0[j];
-        if (m > 0) {
+        if (m < pf_n) {
+            slot = slots_s[m];
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j)
+                st[j] = pf_state && chan && conv && slot >= 0 && slot < p.num_slots
+                            ? (p.state_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(pf)[(m * (K - 1) + j) * kIpM + tid])
+                                            : reinterpret_cast<const float*>(pf)[(m * (K - 1) + j) * kIpM + tid])
+                            : st[j];
+            if (!pf_state && m > 0) {
+#pragma unroll
+                for (int j = 0; j < K - 1; ++j)
+                    st[j] = chan && conv && slot >= 0 && slot < p.num_slots
+                                ? load_elem(p.state, p.state_bf16, ((int64_t)slot * (K - 1) + j) * p.Cc + c)
+                                : 0.f;
+            }
+        } else if (m > 0) {
             slot = b < p.B ? p.indices[b] : -2;
 #pragma unroll
             for (int j = 0; j < K - 1; ++j)
@@ -383,12 +440,15 @@ bool ring_holds(const IpTiling& g, int T) {
 }
 
 // everything but the split, from the shape alone
-IpTiling base_tiling(int B, int T, int H) {
+// (N <= 32: three CTAs per SM, the first owned lane prefetched in registers; N = 48 or 64: two, up to kIpMaxPf
+// lanes gathered in shared memory)
+IpTiling base_tiling(int B, int T, int H, int K) {
     IpTiling g{};
     g.lanes_per_tile = (int64_t)B * T <= kIpMaxN ? B : kIpMaxN / T;
     g.N = (g.lanes_per_tile * T + 15) / 16 * 16;
     g.kchunks = (H + kIpKC - 1) / kIpKC;
-    const uint32_t budget = g.N <= 32 ? 72u * 1024u : g.N <= 64 ? 110u * 1024u : 220u * 1024u;
+    g.pf_lanes = g.N <= 32 ? 0 : std::min(g.lanes_per_tile, kIpMaxPf);
+    const uint32_t budget = (g.N <= 32 ? 72u * 1024u : 110u * 1024u) - ip_pf_bytes(g.pf_lanes, K);
     g.stages = (int)std::min<uint32_t>(kIpMaxStages, std::max<uint32_t>(2, budget / ip_stage_bytes(g.N)));
     g.ks = 1;
     return g;
@@ -396,9 +456,9 @@ IpTiling base_tiling(int B, int T, int H) {
 
 template <int K>
 IpTiling in_proj_tiling(int B, int T, int H, int64_t C) {
-    IpTiling g = base_tiling(B, T, H);
+    IpTiling g = base_tiling(B, T, H, K);
     const int64_t tiles = ((C + kIpM - 1) / kIpM) * (int64_t)((B + g.lanes_per_tile - 1) / g.lanes_per_tile);
-    const uint32_t smem = ip_smem_bytes(g.N, g.stages);
+    const uint32_t smem = ip_smem_bytes(g.N, g.stages, g.pf_lanes, K);
     int64_t best = INT64_MAX;
     for (int ks = 1; ks <= std::min(kIpMaxCluster, g.kchunks); ++ks) {
         IpTiling c = g;
@@ -442,7 +502,7 @@ IpTiling cached_tiling(int B, int T, int H, int64_t C) {
                         (uint64_t)C) & 0x00FFFFFFFFFFFFFFull;
     const uint64_t c = cache[dev].load(std::memory_order_relaxed);
     if (c != 0 && (c >> 8) == h) {
-        IpTiling g = base_tiling(B, T, H);
+        IpTiling g = base_tiling(B, T, H, K);
         g.ks = std::max(1, std::min<int>((int)(c & 0xffu), std::min(kIpMaxCluster, g.kchunks)));
         while (g.ks > 1 && !ring_holds(g, T)) --g.ks;
         return g;
@@ -456,8 +516,8 @@ template <int K>
 cudaError_t launch_in_proj_k(const InProjConvParams& p, const CUtensorMap& wmap, cudaStream_t s) {
     auto kernel = gdn_in_proj_conv_kernel<K>;
     // the ring of this shape (the split does not change it), opened before the occupancy queries see the kernel
-    const IpTiling b = base_tiling(p.B, p.T, p.H);
-    const uint32_t smem = ip_smem_bytes(b.N, b.stages);
+    const IpTiling b = base_tiling(p.B, p.T, p.H, K);
+    const uint32_t smem = ip_smem_bytes(b.N, b.stages, b.pf_lanes, K);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const IpTiling g = cached_tiling<K>(p.B, p.T, p.H, p.C);

@@ -65,6 +65,7 @@ struct InProjConvParams {
     const float* conv_b;    // [Cc] or nullptr
     void* state;            // [num_slots, K - 1, Cc]
     int state_bf16;
+    int state_vec;          // state on 16 bytes and Cc % 8 == 0: its rows are gathered in 16-byte pieces
     const int32_t* indices;
     int write_state;        // decode: the last K - 1 entries of each lane's sequence go back to its slot
     void* q;                // [B, T, HK, DK]

@@ -2,7 +2,8 @@
 
 The cases aim at what the kernel adds:
 * the tile edges: channel counts that leave the last 128-channel tile ragged, hidden sizes that leave the last
-  64-column chunk ragged, more than 256 rows (two row tiles, the second ragged);
+  64-column chunk ragged, more than 64 rows (several row tiles, the last ragged), lanes gathered ahead in shared
+  memory with aligned and unaligned state rows;
 * the split of the hidden dimension over a cluster (every small case runs 2..8 ranks; one chunk runs alone);
 * every tap count (2, 3, 4), T from 1 to 16, bf16 and fp32 state and outputs, SiLU on and off;
 * padded lanes (untouched, bit for bit), a bad index (flag bit), the decode write-back and the verify's records;
@@ -143,6 +144,9 @@ SMALL = [
     small("ip_K2_T8_one_chunk", B=2, T=8, H=64, K=2, conv="f32", out="bf16", seed=603),
     small("ip_T16", B=2, T=16, H=128, HK=1, HV=2, DK=64, DV=48, seed=604),
     small("ip_wide_heads", B=2, T=3, H=512, HK=2, HV=6, DK=128, DV=96, seed=605),
+    # 48 rows (lanes gathered ahead in shared memory) with 9 convolved channels: rows not 16-byte aligned, so the
+    # state comes by direct loads
+    small("ip_odd_channels_gathered", B=12, T=4, H=64, HK=1, HV=1, DK=3, DV=3, seed=608, pad=0.25),
 ]
 
 
@@ -154,7 +158,7 @@ def test_small(w, write_state):
 
 @pytest.mark.parametrize("write_state", [True, False], ids=["decode", "verify"])
 def test_two_row_tiles(write_state):
-    """320 rows: a tile of 64 lanes x 4 rows, then a ragged tile of 16 lanes."""
+    """320 rows: five tiles of 16 lanes x 4 rows (the lanes gathered ahead), a tile of only non-convolved channels."""
     w = small("ip_rows320", B=80, T=4, H=128, HK=1, HV=2, DK=32, DV=32, pad=0.1, seed=606, num_slots=90)
     check_call(w, w.arrays(), write_state)
 
@@ -228,7 +232,7 @@ def test_full_size(make, write_state):
 
 
 def test_full_size_512_rows_sampled():
-    """The 512-row verify (two row tiles of 64 lanes): lanes from both tiles and both tile edges against the oracle
+    """The 512-row verify (eight row tiles of 16 lanes): lanes from several tiles and their edges against the oracle
     run on those lanes alone."""
     w = W.in_proj_verify512()
     x = w.arrays()
