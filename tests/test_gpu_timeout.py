@@ -1,7 +1,8 @@
 """The bounded waits of the copy-fed kernels, made to run out without a fault.
 
 A test build of the library (flags GDN_TEST_MISSING_COPY and a short GDN_WAIT_POLLS) leaves one bulk / TMA
-copy unissued and never arrives on its mbarrier, so the wait for it can only run out.  That is the same path
+copy unissued and never arrives on its mbarrier, so the wait for it can only run out (the staged and chunked
+verify, the replay commit, the chunked prefill, the in_proj + conv1d kernel).  That is the same path
 a copy that never lands would take: the kernel sets GDN_ERRBIT_TIMEOUT, gives up the work it waited for,
 drains the copies it did issue and ends.  Nothing is left in flight, so the GPU context stays usable: the
 product library then runs a normal call in the same process and matches the oracle."""
@@ -14,7 +15,7 @@ import torch
 import gated_deltanet_linear_mtp_gb300 as gdn
 import gdn_workloads as W
 from gated_deltanet_linear_mtp_gb300 import build as gbuild
-from gpu_util import Dev, host, run_verify
+from gpu_util import Dev, dev, host, run_verify
 from test_gpu_parity import compare_verify
 
 pytestmark = pytest.mark.gpu
@@ -101,3 +102,25 @@ def test_chunked_prefill_wait_that_runs_out(timeout_lib, monkeypatch):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     compare_prefill(pw, x, host(o), host(t["pool"]), before)
+
+
+def test_in_proj_wait_that_runs_out(timeout_lib, monkeypatch):
+    """The in_proj + conv1d kernel (W by TMA, the hidden dimension split over a cluster): the first stage of the
+    first CTA is never loaded, so its MMA thread's wait runs out, then the producer's wait for the stage to come
+    free; the bit is set, the CTA drains the loads it did issue, every rank of the cluster still meets at its
+    barriers, and the product library then computes the batch correctly."""
+    from test_gpu_in_proj_conv import check_call, outputs, small
+    w = small("timeout_in_proj", B=4, T=4, H=512, seed=25)
+    x = w.arrays()
+    t = {k: dev(v) for k, v in x.items()}
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call():
+        rec = torch.zeros((w.B, w.T, w.Cc), dtype=torch.bfloat16, device="cuda")
+        gdn.gdn_in_proj_conv(t["x"], t["W"], t["conv_w"], t["conv_b"], t["conv_state"], t["indices"], outputs(w),
+                             False, rec, err)
+        torch.cuda.synchronize()
+
+    run_with(timeout_lib, monkeypatch, call)
+    assert int(err.item()) & gdn.ERRBIT_TIMEOUT, "the wait did not report running out"
+    check_call(w, x, False)
