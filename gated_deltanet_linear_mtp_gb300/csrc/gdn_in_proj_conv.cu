@@ -11,15 +11,16 @@
 //         verify keeps u as its recovery records
 //     channels z | b | a: the projection itself.
 //
-// gdn_in_proj_conv_kernel: one CTA of 4 warps per (128 output channels, a tile of whole lanes, a slice of the
+// gdn_in_proj_conv_kernel: one CTA of 6 warps per (128 output channels, a tile of whole lanes, a slice of the
 // hidden dimension).  W is the dense operand: its 128 x 64 boxes and the rows' N x 64 boxes arrive by TMA (128-byte
-// swizzle) into a ring of stages; one thread issues tcgen05.mma (M = 128 channels, N = the tile's rows padded to 16,
-// K = 16) into a tensor-memory accumulator of 128 lanes x N columns.  The bytes are W's (50 MB for a 12352 x 2048
-// projection), read once, so a small row count is HBM-bound: the grid splits the hidden dimension over a
-// thread-block cluster of up to 8 CTAs so that about two CTAs run per SM, and the partial sums meet through
-// distributed shared memory.  The epilogue moves the accumulator to shared memory (the ring, no longer in use),
-// then each rank of the cluster takes its share of the tile's lanes: thread = channel, so every load and store of
-// the state, the outputs and the records is one coalesced row.
+// swizzle) into a ring of stages (lane 0 of warp 4); lane 0 of warp 5 issues tcgen05.mma (M = 128 channels, N = the
+// tile's rows padded to 16, K = 16) into a tensor-memory accumulator of 128 lanes x N columns.  The bytes are W's
+// (50 MB for a 12352 x 2048 projection), read once, so a small row count is HBM-bound: the grid splits the hidden
+// dimension over a thread-block cluster of up to 8 CTAs, the split chosen from the cluster occupancy on the host,
+// and each rank pushes its partial sums into the owning rank's ring (distributed shared memory) once every ring is
+// free.  Warps 0-3 are the epilogue (thread = channel, so every load and store of the state, the outputs and the
+// records is one coalesced row); they load the taps, indices and state rows they will need while the main loop
+// runs, and keep their loops rolled (after an L2 flush the code itself comes from memory).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
