@@ -144,9 +144,11 @@ SMALL = [
     small("ip_K2_T8_one_chunk", B=2, T=8, H=64, K=2, conv="f32", out="bf16", seed=603),
     small("ip_T16", B=2, T=16, H=128, HK=1, HV=2, DK=64, DV=48, seed=604),
     small("ip_wide_heads", B=2, T=3, H=512, HK=2, HV=6, DK=128, DV=96, seed=605),
-    # 48 rows (lanes gathered ahead in shared memory) with 9 convolved channels: rows not 16-byte aligned, so the
-    # state comes by direct loads
-    small("ip_odd_channels_gathered", B=12, T=4, H=64, HK=1, HV=1, DK=3, DV=3, seed=608, pad=0.25),
+    # 160 rows (64-row tiles, lanes gathered ahead in shared memory) with 9 convolved channels: rows not 16-byte
+    # aligned, so the state comes by direct loads
+    small("ip_odd_channels_gathered", B=40, T=4, H=64, HK=1, HV=1, DK=3, DV=3, seed=608, pad=0.25),
+    # 48 rows: two tiles of 24 rows (6 lanes), ragged 16-row padding
+    small("ip_two_tiles_48_rows", B=12, T=4, H=128, seed=609, pad=0.2),
 ]
 
 
