@@ -471,3 +471,76 @@ def test_conv_commit_checks(L):
     assert conv_commit(L, conv_dims(H=3, out_dtype=9, silu=5)) != 2                # the commit reads neither
     assert conv_commit(L, conv_dims(), acc=ctypes.c_void_p(0x10002)) == 4
     assert conv_commit(L, conv_dims(B=0), state=None, idx=None, rec=None, acc=None) == 0
+
+
+# ---- gdn_in_proj_conv / gdn_conv_commit bindings: shapes, dtypes and devices checked before any launch --------
+def _in_proj_args(dev_of=lambda k: "cuda:0", **shape):
+    import torch
+
+    s = dict(B=2, T=3, H=64, HK=1, HV=2, DK=16, DV=16, K=4, slots=4)
+    s.update(shape)
+    B, T, H, HK, HV, DK, DV, K = (s[k] for k in ("B", "T", "H", "HK", "HV", "DK", "DV", "K"))
+    Cc = 2 * HK * DK + HV * DV
+    C = Cc + HV * DV + 2 * HV
+    bf = torch.bfloat16
+    t = dict(x=torch.zeros(B, T, H, dtype=bf), W=torch.zeros(C, H, dtype=bf), conv_w=torch.zeros(Cc, K),
+             conv_b=torch.zeros(Cc), state=torch.zeros(s["slots"], K - 1, Cc, dtype=bf),
+             idx=torch.zeros(B, dtype=torch.int32), q=torch.zeros(B, T, HK, DK, dtype=bf),
+             k=torch.zeros(B, T, HK, DK, dtype=bf), v=torch.zeros(B, T, HV, DV, dtype=bf),
+             z=torch.zeros(B, T, HV, DV, dtype=bf), b=torch.zeros(B, T, HV, dtype=bf), a=torch.zeros(B, T, HV, dtype=bf),
+             rec=torch.zeros(B, T, Cc, dtype=bf), acc=torch.ones(B, dtype=torch.int32))
+    return {k: _OnDevice(x, dev_of(k)) for k, x in t.items()}
+
+
+def _in_proj(x, **kw):
+    out = gdn.InProjOut(x["q"], x["k"], x["v"], x["z"], x["b"], x["a"])
+    gdn.gdn_in_proj_conv(x["x"], x["W"], x["conv_w"], x["conv_b"], x["state"], x["idx"], out, False, x["rec"], **kw)
+
+
+def test_in_proj_binding_checks_shapes_and_dtypes():
+    import torch
+
+    x = _in_proj_args()
+    x["W"] = _OnDevice(torch.zeros(7, 64, dtype=torch.bfloat16), "cuda:0")
+    with pytest.raises(ValueError, match="W: shape"):
+        _in_proj(x)
+    x = _in_proj_args()
+    x["v"] = _OnDevice(torch.zeros(2, 3, 2, 8, dtype=torch.bfloat16), "cuda:0")  # v's DV disagrees with W's C
+    with pytest.raises(ValueError, match="shape"):
+        _in_proj(x)
+    x = _in_proj_args()
+    x["x"] = _OnDevice(torch.zeros(2, 3, 64), "cuda:0")
+    with pytest.raises(TypeError, match="x must be bf16"):
+        _in_proj(x)
+    x = _in_proj_args()
+    x["z"] = _OnDevice(torch.zeros(2, 3, 2, 16), "cuda:0")
+    with pytest.raises(TypeError, match="z must have q's dtype"):
+        _in_proj(x)
+    x = _in_proj_args()
+    x["rec"] = _OnDevice(torch.zeros(2, 3, 64), "cuda:0")
+    with pytest.raises(TypeError, match="records must have conv_state's dtype"):
+        _in_proj(x)
+    x = _in_proj_args()
+    x["state"] = _OnDevice(torch.zeros(4, 2, 64, dtype=torch.bfloat16), "cuda:0")  # K - 1 rows disagree with conv_w
+    with pytest.raises(ValueError, match="conv_state: shape"):
+        _in_proj(x)
+
+
+@pytest.mark.parametrize("odd", ["x", "W", "state", "idx", "q", "a", "rec"])
+def test_in_proj_binding_rejects_tensors_on_two_gpus(odd):
+    x = _in_proj_args(lambda k: "cuda:1" if k == odd else "cuda:0")
+    with pytest.raises(ValueError, match="same GPU"):
+        _in_proj(x)
+
+
+def test_conv_commit_binding_checks():
+    import torch
+
+    x = _in_proj_args()
+    with pytest.raises(ValueError, match="same GPU"):
+        gdn.gdn_conv_commit(x["state"], x["idx"], x["rec"], _OnDevice(torch.ones(2, dtype=torch.int32), "cuda:1"))
+    with pytest.raises(TypeError, match="accept_len must be int32"):
+        gdn.gdn_conv_commit(x["state"], x["idx"], x["rec"], _OnDevice(torch.ones(2), "cuda:0"))
+    with pytest.raises(ValueError, match="conv_state: shape"):
+        gdn.gdn_conv_commit(_OnDevice(torch.zeros(4, 3, 63, dtype=torch.bfloat16), "cuda:0"), x["idx"], x["rec"],
+                            x["acc"])
