@@ -27,6 +27,8 @@ TIMED = [
     ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128E13__nv_bfloat16S2_Lb1E", 0),     # prefill (TMA)
     ("gdn_prefill_chunked.cu", "gdn_prefill_chunked_kernelILi128EffLb0E", 0),                     # prefill fp32
     ("gdn_gated_norm.cu", "gdn_gated_rmsnorm_reg_kernel", 0),                                    # gated norm
+    ("gdn_in_proj_conv.cu", "gdn_in_proj_conv_kernelILi4E", 0),                                  # in_proj + conv1d
+    ("gdn_in_proj_conv.cu", "gdn_conv_commit_kernel", 0),                                        # conv state commit
 ]
 
 
