@@ -382,8 +382,9 @@ __global__ void __launch_bounds__(kIpThreads, 1)
         }
     }
 
+    // (no final cluster barrier: every remote store came before the one above, so no rank touches another's
+    // shared memory from there on and each may leave when it is done)
     __syncthreads();
-    if (g.ks > 1) cluster_barrier();  // no rank leaves while another may still read its partial sums
     if (warp == kIpMmaWarp) tmem_dealloc(tmem, ncols);
 }
 
