@@ -8,7 +8,9 @@ The cases aim at what the kernel adds:
 * every tap count (2, 3, 4), T from 1 to 16, bf16 and fp32 state and outputs, SiLU on and off;
 * padded lanes (untouched, bit for bit), a bad index (flag bit), the decode write-back and the verify's records;
 * the commit of the records, bit for bit, and verify + commit against decode of the accepted rows;
-* the three timed workloads at full size (hidden 2048, 12352 channels).
+* the three timed workloads at full size (hidden 2048, 12352 channels);
+* two host threads on their own streams (the per-device tiling cache shared), and a new shape captured into a
+  CUDA graph and replayed.
 
 Tolerances (the kernel accumulates in fp32 on the tensor cores, the oracle in fp64):
 * the stored pre-convolution values (records, the written-back state): 1 ulp of the state type as in
@@ -247,3 +249,76 @@ def test_full_size_512_rows_sampled():
                                                         x["conv_state"].copy(), xs["indices"], write_pool=False)
     compare_outputs(ws, xs, {n: v[lanes] for n, v in got.items()}, ref_out, rec_ref, x["conv_state"], xs["indices"])
     compare_stored(ws, rec[lanes], rec_ref, "records")
+
+
+def _eager(w, x, t, write_state, stream=None):
+    out = outputs(w)
+    rec = None if write_state else canary((w.B, w.T, w.Cc), w.conv_dtype)
+    gdn.gdn_in_proj_conv(t["x"], t["W"], t["conv_w"], t["conv_b"], t["conv_state"], t["indices"], out, write_state,
+                         rec, silu=w.silu, stream=stream)
+    return out, rec
+
+
+def test_calls_from_two_host_threads():
+    """Two host threads on their own streams call the kernel over and over with different shapes (different splits:
+    the per-device tiling cache is shared and overwritten by both); every result equals the single-threaded one bit
+    for bit (the split-K sum is formed in rank order, so it is deterministic)."""
+    import threading
+
+    cases = [small("thr_a", B=4, T=4, H=512, seed=630), small("thr_b", B=3, T=2, H=384, HK=2, HV=6, DK=64, DV=48,
+                                                              seed=631)]
+    prepared = []
+    for w in cases:
+        x = w.arrays()
+        t = {k: dev(v) for k, v in x.items()}
+        out, rec = _eager(w, x, t, False)
+        torch.cuda.synchronize()
+        prepared.append((w, x, t, {n: host(getattr(out, n)) for n in ("q", "k", "v", "z", "b", "a")}, host(rec)))
+    failures = []
+
+    def worker(w, x, t, ref, rec_ref):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for _ in range(30):
+                    out, rec = _eager(w, x, t, False, stream=stream)
+                stream.synchronize()
+                for n, r in ref.items():
+                    if not np.array_equal(host(getattr(out, n)), r):
+                        failures.append(f"{w.name}: {n} differs")
+                if not np.array_equal(host(rec), rec_ref):
+                    failures.append(f"{w.name}: records differ")
+        except Exception as e:  # surfaced below
+            failures.append(f"{w.name}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=a) for a in prepared]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not failures, failures
+
+
+def test_graph_capture_of_a_new_shape():
+    """A shape never launched before is captured into a CUDA graph (its split is chosen during the capture) and
+    replayed: decode rows move the state on at every replay, as eager calls do."""
+    w = small("graph_new_shape", B=5, T=1, H=320, HK=3, HV=6, DK=32, DV=40, seed=640)
+    x = w.arrays()
+    t = {k: dev(v) for k, v in x.items()}
+    te = {k: dev(v) for k, v in x.items()}  # eager twin
+    out = outputs(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gdn.gdn_in_proj_conv(t["x"], t["W"], t["conv_w"], t["conv_b"], t["conv_state"], t["indices"], out, True,
+                             None, silu=w.silu)
+    for rep in range(3):
+        g.replay()
+        oe, _ = _eager(w, x, te, True)
+        torch.cuda.synchronize()
+        for n in ("q", "k", "v", "z", "b", "a"):
+            assert np.array_equal(host(getattr(out, n)), host(getattr(oe, n))), (rep, n)
+        assert np.array_equal(host(t["conv_state"]), host(te["conv_state"])), rep
+    # and the first replay's outputs are the oracle's decode from the initial state
+    check_call(w, x, True)
