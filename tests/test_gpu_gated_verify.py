@@ -200,3 +200,32 @@ def test_decode_gated_in_place(state):
                          o, gdn.GatedNorm(dev(z), dev(wt), o, eps=1e-6))
     torch.cuda.synchronize()
     check_y(w, x, host(o_ref), host(o), z, wt, 1e-6, "bf16")
+
+
+@pytest.mark.gpu
+def test_decode_gated_graph_capture():
+    """The fused decode norm (a thread-block-cluster launch) captured into a CUDA graph before any eager call of its
+    shape, then replayed: o, y and the written-back pool as eager calls leave them, step after step."""
+    w = dwl("dg_graph", B=3, HV=4, seed=129)
+    x = w.arrays()
+    z, wt = gate_inputs(w, "bf16", seed=132)
+    t, te = Dev(x), Dev(x)
+    shape = (w.B, 1, w.HV, w.DV)
+    o, y, oe, ye = (canary(shape, w.out_dtype) for _ in range(4))
+    zd, wd = dev(z), dev(wt)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gdn.gdn_decode_gated(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["pool"],
+                             t["indices"], o, gdn.GatedNorm(zd, wd, y))
+    for rep in range(3):
+        g.replay()
+        gdn.gdn_decode_gated(te["q"], te["k"], te["v"], te["a"], te["b"], te["A_log"], te["dt_bias"], te["pool"],
+                             te["indices"], oe, gdn.GatedNorm(zd, wd, ye))
+        torch.cuda.synchronize()
+        for a, b_, what in ((o, oe, "o"), (y, ye, "y"), (t["pool"], te["pool"], "pool")):
+            ha, hb = host(a), host(b_)
+            if ha.dtype == np.float32:
+                ha, hb = ha.view(np.uint32), hb.view(np.uint32)
+            assert np.array_equal(ha, hb), (rep, what)
