@@ -283,15 +283,11 @@ struct NormSmem {
     }
 };
 
-// zs: the CTA's rows row0 .. row0 + rows - 1 of z for T tokens (chunks of rows past DV are not copied).  Returns
-// the norm weight of the one row this thread writes y for when the CTA's rows divide its threads (row
-// row0 + tid mod rows; loaded now, not behind the reduction), else 0.
-__device__ __forceinline__ float norm_begin(const RecurrentParams& p, unsigned char* zs, int rows, int row0, int b,
-                                            int h, int T, int tid, int nt) {
+// zs: the CTA's rows row0 .. row0 + rows - 1 of z for T tokens (chunks of rows past DV are not copied)
+__device__ __forceinline__ void norm_begin(const RecurrentParams& p, unsigned char* zs, int rows, int row0, int b,
+                                           int h, int T, int tid, int nt) {
     cluster_arrive_relaxed();
-    const int wr = row0 + tid % rows;
-    const float w_pre = nt % rows == 0 && wr < p.DV ? p.nw[wr] : 0.f;
-    if (!p.nz_vec) return w_pre;
+    if (!p.nz_vec) return;
     const int zb = p.nz_bf16 ? 2 : 4;
     const int zch = 16 / zb;  // elements per chunk; DV % 8 == 0 puts every chunk wholly inside or past DV
     const int cpt = rows / zch;
@@ -302,14 +298,12 @@ __device__ __forceinline__ float norm_begin(const RecurrentParams& p, unsigned c
             cp_async16(zs + (size_t)(t * rows + c * zch) * zb,
                        z + ((((int64_t)b * T + t) * p.HV + h) * p.DV + row) * zb);
     }
-    return w_pre;
 }
 
-// os: [T][rows] stored o of the CTA's rows row0 .. row0 + rows - 1; zs and w_pre as norm_begin left them
+// os: [T][rows] stored o of the CTA's rows row0 .. row0 + rows - 1; zs as norm_begin left it
 template <int NT>
 __device__ __forceinline__ void norm_epilogue(const RecurrentParams& p, const unsigned char* zs, const float* os,
-                                              float* part, int rows, int row0, int b, int h, int T, int tid,
-                                              float w_pre) {
+                                              float* part, int rows, int row0, int b, int h, int T, int tid) {
     float* inv = part + kNormMaxCluster * GDN_MAX_T;
     const int warp = tid >> 5, lane = tid & 31;
     cp_async_commit_wait_all();
@@ -344,8 +338,7 @@ __device__ __forceinline__ void norm_epilogue(const RecurrentParams& p, const un
         else
             zt = p.nz_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.nz)[off])
                            : static_cast<const float*>(p.nz)[off];
-        const float wv = NT % rows == 0 ? w_pre : p.nw[row];  // i = tid + k NT: the row is tid mod rows
-        const float y = os[i] * inv[t] * wv * (zt / (1.f + expf(-zt)));
+        const float y = os[i] * inv[t] * p.nw[row] * (zt / (1.f + expf(-zt)));
         if (p.out_bf16)
             static_cast<__nv_bfloat16*>(p.ny)[off] = __float2bfloat16_rn(y);
         else
@@ -382,9 +375,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
     if (!lane_work(p, slot, steps, h, tid)) return;
     extern __shared__ __align__(16) float smem[];
     unsigned char* const norm_base = reinterpret_cast<unsigned char*>(smem);
-    float w_pre = 0.f;
-    if constexpr (kNorm)
-        w_pre = norm_begin(p, norm_base + NormSmem::zs(direct_smem_bytes<DK>(T)), RPC, row0, b, h, T, tid, NT);
+    if constexpr (kNorm) norm_begin(p, norm_base + NormSmem::zs(direct_smem_bytes<DK>(T)), RPC, row0, b, h, T, tid, NT);
 
     // state load, in the lane's register-slot order (LaneRows)
     const LaneRows<DK> lr(warp, rg, pp);
@@ -419,8 +410,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Split<DK>::MIN_CTAS_PER_SM
     run_tokens<DK, StT>(p, S, lr, b, h, row0, slot, steps, pp, qs, ks, vs, RPC, gs, bs, kqs, osm, RPC, row0);
     if constexpr (kNorm)
         norm_epilogue<NT>(p, norm_base + NormSmem::zs(nb), osm,
-                          reinterpret_cast<float*>(norm_base + NormSmem::part(nb, T, RPC)), RPC, row0, b, h, T, tid,
-                          w_pre);
+                          reinterpret_cast<float*>(norm_base + NormSmem::part(nb, T, RPC)), RPC, row0, b, h, T, tid);
 }
 
 // ---- TMA-staged kernel ------------------------------------------------------------------------------------
@@ -473,8 +463,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
 
     extern __shared__ __align__(16) unsigned char staged_smem[];
     const size_t nb = ST::norm_offset(T);
-    float w_pre = 0.f;
-    if constexpr (kNorm) w_pre = norm_begin(p, staged_smem + NormSmem::zs(nb), ROWS, row0, b, h, T, tid, NT);
+    if constexpr (kNorm) norm_begin(p, staged_smem + NormSmem::zs(nb), ROWS, row0, b, h, T, tid, NT);
     const uint32_t sbase = smem_u32(staged_smem);
     const uint32_t mbar0 = sbase + ST::mbar_offset(T);
     if (tid == 0) {
@@ -532,8 +521,7 @@ __global__ void __launch_bounds__(Split<DK>::THREADS, Staged<DK, StT, KIB>::MIN_
     if (failed && lane == 0 && p.err != nullptr) atomicOr(p.err, GDN_ERRBIT_TIMEOUT);
     if constexpr (kNorm)
         norm_epilogue<NT>(p, staged_smem + NormSmem::zs(nb), osm,
-                          reinterpret_cast<float*>(staged_smem + NormSmem::part(nb, T, ROWS)), ROWS, row0, b, h, T, tid,
-                          w_pre);
+                          reinterpret_cast<float*>(staged_smem + NormSmem::part(nb, T, ROWS)), ROWS, row0, b, h, T, tid);
 }
 
 }  // namespace gdn
