@@ -1,4 +1,5 @@
-"""The oracle reproduces its stored outputs on the tiny workload (``tests/golden/tiny_oracle.txt``)."""
+"""The oracle reproduces its stored outputs on the tiny workloads (``tests/golden/tiny_oracle.txt``,
+``tests/golden/tiny_in_proj_oracle.txt``)."""
 import os
 
 import numpy as np
@@ -6,9 +7,9 @@ import numpy as np
 from golden import make_golden
 
 
-def _load():
+def _load(path=None):
     rows = {}
-    with open(make_golden.OUT) as f:
+    with open(path or make_golden.OUT) as f:
         for line in f:
             if line.startswith("#"):
                 continue
@@ -31,3 +32,14 @@ def test_tiny_golden():
     pool = r["pool_bits"].view(np.float32)
     assert np.abs(cache - cache_ref).max() <= 1e-6 * np.abs(cache_ref).max()
     assert np.abs(pool - pool_ref).max() <= 1e-6 * np.abs(pool_ref).max()
+
+
+def test_tiny_in_proj_golden():
+    g = _load(make_golden.OUT_IN_PROJ)
+    r = make_golden.compute_in_proj()
+    assert [int(v) for v in g["indices"]] == list(r["indices"])
+    out_ref = np.array([float.fromhex(v) for v in g["out"]])
+    # SiLU's exp may differ in the last bit between machines' libm: 1e-14 relative
+    assert np.abs(r["out"] - out_ref).max() <= 1e-14 * np.abs(out_ref).max()
+    for key in ("rec_bits", "state_bits"):  # stored products (no libm): identical
+        assert np.array_equal(np.array([int(v, 16) for v in g[key]], np.uint32), r[key]), key
