@@ -246,3 +246,35 @@ def test_prefill_roofline_counts():
     assert bench.prefill_bytes(pw, x) == 40 * per_tok + 2 * (2 * 128 * 128 * 2)
     assert bench.prefill_mma_flops(pw.replace(qkv_dtype="f32"), x) is None  # the other token path: not counted
     assert not bench.prefill_is_chunked(pw.replace(DK=256))
+
+
+def test_in_proj_counts():
+    """The in_proj line's algorithmic bytes and flops, recomputed by hand: W once, the active rows' x and outputs,
+    the state read (and written back, or the records), taps and bias, indices; 2 x rows x C x H flops plus the
+    convolution's 2 K per convolved output."""
+    import bench
+    w = W.InProjWorkload("t", B=3, T=2, H=64, HK=1, HV=2, DK=16, DV=8, K=4, num_slots=5, conv_dtype="bf16",
+                         out_dtype="f32", seed=1)
+    Cc, C = 2 * 16 + 2 * 8, 2 * 16 + 2 * 8 + 2 * 8 + 2 * 2
+    assert (w.Cc, w.C) == (Cc, C)
+    rows = 2 * 2  # two active lanes
+    common = C * 64 * 2 + rows * 64 * 2 + rows * C * 4 + 2 * 3 * Cc * 2 + Cc * 5 * 4 + 3 * 4
+    assert bench.in_proj_counts(w, 2, decode=True) == (common + 2 * 3 * Cc * 2, 2 * rows * C * 64 + 2 * 4 * rows * Cc)
+    assert bench.in_proj_counts(w, 2, decode=False)[0] == common + rows * Cc * 2
+
+
+def test_in_proj_reference_arm_small(monkeypatch):
+    """The oracle arm of an in_proj line on a small projection: one JSON line, the oracle as the reference."""
+    import argparse
+
+    small = W.InProjWorkload("in_proj_small", B=3, T=2, H=64, HK=1, HV=2, DK=16, DV=8, K=4, num_slots=5,
+                             conv_dtype="bf16", out_dtype="bf16", seed=2)
+    monkeypatch.setitem(bench.IN_PROJ_NAMED, "in_proj16", lambda: small)
+    args = argparse.Namespace(steps=3, warmup=3, ref_seconds=1.0)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_in_proj_reference_arm(args, "in_proj16", 0, 1)
+    j = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "rows/s"
+    assert j["config"]["workload"] == "in_proj_small" and j["cpu_baseline"]["kind"] == "oracle"
+    assert j["e2e"]["h2d_bytes_per_step"] == 0
